@@ -1,0 +1,283 @@
+"""CPU oracle for the dense BF16 GEMM and the fused gate/up projection.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product library
+(``dense_bf16_gemm_gb300``) never imports, links or runs anything here, and this
+package never imports the product: the two share no code.
+
+Contents
+--------
+* ``gemm_full`` / ``gemm_entries``: ``alpha * A.B + beta * C`` in float64 from
+  the BF16 inputs, one running double sum per output (C implementation in
+  ``gemm_oracle.c``).  The epilogue semantics follow "Tiles and shared memory",
+  section "var and let" (``C[...] = alpha * acc + beta * c_old``); the operand
+  storage follows "TMA and Hopper WGMMA", section "The same storage contract
+  on both sides" (A(M,K) with K contiguous, B(K,N) stored with K inner, i.e.
+  ``B[n*ldb + k]``).
+* ``gate_up_entries``: ``silu(X.Wg) * (X.Wu)`` in float64 ("TMA and Hopper
+  WGMMA", sections "TMA and Hopper WGMMA" and "Worked consumers and current
+  validation", which name the fused gate/up projection; it is read as the
+  SwiGLU form with no bias and no scaling).
+* ``bf16_bits_to_f64`` / ``round_to_bf16_bits``: exact BF16 widening and
+  round-to-nearest-even narrowing ("TMEM tiles and transfers", section
+  "Representation and windows": ``pack(BFloat16, f)`` converts FP32 values to
+  BF16; the rounding mode is not stated there and is read as nearest-even).
+* ``gemm_tolerance`` / ``gate_up_tolerance``: the admissible distance between a
+  result accumulated in FP32 and the float64 reference.
+
+Every function here is pinned in ``tests/test_oracle.py`` to closed forms,
+identities, brute force on tiny shapes and library routines.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gemm_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_dbl = ctypes.c_double
+_vp = ctypes.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with the host compiler (plain -O2, OpenMP)."""
+    if not force and os.path.exists(_LIB_PATH) and \
+            os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_silu.restype = _dbl
+            lib.oracle_silu.argtypes = [_dbl]
+            lib.oracle_gemm_entries.restype = None
+            lib.oracle_gemm_entries.argtypes = [
+                _i64, _dbl, _vp, _i64, _vp, _i64, _dbl, _vp, _i64,
+                _i64, _vp, _vp, _vp, _vp]
+            lib.oracle_gemm_full.restype = None
+            lib.oracle_gemm_full.argtypes = [
+                _i64, _i64, _i64, _dbl, _vp, _i64, _vp, _i64, _dbl, _vp, _i64,
+                _vp, _vp]
+            lib.oracle_gate_up_entries.restype = None
+            lib.oracle_gate_up_entries.argtypes = [
+                _i64, _vp, _i64, _vp, _vp, _i64,
+                _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle uses (``OMP_NUM_THREADS`` or all cores)."""
+    return int(_load().oracle_num_threads())
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data
+
+
+def _as_bits(x) -> np.ndarray:
+    """Accept a uint16 array of BF16 bit patterns or a torch bfloat16 tensor."""
+    if isinstance(x, np.ndarray):
+        if x.dtype != np.uint16:
+            raise TypeError("BF16 operands are passed as uint16 bit patterns")
+        return np.ascontiguousarray(x)
+    import torch  # only for accepting CPU tensors from the input generator
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16:
+        raise TypeError("expected a bfloat16 tensor or uint16 bits")
+    return np.ascontiguousarray(x.contiguous().view(torch.int16).numpy()).view(np.uint16)
+
+
+def _as_f32(x) -> np.ndarray | None:
+    if x is None:
+        return None
+    if isinstance(x, np.ndarray):
+        return np.ascontiguousarray(x, dtype=np.float32)
+    return np.ascontiguousarray(x.contiguous().numpy(), dtype=np.float32)
+
+
+# --------------------------------------------------------------------------
+# GEMM
+# --------------------------------------------------------------------------
+def gemm_full(A, B, alpha=1.0, beta=0.0, C=None, want_abs=True):
+    """Every entry of ``alpha * A.B + beta * C``.
+
+    ``A`` is (M, K) K-contiguous, ``B`` is stored (N, K) K-contiguous, ``C`` is
+    (M, N) float32 (read only when ``beta != 0``).  Returns ``(value, abs_sum)``
+    as float64 (M, N) arrays, ``abs_sum[m, n] = sum_k |a(m,k) b(k,n)|``.
+    """
+    a, b = _as_bits(A), _as_bits(B)
+    M, K = a.shape
+    N, K2 = b.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ")
+    c = _as_f32(C) if beta != 0.0 else None
+    if beta != 0.0 and (c is None or c.shape != (M, N)):
+        raise ValueError("C must be (M, N) when beta != 0")
+    out = np.empty((M, N), np.float64)
+    ab = np.empty((M, N), np.float64) if want_abs else None
+    _load().oracle_gemm_full(M, N, K, float(alpha), _ptr(a), K, _ptr(b), K,
+                             float(beta), _ptr(c), N, _ptr(out), _ptr(ab))
+    return out, ab
+
+
+def gemm_entries(A, B, rows, cols, alpha=1.0, beta=0.0, C=None):
+    """Entries ``(rows[i], cols[i])`` of ``alpha * A.B + beta * C``.
+
+    Same storage as :func:`gemm_full`; returns ``(value, abs_sum)`` 1-D arrays.
+    """
+    a, b = _as_bits(A), _as_bits(B)
+    M, K = a.shape
+    N, K2 = b.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ")
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    c_ = np.ascontiguousarray(cols, dtype=np.int64)
+    if r.shape != c_.shape:
+        raise ValueError("rows and cols differ in length")
+    if r.size and (r.min() < 0 or r.max() >= M or c_.min() < 0 or c_.max() >= N):
+        raise IndexError("entry outside the result")
+    cm = _as_f32(C) if beta != 0.0 else None
+    out = np.empty(r.size, np.float64)
+    ab = np.empty(r.size, np.float64)
+    _load().oracle_gemm_entries(K, float(alpha), _ptr(a), K, _ptr(b), K,
+                                float(beta), _ptr(cm), N, r.size, _ptr(r),
+                                _ptr(c_), _ptr(out), _ptr(ab))
+    return out, ab
+
+
+# --------------------------------------------------------------------------
+# gate/up projection
+# --------------------------------------------------------------------------
+def silu(t: float) -> float:
+    """``t / (1 + exp(-t))`` evaluated by the C oracle in double."""
+    return float(_load().oracle_silu(float(t)))
+
+
+def gate_up_entries(X, Wg, Wu, rows, cols):
+    """Entries of ``Y = silu(X.Wg) * (X.Wu)``.
+
+    ``X`` is (M, K) K-contiguous, ``Wg`` and ``Wu`` are stored (N, K)
+    K-contiguous.  Returns a dict with float64 arrays ``y``, ``g``, ``u``,
+    ``abs_g``, ``abs_u``.
+    """
+    x, wg, wu = _as_bits(X), _as_bits(Wg), _as_bits(Wu)
+    M, K = x.shape
+    N = wg.shape[0]
+    if wg.shape != (N, K) or wu.shape != (N, K):
+        raise ValueError("weights must both be (N, K)")
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    c_ = np.ascontiguousarray(cols, dtype=np.int64)
+    if r.size and (r.min() < 0 or r.max() >= M or c_.min() < 0 or c_.max() >= N):
+        raise IndexError("entry outside the result")
+    res = {k: np.empty(r.size, np.float64) for k in ("y", "g", "u", "abs_g", "abs_u")}
+    _load().oracle_gate_up_entries(K, _ptr(x), K, _ptr(wg), _ptr(wu), K,
+                                   r.size, _ptr(r), _ptr(c_),
+                                   _ptr(res["y"]), _ptr(res["g"]), _ptr(res["u"]),
+                                   _ptr(res["abs_g"]), _ptr(res["abs_u"]))
+    return res
+
+
+# --------------------------------------------------------------------------
+# BF16 encoding
+# --------------------------------------------------------------------------
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Exact value of BF16 bit patterns (the upper half of a binary32)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    with np.errstate(invalid="ignore"):
+        return b.view(np.float32).astype(np.float64)
+
+
+def round_to_bf16_bits(x) -> np.ndarray:
+    """Round float64 values to the nearest BF16, ties to even; NaN -> 0x7FC0.
+
+    BF16 keeps 8 significant bits and the binary32 exponent range: normal
+    values have spacing ``2**(e-7)`` in the binade ``[2**e, 2**(e+1))`` and the
+    subnormal spacing is ``2**-133``.  The value is divided by the spacing,
+    rounded half-to-even to an integer (exact in float64), scaled back
+    (exact) and re-encoded; results beyond the largest finite BF16 become
+    infinities, as nearest-even rounding prescribes.
+    """
+    v = np.asarray(x, dtype=np.float64)
+    out = np.zeros(v.shape, dtype=np.uint16)
+    nan = np.isnan(v)
+    fin = np.isfinite(v)
+    with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
+        mag = np.abs(np.where(fin, v, 0.0))
+        _, e = np.frexp(mag)               # mag = f * 2**e, f in [0.5, 1)
+        e = e - 1                          # binade exponent: mag in [2**e, 2**(e+1))
+        spacing_exp = np.maximum(e - 7, -133)
+        q = np.ldexp(1.0, spacing_exp)
+        r = np.rint(mag / q) * q           # rint is half-to-even
+        r32 = r.astype(np.float32)         # exact: r has <= 8 significant bits
+        bits = (r32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    sign = np.where(np.signbit(v), np.uint16(0x8000), np.uint16(0))
+    out = np.where(fin, bits | sign, out)
+    out = np.where(np.isinf(v), np.uint16(0x7F80) | sign, out)
+    out = np.where(nan, np.uint16(0x7FC0), out)
+    return out.astype(np.uint16)
+
+
+def bf16_half_ulp(mag) -> np.ndarray:
+    """Half the BF16 spacing at magnitude ``mag``: ``2**(floor(log2 mag) - 8)``,
+    never below half the subnormal spacing (``2**-134``)."""
+    m = np.abs(np.asarray(mag, dtype=np.float64))
+    _, e = np.frexp(m)
+    return np.maximum(np.ldexp(1.0, e - 1 - 8), np.ldexp(1.0, -134))
+
+
+# --------------------------------------------------------------------------
+# tolerances
+# --------------------------------------------------------------------------
+REL_ACC = 4e-3      # admissible FP32-accumulation error per unit of sum |a b|
+SILU_LIPSCHITZ = 1.1  # max |silu'(t)| = 1.0998... (at t ~ 2.3994)
+
+
+def gemm_tolerance(ref, abs_sum, alpha, beta, c=None, out_bf16=False):
+    """``4e-3 * (|alpha| sum|ab| + |beta| |c|)`` plus, for a BF16 output, the
+    half-ulp of BF16 at the largest magnitude the FP32 result can take."""
+    tol = REL_ACC * abs(alpha) * np.asarray(abs_sum, np.float64)
+    if beta != 0.0 and c is not None:
+        tol = tol + REL_ACC * abs(beta) * np.abs(np.asarray(c, np.float64))
+    if out_bf16:
+        tol = tol + bf16_half_ulp(np.abs(ref) + tol)
+    return tol
+
+
+def gate_up_tolerance(res):
+    """Propagate the accumulation bound through ``silu(g) * u``.
+
+    With ``|g' - g| <= e_g`` and ``|u' - u| <= e_u``:
+    ``|silu(g')u' - silu(g)u| <= L e_g (|u| + e_u) + |silu(g)| e_u``, ``L`` the
+    Lipschitz constant of silu.  ``1e-5 |y|`` covers the FP32 epilogue
+    arithmetic (exp, divide, multiply) and the BF16 half-ulp the final
+    rounding.
+    """
+    g, u, y = res["g"], res["u"], res["y"]
+    e_g = REL_ACC * res["abs_g"]
+    e_u = REL_ACC * res["abs_u"]
+    sg = np.abs(g / (1.0 + np.exp(-np.clip(g, -700, 700))))
+    tol = SILU_LIPSCHITZ * e_g * (np.abs(u) + e_u) + sg * e_u + 1e-5 * np.abs(y)
+    return tol + bf16_half_ulp(np.abs(y) + tol)

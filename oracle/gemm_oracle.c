@@ -1,0 +1,157 @@
+/*
+ * CPU oracle for the dense BF16 GEMM and the fused gate/up projection.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file; only the test-suite, the smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header, table or helper with the
+ * CUDA library.
+ *
+ * What it computes (the plain definitions, no blocking, no reordering):
+ *
+ *   GEMM   C_ref(m,n) = alpha * sum_k a(m,k) * b(k,n) + beta * c(m,n)
+ *          ("Tiles and shared memory", section "var and let": the tile
+ *          epilogue writes alpha * acc + beta * c_old over the C slice, so
+ *          C is read and then overwritten.)
+ *          Operands are stored K-contiguous: a(m,k) at A[m*lda + k] and
+ *          b(k,n) at B[n*ldb + k] ("TMA and Hopper WGMMA", section "The same
+ *          storage contract on both sides": A(M,K) with K contiguous, B(K,N)
+ *          with K as the inner axis).  C(m,n) sits at C[m*ldc + n].
+ *
+ *   gate/up  g(m,n) = sum_k x(m,k) wg(k,n),  u(m,n) = sum_k x(m,k) wu(k,n),
+ *            y(m,n) = silu(g) * u,  silu(t) = t / (1 + exp(-t))
+ *          ("TMA and Hopper WGMMA", sections "TMA and Hopper WGMMA" and
+ *          "Worked consumers and current validation" name the fused gate/up
+ *          projection without defining it; it is read as the SwiGLU form
+ *          above, with no bias and no scaling.)
+ *
+ * Precision: every BF16 input is widened exactly to double and every sum is
+ * one running double accumulator over k = 0 .. K-1 in order.  Beside each
+ * result the oracle also returns sum_k |a(m,k) b(k,n)|, which the tests use
+ * to scale the rounding tolerance of the FP32-accumulating GPU path.
+ *
+ * Rows are spread over OpenMP threads; each output is still computed by one
+ * thread in the order above, so the result does not depend on the thread
+ * count.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* A BF16 value is the upper half of an IEEE binary32; widening is exact. */
+static double bf16_to_double(uint16_t bits)
+{
+    uint32_t w = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+static void dot_bf16(int64_t K, const uint16_t *x, const uint16_t *y,
+                     double *sum, double *abs_sum)
+{
+    double s = 0.0, a = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double p = bf16_to_double(x[k]) * bf16_to_double(y[k]);
+        s += p;
+        a += fabs(p);
+    }
+    *sum = s;
+    *abs_sum = a;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Entries (rows[i], cols[i]) of alpha*A*B + beta*C, i = 0 .. count-1.
+ * C is read only when beta != 0 (it may be NULL otherwise).
+ * out[i] receives the value, abs_out[i] (if not NULL) receives
+ * sum_k |a(m,k) b(k,n)|.
+ */
+void oracle_gemm_entries(int64_t K, double alpha,
+                         const uint16_t *A, int64_t lda,
+                         const uint16_t *B, int64_t ldb,
+                         double beta, const float *C, int64_t ldc,
+                         int64_t count, const int64_t *rows, const int64_t *cols,
+                         double *out, double *abs_out)
+{
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t m = rows[i], n = cols[i];
+        double s, a;
+        dot_bf16(K, A + m * lda, B + n * ldb, &s, &a);
+        double v = alpha * s;
+        if (beta != 0.0)
+            v += beta * (double)C[m * ldc + n];
+        out[i] = v;
+        if (abs_out)
+            abs_out[i] = a;
+    }
+}
+
+/*
+ * Every entry of alpha*A*B + beta*C for an M x N result, written row-major
+ * to out[m*N + n] (and abs_out likewise when not NULL).
+ */
+void oracle_gemm_full(int64_t M, int64_t N, int64_t K, double alpha,
+                      const uint16_t *A, int64_t lda,
+                      const uint16_t *B, int64_t ldb,
+                      double beta, const float *C, int64_t ldc,
+                      double *out, double *abs_out)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double s, a;
+            dot_bf16(K, A + m * lda, B + n * ldb, &s, &a);
+            double v = alpha * s;
+            if (beta != 0.0)
+                v += beta * (double)C[m * ldc + n];
+            out[m * N + n] = v;
+            if (abs_out)
+                abs_out[m * N + n] = a;
+        }
+    }
+}
+
+/* silu(t) = t * sigmoid(t), written directly. */
+double oracle_silu(double t)
+{
+    return t / (1.0 + exp(-t));
+}
+
+/*
+ * Entries (rows[i], cols[i]) of the gate/up projection.  X(m,k) at
+ * X[m*ldx + k]; Wg(k,n) at Wg[n*ldw + k] and Wu(k,n) at Wu[n*ldw + k]
+ * (K-contiguous like B).  Outputs y, and the intermediates g, u with their
+ * absolute sums; any of g, u, abs_g, abs_u may be NULL.
+ */
+void oracle_gate_up_entries(int64_t K,
+                            const uint16_t *X, int64_t ldx,
+                            const uint16_t *Wg, const uint16_t *Wu, int64_t ldw,
+                            int64_t count, const int64_t *rows, const int64_t *cols,
+                            double *y, double *g_out, double *u_out,
+                            double *abs_g, double *abs_u)
+{
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t m = rows[i], n = cols[i];
+        double g, ag, u, au;
+        dot_bf16(K, X + m * ldx, Wg + n * ldw, &g, &ag);
+        dot_bf16(K, X + m * ldx, Wu + n * ldw, &u, &au);
+        y[i] = oracle_silu(g) * u;
+        if (g_out) g_out[i] = g;
+        if (u_out) u_out[i] = u;
+        if (abs_g) abs_g[i] = ag;
+        if (abs_u) abs_u[i] = au;
+    }
+}

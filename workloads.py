@@ -1,0 +1,174 @@
+"""Seeded synthetic inputs for the GEMM and gate/up workloads.
+
+This module holds the random-number recipe only and none of the arithmetic of
+the method: it draws float32 values with a seeded ``torch.Generator`` on the
+CPU, rounds them to BF16 (round-to-nearest-even, ``Tensor.to``) and returns the
+CPU tensors.  The CUDA path receives device copies of exactly these bytes and
+the oracle reads the same host bytes, so both sides see identical inputs.
+
+Storage (both operands K-contiguous):
+  A  (M, K)  a(m,k) = A[m, k]
+  B  (N, K)  b(k,n) = B[n, k]
+  C  (M, N)  float32, only for beta != 0
+Gate/up:  X (M, K), Wg (N, K), Wu (N, K).
+
+Draw order within one generator: A, then B, then C (or X, Wg, Wu).
+"uniform" is ``2 * rand - 1`` (uniform on [-1, 1)); "normal" is
+``std * randn``.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str                 # "gemm" or "gate_up"
+    M: int
+    N: int
+    K: int
+    seed: int
+    dist_a: tuple             # ("uniform",) or ("normal", std)
+    dist_b: tuple
+    alpha: float = 1.0
+    beta: float = 0.0
+    dist_c: tuple | None = None
+    out_bf16: bool = False
+    check: str = "full"       # "full" or "sampled"
+    notes: str = ""
+
+    @property
+    def flops(self) -> float:
+        """Useful floating-point operations: 2MNK per GEMM (two for gate/up)."""
+        per = 2.0 * self.M * self.N * self.K
+        return 2.0 * per if self.kind == "gate_up" else per
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """Compulsory HBM bytes: each input read once, the output written once
+        (plus C read when beta != 0)."""
+        if self.kind == "gate_up":
+            return 2 * (self.M * self.K + 2 * self.N * self.K + self.M * self.N)
+        out_elem = 2 if self.out_bf16 else 4
+        b = 2 * (self.M * self.K + self.N * self.K) + out_elem * self.M * self.N
+        if self.beta != 0.0:
+            b += out_elem * self.M * self.N
+        return b
+
+
+WORKLOADS = {
+    "gemm_256_f32": Workload(
+        "gemm_256_f32", "gemm", 256, 256, 256, seed=0,
+        dist_a=("uniform",), dist_b=("uniform",), out_bf16=False,
+        notes="M=N=K=256, FP32 output, alpha=1, beta=0"),
+    "gemm_4096_bf16": Workload(
+        "gemm_4096_bf16", "gemm", 4096, 4096, 4096, seed=1,
+        dist_a=("normal", 1.0), dist_b=("normal", 1.0), out_bf16=True,
+        notes="M=N=K=4096, BF16 output, alpha=1, beta=0"),
+    "gemm_ragged_3000x5000x2000": Workload(
+        "gemm_ragged_3000x5000x2000", "gemm", 3000, 5000, 2000, seed=2,
+        dist_a=("uniform",), dist_b=("uniform",), alpha=0.5, beta=2.0,
+        dist_c=("normal", 1.0), out_bf16=False,
+        notes="ragged tails in M, N and K; FP32 C read and written"),
+    "gate_up_4096x14336x4096": Workload(
+        "gate_up_4096x14336x4096", "gate_up", 4096, 14336, 4096, seed=3,
+        dist_a=("normal", 1.0), dist_b=("normal", 1.0 / 64.0), out_bf16=True,
+        check="sampled",
+        notes="Y = silu(X Wg) * (X Wu), BF16 [4096, 14336]"),
+    "skinny_16x28672x8192": Workload(
+        "skinny_16x28672x8192", "gemm", 16, 28672, 8192, seed=4,
+        dist_a=("normal", 1.0), dist_b=("normal", 1.0 / math.sqrt(8192)),
+        out_bf16=True, check="sampled",
+        notes="decode-shaped, weight 470 MB, HBM-bound"),
+}
+
+# The workload the benchmark times by default.
+HEADLINE = "gemm_4096_bf16"
+
+
+def _draw(gen: torch.Generator, shape, dist) -> torch.Tensor:
+    if dist[0] == "uniform":
+        return torch.rand(shape, generator=gen, dtype=torch.float32) * 2.0 - 1.0
+    if dist[0] == "normal":
+        return torch.randn(shape, generator=gen, dtype=torch.float32) * float(dist[1])
+    if dist[0] == "int":
+        lo, hi = dist[1], dist[2]
+        return torch.randint(lo, hi + 1, shape, generator=gen).to(torch.float32)
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+def gemm_inputs(M: int, N: int, K: int, seed: int, dist_a=("uniform",),
+                dist_b=("uniform",), dist_c=None):
+    """CPU tensors ``A`` (M,K) bf16, ``B`` (N,K) bf16 and ``C`` (M,N) f32 or None."""
+    gen = torch.Generator(device="cpu").manual_seed(int(seed))
+    A = _draw(gen, (M, K), dist_a).to(torch.bfloat16)
+    B = _draw(gen, (N, K), dist_b).to(torch.bfloat16)
+    C = _draw(gen, (M, N), dist_c) if dist_c is not None else None
+    return A, B, C
+
+
+def gate_up_inputs(M: int, N: int, K: int, seed: int, dist_x=("normal", 1.0),
+                   dist_w=("normal", 1.0)):
+    """CPU tensors ``X`` (M,K), ``Wg`` (N,K), ``Wu`` (N,K), all bf16."""
+    gen = torch.Generator(device="cpu").manual_seed(int(seed))
+    X = _draw(gen, (M, K), dist_x).to(torch.bfloat16)
+    Wg = _draw(gen, (N, K), dist_w).to(torch.bfloat16)
+    Wu = _draw(gen, (N, K), dist_w).to(torch.bfloat16)
+    return X, Wg, Wu
+
+
+def inputs_for(w: Workload):
+    if w.kind == "gate_up":
+        return gate_up_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.dist_b)
+    return gemm_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.dist_b, w.dist_c)
+
+
+def sample_entries(M: int, N: int, seed: int, count: int = 65536, edge: int = 256):
+    """Output coordinates to check for a large result.
+
+    Every entry within ``edge`` rows of the top or bottom edge or within
+    ``edge`` columns of the left or right edge, plus ``count`` further
+    distinct entries drawn uniformly (without replacement, by a generator
+    seeded with ``seed + 1000``).  Returns ``(rows, cols)`` int64 arrays.
+    """
+    mask = np.zeros((M, N), dtype=bool) if M * N <= (1 << 28) else None
+    rows_e, cols_e = [], []
+    r_edge = np.unique(np.concatenate([np.arange(min(edge, M)),
+                                       np.arange(max(M - edge, 0), M)]))
+    c_edge = np.unique(np.concatenate([np.arange(min(edge, N)),
+                                       np.arange(max(N - edge, 0), N)]))
+    rr, cc = np.meshgrid(r_edge, np.arange(N), indexing="ij")
+    rows_e.append(rr.ravel()); cols_e.append(cc.ravel())
+    mid = np.setdiff1d(np.arange(M), r_edge)
+    rr, cc = np.meshgrid(mid, c_edge, indexing="ij")
+    rows_e.append(rr.ravel()); cols_e.append(cc.ravel())
+    rows_e = np.concatenate(rows_e).astype(np.int64)
+    cols_e = np.concatenate(cols_e).astype(np.int64)
+    if mask is not None:
+        mask[rows_e, cols_e] = True
+    total = M * N
+    gen = torch.Generator(device="cpu").manual_seed(int(seed) + 1000)
+    want = min(count, total - rows_e.size)
+    picked = np.empty(0, dtype=np.int64)
+    draws = max(2 * want, 1024)
+    while picked.size < want:
+        r = torch.randint(0, total, (draws,), generator=gen).numpy()
+        _, first = np.unique(r, return_index=True)
+        r = r[np.sort(first)]
+        if mask is not None:
+            r = r[~mask.ravel()[r]]
+        else:
+            rm, cm = r // N, r % N
+            in_edge = (rm < edge) | (rm >= M - edge) | (cm < edge) | (cm >= N - edge)
+            r = r[~in_edge]
+        if picked.size:
+            r = r[~np.isin(r, picked)]   # keeps draw order
+        picked = np.concatenate([picked, r])[:want]
+    rows = np.concatenate([rows_e, picked // N])
+    cols = np.concatenate([cols_e, picked % N])
+    return rows, cols
