@@ -1,0 +1,144 @@
+"""GB300 (sm_103a) dense BF16 GEMM and fused gate/up projection.
+
+The computation runs in the CUDA library declared by ``include/gemm_bf16.h``
+(tcgen05 tensor cores, TMA, Tensor Memory).  This module only marshals torch
+tensors into that C ABI: PyTorch supplies device memory and streams.
+
+    C = alpha * A @ B + beta * C       gemm(A, B, C, alpha, beta)
+    Y = silu(X @ Wg) * (X @ Wu)        gate_up_silu(X, Wg, Wu)
+
+Operands are K-contiguous: ``A`` is (M, K) and ``B`` is passed as its (N, K)
+storage, so ``gemm(A, B)`` equals ``A @ B.T`` in torch notation.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _native
+from ._native import (GEMM_ERR_ALIGNMENT, GEMM_ERR_CUDA, GEMM_ERR_INVALID_ARG,  # noqa: F401
+                      GEMM_ERR_TIMEOUT, GEMM_ERR_UNSUPPORTED, GEMM_OK, GEMM_OUT_BF16,
+                      GEMM_OUT_F32, GemmError)
+
+__all__ = ["gemm", "gate_up_silu", "device_status", "plan", "gate_up_plan", "prepare",
+           "GemmError", "library_path"]
+
+_OUT_CODES = {torch.float32: GEMM_OUT_F32, torch.bfloat16: GEMM_OUT_BF16}
+
+
+def library_path() -> str:
+    return _native.library_path()
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _check_operand(name, t, dtype=torch.bfloat16):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != 2 or (t.numel() > 0 and t.stride(1) != 1):
+        raise ValueError(f"{name} must be 2-D with a contiguous last dimension")
+
+
+def _ld(t) -> int:
+    return max(t.stride(0), t.shape[1]) if t.numel() > 0 else t.shape[1]
+
+
+def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
+         alpha: float = 1.0, beta: float = 0.0, out_dtype: torch.dtype | None = None,
+         stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """``C = alpha * A.B + beta * C`` with FP32 accumulation.
+
+    A: (M, K) bfloat16.  B: (N, K) bfloat16 (the K-contiguous storage of the
+    (K, N) operand).  C: (M, N) float32 or bfloat16; created when None (then
+    ``beta`` must be 0).  Asynchronous on ``stream`` (default: current stream).
+    """
+    _check_operand("A", A)
+    _check_operand("B", B)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: A has K={K}, B has K={K2}")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs an input C")
+        C = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=A.device)
+    else:
+        if out_dtype is not None and C.dtype != out_dtype:
+            raise TypeError("C dtype and out_dtype differ")
+        _check_operand("C", C, C.dtype if C.dtype in _OUT_CODES else torch.float32)
+        if tuple(C.shape) != (M, N):
+            raise ValueError(f"C must be ({M}, {N})")
+    code = _OUT_CODES[C.dtype]
+    with torch.cuda.device(A.device):
+        st = _native.gemm_bf16(M, N, K, float(alpha), A.data_ptr(), _ld(A), B.data_ptr(), _ld(B),
+                               float(beta), C.data_ptr(), _ld(C), code, _stream(stream, A.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_bf16")
+    return C
+
+
+def gate_up_silu(X: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor,
+                 Y: torch.Tensor | None = None,
+                 stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """``Y = silu(X.Wg) * (X.Wu)``; X (M, K), Wg and Wu stored (N, K), Y (M, N), all bf16."""
+    _check_operand("X", X)
+    _check_operand("Wg", Wg)
+    _check_operand("Wu", Wu)
+    M, K = X.shape
+    N = Wg.shape[0]
+    if tuple(Wg.shape) != (N, K) or tuple(Wu.shape) != (N, K):
+        raise ValueError("Wg and Wu must both be (N, K)")
+    if Wg.stride(0) != Wu.stride(0):
+        raise ValueError("Wg and Wu must share a row pitch")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    else:
+        _check_operand("Y", Y)
+        if tuple(Y.shape) != (M, N):
+            raise ValueError(f"Y must be ({M}, {N})")
+    with torch.cuda.device(X.device):
+        st = _native.gemm_gate_up_silu(M, N, K, X.data_ptr(), _ld(X), Wg.data_ptr(),
+                                       Wu.data_ptr(), _ld(Wg), Y.data_ptr(), _ld(Y),
+                                       _stream(stream, X.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_gate_up_silu")
+    return Y
+
+
+def device_status(stream: torch.cuda.Stream | None = None, device=None):
+    """Synchronize ``stream`` and return (status, site) of the device status
+    word, clearing it."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        return _native.gemm_get_device_status(_stream(stream, dev))
+
+
+def prepare(max_n: int, stream: torch.cuda.Stream | None = None, device=None) -> None:
+    """Allocate the split-K workspace for M <= 16 calls up to ``max_n`` columns."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        st = _native.gemm_prepare(int(max_n), _stream(stream, dev))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_prepare")
+
+
+def plan(M: int, N: int, K: int, out_dtype: torch.dtype = torch.bfloat16, num_sms: int = 0) -> dict:
+    """How ``gemm`` would run a problem (host-side planning)."""
+    st, p = _native.gemm_bf16_plan(M, N, K, _OUT_CODES[out_dtype], num_sms)
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_bf16_plan")
+    return p.as_dict()
+
+
+def gate_up_plan(M: int, N: int, K: int, num_sms: int = 0) -> dict:
+    st, p = _native.gemm_gate_up_plan(M, N, K, num_sms)
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_gate_up_plan")
+    return p.as_dict()

@@ -1,0 +1,152 @@
+"""ctypes binding of the C ABI in ``include/gemm_bf16.h``.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  Loading fails loudly when the library has not been built; there is
+no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = 1
+GEMM_ERR_ALIGNMENT = 2
+GEMM_ERR_UNSUPPORTED = 3
+GEMM_ERR_CUDA = 4
+GEMM_ERR_TIMEOUT = 5
+
+GEMM_OUT_F32 = 0
+GEMM_OUT_BF16 = 1
+
+KERNEL_NAMES = {0: "none", 1: "tiled", 2: "skinny_splitk", 3: "scale", 4: "gate_up"}
+
+# Every symbol the header declares.
+EXPORTED = (
+    "gemm_bf16",
+    "gemm_gate_up_silu",
+    "gemm_status_string",
+    "gemm_get_device_status",
+    "gemm_prepare",
+    "gemm_bf16_plan",
+    "gemm_gate_up_plan",
+    "gemm_selftest_wait_timeout",
+)
+
+
+class GemmPlan(ctypes.Structure):
+    _fields_ = [
+        ("kernel", ctypes.c_int),
+        ("tile_m", ctypes.c_int),
+        ("tile_n", ctypes.c_int),
+        ("tile_k", ctypes.c_int),
+        ("stages", ctypes.c_int),
+        ("split_k", ctypes.c_int),
+        ("tiles", ctypes.c_int64),
+        ("grid", ctypes.c_int),
+        ("smem_bytes", ctypes.c_int),
+        ("launches", ctypes.c_int),
+        ("stage_tx_bytes", ctypes.c_int64),
+    ]
+
+    def as_dict(self) -> dict:
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d["kernel_name"] = KERNEL_NAMES.get(self.kernel, "?")
+        return d
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = status_string(status) if _lib is not None else str(status)
+        super().__init__(f"{what}: {msg} (status {status})" if what else msg)
+
+
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+_f32 = ctypes.c_float
+_int = ctypes.c_int
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library {path} is missing: build it with "
+                    "`python -m dense_bf16_gemm_gb300.build` (there is no CPU fallback)")
+            l = ctypes.CDLL(path)
+            l.gemm_bf16.restype = _int
+            l.gemm_bf16.argtypes = [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32,
+                                    _vp, _i64, _int, _vp]
+            l.gemm_gate_up_silu.restype = _int
+            l.gemm_gate_up_silu.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64,
+                                            _vp, _i64, _vp]
+            l.gemm_status_string.restype = ctypes.c_char_p
+            l.gemm_status_string.argtypes = [_int]
+            l.gemm_get_device_status.restype = _int
+            l.gemm_get_device_status.argtypes = [_vp, ctypes.POINTER(_int)]
+            l.gemm_prepare.restype = _int
+            l.gemm_prepare.argtypes = [_i64, _vp]
+            l.gemm_bf16_plan.restype = _int
+            l.gemm_bf16_plan.argtypes = [_i64, _i64, _i64, _int, _int, ctypes.POINTER(GemmPlan)]
+            l.gemm_selftest_wait_timeout.restype = _int
+            l.gemm_selftest_wait_timeout.argtypes = [_i64, _vp]
+            l.gemm_gate_up_plan.restype = _int
+            l.gemm_gate_up_plan.argtypes = [_i64, _i64, _i64, _int, ctypes.POINTER(GemmPlan)]
+            _lib = l
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gemm_status_string(int(status)).decode()
+
+
+def gemm_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, out_dtype, stream) -> int:
+    """Raw C call; pointers and the stream are integers (0 = NULL)."""
+    return lib().gemm_bf16(M, N, K, alpha, A or None, lda, B or None, ldb, beta, C or None,
+                           ldc, out_dtype, stream or None)
+
+
+def gemm_gate_up_silu(M, N, K, X, ldx, Wg, Wu, ldw, Y, ldy, stream) -> int:
+    return lib().gemm_gate_up_silu(M, N, K, X or None, ldx, Wg or None, Wu or None, ldw,
+                                   Y or None, ldy, stream or None)
+
+
+def gemm_get_device_status(stream=0):
+    site = _int(0)
+    st = lib().gemm_get_device_status(stream or None, ctypes.byref(site))
+    return st, site.value
+
+
+def gemm_prepare(max_n: int, stream=0) -> int:
+    return lib().gemm_prepare(max_n, stream or None)
+
+
+def gemm_selftest_wait_timeout(limit_ns: int, stream=0) -> int:
+    return lib().gemm_selftest_wait_timeout(limit_ns, stream or None)
+
+
+def gemm_bf16_plan(M, N, K, out_dtype=GEMM_OUT_BF16, num_sms=0):
+    plan = GemmPlan()
+    st = lib().gemm_bf16_plan(M, N, K, out_dtype, num_sms, ctypes.byref(plan))
+    return st, plan
+
+
+def gemm_gate_up_plan(M, N, K, num_sms=0):
+    plan = GemmPlan()
+    st = lib().gemm_gate_up_plan(M, N, K, num_sms, ctypes.byref(plan))
+    return st, plan

@@ -1,0 +1,663 @@
+// gemm_api.cu -- host side of the library: argument validation, tile
+// planning, TMA descriptor encoding (cuTensorMapEncodeTiled, 128-byte
+// swizzle) with a descriptor cache, kernel launch and the C ABI declared in
+// include/gemm_bf16.h.
+//
+// Descriptor contract ("TMA and Hopper WGMMA", section "The same storage
+// contract on both sides"): a descriptor names the element type, the tile
+// (box) shape, the inner axis and a 128-byte swizzle row; the box's inner
+// extent is one swizzle row (64 BF16 or 32 FP32) and its outer extent is at
+// most 256.  Section "The same storage contract on both sides" also states
+// that a descriptor stays valid while values change and must be re-encoded
+// for a new address or new dimensions: the cache key is therefore (address,
+// element type, dimensions, row pitch, box).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/gemm_bf16.h"
+#include "gemm_kernels.cuh"
+#include "gemm_skinny.cuh"
+
+namespace {
+
+using namespace gb3;
+
+// ----------------------------------------------------------------------------
+// Kernel configurations
+// ----------------------------------------------------------------------------
+constexpr int kTileN = 256;        // output columns per tile of the tiled GEMM
+constexpr int kStages = 4;         // ring depth of the tiled GEMM (48 KB per stage)
+constexpr int kGateUpStages = 4;   // gate/up: 16 KB X + 16 KB Wg + 16 KB Wu per stage
+constexpr int kSkinnyStages = 12;  // 18 KB per stage
+constexpr int kSkinnyMaxM = 16;
+constexpr int kGroupM = 16;
+
+using CfgF32 = GemmCfg<kTileN, kStages, EPI_F32>;
+using CfgBF16 = GemmCfg<kTileN, kStages, EPI_BF16>;
+using CfgGU = GemmCfg<256, kGateUpStages, EPI_GATE_UP>;
+using CfgSkinny = SkinnyCfg<kSkinnyStages>;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ----------------------------------------------------------------------------
+// Planning (pure host logic)
+// ----------------------------------------------------------------------------
+enum KernelKind { K_NONE = 0, K_TILED = 1, K_SKINNY = 2, K_SCALE = 3, K_GATE_UP = 4 };
+
+// Split of K for the skinny path: minimise the k-blocks of the busiest CTA,
+// ceil(units / grid) * ceil(k_blocks / S), with a small charge per extra split
+// for the partial-sum traffic.
+void choose_split(int64_t n_blocks, int64_t k_blocks, int sms, int* splits, int* kb_per) {
+  int best_s = 1;
+  double best = 1e300;
+  for (int s = 1; s <= 32; ++s) {
+    const int64_t kbp = ceil_div(k_blocks, s);
+    if (s > 1 && kbp < 4) break;
+    const int64_t real_s = ceil_div(k_blocks, kbp);  // splits that get work
+    if (real_s != s) continue;
+    const int64_t units = n_blocks * s;
+    const double cost = static_cast<double>(ceil_div(units, sms)) * static_cast<double>(kbp) +
+                        0.5 * static_cast<double>(s - 1);
+    if (cost < best) {
+      best = cost;
+      best_s = s;
+    }
+  }
+  *splits = best_s;
+  *kb_per = static_cast<int>(ceil_div(k_blocks, best_s));
+}
+
+int plan_gemm(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl) {
+  std::memset(pl, 0, sizeof(*pl));
+  pl->split_k = 1;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (K == 0) {
+    pl->kernel = K_SCALE;
+    pl->tiles = 1;
+    pl->grid = static_cast<int>(std::min<int64_t>(ceil_div(M * N, 256), 4 * sms));
+    pl->launches = 1;
+    return GEMM_OK;
+  }
+  pl->tile_k = kBK;
+  if (M <= kSkinnyMaxM) {
+    const int64_t nb = ceil_div(N, kSkinnyRows), kb = ceil_div(K, kBK);
+    int s, kbp;
+    choose_split(nb, kb, sms, &s, &kbp);
+    pl->kernel = K_SKINNY;
+    pl->tile_m = kSkinnyRows;
+    pl->tile_n = kSkinnyNX;
+    pl->stages = kSkinnyStages;
+    pl->split_k = s;
+    pl->tiles = nb * s;
+    pl->grid = static_cast<int>(std::min<int64_t>(pl->tiles, sms));
+    pl->smem_bytes = CfgSkinny::kSmemBytes;
+    pl->launches = 1;
+    pl->stage_tx_bytes = CfgSkinny::kStageBytes;
+    return GEMM_OK;
+  }
+  pl->kernel = K_TILED;
+  pl->tile_m = kBM;
+  pl->tile_n = kTileN;
+  pl->stages = kStages;
+  pl->tiles = ceil_div(M, kBM) * ceil_div(N, kTileN);
+  pl->grid = static_cast<int>(std::min<int64_t>(pl->tiles, sms));
+  pl->smem_bytes = CfgBF16::kSmemBytes;
+  pl->launches = 1;
+  pl->stage_tx_bytes = CfgBF16::kStageBytes;
+  return GEMM_OK;
+}
+
+int plan_gate_up(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl) {
+  std::memset(pl, 0, sizeof(*pl));
+  pl->split_k = 1;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (K == 0) {
+    pl->kernel = K_SCALE;
+    pl->tiles = 1;
+    pl->grid = static_cast<int>(std::min<int64_t>(ceil_div(M * N, 256), 4 * sms));
+    pl->launches = 1;
+    return GEMM_OK;
+  }
+  pl->kernel = K_GATE_UP;
+  pl->tile_m = kBM;
+  pl->tile_n = CfgGU::kOutCols;
+  pl->tile_k = kBK;
+  pl->stages = kGateUpStages;
+  pl->tiles = ceil_div(M, kBM) * ceil_div(N, CfgGU::kOutCols);
+  pl->grid = static_cast<int>(std::min<int64_t>(pl->tiles, sms));
+  pl->smem_bytes = CfgGU::kSmemBytes;
+  pl->launches = 1;
+  pl->stage_tx_bytes = CfgGU::kStageBytes;
+  return GEMM_OK;
+}
+
+// ----------------------------------------------------------------------------
+// Validation (no CUDA calls)
+// ----------------------------------------------------------------------------
+constexpr int64_t kMaxDim = 0x7FFFFFFF;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                  int64_t ldb, float beta, const void* C, int64_t ldc, int out_dtype) {
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return GEMM_ERR_INVALID_ARG;
+  if (out_dtype != GEMM_OUT_F32 && out_dtype != GEMM_OUT_BF16) return GEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_OK;
+  const int64_t esize = out_dtype == GEMM_OUT_F32 ? 4 : 2;
+  if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
+  if (K > 0) {
+    if (A == nullptr || B == nullptr || lda < K || ldb < K) return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0)
+      return GEMM_ERR_ALIGNMENT;
+  }
+  if (!aligned16(C) || (ldc * esize) % 16 != 0) return GEMM_ERR_ALIGNMENT;
+  (void)beta;
+  return GEMM_OK;
+}
+
+int validate_gate_up(int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx, const void* Wg,
+                     const void* Wu, int64_t ldw, const void* Y, int64_t ldy) {
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return GEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (Y == nullptr || ldy < N) return GEMM_ERR_INVALID_ARG;
+  if (K > 0) {
+    if (X == nullptr || Wg == nullptr || Wu == nullptr || ldx < K || ldw < K)
+      return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Wg) || !aligned16(Wu) || (ldx * 2) % 16 != 0 ||
+        (ldw * 2) % 16 != 0)
+      return GEMM_ERR_ALIGNMENT;
+  }
+  if (!aligned16(Y) || (ldy * 2) % 16 != 0) return GEMM_ERR_ALIGNMENT;
+  return GEMM_OK;
+}
+
+// ----------------------------------------------------------------------------
+// Device state
+// ----------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool probed = false;
+  bool supported = false;
+  int sms = 0;
+  // kernels whose shared-memory limit has been raised on this device
+  std::vector<const void*> configured;
+  // split-K workspace of the skinny path
+  float* ws = nullptr;
+  size_t ws_bytes = 0;
+  int* counters = nullptr;
+  size_t counter_count = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (*dev < 0 || *dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED;
+  return GEMM_OK;
+}
+
+// Caller holds g_mu.
+int probe_device(int dev) {
+  DeviceState& d = g_dev[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    d.probed = true;
+    d.supported = (major == 10 && minor == 3);
+    d.sms = sms;
+  }
+  return d.supported ? GEMM_OK : GEMM_ERR_UNSUPPORTED;
+}
+
+int device_sms(int* sms) {
+  int dev;
+  int st = current_device(&dev);
+  if (st != GEMM_OK) return st;
+  std::lock_guard<std::mutex> lk(g_mu);
+  st = probe_device(dev);
+  if (st != GEMM_OK) return st;
+  *sms = g_dev[dev].sms;
+  return GEMM_OK;
+}
+
+// Caller holds g_mu.
+int ensure_smem_attr(int dev, const void* fn, int smem) {
+  DeviceState& d = g_dev[dev];
+  if (std::find(d.configured.begin(), d.configured.end(), fn) != d.configured.end())
+    return GEMM_OK;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  d.configured.push_back(fn);
+  return GEMM_OK;
+}
+
+// Caller holds g_mu.  Grows the split-K workspace; refuses to allocate while
+// the stream is being captured.
+int ensure_workspace(int dev, size_t ws_bytes, size_t counters, cudaStream_t stream) {
+  DeviceState& d = g_dev[dev];
+  if (d.ws_bytes >= ws_bytes && d.counter_count >= counters) return GEMM_OK;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return GEMM_ERR_CUDA;
+  // Work already queued may still use the old buffers.
+  if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
+  if (d.ws_bytes < ws_bytes) {
+    if (d.ws) cudaFree(d.ws);
+    d.ws = nullptr;
+    d.ws_bytes = 0;
+    if (cudaMalloc(&d.ws, ws_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    d.ws_bytes = ws_bytes;
+  }
+  if (d.counter_count < counters) {
+    if (d.counters) cudaFree(d.counters);
+    d.counters = nullptr;
+    d.counter_count = 0;
+    if (cudaMalloc(&d.counters, counters * sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    if (cudaMemset(d.counters, 0, counters * sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    d.counter_count = counters;
+  }
+  return GEMM_OK;
+}
+
+// ----------------------------------------------------------------------------
+// Tensor-map descriptors
+// ----------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+struct MapKey {
+  const void* ptr;
+  int dtype;
+  uint64_t inner, outer, pitch;
+  uint32_t box_inner, box_outer;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && dtype == o.dtype && inner == o.inner && outer == o.outer &&
+           pitch == o.pitch && box_inner == o.box_inner && box_outer == o.box_outer;
+  }
+};
+
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  uint64_t used;
+};
+
+constexpr size_t kMapCacheSize = 64;
+std::mutex g_map_mu;
+std::vector<MapEntry> g_maps;
+uint64_t g_map_clock = 0;
+
+// 2-D map over a row-major matrix of `outer` rows of `inner` elements with a
+// row pitch of `pitch` bytes; box of box_inner x box_outer elements, 128-byte
+// swizzle, out-of-bounds elements read as zero.
+int tensor_map_2d(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, uint64_t inner,
+                  uint64_t outer, uint64_t pitch, uint32_t box_inner, uint32_t box_outer) {
+  const MapKey key{ptr, static_cast<int>(dtype), inner, outer, pitch, box_inner, box_outer};
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  for (MapEntry& e : g_maps) {
+    if (e.key == key) {
+      e.used = ++g_map_clock;
+      *out = e.map;
+      return GEMM_OK;
+    }
+  }
+  auto fn = encode_fn();
+  if (fn == nullptr) return GEMM_ERR_CUDA;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {pitch};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estrides[2] = {1, 1};
+  const CUresult r = fn(&map, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estrides,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return GEMM_ERR_CUDA;
+  if (g_maps.size() < kMapCacheSize) {
+    g_maps.push_back(MapEntry{key, map, ++g_map_clock});
+  } else {
+    auto victim = std::min_element(g_maps.begin(), g_maps.end(),
+                                   [](const MapEntry& a, const MapEntry& b) { return a.used < b.used; });
+    *victim = MapEntry{key, map, ++g_map_clock};
+  }
+  *out = map;
+  return GEMM_OK;
+}
+
+// ----------------------------------------------------------------------------
+// Launch
+// ----------------------------------------------------------------------------
+template <typename... ExpT, typename... ActT>
+int launch(void (*kernel)(ExpT...), int grid, int block, int smem, cudaStream_t stream,
+           ActT&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(block), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  if (cudaLaunchKernelEx(&cfg, kernel, std::forward<ActT>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  return GEMM_OK;
+}
+
+// C = beta * C (K == 0); C is not read when beta == 0.
+__global__ void scale_kernel(void* C, long long ldc, int M, int N, float beta, int bf16) {
+  const long long total = static_cast<long long>(M) * N;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long m = i / N, n = i % N;
+    const long long off = m * ldc + n;
+    if (bf16) {
+      uint16_t* c = static_cast<uint16_t*>(C);
+      const float v = beta == 0.0f ? 0.0f : beta * bf16_bits_to_float(c[off]);
+      c[off] = static_cast<uint16_t>(pack_bf16x2(v, 0.0f) & 0xFFFFu);
+    } else {
+      float* c = static_cast<float*>(C);
+      c[off] = beta == 0.0f ? 0.0f : beta * c[off];
+    }
+  }
+}
+
+int run_scale(const gemm_plan& pl, void* C, int64_t ldc, int64_t M, int64_t N, float beta,
+              bool bf16, cudaStream_t stream) {
+  return launch(scale_kernel, pl.grid, 256, 0, stream, C, static_cast<long long>(ldc),
+                static_cast<int>(M), static_cast<int>(N), beta, bf16 ? 1 : 0);
+}
+
+TileParams tile_params(int64_t M, int64_t N, int64_t K, int tile_n_out, float alpha, float beta,
+                       const void* C, int64_t ldc, int64_t tiles) {
+  TileParams p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.m_blocks = static_cast<int>(ceil_div(M, kBM));
+  p.n_blocks = static_cast<int>(ceil_div(N, tile_n_out));
+  p.k_blocks = static_cast<int>(ceil_div(K, kBK));
+  p.num_tiles = static_cast<int>(tiles);
+  p.group_m = kGroupM;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.C = C;
+  p.ldc = ldc;
+  return p;
+}
+
+}  // namespace
+
+// ============================================================================
+// C ABI
+// ============================================================================
+extern "C" {
+
+const char* gemm_status_string(int status) {
+  switch (status) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_ALIGNMENT: return "pointer or row pitch not 16-byte aligned";
+    case GEMM_ERR_UNSUPPORTED: return "unsupported device (needs compute capability 10.3)";
+    case GEMM_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case GEMM_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int num_sms,
+                   gemm_plan* plan) {
+  if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return GEMM_ERR_INVALID_ARG;
+  if (out_dtype != GEMM_OUT_F32 && out_dtype != GEMM_OUT_BF16) return GEMM_ERR_INVALID_ARG;
+  if (num_sms <= 0) {
+    const int st = device_sms(&num_sms);
+    if (st != GEMM_OK) return st;
+  }
+  return plan_gemm(M, N, K, num_sms, plan);
+}
+
+int gemm_gate_up_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_plan* plan) {
+  if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return GEMM_ERR_INVALID_ARG;
+  if (num_sms <= 0) {
+    const int st = device_sms(&num_sms);
+    if (st != GEMM_OK) return st;
+  }
+  return plan_gate_up(M, N, K, num_sms, plan);
+}
+
+int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+              const void* B, int64_t ldb, float beta, void* C, int64_t ldc, int out_dtype,
+              void* stream_) {
+  int st = validate_gemm(M, N, K, A, lda, B, ldb, beta, C, ldc, out_dtype);
+  if (st != GEMM_OK) return st;
+  if (M == 0 || N == 0) return GEMM_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev;
+  if ((st = current_device(&dev)) != GEMM_OK) return st;
+  int sms;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = probe_device(dev)) != GEMM_OK) return st;
+    sms = g_dev[dev].sms;
+  }
+  gemm_plan pl;
+  plan_gemm(M, N, K, sms, &pl);
+  const bool bf16 = out_dtype == GEMM_OUT_BF16;
+
+  if (pl.kernel == K_SCALE) return run_scale(pl, C, ldc, M, N, beta, bf16, stream);
+
+  if (pl.kernel == K_SKINNY) {
+    CUtensorMap tmW, tmX;
+    if ((st = tensor_map_2d(&tmW, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldb * 2, kBK,
+                            kSkinnyRows)) != GEMM_OK)
+      return st;
+    if ((st = tensor_map_2d(&tmX, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, lda * 2, kBK,
+                            kSkinnyNX)) != GEMM_OK)
+      return st;
+    SkinnyParams p;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.n_blocks = static_cast<int>(ceil_div(N, kSkinnyRows));
+    p.k_blocks = static_cast<int>(ceil_div(K, kBK));
+    p.splits = pl.split_k;
+    p.kb_per_split = static_cast<int>(ceil_div(p.k_blocks, p.splits));
+    p.num_units = static_cast<int>(pl.tiles);
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = C;
+    p.ldc = ldc;
+    p.out_bf16 = bf16 ? 1 : 0;
+    p.ws = nullptr;
+    p.counters = nullptr;
+    auto kern = gemm_skinny_kernel<kSkinnyStages>;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if ((st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), pl.smem_bytes)) !=
+          GEMM_OK)
+        return st;
+      if (p.splits > 1) {
+        const size_t ws_bytes = static_cast<size_t>(p.splits) * M * N * sizeof(float);
+        const size_t counters = static_cast<size_t>(p.n_blocks) * 4;
+        if ((st = ensure_workspace(dev, ws_bytes, counters, stream)) != GEMM_OK) return st;
+        p.ws = g_dev[dev].ws;
+        p.counters = g_dev[dev].counters;
+      }
+    }
+    return launch(kern, pl.grid, kThreads, pl.smem_bytes, stream, tmW, tmX, p);
+  }
+
+  // Tiled tcgen05 GEMM.
+  CUtensorMap tmA, tmB, tmOut;
+  if ((st = tensor_map_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, lda * 2, kBK, kBM)) !=
+      GEMM_OK)
+    return st;
+  if ((st = tensor_map_2d(&tmB, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldb * 2, kBK,
+                          kTileN)) != GEMM_OK)
+    return st;
+  if (bf16) {
+    st = tensor_map_2d(&tmOut, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldc * 2, 64, 32);
+  } else {
+    st = tensor_map_2d(&tmOut, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, M, ldc * 4, 32, 32);
+  }
+  if (st != GEMM_OK) return st;
+  const TileParams p = tile_params(M, N, K, kTileN, alpha, beta, C, ldc, pl.tiles);
+  if (bf16) {
+    auto kern = gemm_tc_kernel<kTileN, kStages, EPI_BF16>;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if ((st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern),
+                                 CfgBF16::kSmemBytes)) != GEMM_OK)
+        return st;
+    }
+    return launch(kern, pl.grid, kThreads, CfgBF16::kSmemBytes, stream, tmA, tmB, tmB, tmOut, p);
+  }
+  auto kern = gemm_tc_kernel<kTileN, kStages, EPI_F32>;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), CfgF32::kSmemBytes)) !=
+        GEMM_OK)
+      return st;
+  }
+  return launch(kern, pl.grid, kThreads, CfgF32::kSmemBytes, stream, tmA, tmB, tmB, tmOut, p);
+}
+
+int gemm_gate_up_silu(int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx,
+                      const void* Wg, const void* Wu, int64_t ldw, void* Y, int64_t ldy,
+                      void* stream_) {
+  int st = validate_gate_up(M, N, K, X, ldx, Wg, Wu, ldw, Y, ldy);
+  if (st != GEMM_OK) return st;
+  if (M == 0 || N == 0) return GEMM_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev;
+  if ((st = current_device(&dev)) != GEMM_OK) return st;
+  int sms;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = probe_device(dev)) != GEMM_OK) return st;
+    sms = g_dev[dev].sms;
+  }
+  gemm_plan pl;
+  plan_gate_up(M, N, K, sms, &pl);
+  if (pl.kernel == K_SCALE) return run_scale(pl, Y, ldy, M, N, 0.0f, true, stream);
+
+  CUtensorMap tmX, tmWg, tmWu, tmY;
+  if ((st = tensor_map_2d(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, ldx * 2, kBK, kBM)) !=
+      GEMM_OK)
+    return st;
+  if ((st = tensor_map_2d(&tmWg, Wg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldw * 2, kBK,
+                          CfgGU::kOutCols)) != GEMM_OK)
+    return st;
+  if ((st = tensor_map_2d(&tmWu, Wu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldw * 2, kBK,
+                          CfgGU::kOutCols)) != GEMM_OK)
+    return st;
+  if ((st = tensor_map_2d(&tmY, Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldy * 2, 64, 32)) !=
+      GEMM_OK)
+    return st;
+  const TileParams p = tile_params(M, N, K, CfgGU::kOutCols, 1.0f, 0.0f, nullptr, ldy, pl.tiles);
+  auto kern = gemm_tc_kernel<256, kGateUpStages, EPI_GATE_UP>;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), CfgGU::kSmemBytes)) !=
+        GEMM_OK)
+      return st;
+  }
+  return launch(kern, pl.grid, kThreads, CfgGU::kSmemBytes, stream, tmX, tmWg, tmWu, tmY, p);
+}
+
+int gemm_get_device_status(void* stream, int* site) {
+  int dev;
+  int st = current_device(&dev);
+  if (st != GEMM_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  int h[4] = {0, 0, 0, 0};
+  const int zero[4] = {0, 0, 0, 0};
+  if (cudaMemcpyFromSymbol(h, g_gemm_status, sizeof(h)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_gemm_status, zero, sizeof(zero)) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (site != nullptr) *site = h[1];
+  return h[0];
+}
+
+int gemm_selftest_wait_timeout(int64_t limit_ns, void* stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000) return GEMM_ERR_INVALID_ARG;
+  int dev;
+  int st = current_device(&dev);
+  if (st != GEMM_OK) return st;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = probe_device(dev)) != GEMM_OK) return st;
+  }
+  return launch(wait_timeout_probe_kernel, 1, 32, 0, static_cast<cudaStream_t>(stream),
+                static_cast<unsigned long long>(limit_ns));
+}
+
+int gemm_prepare(int64_t max_N, void* stream) {
+  if (max_N < 0 || max_N > kMaxDim) return GEMM_ERR_INVALID_ARG;
+  int dev;
+  int st = current_device(&dev);
+  if (st != GEMM_OK) return st;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if ((st = probe_device(dev)) != GEMM_OK) return st;
+  // Largest split the planner can choose is 32.
+  const int64_t nb = ceil_div(std::max<int64_t>(max_N, 1), kSkinnyRows);
+  const size_t ws_bytes = static_cast<size_t>(32) * kSkinnyMaxM * max_N * sizeof(float);
+  return ensure_workspace(dev, ws_bytes, static_cast<size_t>(nb) * 4,
+                          static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,475 @@
+// gemm_kernels.cuh -- persistent, warp-specialised tcgen05 GEMM kernels for
+// sm_103a.
+//
+//   warp 0      TMA producer: one thread streams A and B k-blocks into a
+//               STAGES-deep shared-memory ring (full/empty mbarriers with
+//               transaction counts).
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (BF16 x BF16 -> FP32)
+//               into one of two TMEM accumulators and commits completion to
+//               the ring's empty barriers and to the accumulator's full
+//               barrier.  The same warp allocates and frees TMEM.
+//   warps 2-5   epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (the row band
+//               it may access) with tcgen05.ld, applies alpha/beta or
+//               silu(gate)*up in FP32, packs, stages the tile in 128-byte
+//               swizzled shared memory and writes it with TMA stores.
+//
+// Two accumulators let the epilogue of one tile overlap the main loop of the
+// next.  Tiles are visited by a static persistent schedule (tile = blockIdx.x
+// + i*gridDim.x) in grouped row order for L2 reuse.
+//
+// Every pipeline wait is bounded: past kWaitLimitNs the waiting thread sets a
+// CTA abort flag and the device status word, every role leaves its loop, the
+// in-flight copies and MMAs are drained (again with a bound), TMEM is freed
+// and the kernel returns.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace gb3 {
+
+constexpr int kBM = 128;          // tile rows = tcgen05 M (cta_group::1)
+constexpr int kBK = 64;           // K per stage: one 128-byte swizzle row of BF16
+constexpr int kUmmaK = 16;        // K of one tcgen05.mma kind::f16
+constexpr int kThreads = 192;     // 6 warps
+constexpr int kEpiWarps = 4;
+constexpr int kStageBox = 4096;   // one epilogue store box: 32 rows x 128 bytes
+constexpr int kStagingPerWarp = 2;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+enum EpiMode : int { EPI_F32 = 0, EPI_BF16 = 1, EPI_GATE_UP = 2 };
+
+enum WaitSite : int {
+  SITE_PRODUCER_EMPTY = 1,
+  SITE_MMA_FULL = 2,
+  SITE_MMA_ACC_EMPTY = 3,
+  SITE_EPI_ACC_FULL = 4,
+  SITE_DRAIN = 5,
+  SITE_SKINNY = 6,
+  SITE_SELFTEST = 7
+};
+
+// [0] status code, [1] wait site, [2] block index of the first failure.
+__device__ int g_gemm_status[4];
+
+__device__ __noinline__ void record_timeout(int site) {
+  if (atomicCAS(&g_gemm_status[0], 0, 5) == 0) {
+    g_gemm_status[1] = site;
+    g_gemm_status[2] = static_cast<int>(blockIdx.x);
+  }
+}
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       int site, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (abort_flag != nullptr && *abort_flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        if (abort_flag != nullptr) *abort_flag = 1;
+        record_timeout(site);
+        return false;
+      }
+    }
+  }
+}
+
+// Waits for the phase of parity `parity` of `bar` to complete.  Returns false
+// if the CTA aborted or the wait exceeded its limit.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag, int site,
+                                             uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, abort_flag, site, limit_ns);
+}
+
+// Self-test of the failure path: one thread waits on a barrier nothing
+// arrives on, so the wait runs out after limit_ns and records
+// GEMM_ERR_TIMEOUT with site SITE_SELFTEST.  Uses no TMA and no TMEM.
+__global__ void wait_timeout_probe_kernel(unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    wait_bounded(smem_u32(&bar), 0, &abort_flag, SITE_SELFTEST, limit_ns);
+  }
+}
+
+struct TileParams {
+  int M, N, K;
+  int m_blocks, n_blocks, k_blocks;
+  int num_tiles;
+  int group_m;
+  float alpha, beta;
+  const void* C;      // read when beta != 0 (same storage as the output)
+  long long ldc;      // elements
+};
+
+// Grouped raster: group_m consecutive row blocks share each column block.
+__device__ __forceinline__ void tile_coords(int tile, const TileParams& p, int& mb, int& nb) {
+  const int span = p.group_m * p.n_blocks;
+  const int g = tile / span;
+  const int first = g * p.group_m;
+  const int rows = min(p.m_blocks - first, p.group_m);
+  const int r = tile - g * span;
+  mb = first + r % rows;
+  nb = r / rows;
+}
+
+template <int BN, int STAGES, int EPI>
+struct GemmCfg {
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile width");
+  static constexpr int kABytes = kBM * kBK * 2;  // 16 KB
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kRingBytes = STAGES * kStageBytes;
+  static constexpr int kStagingBytes = kEpiWarps * kStagingPerWarp * kStageBox;
+  static constexpr int kBarOffset = kRingBytes + kStagingBytes;
+  // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
+  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+  static constexpr int kOutCols = (EPI == EPI_GATE_UP) ? BN / 2 : BN;
+  static constexpr int kAccStride = 256;  // TMEM columns between the two accumulators
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// Epilogue arithmetic for one 32-column slice of a thread's row.
+template <int EPI>
+__device__ __forceinline__ void scale_slice(float (&v)[32], const TileParams& p, int row,
+                                            int col0) {
+  const float alpha = p.alpha;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] *= alpha;
+  if (p.beta != 0.0f && row < p.M) {
+    const float beta = p.beta;
+    if constexpr (EPI == EPI_F32) {
+      const float* c = static_cast<const float*>(p.C) + static_cast<long long>(row) * p.ldc + col0;
+      if (col0 + 32 <= p.N) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 x = reinterpret_cast<const float4*>(c)[q];
+          v[4 * q + 0] += beta * x.x;
+          v[4 * q + 1] += beta * x.y;
+          v[4 * q + 2] += beta * x.z;
+          v[4 * q + 3] += beta * x.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col0 + i < p.N) v[i] += beta * c[i];
+      }
+    } else {
+      const uint16_t* c =
+          static_cast<const uint16_t*>(p.C) + static_cast<long long>(row) * p.ldc + col0;
+      if (col0 + 32 <= p.N) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 x = reinterpret_cast<const uint4*>(c)[q];
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            v[8 * q + 2 * j + 0] += beta * bf16_bits_to_float(w[j] & 0xFFFFu);
+            v[8 * q + 2 * j + 1] += beta * bf16_bits_to_float(w[j] >> 16);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col0 + i < p.N) v[i] += beta * bf16_bits_to_float(c[i]);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + __expf(-g)); }
+
+template <int BN, int STAGES, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmB2,
+                   const __grid_constant__ CUtensorMap tmOut, const TileParams p) {
+  using Cfg = GemmCfg<BN, STAGES, EPI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOffset);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    if constexpr (EPI == EPI_GATE_UP) prefetch_tensormap(&tmB2);
+    prefetch_tensormap(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, p, mb, nb);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint32_t a_dst = sbase + s * Cfg::kStageBytes;
+          const uint32_t b_dst = a_dst + Cfg::kABytes;
+          mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);
+          tma_load_2d(a_dst, &tmA, full_bar(s), kb * kBK, mb * kBM);
+          if constexpr (EPI == EPI_GATE_UP) {
+            tma_load_2d(b_dst, &tmB, full_bar(s), kb * kBK, nb * (BN / 2));
+            tma_load_2d(b_dst + Cfg::kBBytes / 2, &tmB2, full_bar(s), kb * kBK, nb * (BN / 2));
+          } else {
+            tma_load_2d(b_dst, &tmB, full_bar(s), kb * kBK, nb * BN);
+          }
+          ++issued;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      {
+        // Let the copies already issued land before shared memory goes away
+        // (they have, unless a wait gave up; then this waits, bounded, for
+        // the last STAGES of them).
+        const long long first = issued > STAGES ? issued - STAGES : 0;
+        for (long long i = first; i < issued; ++i)
+          wait_bounded(full_bar(static_cast<int>(i % STAGES)),
+                       static_cast<uint32_t>((i / STAGES) & 1), nullptr, SITE_DRAIN);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
+        if (!wait_bounded(acce_bar(buf), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_bounded(full_bar(s), ph, abort_flag, SITE_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_addr = sbase + s * Cfg::kStageBytes;
+          const uint64_t adesc = smem_desc_sw128(a_addr);
+          const uint64_t bdesc = smem_desc_sw128(a_addr + Cfg::kABytes);
+#pragma unroll
+          for (int j = 0; j < kBK / kUmmaK; ++j) {
+            // +32 bytes along K inside the swizzled row = +2 in the address field.
+            umma_bf16(d_tmem, adesc + 2u * j, bdesc + 2u * j, Cfg::kIdesc,
+                      (kb | j) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(s));
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(accf_bar(buf));
+      }
+      // Every MMA issued by this thread has completed once this arrives.
+      umma_commit(drain_bar);
+      wait_bounded(drain_bar, 0, nullptr, SITE_DRAIN);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;                 // staging slot owner
+    const int band = (warp & 3) * 32;        // TMEM lanes this warp may access
+    const uint32_t staging = sbase + Cfg::kRingBytes + ew * kStagingPerWarp * kStageBox;
+    const uint32_t swz = static_cast<uint32_t>(lane & 7);
+    const uint32_t row_off = static_cast<uint32_t>(lane) * 128u;
+    int local = 0;
+    int sc = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+      int mb, nb;
+      tile_coords(tile, p, mb, nb);
+      const int buf = local & 1;
+      const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
+      const bool got = wait_bounded(accf_bar(buf), aph, abort_flag, SITE_EPI_ACC_FULL);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after_sync();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(band) << 16) +
+                            static_cast<uint32_t>(buf * Cfg::kAccStride);
+      const int m0 = mb * kBM + band;
+      const int row = m0 + lane;
+      const bool have_acc = p.k_blocks > 0;
+
+      if constexpr (EPI == EPI_F32) {
+        const int n0 = nb * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          // Boxes wholly outside C are neither computed nor stored (warp-uniform).
+          if (m0 >= p.M || n0 + c0 >= p.N) continue;
+          const uint32_t stg = staging + (sc & 1) * kStageBox;
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+          float v[32];
+          if (have_acc) {
+            tmem_load_32x32b_x32(tacc + c0, v);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+          }
+          scale_slice<EPI>(v, p, row, n0 + c0);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(stg + row_off + ((static_cast<uint32_t>(q) ^ swz) << 4),
+                         __float_as_uint(v[4 * q + 0]), __float_as_uint(v[4 * q + 1]),
+                         __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
+          fence_proxy_async_shared();
+          __syncwarp();
+          // Every staged box is stored and committed as its own bulk group, so
+          // wait_group.read<1> above always refers to this buffer's last store.
+          if (lane == 0) {
+            tma_store_2d(&tmOut, stg, n0 + c0, m0);
+            bulk_commit_group();
+          }
+          ++sc;
+        }
+      } else if constexpr (EPI == EPI_BF16) {
+        const int n0 = nb * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 64) {
+          if (m0 >= p.M || n0 + c0 >= p.N) continue;
+          const uint32_t stg = staging + (sc & 1) * kStageBox;
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float v[32];
+            if (have_acc) {
+              tmem_load_32x32b_x32(tacc + c0 + 32 * h, v);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+            }
+            scale_slice<EPI>(v, p, row, n0 + c0 + 32 * h);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t chunk = static_cast<uint32_t>(4 * h + q);
+              st_shared_v4(stg + row_off + ((chunk ^ swz) << 4),
+                           pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
+                           pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                           pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+            }
+          }
+          fence_proxy_async_shared();
+          __syncwarp();
+          // Every staged box is stored and committed as its own bulk group, so
+          // wait_group.read<1> above always refers to this buffer's last store.
+          if (lane == 0) {
+            tma_store_2d(&tmOut, stg, n0 + c0, m0);
+            bulk_commit_group();
+          }
+          ++sc;
+        }
+      } else {
+        // gate/up: accumulator columns [0, BN/2) hold X.Wg, [BN/2, BN) hold X.Wu.
+        const int n0 = nb * (BN / 2);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN / 2; c0 += 64) {
+          if (m0 >= p.M || n0 + c0 >= p.N) continue;
+          const uint32_t stg = staging + (sc & 1) * kStageBox;
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float g[32], u[32];
+            if (have_acc) {
+              tmem_load_32x32b_x32(tacc + c0 + 32 * h, g);
+              tmem_load_32x32b_x32(tacc + BN / 2 + c0 + 32 * h, u);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) g[i] = u[i] = 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) g[i] = silu_f32(g[i]) * u[i];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t chunk = static_cast<uint32_t>(4 * h + q);
+              st_shared_v4(stg + row_off + ((chunk ^ swz) << 4),
+                           pack_bf16x2(g[8 * q + 0], g[8 * q + 1]),
+                           pack_bf16x2(g[8 * q + 2], g[8 * q + 3]),
+                           pack_bf16x2(g[8 * q + 4], g[8 * q + 5]),
+                           pack_bf16x2(g[8 * q + 6], g[8 * q + 7]));
+            }
+          }
+          fence_proxy_async_shared();
+          __syncwarp();
+          // Every staged box is stored and committed as its own bulk group, so
+          // wait_group.read<1> above always refers to this buffer's last store.
+          if (lane == 0) {
+            tma_store_2d(&tmOut, stg, n0 + c0, m0);
+            bulk_commit_group();
+          }
+          ++sc;
+        }
+      }
+      // The accumulator may be overwritten once every lane's TMEM reads are done.
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(buf));
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace gb3

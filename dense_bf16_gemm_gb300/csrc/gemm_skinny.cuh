@@ -1,0 +1,278 @@
+// gemm_skinny.cuh -- decode-shaped GEMM (M <= 16) on the tensor cores, bound by
+// the HBM stream of B.
+//
+// The operands are swapped: C^T = B^T-stored-as-(N,K) times A^T, so the long
+// weight dimension N fills the 128-row M side of tcgen05.mma and the M <= 16
+// activation rows become its N = 16 side.  Both operands are K-contiguous, so
+// the swap needs no data movement.
+//
+// Work units are (128-row block of B, slice of K).  Each unit's FP32 partial
+// (16 x 128) goes to a workspace; the last unit to finish a block (counted
+// per 32-row band with an atomic) adds the partials in split order 0..S-1,
+// applies alpha/beta and writes C, so the result does not depend on which
+// unit finishes last.  No CTA waits for another.
+//
+// Roles as in the tiled kernel: warp 0 TMA producer, warp 1 MMA issuer and
+// TMEM owner, warps 2-5 epilogue (warp w reads TMEM lanes 32*(w%4)..+31, i.e.
+// rows n of B; lane i holds the 16 activation rows of output column n).
+#pragma once
+
+#include "gemm_kernels.cuh"
+
+namespace gb3 {
+
+constexpr int kSkinnyRows = 128;  // rows of B per unit (the MMA's M)
+constexpr int kSkinnyNX = 16;     // activation rows per MMA (the MMA's N)
+
+struct SkinnyParams {
+  int M, N, K;
+  int n_blocks, k_blocks;
+  int splits, kb_per_split;
+  int num_units;
+  float alpha, beta;
+  void* C;
+  long long ldc;
+  int out_bf16;
+  float* ws;      // [splits][M][N] FP32 partial sums (splits > 1)
+  int* counters;  // [n_blocks * 4] arrival counters, zero between calls
+};
+
+template <int STAGES>
+struct SkinnyCfg {
+  static constexpr int kWBytes = kSkinnyRows * kBK * 2;  // 16 KB
+  static constexpr int kXBytes = kSkinnyNX * kBK * 2;    // 2 KB
+  static constexpr int kStageBytes = kWBytes + kXBytes;  // 18 KB, keeps 1024-byte alignment
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+  static constexpr int kRingBytes = STAGES * kStageBytes;
+  static constexpr int kBarOffset = kRingBytes;
+  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+  static constexpr int kAccStride = kSkinnyNX;
+  static constexpr int kTmemCols = 32;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(kSkinnyRows, kSkinnyNX);
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ void skinny_unit(int u, const SkinnyParams& p, int& nb, int& sp,
+                                            int& kb0, int& kb1) {
+  nb = u % p.n_blocks;
+  sp = u / p.n_blocks;
+  kb0 = sp * p.kb_per_split;
+  kb1 = min(p.k_blocks, kb0 + p.kb_per_split);
+}
+
+// Writes alpha * acc + beta * c for the M rows of output column n.
+__device__ __forceinline__ void skinny_store(const SkinnyParams& p, int n, const float (&acc)[16]) {
+  if (n >= p.N) return;
+#pragma unroll
+  for (int m = 0; m < kSkinnyNX; ++m) {
+    if (m < p.M) {
+      const long long off = static_cast<long long>(m) * p.ldc + n;
+      float v = p.alpha * acc[m];
+      if (p.out_bf16) {
+        uint16_t* c = static_cast<uint16_t*>(p.C);
+        if (p.beta != 0.0f) v += p.beta * bf16_bits_to_float(c[off]);
+        c[off] = static_cast<uint16_t>(pack_bf16x2(v, 0.0f) & 0xFFFFu);
+      } else {
+        float* c = static_cast<float*>(p.C);
+        if (p.beta != 0.0f) v += p.beta * c[off];
+        c[off] = v;
+      }
+    }
+  }
+}
+
+template <int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW,
+                       const __grid_constant__ CUtensorMap tmX, const SkinnyParams p) {
+  using Cfg = SkinnyCfg<STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOffset);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmW);
+    prefetch_tensormap(&tmX);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t stream_policy = l2_policy_evict_first();  // B is read once
+      const uint64_t keep_policy = l2_policy_evict_last();     // A is re-read by every unit
+      int s = 0;
+      uint32_t ph = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        int nb, sp, kb0, kb1;
+        skinny_unit(u, p, nb, sp, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint32_t w_dst = sbase + s * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);
+          tma_load_2d_hint(w_dst, &tmW, full_bar(s), kb * kBK, nb * kSkinnyRows, stream_policy);
+          tma_load_2d_hint(w_dst + Cfg::kWBytes, &tmX, full_bar(s), kb * kBK, 0, keep_policy);
+          ++issued;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      {
+        const long long first = issued > STAGES ? issued - STAGES : 0;
+        for (long long i = first; i < issued; ++i)
+          wait_bounded(full_bar(static_cast<int>(i % STAGES)),
+                       static_cast<uint32_t>((i / STAGES) & 1), nullptr, SITE_DRAIN);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int local = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++local) {
+        int nb, sp, kb0, kb1;
+        skinny_unit(u, p, nb, sp, kb0, kb1);
+        const int buf = local & 1;
+        const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
+        if (!wait_bounded(acce_bar(buf), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_bounded(full_bar(s), ph, abort_flag, SITE_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t w_addr = sbase + s * Cfg::kStageBytes;
+          const uint64_t wdesc = smem_desc_sw128(w_addr);
+          const uint64_t xdesc = smem_desc_sw128(w_addr + Cfg::kWBytes);
+#pragma unroll
+          for (int j = 0; j < kBK / kUmmaK; ++j)
+            umma_bf16(d_tmem, wdesc + 2u * j, xdesc + 2u * j, Cfg::kIdesc,
+                      (kb != kb0 || j != 0) ? 1u : 0u);
+          umma_commit(empty_bar(s));
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(accf_bar(buf));
+      }
+      umma_commit(drain_bar);
+      wait_bounded(drain_bar, 0, nullptr, SITE_DRAIN);
+    }
+  } else {
+    const int band = (warp & 3) * 32;
+    int local = 0;
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++local) {
+      int nb, sp, kb0, kb1;
+      skinny_unit(u, p, nb, sp, kb0, kb1);
+      const int buf = local & 1;
+      const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
+      const bool got = wait_bounded(accf_bar(buf), aph, abort_flag, SITE_EPI_ACC_FULL);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after_sync();
+      float acc[16];
+      if (kb1 > kb0) {
+        tmem_load_32x32b_x16(tmem_base + (static_cast<uint32_t>(band) << 16) +
+                                 static_cast<uint32_t>(buf * Cfg::kAccStride),
+                             acc);
+      } else {
+#pragma unroll
+        for (int m = 0; m < 16; ++m) acc[m] = 0.0f;
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(buf));
+
+      const int n = nb * kSkinnyRows + band + lane;
+      if (p.splits == 1) {
+        skinny_store(p, n, acc);
+        continue;
+      }
+      // Publish this unit's partial, then count arrivals for this band.
+      if (n < p.N) {
+#pragma unroll
+        for (int m = 0; m < kSkinnyNX; ++m)
+          if (m < p.M) p.ws[(static_cast<long long>(sp) * p.M + m) * p.N + n] = acc[m];
+      }
+      __threadfence();
+      __syncwarp();
+      int prev = 0;
+      int* counter = p.counters + nb * 4 + (warp & 3);
+      if (lane == 0) prev = atomicAdd(counter, 1);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev == p.splits - 1) {
+        __threadfence();
+        float sum[16];
+#pragma unroll
+        for (int m = 0; m < kSkinnyNX; ++m) sum[m] = 0.0f;
+        if (n < p.N) {
+          for (int s = 0; s < p.splits; ++s) {
+#pragma unroll
+            for (int m = 0; m < kSkinnyNX; ++m) {
+              if (m < p.M) {
+                const float part =
+                    (s == sp) ? acc[m]
+                              : __ldcg(p.ws + (static_cast<long long>(s) * p.M + m) * p.N + n);
+                sum[m] += part;
+              }
+            }
+          }
+        }
+        skinny_store(p, n, sum);
+        if (lane == 0) *counter = 0;  // ready for the next call
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace gb3

@@ -1,0 +1,165 @@
+/*
+ * gemm_bf16.h -- C ABI of the GB300 (sm_103a) dense BF16 GEMM library.
+ *
+ * Every entry point takes plain pointers and sizes.  Device buffers are owned
+ * by the caller: the library never frees them, never keeps them past the call
+ * (beyond caching the tensor-map descriptor keyed by address and shape) and
+ * does not check for aliasing between inputs and outputs (the tile
+ * abstractions of "TMEM tiles and transfers", section "Completion and
+ * validation", leave allocation, bounds and lifetime to the caller in the same
+ * way).
+ *
+ * Compute calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream) and never synchronize the host.  A status other
+ * than GEMM_OK means nothing was launched.  Errors raised by a kernel while
+ * it runs (a pipeline wait that exceeded its limit) are recorded in a device
+ * status word and read back with gemm_get_device_status().
+ *
+ * Storage convention ("TMA and Hopper WGMMA", section "The same storage
+ * contract on both sides": A(M,K) has K contiguous and B(K,N) is stored with
+ * K as its inner axis, so both operands are K-contiguous):
+ *   a(m,k) = A[m*lda + k]      BF16
+ *   b(k,n) = B[n*ldb + k]      BF16
+ *   c(m,n) = C[m*ldc + n]      FP32 or BF16 (out_dtype), row-major
+ * TMA requires 16-byte aligned base addresses and row pitches that are
+ * multiples of 16 bytes ("TMA and Hopper WGMMA", section "Copy and
+ * completion": the inner origin starts a 16-byte chunk).
+ */
+#ifndef GEMM_BF16_H
+#define GEMM_BF16_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+enum gemm_status {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,  /* negative or too large sizes, ld < extent, NULL with nonzero size, bad dtype */
+    GEMM_ERR_ALIGNMENT = 2,    /* pointer not 16-byte aligned or row pitch not a multiple of 16 bytes */
+    GEMM_ERR_UNSUPPORTED = 3,  /* current device is not compute capability 10.3 (GB300) */
+    GEMM_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (descriptor encode, launch, allocation) */
+    GEMM_ERR_TIMEOUT = 5       /* a kernel's bounded pipeline wait expired (read via gemm_get_device_status) */
+};
+
+/* Output element type of gemm_bf16. */
+enum gemm_out_dtype {
+    GEMM_OUT_F32 = 0,
+    GEMM_OUT_BF16 = 1
+};
+
+/*
+ * C = alpha * A.B + beta * C            ("Tiles and shared memory", section
+ *                                        "var and let": the tile epilogue
+ *                                        writes alpha*acc + beta*c_old over
+ *                                        the slice of C it read)
+ *
+ * M, N, K    problem sizes, 0 <= M, N, K < 2^31.  M == 0 or N == 0 does
+ *            nothing and returns GEMM_OK.  K == 0 gives C = beta * C.
+ * A, lda     device BF16 matrix, a(m,k) = A[m*lda + k], lda >= K.
+ * B, ldb     device BF16 matrix, b(k,n) = B[n*ldb + k], ldb >= K.
+ * C, ldc     device matrix of type out_dtype, c(m,n) = C[m*ldc + n],
+ *            ldc >= N.  Read only when beta != 0 (with beta == 0 it may hold
+ *            NaN or garbage), always written.
+ * out_dtype  GEMM_OUT_F32 or GEMM_OUT_BF16.  Accumulation is FP32; a BF16
+ *            output is rounded to nearest-even once, from the FP32 value of
+ *            alpha*acc + beta*c.
+ * stream     cudaStream_t the work is enqueued on.
+ *
+ * For M <= 16 the call uses a split-K path whose FP32 partial sums live in a
+ * per-device workspace the library allocates on first use (a call made
+ * while `stream` is being captured into a CUDA graph cannot allocate, so
+ * make one such call, or gemm_prepare(), before capturing).  Calls of that
+ * path that run concurrently on different streams share the workspace and
+ * must not overlap on the GPU.
+ */
+GEMM_API int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha,
+              const void *A, int64_t lda,
+              const void *B, int64_t ldb,
+              float beta, void *C, int64_t ldc,
+              int out_dtype, void *stream);
+
+/*
+ * Y = silu(X.Wg) * (X.Wu), elementwise product, silu(t) = t / (1 + exp(-t)).
+ * ("TMA and Hopper WGMMA", sections "TMA and Hopper WGMMA" and "Worked
+ * consumers and current validation": the fused gate/up projection epilogue.)
+ *
+ * X, ldx     device BF16, x(m,k) = X[m*ldx + k], ldx >= K.
+ * Wg, Wu     device BF16, wg(k,n) = Wg[n*ldw + k], wu(k,n) = Wu[n*ldw + k],
+ *            ldw >= K (both K-contiguous like B of gemm_bf16).
+ * Y, ldy     device BF16 output, y(m,n) = Y[m*ldy + n], ldy >= N.
+ * Both products accumulate in FP32; silu(g)*u is evaluated in FP32 and
+ * rounded to BF16 once.  K == 0 gives Y = 0.
+ */
+GEMM_API int gemm_gate_up_silu(int64_t M, int64_t N, int64_t K,
+                      const void *X, int64_t ldx,
+                      const void *Wg, const void *Wu, int64_t ldw,
+                      void *Y, int64_t ldy, void *stream);
+
+/* Static, NUL-terminated description of a return code. */
+GEMM_API const char *gemm_status_string(int status);
+
+/*
+ * Synchronizes `stream`, then returns and clears the device status word of
+ * the current device (GEMM_OK if no kernel reported an error since the last
+ * read).  The site of the failure (which pipeline wait) is written to
+ * *site when site is not NULL.
+ */
+GEMM_API int gemm_get_device_status(void *stream, int *site);
+
+/*
+ * Allocates, on the current device, the split-K workspace that a gemm_bf16
+ * call with M <= 16 and the given N would need, so that later calls (for
+ * example inside CUDA-graph capture) allocate nothing.  Ordered on `stream`.
+ */
+GEMM_API int gemm_prepare(int64_t max_N, void *stream);
+
+/*
+ * Self-test of failure detection: launches one thread that waits, through the
+ * same bounded mbarrier wait the GEMM pipelines use, on a barrier nothing
+ * arrives on.  After limit_ns (1 us .. 1 s) the wait gives up and records
+ * GEMM_ERR_TIMEOUT in the device status word, so a following
+ * gemm_get_device_status() returns GEMM_ERR_TIMEOUT.  Touches no memory of
+ * the caller.  Returns GEMM_ERR_INVALID_ARG for a limit outside the range.
+ */
+GEMM_API int gemm_selftest_wait_timeout(int64_t limit_ns, void *stream);
+
+/* How a call would be executed (host-side planning only). */
+typedef struct gemm_plan {
+    int kernel;       /* 0 none, 1 tiled tcgen05 GEMM, 2 skinny split-K, 3 scale only (K == 0), 4 gate/up */
+    int tile_m;       /* output rows per tile (tcgen05 M, or weight rows for the skinny path) */
+    int tile_n;       /* output columns per tile */
+    int tile_k;       /* K per pipeline stage */
+    int stages;       /* shared-memory ring depth */
+    int split_k;      /* K splits (skinny path), else 1 */
+    int64_t tiles;    /* work units (output tiles x splits) */
+    int grid;         /* CTAs launched (persistent: at most one per SM) */
+    int smem_bytes;   /* dynamic shared memory per CTA */
+    int launches;     /* kernels one call launches */
+    int64_t stage_tx_bytes; /* bytes one pipeline stage receives through TMA */
+} gemm_plan;
+
+/*
+ * Plan of gemm_bf16(M, N, K, ...) on a device with num_sms SMs (num_sms <= 0:
+ * query the current device).  Pure host logic; returns GEMM_INVALID_ARG for
+ * invalid sizes or dtype.
+ */
+GEMM_API int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int num_sms,
+                   gemm_plan *plan);
+
+/* Plan of gemm_gate_up_silu(M, N, K, ...), as gemm_bf16_plan. */
+GEMM_API int gemm_gate_up_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_plan *plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_BF16_H */

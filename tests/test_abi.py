@@ -1,0 +1,161 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, rejects invalid arguments before touching CUDA, and plans work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from dense_bf16_gemm_gb300 import _native, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm_bf16.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _native.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^GEMM_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_binding_list():
+    assert declared_symbols() == sorted(_native.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    # and nothing else is exported with C linkage besides the header's symbols
+    out = os.popen(f"nm -D --defined-only {_native.library_path()}").read()
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    gemm_like = {s for s in exported if s.startswith("gemm_")}
+    assert gemm_like == set(declared_symbols())
+
+
+def test_status_strings(lib):
+    for st in range(6):
+        assert _native.status_string(st)
+    assert _native.status_string(99) == "unknown status"
+
+
+A16 = 1 << 20   # a 16-byte aligned fake address: validation never dereferences it
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (M, N, K, A, lda, B, ldb, C, ldc, dtype)
+    ((-1, 8, 8, A16, 8, A16, 8, A16, 8, 1), _native.GEMM_ERR_INVALID_ARG),
+    ((8, -1, 8, A16, 8, A16, 8, A16, 8, 1), _native.GEMM_ERR_INVALID_ARG),
+    ((8, 8, -1, A16, 8, A16, 8, A16, 8, 1), _native.GEMM_ERR_INVALID_ARG),
+    ((1 << 31, 8, 8, A16, 8, A16, 8, A16, 8, 1), _native.GEMM_ERR_INVALID_ARG),
+    ((8, 8, 8, A16, 8, A16, 8, A16, 8, 7), _native.GEMM_ERR_INVALID_ARG),
+    ((8, 8, 16, A16, 8, A16, 16, A16, 8, 1), _native.GEMM_ERR_INVALID_ARG),   # lda < K
+    ((8, 8, 16, A16, 16, A16, 8, A16, 8, 1), _native.GEMM_ERR_INVALID_ARG),   # ldb < K
+    ((8, 16, 8, A16, 8, A16, 8, A16, 8, 1), _native.GEMM_ERR_INVALID_ARG),    # ldc < N
+    ((8, 8, 8, 0, 8, A16, 8, A16, 8, 1), _native.GEMM_ERR_INVALID_ARG),       # NULL A
+    ((8, 8, 8, A16, 8, 0, 8, A16, 8, 1), _native.GEMM_ERR_INVALID_ARG),       # NULL B
+    ((8, 8, 8, A16, 8, A16, 8, 0, 8, 1), _native.GEMM_ERR_INVALID_ARG),       # NULL C
+    ((8, 8, 8, A16 + 2, 8, A16, 8, A16, 8, 1), _native.GEMM_ERR_ALIGNMENT),
+    ((8, 8, 8, A16, 8, A16 + 8, 8, A16, 8, 1), _native.GEMM_ERR_ALIGNMENT),
+    ((8, 8, 8, A16, 8, A16, 8, A16 + 4, 8, 1), _native.GEMM_ERR_ALIGNMENT),
+    ((8, 8, 12, A16, 12, A16, 16, A16, 8, 1), _native.GEMM_ERR_ALIGNMENT),    # lda*2 % 16
+    ((8, 8, 12, A16, 16, A16, 12, A16, 8, 1), _native.GEMM_ERR_ALIGNMENT),    # ldb*2 % 16
+    ((8, 6, 8, A16, 8, A16, 8, A16, 6, 0), _native.GEMM_ERR_ALIGNMENT),       # ldc*4 % 16
+    ((8, 12, 8, A16, 8, A16, 8, A16, 12, 1), _native.GEMM_ERR_ALIGNMENT),     # ldc*2 % 16
+    ((0, 8, 8, 0, 8, 0, 8, 0, 8, 1), _native.GEMM_OK),                        # empty: no-op
+    ((8, 0, 8, 0, 8, 0, 8, 0, 0, 0), _native.GEMM_OK),
+])
+def test_gemm_validation_without_gpu(lib, args, expect):
+    M, N, K, A, lda, B, ldb, C, ldc, dt = args
+    st = _native.gemm_bf16(M, N, K, 1.0, A, lda, B, ldb, 0.0, C, ldc, dt, 0)
+    assert st == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((-1, 8, 8, A16, 8, A16, A16, 8, A16, 8), _native.GEMM_ERR_INVALID_ARG),
+    ((8, 8, 16, A16, 8, A16, A16, 16, A16, 8), _native.GEMM_ERR_INVALID_ARG),
+    ((8, 8, 8, A16, 8, 0, A16, 8, A16, 8), _native.GEMM_ERR_INVALID_ARG),
+    ((8, 8, 8, A16, 8, A16, 0, 8, A16, 8), _native.GEMM_ERR_INVALID_ARG),
+    ((8, 16, 8, A16, 8, A16, A16, 8, A16, 8), _native.GEMM_ERR_INVALID_ARG),
+    ((8, 8, 8, A16, 8, A16, A16 + 2, 8, A16, 8), _native.GEMM_ERR_ALIGNMENT),
+    ((8, 12, 8, A16, 8, A16, A16, 8, A16, 12), _native.GEMM_ERR_ALIGNMENT),
+    ((8, 0, 8, 0, 8, 0, 0, 8, 0, 0), _native.GEMM_OK),
+])
+def test_gate_up_validation_without_gpu(lib, args, expect):
+    M, N, K, X, ldx, Wg, Wu, ldw, Y, ldy = args
+    assert _native.gemm_gate_up_silu(M, N, K, X, ldx, Wg, Wu, ldw, Y, ldy, 0) == expect
+
+
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = _native.gemm_bf16(8, 8, 8, 1.0, A16, 8, A16, 8, 0.0, A16, 8, 1, 0)
+    assert st in (_native.GEMM_ERR_CUDA, _native.GEMM_ERR_UNSUPPORTED)
+
+
+def test_plan_tiled(lib):
+    st, p = _native.gemm_bf16_plan(4096, 4096, 4096, _native.GEMM_OUT_BF16, 152)
+    assert st == 0
+    d = p.as_dict()
+    assert d["kernel_name"] == "tiled"
+    assert d["tile_m"] == 128 and d["tile_k"] == 64
+    assert d["tiles"] == (4096 // 128) * -(-4096 // d["tile_n"])
+    assert d["grid"] == min(d["tiles"], 152)
+    assert d["launches"] == 1
+    # one stage = a 128x64 BF16 A box (16384 bytes) plus the B box
+    assert d["stage_tx_bytes"] == 16384 + d["tile_n"] * 64 * 2
+    assert d["smem_bytes"] <= 232448
+
+
+def test_plan_ragged_tiles_cover_the_output(lib):
+    st, p = _native.gemm_bf16_plan(3000, 5000, 2000, _native.GEMM_OUT_F32, 152)
+    assert st == 0
+    d = p.as_dict()
+    assert d["tiles"] == -(-3000 // d["tile_m"]) * -(-5000 // d["tile_n"])
+
+
+def test_plan_skinny_split_k(lib):
+    st, p = _native.gemm_bf16_plan(16, 28672, 8192, _native.GEMM_OUT_BF16, 152)
+    assert st == 0
+    d = p.as_dict()
+    assert d["kernel_name"] == "skinny_splitk"
+    assert d["tile_m"] == 128 and d["tile_n"] == 16
+    assert d["split_k"] >= 2               # 224 row blocks alone leave SMs idle
+    kb = 8192 // 64
+    kb_per = -(-kb // d["split_k"])
+    assert -(-kb // kb_per) == d["split_k"]   # every split gets work
+    assert d["tiles"] == 224 * d["split_k"]
+    assert d["grid"] == 152
+    # busiest CTA within 5% of a perfectly even spread of k-blocks
+    busiest = -(-d["tiles"] // d["grid"]) * kb_per
+    assert busiest <= 1.05 * (224 * kb) / 152
+    assert d["stage_tx_bytes"] == 128 * 64 * 2 + 16 * 64 * 2
+
+
+def test_plan_degenerate(lib):
+    st, p = _native.gemm_bf16_plan(0, 10, 10, 1, 152)
+    assert st == 0 and p.kernel == 0 and p.launches == 0
+    st, p = _native.gemm_bf16_plan(10, 10, 0, 1, 152)
+    assert st == 0 and p.as_dict()["kernel_name"] == "scale" and p.launches == 1
+    assert _native.gemm_bf16_plan(-1, 10, 10, 1, 152)[0] == _native.GEMM_ERR_INVALID_ARG
+    assert _native.gemm_bf16_plan(1, 10, 10, 5, 152)[0] == _native.GEMM_ERR_INVALID_ARG
+
+
+def test_plan_gate_up(lib):
+    st, p = _native.gemm_gate_up_plan(4096, 14336, 4096, 152)
+    assert st == 0
+    d = p.as_dict()
+    assert d["kernel_name"] == "gate_up"
+    assert d["tiles"] == 32 * (14336 // d["tile_n"])
+    # X box + Wg box + Wu box per stage
+    assert d["stage_tx_bytes"] == 3 * 16384
+
+
+def test_selftest_rejects_out_of_range_limits(lib):
+    assert _native.gemm_selftest_wait_timeout(10, 0) == _native.GEMM_ERR_INVALID_ARG
+    assert _native.gemm_selftest_wait_timeout(5 * 10**9, 0) == _native.GEMM_ERR_INVALID_ARG

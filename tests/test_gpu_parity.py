@@ -1,0 +1,366 @@
+"""Parity of the CUDA library with the CPU oracle, element by element, on the
+same seeded inputs.  All calls go through the C ABI (via the thin torch
+binding, which only marshals pointers)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def g():
+    from dense_bf16_gemm_gb300 import build
+    build.build()
+    import dense_bf16_gemm_gb300 as lib
+    # the product path must be the native library
+    lib._native.lib()
+    return lib
+
+
+def bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def to_f64(t):
+    return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def assert_within(got, ref, tol, what):
+    err = np.abs(got - ref)
+    bad = ~(err <= tol)
+    if bad.any():
+        idx = np.argwhere(bad)
+        i = tuple(idx[0])
+        worst = np.unravel_index(np.nanargmax(np.where(bad, err / np.maximum(tol, 1e-300), 0)),
+                                 err.shape)
+        raise AssertionError(
+            f"{what}: {bad.sum()} of {bad.size} entries out of tolerance; first {i}: "
+            f"got {got[i]!r} ref {ref[i]!r} tol {tol[i]!r}; worst {worst}: got {got[worst]!r} "
+            f"ref {ref[worst]!r} tol {tol[worst]!r}")
+
+
+def run_gemm(g, A, B, C=None, alpha=1.0, beta=0.0, out_dtype=torch.bfloat16, fill=float("nan")):
+    M, N = A.shape[0], B.shape[0]
+    Ad, Bd = A.cuda(), B.cuda()
+    if C is not None:
+        Cd = C.to(out_dtype).cuda()
+    else:
+        Cd = torch.full((M, N), fill, dtype=out_dtype, device="cuda")
+    g.gemm(Ad, Bd, Cd, alpha=alpha, beta=beta)
+    torch.cuda.synchronize()
+    return Cd
+
+
+def int_inputs(M, N, K, seed):
+    return workloads.gemm_inputs(M, N, K, seed, ("int", -2, 2), ("int", -2, 2), ("int", -3, 3))
+
+
+def assert_status_ok(g):
+    st, site = g.device_status()
+    assert st == 0, f"device status {st} at wait site {site}"
+
+
+# ---------------------------------------------------------------------------
+# bit-exact: integer-valued inputs make every FP32 partial sum exact, so any
+# layout, swizzle, descriptor or indexing error shows as a wrong integer.
+# ---------------------------------------------------------------------------
+EXACT_SHAPES = [
+    (128, 256, 64),      # one tile, one k-block
+    (300, 520, 200),     # ragged in M, N and K
+    (1000, 712, 1000),   # many tiles, slot reuse
+    (17, 296, 64),       # just above the skinny threshold
+    (256, 256, 8),       # K smaller than one k-block
+    (200, 264, 72),      # K tail of 8
+    (16, 1000, 4096),    # skinny split-K
+    (3, 520, 1000),      # skinny, M < 16, ragged N
+]
+
+
+@pytest.mark.parametrize("M,N,K", EXACT_SHAPES)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_integer_inputs_bit_exact(g, M, N, K, out_dtype):
+    A, B, _ = int_inputs(M, N, K, seed=M + N + K)
+    ref, _ = oracle.gemm_full(A, B)
+    out = run_gemm(g, A, B, out_dtype=out_dtype)
+    if out_dtype == torch.float32:
+        assert np.array_equal(to_f64(out), ref)
+    else:
+        want = oracle.round_to_bf16_bits(ref)
+        assert np.array_equal(bits(out.cpu()), want)
+    assert_status_ok(g)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (16, 1000, 4096), (5, 136, 640)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_integer_inputs_alpha_beta_exact(g, M, N, K, out_dtype):
+    A, B, C = int_inputs(M, N, K, seed=7 * M + K)
+    alpha, beta = 2.0, -0.5   # powers of two keep the result exact
+    Cq = C.to(out_dtype)      # the output storage type is also the input type of C
+    ref, _ = oracle.gemm_full(A, B, alpha=alpha, beta=beta, C=Cq.to(torch.float32))
+    out = run_gemm(g, A, B, C=Cq, alpha=alpha, beta=beta, out_dtype=out_dtype)
+    if out_dtype == torch.float32:
+        assert np.array_equal(to_f64(out), ref)
+    else:
+        assert np.array_equal(bits(out.cpu()), oracle.round_to_bf16_bits(ref))
+
+
+# ---------------------------------------------------------------------------
+# The five workloads
+# ---------------------------------------------------------------------------
+def check_gemm_workload(g, w, rows=None, cols=None):
+    A, B, C = workloads.inputs_for(w)
+    out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
+    out = run_gemm(g, A, B, C=C, alpha=w.alpha, beta=w.beta, out_dtype=out_dtype)
+    got = to_f64(out)
+    if rows is None:
+        ref, ab = oracle.gemm_full(A, B, alpha=w.alpha, beta=w.beta, C=C)
+        cm = C.numpy() if C is not None else None
+    else:
+        ref, ab = oracle.gemm_entries(A, B, rows, cols, alpha=w.alpha, beta=w.beta, C=C)
+        got = got[rows, cols]
+        cm = C.numpy()[rows, cols] if C is not None else None
+    tol = oracle.gemm_tolerance(ref, ab, w.alpha, w.beta, cm, out_bf16=w.out_bf16)
+    assert_within(got, ref, tol, w.name)
+    assert_status_ok(g)
+
+
+def test_workload_gemm_256_f32(g):
+    check_gemm_workload(g, workloads.WORKLOADS["gemm_256_f32"])
+
+
+@pytest.mark.slow
+def test_workload_gemm_4096_bf16(g):
+    check_gemm_workload(g, workloads.WORKLOADS["gemm_4096_bf16"])
+
+
+@pytest.mark.slow
+def test_workload_gemm_ragged(g):
+    check_gemm_workload(g, workloads.WORKLOADS["gemm_ragged_3000x5000x2000"])
+
+
+@pytest.mark.slow
+def test_workload_skinny(g):
+    w = workloads.WORKLOADS["skinny_16x28672x8192"]
+    rows, cols = workloads.sample_entries(w.M, w.N, w.seed)
+    assert rows.size == w.M * w.N  # the edge region covers every entry
+    check_gemm_workload(g, w, rows, cols)
+
+
+def check_gate_up(g, M, N, K, seed, dist_w, rows=None, cols=None):
+    X, Wg, Wu = workloads.gate_up_inputs(M, N, K, seed, ("normal", 1.0), dist_w)
+    Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    g.gate_up_silu(X.cuda(), Wg.cuda(), Wu.cuda(), Y)
+    torch.cuda.synchronize()
+    if rows is None:
+        rr, cc = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+        rows, cols = rr.ravel(), cc.ravel()
+    res = oracle.gate_up_entries(X, Wg, Wu, rows, cols)
+    got = to_f64(Y)[rows, cols]
+    assert_within(got, res["y"], oracle.gate_up_tolerance(res), f"gate_up {M}x{N}x{K}")
+    assert_status_ok(g)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (200, 296, 104), (513, 1000, 640)])
+def test_gate_up_ragged(g, M, N, K):
+    check_gate_up(g, M, N, K, seed=M + N, dist_w=("normal", 1.0 / np.sqrt(K)))
+
+
+@pytest.mark.slow
+def test_workload_gate_up(g):
+    w = workloads.WORKLOADS["gate_up_4096x14336x4096"]
+    rows, cols = workloads.sample_entries(w.M, w.N, w.seed)
+    check_gate_up(g, w.M, w.N, w.K, w.seed, w.dist_b, rows, cols)
+
+
+# ---------------------------------------------------------------------------
+# Edge cases and contracts
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("K", [1, 16, 72, 2000])
+def test_k_tails(g, K):
+    M, N = 260, 300
+    lda = max(8, (K + 7) // 8 * 8)
+    A, B, _ = workloads.gemm_inputs(M, N, K, K, ("uniform",), ("uniform",))
+    Ap = torch.zeros((M, lda), dtype=torch.bfloat16)
+    Bp = torch.zeros((N, lda), dtype=torch.bfloat16)
+    Ap[:, :K] = A
+    Bp[:, :K] = B
+    Ad, Bd = Ap.cuda()[:, :K], Bp.cuda()[:, :K]   # row pitch lda > K
+    Cd = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    g.gemm(Ad, Bd, Cd)
+    torch.cuda.synchronize()
+    ref, ab = oracle.gemm_full(A, B)
+    assert_within(to_f64(Cd), ref, oracle.gemm_tolerance(ref, ab, 1.0, 0.0), f"K={K}")
+
+
+def test_leading_dimensions_larger_than_extents(g):
+    M, N, K = 300, 260, 200
+    A, B, C = workloads.gemm_inputs(M, N, K, 5, ("uniform",), ("uniform",), ("normal", 1.0))
+    Abig = torch.zeros((M, K + 40), dtype=torch.bfloat16, device="cuda")
+    Bbig = torch.zeros((N, K + 24), dtype=torch.bfloat16, device="cuda")
+    Cbig = torch.full((M, N + 12), 7.0, dtype=torch.float32, device="cuda")
+    Abig[:, :K] = A.cuda()
+    Bbig[:, :K] = B.cuda()
+    Cbig[:, :N] = C.cuda()
+    g.gemm(Abig[:, :K], Bbig[:, :K], Cbig[:, :N], alpha=-1.0, beta=0.5)
+    torch.cuda.synchronize()
+    ref, ab = oracle.gemm_full(A, B, alpha=-1.0, beta=0.5, C=C)
+    out = to_f64(Cbig)
+    assert_within(out[:, :N], ref, oracle.gemm_tolerance(ref, ab, -1.0, 0.5, C.numpy()), "ld")
+    assert np.all(out[:, N:] == 7.0)   # padding columns untouched
+
+
+def test_beta_zero_does_not_read_nan_C(g):
+    A, B, _ = workloads.gemm_inputs(256, 512, 256, 9, ("uniform",), ("uniform",))
+    for dt in (torch.float32, torch.bfloat16):
+        out = run_gemm(g, A, B, out_dtype=dt, fill=float("nan"))
+        assert torch.isfinite(out).all()
+
+
+def test_k_zero_scales_C(g):
+    M, N = 70, 92
+    C = torch.randn(M, N)
+    Cd = C.cuda()
+    A = torch.empty((M, 0), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((N, 0), dtype=torch.bfloat16, device="cuda")
+    g.gemm(A, B, Cd, alpha=3.0, beta=-2.0)
+    torch.cuda.synchronize()
+    assert torch.equal(Cd.cpu(), -2.0 * C)
+    Cd = torch.full((M, N), float("nan"), device="cuda")
+    g.gemm(A, B, Cd, beta=0.0)
+    torch.cuda.synchronize()
+    assert torch.equal(Cd.cpu(), torch.zeros(M, N))
+
+
+def test_empty_problems_are_noops(g):
+    A = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    B = torch.ones((32, 64), dtype=torch.bfloat16, device="cuda")
+    C = torch.empty((0, 32), dtype=torch.float32, device="cuda")
+    g.gemm(A, B, C)
+    A = torch.ones((32, 64), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    C = torch.empty((32, 0), dtype=torch.float32, device="cuda")
+    g.gemm(A, B, C)
+    torch.cuda.synchronize()
+    assert_status_ok(g)
+
+
+def test_modified_inputs_reuse_cached_descriptor(g):
+    M, N, K = 256, 512, 512
+    A, B, _ = int_inputs(M, N, K, 31)
+    Ad, Bd = A.cuda(), B.cuda()
+    Cd = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    g.gemm(Ad, Bd, Cd)
+    Ad.mul_(-1)                    # same address, new values
+    g.gemm(Ad, Bd, Cd)
+    torch.cuda.synchronize()
+    ref, _ = oracle.gemm_full(A, B)
+    assert np.array_equal(to_f64(Cd), -ref)
+
+
+def test_new_pointer_forces_new_descriptor(g):
+    M, N, K = 200, 300, 128
+    A1, B, _ = int_inputs(M, N, K, 32)
+    A2, _, _ = int_inputs(M, N, K, 33)
+    Bd = B.cuda()
+    outs = []
+    for A in (A1, A2, A1):
+        Cd = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        g.gemm(A.cuda(), Bd, Cd)
+        outs.append(Cd)
+    torch.cuda.synchronize()
+    for A, out in zip((A1, A2, A1), outs):
+        ref, _ = oracle.gemm_full(A, B)
+        assert np.array_equal(to_f64(out), ref)
+
+
+@pytest.mark.parametrize("M", [512, 16])
+def test_cuda_graph_capture_and_replay(g, M):
+    N, K = 768, 1024
+    A, B, _ = int_inputs(M, N, K, 34)
+    Ad, Bd = A.cuda(), B.cuda()
+    Cd = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    g.gemm(Ad, Bd, Cd)      # eager call first: sets up descriptors and workspace
+    torch.cuda.synchronize()
+    eager = Cd.clone()
+    Cd.zero_()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            g.gemm(Ad, Bd, Cd, stream=s)
+    for _ in range(3):
+        Cd.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(Cd, eager)
+    Ad.mul_(2)               # graph replay sees new values at the same address
+    graph.replay()
+    torch.cuda.synchronize()
+    ref, _ = oracle.gemm_full(A, B, alpha=2.0)
+    assert np.array_equal(bits(Cd.cpu()), oracle.round_to_bf16_bits(ref))
+
+
+@pytest.mark.parametrize("M,K", [(512, 1024), (16, 2048)])
+def test_sharding_over_N_matches_full_result(g, M, K):
+    """Independent column shards (the multi-GPU split, run one after another
+    here) concatenate to the unsharded result."""
+    N, shards = 1536, 4
+    A, B, _ = workloads.gemm_inputs(M, N, K, 35, ("normal", 1.0), ("normal", 1.0))
+    Ad, Bd = A.cuda(), B.cuda()
+    full = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    g.gemm(Ad, Bd, full)
+    parts = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    w = N // shards
+    for s in range(shards):
+        g.gemm(Ad, Bd[s * w:(s + 1) * w], parts[:, s * w:(s + 1) * w])
+    torch.cuda.synchronize()
+    ref, ab = oracle.gemm_full(A, B)
+    tol = oracle.gemm_tolerance(ref, ab, 1.0, 0.0)
+    assert_within(to_f64(parts), ref, tol, "sharded")
+    assert_within(to_f64(full), ref, tol, "full")
+    if M > 16:   # tiled path: the per-entry K order does not depend on N
+        assert torch.equal(parts, full)
+
+
+def test_repeated_calls_are_deterministic(g):
+    w = workloads.WORKLOADS["skinny_16x28672x8192"]
+    A, B, _ = workloads.gemm_inputs(16, 4096, 8192, 36, ("normal", 1.0), ("normal", 0.01))
+    Ad, Bd = A.cuda(), B.cuda()
+    outs = []
+    for _ in range(3):
+        C = torch.empty((16, 4096), dtype=torch.float32, device="cuda")
+        g.gemm(Ad, Bd, C)
+        outs.append(C)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    del w
+
+
+def test_plan_matches_device(g):
+    p = g.plan(4096, 4096, 4096)
+    props = torch.cuda.get_device_properties(0)
+    assert p["grid"] == min(p["tiles"], props.multi_processor_count)
+    assert (props.major, props.minor) == (10, 3)
+
+
+def test_bounded_wait_reports_timeout(g):
+    """A pipeline wait that nothing completes gives up after its limit and
+    leaves GEMM_ERR_TIMEOUT in the device status word; the context stays
+    usable."""
+    from dense_bf16_gemm_gb300 import _native
+    assert_status_ok(g)
+    st = _native.gemm_selftest_wait_timeout(20_000_000, torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    st, site = g.device_status()
+    assert st == _native.GEMM_ERR_TIMEOUT and site == 7
+    st, site = g.device_status()        # reading clears the word
+    assert st == 0
+    # and the GPU still computes
+    A, B, _ = int_inputs(128, 256, 64, 3)
+    out = run_gemm(g, A, B, out_dtype=torch.float32)
+    ref, _ = oracle.gemm_full(A, B)
+    assert np.array_equal(to_f64(out), ref)
