@@ -34,6 +34,7 @@ EXPORTED = (
     "gemm_bf16_plan",
     "gemm_gate_up_plan",
     "gemm_selftest_wait_timeout",
+    "gemm_bf16_skinny_noalloc",
 )
 
 
@@ -103,6 +104,9 @@ def lib() -> ctypes.CDLL:
             l.gemm_prepare.argtypes = [_i64, _vp]
             l.gemm_bf16_plan.restype = _int
             l.gemm_bf16_plan.argtypes = [_i64, _i64, _i64, _int, _int, ctypes.POINTER(GemmPlan)]
+            l.gemm_bf16_skinny_noalloc.restype = _int
+            l.gemm_bf16_skinny_noalloc.argtypes = [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64,
+                                                   _f32, _vp, _i64, _int, _vp]
             l.gemm_selftest_wait_timeout.restype = _int
             l.gemm_selftest_wait_timeout.argtypes = [_i64, _vp]
             l.gemm_gate_up_plan.restype = _int
@@ -119,6 +123,14 @@ def gemm_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, out_dtype, stream) -
     """Raw C call; pointers and the stream are integers (0 = NULL)."""
     return lib().gemm_bf16(M, N, K, alpha, A or None, lda, B or None, ldb, beta, C or None,
                            ldc, out_dtype, stream or None)
+
+
+def gemm_bf16_skinny_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, out_dtype,
+                             stream) -> int:
+    """gemm_bf16 for M <= 16 using the library's fixed scratch array instead of
+    an allocated workspace (for callers that may not allocate)."""
+    return lib().gemm_bf16_skinny_noalloc(M, N, K, alpha, A or None, lda, B or None, ldb, beta,
+                                          C or None, ldc, out_dtype, stream or None)
 
 
 def gemm_gate_up_silu(M, N, K, X, ldx, Wg, Wu, ldw, Y, ldy, stream) -> int:

@@ -661,3 +661,130 @@ int gemm_prepare(int64_t max_N, void* stream) {
 }
 
 }  // extern "C"
+
+// ============================================================================
+// Decode-shaped GEMM without any allocation
+// ============================================================================
+// Some callers cannot allocate device memory at the moment they call: code
+// running under a custom allocator or memory pool that forbids stray
+// cudaMalloc, code inside a region where allocation would synchronize the
+// device, or callers whose memory budget is fixed up front.  For them the
+// split-K partial sums of the M <= 16 path live in one fixed array in the
+// library's device image instead of an allocated workspace.  The array is
+// created when the library is loaded onto a GPU and held until the process
+// exits, on every GPU that loads the library.
+namespace {
+
+// 8 MiB: arrival counters first (rounded up to 256 bytes), FP32 partial sums
+// after them.  Enough for split * M * N * 4 bytes up to about 8 MB, e.g. two
+// splits of a 16 x 28672 output (3.7 MB).
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(8) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+unsigned char* g_noalloc_base[kMaxDevices];  // device address of the array, per device
+bool g_noalloc_smem_set[kMaxDevices];
+
+// Encodes a 2-D map straight into *out (no descriptor cache, no allocation).
+int encode_map_2d_direct(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype,
+                         uint64_t inner, uint64_t outer, uint64_t pitch, uint32_t box_inner,
+                         uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return GEMM_ERR_CUDA;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {pitch};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estrides[2] = {1, 1};
+  const CUresult r = fn(out, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estrides,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int gemm_bf16_skinny_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                                        const void* A, int64_t lda, const void* B, int64_t ldb,
+                                        float beta, void* C, int64_t ldc, int out_dtype,
+                                        void* stream_) {
+  int st = validate_gemm(M, N, K, A, lda, B, ldb, beta, C, ldc, out_dtype);
+  if (st != GEMM_OK) return st;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (M > kSkinnyMaxM) return GEMM_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev;
+  if ((st = current_device(&dev)) != GEMM_OK) return st;
+  int sms;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = probe_device(dev)) != GEMM_OK) return st;
+    sms = g_dev[dev].sms;
+  }
+  gemm_plan pl;
+  plan_gemm(M, N, K, sms, &pl);
+  const bool bf16 = out_dtype == GEMM_OUT_BF16;
+  if (pl.kernel == K_SCALE) return run_scale(pl, C, ldc, M, N, beta, bf16, stream);
+
+  SkinnyParams p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.n_blocks = static_cast<int>(ceil_div(N, kSkinnyRows));
+  p.k_blocks = static_cast<int>(ceil_div(K, kBK));
+  p.splits = pl.split_k;
+  p.kb_per_split = static_cast<int>(ceil_div(p.k_blocks, p.splits));
+  p.num_units = static_cast<int>(pl.tiles);
+  p.alpha = alpha;
+  p.beta = beta;
+  p.C = C;
+  p.ldc = ldc;
+  p.out_bf16 = bf16 ? 1 : 0;
+  const size_t counter_bytes =
+      (static_cast<size_t>(p.n_blocks) * 4 * sizeof(int) + 255) & ~static_cast<size_t>(255);
+  const size_t partial_bytes =
+      p.splits > 1 ? static_cast<size_t>(p.splits) * M * N * sizeof(float) : 0;
+  if (counter_bytes + partial_bytes > kNoAllocScratchBytes) return GEMM_ERR_INVALID_ARG;
+
+  auto kern = gemm_skinny_kernel<kSkinnyStages>;
+  unsigned char* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_base[dev] == nullptr) {
+      // One-time set-up on this device (the device is current): the host-side
+      // name of the array is not a device address; ask the runtime for it.
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+      }
+      g_noalloc_base[dev] = static_cast<unsigned char*>(addr);
+    }
+    if (!g_noalloc_smem_set[dev]) {
+      if (cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               pl.smem_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+      }
+      g_noalloc_smem_set[dev] = true;
+    }
+    base = g_noalloc_base[dev];
+  }
+  p.counters = reinterpret_cast<int*>(base);
+  p.ws = reinterpret_cast<float*>(base + counter_bytes);
+
+  CUtensorMap tmW, tmX;
+  if ((st = encode_map_2d_direct(&tmW, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldb * 2, kBK,
+                                 kSkinnyRows)) != GEMM_OK)
+    return st;
+  if ((st = encode_map_2d_direct(&tmX, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, lda * 2, kBK,
+                                 kSkinnyNX)) != GEMM_OK)
+    return st;
+  // The arrival counters must start at zero; the array keeps whatever the
+  // previous call left, so clear them on the stream first.
+  if (p.splits > 1 && cudaMemsetAsync(p.counters, 0, counter_bytes, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  return launch(kern, pl.grid, kThreads, pl.smem_bytes, stream, tmW, tmX, p);
+}

@@ -123,6 +123,34 @@ GEMM_API int gemm_get_device_status(void *stream, int *site);
 GEMM_API int gemm_prepare(int64_t max_N, void *stream);
 
 /*
+ * gemm_bf16 for M <= 16 that allocates nothing.  The pages have no
+ * counterpart of this call; it exists for callers that may not allocate
+ * device memory while they run (a caching allocator or memory pool that must
+ * stay in charge of every byte, a fixed memory budget, code that cannot
+ * afford the device synchronization an allocation can cause).
+ *
+ * Same arguments, storage and results as gemm_bf16, restricted to
+ * 1 <= M <= 16 (GEMM_ERR_INVALID_ARG otherwise; M == 0 or N == 0 still does
+ * nothing).  The split-K partial sums live in one 8 MiB array compiled into
+ * the library, which every GPU that loads the library holds until the process
+ * exits.  A problem whose split * M * N * 4 bytes of partial sums plus its
+ * arrival counters do not fit in that array is rejected with
+ * GEMM_ERR_INVALID_ARG before anything is launched.
+ *
+ * The first call on each device looks the array's device address up (a
+ * runtime query, not an allocation); make that first call before capturing
+ * the stream into a CUDA graph.  Every call re-zeroes the counters on
+ * `stream` before its kernel.  All calls on a device share the one array, so
+ * calls that overlap on the GPU (different streams running at the same time)
+ * race and must be serialized by the caller.
+ */
+GEMM_API int gemm_bf16_skinny_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                                      const void *A, int64_t lda,
+                                      const void *B, int64_t ldb,
+                                      float beta, void *C, int64_t ldc,
+                                      int out_dtype, void *stream);
+
+/*
  * Self-test of failure detection: launches one thread that waits, through the
  * same bounded mbarrier wait the GEMM pipelines use, on a barrier nothing
  * arrives on.  After limit_ns (1 us .. 1 s) the wait gives up and records
