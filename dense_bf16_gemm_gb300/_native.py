@@ -22,7 +22,8 @@ GEMM_ERR_TIMEOUT = 5
 GEMM_OUT_F32 = 0
 GEMM_OUT_BF16 = 1
 
-KERNEL_NAMES = {0: "none", 1: "tiled", 2: "skinny_splitk", 3: "scale", 4: "gate_up"}
+KERNEL_NAMES = {0: "none", 1: "tiled", 2: "skinny_splitk", 3: "scale", 4: "gate_up",
+                5: "pair", 6: "pair_gate_up"}
 
 # Every symbol the header declares.
 EXPORTED = (

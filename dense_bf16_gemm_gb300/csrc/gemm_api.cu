@@ -17,12 +17,14 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
 
 #include "../../include/gemm_bf16.h"
 #include "gemm_kernels.cuh"
+#include "gemm_kernels_pair.cuh"
 #include "gemm_skinny.cuh"
 
 namespace {
@@ -39,17 +41,47 @@ constexpr int kSkinnyStages = 12;  // 18 KB per stage
 constexpr int kSkinnyMaxM = 16;
 constexpr int kGroupM = 16;
 
+constexpr int kPairStages = 6;     // CTA-pair kernels: 16 KB A + BN*64 B per stage and CTA
+constexpr int kPairMinM = 129;     // pair tiles (256 rows) from this M on
+
 using CfgF32 = GemmCfg<kTileN, kStages, EPI_F32>;
 using CfgBF16 = GemmCfg<kTileN, kStages, EPI_BF16>;
 using CfgGU = GemmCfg<256, kGateUpStages, EPI_GATE_UP>;
 using CfgSkinny = SkinnyCfg<kSkinnyStages>;
+using CfgPairGU = PairCfg<256, kPairStages, EPI_GATE_UP>;
+
+// Tile widths compiled for the CTA-pair GEMM.
+constexpr int kPairWidths[] = {256, 224};
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ----------------------------------------------------------------------------
 // Planning (pure host logic)
 // ----------------------------------------------------------------------------
-enum KernelKind { K_NONE = 0, K_TILED = 1, K_SKINNY = 2, K_SCALE = 3, K_GATE_UP = 4 };
+enum KernelKind {
+  K_NONE = 0,
+  K_TILED = 1,
+  K_SKINNY = 2,
+  K_SCALE = 3,
+  K_GATE_UP = 4,
+  K_PAIR = 5,
+  K_PAIR_GATE_UP = 6
+};
+
+template <int BN>
+constexpr int pair_smem_bytes() {
+  return PairCfg<BN, kPairStages, EPI_BF16>::kSmemBytes;
+}
+
+int pair_smem_for(int bn) {
+  switch (bn) {
+    case 256: return pair_smem_bytes<256>();
+    case 224: return pair_smem_bytes<224>();
+    default: return 0;
+  }
+}
+
+int pair_stage_bytes(int bn) { return 128 * kBK * 2 + (bn / 2) * kBK * 2; }
 
 // Split of K for the skinny path: minimise the k-blocks of the busiest CTA,
 // ceil(units / grid) * ceil(k_blocks / S), with a small charge per extra split
@@ -74,7 +106,35 @@ void choose_split(int64_t n_blocks, int64_t k_blocks, int sms, int* splits, int*
   *kb_per = static_cast<int>(ceil_div(k_blocks, best_s));
 }
 
-int plan_gemm(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl) {
+// Tile width of the CTA-pair GEMM: fewest "waves" of pair tiles weighted by
+// the width (time per tile grows with it), with a fixed per-tile charge.
+int choose_pair_width(int64_t M, int64_t N, int slots, int64_t* tiles_out) {
+  int best = 256;
+  double best_cost = 1e300;
+  const int64_t mb = ceil_div(M, kPairBM);
+  // GB3_GEMM_PAIR_TILE_N=<width> restricts the choice to one compiled width
+  // (tuning and tests); other values are ignored.
+  int forced = 0;
+  if (const char* env = std::getenv("GB3_GEMM_PAIR_TILE_N")) forced = std::atoi(env);
+  bool forced_valid = false;
+  for (int bn : kPairWidths) forced_valid |= (bn == forced);
+  for (int bn : kPairWidths) {
+    if (forced_valid && bn != forced) continue;
+    const int64_t tiles = mb * ceil_div(N, bn);
+    const double cost =
+        static_cast<double>(ceil_div(tiles, slots)) * static_cast<double>(bn + 32);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+      *tiles_out = tiles;
+    }
+  }
+  return best;
+}
+
+// pair_slots: CTA pairs that fit on the device at once (0: assume sms / 2,
+// negative: pair kernels unavailable).
+int plan_gemm(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pair_slots = 0) {
   std::memset(pl, 0, sizeof(*pl));
   pl->split_k = 1;
   if (M == 0 || N == 0) return GEMM_OK;
@@ -102,6 +162,21 @@ int plan_gemm(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl) {
     pl->stage_tx_bytes = CfgSkinny::kStageBytes;
     return GEMM_OK;
   }
+  if (M >= kPairMinM && pair_slots >= 0) {
+    const int slots = pair_slots > 0 ? pair_slots : std::max(1, sms / 2);
+    int64_t tiles = 0;
+    const int bn = choose_pair_width(M, N, slots, &tiles);
+    pl->kernel = K_PAIR;
+    pl->tile_m = kPairBM;
+    pl->tile_n = bn;
+    pl->stages = kPairStages;
+    pl->tiles = tiles;
+    pl->grid = 2 * static_cast<int>(std::min<int64_t>(tiles, slots));
+    pl->smem_bytes = pair_smem_for(bn);
+    pl->launches = 1;
+    pl->stage_tx_bytes = 2 * pair_stage_bytes(bn);
+    return GEMM_OK;
+  }
   pl->kernel = K_TILED;
   pl->tile_m = kBM;
   pl->tile_n = kTileN;
@@ -114,7 +189,7 @@ int plan_gemm(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl) {
   return GEMM_OK;
 }
 
-int plan_gate_up(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl) {
+int plan_gate_up(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pair_slots = 0) {
   std::memset(pl, 0, sizeof(*pl));
   pl->split_k = 1;
   if (M == 0 || N == 0) return GEMM_OK;
@@ -123,6 +198,20 @@ int plan_gate_up(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl) {
     pl->tiles = 1;
     pl->grid = static_cast<int>(std::min<int64_t>(ceil_div(M * N, 256), 4 * sms));
     pl->launches = 1;
+    return GEMM_OK;
+  }
+  if (M >= kPairMinM && pair_slots >= 0) {
+    const int slots = pair_slots > 0 ? pair_slots : std::max(1, sms / 2);
+    pl->kernel = K_PAIR_GATE_UP;
+    pl->tile_m = kPairBM;
+    pl->tile_n = CfgPairGU::kOutCols;
+    pl->tile_k = kBK;
+    pl->stages = kPairStages;
+    pl->tiles = ceil_div(M, kPairBM) * ceil_div(N, CfgPairGU::kOutCols);
+    pl->grid = 2 * static_cast<int>(std::min<int64_t>(pl->tiles, slots));
+    pl->smem_bytes = CfgPairGU::kSmemBytes;
+    pl->launches = 1;
+    pl->stage_tx_bytes = 2 * CfgPairGU::kStageBytes;
     return GEMM_OK;
   }
   pl->kernel = K_GATE_UP;
@@ -191,6 +280,8 @@ struct DeviceState {
   int sms = 0;
   // kernels whose shared-memory limit has been raised on this device
   std::vector<const void*> configured;
+  // CTA pairs that fit on the device at once (0: not queried yet, -1: none)
+  int pair_slots = 0;
   // split-K workspace of the skinny path
   float* ws = nullptr;
   size_t ws_bytes = 0;
@@ -316,9 +407,11 @@ struct MapKey {
   int dtype;
   uint64_t inner, outer, pitch;
   uint32_t box_inner, box_outer;
+  int swizzle;
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && dtype == o.dtype && inner == o.inner && outer == o.outer &&
-           pitch == o.pitch && box_inner == o.box_inner && box_outer == o.box_outer;
+           pitch == o.pitch && box_inner == o.box_inner && box_outer == o.box_outer &&
+           swizzle == o.swizzle;
   }
 };
 
@@ -337,8 +430,10 @@ uint64_t g_map_clock = 0;
 // row pitch of `pitch` bytes; box of box_inner x box_outer elements, 128-byte
 // swizzle, out-of-bounds elements read as zero.
 int tensor_map_2d(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, uint64_t inner,
-                  uint64_t outer, uint64_t pitch, uint32_t box_inner, uint32_t box_outer) {
-  const MapKey key{ptr, static_cast<int>(dtype), inner, outer, pitch, box_inner, box_outer};
+                  uint64_t outer, uint64_t pitch, uint32_t box_inner, uint32_t box_outer,
+                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+  const MapKey key{ptr, static_cast<int>(dtype), inner, outer, pitch, box_inner, box_outer,
+                   static_cast<int>(swizzle)};
   std::lock_guard<std::mutex> lk(g_map_mu);
   for (MapEntry& e : g_maps) {
     if (e.key == key) {
@@ -355,7 +450,7 @@ int tensor_map_2d(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, 
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estrides[2] = {1, 1};
   const CUresult r = fn(&map, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estrides,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return GEMM_ERR_CUDA;
   if (g_maps.size() < kMapCacheSize) {
@@ -389,6 +484,62 @@ int launch(void (*kernel)(ExpT...), int grid, int block, int smem, cudaStream_t 
   return GEMM_OK;
 }
 
+template <typename... ExpT, typename... ActT>
+int launch_pair(void (*kernel)(ExpT...), int grid, int smem, cudaStream_t stream,
+                ActT&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(kThreads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, std::forward<ActT>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  return GEMM_OK;
+}
+
+// Caller holds g_mu.  Number of CTA pairs of the pair kernels (about 226 KB of
+// shared memory each, one CTA per SM) that can be resident at once.
+int query_pair_slots(int dev) {
+  DeviceState& d = g_dev[dev];
+  if (d.pair_slots != 0) return d.pair_slots;
+  auto kern = gemm_pair_kernel<256, kPairStages, EPI_BF16>;
+  const int smem = pair_smem_bytes<256>();
+  if (ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), smem) != GEMM_OK) {
+    d.pair_slots = -1;
+    return d.pair_slots;
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * std::max(1, d.sms / 2)), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kern), &cfg) !=
+          cudaSuccess ||
+      n <= 0) {
+    cudaGetLastError();
+    d.pair_slots = -1;
+  } else {
+    d.pair_slots = n;
+  }
+  return d.pair_slots;
+}
+
 // C = beta * C (K == 0); C is not read when beta == 0.
 __global__ void scale_kernel(void* C, long long ldc, int M, int N, float beta, int bf16) {
   const long long total = static_cast<long long>(M) * N;
@@ -413,13 +564,13 @@ int run_scale(const gemm_plan& pl, void* C, int64_t ldc, int64_t M, int64_t N, f
                 static_cast<int>(M), static_cast<int>(N), beta, bf16 ? 1 : 0);
 }
 
-TileParams tile_params(int64_t M, int64_t N, int64_t K, int tile_n_out, float alpha, float beta,
-                       const void* C, int64_t ldc, int64_t tiles) {
+TileParams tile_params(int64_t M, int64_t N, int64_t K, int tile_m, int tile_n_out, float alpha,
+                       float beta, const void* C, int64_t ldc, int64_t tiles) {
   TileParams p;
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.m_blocks = static_cast<int>(ceil_div(M, kBM));
+  p.m_blocks = static_cast<int>(ceil_div(M, tile_m));
   p.n_blocks = static_cast<int>(ceil_div(N, tile_n_out));
   p.k_blocks = static_cast<int>(ceil_div(K, kBK));
   p.num_tiles = static_cast<int>(tiles);
@@ -429,6 +580,59 @@ TileParams tile_params(int64_t M, int64_t N, int64_t K, int tile_n_out, float al
   p.C = C;
   p.ldc = ldc;
   return p;
+}
+
+template <int BN, int EPI>
+int launch_pair_gemm(const gemm_plan& pl, int dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                     const CUtensorMap& tmB2, const CUtensorMap& tmOut, const TileParams& p,
+                     cudaStream_t stream) {
+  using Cfg = PairCfg<BN, kPairStages, EPI>;
+  auto kern = gemm_pair_kernel<BN, kPairStages, EPI>;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const int st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), Cfg::kSmemBytes);
+    if (st != GEMM_OK) return st;
+  }
+  return launch_pair(kern, pl.grid, Cfg::kSmemBytes, stream, tmA, tmB, tmB2, tmOut, p);
+}
+
+// Output descriptor of an epilogue box: FP32 32 x 32 (128-byte swizzle);
+// BF16 64 x 32 (128-byte swizzle) or, for tile widths not a multiple of 64,
+// 32 x 32 (64-byte swizzle).  Must match EpiBox in gemm_kernels.cuh.
+int output_map(CUtensorMap* out, void* C, int64_t M, int64_t N, int64_t ldc, bool bf16,
+               int tile_out_cols) {
+  if (!bf16)
+    return tensor_map_2d(out, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, M, ldc * 4, 32, 32);
+  if (tile_out_cols % 64 == 0)
+    return tensor_map_2d(out, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldc * 2, 64, 32);
+  return tensor_map_2d(out, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldc * 2, 32, 32,
+                       CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+int run_pair(const gemm_plan& pl, int dev, int64_t M, int64_t N, int64_t K, float alpha,
+             const void* A, int64_t lda, const void* B, int64_t ldb, float beta, void* C,
+             int64_t ldc, bool bf16, cudaStream_t stream) {
+  const int bn = pl.tile_n;
+  CUtensorMap tmA, tmB, tmOut;
+  int st;
+  if ((st = tensor_map_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, lda * 2, kBK, 128)) !=
+      GEMM_OK)
+    return st;
+  if ((st = tensor_map_2d(&tmB, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldb * 2, kBK,
+                          bn / 2)) != GEMM_OK)
+    return st;
+  if ((st = output_map(&tmOut, C, M, N, ldc, bf16, bn)) != GEMM_OK) return st;
+  const TileParams p = tile_params(M, N, K, kPairBM, bn, alpha, beta, C, ldc, pl.tiles);
+  switch (bn) {
+    case 256:
+      return bf16 ? launch_pair_gemm<256, EPI_BF16>(pl, dev, tmA, tmB, tmB, tmOut, p, stream)
+                  : launch_pair_gemm<256, EPI_F32>(pl, dev, tmA, tmB, tmB, tmOut, p, stream);
+    case 224:
+      return bf16 ? launch_pair_gemm<224, EPI_BF16>(pl, dev, tmA, tmB, tmB, tmOut, p, stream)
+                  : launch_pair_gemm<224, EPI_F32>(pl, dev, tmA, tmB, tmB, tmOut, p, stream);
+    default:
+      return GEMM_ERR_UNSUPPORTED;
+  }
 }
 
 }  // namespace
@@ -483,17 +687,20 @@ int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int dev;
   if ((st = current_device(&dev)) != GEMM_OK) return st;
-  int sms;
+  int sms, slots;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if ((st = probe_device(dev)) != GEMM_OK) return st;
     sms = g_dev[dev].sms;
+    slots = query_pair_slots(dev);
   }
   gemm_plan pl;
-  plan_gemm(M, N, K, sms, &pl);
+  plan_gemm(M, N, K, sms, &pl, slots);
   const bool bf16 = out_dtype == GEMM_OUT_BF16;
 
   if (pl.kernel == K_SCALE) return run_scale(pl, C, ldc, M, N, beta, bf16, stream);
+  if (pl.kernel == K_PAIR) return run_pair(pl, dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                           bf16, stream);
 
   if (pl.kernel == K_SKINNY) {
     CUtensorMap tmW, tmX;
@@ -550,7 +757,7 @@ int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64
     st = tensor_map_2d(&tmOut, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, M, ldc * 4, 32, 32);
   }
   if (st != GEMM_OK) return st;
-  const TileParams p = tile_params(M, N, K, kTileN, alpha, beta, C, ldc, pl.tiles);
+  const TileParams p = tile_params(M, N, K, kBM, kTileN, alpha, beta, C, ldc, pl.tiles);
   if (bf16) {
     auto kern = gemm_tc_kernel<kTileN, kStages, EPI_BF16>;
     {
@@ -580,15 +787,32 @@ int gemm_gate_up_silu(int64_t M, int64_t N, int64_t K, const void* X, int64_t ld
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int dev;
   if ((st = current_device(&dev)) != GEMM_OK) return st;
-  int sms;
+  int sms, slots;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if ((st = probe_device(dev)) != GEMM_OK) return st;
     sms = g_dev[dev].sms;
+    slots = query_pair_slots(dev);
   }
   gemm_plan pl;
-  plan_gate_up(M, N, K, sms, &pl);
+  plan_gate_up(M, N, K, sms, &pl, slots);
   if (pl.kernel == K_SCALE) return run_scale(pl, Y, ldy, M, N, 0.0f, true, stream);
+  if (pl.kernel == K_PAIR_GATE_UP) {
+    CUtensorMap tmX, tmWg, tmWu, tmY;
+    if ((st = tensor_map_2d(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, ldx * 2, kBK, 128)) !=
+        GEMM_OK)
+      return st;
+    if ((st = tensor_map_2d(&tmWg, Wg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldw * 2, kBK,
+                            CfgPairGU::kOutCols)) != GEMM_OK)
+      return st;
+    if ((st = tensor_map_2d(&tmWu, Wu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldw * 2, kBK,
+                            CfgPairGU::kOutCols)) != GEMM_OK)
+      return st;
+    if ((st = output_map(&tmY, Y, M, N, ldy, true, CfgPairGU::kOutCols)) != GEMM_OK) return st;
+    const TileParams p = tile_params(M, N, K, kPairBM, CfgPairGU::kOutCols, 1.0f, 0.0f, nullptr,
+                                     ldy, pl.tiles);
+    return launch_pair_gemm<256, EPI_GATE_UP>(pl, dev, tmX, tmWg, tmWu, tmY, p, stream);
+  }
 
   CUtensorMap tmX, tmWg, tmWu, tmY;
   if ((st = tensor_map_2d(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, ldx * 2, kBK, kBM)) !=
@@ -603,7 +827,8 @@ int gemm_gate_up_silu(int64_t M, int64_t N, int64_t K, const void* X, int64_t ld
   if ((st = tensor_map_2d(&tmY, Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldy * 2, 64, 32)) !=
       GEMM_OK)
     return st;
-  const TileParams p = tile_params(M, N, K, CfgGU::kOutCols, 1.0f, 0.0f, nullptr, ldy, pl.tiles);
+  const TileParams p =
+      tile_params(M, N, K, kBM, CfgGU::kOutCols, 1.0f, 0.0f, nullptr, ldy, pl.tiles);
   auto kern = gemm_tc_kernel<256, kGateUpStages, EPI_GATE_UP>;
   {
     std::lock_guard<std::mutex> lk(g_mu);

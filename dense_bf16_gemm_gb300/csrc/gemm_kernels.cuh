@@ -58,11 +58,20 @@ __device__ __noinline__ void record_timeout(int site) {
   }
 }
 
+template <bool kClusterScope = false>
+__device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
+  if constexpr (kClusterScope)
+    return mbar_try_wait_cluster(bar, parity);
+  else
+    return mbar_try_wait(bar, parity);
+}
+
+template <bool kClusterScope>
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                        int site, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_wait_scoped<kClusterScope>(bar, parity)) return true;
     if ((i & 255u) == 0) {
       if (abort_flag != nullptr && *abort_flag) return false;
       if (global_timer_ns() - t0 > limit_ns) {
@@ -80,7 +89,15 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile int* abort_flag, int site,
                                              uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, abort_flag, site, limit_ns);
+  return wait_slow<false>(bar, parity, abort_flag, site, limit_ns);
+}
+
+// Same for a barrier that threads of the other CTA of a cluster arrive on
+// (acquires at cluster scope).
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                     volatile int* abort_flag, int site) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  return wait_slow<true>(bar, parity, abort_flag, site, kWaitLimitNs);
 }
 
 // Self-test of the failure path: one thread waits on a barrier nothing
@@ -186,6 +203,101 @@ __device__ __forceinline__ void scale_slice(float (&v)[32], const TileParams& p,
 }
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + __expf(-g)); }
+
+// Geometry of one epilogue store box: 32 rows (one warp's TMEM band) by kCols
+// output columns.  FP32: 32 columns = 128-byte rows with the 128-byte swizzle.
+// BF16: 64 columns (128-byte rows, 128-byte swizzle) when the tile's output
+// width is a multiple of 64, else 32 columns (64-byte rows, 64-byte swizzle).
+template <int EPI, int OUT_COLS>
+struct EpiBox {
+  static constexpr int kCols = (EPI == EPI_F32) ? 32 : (OUT_COLS % 64 == 0 ? 64 : 32);
+  static constexpr int kRowBytes = (EPI == EPI_F32) ? 128 : kCols * 2;
+  static constexpr bool kSwizzle128 = kRowBytes == 128;
+  static_assert(OUT_COLS % kCols == 0, "tile width must be a whole number of boxes");
+  static_assert(32 * kRowBytes <= kStageBox, "staging slot");
+};
+
+// Shared-memory byte offset of 16-byte chunk `chunk` of staging row `row`, as
+// the TMA swizzle lays the box out: 128-byte rows XOR the chunk with row % 8,
+// 64-byte rows XOR it with (row / 2) % 4 (both are the address bits 7.. folded
+// into bits 4..).  Consecutive rows then hit different banks.
+template <bool kSw128>
+__device__ __forceinline__ uint32_t staging_offset(int row, uint32_t chunk) {
+  if constexpr (kSw128)
+    return static_cast<uint32_t>(row) * 128u + ((chunk ^ static_cast<uint32_t>(row & 7)) << 4);
+  else
+    return static_cast<uint32_t>(row) * 64u +
+           ((chunk ^ static_cast<uint32_t>((row >> 1) & 3)) << 4);
+}
+
+// One warp's share of a tile epilogue: rows m0..m0+31 (this warp's TMEM lane
+// band, accumulator at TMEM address `tacc`) and the tile's output columns
+// from n0.  Each box is loaded from TMEM 32 columns at a time, transformed in
+// FP32, written to a staging slot in the swizzled layout and stored with TMA.
+// `sc` counts the boxes this warp staged (two slots alternate); every staged
+// box is committed as its own bulk group.
+template <int BN, int EPI>
+__device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtensorMap* tmOut,
+                                              uint32_t tacc, int m0, int n0, uint32_t staging,
+                                              int lane, int& sc, bool have_acc) {
+  constexpr int OUT = (EPI == EPI_GATE_UP) ? BN / 2 : BN;
+  using Box = EpiBox<EPI, OUT>;
+  const int row = m0 + lane;
+#pragma unroll 1
+  for (int c0 = 0; c0 < OUT; c0 += Box::kCols) {
+    // Boxes wholly outside C are neither computed nor stored (warp-uniform).
+    if (m0 >= p.M || n0 + c0 >= p.N) continue;
+    const uint32_t stg = staging + (sc & 1) * kStageBox;
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < Box::kCols / 32; ++h) {
+      float v[32];
+      if constexpr (EPI == EPI_GATE_UP) {
+        float u[32];
+        if (have_acc) {
+          tmem_load_32x32b_x32(tacc + c0 + 32 * h, v);
+          tmem_load_32x32b_x32(tacc + OUT + c0 + 32 * h, u);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = u[i] = 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = silu_f32(v[i]) * u[i];
+      } else {
+        if (have_acc) {
+          tmem_load_32x32b_x32(tacc + c0 + 32 * h, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        }
+        scale_slice<EPI>(v, p, row, n0 + c0 + 32 * h);
+      }
+      if constexpr (EPI == EPI_F32) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          st_shared_v4(stg + staging_offset<true>(lane, static_cast<uint32_t>(q)),
+                       __float_as_uint(v[4 * q + 0]), __float_as_uint(v[4 * q + 1]),
+                       __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          st_shared_v4(stg + staging_offset<Box::kSwizzle128>(lane, static_cast<uint32_t>(4 * h + q)),
+                       pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
+                       pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                       pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                       pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+      }
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmOut, stg, n0 + c0, m0);
+      bulk_commit_group();
+    }
+    ++sc;
+  }
+}
 
 template <int BN, int STAGES, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -325,8 +437,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 2;                 // staging slot owner
     const int band = (warp & 3) * 32;        // TMEM lanes this warp may access
     const uint32_t staging = sbase + Cfg::kRingBytes + ew * kStagingPerWarp * kStageBox;
-    const uint32_t swz = static_cast<uint32_t>(lane & 7);
-    const uint32_t row_off = static_cast<uint32_t>(lane) * 128u;
     int local = 0;
     int sc = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
@@ -340,121 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(band) << 16) +
                             static_cast<uint32_t>(buf * Cfg::kAccStride);
       const int m0 = mb * kBM + band;
-      const int row = m0 + lane;
-      const bool have_acc = p.k_blocks > 0;
-
-      if constexpr (EPI == EPI_F32) {
-        const int n0 = nb * BN;
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          // Boxes wholly outside C are neither computed nor stored (warp-uniform).
-          if (m0 >= p.M || n0 + c0 >= p.N) continue;
-          const uint32_t stg = staging + (sc & 1) * kStageBox;
-          if (lane == 0) bulk_wait_group_read<1>();
-          __syncwarp();
-          float v[32];
-          if (have_acc) {
-            tmem_load_32x32b_x32(tacc + c0, v);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-          }
-          scale_slice<EPI>(v, p, row, n0 + c0);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            st_shared_v4(stg + row_off + ((static_cast<uint32_t>(q) ^ swz) << 4),
-                         __float_as_uint(v[4 * q + 0]), __float_as_uint(v[4 * q + 1]),
-                         __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
-          fence_proxy_async_shared();
-          __syncwarp();
-          // Every staged box is stored and committed as its own bulk group, so
-          // wait_group.read<1> above always refers to this buffer's last store.
-          if (lane == 0) {
-            tma_store_2d(&tmOut, stg, n0 + c0, m0);
-            bulk_commit_group();
-          }
-          ++sc;
-        }
-      } else if constexpr (EPI == EPI_BF16) {
-        const int n0 = nb * BN;
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 64) {
-          if (m0 >= p.M || n0 + c0 >= p.N) continue;
-          const uint32_t stg = staging + (sc & 1) * kStageBox;
-          if (lane == 0) bulk_wait_group_read<1>();
-          __syncwarp();
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float v[32];
-            if (have_acc) {
-              tmem_load_32x32b_x32(tacc + c0 + 32 * h, v);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-            }
-            scale_slice<EPI>(v, p, row, n0 + c0 + 32 * h);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t chunk = static_cast<uint32_t>(4 * h + q);
-              st_shared_v4(stg + row_off + ((chunk ^ swz) << 4),
-                           pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
-                           pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                           pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-            }
-          }
-          fence_proxy_async_shared();
-          __syncwarp();
-          // Every staged box is stored and committed as its own bulk group, so
-          // wait_group.read<1> above always refers to this buffer's last store.
-          if (lane == 0) {
-            tma_store_2d(&tmOut, stg, n0 + c0, m0);
-            bulk_commit_group();
-          }
-          ++sc;
-        }
-      } else {
-        // gate/up: accumulator columns [0, BN/2) hold X.Wg, [BN/2, BN) hold X.Wu.
-        const int n0 = nb * (BN / 2);
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN / 2; c0 += 64) {
-          if (m0 >= p.M || n0 + c0 >= p.N) continue;
-          const uint32_t stg = staging + (sc & 1) * kStageBox;
-          if (lane == 0) bulk_wait_group_read<1>();
-          __syncwarp();
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float g[32], u[32];
-            if (have_acc) {
-              tmem_load_32x32b_x32(tacc + c0 + 32 * h, g);
-              tmem_load_32x32b_x32(tacc + BN / 2 + c0 + 32 * h, u);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) g[i] = u[i] = 0.0f;
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) g[i] = silu_f32(g[i]) * u[i];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t chunk = static_cast<uint32_t>(4 * h + q);
-              st_shared_v4(stg + row_off + ((chunk ^ swz) << 4),
-                           pack_bf16x2(g[8 * q + 0], g[8 * q + 1]),
-                           pack_bf16x2(g[8 * q + 2], g[8 * q + 3]),
-                           pack_bf16x2(g[8 * q + 4], g[8 * q + 5]),
-                           pack_bf16x2(g[8 * q + 6], g[8 * q + 7]));
-            }
-          }
-          fence_proxy_async_shared();
-          __syncwarp();
-          // Every staged box is stored and committed as its own bulk group, so
-          // wait_group.read<1> above always refers to this buffer's last store.
-          if (lane == 0) {
-            tma_store_2d(&tmOut, stg, n0 + c0, m0);
-            bulk_commit_group();
-          }
-          ++sc;
-        }
-      }
+      const int n0 = nb * Cfg::kOutCols;
+      epilogue_tile<BN, EPI>(p, &tmOut, tacc, m0, n0, staging, lane, sc, p.k_blocks > 0);
       // The accumulator may be overwritten once every lane's TMEM reads are done.
       tc_fence_before_sync();
       __syncwarp();

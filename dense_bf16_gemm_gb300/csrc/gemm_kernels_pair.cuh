@@ -1,0 +1,223 @@
+// gemm_kernels_pair.cuh -- the persistent GEMM on CTA pairs (tcgen05
+// cta_group::2): a cluster of two CTAs on the two SMs of a TPC computes one
+// 256 x BN output tile.
+//
+//   * Each CTA stages its own 128 rows of A and its own half (BN/2 rows) of
+//     B per k-block, so each SM streams half the B traffic of a 128 x BN
+//     single-CTA tile for the same MMA work, and a stage is 16 KB + BN*64 B
+//     (6 stages fit beside the epilogue staging).
+//   * The even CTA's MMA thread issues tcgen05.mma.cta_group::2 (M = 256);
+//     the hardware reads A and B from both CTAs' shared memory at the same
+//     offsets and writes D rows 0..127 to the even CTA's TMEM and rows
+//     128..255 to the odd CTA's TMEM.
+//   * Both producers count their TMA bytes on the even CTA's `full` barrier
+//     (which expects the pair's total); the MMA completion is multicast to
+//     both CTAs' `empty` and `acc_full` barriers; both CTAs' epilogue warps
+//     arrive on the even CTA's `acc_empty` (8 arrivals).
+//   * Gate/up: the even CTA stages the Wg tile and the odd CTA the Wu tile,
+//     so one MMA of N = 256 yields gate (columns 0..127) and up (128..255)
+//     for all 256 rows.
+//
+// The epilogue, the bounded waits and the tile order are those of the
+// single-CTA kernel (gemm_kernels.cuh).
+#pragma once
+
+#include "gemm_kernels.cuh"
+
+namespace gb3 {
+
+constexpr int kPairBM = 256;  // tile rows of a CTA pair
+
+template <int BN, int STAGES, int EPI>
+struct PairCfg {
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile width");
+  static constexpr int kABytes = 128 * kBK * 2;       // this CTA's 128 rows of A
+  static constexpr int kBBytes = (BN / 2) * kBK * 2;  // this CTA's half of B
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static_assert(kStageBytes % 1024 == 0, "stages must keep the 1024-byte swizzle phase");
+  static constexpr int kRingBytes = STAGES * kStageBytes;
+  static constexpr int kStagingBytes = kEpiWarps * kStagingPerWarp * kStageBox;
+  static constexpr int kBarOffset = kRingBytes + kStagingBytes;
+  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+  static constexpr int kOutCols = (EPI == EPI_GATE_UP) ? BN / 2 : BN;
+  static constexpr int kAccStride = 256;
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(kPairBM, BN);
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+template <int BN, int STAGES, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmB2,
+                     const __grid_constant__ CUtensorMap tmOut, const TileParams p) {
+  using Cfg = PairCfg<BN, STAGES, EPI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOffset);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs, 1: its peer
+  const int cluster = static_cast<int>(cluster_id_x());
+  const int nclusters = static_cast<int>(num_clusters_x());
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 2 * kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    if constexpr (EPI == EPI_GATE_UP) prefetch_tensormap(&tmB2);
+    prefetch_tensormap(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish_alloc_permit_pair();
+  }
+  tc_fence_before_sync();
+  cluster_sync();  // both CTAs' barriers exist and TMEM is allocated in both
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint32_t full0_even = mapa_shared(full_bar(0), 0);
+      int s = 0;
+      uint32_t ph = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters) {
+        int mb, nb;
+        tile_coords(tile, p, mb, nb);
+        const int a_row = mb * kPairBM + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint32_t a_dst = sbase + s * Cfg::kStageBytes;
+          const uint32_t b_dst = a_dst + Cfg::kABytes;
+          const uint32_t fbar = full0_even + 8u * s;
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * Cfg::kStageBytes);
+          tma_load_2d_pair(a_dst, &tmA, fbar, kb * kBK, a_row);
+          if constexpr (EPI == EPI_GATE_UP) {
+            tma_load_2d_pair(b_dst, rank == 0 ? &tmB : &tmB2, fbar, kb * kBK, nb * (BN / 2));
+          } else {
+            tma_load_2d_pair(b_dst, &tmB, fbar, kb * kBK,
+                             nb * BN + static_cast<int>(rank) * (BN / 2));
+          }
+          ++issued;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (rank == 0) {
+        // The even CTA's full barriers count both CTAs' copies: wait (bounded)
+        // until the last STAGES rounds have landed before shared memory goes.
+        const long long first = issued > STAGES ? issued - STAGES : 0;
+        for (long long i = first; i < issued; ++i)
+          wait_bounded(full_bar(static_cast<int>(i % STAGES)),
+                       static_cast<uint32_t>((i / STAGES) & 1), nullptr, SITE_DRAIN);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters, ++local) {
+        const int buf = local & 1;
+        const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
+        if (!wait_bounded_cluster(acce_bar(buf), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_bounded(full_bar(s), ph, abort_flag, SITE_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_addr = sbase + s * Cfg::kStageBytes;
+          const uint64_t adesc = smem_desc_sw128(a_addr);
+          const uint64_t bdesc = smem_desc_sw128(a_addr + Cfg::kABytes);
+#pragma unroll
+          for (int j = 0; j < kBK / kUmmaK; ++j)
+            umma_bf16_pair(d_tmem, adesc + 2u * j, bdesc + 2u * j, Cfg::kIdesc,
+                           (kb | j) != 0 ? 1u : 0u);
+          umma_commit_pair_multicast(empty_bar(s), 0x3);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_multicast(accf_bar(buf), 0x3);
+      }
+      umma_commit_pair_multicast(drain_bar, 0x1);
+      wait_bounded(drain_bar, 0, nullptr, SITE_DRAIN);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int ew = warp - 2;
+    const int band = (warp & 3) * 32;
+    const uint32_t staging = sbase + Cfg::kRingBytes + ew * kStagingPerWarp * kStageBox;
+    const uint32_t acce0_even = mapa_shared(acce_bar(0), 0);
+    int local = 0;
+    int sc = 0;
+    for (int tile = cluster; tile < p.num_tiles; tile += nclusters, ++local) {
+      int mb, nb;
+      tile_coords(tile, p, mb, nb);
+      const int buf = local & 1;
+      const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
+      const bool got = wait_bounded(accf_bar(buf), aph, abort_flag, SITE_EPI_ACC_FULL);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after_sync();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(band) << 16) +
+                            static_cast<uint32_t>(buf * Cfg::kAccStride);
+      const int m0 = mb * kPairBM + static_cast<int>(rank) * 128 + band;
+      const int n0 = nb * Cfg::kOutCols;
+      epilogue_tile<BN, EPI>(p, &tmOut, tacc, m0, n0, staging, lane, sc, p.k_blocks > 0);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acce0_even + 8u * buf);
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  cluster_sync();  // neither CTA leaves while its peer may still signal it
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace gb3

@@ -162,7 +162,8 @@ GEMM_API int gemm_selftest_wait_timeout(int64_t limit_ns, void *stream);
 
 /* How a call would be executed (host-side planning only). */
 typedef struct gemm_plan {
-    int kernel;       /* 0 none, 1 tiled tcgen05 GEMM, 2 skinny split-K, 3 scale only (K == 0), 4 gate/up */
+    int kernel;       /* 0 none, 1 single-CTA tiled GEMM, 2 skinny split-K, 3 scale only (K == 0),
+                         4 single-CTA gate/up, 5 CTA-pair tiled GEMM, 6 CTA-pair gate/up */
     int tile_m;       /* output rows per tile (tcgen05 M, or weight rows for the skinny path) */
     int tile_n;       /* output columns per tile */
     int tile_k;       /* K per pipeline stage */
@@ -177,8 +178,11 @@ typedef struct gemm_plan {
 
 /*
  * Plan of gemm_bf16(M, N, K, ...) on a device with num_sms SMs (num_sms <= 0:
- * query the current device).  Pure host logic; returns GEMM_INVALID_ARG for
- * invalid sizes or dtype.
+ * query the current device, including how many CTA pairs fit at once).  Pure
+ * host logic otherwise; returns GEMM_INVALID_ARG for invalid sizes or dtype.
+ * M > 128 runs on CTA pairs (256-row tiles) with the tile width that needs the
+ * fewest waves; the environment variable GB3_GEMM_PAIR_TILE_N (256 or 224)
+ * forces one width, for tuning and tests.
  */
 GEMM_API int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int num_sms,
                    gemm_plan *plan);

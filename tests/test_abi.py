@@ -98,18 +98,51 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
     assert st in (_native.GEMM_ERR_CUDA, _native.GEMM_ERR_UNSUPPORTED)
 
 
-def test_plan_tiled(lib):
+def test_plan_pair_4096(lib):
     st, p = _native.gemm_bf16_plan(4096, 4096, 4096, _native.GEMM_OUT_BF16, 152)
     assert st == 0
     d = p.as_dict()
-    assert d["kernel_name"] == "tiled"
-    assert d["tile_m"] == 128 and d["tile_k"] == 64
-    assert d["tiles"] == (4096 // 128) * -(-4096 // d["tile_n"])
-    assert d["grid"] == min(d["tiles"], 152)
+    assert d["kernel_name"] == "pair"
+    assert d["tile_m"] == 256 and d["tile_k"] == 64 and d["stages"] == 6
+    # width 224 makes 16 x 19 = 304 pair tiles: exactly 4 waves of 76 pairs
+    assert d["tile_n"] == 224
+    assert d["tiles"] == 16 * 19
+    assert d["grid"] == 152
     assert d["launches"] == 1
-    # one stage = a 128x64 BF16 A box (16384 bytes) plus the B box
-    assert d["stage_tx_bytes"] == 16384 + d["tile_n"] * 64 * 2
+    # per stage each CTA receives a 128x64 A box (16384 bytes, the pages'
+    # transfer size of a 128x64 BF16 tile) and half the B rows
+    assert d["stage_tx_bytes"] == 2 * (16384 + 112 * 64 * 2)
     assert d["smem_bytes"] <= 232448
+
+
+def test_plan_pair_width_minimises_waves(lib):
+    for (M, N), want in {(4096, 14336): 256, (3000, 5000): 224, (8192, 8192): 256}.items():
+        st, p = _native.gemm_bf16_plan(M, N, 4096, _native.GEMM_OUT_F32, 152)
+        d = p.as_dict()
+        assert st == 0 and d["kernel_name"] == "pair"
+        costs = {}
+        for bn in (256, 224):
+            tiles = -(-M // 256) * -(-N // bn)
+            costs[bn] = -(-tiles // 76) * (bn + 32)
+        assert d["tile_n"] == min(costs, key=costs.get) == want
+
+
+def test_plan_forced_pair_width(lib, monkeypatch):
+    monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", "256")
+    st, p = _native.gemm_bf16_plan(4096, 4096, 4096, _native.GEMM_OUT_BF16, 152)
+    assert st == 0 and p.tile_n == 256 and p.tiles == 16 * 16
+    monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", "100")   # not compiled: ignored
+    st, p = _native.gemm_bf16_plan(4096, 4096, 4096, _native.GEMM_OUT_BF16, 152)
+    assert st == 0 and p.tile_n == 224
+
+
+def test_plan_single_cta_below_two_row_blocks(lib):
+    st, p = _native.gemm_bf16_plan(128, 4096, 4096, _native.GEMM_OUT_BF16, 152)
+    d = p.as_dict()
+    assert st == 0 and d["kernel_name"] == "tiled"
+    assert d["tile_m"] == 128 and d["tile_n"] == 256
+    assert d["tiles"] == 16 and d["grid"] == 16
+    assert d["stage_tx_bytes"] == 16384 + 256 * 64 * 2
 
 
 def test_plan_ragged_tiles_cover_the_output(lib):
@@ -150,9 +183,14 @@ def test_plan_gate_up(lib):
     st, p = _native.gemm_gate_up_plan(4096, 14336, 4096, 152)
     assert st == 0
     d = p.as_dict()
-    assert d["kernel_name"] == "gate_up"
-    assert d["tiles"] == 32 * (14336 // d["tile_n"])
-    # X box + Wg box + Wu box per stage
+    assert d["kernel_name"] == "pair_gate_up"
+    assert d["tile_m"] == 256 and d["tile_n"] == 128
+    assert d["tiles"] == 16 * 112
+    # per CTA: X box + (Wg box on the even CTA | Wu box on the odd CTA)
+    assert d["stage_tx_bytes"] == 2 * 2 * 16384
+    st, p = _native.gemm_gate_up_plan(100, 14336, 4096, 152)
+    d = p.as_dict()
+    assert d["kernel_name"] == "gate_up" and d["tile_m"] == 128
     assert d["stage_tx_bytes"] == 3 * 16384
 
 

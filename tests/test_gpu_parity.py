@@ -364,3 +364,21 @@ def test_bounded_wait_reports_timeout(g):
     out = run_gemm(g, A, B, out_dtype=torch.float32)
     ref, _ = oracle.gemm_full(A, B)
     assert np.array_equal(to_f64(out), ref)
+
+
+@pytest.mark.parametrize("width", ["256", "224"])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (512, 1000, 1000), (2000, 712, 136)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_pair_widths_bit_exact(g, monkeypatch, width, M, N, K, out_dtype):
+    """Every compiled CTA-pair tile width, forced, on integer inputs."""
+    monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", width)
+    p = g.plan(M, N, K, out_dtype)
+    assert p["kernel_name"] == "pair" and p["tile_n"] == int(width)
+    A, B, _ = int_inputs(M, N, K, seed=M + 3 * N + K)
+    ref, _ = oracle.gemm_full(A, B)
+    out = run_gemm(g, A, B, out_dtype=out_dtype)
+    if out_dtype == torch.float32:
+        assert np.array_equal(to_f64(out), ref)
+    else:
+        assert np.array_equal(bits(out.cpu()), oracle.round_to_bf16_bits(ref))
+    assert_status_ok(g)
