@@ -154,50 +154,48 @@ struct GemmCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// Epilogue arithmetic for one 32-column slice of a thread's row.
+// The 32 values of C at (row, col0..col0+31) in FP32, zero outside C.  The
+// loads are plain (C is written later by this same CTA's TMA stores).
 template <int EPI>
-__device__ __forceinline__ void scale_slice(float (&v)[32], const TileParams& p, int row,
-                                            int col0) {
-  const float alpha = p.alpha;
+__device__ __forceinline__ void load_c_slice(float (&c)[32], const TileParams& p, int row,
+                                             int col0) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] *= alpha;
-  if (p.beta != 0.0f && row < p.M) {
-    const float beta = p.beta;
-    if constexpr (EPI == EPI_F32) {
-      const float* c = static_cast<const float*>(p.C) + static_cast<long long>(row) * p.ldc + col0;
-      if (col0 + 32 <= p.N) {
+  for (int i = 0; i < 32; ++i) c[i] = 0.0f;
+  if (row >= p.M || col0 >= p.N) return;
+  if constexpr (EPI == EPI_F32) {
+    const float* src = static_cast<const float*>(p.C) + static_cast<long long>(row) * p.ldc + col0;
+    if (col0 + 32 <= p.N) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 x = reinterpret_cast<const float4*>(c)[q];
-          v[4 * q + 0] += beta * x.x;
-          v[4 * q + 1] += beta * x.y;
-          v[4 * q + 2] += beta * x.z;
-          v[4 * q + 3] += beta * x.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (col0 + i < p.N) v[i] += beta * c[i];
+      for (int q = 0; q < 8; ++q) {
+        const float4 x = reinterpret_cast<const float4*>(src)[q];
+        c[4 * q + 0] = x.x;
+        c[4 * q + 1] = x.y;
+        c[4 * q + 2] = x.z;
+        c[4 * q + 3] = x.w;
       }
     } else {
-      const uint16_t* c =
-          static_cast<const uint16_t*>(p.C) + static_cast<long long>(row) * p.ldc + col0;
-      if (col0 + 32 <= p.N) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 x = reinterpret_cast<const uint4*>(c)[q];
-          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      for (int i = 0; i < 32; ++i)
+        if (col0 + i < p.N) c[i] = src[i];
+    }
+  } else {
+    const uint16_t* src =
+        static_cast<const uint16_t*>(p.C) + static_cast<long long>(row) * p.ldc + col0;
+    if (col0 + 32 <= p.N) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            v[8 * q + 2 * j + 0] += beta * bf16_bits_to_float(w[j] & 0xFFFFu);
-            v[8 * q + 2 * j + 1] += beta * bf16_bits_to_float(w[j] >> 16);
-          }
+      for (int q = 0; q < 4; ++q) {
+        const uint4 x = reinterpret_cast<const uint4*>(src)[q];
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          c[8 * q + 2 * j + 0] = bf16_bits_to_float(w[j] & 0xFFFFu);
+          c[8 * q + 2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (col0 + i < p.N) v[i] += beta * bf16_bits_to_float(c[i]);
       }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (col0 + i < p.N) c[i] = bf16_bits_to_float(src[i]);
     }
   }
 }
@@ -242,7 +240,13 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
                                               int lane, int& sc, bool have_acc) {
   constexpr int OUT = (EPI == EPI_GATE_UP) ? BN / 2 : BN;
   using Box = EpiBox<EPI, OUT>;
+  constexpr int kSub = Box::kCols / 32;  // 32-column slices per box
   const int row = m0 + lane;
+  const bool read_c = (EPI != EPI_GATE_UP) && p.beta != 0.0f;
+  // C of the next slice is loaded one slice ahead so its latency overlaps the
+  // TMEM load and conversion of the current one.
+  float c_next[32];
+  if (read_c) load_c_slice<EPI>(c_next, p, row, n0);
 #pragma unroll 1
   for (int c0 = 0; c0 < OUT; c0 += Box::kCols) {
     // Boxes wholly outside C are neither computed nor stored (warp-uniform).
@@ -251,7 +255,7 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
     if (lane == 0) bulk_wait_group_read<1>();
     __syncwarp();
 #pragma unroll
-    for (int h = 0; h < Box::kCols / 32; ++h) {
+    for (int h = 0; h < kSub; ++h) {
       float v[32];
       if constexpr (EPI == EPI_GATE_UP) {
         float u[32];
@@ -265,13 +269,27 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = silu_f32(v[i]) * u[i];
       } else {
+        float c_cur[32];
+        if (read_c) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) c_cur[i] = c_next[i];
+          const int next = c0 + 32 * (h + 1);
+          if (next < OUT) load_c_slice<EPI>(c_next, p, row, n0 + next);
+        }
         if (have_acc) {
           tmem_load_32x32b_x32(tacc + c0 + 32 * h, v);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.0f;
         }
-        scale_slice<EPI>(v, p, row, n0 + c0 + 32 * h);
+        const float alpha = p.alpha;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= alpha;
+        if (read_c) {
+          const float beta = p.beta;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] += beta * c_cur[i];
+        }
       }
       if constexpr (EPI == EPI_F32) {
 #pragma unroll
@@ -296,6 +314,20 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
       bulk_commit_group();
     }
     ++sc;
+  }
+}
+
+// When C is read (beta != 0): ask L2 for this warp's band of C of a coming
+// tile (rows m0..m0+31, the tile's columns from n0), box by box.
+template <int BN, int EPI>
+__device__ __forceinline__ void prefetch_c_band(const TileParams& p, const CUtensorMap* tmOut,
+                                                int m0, int n0) {
+  if constexpr (EPI == EPI_GATE_UP) {
+    return;
+  } else {
+    if (p.beta == 0.0f || m0 >= p.M) return;
+    using Box = EpiBox<EPI, BN>;
+    for (int c0 = 0; c0 < BN && n0 + c0 < p.N; c0 += Box::kCols) tma_prefetch_l2_2d(tmOut, n0 + c0, m0);
   }
 }
 
@@ -439,9 +471,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t staging = sbase + Cfg::kRingBytes + ew * kStagingPerWarp * kStageBox;
     int local = 0;
     int sc = 0;
+    if (lane == 0 && blockIdx.x < p.num_tiles) {
+      int mb_, nb_;
+      tile_coords(blockIdx.x, p, mb_, nb_);
+      prefetch_c_band<BN, EPI>(p, &tmOut, mb_ * kBM + band, nb_ * Cfg::kOutCols);
+    }
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
       int mb, nb;
       tile_coords(tile, p, mb, nb);
+      // C of the next tile of this CTA travels to L2 during this tile's
+      // epilogue and the next tile's main loop.
+      if (lane == 0 && tile + gridDim.x < p.num_tiles) {
+        int mb_, nb_;
+        tile_coords(tile + gridDim.x, p, mb_, nb_);
+        prefetch_c_band<BN, EPI>(p, &tmOut, mb_ * kBM + band, nb_ * Cfg::kOutCols);
+      }
       const int buf = local & 1;
       const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
       const bool got = wait_bounded(accf_bar(buf), aph, abort_flag, SITE_EPI_ACC_FULL);

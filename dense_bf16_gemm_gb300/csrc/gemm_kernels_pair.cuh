@@ -191,9 +191,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t acce0_even = mapa_shared(acce_bar(0), 0);
     int local = 0;
     int sc = 0;
+    if (lane == 0 && cluster < p.num_tiles) {
+      int mb_, nb_;
+      tile_coords(cluster, p, mb_, nb_);
+      prefetch_c_band<BN, EPI>(p, &tmOut, mb_ * kPairBM + static_cast<int>(rank) * 128 + band, nb_ * Cfg::kOutCols);
+    }
     for (int tile = cluster; tile < p.num_tiles; tile += nclusters, ++local) {
       int mb, nb;
       tile_coords(tile, p, mb, nb);
+      // C of the next tile of this CTA travels to L2 during this tile's
+      // epilogue and the next tile's main loop.
+      if (lane == 0 && tile + nclusters < p.num_tiles) {
+        int mb_, nb_;
+        tile_coords(tile + nclusters, p, mb_, nb_);
+        prefetch_c_band<BN, EPI>(p, &tmOut, mb_ * kPairBM + static_cast<int>(rank) * 128 + band, nb_ * Cfg::kOutCols);
+      }
       const int buf = local & 1;
       const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
       const bool got = wait_bounded(accf_bar(buf), aph, abort_flag, SITE_EPI_ACC_FULL);
