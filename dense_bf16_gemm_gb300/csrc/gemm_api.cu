@@ -106,35 +106,91 @@ void choose_split(int64_t n_blocks, int64_t k_blocks, int sms, int* splits, int*
   *kb_per = static_cast<int>(ceil_div(k_blocks, best_s));
 }
 
-// Tile width of the CTA-pair GEMM: fewest "waves" of pair tiles weighted by
-// the width (time per tile grows with it), with a fixed per-tile charge.
-int choose_pair_width(int64_t M, int64_t N, int slots, int64_t* tiles_out) {
-  int best = 256;
+constexpr int kMinPieceKb = 24;       // shortest K piece of a split tail tile (1536 of K)
+constexpr int kMaxTailSplit = 2;      // more pieces cost more partial-sum traffic than they save
+constexpr double kSplitCharge = 0.1;  // partial-sum traffic of a split tail, in waves
+constexpr int kWidthCostOffset = 320;  // per-wave time model of a pair tile: width + 320
+
+int env_int(const char* name, int fallback) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : fallback;
+}
+
+struct PairChoice {
+  int bn = 256;
+  int64_t tiles = 0;
+  int64_t full = 0;      // tiles run whole
+  int split = 1;         // K pieces per tail tile
+  int kb_per_piece = 0;
+};
+
+// Tail split of `tiles` pair tiles on `slots` resident pairs: the last,
+// partial wave's tiles are cut along K so that their pieces fill the pairs.
+void plan_tail(int64_t tiles, int64_t k_blocks, int slots, bool allow_split, PairChoice* c) {
+  c->tiles = tiles;
+  c->full = tiles;
+  c->split = 1;
+  c->kb_per_piece = static_cast<int>(k_blocks);
+  const int64_t tail = tiles % slots;
+  const int split_all = env_int("GB3_GEMM_SPLIT_ALL", 0);
+  if (allow_split && split_all > 1) {  // tests: every tile split into split_all pieces
+    const int64_t kbp = ceil_div(k_blocks, std::min<int64_t>(split_all, k_blocks));
+    c->full = 0;
+    c->kb_per_piece = static_cast<int>(kbp);
+    c->split = static_cast<int>(ceil_div(k_blocks, kbp));
+    return;
+  }
+  if (!allow_split || tail == 0 || env_int("GB3_GEMM_TAIL_SPLIT", 1) == 0) return;
+  int64_t s = std::min<int64_t>({static_cast<int64_t>(kMaxTailSplit), slots / tail,
+                                  k_blocks / kMinPieceKb});
+  if (s < 2) return;
+  const int64_t kbp = ceil_div(k_blocks, s);
+  c->full = tiles - tail;
+  c->kb_per_piece = static_cast<int>(kbp);
+  c->split = static_cast<int>(ceil_div(k_blocks, kbp));
+}
+
+// Tile width of the CTA-pair GEMM and its tail split: the fewest waves of
+// pair tiles (a split tail wave counts 1/split of a wave plus a charge for its
+// partial sums) weighted by the time a wave of that width takes.
+PairChoice choose_pair(int64_t M, int64_t N, int64_t K, int slots, bool allow_split) {
+  PairChoice best;
   double best_cost = 1e300;
   const int64_t mb = ceil_div(M, kPairBM);
+  const int64_t kb = ceil_div(K, kBK);
   // GB3_GEMM_PAIR_TILE_N=<width> restricts the choice to one compiled width
   // (tuning and tests); other values are ignored.
-  int forced = 0;
-  if (const char* env = std::getenv("GB3_GEMM_PAIR_TILE_N")) forced = std::atoi(env);
+  const int forced = env_int("GB3_GEMM_PAIR_TILE_N", 0);
   bool forced_valid = false;
   for (int bn : kPairWidths) forced_valid |= (bn == forced);
   for (int bn : kPairWidths) {
     if (forced_valid && bn != forced) continue;
-    const int64_t tiles = mb * ceil_div(N, bn);
-    const double cost =
-        static_cast<double>(ceil_div(tiles, slots)) * static_cast<double>(bn + 32);
+    PairChoice c;
+    c.bn = bn;
+    plan_tail(mb * ceil_div(N, bn), kb, slots, allow_split, &c);
+    double waves = static_cast<double>(c.full / slots);
+    const int64_t left = c.tiles - (c.full / slots) * slots;
+    if (left > 0) waves += c.split > 1 ? 1.0 / c.split + kSplitCharge : 1.0;
+    // Measured on GB300 (8192^3): a wave of 256-wide pair tiles takes 1.057x
+    // the time of 224-wide ones for 1.143x the work, i.e. time ~ width + 320.
+    const double cost = waves * static_cast<double>(bn + kWidthCostOffset);
     if (cost < best_cost) {
       best_cost = cost;
-      best = bn;
-      *tiles_out = tiles;
+      best = c;
     }
   }
   return best;
 }
 
+int64_t pair_workspace_bytes(const PairChoice& c) {
+  if (c.split <= 1) return 0;
+  return (c.tiles - c.full) * c.split * static_cast<int64_t>(kPairBM) * c.bn * 4;
+}
+
 // pair_slots: CTA pairs that fit on the device at once (0: assume sms / 2,
 // negative: pair kernels unavailable).
-int plan_gemm(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pair_slots = 0) {
+int plan_gemm(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pair_slots = 0,
+              bool allow_split = true) {
   std::memset(pl, 0, sizeof(*pl));
   pl->split_k = 1;
   if (M == 0 || N == 0) return GEMM_OK;
@@ -164,17 +220,18 @@ int plan_gemm(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pair_
   }
   if (M >= kPairMinM && pair_slots >= 0) {
     const int slots = pair_slots > 0 ? pair_slots : std::max(1, sms / 2);
-    int64_t tiles = 0;
-    const int bn = choose_pair_width(M, N, slots, &tiles);
+    const PairChoice c = choose_pair(M, N, K, slots, allow_split);
+    const int64_t units = c.full + (c.tiles - c.full) * c.split;
     pl->kernel = K_PAIR;
     pl->tile_m = kPairBM;
-    pl->tile_n = bn;
+    pl->tile_n = c.bn;
     pl->stages = kPairStages;
-    pl->tiles = tiles;
-    pl->grid = 2 * static_cast<int>(std::min<int64_t>(tiles, slots));
-    pl->smem_bytes = pair_smem_for(bn);
+    pl->split_k = c.split;
+    pl->tiles = units;
+    pl->grid = 2 * static_cast<int>(std::min<int64_t>(units, slots));
+    pl->smem_bytes = pair_smem_for(c.bn);
     pl->launches = 1;
-    pl->stage_tx_bytes = 2 * pair_stage_bytes(bn);
+    pl->stage_tx_bytes = 2 * pair_stage_bytes(c.bn);
     return GEMM_OK;
   }
   pl->kernel = K_TILED;
@@ -189,7 +246,8 @@ int plan_gemm(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pair_
   return GEMM_OK;
 }
 
-int plan_gate_up(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pair_slots = 0) {
+int plan_gate_up(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pair_slots = 0,
+                 bool allow_split = true) {
   std::memset(pl, 0, sizeof(*pl));
   pl->split_k = 1;
   if (M == 0 || N == 0) return GEMM_OK;
@@ -202,13 +260,19 @@ int plan_gate_up(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pa
   }
   if (M >= kPairMinM && pair_slots >= 0) {
     const int slots = pair_slots > 0 ? pair_slots : std::max(1, sms / 2);
+    PairChoice c;
+    c.bn = 256;
+    plan_tail(ceil_div(M, kPairBM) * ceil_div(N, CfgPairGU::kOutCols), ceil_div(K, kBK), slots,
+              allow_split, &c);
+    const int64_t units = c.full + (c.tiles - c.full) * c.split;
     pl->kernel = K_PAIR_GATE_UP;
     pl->tile_m = kPairBM;
     pl->tile_n = CfgPairGU::kOutCols;
     pl->tile_k = kBK;
     pl->stages = kPairStages;
-    pl->tiles = ceil_div(M, kPairBM) * ceil_div(N, CfgPairGU::kOutCols);
-    pl->grid = 2 * static_cast<int>(std::min<int64_t>(pl->tiles, slots));
+    pl->split_k = c.split;
+    pl->tiles = units;
+    pl->grid = 2 * static_cast<int>(std::min<int64_t>(units, slots));
     pl->smem_bytes = CfgPairGU::kSmemBytes;
     pl->launches = 1;
     pl->stage_tx_bytes = 2 * CfgPairGU::kStageBytes;
@@ -579,7 +643,56 @@ TileParams tile_params(int64_t M, int64_t N, int64_t K, int tile_m, int tile_n_o
   p.beta = beta;
   p.C = C;
   p.ldc = ldc;
+  p.num_full = p.num_tiles;
+  p.tail_split = 1;
+  p.kb_per_piece = p.k_blocks;
+  p.num_units = p.num_tiles;
+  p.ws = nullptr;
+  p.counters = nullptr;
   return p;
+}
+
+// Work units of a pair plan (whole tiles, then split tail pieces) and the
+// workspace they need.  A plan that needs a workspace the device cannot get
+// (the stream is being captured) is redone without the split.
+int pair_units(int dev, gemm_plan* pl, int64_t M, int64_t N, int64_t K, int bn_out_cols,
+               TileParams* p, cudaStream_t stream, bool gate_up, int slots) {
+  const int64_t tiles = ceil_div(M, kPairBM) * ceil_div(N, bn_out_cols);
+  p->num_tiles = static_cast<int>(tiles);
+  PairChoice c;
+  if (gate_up) {
+    c.bn = 256;
+    plan_tail(tiles, p->k_blocks, slots, true, &c);
+  } else {
+    c = choose_pair(M, N, K, slots, true);
+  }
+  if (c.split > 1) {
+    const size_t ws = static_cast<size_t>(pair_workspace_bytes(c));
+    const size_t counters = static_cast<size_t>(c.tiles - c.full) * 8;
+    int st;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      st = ensure_workspace(dev, ws, counters, stream);
+      if (st == GEMM_OK) {
+        p->ws = g_dev[dev].ws;
+        p->counters = g_dev[dev].counters;
+      }
+    }
+    if (st != GEMM_OK) {
+      // Without a workspace (graph capture): the same tiles, all whole.
+      c.full = c.tiles;
+      c.split = 1;
+      c.kb_per_piece = p->k_blocks;
+      pl->split_k = 1;
+      pl->tiles = c.tiles;
+      pl->grid = 2 * static_cast<int>(std::min<int64_t>(c.tiles, slots));
+    }
+  }
+  p->num_full = static_cast<int>(c.full);
+  p->tail_split = c.split;
+  p->kb_per_piece = c.kb_per_piece;
+  p->num_units = static_cast<int>(c.full + (c.tiles - c.full) * c.split);
+  return GEMM_OK;
 }
 
 template <int BN, int EPI>
@@ -609,9 +722,9 @@ int output_map(CUtensorMap* out, void* C, int64_t M, int64_t N, int64_t ldc, boo
                        CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-int run_pair(const gemm_plan& pl, int dev, int64_t M, int64_t N, int64_t K, float alpha,
-             const void* A, int64_t lda, const void* B, int64_t ldb, float beta, void* C,
-             int64_t ldc, bool bf16, cudaStream_t stream) {
+int run_pair(gemm_plan& pl, int dev, int sms, int slots, int64_t M, int64_t N, int64_t K,
+             float alpha, const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
+             void* C, int64_t ldc, bool bf16, cudaStream_t stream) {
   const int bn = pl.tile_n;
   CUtensorMap tmA, tmB, tmOut;
   int st;
@@ -622,7 +735,8 @@ int run_pair(const gemm_plan& pl, int dev, int64_t M, int64_t N, int64_t K, floa
                           bn / 2)) != GEMM_OK)
     return st;
   if ((st = output_map(&tmOut, C, M, N, ldc, bf16, bn)) != GEMM_OK) return st;
-  const TileParams p = tile_params(M, N, K, kPairBM, bn, alpha, beta, C, ldc, pl.tiles);
+  TileParams p = tile_params(M, N, K, kPairBM, bn, alpha, beta, C, ldc, pl.tiles);
+  pair_units(dev, &pl, M, N, K, bn, &p, stream, false, slots);
   switch (bn) {
     case 256:
       return bf16 ? launch_pair_gemm<256, EPI_BF16>(pl, dev, tmA, tmB, tmB, tmOut, p, stream)
@@ -699,8 +813,9 @@ int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64
   const bool bf16 = out_dtype == GEMM_OUT_BF16;
 
   if (pl.kernel == K_SCALE) return run_scale(pl, C, ldc, M, N, beta, bf16, stream);
-  if (pl.kernel == K_PAIR) return run_pair(pl, dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
-                                           bf16, stream);
+  if (pl.kernel == K_PAIR)
+    return run_pair(pl, dev, sms, slots, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bf16,
+                    stream);
 
   if (pl.kernel == K_SKINNY) {
     CUtensorMap tmW, tmX;
@@ -809,8 +924,9 @@ int gemm_gate_up_silu(int64_t M, int64_t N, int64_t K, const void* X, int64_t ld
                             CfgPairGU::kOutCols)) != GEMM_OK)
       return st;
     if ((st = output_map(&tmY, Y, M, N, ldy, true, CfgPairGU::kOutCols)) != GEMM_OK) return st;
-    const TileParams p = tile_params(M, N, K, kPairBM, CfgPairGU::kOutCols, 1.0f, 0.0f, nullptr,
-                                     ldy, pl.tiles);
+    TileParams p = tile_params(M, N, K, kPairBM, CfgPairGU::kOutCols, 1.0f, 0.0f, nullptr, ldy,
+                               pl.tiles);
+    pair_units(dev, &pl, M, N, K, CfgPairGU::kOutCols, &p, stream, true, slots);
     return launch_pair_gemm<256, EPI_GATE_UP>(pl, dev, tmX, tmWg, tmWu, tmY, p, stream);
   }
 
@@ -855,6 +971,14 @@ int gemm_get_device_status(void* stream, int* site) {
     return GEMM_ERR_CUDA;
   }
   if (site != nullptr) *site = h[1];
+  if (h[0] != GEMM_OK) {
+    // A kernel gave up mid-way: arrival counters of split work may be left
+    // non-zero; clear them so that later calls start from a clean state.
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (d.counters != nullptr && cudaMemset(d.counters, 0, d.counter_count * sizeof(int)) != cudaSuccess)
+      cudaGetLastError();
+  }
   return h[0];
 }
 

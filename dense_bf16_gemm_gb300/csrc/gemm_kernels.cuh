@@ -122,7 +122,51 @@ struct TileParams {
   float alpha, beta;
   const void* C;      // read when beta != 0 (same storage as the output)
   long long ldc;      // elements
+  // Work units: first the pieces of the "tail" tiles num_full .. num_tiles-1,
+  // each cut into tail_split pieces of kb_per_piece k-blocks (the last piece
+  // may be shorter), then tiles 0 .. num_full-1 whole.  The pieces come first
+  // so that their partial-sum epilogues overlap later main loops.
+  // num_units = (num_tiles - num_full) * tail_split + num_full.
+  int num_full;
+  int tail_split;
+  int kb_per_piece;
+  int num_units;
+  float* ws;          // FP32 partial tiles of the tail pieces (tail_split > 1)
+  int* counters;      // arrivals per (tail tile, 32-row band), zero between calls
 };
+
+// Tile, k-block range and piece (-1: whole tile) of work unit u.
+__device__ __forceinline__ void unit_of(int u, const TileParams& p, int& tile, int& kb0, int& kb1,
+                                        int& piece) {
+  const int split_units = (p.num_tiles - p.num_full) * p.tail_split;
+  if (u >= split_units) {
+    tile = u - split_units;
+    kb0 = 0;
+    kb1 = p.k_blocks;
+    piece = -1;
+  } else {
+    tile = p.num_full + u / p.tail_split;
+    piece = u % p.tail_split;
+    kb0 = piece * p.kb_per_piece;
+    kb1 = min(p.k_blocks, kb0 + p.kb_per_piece);
+  }
+}
+
+// Where one warp band (32 rows) of a split tile keeps its partial sums.  The
+// layout is private to the kernel and chosen for coalescing: 32-column slice
+// c of the band is stored as 8 runs of 32 float4, run q holding lane i's
+// q-th float4 at position i, so every warp-wide store or load of a run moves
+// 512 contiguous bytes.  A band's partial is 32 * width floats.
+struct SplitCtx {
+  int pieces;              // 1: the unit is a whole tile
+  int piece;               // this unit's piece
+  const float4* ws0;       // band partial of piece 0
+  long long piece_stride;  // float4s between the partials of consecutive pieces
+};
+
+__device__ __forceinline__ long long split_index(int col, int q, int lane) {
+  return (static_cast<long long>(col >> 5) * 8 + q) * 32 + lane;
+}
 
 // Grouped raster: group_m consecutive row blocks share each column block.
 __device__ __forceinline__ void tile_coords(int tile, const TileParams& p, int& mb, int& nb) {
@@ -202,10 +246,83 @@ __device__ __forceinline__ void load_c_slice(float (&c)[32], const TileParams& p
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + __expf(-g)); }
 
-// Geometry of one epilogue store box: 32 rows (one warp's TMEM band) by kCols
-// output columns.  FP32: 32 columns = 128-byte rows with the 128-byte swizzle.
-// BF16: 64 columns (128-byte rows, 128-byte swizzle) when the tile's output
-// width is a multiple of 64, else 32 columns (64-byte rows, 64-byte swizzle).
+// The raw FP32 accumulator slice (32 columns from `col`) of this lane's row:
+// from TMEM for a whole tile; for the last piece of a split tile, the sum of
+// every piece's partial in piece order 0, 1, ..., with this piece's own
+// partial taken from TMEM (bit-identical to the copy it wrote), so the result
+// does not depend on which piece finished last.
+__device__ __forceinline__ void acc_slice(float (&v)[32], uint32_t tacc, int col, int lane,
+                                          const SplitCtx& sp) {
+  if (sp.pieces <= 1) {
+    tmem_load_32x32b_x32(tacc + col, v);
+    return;
+  }
+  float sum[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) sum[i] = 0.0f;
+  // Pieces are visited two at a time so that the workspace loads of both are
+  // in flight together; the addition order stays 0, 1, 2, ...
+  for (int q0 = 0; q0 < sp.pieces; q0 += 2) {
+    float4 x[2][8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int q = q0 + h;
+      if (q < sp.pieces && q != sp.piece) {
+        const float4* src = sp.ws0 + q * sp.piece_stride;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[h][j] = __ldcg(src + split_index(col, j, lane));
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int q = q0 + h;
+      if (q >= sp.pieces) break;
+      if (q == sp.piece) {
+        tmem_load_32x32b_x32(tacc + col, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sum[i] += v[i];
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          sum[4 * j + 0] += x[h][j].x;
+          sum[4 * j + 1] += x[h][j].y;
+          sum[4 * j + 2] += x[h][j].z;
+          sum[4 * j + 3] += x[h][j].w;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = sum[i];
+}
+
+// Writes this warp band's raw accumulator (acc_cols columns) to its piece's
+// partial in the workspace, then counts the band's arrival.  Returns true on
+// the band's last arrival (the caller then runs the epilogue on the sum).
+__device__ __forceinline__ bool publish_partial(uint32_t tacc, int acc_cols, int lane,
+                                                const SplitCtx& sp, int* counter, int pieces) {
+  float4* dst = const_cast<float4*>(sp.ws0) + sp.piece * sp.piece_stride;
+#pragma unroll 1
+  for (int c = 0; c < acc_cols; c += 32) {
+    float v[32];
+    tmem_load_32x32b_x32(tacc + c, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      __stcg(dst + split_index(c, j, lane), make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+  }
+  __threadfence();
+  __syncwarp();
+  int prev = 0;
+  if (lane == 0) prev = atomicAdd(counter, 1);
+  prev = __shfl_sync(0xffffffffu, prev, 0);
+  const bool last = prev == pieces - 1;
+  if (last) {
+    __threadfence();
+    if (lane == 0) *counter = 0;  // ready for the next call
+  }
+  return last;
+}
+
 template <int EPI, int OUT_COLS>
 struct EpiBox {
   static constexpr int kCols = (EPI == EPI_F32) ? 32 : (OUT_COLS % 64 == 0 ? 64 : 32);
@@ -237,7 +354,8 @@ __device__ __forceinline__ uint32_t staging_offset(int row, uint32_t chunk) {
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtensorMap* tmOut,
                                               uint32_t tacc, int m0, int n0, uint32_t staging,
-                                              int lane, int& sc, bool have_acc) {
+                                              int lane, int& sc, bool have_acc,
+                                              const SplitCtx& split) {
   constexpr int OUT = (EPI == EPI_GATE_UP) ? BN / 2 : BN;
   using Box = EpiBox<EPI, OUT>;
   constexpr int kSub = Box::kCols / 32;  // 32-column slices per box
@@ -260,8 +378,8 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
       if constexpr (EPI == EPI_GATE_UP) {
         float u[32];
         if (have_acc) {
-          tmem_load_32x32b_x32(tacc + c0 + 32 * h, v);
-          tmem_load_32x32b_x32(tacc + OUT + c0 + 32 * h, u);
+          acc_slice(v, tacc, c0 + 32 * h, lane, split);
+          acc_slice(u, tacc, OUT + c0 + 32 * h, lane, split);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = u[i] = 0.0f;
@@ -277,7 +395,7 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
           if (next < OUT) load_c_slice<EPI>(c_next, p, row, n0 + next);
         }
         if (have_acc) {
-          tmem_load_32x32b_x32(tacc + c0 + 32 * h, v);
+          acc_slice(v, tacc, c0 + 32 * h, lane, split);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.0f;
@@ -495,7 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             static_cast<uint32_t>(buf * Cfg::kAccStride);
       const int m0 = mb * kBM + band;
       const int n0 = nb * Cfg::kOutCols;
-      epilogue_tile<BN, EPI>(p, &tmOut, tacc, m0, n0, staging, lane, sc, p.k_blocks > 0);
+      const SplitCtx whole{1, 0, nullptr, 0};
+      epilogue_tile<BN, EPI>(p, &tmOut, tacc, m0, n0, staging, lane, sc, p.k_blocks > 0, whole);
       // The accumulator may be overwritten once every lane's TMEM reads are done.
       tc_fence_before_sync();
       __syncwarp();

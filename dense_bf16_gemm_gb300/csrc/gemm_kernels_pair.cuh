@@ -109,11 +109,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       long long issued = 0;
       bool ok = true;
-      for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters) {
+      for (int u = cluster; ok && u < p.num_units; u += nclusters) {
+        int tile, kb0, kb1, piece;
+        unit_of(u, p, tile, kb0, kb1, piece);
         int mb, nb;
         tile_coords(tile, p, mb, nb);
         const int a_row = mb * kPairBM + static_cast<int>(rank) * 128;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY)) {
             ok = false;
             break;
@@ -152,13 +154,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       int local = 0;
       bool ok = true;
-      for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters, ++local) {
+      for (int u = cluster; ok && u < p.num_units; u += nclusters, ++local) {
+        int tile, kb0, kb1, piece;
+        unit_of(u, p, tile, kb0, kb1, piece);
         const int buf = local & 1;
         const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
         if (!wait_bounded_cluster(acce_bar(buf), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bounded(full_bar(s), ph, abort_flag, SITE_MMA_FULL)) {
             ok = false;
             break;
@@ -170,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < kBK / kUmmaK; ++j)
             umma_bf16_pair(d_tmem, adesc + 2u * j, bdesc + 2u * j, Cfg::kIdesc,
-                           (kb | j) != 0 ? 1u : 0u);
+                           (kb != kb0 || j != 0) ? 1u : 0u);
           umma_commit_pair_multicast(empty_bar(s), 0x3);
           if (++s == STAGES) {
             s = 0;
@@ -189,23 +193,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int band = (warp & 3) * 32;
     const uint32_t staging = sbase + Cfg::kRingBytes + ew * kStagingPerWarp * kStageBox;
     const uint32_t acce0_even = mapa_shared(acce_bar(0), 0);
+    const int band_id = static_cast<int>(rank) * 4 + (warp & 3);  // 32-row band of the pair tile
     int local = 0;
     int sc = 0;
-    if (lane == 0 && cluster < p.num_tiles) {
-      int mb_, nb_;
-      tile_coords(cluster, p, mb_, nb_);
-      prefetch_c_band<BN, EPI>(p, &tmOut, mb_ * kPairBM + static_cast<int>(rank) * 128 + band, nb_ * Cfg::kOutCols);
-    }
-    for (int tile = cluster; tile < p.num_tiles; tile += nclusters, ++local) {
+    auto prefetch_unit = [&](int u) {
+      if (u < p.num_units) {
+        int tile_, kb0_, kb1_, piece_, mb_, nb_;
+        unit_of(u, p, tile_, kb0_, kb1_, piece_);
+        tile_coords(tile_, p, mb_, nb_);
+        prefetch_c_band<BN, EPI>(p, &tmOut, mb_ * kPairBM + static_cast<int>(rank) * 128 + band,
+                                 nb_ * Cfg::kOutCols);
+      }
+    };
+    if (lane == 0) prefetch_unit(cluster);
+    for (int u = cluster; u < p.num_units; u += nclusters, ++local) {
+      int tile, kb0, kb1, piece;
+      unit_of(u, p, tile, kb0, kb1, piece);
       int mb, nb;
       tile_coords(tile, p, mb, nb);
-      // C of the next tile of this CTA travels to L2 during this tile's
-      // epilogue and the next tile's main loop.
-      if (lane == 0 && tile + nclusters < p.num_tiles) {
-        int mb_, nb_;
-        tile_coords(tile + nclusters, p, mb_, nb_);
-        prefetch_c_band<BN, EPI>(p, &tmOut, mb_ * kPairBM + static_cast<int>(rank) * 128 + band, nb_ * Cfg::kOutCols);
-      }
+      // C of this CTA's next unit travels to L2 during this unit's epilogue
+      // and the next unit's main loop.
+      if (lane == 0) prefetch_unit(u + nclusters);
       const int buf = local & 1;
       const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
       const bool got = wait_bounded(accf_bar(buf), aph, abort_flag, SITE_EPI_ACC_FULL);
@@ -215,7 +223,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                             static_cast<uint32_t>(buf * Cfg::kAccStride);
       const int m0 = mb * kPairBM + static_cast<int>(rank) * 128 + band;
       const int n0 = nb * Cfg::kOutCols;
-      epilogue_tile<BN, EPI>(p, &tmOut, tacc, m0, n0, staging, lane, sc, p.k_blocks > 0);
+      SplitCtx split{1, 0, nullptr, 0};
+      bool store = true;
+      if (piece >= 0) {
+        // One K piece of a tail tile: publish the partial; the band's last
+        // piece adds them all up and writes C.  Workspace: [tail tile][piece]
+        // [band 0..7][32 x BN floats].
+        const int tail = tile - p.num_full;
+        const long long band_f4 = 32LL * BN / 4;
+        split.pieces = p.tail_split;
+        split.piece = piece;
+        split.piece_stride = 8 * band_f4;
+        split.ws0 = reinterpret_cast<const float4*>(p.ws) +
+                    static_cast<long long>(tail) * p.tail_split * split.piece_stride +
+                    band_id * band_f4;
+        store = publish_partial(tacc, BN, lane, split, p.counters + tail * 8 + band_id,
+                                p.tail_split);
+      }
+      if (store) epilogue_tile<BN, EPI>(p, &tmOut, tacc, m0, n0, staging, lane, sc, kb1 > kb0, split);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acce0_even + 8u * buf);

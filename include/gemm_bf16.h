@@ -74,12 +74,15 @@ enum gemm_out_dtype {
  *            alpha*acc + beta*c.
  * stream     cudaStream_t the work is enqueued on.
  *
- * For M <= 16 the call uses a split-K path whose FP32 partial sums live in a
- * per-device workspace the library allocates on first use (a call made
- * while `stream` is being captured into a CUDA graph cannot allocate, so
- * make one such call, or gemm_prepare(), before capturing).  Calls of that
- * path that run concurrently on different streams share the workspace and
- * must not overlap on the GPU.
+ * Split K: for M <= 16, and for the tiles of a last, partial wave of the
+ * CTA-pair kernel, K is cut into pieces whose FP32 partial sums live in a
+ * per-device workspace the library allocates on first use; the last piece
+ * of each tile adds them in a fixed order, so results do not depend on
+ * timing.  A call made while `stream` is being captured into a CUDA graph
+ * cannot allocate: the M <= 16 path then returns GEMM_ERR_CUDA (make one such
+ * call, or gemm_prepare(), before capturing) and the tiled path runs its
+ * tiles whole.  Calls that use the workspace and run concurrently on
+ * different streams share it and must not overlap on the GPU.
  */
 GEMM_API int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha,
               const void *A, int64_t lda,

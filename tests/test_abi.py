@@ -98,42 +98,84 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
     assert st in (_native.GEMM_ERR_CUDA, _native.GEMM_ERR_UNSUPPORTED)
 
 
+def pair_model(M, N, K, slots=76, widths=(256, 224)):
+    """Restatement of the planner's rule: fewest waves (a split tail wave counts
+    1/split + 0.1) weighted by width + 320."""
+    best = None
+    kb = -(-K // 64)
+    for bn in widths:
+        tiles = -(-M // 256) * -(-N // bn)
+        full, tail = tiles - tiles % slots, tiles % slots
+        split = 1
+        if tail:
+            s_ = min(2, slots // tail, kb // 24)
+            if s_ >= 2:
+                kbp = -(-kb // s_)
+                split = -(-kb // kbp)
+        if split == 1:
+            full = tiles
+        waves = full // slots + ((1 / split + 0.1) if split > 1 else (1 if tiles - full // slots * slots else 0))
+        cost = waves * (bn + 320)
+        if best is None or cost < best[0]:
+            best = (cost, bn, split, full + (tiles - full) * split)
+    return best[1:]
+
+
 def test_plan_pair_4096(lib):
     st, p = _native.gemm_bf16_plan(4096, 4096, 4096, _native.GEMM_OUT_BF16, 152)
     assert st == 0
     d = p.as_dict()
     assert d["kernel_name"] == "pair"
     assert d["tile_m"] == 256 and d["tile_k"] == 64 and d["stages"] == 6
-    # width 224 makes 16 x 19 = 304 pair tiles: exactly 4 waves of 76 pairs
-    assert d["tile_n"] == 224
-    assert d["tiles"] == 16 * 19
+    # 16 x 16 = 256 pair tiles on 76 pairs: 3 whole waves, and the 28 tiles of
+    # the last wave each cut into 2 K pieces (56 units) so that wave is half long
+    assert d["tile_n"] == 256 and d["split_k"] == 2
+    assert d["tiles"] == 228 + 28 * 2
     assert d["grid"] == 152
     assert d["launches"] == 1
     # per stage each CTA receives a 128x64 A box (16384 bytes, the pages'
     # transfer size of a 128x64 BF16 tile) and half the B rows
-    assert d["stage_tx_bytes"] == 2 * (16384 + 112 * 64 * 2)
+    assert d["stage_tx_bytes"] == 2 * (16384 + 128 * 64 * 2)
     assert d["smem_bytes"] <= 232448
 
 
-def test_plan_pair_width_minimises_waves(lib):
-    for (M, N), want in {(4096, 14336): 256, (3000, 5000): 224, (8192, 8192): 256}.items():
-        st, p = _native.gemm_bf16_plan(M, N, 4096, _native.GEMM_OUT_F32, 152)
-        d = p.as_dict()
-        assert st == 0 and d["kernel_name"] == "pair"
-        costs = {}
-        for bn in (256, 224):
-            tiles = -(-M // 256) * -(-N // bn)
-            costs[bn] = -(-tiles // 76) * (bn + 32)
-        assert d["tile_n"] == min(costs, key=costs.get) == want
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (4096, 14336, 4096), (3000, 5000, 2000),
+                                   (8192, 8192, 8192), (512, 1000, 1000), (1000, 712, 136)])
+def test_plan_pair_matches_wave_model(lib, M, N, K):
+    st, p = _native.gemm_bf16_plan(M, N, K, _native.GEMM_OUT_F32, 152)
+    d = p.as_dict()
+    assert st == 0 and d["kernel_name"] == "pair"
+    bn, split, units = pair_model(M, N, K)
+    assert (d["tile_n"], d["split_k"], d["tiles"]) == (bn, split, units)
+
+
+def test_plan_tail_split_pieces_are_long_enough(lib):
+    # K = 2048 is 32 k-blocks: two pieces would be shorter than 24 k-blocks
+    st, p = _native.gemm_bf16_plan(4096, 4096, 2048, _native.GEMM_OUT_BF16, 152)
+    assert st == 0 and p.split_k == 1
+    st, p = _native.gemm_bf16_plan(4096, 4096, 3072, _native.GEMM_OUT_BF16, 152)
+    assert st == 0 and p.split_k == 2
 
 
 def test_plan_forced_pair_width(lib, monkeypatch):
-    monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", "256")
+    monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", "224")
     st, p = _native.gemm_bf16_plan(4096, 4096, 4096, _native.GEMM_OUT_BF16, 152)
-    assert st == 0 and p.tile_n == 256 and p.tiles == 16 * 16
+    assert st == 0 and p.tile_n == 224 and p.tiles == 16 * 19 and p.split_k == 1
     monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", "100")   # not compiled: ignored
     st, p = _native.gemm_bf16_plan(4096, 4096, 4096, _native.GEMM_OUT_BF16, 152)
-    assert st == 0 and p.tile_n == 224
+    assert st == 0 and p.tile_n == 256
+
+
+def test_plan_split_overrides(lib, monkeypatch):
+    monkeypatch.setenv("GB3_GEMM_TAIL_SPLIT", "0")
+    st, p = _native.gemm_bf16_plan(4096, 4096, 4096, _native.GEMM_OUT_BF16, 152)
+    assert st == 0 and p.split_k == 1
+    monkeypatch.delenv("GB3_GEMM_TAIL_SPLIT")
+    monkeypatch.setenv("GB3_GEMM_SPLIT_ALL", "3")
+    st, p = _native.gemm_bf16_plan(512, 1024, 1024, _native.GEMM_OUT_BF16, 152)
+    assert st == 0 and p.split_k == 3
+    tiles = 2 * -(-1024 // p.tile_n)
+    assert p.tiles == tiles * 3
 
 
 def test_plan_single_cta_below_two_row_blocks(lib):
@@ -149,7 +191,10 @@ def test_plan_ragged_tiles_cover_the_output(lib):
     st, p = _native.gemm_bf16_plan(3000, 5000, 2000, _native.GEMM_OUT_F32, 152)
     assert st == 0
     d = p.as_dict()
-    assert d["tiles"] == -(-3000 // d["tile_m"]) * -(-5000 // d["tile_n"])
+    tiles = -(-3000 // d["tile_m"]) * -(-5000 // d["tile_n"])
+    # units: whole tiles plus split pieces of the tail tiles; every tile is covered
+    whole = tiles - (tiles % 76 if d["split_k"] > 1 else 0)
+    assert d["tiles"] == whole + (tiles - whole) * d["split_k"]
 
 
 def test_plan_skinny_split_k(lib):

@@ -382,3 +382,49 @@ def test_pair_widths_bit_exact(g, monkeypatch, width, M, N, K, out_dtype):
     else:
         assert np.array_equal(bits(out.cpu()), oracle.round_to_bf16_bits(ref))
     assert_status_ok(g)
+
+
+@pytest.mark.parametrize("pieces", ["2", "3", "5"])
+@pytest.mark.parametrize("M,N,K", [(512, 1000, 1000), (300, 520, 704), (1000, 712, 2048)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_split_k_pieces_bit_exact(g, monkeypatch, pieces, M, N, K, out_dtype):
+    """Every pair tile cut into K pieces whose partials are summed by the last
+    piece; integer inputs keep every partial exact."""
+    monkeypatch.setenv("GB3_GEMM_SPLIT_ALL", pieces)
+    p = g.plan(M, N, K, out_dtype)
+    kb = -(-K // 64)
+    kbp = -(-kb // min(int(pieces), kb))
+    assert p["kernel_name"] == "pair" and p["split_k"] == -(-kb // kbp)   # pieces that get work
+    A, B, C = int_inputs(M, N, K, seed=M + N + 7 * K)
+    Cq = C.to(out_dtype)
+    ref, _ = oracle.gemm_full(A, B, alpha=2.0, beta=-0.5, C=Cq.to(torch.float32))
+    out = run_gemm(g, A, B, C=Cq, alpha=2.0, beta=-0.5, out_dtype=out_dtype)
+    if out_dtype == torch.float32:
+        assert np.array_equal(to_f64(out), ref)
+    else:
+        assert np.array_equal(bits(out.cpu()), oracle.round_to_bf16_bits(ref))
+    assert_status_ok(g)
+
+
+def test_split_k_is_deterministic_and_within_tolerance(g, monkeypatch):
+    monkeypatch.setenv("GB3_GEMM_SPLIT_ALL", "4")
+    M, N, K = 768, 1024, 4096
+    A, B, _ = workloads.gemm_inputs(M, N, K, 51, ("normal", 1.0), ("normal", 1.0))
+    Ad, Bd = A.cuda(), B.cuda()
+    outs = []
+    for _ in range(3):
+        C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        g.gemm(Ad, Bd, C)
+        outs.append(C)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    ref, ab = oracle.gemm_full(A, B)
+    assert_within(to_f64(outs[0]), ref, oracle.gemm_tolerance(ref, ab, 1.0, 0.0), "split 4")
+    assert_status_ok(g)
+
+
+@pytest.mark.parametrize("pieces", ["2", "3"])
+def test_gate_up_split_k(g, monkeypatch, pieces):
+    monkeypatch.setenv("GB3_GEMM_SPLIT_ALL", pieces)
+    assert g.gate_up_plan(512, 640, 1024)["split_k"] == int(pieces)
+    check_gate_up(g, 512, 640, 1024, seed=52, dist_w=("normal", 1.0 / 32))
