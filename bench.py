@@ -40,7 +40,10 @@ FLUSH_BYTES = 256 << 20
 
 # DRAM traffic per launch from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`
 # (summarised under profiles/), valid only for the kernel sources it was taken with.
-NCU_TRAFFIC: dict = {}
+NCU_TRAFFIC: dict = {
+    # profiles/gemm_pair_bf16_4096.md: 75.04 MB read + 29.95 MB written per launch
+    "gemm_4096_bf16": {"bytes": 104986880, "src_sha": "f94514fd18d78c37"},
+}
 
 
 def kernel_source_hash() -> str:
@@ -316,6 +319,8 @@ def cpu_baseline(w, target_s=12.0):
             Cs = C[:rows] if C is not None else None
             oracle.gemm_full(A[:rows], B, alpha=w.alpha, beta=w.beta, C=Cs)
     rows = 1
+    run(rows)                       # threads up, pages touched
+    rows = min(w.M, 32)
     t0 = time.perf_counter()
     run(rows)
     dt = time.perf_counter() - t0
