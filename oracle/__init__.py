@@ -18,6 +18,9 @@ Contents
   WGMMA", sections "TMA and Hopper WGMMA" and "Worked consumers and current
   validation", which name the fused gate/up projection; it is read as the
   SwiGLU form with no bias and no scaling).
+* FP16 operands (``in_f16``) are decoded exactly as IEEE binary16; FP16
+  outputs are rounded with ``round_to_f16_bits`` ("TMEM tiles and transfers",
+  section "Representation and windows": pack(Float16, f)).
 * ``bf16_bits_to_f64`` / ``round_to_bf16_bits``: exact BF16 widening and
   round-to-nearest-even narrowing ("TMEM tiles and transfers", section
   "Representation and windows": ``pack(BFloat16, f)`` converts FP32 values to
@@ -76,11 +79,13 @@ def _load():
             lib.oracle_gemm_entries.restype = None
             lib.oracle_gemm_entries.argtypes = [
                 _i64, _dbl, _vp, _i64, _vp, _i64, _dbl, _vp, _i64,
-                _i64, _vp, _vp, _vp, _vp]
+                _i64, _vp, _vp, _vp, _vp, ctypes.c_int]
             lib.oracle_gemm_full.restype = None
             lib.oracle_gemm_full.argtypes = [
                 _i64, _i64, _i64, _dbl, _vp, _i64, _vp, _i64, _dbl, _vp, _i64,
-                _vp, _vp]
+                _vp, _vp, ctypes.c_int]
+            lib.oracle_decode16.restype = _dbl
+            lib.oracle_decode16.argtypes = [ctypes.c_uint16, ctypes.c_int]
             lib.oracle_gate_up_entries.restype = None
             lib.oracle_gate_up_entries.argtypes = [
                 _i64, _vp, _i64, _vp, _vp, _i64,
@@ -99,15 +104,33 @@ def _ptr(a: np.ndarray | None):
 
 
 def _as_bits(x) -> np.ndarray:
-    """Accept a uint16 array of BF16 bit patterns or a torch bfloat16 tensor."""
+    """Accept a uint16 array of 16-bit patterns or a torch bfloat16/float16 tensor."""
     if isinstance(x, np.ndarray):
         if x.dtype != np.uint16:
-            raise TypeError("BF16 operands are passed as uint16 bit patterns")
+            raise TypeError("16-bit operands are passed as uint16 bit patterns")
         return np.ascontiguousarray(x)
     import torch  # only for accepting CPU tensors from the input generator
-    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16:
-        raise TypeError("expected a bfloat16 tensor or uint16 bits")
+    if not isinstance(x, torch.Tensor) or x.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("expected a bfloat16/float16 tensor or uint16 bits")
     return np.ascontiguousarray(x.contiguous().view(torch.int16).numpy()).view(np.uint16)
+
+
+def _is_f16(*xs) -> int:
+    """1 when the operands are float16 tensors (uint16 bits are BF16 unless
+    in_f16 is given explicitly)."""
+    try:
+        import torch
+    except ImportError:  # pragma: no cover
+        return 0
+    kinds = {x.dtype for x in xs if isinstance(x, torch.Tensor)}
+    if len(kinds) > 1:
+        raise TypeError("operands must share one type")
+    return 1 if kinds == {torch.float16} else 0
+
+
+def decode16(bits: int, in_f16: bool) -> float:
+    """Exact value of a BF16 (in_f16 False) or FP16 bit pattern, from the C oracle."""
+    return float(_load().oracle_decode16(int(bits) & 0xFFFF, int(bool(in_f16))))
 
 
 def _as_f32(x) -> np.ndarray | None:
@@ -121,13 +144,14 @@ def _as_f32(x) -> np.ndarray | None:
 # --------------------------------------------------------------------------
 # GEMM
 # --------------------------------------------------------------------------
-def gemm_full(A, B, alpha=1.0, beta=0.0, C=None, want_abs=True):
+def gemm_full(A, B, alpha=1.0, beta=0.0, C=None, want_abs=True, in_f16=None):
     """Every entry of ``alpha * A.B + beta * C``.
 
     ``A`` is (M, K) K-contiguous, ``B`` is stored (N, K) K-contiguous, ``C`` is
     (M, N) float32 (read only when ``beta != 0``).  Returns ``(value, abs_sum)``
     as float64 (M, N) arrays, ``abs_sum[m, n] = sum_k |a(m,k) b(k,n)|``.
     """
+    f16 = _is_f16(A, B) if in_f16 is None else int(bool(in_f16))
     a, b = _as_bits(A), _as_bits(B)
     M, K = a.shape
     N, K2 = b.shape
@@ -139,15 +163,16 @@ def gemm_full(A, B, alpha=1.0, beta=0.0, C=None, want_abs=True):
     out = np.empty((M, N), np.float64)
     ab = np.empty((M, N), np.float64) if want_abs else None
     _load().oracle_gemm_full(M, N, K, float(alpha), _ptr(a), K, _ptr(b), K,
-                             float(beta), _ptr(c), N, _ptr(out), _ptr(ab))
+                             float(beta), _ptr(c), N, _ptr(out), _ptr(ab), f16)
     return out, ab
 
 
-def gemm_entries(A, B, rows, cols, alpha=1.0, beta=0.0, C=None):
+def gemm_entries(A, B, rows, cols, alpha=1.0, beta=0.0, C=None, in_f16=None):
     """Entries ``(rows[i], cols[i])`` of ``alpha * A.B + beta * C``.
 
     Same storage as :func:`gemm_full`; returns ``(value, abs_sum)`` 1-D arrays.
     """
+    f16 = _is_f16(A, B) if in_f16 is None else int(bool(in_f16))
     a, b = _as_bits(A), _as_bits(B)
     M, K = a.shape
     N, K2 = b.shape
@@ -164,7 +189,7 @@ def gemm_entries(A, B, rows, cols, alpha=1.0, beta=0.0, C=None):
     ab = np.empty(r.size, np.float64)
     _load().oracle_gemm_entries(K, float(alpha), _ptr(a), K, _ptr(b), K,
                                 float(beta), _ptr(cm), N, r.size, _ptr(r),
-                                _ptr(c_), _ptr(out), _ptr(ab))
+                                _ptr(c_), _ptr(out), _ptr(ab), f16)
     return out, ab
 
 
@@ -240,11 +265,33 @@ def round_to_bf16_bits(x) -> np.ndarray:
     return out.astype(np.uint16)
 
 
+def f16_bits_to_f64(bits) -> np.ndarray:
+    """Exact value of IEEE binary16 bit patterns (numpy's float16)."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def round_to_f16_bits(x) -> np.ndarray:
+    """Round float64 values to the nearest IEEE binary16, ties to even
+    (numpy's float64 -> float16 conversion, pinned in the tests)."""
+    with np.errstate(over="ignore", invalid="ignore"):
+        return np.asarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def f16_half_ulp(mag) -> np.ndarray:
+    """Half the binary16 spacing at magnitude ``mag``: ``2**(floor(log2 mag) - 11)``,
+    never below half the subnormal spacing (``2**-25``)."""
+    m = np.abs(np.asarray(mag, dtype=np.float64))
+    _, e = np.frexp(m)
+    e = np.where(m == 0.0, -1000, e)   # zero: only the subnormal floor applies
+    return np.maximum(np.ldexp(1.0, e - 1 - 11), np.ldexp(1.0, -25))
+
+
 def bf16_half_ulp(mag) -> np.ndarray:
     """Half the BF16 spacing at magnitude ``mag``: ``2**(floor(log2 mag) - 8)``,
     never below half the subnormal spacing (``2**-134``)."""
     m = np.abs(np.asarray(mag, dtype=np.float64))
     _, e = np.frexp(m)
+    e = np.where(m == 0.0, -1000, e)   # zero: only the subnormal floor applies
     return np.maximum(np.ldexp(1.0, e - 1 - 8), np.ldexp(1.0, -134))
 
 
@@ -255,14 +302,16 @@ REL_ACC = 4e-3      # admissible FP32-accumulation error per unit of sum |a b|
 SILU_LIPSCHITZ = 1.1  # max |silu'(t)| = 1.0998... (at t ~ 2.3994)
 
 
-def gemm_tolerance(ref, abs_sum, alpha, beta, c=None, out_bf16=False):
-    """``4e-3 * (|alpha| sum|ab| + |beta| |c|)`` plus, for a BF16 output, the
-    half-ulp of BF16 at the largest magnitude the FP32 result can take."""
+def gemm_tolerance(ref, abs_sum, alpha, beta, c=None, out_bf16=False, out_f16=False):
+    """``4e-3 * (|alpha| sum|ab| + |beta| |c|)`` plus, for a 16-bit output, the
+    half-ulp of that format at the largest magnitude the FP32 result can take."""
     tol = REL_ACC * abs(alpha) * np.asarray(abs_sum, np.float64)
     if beta != 0.0 and c is not None:
         tol = tol + REL_ACC * abs(beta) * np.abs(np.asarray(c, np.float64))
     if out_bf16:
         tol = tol + bf16_half_ulp(np.abs(ref) + tol)
+    if out_f16:
+        tol = tol + f16_half_ulp(np.abs(ref) + tol)
     return tol
 
 

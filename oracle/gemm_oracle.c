@@ -24,7 +24,11 @@
  *          projection without defining it; it is read as the SwiGLU form
  *          above, with no bias and no scaling.)
  *
- * Precision: every BF16 input is widened exactly to double and every sum is
+ * Operands are BF16 or, for the FP16 variant, IEEE binary16 ("TMEM tiles and
+ * transfers", section "Representation and windows": FP16 values packed with
+ * pack(Float16, f)); the GEMM functions take the operand type as in_f16.
+ *
+ * Precision: every 16-bit input is widened exactly to double and every sum is
  * one running double accumulator over k = 0 .. K-1 in order.  Beside each
  * result the oracle also returns sum_k |a(m,k) b(k,n)|, which the tests use
  * to scale the rounding tolerance of the FP32-accumulating GPU path.
@@ -49,17 +53,49 @@ static double bf16_to_double(uint16_t bits)
     return (double)f;
 }
 
-static void dot_bf16(int64_t K, const uint16_t *x, const uint16_t *y,
-                     double *sum, double *abs_sum)
+/* IEEE binary16: sign, 5 exponent bits (bias 15), 10 fraction bits. */
+static double f16_to_double(uint16_t bits)
+{
+    int sign = bits >> 15, e = (bits >> 10) & 0x1F, m = bits & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);                 /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);     /* (1 + m/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* Operand element decoding: in_f16 = 0 for BF16, 1 for FP16. */
+static double to_double(uint16_t bits, int in_f16)
+{
+    return in_f16 ? f16_to_double(bits) : bf16_to_double(bits);
+}
+
+static void dot_16(int64_t K, const uint16_t *x, const uint16_t *y, int in_f16,
+                   double *sum, double *abs_sum)
 {
     double s = 0.0, a = 0.0;
     for (int64_t k = 0; k < K; ++k) {
-        double p = bf16_to_double(x[k]) * bf16_to_double(y[k]);
+        double p = to_double(x[k], in_f16) * to_double(y[k], in_f16);
         s += p;
         a += fabs(p);
     }
     *sum = s;
     *abs_sum = a;
+}
+
+static void dot_bf16(int64_t K, const uint16_t *x, const uint16_t *y,
+                     double *sum, double *abs_sum)
+{
+    dot_16(K, x, y, 0, sum, abs_sum);
+}
+
+/* Exact value of one 16-bit pattern (for pinning the decoders). */
+double oracle_decode16(uint16_t bits, int in_f16)
+{
+    return to_double(bits, in_f16);
 }
 
 int oracle_num_threads(void)
@@ -82,13 +118,13 @@ void oracle_gemm_entries(int64_t K, double alpha,
                          const uint16_t *B, int64_t ldb,
                          double beta, const float *C, int64_t ldc,
                          int64_t count, const int64_t *rows, const int64_t *cols,
-                         double *out, double *abs_out)
+                         double *out, double *abs_out, int in_f16)
 {
 #pragma omp parallel for schedule(dynamic, 64)
     for (int64_t i = 0; i < count; ++i) {
         int64_t m = rows[i], n = cols[i];
         double s, a;
-        dot_bf16(K, A + m * lda, B + n * ldb, &s, &a);
+        dot_16(K, A + m * lda, B + n * ldb, in_f16, &s, &a);
         double v = alpha * s;
         if (beta != 0.0)
             v += beta * (double)C[m * ldc + n];
@@ -106,13 +142,13 @@ void oracle_gemm_full(int64_t M, int64_t N, int64_t K, double alpha,
                       const uint16_t *A, int64_t lda,
                       const uint16_t *B, int64_t ldb,
                       double beta, const float *C, int64_t ldc,
-                      double *out, double *abs_out)
+                      double *out, double *abs_out, int in_f16)
 {
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t m = 0; m < M; ++m) {
         for (int64_t n = 0; n < N; ++n) {
             double s, a;
-            dot_bf16(K, A + m * lda, B + n * ldb, &s, &a);
+            dot_16(K, A + m * lda, B + n * ldb, in_f16, &s, &a);
             double v = alpha * s;
             if (beta != 0.0)
                 v += beta * (double)C[m * ldc + n];

@@ -256,6 +256,7 @@ def test_half_ulp_bounds_rounding_error():
     assert oracle.bf16_half_ulp(1.99) == 2.0**-8
     assert oracle.bf16_half_ulp(2.0) == 2.0**-7
     assert oracle.bf16_half_ulp(0.75) == 2.0**-9
+    assert oracle.bf16_half_ulp(0.0) == 2.0**-134
     rng = np.random.default_rng(6)
     x = rng.standard_normal(200000) * np.exp2(rng.integers(-30, 30, 200000))
     err = np.abs(oracle.bf16_bits_to_f64(oracle.round_to_bf16_bits(x)) - x)
@@ -270,3 +271,65 @@ def test_tolerance_flags_a_planted_error():
     bad = v.copy()
     bad[3, 4] += 2.0 * tol[3, 4]
     assert np.sum(np.abs(bad - v) > tol) == 1
+
+
+# ---------------------------------------------------------------------------
+# FP16 operands and outputs
+# ---------------------------------------------------------------------------
+def py_f16(b: int) -> float:
+    """binary16 bits -> float via struct's 'e' format (independent of numpy)."""
+    return struct.unpack("<e", struct.pack("<H", int(b) & 0xFFFF))[0]
+
+
+def test_decode16_every_pattern():
+    pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    f16_np = pats.view(np.float16).astype(np.float64)
+    bf16_t = torch.from_numpy(pats.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    for i in range(0, 1 << 16, 7):            # a seventh of them through ctypes
+        a, b = oracle.decode16(i, True), oracle.decode16(i, False)
+        assert (a == f16_np[i]) or (math.isnan(a) and math.isnan(f16_np[i]))
+        assert (b == bf16_t[i]) or (math.isnan(b) and math.isnan(bf16_t[i]))
+        if not math.isnan(a):
+            assert a == py_f16(i)
+
+
+def test_round_to_f16_matches_struct_half_rounding():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal(20000) * np.exp2(rng.integers(-26, 16, 20000))
+    # exact ties between neighbours, including subnormals, must go to even
+    ties = np.array([1 + 2.0**-11, 1 + 3 * 2.0**-11, 2.0**-24 * 1.5, 2.0**-24 * 2.5,
+                     65504 + 16, 65520.0, -65520.0, 2.0**-25, 3 * 2.0**-26])
+    for v in np.concatenate([x, ties]):
+        try:
+            want = struct.unpack("<H", struct.pack("<e", float(v)))[0]
+        except OverflowError:            # struct refuses values that round to inf
+            want = 0x7C00 if v > 0 else 0xFC00
+        assert oracle.round_to_f16_bits(v) == want, v
+
+
+def test_f16_half_ulp_bounds_rounding_error():
+    assert oracle.f16_half_ulp(1.0) == 2.0**-11
+    assert oracle.f16_half_ulp(1024.0) == 0.5
+    assert oracle.f16_half_ulp(0.0) == 2.0**-25
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal(100000) * np.exp2(rng.integers(-20, 14, 100000))
+    err = np.abs(oracle.f16_bits_to_f64(oracle.round_to_f16_bits(x)) - x)
+    assert np.all(err <= oracle.f16_half_ulp(x))
+
+
+def test_f16_operands_match_bruteforce_and_numpy():
+    g = torch.Generator().manual_seed(9)
+    A = (torch.rand(7, 19, generator=g) * 4 - 2).to(torch.float16)
+    B = (torch.rand(5, 19, generator=g) * 4 - 2).to(torch.float16)
+    v, ab = oracle.gemm_full(A, B)
+    a = A.view(torch.int16).numpy().view(np.uint16)
+    b = B.view(torch.int16).numpy().view(np.uint16)
+    brute = np.array([[sum(py_f16(a[m, k]) * py_f16(b[n, k]) for k in range(19))
+                       for n in range(5)] for m in range(7)])
+    assert np.allclose(v, brute, rtol=1e-14, atol=1e-14)
+    assert np.allclose(v, A.double().numpy() @ B.double().numpy().T, rtol=1e-13, atol=1e-13)
+    # the same bits read as BF16 give a different product: the flag is honoured
+    vb, _ = oracle.gemm_full(a, b)
+    assert not np.allclose(vb, v)
+    ve, _ = oracle.gemm_entries(A, B, [0, 6], [4, 0])
+    assert np.array_equal(ve, v[[0, 6], [4, 0]])
