@@ -4,7 +4,8 @@ The computation runs in the CUDA library declared by ``include/gemm_bf16.h``
 (tcgen05 tensor cores, TMA, Tensor Memory).  This module only marshals torch
 tensors into that C ABI: PyTorch supplies device memory and streams.
 
-    C = alpha * A @ B + beta * C       gemm(A, B, C, alpha, beta)
+    C = alpha * A @ B + beta * C       gemm(A, B, C, alpha, beta)   (2-D or batched 3-D,
+                                                                     BF16 or FP16 operands)
     Y = silu(X @ Wg) * (X @ Wu)        gate_up_silu(X, Wg, Wu)
 
 Operands are K-contiguous: ``A`` is (M, K) and ``B`` is passed as its (N, K)
@@ -16,13 +17,15 @@ import torch
 
 from . import _native
 from ._native import (GEMM_ERR_ALIGNMENT, GEMM_ERR_CUDA, GEMM_ERR_INVALID_ARG,  # noqa: F401
-                      GEMM_ERR_TIMEOUT, GEMM_ERR_UNSUPPORTED, GEMM_OK, GEMM_OUT_BF16,
-                      GEMM_OUT_F32, GemmError)
+                      GEMM_ERR_TIMEOUT, GEMM_ERR_UNSUPPORTED, GEMM_IN_BF16, GEMM_IN_F16,
+                      GEMM_OK, GEMM_OUT_BF16, GEMM_OUT_F16, GEMM_OUT_F32, GemmError)
 
-__all__ = ["gemm", "gate_up_silu", "device_status", "plan", "gate_up_plan", "prepare",
-           "GemmError", "library_path"]
+__all__ = ["gemm", "gate_up_silu", "device_status", "plan", "batched_plan", "gate_up_plan",
+           "prepare", "GemmError", "library_path"]
 
-_OUT_CODES = {torch.float32: GEMM_OUT_F32, torch.bfloat16: GEMM_OUT_BF16}
+_OUT_CODES = {torch.float32: GEMM_OUT_F32, torch.bfloat16: GEMM_OUT_BF16,
+              torch.float16: GEMM_OUT_F16}
+_IN_CODES = {torch.bfloat16: GEMM_IN_BF16, torch.float16: GEMM_IN_F16}
 
 
 def library_path() -> str:
@@ -35,19 +38,24 @@ def _stream(stream, device) -> int:
     return int(stream.cuda_stream)
 
 
-def _check_operand(name, t, dtype=torch.bfloat16):
+def _check_operand(name, t, dtypes=(torch.bfloat16,), dims=(2,)):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
-    if t.dtype != dtype:
-        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if t.dim() != 2 or (t.numel() > 0 and t.stride(1) != 1):
-        raise ValueError(f"{name} must be 2-D with a contiguous last dimension")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must be one of {dtypes}, got {t.dtype}")
+    if t.dim() not in dims or (t.numel() > 0 and t.stride(-1) != 1):
+        raise ValueError(f"{name} must be {dims}-D with a contiguous last dimension")
 
 
 def _ld(t) -> int:
-    return max(t.stride(0), t.shape[1]) if t.numel() > 0 else t.shape[1]
+    """Row pitch in elements of a (.., rows, cols) tensor."""
+    return max(t.stride(-2), t.shape[-1]) if t.numel() > 0 else t.shape[-1]
+
+
+def _bstride(t) -> int:
+    return t.stride(0) if t.dim() == 3 else 0
 
 
 def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
@@ -55,32 +63,45 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
          stream: torch.cuda.Stream | None = None) -> torch.Tensor:
     """``C = alpha * A.B + beta * C`` with FP32 accumulation.
 
-    A: (M, K) bfloat16.  B: (N, K) bfloat16 (the K-contiguous storage of the
-    (K, N) operand).  C: (M, N) float32 or bfloat16; created when None (then
-    ``beta`` must be 0).  Asynchronous on ``stream`` (default: current stream).
+    A: (M, K) or a batch (b, M, K).  B: (N, K) or (b, N, K): the K-contiguous
+    storage of the (K, N) operand.  A and B are both bfloat16 or both float16.
+    C: (M, N) or (b, M, N), float32, bfloat16 or float16; created when None
+    (then ``beta`` must be 0).  Asynchronous on ``stream`` (default: current).
     """
-    _check_operand("A", A)
-    _check_operand("B", B)
-    M, K = A.shape
-    N, K2 = B.shape
-    if K2 != K:
-        raise ValueError(f"inner dimensions differ: A has K={K}, B has K={K2}")
+    _check_operand("A", A, tuple(_IN_CODES), (2, 3))
+    _check_operand("B", B, tuple(_IN_CODES), (A.dim(),))
+    if B.dtype != A.dtype:
+        raise TypeError("A and B must have the same dtype")
+    batched = A.dim() == 3
+    batch = A.shape[0] if batched else 1
+    M, K = A.shape[-2:]
+    N, K2 = B.shape[-2:]
+    if K2 != K or (batched and B.shape[0] != batch):
+        raise ValueError(f"shapes differ: A {tuple(A.shape)}, B {tuple(B.shape)}")
+    shape = (batch, M, N) if batched else (M, N)
     if C is None:
         if beta != 0.0:
             raise ValueError("beta != 0 needs an input C")
-        C = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=A.device)
+        C = torch.empty(shape, dtype=out_dtype or A.dtype, device=A.device)
     else:
         if out_dtype is not None and C.dtype != out_dtype:
             raise TypeError("C dtype and out_dtype differ")
-        _check_operand("C", C, C.dtype if C.dtype in _OUT_CODES else torch.float32)
-        if tuple(C.shape) != (M, N):
-            raise ValueError(f"C must be ({M}, {N})")
+        _check_operand("C", C, tuple(_OUT_CODES), (A.dim(),))
+        if tuple(C.shape) != shape:
+            raise ValueError(f"C must be {shape}")
     code = _OUT_CODES[C.dtype]
     with torch.cuda.device(A.device):
-        st = _native.gemm_bf16(M, N, K, float(alpha), A.data_ptr(), _ld(A), B.data_ptr(), _ld(B),
-                               float(beta), C.data_ptr(), _ld(C), code, _stream(stream, A.device))
+        if not batched and A.dtype == torch.bfloat16:
+            st = _native.gemm_bf16(M, N, K, float(alpha), A.data_ptr(), _ld(A), B.data_ptr(),
+                                   _ld(B), float(beta), C.data_ptr(), _ld(C), code,
+                                   _stream(stream, A.device))
+        else:
+            st = _native.gemm_batched(batch, M, N, K, float(alpha), A.data_ptr(), _ld(A),
+                                      _bstride(A), B.data_ptr(), _ld(B), _bstride(B),
+                                      float(beta), C.data_ptr(), _ld(C), _bstride(C),
+                                      _IN_CODES[A.dtype], code, _stream(stream, A.device))
     if st != GEMM_OK:
-        raise GemmError(st, "gemm_bf16")
+        raise GemmError(st, "gemm")
     return C
 
 
@@ -134,6 +155,16 @@ def plan(M: int, N: int, K: int, out_dtype: torch.dtype = torch.bfloat16, num_sm
     st, p = _native.gemm_bf16_plan(M, N, K, _OUT_CODES[out_dtype], num_sms)
     if st != GEMM_OK:
         raise GemmError(st, "gemm_bf16_plan")
+    return p.as_dict()
+
+
+def batched_plan(batch: int, M: int, N: int, K: int, in_dtype: torch.dtype = torch.bfloat16,
+                 out_dtype: torch.dtype = torch.bfloat16, num_sms: int = 0) -> dict:
+    """How ``gemm`` would run a batch of problems (host-side planning)."""
+    st, p = _native.gemm_batched_plan(batch, M, N, K, _IN_CODES[in_dtype], _OUT_CODES[out_dtype],
+                                      num_sms)
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_batched_plan")
     return p.as_dict()
 
 

@@ -21,6 +21,10 @@ GEMM_ERR_TIMEOUT = 5
 
 GEMM_OUT_F32 = 0
 GEMM_OUT_BF16 = 1
+GEMM_OUT_F16 = 2
+
+GEMM_IN_BF16 = 0
+GEMM_IN_F16 = 1
 
 KERNEL_NAMES = {0: "none", 1: "tiled", 2: "skinny_splitk", 3: "scale", 4: "gate_up",
                 5: "pair", 6: "pair_gate_up"}
@@ -36,6 +40,8 @@ EXPORTED = (
     "gemm_gate_up_plan",
     "gemm_selftest_wait_timeout",
     "gemm_bf16_skinny_noalloc",
+    "gemm_batched",
+    "gemm_batched_plan",
 )
 
 
@@ -105,6 +111,12 @@ def lib() -> ctypes.CDLL:
             l.gemm_prepare.argtypes = [_i64, _vp]
             l.gemm_bf16_plan.restype = _int
             l.gemm_bf16_plan.argtypes = [_i64, _i64, _i64, _int, _int, ctypes.POINTER(GemmPlan)]
+            l.gemm_batched.restype = _int
+            l.gemm_batched.argtypes = [_i64, _i64, _i64, _i64, _f32, _vp, _i64, _i64, _vp, _i64,
+                                       _i64, _f32, _vp, _i64, _i64, _int, _int, _vp]
+            l.gemm_batched_plan.restype = _int
+            l.gemm_batched_plan.argtypes = [_i64, _i64, _i64, _i64, _int, _int, _int,
+                                            ctypes.POINTER(GemmPlan)]
             l.gemm_bf16_skinny_noalloc.restype = _int
             l.gemm_bf16_skinny_noalloc.argtypes = [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64,
                                                    _f32, _vp, _i64, _int, _vp]
@@ -132,6 +144,19 @@ def gemm_bf16_skinny_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, out_d
     an allocated workspace (for callers that may not allocate)."""
     return lib().gemm_bf16_skinny_noalloc(M, N, K, alpha, A or None, lda, B or None, ldb, beta,
                                           C or None, ldc, out_dtype, stream or None)
+
+
+def gemm_batched(batch, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b, beta, C, ldc,
+                 stride_c, in_dtype, out_dtype, stream) -> int:
+    return lib().gemm_batched(batch, M, N, K, alpha, A or None, lda, stride_a, B or None, ldb,
+                              stride_b, beta, C or None, ldc, stride_c, in_dtype, out_dtype,
+                              stream or None)
+
+
+def gemm_batched_plan(batch, M, N, K, in_dtype=GEMM_IN_BF16, out_dtype=GEMM_OUT_BF16, num_sms=0):
+    plan = GemmPlan()
+    st = lib().gemm_batched_plan(batch, M, N, K, in_dtype, out_dtype, num_sms, ctypes.byref(plan))
+    return st, plan
 
 
 def gemm_gate_up_silu(M, N, K, X, ldx, Wg, Wu, ldw, Y, ldy, stream) -> int:

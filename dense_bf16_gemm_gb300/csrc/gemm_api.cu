@@ -6,11 +6,13 @@
 // Descriptor contract ("TMA and Hopper WGMMA", section "The same storage
 // contract on both sides"): a descriptor names the element type, the tile
 // (box) shape, the inner axis and a 128-byte swizzle row; the box's inner
-// extent is one swizzle row (64 BF16 or 32 FP32) and its outer extent is at
-// most 256.  Section "The same storage contract on both sides" also states
-// that a descriptor stays valid while values change and must be re-encoded
-// for a new address or new dimensions: the cache key is therefore (address,
-// element type, dimensions, row pitch, box).
+// extent is one swizzle row (64 16-bit or 32 FP32 elements) and its outer
+// extent is at most 256.  The same section states that a descriptor stays
+// valid while values change and must be re-encoded for a new address or new
+// dimensions: the cache key is therefore (address, element type, dimensions,
+// pitches, box, swizzle).  Every descriptor is three-dimensional, the third
+// coordinate selecting one matrix of a batch, bounded on its own (the same
+// section's three-dimensional binding); a single matrix is a batch of one.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -34,9 +36,9 @@ using namespace gb3;
 // ----------------------------------------------------------------------------
 // Kernel configurations
 // ----------------------------------------------------------------------------
-constexpr int kTileN = 256;        // output columns per tile of the tiled GEMM
-constexpr int kStages = 4;         // ring depth of the tiled GEMM (48 KB per stage)
-constexpr int kGateUpStages = 4;   // gate/up: 16 KB X + 16 KB Wg + 16 KB Wu per stage
+constexpr int kTileN = 256;        // output columns per tile of the single-CTA GEMM
+constexpr int kStages = 4;         // its ring depth (48 KB per stage)
+constexpr int kGateUpStages = 4;   // single-CTA gate/up: 16 KB X + 16 KB Wg + 16 KB Wu per stage
 constexpr int kSkinnyStages = 12;  // 18 KB per stage
 constexpr int kSkinnyMaxM = 16;
 constexpr int kGroupM = 16;
@@ -53,7 +55,37 @@ using CfgPairGU = PairCfg<256, kPairStages, EPI_GATE_UP>;
 // Tile widths compiled for the CTA-pair GEMM.
 constexpr int kPairWidths[] = {256, 224};
 
+constexpr int64_t kMaxDim = 0x7FFFFFFF;
+
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int env_int(const char* name, int fallback) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : fallback;
+}
+
+// ----------------------------------------------------------------------------
+// The problem a call describes
+// ----------------------------------------------------------------------------
+struct Problem {
+  int64_t batch, M, N, K;
+  float alpha, beta;
+  const void* A;
+  int64_t lda, sa;   // row pitch and matrix stride, elements
+  const void* B;
+  int64_t ldb, sb;
+  void* C;
+  int64_t ldc, sc;
+  int in_dtype;      // gemm_in_dtype
+  int out_dtype;     // gemm_out_dtype
+};
+
+int out_elem_bytes(int out_dtype) { return out_dtype == GEMM_OUT_F32 ? 4 : 2; }
+
+CUtensorMapDataType in_tma_type(int in_dtype) {
+  return in_dtype == GEMM_IN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
 
 // ----------------------------------------------------------------------------
 // Planning (pure host logic)
@@ -106,15 +138,10 @@ void choose_split(int64_t n_blocks, int64_t k_blocks, int sms, int* splits, int*
   *kb_per = static_cast<int>(ceil_div(k_blocks, best_s));
 }
 
-constexpr int kMinPieceKb = 24;       // shortest K piece of a split tail tile (1536 of K)
-constexpr int kMaxTailSplit = 2;      // more pieces cost more partial-sum traffic than they save
-constexpr double kSplitCharge = 0.1;  // partial-sum traffic of a split tail, in waves
+constexpr int kMinPieceKb = 24;        // shortest K piece of a split tail tile (1536 of K)
+constexpr int kMaxTailSplit = 2;       // more pieces cost more partial-sum traffic than they save
+constexpr double kSplitCharge = 0.1;   // partial-sum traffic of a split tail, in waves
 constexpr int kWidthCostOffset = 320;  // per-wave time model of a pair tile: width + 320
-
-int env_int(const char* name, int fallback) {
-  const char* v = std::getenv(name);
-  return v ? std::atoi(v) : fallback;
-}
 
 struct PairChoice {
   int bn = 256;
@@ -141,8 +168,8 @@ void plan_tail(int64_t tiles, int64_t k_blocks, int slots, bool allow_split, Pai
     return;
   }
   if (!allow_split || tail == 0 || env_int("GB3_GEMM_TAIL_SPLIT", 1) == 0) return;
-  int64_t s = std::min<int64_t>({static_cast<int64_t>(kMaxTailSplit), slots / tail,
-                                  k_blocks / kMinPieceKb});
+  const int64_t s = std::min<int64_t>(
+      {static_cast<int64_t>(kMaxTailSplit), slots / tail, k_blocks / kMinPieceKb});
   if (s < 2) return;
   const int64_t kbp = ceil_div(k_blocks, s);
   c->full = tiles - tail;
@@ -153,7 +180,8 @@ void plan_tail(int64_t tiles, int64_t k_blocks, int slots, bool allow_split, Pai
 // Tile width of the CTA-pair GEMM and its tail split: the fewest waves of
 // pair tiles (a split tail wave counts 1/split of a wave plus a charge for its
 // partial sums) weighted by the time a wave of that width takes.
-PairChoice choose_pair(int64_t M, int64_t N, int64_t K, int slots, bool allow_split) {
+PairChoice choose_pair(int64_t batch, int64_t M, int64_t N, int64_t K, int slots,
+                       bool allow_split) {
   PairChoice best;
   double best_cost = 1e300;
   const int64_t mb = ceil_div(M, kPairBM);
@@ -167,7 +195,7 @@ PairChoice choose_pair(int64_t M, int64_t N, int64_t K, int slots, bool allow_sp
     if (forced_valid && bn != forced) continue;
     PairChoice c;
     c.bn = bn;
-    plan_tail(mb * ceil_div(N, bn), kb, slots, allow_split, &c);
+    plan_tail(batch * mb * ceil_div(N, bn), kb, slots, allow_split, &c);
     double waves = static_cast<double>(c.full / slots);
     const int64_t left = c.tiles - (c.full / slots) * slots;
     if (left > 0) waves += c.split > 1 ? 1.0 / c.split + kSplitCharge : 1.0;
@@ -189,15 +217,15 @@ int64_t pair_workspace_bytes(const PairChoice& c) {
 
 // pair_slots: CTA pairs that fit on the device at once (0: assume sms / 2,
 // negative: pair kernels unavailable).
-int plan_gemm(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pair_slots = 0,
-              bool allow_split = true) {
+int plan_gemm(int64_t batch, int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl,
+              int pair_slots = 0, bool allow_split = true) {
   std::memset(pl, 0, sizeof(*pl));
   pl->split_k = 1;
-  if (M == 0 || N == 0) return GEMM_OK;
+  if (batch == 0 || M == 0 || N == 0) return GEMM_OK;
   if (K == 0) {
     pl->kernel = K_SCALE;
     pl->tiles = 1;
-    pl->grid = static_cast<int>(std::min<int64_t>(ceil_div(M * N, 256), 4 * sms));
+    pl->grid = static_cast<int>(std::min<int64_t>(ceil_div(batch * M * N, 256), 4 * sms));
     pl->launches = 1;
     return GEMM_OK;
   }
@@ -205,13 +233,13 @@ int plan_gemm(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pair_
   if (M <= kSkinnyMaxM) {
     const int64_t nb = ceil_div(N, kSkinnyRows), kb = ceil_div(K, kBK);
     int s, kbp;
-    choose_split(nb, kb, sms, &s, &kbp);
+    choose_split(batch * nb, kb, sms, &s, &kbp);
     pl->kernel = K_SKINNY;
     pl->tile_m = kSkinnyRows;
     pl->tile_n = kSkinnyNX;
     pl->stages = kSkinnyStages;
     pl->split_k = s;
-    pl->tiles = nb * s;
+    pl->tiles = batch * nb * s;
     pl->grid = static_cast<int>(std::min<int64_t>(pl->tiles, sms));
     pl->smem_bytes = CfgSkinny::kSmemBytes;
     pl->launches = 1;
@@ -220,7 +248,7 @@ int plan_gemm(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pair_
   }
   if (M >= kPairMinM && pair_slots >= 0) {
     const int slots = pair_slots > 0 ? pair_slots : std::max(1, sms / 2);
-    const PairChoice c = choose_pair(M, N, K, slots, allow_split);
+    const PairChoice c = choose_pair(batch, M, N, K, slots, allow_split);
     const int64_t units = c.full + (c.tiles - c.full) * c.split;
     pl->kernel = K_PAIR;
     pl->tile_m = kPairBM;
@@ -238,7 +266,7 @@ int plan_gemm(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pair_
   pl->tile_m = kBM;
   pl->tile_n = kTileN;
   pl->stages = kStages;
-  pl->tiles = ceil_div(M, kBM) * ceil_div(N, kTileN);
+  pl->tiles = batch * ceil_div(M, kBM) * ceil_div(N, kTileN);
   pl->grid = static_cast<int>(std::min<int64_t>(pl->tiles, sms));
   pl->smem_bytes = CfgBF16::kSmemBytes;
   pl->launches = 1;
@@ -294,32 +322,38 @@ int plan_gate_up(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pa
 // ----------------------------------------------------------------------------
 // Validation (no CUDA calls)
 // ----------------------------------------------------------------------------
-constexpr int64_t kMaxDim = 0x7FFFFFFF;
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int validate_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
-                  int64_t ldb, float beta, const void* C, int64_t ldc, int out_dtype) {
-  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+bool bad_dims(int64_t batch, int64_t M, int64_t N, int64_t K) {
+  return batch < 0 || M < 0 || N < 0 || K < 0 || batch > kMaxDim || M > kMaxDim || N > kMaxDim ||
+         K > kMaxDim;
+}
+
+int validate_problem(const Problem& p) {
+  if (bad_dims(p.batch, p.M, p.N, p.K)) return GEMM_ERR_INVALID_ARG;
+  if (p.in_dtype != GEMM_IN_BF16 && p.in_dtype != GEMM_IN_F16) return GEMM_ERR_INVALID_ARG;
+  if (p.out_dtype != GEMM_OUT_F32 && p.out_dtype != GEMM_OUT_BF16 && p.out_dtype != GEMM_OUT_F16)
     return GEMM_ERR_INVALID_ARG;
-  if (out_dtype != GEMM_OUT_F32 && out_dtype != GEMM_OUT_BF16) return GEMM_ERR_INVALID_ARG;
-  if (M == 0 || N == 0) return GEMM_OK;
-  const int64_t esize = out_dtype == GEMM_OUT_F32 ? 4 : 2;
-  if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
-  if (K > 0) {
-    if (A == nullptr || B == nullptr || lda < K || ldb < K) return GEMM_ERR_INVALID_ARG;
-    if (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0)
+  if (p.batch == 0 || p.M == 0 || p.N == 0) return GEMM_OK;
+  const int64_t esize = out_elem_bytes(p.out_dtype);
+  if (p.C == nullptr || p.ldc < p.N) return GEMM_ERR_INVALID_ARG;
+  if (p.batch > 1 && p.sc < p.M * p.ldc) return GEMM_ERR_INVALID_ARG;
+  if (p.K > 0) {
+    if (p.A == nullptr || p.B == nullptr || p.lda < p.K || p.ldb < p.K)
+      return GEMM_ERR_INVALID_ARG;
+    if (p.batch > 1 && (p.sa < p.M * p.lda || p.sb < p.N * p.ldb)) return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(p.A) || !aligned16(p.B) || (p.lda * 2) % 16 != 0 || (p.ldb * 2) % 16 != 0)
       return GEMM_ERR_ALIGNMENT;
+    if (p.batch > 1 && ((p.sa * 2) % 16 != 0 || (p.sb * 2) % 16 != 0)) return GEMM_ERR_ALIGNMENT;
   }
-  if (!aligned16(C) || (ldc * esize) % 16 != 0) return GEMM_ERR_ALIGNMENT;
-  (void)beta;
+  if (!aligned16(p.C) || (p.ldc * esize) % 16 != 0) return GEMM_ERR_ALIGNMENT;
+  if (p.batch > 1 && (p.sc * esize) % 16 != 0) return GEMM_ERR_ALIGNMENT;
   return GEMM_OK;
 }
 
 int validate_gate_up(int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx, const void* Wg,
                      const void* Wu, int64_t ldw, const void* Y, int64_t ldy) {
-  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
-    return GEMM_ERR_INVALID_ARG;
+  if (bad_dims(1, M, N, K)) return GEMM_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return GEMM_OK;
   if (Y == nullptr || ldy < N) return GEMM_ERR_INVALID_ARG;
   if (K > 0) {
@@ -342,11 +376,11 @@ struct DeviceState {
   bool probed = false;
   bool supported = false;
   int sms = 0;
-  // kernels whose shared-memory limit has been raised on this device
-  std::vector<const void*> configured;
   // CTA pairs that fit on the device at once (0: not queried yet, -1: none)
   int pair_slots = 0;
-  // split-K workspace of the skinny path
+  // kernels whose shared-memory limit has been raised on this device
+  std::vector<const void*> configured;
+  // split-K workspace (skinny path and split tail tiles)
   float* ws = nullptr;
   size_t ws_bytes = 0;
   int* counters = nullptr;
@@ -381,17 +415,6 @@ int probe_device(int dev) {
     d.sms = sms;
   }
   return d.supported ? GEMM_OK : GEMM_ERR_UNSUPPORTED;
-}
-
-int device_sms(int* sms) {
-  int dev;
-  int st = current_device(&dev);
-  if (st != GEMM_OK) return st;
-  std::lock_guard<std::mutex> lk(g_mu);
-  st = probe_device(dev);
-  if (st != GEMM_OK) return st;
-  *sms = g_dev[dev].sms;
-  return GEMM_OK;
 }
 
 // Caller holds g_mu.
@@ -469,13 +492,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct MapKey {
   const void* ptr;
   int dtype;
-  uint64_t inner, outer, pitch;
+  uint64_t inner, outer, batch, pitch, bstride;
   uint32_t box_inner, box_outer;
   int swizzle;
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && dtype == o.dtype && inner == o.inner && outer == o.outer &&
-           pitch == o.pitch && box_inner == o.box_inner && box_outer == o.box_outer &&
-           swizzle == o.swizzle;
+           batch == o.batch && pitch == o.pitch && bstride == o.bstride &&
+           box_inner == o.box_inner && box_outer == o.box_outer && swizzle == o.swizzle;
   }
 };
 
@@ -490,13 +513,33 @@ std::mutex g_map_mu;
 std::vector<MapEntry> g_maps;
 uint64_t g_map_clock = 0;
 
-// 2-D map over a row-major matrix of `outer` rows of `inner` elements with a
-// row pitch of `pitch` bytes; box of box_inner x box_outer elements, 128-byte
-// swizzle, out-of-bounds elements read as zero.
-int tensor_map_2d(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, uint64_t inner,
-                  uint64_t outer, uint64_t pitch, uint32_t box_inner, uint32_t box_outer,
+// Encodes a 3-D map: `batch` matrices `bstride` bytes apart, each of `outer`
+// rows of `inner` elements with a row pitch of `pitch` bytes; box of
+// box_inner x box_outer elements of one matrix; out-of-bounds elements read
+// as zero.  No cache, no allocation.
+int encode_map_3d(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, uint64_t inner,
+                  uint64_t outer, uint64_t batch, uint64_t pitch, uint64_t bstride,
+                  uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return GEMM_ERR_CUDA;
+  const cuuint64_t dims[3] = {inner, outer, batch};
+  const cuuint64_t strides[2] = {pitch, bstride};
+  const cuuint32_t box[3] = {box_inner, box_outer, 1};
+  const cuuint32_t estrides[3] = {1, 1, 1};
+  const CUresult r = fn(out, dtype, 3, const_cast<void*>(ptr), dims, strides, box, estrides,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// encode_map_3d through the descriptor cache.  A single matrix passes
+// batch = 1 and bstride = pitch * outer.
+int tensor_map_3d(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, uint64_t inner,
+                  uint64_t outer, uint64_t batch, uint64_t pitch, uint64_t bstride,
+                  uint32_t box_inner, uint32_t box_outer,
                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
-  const MapKey key{ptr, static_cast<int>(dtype), inner, outer, pitch, box_inner, box_outer,
+  const MapKey key{ptr,     static_cast<int>(dtype), inner,     outer, batch,
+                   pitch,   bstride,                 box_inner, box_outer,
                    static_cast<int>(swizzle)};
   std::lock_guard<std::mutex> lk(g_map_mu);
   for (MapEntry& e : g_maps) {
@@ -506,17 +549,10 @@ int tensor_map_2d(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, 
       return GEMM_OK;
     }
   }
-  auto fn = encode_fn();
-  if (fn == nullptr) return GEMM_ERR_CUDA;
   CUtensorMap map;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {pitch};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estrides[2] = {1, 1};
-  const CUresult r = fn(&map, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estrides,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return GEMM_ERR_CUDA;
+  const int st = encode_map_3d(&map, ptr, dtype, inner, outer, batch, pitch, bstride, box_inner,
+                               box_outer, swizzle);
+  if (st != GEMM_OK) return st;
   if (g_maps.size() < kMapCacheSize) {
     g_maps.push_back(MapEntry{key, map, ++g_map_clock});
   } else {
@@ -526,6 +562,33 @@ int tensor_map_2d(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, 
   }
   *out = map;
   return GEMM_OK;
+}
+
+// Operand map of A (rows = M) or B (rows = N): box of 64 K-elements by `rows_box` rows.
+int operand_map(CUtensorMap* out, const void* ptr, int in_dtype, int64_t K, int64_t rows,
+                int64_t batch, int64_t ld, int64_t stride, uint32_t rows_box) {
+  const uint64_t pitch = static_cast<uint64_t>(ld) * 2;
+  const uint64_t bstride = batch > 1 ? static_cast<uint64_t>(stride) * 2 : pitch * rows;
+  return tensor_map_3d(out, ptr, in_tma_type(in_dtype), K, rows, batch, pitch, bstride, kBK,
+                       rows_box);
+}
+
+// Output descriptor of an epilogue box: FP32 32 x 32 (128-byte swizzle);
+// 16-bit 64 x 32 (128-byte swizzle) or, for tile widths not a multiple of 64,
+// 32 x 32 (64-byte swizzle).  Must match EpiBox in gemm_kernels.cuh.
+int output_map(CUtensorMap* out, void* C, int64_t batch, int64_t M, int64_t N, int64_t ldc,
+               int64_t sc, int out_dtype, int tile_out_cols) {
+  const int es = out_elem_bytes(out_dtype);
+  const uint64_t pitch = static_cast<uint64_t>(ldc) * es;
+  const uint64_t bstride = batch > 1 ? static_cast<uint64_t>(sc) * es : pitch * M;
+  if (out_dtype == GEMM_OUT_F32)
+    return tensor_map_3d(out, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, M, batch, pitch, bstride, 32,
+                         32);
+  const CUtensorMapDataType t = out_dtype == GEMM_OUT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                          : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (tile_out_cols % 64 == 0)
+    return tensor_map_3d(out, C, t, N, M, batch, pitch, bstride, 64, 32);
+  return tensor_map_3d(out, C, t, N, M, batch, pitch, bstride, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // ----------------------------------------------------------------------------
@@ -604,17 +667,22 @@ int query_pair_slots(int dev) {
   return d.pair_slots;
 }
 
-// C = beta * C (K == 0); C is not read when beta == 0.
-__global__ void scale_kernel(void* C, long long ldc, int M, int N, float beta, int bf16) {
-  const long long total = static_cast<long long>(M) * N;
+// C = beta * C for every matrix of the batch (K == 0); C is not read when
+// beta == 0.  out_kind: 0 FP32, 1 BF16, 2 FP16.
+__global__ void scale_kernel(void* C, long long ldc, long long sc, int batch, int M, int N,
+                             float beta, int out_kind) {
+  const long long per = static_cast<long long>(M) * N;
+  const long long total = per * batch;
+  const bool f16 = out_kind == 2;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long m = i / N, n = i % N;
-    const long long off = m * ldc + n;
-    if (bf16) {
+    const long long b = i / per, r = i % per;
+    const long long m = r / N, n = r % N;
+    const long long off = b * sc + m * ldc + n;
+    if (out_kind != 0) {
       uint16_t* c = static_cast<uint16_t*>(C);
-      const float v = beta == 0.0f ? 0.0f : beta * bf16_bits_to_float(c[off]);
-      c[off] = static_cast<uint16_t>(pack_bf16x2(v, 0.0f) & 0xFFFFu);
+      const float v = beta == 0.0f ? 0.0f : beta * half16_to_float(c[off], f16);
+      c[off] = static_cast<uint16_t>(pack_half16x2(v, 0.0f, f16) & 0xFFFFu);
     } else {
       float* c = static_cast<float*>(C);
       c[off] = beta == 0.0f ? 0.0f : beta * c[off];
@@ -622,27 +690,32 @@ __global__ void scale_kernel(void* C, long long ldc, int M, int N, float beta, i
   }
 }
 
-int run_scale(const gemm_plan& pl, void* C, int64_t ldc, int64_t M, int64_t N, float beta,
-              bool bf16, cudaStream_t stream) {
+int run_scale(const gemm_plan& pl, void* C, int64_t ldc, int64_t sc, int64_t batch, int64_t M,
+              int64_t N, float beta, int out_dtype, cudaStream_t stream) {
   return launch(scale_kernel, pl.grid, 256, 0, stream, C, static_cast<long long>(ldc),
-                static_cast<int>(M), static_cast<int>(N), beta, bf16 ? 1 : 0);
+                static_cast<long long>(sc), static_cast<int>(batch), static_cast<int>(M),
+                static_cast<int>(N), beta, out_dtype);
 }
 
-TileParams tile_params(int64_t M, int64_t N, int64_t K, int tile_m, int tile_n_out, float alpha,
-                       float beta, const void* C, int64_t ldc, int64_t tiles) {
+TileParams tile_params(const Problem& q, int tile_m, int tile_n_out, uint32_t idesc) {
   TileParams p;
-  p.M = static_cast<int>(M);
-  p.N = static_cast<int>(N);
-  p.K = static_cast<int>(K);
-  p.m_blocks = static_cast<int>(ceil_div(M, tile_m));
-  p.n_blocks = static_cast<int>(ceil_div(N, tile_n_out));
-  p.k_blocks = static_cast<int>(ceil_div(K, kBK));
-  p.num_tiles = static_cast<int>(tiles);
+  p.M = static_cast<int>(q.M);
+  p.N = static_cast<int>(q.N);
+  p.K = static_cast<int>(q.K);
+  p.m_blocks = static_cast<int>(ceil_div(q.M, tile_m));
+  p.n_blocks = static_cast<int>(ceil_div(q.N, tile_n_out));
+  p.k_blocks = static_cast<int>(ceil_div(q.K, kBK));
+  p.batch = static_cast<int>(q.batch);
+  p.tiles_per_matrix = p.m_blocks * p.n_blocks;
+  p.num_tiles = static_cast<int>(q.batch * p.tiles_per_matrix);
   p.group_m = kGroupM;
-  p.alpha = alpha;
-  p.beta = beta;
-  p.C = C;
-  p.ldc = ldc;
+  p.idesc = idesc;
+  p.out_f16 = q.out_dtype == GEMM_OUT_F16 ? 1 : 0;
+  p.c_stride = q.batch > 1 ? q.sc : 0;
+  p.alpha = q.alpha;
+  p.beta = q.beta;
+  p.C = q.C;
+  p.ldc = q.ldc;
   p.num_full = p.num_tiles;
   p.tail_split = 1;
   p.kb_per_piece = p.k_blocks;
@@ -652,20 +725,19 @@ TileParams tile_params(int64_t M, int64_t N, int64_t K, int tile_m, int tile_n_o
   return p;
 }
 
-// Work units of a pair plan (whole tiles, then split tail pieces) and the
+// Work units of a pair plan (split tail pieces, then whole tiles) and the
 // workspace they need.  A plan that needs a workspace the device cannot get
-// (the stream is being captured) is redone without the split.
-int pair_units(int dev, gemm_plan* pl, int64_t M, int64_t N, int64_t K, int bn_out_cols,
-               TileParams* p, cudaStream_t stream, bool gate_up, int slots) {
-  const int64_t tiles = ceil_div(M, kPairBM) * ceil_div(N, bn_out_cols);
-  p->num_tiles = static_cast<int>(tiles);
+// (the stream is being captured) runs its tiles whole instead.
+void pair_units(int dev, gemm_plan* pl, const Problem& q, int out_cols, TileParams* p,
+                cudaStream_t stream, bool gate_up, int slots) {
   PairChoice c;
   if (gate_up) {
     c.bn = 256;
-    plan_tail(tiles, p->k_blocks, slots, true, &c);
+    plan_tail(p->num_tiles, p->k_blocks, slots, true, &c);
   } else {
-    c = choose_pair(M, N, K, slots, true);
+    c = choose_pair(q.batch, q.M, q.N, q.K, slots, true);
   }
+  (void)out_cols;
   if (c.split > 1) {
     const size_t ws = static_cast<size_t>(pair_workspace_bytes(c));
     const size_t counters = static_cast<size_t>(c.tiles - c.full) * 8;
@@ -679,7 +751,6 @@ int pair_units(int dev, gemm_plan* pl, int64_t M, int64_t N, int64_t K, int bn_o
       }
     }
     if (st != GEMM_OK) {
-      // Without a workspace (graph capture): the same tiles, all whole.
       c.full = c.tiles;
       c.split = 1;
       c.kb_per_piece = p->k_blocks;
@@ -692,7 +763,6 @@ int pair_units(int dev, gemm_plan* pl, int64_t M, int64_t N, int64_t K, int bn_o
   p->tail_split = c.split;
   p->kb_per_piece = c.kb_per_piece;
   p->num_units = static_cast<int>(c.full + (c.tiles - c.full) * c.split);
-  return GEMM_OK;
 }
 
 template <int BN, int EPI>
@@ -709,43 +779,142 @@ int launch_pair_gemm(const gemm_plan& pl, int dev, const CUtensorMap& tmA, const
   return launch_pair(kern, pl.grid, Cfg::kSmemBytes, stream, tmA, tmB, tmB2, tmOut, p);
 }
 
-// Output descriptor of an epilogue box: FP32 32 x 32 (128-byte swizzle);
-// BF16 64 x 32 (128-byte swizzle) or, for tile widths not a multiple of 64,
-// 32 x 32 (64-byte swizzle).  Must match EpiBox in gemm_kernels.cuh.
-int output_map(CUtensorMap* out, void* C, int64_t M, int64_t N, int64_t ldc, bool bf16,
-               int tile_out_cols) {
-  if (!bf16)
-    return tensor_map_2d(out, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, M, ldc * 4, 32, 32);
-  if (tile_out_cols % 64 == 0)
-    return tensor_map_2d(out, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldc * 2, 64, 32);
-  return tensor_map_2d(out, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldc * 2, 32, 32,
-                       CU_TENSOR_MAP_SWIZZLE_64B);
+template <int BN, int STAGES, int EPI>
+int launch_single_gemm(const gemm_plan& pl, int dev, const CUtensorMap& tmA,
+                       const CUtensorMap& tmB, const CUtensorMap& tmB2, const CUtensorMap& tmOut,
+                       const TileParams& p, cudaStream_t stream) {
+  using Cfg = GemmCfg<BN, STAGES, EPI>;
+  auto kern = gemm_tc_kernel<BN, STAGES, EPI>;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const int st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), Cfg::kSmemBytes);
+    if (st != GEMM_OK) return st;
+  }
+  return launch(kern, pl.grid, kThreads, Cfg::kSmemBytes, stream, tmA, tmB, tmB2, tmOut, p);
 }
 
-int run_pair(gemm_plan& pl, int dev, int sms, int slots, int64_t M, int64_t N, int64_t K,
-             float alpha, const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
-             void* C, int64_t ldc, bool bf16, cudaStream_t stream) {
+int run_pair(gemm_plan& pl, int dev, int slots, const Problem& q, cudaStream_t stream) {
   const int bn = pl.tile_n;
+  const bool f16in = q.in_dtype == GEMM_IN_F16;
   CUtensorMap tmA, tmB, tmOut;
   int st;
-  if ((st = tensor_map_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, lda * 2, kBK, 128)) !=
+  if ((st = operand_map(&tmA, q.A, q.in_dtype, q.K, q.M, q.batch, q.lda, q.sa, 128)) != GEMM_OK)
+    return st;
+  if ((st = operand_map(&tmB, q.B, q.in_dtype, q.K, q.N, q.batch, q.ldb, q.sb, bn / 2)) !=
       GEMM_OK)
     return st;
-  if ((st = tensor_map_2d(&tmB, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldb * 2, kBK,
-                          bn / 2)) != GEMM_OK)
+  if ((st = output_map(&tmOut, q.C, q.batch, q.M, q.N, q.ldc, q.sc, q.out_dtype, bn)) != GEMM_OK)
     return st;
-  if ((st = output_map(&tmOut, C, M, N, ldc, bf16, bn)) != GEMM_OK) return st;
-  TileParams p = tile_params(M, N, K, kPairBM, bn, alpha, beta, C, ldc, pl.tiles);
-  pair_units(dev, &pl, M, N, K, bn, &p, stream, false, slots);
+  TileParams p = tile_params(q, kPairBM, bn, idesc_f32_acc(kPairBM, bn, f16in));
+  pair_units(dev, &pl, q, bn, &p, stream, false, slots);
+  const bool f32 = q.out_dtype == GEMM_OUT_F32;
   switch (bn) {
     case 256:
-      return bf16 ? launch_pair_gemm<256, EPI_BF16>(pl, dev, tmA, tmB, tmB, tmOut, p, stream)
-                  : launch_pair_gemm<256, EPI_F32>(pl, dev, tmA, tmB, tmB, tmOut, p, stream);
+      return f32 ? launch_pair_gemm<256, EPI_F32>(pl, dev, tmA, tmB, tmB, tmOut, p, stream)
+                 : launch_pair_gemm<256, EPI_BF16>(pl, dev, tmA, tmB, tmB, tmOut, p, stream);
     case 224:
-      return bf16 ? launch_pair_gemm<224, EPI_BF16>(pl, dev, tmA, tmB, tmB, tmOut, p, stream)
-                  : launch_pair_gemm<224, EPI_F32>(pl, dev, tmA, tmB, tmB, tmOut, p, stream);
+      return f32 ? launch_pair_gemm<224, EPI_F32>(pl, dev, tmA, tmB, tmB, tmOut, p, stream)
+                 : launch_pair_gemm<224, EPI_BF16>(pl, dev, tmA, tmB, tmB, tmOut, p, stream);
     default:
       return GEMM_ERR_UNSUPPORTED;
+  }
+}
+
+int run_single(const gemm_plan& pl, int dev, const Problem& q, cudaStream_t stream) {
+  const bool f16in = q.in_dtype == GEMM_IN_F16;
+  CUtensorMap tmA, tmB, tmOut;
+  int st;
+  if ((st = operand_map(&tmA, q.A, q.in_dtype, q.K, q.M, q.batch, q.lda, q.sa, kBM)) != GEMM_OK)
+    return st;
+  if ((st = operand_map(&tmB, q.B, q.in_dtype, q.K, q.N, q.batch, q.ldb, q.sb, kTileN)) !=
+      GEMM_OK)
+    return st;
+  if ((st = output_map(&tmOut, q.C, q.batch, q.M, q.N, q.ldc, q.sc, q.out_dtype, kTileN)) !=
+      GEMM_OK)
+    return st;
+  const TileParams p = tile_params(q, kBM, kTileN, idesc_f32_acc(kBM, kTileN, f16in));
+  if (q.out_dtype == GEMM_OUT_F32)
+    return launch_single_gemm<kTileN, kStages, EPI_F32>(pl, dev, tmA, tmB, tmB, tmOut, p, stream);
+  return launch_single_gemm<kTileN, kStages, EPI_BF16>(pl, dev, tmA, tmB, tmB, tmOut, p, stream);
+}
+
+SkinnyParams skinny_params(const gemm_plan& pl, const Problem& q) {
+  SkinnyParams p;
+  p.M = static_cast<int>(q.M);
+  p.N = static_cast<int>(q.N);
+  p.K = static_cast<int>(q.K);
+  p.n_blocks = static_cast<int>(ceil_div(q.N, kSkinnyRows));
+  p.k_blocks = static_cast<int>(ceil_div(q.K, kBK));
+  p.splits = pl.split_k;
+  p.kb_per_split = static_cast<int>(ceil_div(p.k_blocks, p.splits));
+  p.batch = static_cast<int>(q.batch);
+  p.num_units = static_cast<int>(pl.tiles);
+  p.alpha = q.alpha;
+  p.beta = q.beta;
+  p.C = q.C;
+  p.ldc = q.ldc;
+  p.c_stride = q.batch > 1 ? q.sc : 0;
+  p.out_kind = q.out_dtype;
+  p.idesc = idesc_f32_acc(kSkinnyRows, kSkinnyNX, q.in_dtype == GEMM_IN_F16);
+  p.ws = nullptr;
+  p.counters = nullptr;
+  return p;
+}
+
+int run_skinny(const gemm_plan& pl, int dev, const Problem& q, cudaStream_t stream) {
+  CUtensorMap tmW, tmX;
+  int st;
+  if ((st = operand_map(&tmW, q.B, q.in_dtype, q.K, q.N, q.batch, q.ldb, q.sb, kSkinnyRows)) !=
+      GEMM_OK)
+    return st;
+  if ((st = operand_map(&tmX, q.A, q.in_dtype, q.K, q.M, q.batch, q.lda, q.sa, kSkinnyNX)) !=
+      GEMM_OK)
+    return st;
+  SkinnyParams p = skinny_params(pl, q);
+  auto kern = gemm_skinny_kernel<kSkinnyStages>;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), pl.smem_bytes)) !=
+        GEMM_OK)
+      return st;
+    if (p.splits > 1) {
+      const size_t ws_bytes =
+          static_cast<size_t>(q.batch) * p.splits * q.M * q.N * sizeof(float);
+      const size_t counters = static_cast<size_t>(q.batch) * p.n_blocks * 4;
+      if ((st = ensure_workspace(dev, ws_bytes, counters, stream)) != GEMM_OK) return st;
+      p.ws = g_dev[dev].ws;
+      p.counters = g_dev[dev].counters;
+    }
+  }
+  return launch(kern, pl.grid, kThreads, pl.smem_bytes, stream, tmW, tmX, p);
+}
+
+int run_problem(const Problem& q, void* stream_) {
+  int st = validate_problem(q);
+  if (st != GEMM_OK) return st;
+  if (q.batch == 0 || q.M == 0 || q.N == 0) return GEMM_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev;
+  if ((st = current_device(&dev)) != GEMM_OK) return st;
+  int sms, slots;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = probe_device(dev)) != GEMM_OK) return st;
+    sms = g_dev[dev].sms;
+    slots = query_pair_slots(dev);
+  }
+  gemm_plan pl;
+  plan_gemm(q.batch, q.M, q.N, q.K, sms, &pl, slots);
+  switch (pl.kernel) {
+    case K_SCALE:
+      return run_scale(pl, q.C, q.ldc, q.batch > 1 ? q.sc : 0, q.batch, q.M, q.N, q.beta,
+                       q.out_dtype, stream);
+    case K_PAIR:
+      return run_pair(pl, dev, slots, q, stream);
+    case K_SKINNY:
+      return run_skinny(pl, dev, q, stream);
+    default:
+      return run_single(pl, dev, q, stream);
   }
 }
 
@@ -768,129 +937,62 @@ const char* gemm_status_string(int status) {
   }
 }
 
+int gemm_batched_plan(int64_t batch, int64_t M, int64_t N, int64_t K, int in_dtype,
+                      int out_dtype, int num_sms, gemm_plan* plan) {
+  if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
+  if (bad_dims(batch, M, N, K)) return GEMM_ERR_INVALID_ARG;
+  if (in_dtype != GEMM_IN_BF16 && in_dtype != GEMM_IN_F16) return GEMM_ERR_INVALID_ARG;
+  if (out_dtype != GEMM_OUT_F32 && out_dtype != GEMM_OUT_BF16 && out_dtype != GEMM_OUT_F16)
+    return GEMM_ERR_INVALID_ARG;
+  int slots = 0;
+  if (num_sms <= 0) {
+    int dev;
+    int st = current_device(&dev);
+    if (st != GEMM_OK) return st;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = probe_device(dev)) != GEMM_OK) return st;
+    num_sms = g_dev[dev].sms;
+    slots = query_pair_slots(dev);
+  }
+  return plan_gemm(batch, M, N, K, num_sms, plan, slots);
+}
+
 int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int num_sms,
                    gemm_plan* plan) {
-  if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
-  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
-    return GEMM_ERR_INVALID_ARG;
-  if (out_dtype != GEMM_OUT_F32 && out_dtype != GEMM_OUT_BF16) return GEMM_ERR_INVALID_ARG;
-  if (num_sms <= 0) {
-    const int st = device_sms(&num_sms);
-    if (st != GEMM_OK) return st;
-  }
-  return plan_gemm(M, N, K, num_sms, plan);
+  return gemm_batched_plan(1, M, N, K, GEMM_IN_BF16, out_dtype, num_sms, plan);
 }
 
 int gemm_gate_up_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_plan* plan) {
   if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
-  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
-    return GEMM_ERR_INVALID_ARG;
+  if (bad_dims(1, M, N, K)) return GEMM_ERR_INVALID_ARG;
+  int slots = 0;
   if (num_sms <= 0) {
-    const int st = device_sms(&num_sms);
+    int dev;
+    int st = current_device(&dev);
     if (st != GEMM_OK) return st;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = probe_device(dev)) != GEMM_OK) return st;
+    num_sms = g_dev[dev].sms;
+    slots = query_pair_slots(dev);
   }
-  return plan_gate_up(M, N, K, num_sms, plan);
+  return plan_gate_up(M, N, K, num_sms, plan, slots);
 }
 
 int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
               const void* B, int64_t ldb, float beta, void* C, int64_t ldc, int out_dtype,
-              void* stream_) {
-  int st = validate_gemm(M, N, K, A, lda, B, ldb, beta, C, ldc, out_dtype);
-  if (st != GEMM_OK) return st;
-  if (M == 0 || N == 0) return GEMM_OK;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  int dev;
-  if ((st = current_device(&dev)) != GEMM_OK) return st;
-  int sms, slots;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if ((st = probe_device(dev)) != GEMM_OK) return st;
-    sms = g_dev[dev].sms;
-    slots = query_pair_slots(dev);
-  }
-  gemm_plan pl;
-  plan_gemm(M, N, K, sms, &pl, slots);
-  const bool bf16 = out_dtype == GEMM_OUT_BF16;
+              void* stream) {
+  const Problem q{1, M, N, K, alpha, beta, A, lda, 0, B, ldb, 0, C, ldc, 0, GEMM_IN_BF16,
+                  out_dtype};
+  return run_problem(q, stream);
+}
 
-  if (pl.kernel == K_SCALE) return run_scale(pl, C, ldc, M, N, beta, bf16, stream);
-  if (pl.kernel == K_PAIR)
-    return run_pair(pl, dev, sms, slots, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bf16,
-                    stream);
-
-  if (pl.kernel == K_SKINNY) {
-    CUtensorMap tmW, tmX;
-    if ((st = tensor_map_2d(&tmW, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldb * 2, kBK,
-                            kSkinnyRows)) != GEMM_OK)
-      return st;
-    if ((st = tensor_map_2d(&tmX, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, lda * 2, kBK,
-                            kSkinnyNX)) != GEMM_OK)
-      return st;
-    SkinnyParams p;
-    p.M = static_cast<int>(M);
-    p.N = static_cast<int>(N);
-    p.K = static_cast<int>(K);
-    p.n_blocks = static_cast<int>(ceil_div(N, kSkinnyRows));
-    p.k_blocks = static_cast<int>(ceil_div(K, kBK));
-    p.splits = pl.split_k;
-    p.kb_per_split = static_cast<int>(ceil_div(p.k_blocks, p.splits));
-    p.num_units = static_cast<int>(pl.tiles);
-    p.alpha = alpha;
-    p.beta = beta;
-    p.C = C;
-    p.ldc = ldc;
-    p.out_bf16 = bf16 ? 1 : 0;
-    p.ws = nullptr;
-    p.counters = nullptr;
-    auto kern = gemm_skinny_kernel<kSkinnyStages>;
-    {
-      std::lock_guard<std::mutex> lk(g_mu);
-      if ((st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), pl.smem_bytes)) !=
-          GEMM_OK)
-        return st;
-      if (p.splits > 1) {
-        const size_t ws_bytes = static_cast<size_t>(p.splits) * M * N * sizeof(float);
-        const size_t counters = static_cast<size_t>(p.n_blocks) * 4;
-        if ((st = ensure_workspace(dev, ws_bytes, counters, stream)) != GEMM_OK) return st;
-        p.ws = g_dev[dev].ws;
-        p.counters = g_dev[dev].counters;
-      }
-    }
-    return launch(kern, pl.grid, kThreads, pl.smem_bytes, stream, tmW, tmX, p);
-  }
-
-  // Tiled tcgen05 GEMM.
-  CUtensorMap tmA, tmB, tmOut;
-  if ((st = tensor_map_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, lda * 2, kBK, kBM)) !=
-      GEMM_OK)
-    return st;
-  if ((st = tensor_map_2d(&tmB, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldb * 2, kBK,
-                          kTileN)) != GEMM_OK)
-    return st;
-  if (bf16) {
-    st = tensor_map_2d(&tmOut, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldc * 2, 64, 32);
-  } else {
-    st = tensor_map_2d(&tmOut, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, M, ldc * 4, 32, 32);
-  }
-  if (st != GEMM_OK) return st;
-  const TileParams p = tile_params(M, N, K, kBM, kTileN, alpha, beta, C, ldc, pl.tiles);
-  if (bf16) {
-    auto kern = gemm_tc_kernel<kTileN, kStages, EPI_BF16>;
-    {
-      std::lock_guard<std::mutex> lk(g_mu);
-      if ((st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern),
-                                 CfgBF16::kSmemBytes)) != GEMM_OK)
-        return st;
-    }
-    return launch(kern, pl.grid, kThreads, CfgBF16::kSmemBytes, stream, tmA, tmB, tmB, tmOut, p);
-  }
-  auto kern = gemm_tc_kernel<kTileN, kStages, EPI_F32>;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if ((st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), CfgF32::kSmemBytes)) !=
-        GEMM_OK)
-      return st;
-  }
-  return launch(kern, pl.grid, kThreads, CfgF32::kSmemBytes, stream, tmA, tmB, tmB, tmOut, p);
+int gemm_batched(int64_t batch, int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                 int64_t lda, int64_t stride_a, const void* B, int64_t ldb, int64_t stride_b,
+                 float beta, void* C, int64_t ldc, int64_t stride_c, int in_dtype, int out_dtype,
+                 void* stream) {
+  const Problem q{batch, M,        N,   K,   alpha, beta,     A,        lda,      stride_a,
+                  B,     ldb,      stride_b, C, ldc, stride_c, in_dtype, out_dtype};
+  return run_problem(q, stream);
 }
 
 int gemm_gate_up_silu(int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx,
@@ -911,48 +1013,26 @@ int gemm_gate_up_silu(int64_t M, int64_t N, int64_t K, const void* X, int64_t ld
   }
   gemm_plan pl;
   plan_gate_up(M, N, K, sms, &pl, slots);
-  if (pl.kernel == K_SCALE) return run_scale(pl, Y, ldy, M, N, 0.0f, true, stream);
-  if (pl.kernel == K_PAIR_GATE_UP) {
-    CUtensorMap tmX, tmWg, tmWu, tmY;
-    if ((st = tensor_map_2d(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, ldx * 2, kBK, 128)) !=
-        GEMM_OK)
-      return st;
-    if ((st = tensor_map_2d(&tmWg, Wg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldw * 2, kBK,
-                            CfgPairGU::kOutCols)) != GEMM_OK)
-      return st;
-    if ((st = tensor_map_2d(&tmWu, Wu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldw * 2, kBK,
-                            CfgPairGU::kOutCols)) != GEMM_OK)
-      return st;
-    if ((st = output_map(&tmY, Y, M, N, ldy, true, CfgPairGU::kOutCols)) != GEMM_OK) return st;
-    TileParams p = tile_params(M, N, K, kPairBM, CfgPairGU::kOutCols, 1.0f, 0.0f, nullptr, ldy,
-                               pl.tiles);
-    pair_units(dev, &pl, M, N, K, CfgPairGU::kOutCols, &p, stream, true, slots);
+  if (pl.kernel == K_SCALE) return run_scale(pl, Y, ldy, 0, 1, M, N, 0.0f, GEMM_OUT_BF16, stream);
+  // Wg and Wu play the part of B; the output is BF16.
+  const Problem q{1, M, N, K, 1.0f, 0.0f, X, ldx, 0, Wg, ldw, 0, Y, ldy, 0, GEMM_IN_BF16,
+                  GEMM_OUT_BF16};
+  const bool pair = pl.kernel == K_PAIR_GATE_UP;
+  const int out_cols = pair ? CfgPairGU::kOutCols : CfgGU::kOutCols;
+  CUtensorMap tmX, tmWg, tmWu, tmY;
+  if ((st = operand_map(&tmX, X, GEMM_IN_BF16, K, M, 1, ldx, 0, pair ? 128 : kBM)) != GEMM_OK)
+    return st;
+  if ((st = operand_map(&tmWg, Wg, GEMM_IN_BF16, K, N, 1, ldw, 0, out_cols)) != GEMM_OK) return st;
+  if ((st = operand_map(&tmWu, Wu, GEMM_IN_BF16, K, N, 1, ldw, 0, out_cols)) != GEMM_OK) return st;
+  if ((st = output_map(&tmY, Y, 1, M, N, ldy, 0, GEMM_OUT_BF16, out_cols)) != GEMM_OK) return st;
+  if (pair) {
+    TileParams p = tile_params(q, kPairBM, out_cols, idesc_f32_acc(kPairBM, 256, false));
+    pair_units(dev, &pl, q, out_cols, &p, stream, true, slots);
     return launch_pair_gemm<256, EPI_GATE_UP>(pl, dev, tmX, tmWg, tmWu, tmY, p, stream);
   }
-
-  CUtensorMap tmX, tmWg, tmWu, tmY;
-  if ((st = tensor_map_2d(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, ldx * 2, kBK, kBM)) !=
-      GEMM_OK)
-    return st;
-  if ((st = tensor_map_2d(&tmWg, Wg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldw * 2, kBK,
-                          CfgGU::kOutCols)) != GEMM_OK)
-    return st;
-  if ((st = tensor_map_2d(&tmWu, Wu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldw * 2, kBK,
-                          CfgGU::kOutCols)) != GEMM_OK)
-    return st;
-  if ((st = tensor_map_2d(&tmY, Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldy * 2, 64, 32)) !=
-      GEMM_OK)
-    return st;
-  const TileParams p =
-      tile_params(M, N, K, kBM, CfgGU::kOutCols, 1.0f, 0.0f, nullptr, ldy, pl.tiles);
-  auto kern = gemm_tc_kernel<256, kGateUpStages, EPI_GATE_UP>;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if ((st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), CfgGU::kSmemBytes)) !=
-        GEMM_OK)
-      return st;
-  }
-  return launch(kern, pl.grid, kThreads, CfgGU::kSmemBytes, stream, tmX, tmWg, tmWu, tmY, p);
+  const TileParams p = tile_params(q, kBM, out_cols, idesc_f32_acc(kBM, 256, false));
+  return launch_single_gemm<256, kGateUpStages, EPI_GATE_UP>(pl, dev, tmX, tmWg, tmWu, tmY, p,
+                                                             stream);
 }
 
 int gemm_get_device_status(void* stream, int* site) {
@@ -976,7 +1056,8 @@ int gemm_get_device_status(void* stream, int* site) {
     // non-zero; clear them so that later calls start from a clean state.
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState& d = g_dev[dev];
-    if (d.counters != nullptr && cudaMemset(d.counters, 0, d.counter_count * sizeof(int)) != cudaSuccess)
+    if (d.counters != nullptr &&
+        cudaMemset(d.counters, 0, d.counter_count * sizeof(int)) != cudaSuccess)
       cudaGetLastError();
   }
   return h[0];
@@ -1034,29 +1115,15 @@ std::mutex g_noalloc_mu;
 unsigned char* g_noalloc_base[kMaxDevices];  // device address of the array, per device
 bool g_noalloc_smem_set[kMaxDevices];
 
-// Encodes a 2-D map straight into *out (no descriptor cache, no allocation).
-int encode_map_2d_direct(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype,
-                         uint64_t inner, uint64_t outer, uint64_t pitch, uint32_t box_inner,
-                         uint32_t box_outer) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return GEMM_ERR_CUDA;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {pitch};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estrides[2] = {1, 1};
-  const CUresult r = fn(out, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estrides,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
-}
-
 }  // namespace
 
 extern "C" int gemm_bf16_skinny_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
                                         const void* A, int64_t lda, const void* B, int64_t ldb,
                                         float beta, void* C, int64_t ldc, int out_dtype,
                                         void* stream_) {
-  int st = validate_gemm(M, N, K, A, lda, B, ldb, beta, C, ldc, out_dtype);
+  const Problem q{1, M, N, K, alpha, beta, A, lda, 0, B, ldb, 0, C, ldc, 0, GEMM_IN_BF16,
+                  out_dtype};
+  int st = validate_problem(q);
   if (st != GEMM_OK) return st;
   if (M == 0 || N == 0) return GEMM_OK;
   if (M > kSkinnyMaxM) return GEMM_ERR_INVALID_ARG;
@@ -1070,24 +1137,10 @@ extern "C" int gemm_bf16_skinny_noalloc(int64_t M, int64_t N, int64_t K, float a
     sms = g_dev[dev].sms;
   }
   gemm_plan pl;
-  plan_gemm(M, N, K, sms, &pl);
-  const bool bf16 = out_dtype == GEMM_OUT_BF16;
-  if (pl.kernel == K_SCALE) return run_scale(pl, C, ldc, M, N, beta, bf16, stream);
+  plan_gemm(1, M, N, K, sms, &pl);
+  if (pl.kernel == K_SCALE) return run_scale(pl, C, ldc, 0, 1, M, N, beta, out_dtype, stream);
 
-  SkinnyParams p;
-  p.M = static_cast<int>(M);
-  p.N = static_cast<int>(N);
-  p.K = static_cast<int>(K);
-  p.n_blocks = static_cast<int>(ceil_div(N, kSkinnyRows));
-  p.k_blocks = static_cast<int>(ceil_div(K, kBK));
-  p.splits = pl.split_k;
-  p.kb_per_split = static_cast<int>(ceil_div(p.k_blocks, p.splits));
-  p.num_units = static_cast<int>(pl.tiles);
-  p.alpha = alpha;
-  p.beta = beta;
-  p.C = C;
-  p.ldc = ldc;
-  p.out_bf16 = bf16 ? 1 : 0;
+  SkinnyParams p = skinny_params(pl, q);
   const size_t counter_bytes =
       (static_cast<size_t>(p.n_blocks) * 4 * sizeof(int) + 255) & ~static_cast<size_t>(255);
   const size_t partial_bytes =
@@ -1122,12 +1175,15 @@ extern "C" int gemm_bf16_skinny_noalloc(int64_t M, int64_t N, int64_t K, float a
   p.counters = reinterpret_cast<int*>(base);
   p.ws = reinterpret_cast<float*>(base + counter_bytes);
 
+  // Descriptors encoded straight into the parameter block (no cache, no allocation).
   CUtensorMap tmW, tmX;
-  if ((st = encode_map_2d_direct(&tmW, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, ldb * 2, kBK,
-                                 kSkinnyRows)) != GEMM_OK)
+  if ((st = encode_map_3d(&tmW, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, 1, ldb * 2,
+                          static_cast<uint64_t>(ldb) * 2 * N, kBK, kSkinnyRows,
+                          CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_OK)
     return st;
-  if ((st = encode_map_2d_direct(&tmX, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, lda * 2, kBK,
-                                 kSkinnyNX)) != GEMM_OK)
+  if ((st = encode_map_3d(&tmX, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, 1, lda * 2,
+                          static_cast<uint64_t>(lda) * 2 * M, kBK, kSkinnyNX,
+                          CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_OK)
     return st;
   // The arrival counters must start at zero; the array keeps whatever the
   // previous call left, so clear them on the stream first.

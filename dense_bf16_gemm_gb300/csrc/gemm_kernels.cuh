@@ -115,10 +115,15 @@ __global__ void wait_timeout_probe_kernel(unsigned long long limit_ns) {
 }
 
 struct TileParams {
-  int M, N, K;
+  int M, N, K;                // sizes of each matrix of the batch
   int m_blocks, n_blocks, k_blocks;
-  int num_tiles;
+  int batch;                  // matrices (the third TMA coordinate)
+  int tiles_per_matrix;       // m_blocks * n_blocks
+  int num_tiles;              // batch * tiles_per_matrix
   int group_m;
+  uint32_t idesc;             // tcgen05 instruction descriptor (BF16 or FP16 operands)
+  int out_f16;                // a 16-bit output is FP16 (else BF16)
+  long long c_stride;         // elements between consecutive matrices of C
   float alpha, beta;
   const void* C;      // read when beta != 0 (same storage as the output)
   long long ldc;      // elements
@@ -168,13 +173,17 @@ __device__ __forceinline__ long long split_index(int col, int q, int lane) {
   return (static_cast<long long>(col >> 5) * 8 + q) * 32 + lane;
 }
 
-// Grouped raster: group_m consecutive row blocks share each column block.
-__device__ __forceinline__ void tile_coords(int tile, const TileParams& p, int& mb, int& nb) {
+// Matrix b of the batch, then a grouped raster inside it: group_m
+// consecutive row blocks share each column block.
+__device__ __forceinline__ void tile_coords(int tile, const TileParams& p, int& b, int& mb,
+                                            int& nb) {
+  b = tile / p.tiles_per_matrix;
+  const int t = tile - b * p.tiles_per_matrix;
   const int span = p.group_m * p.n_blocks;
-  const int g = tile / span;
+  const int g = t / span;
   const int first = g * p.group_m;
   const int rows = min(p.m_blocks - first, p.group_m);
-  const int r = tile - g * span;
+  const int r = t - g * span;
   mb = first + r % rows;
   nb = r / rows;
 }
@@ -194,20 +203,20 @@ struct GemmCfg {
   static constexpr int kOutCols = (EPI == EPI_GATE_UP) ? BN / 2 : BN;
   static constexpr int kAccStride = 256;  // TMEM columns between the two accumulators
   static constexpr int kTmemCols = 512;
-  static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 // The 32 values of C at (row, col0..col0+31) in FP32, zero outside C.  The
 // loads are plain (C is written later by this same CTA's TMA stores).
 template <int EPI>
-__device__ __forceinline__ void load_c_slice(float (&c)[32], const TileParams& p, int row,
+__device__ __forceinline__ void load_c_slice(float (&c)[32], const TileParams& p, int b, int row,
                                              int col0) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) c[i] = 0.0f;
   if (row >= p.M || col0 >= p.N) return;
   if constexpr (EPI == EPI_F32) {
-    const float* src = static_cast<const float*>(p.C) + static_cast<long long>(row) * p.ldc + col0;
+    const float* src = static_cast<const float*>(p.C) + b * p.c_stride +
+                       static_cast<long long>(row) * p.ldc + col0;
     if (col0 + 32 <= p.N) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -223,8 +232,9 @@ __device__ __forceinline__ void load_c_slice(float (&c)[32], const TileParams& p
         if (col0 + i < p.N) c[i] = src[i];
     }
   } else {
-    const uint16_t* src =
-        static_cast<const uint16_t*>(p.C) + static_cast<long long>(row) * p.ldc + col0;
+    const uint16_t* src = static_cast<const uint16_t*>(p.C) + b * p.c_stride +
+                          static_cast<long long>(row) * p.ldc + col0;
+    const bool f16 = p.out_f16 != 0;
     if (col0 + 32 <= p.N) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -232,14 +242,14 @@ __device__ __forceinline__ void load_c_slice(float (&c)[32], const TileParams& p
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          c[8 * q + 2 * j + 0] = bf16_bits_to_float(w[j] & 0xFFFFu);
-          c[8 * q + 2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
+          c[8 * q + 2 * j + 0] = half16_to_float(w[j] & 0xFFFFu, f16);
+          c[8 * q + 2 * j + 1] = half16_to_float(w[j] >> 16, f16);
         }
       }
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        if (col0 + i < p.N) c[i] = bf16_bits_to_float(src[i]);
+        if (col0 + i < p.N) c[i] = half16_to_float(src[i], f16);
     }
   }
 }
@@ -353,8 +363,8 @@ __device__ __forceinline__ uint32_t staging_offset(int row, uint32_t chunk) {
 // box is committed as its own bulk group.
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtensorMap* tmOut,
-                                              uint32_t tacc, int m0, int n0, uint32_t staging,
-                                              int lane, int& sc, bool have_acc,
+                                              uint32_t tacc, int b, int m0, int n0,
+                                              uint32_t staging, int lane, int& sc, bool have_acc,
                                               const SplitCtx& split) {
   constexpr int OUT = (EPI == EPI_GATE_UP) ? BN / 2 : BN;
   using Box = EpiBox<EPI, OUT>;
@@ -364,7 +374,7 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
   // C of the next slice is loaded one slice ahead so its latency overlaps the
   // TMEM load and conversion of the current one.
   float c_next[32];
-  if (read_c) load_c_slice<EPI>(c_next, p, row, n0);
+  if (read_c) load_c_slice<EPI>(c_next, p, b, row, n0);
 #pragma unroll 1
   for (int c0 = 0; c0 < OUT; c0 += Box::kCols) {
     // Boxes wholly outside C are neither computed nor stored (warp-uniform).
@@ -392,7 +402,7 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
 #pragma unroll
           for (int i = 0; i < 32; ++i) c_cur[i] = c_next[i];
           const int next = c0 + 32 * (h + 1);
-          if (next < OUT) load_c_slice<EPI>(c_next, p, row, n0 + next);
+          if (next < OUT) load_c_slice<EPI>(c_next, p, b, row, n0 + next);
         }
         if (have_acc) {
           acc_slice(v, tacc, c0 + 32 * h, lane, split);
@@ -416,19 +426,20 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
                        __float_as_uint(v[4 * q + 0]), __float_as_uint(v[4 * q + 1]),
                        __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
       } else {
+        const bool f16 = p.out_f16 != 0;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           st_shared_v4(stg + staging_offset<Box::kSwizzle128>(lane, static_cast<uint32_t>(4 * h + q)),
-                       pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
-                       pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                       pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                       pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+                       pack_half16x2(v[8 * q + 0], v[8 * q + 1], f16),
+                       pack_half16x2(v[8 * q + 2], v[8 * q + 3], f16),
+                       pack_half16x2(v[8 * q + 4], v[8 * q + 5], f16),
+                       pack_half16x2(v[8 * q + 6], v[8 * q + 7], f16));
       }
     }
     fence_proxy_async_shared();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(tmOut, stg, n0 + c0, m0);
+      tma_store_3d(tmOut, stg, n0 + c0, m0, b);
       bulk_commit_group();
     }
     ++sc;
@@ -439,13 +450,14 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
 // tile (rows m0..m0+31, the tile's columns from n0), box by box.
 template <int BN, int EPI>
 __device__ __forceinline__ void prefetch_c_band(const TileParams& p, const CUtensorMap* tmOut,
-                                                int m0, int n0) {
+                                                int b, int m0, int n0) {
   if constexpr (EPI == EPI_GATE_UP) {
     return;
   } else {
     if (p.beta == 0.0f || m0 >= p.M) return;
     using Box = EpiBox<EPI, BN>;
-    for (int c0 = 0; c0 < BN && n0 + c0 < p.N; c0 += Box::kCols) tma_prefetch_l2_2d(tmOut, n0 + c0, m0);
+    for (int c0 = 0; c0 < BN && n0 + c0 < p.N; c0 += Box::kCols)
+      tma_prefetch_l2_3d(tmOut, n0 + c0, m0, b);
   }
 }
 
@@ -507,8 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        int mb, nb;
-        tile_coords(tile, p, mb, nb);
+        int bt, mb, nb;
+        tile_coords(tile, p, bt, mb, nb);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY)) {
             ok = false;
@@ -517,12 +529,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_dst = sbase + s * Cfg::kStageBytes;
           const uint32_t b_dst = a_dst + Cfg::kABytes;
           mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);
-          tma_load_2d(a_dst, &tmA, full_bar(s), kb * kBK, mb * kBM);
+          tma_load_3d(a_dst, &tmA, full_bar(s), kb * kBK, mb * kBM, bt);
           if constexpr (EPI == EPI_GATE_UP) {
-            tma_load_2d(b_dst, &tmB, full_bar(s), kb * kBK, nb * (BN / 2));
-            tma_load_2d(b_dst + Cfg::kBBytes / 2, &tmB2, full_bar(s), kb * kBK, nb * (BN / 2));
+            tma_load_3d(b_dst, &tmB, full_bar(s), kb * kBK, nb * (BN / 2), bt);
+            tma_load_3d(b_dst + Cfg::kBBytes / 2, &tmB2, full_bar(s), kb * kBK, nb * (BN / 2), bt);
           } else {
-            tma_load_2d(b_dst, &tmB, full_bar(s), kb * kBK, nb * BN);
+            tma_load_3d(b_dst, &tmB, full_bar(s), kb * kBK, nb * BN, bt);
           }
           ++issued;
           if (++s == STAGES) {
@@ -566,8 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < kBK / kUmmaK; ++j) {
             // +32 bytes along K inside the swizzled row = +2 in the address field.
-            umma_bf16(d_tmem, adesc + 2u * j, bdesc + 2u * j, Cfg::kIdesc,
-                      (kb | j) != 0 ? 1u : 0u);
+            umma_bf16(d_tmem, adesc + 2u * j, bdesc + 2u * j, p.idesc, (kb | j) != 0 ? 1u : 0u);
           }
           umma_commit(empty_bar(s));
           if (++s == STAGES) {
@@ -590,19 +601,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     int local = 0;
     int sc = 0;
     if (lane == 0 && blockIdx.x < p.num_tiles) {
-      int mb_, nb_;
-      tile_coords(blockIdx.x, p, mb_, nb_);
-      prefetch_c_band<BN, EPI>(p, &tmOut, mb_ * kBM + band, nb_ * Cfg::kOutCols);
+      int b_, mb_, nb_;
+      tile_coords(blockIdx.x, p, b_, mb_, nb_);
+      prefetch_c_band<BN, EPI>(p, &tmOut, b_, mb_ * kBM + band, nb_ * Cfg::kOutCols);
     }
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
-      int mb, nb;
-      tile_coords(tile, p, mb, nb);
+      int bt, mb, nb;
+      tile_coords(tile, p, bt, mb, nb);
       // C of the next tile of this CTA travels to L2 during this tile's
       // epilogue and the next tile's main loop.
       if (lane == 0 && tile + gridDim.x < p.num_tiles) {
-        int mb_, nb_;
-        tile_coords(tile + gridDim.x, p, mb_, nb_);
-        prefetch_c_band<BN, EPI>(p, &tmOut, mb_ * kBM + band, nb_ * Cfg::kOutCols);
+        int b_, mb_, nb_;
+        tile_coords(tile + gridDim.x, p, b_, mb_, nb_);
+        prefetch_c_band<BN, EPI>(p, &tmOut, b_, mb_ * kBM + band, nb_ * Cfg::kOutCols);
       }
       const int buf = local & 1;
       const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
@@ -614,7 +625,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m0 = mb * kBM + band;
       const int n0 = nb * Cfg::kOutCols;
       const SplitCtx whole{1, 0, nullptr, 0};
-      epilogue_tile<BN, EPI>(p, &tmOut, tacc, m0, n0, staging, lane, sc, p.k_blocks > 0, whole);
+      epilogue_tile<BN, EPI>(p, &tmOut, tacc, bt, m0, n0, staging, lane, sc, p.k_blocks > 0,
+                             whole);
       // The accumulator may be overwritten once every lane's TMEM reads are done.
       tc_fence_before_sync();
       __syncwarp();

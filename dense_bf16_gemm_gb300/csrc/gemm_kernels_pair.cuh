@@ -43,7 +43,6 @@ struct PairCfg {
   static constexpr int kOutCols = (EPI == EPI_GATE_UP) ? BN / 2 : BN;
   static constexpr int kAccStride = 256;
   static constexpr int kTmemCols = 512;
-  static constexpr uint32_t kIdesc = idesc_bf16_f32(kPairBM, BN);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -112,8 +111,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = cluster; ok && u < p.num_units; u += nclusters) {
         int tile, kb0, kb1, piece;
         unit_of(u, p, tile, kb0, kb1, piece);
-        int mb, nb;
-        tile_coords(tile, p, mb, nb);
+        int bt, mb, nb;
+        tile_coords(tile, p, bt, mb, nb);
         const int a_row = mb * kPairBM + static_cast<int>(rank) * 128;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY)) {
@@ -124,12 +123,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_dst = a_dst + Cfg::kABytes;
           const uint32_t fbar = full0_even + 8u * s;
           if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * Cfg::kStageBytes);
-          tma_load_2d_pair(a_dst, &tmA, fbar, kb * kBK, a_row);
+          tma_load_3d_pair(a_dst, &tmA, fbar, kb * kBK, a_row, bt);
           if constexpr (EPI == EPI_GATE_UP) {
-            tma_load_2d_pair(b_dst, rank == 0 ? &tmB : &tmB2, fbar, kb * kBK, nb * (BN / 2));
+            tma_load_3d_pair(b_dst, rank == 0 ? &tmB : &tmB2, fbar, kb * kBK, nb * (BN / 2), bt);
           } else {
-            tma_load_2d_pair(b_dst, &tmB, fbar, kb * kBK,
-                             nb * BN + static_cast<int>(rank) * (BN / 2));
+            tma_load_3d_pair(b_dst, &tmB, fbar, kb * kBK,
+                             nb * BN + static_cast<int>(rank) * (BN / 2), bt);
           }
           ++issued;
           if (++s == STAGES) {
@@ -173,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bdesc = smem_desc_sw128(a_addr + Cfg::kABytes);
 #pragma unroll
           for (int j = 0; j < kBK / kUmmaK; ++j)
-            umma_bf16_pair(d_tmem, adesc + 2u * j, bdesc + 2u * j, Cfg::kIdesc,
+            umma_bf16_pair(d_tmem, adesc + 2u * j, bdesc + 2u * j, p.idesc,
                            (kb != kb0 || j != 0) ? 1u : 0u);
           umma_commit_pair_multicast(empty_bar(s), 0x3);
           if (++s == STAGES) {
@@ -198,10 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int sc = 0;
     auto prefetch_unit = [&](int u) {
       if (u < p.num_units) {
-        int tile_, kb0_, kb1_, piece_, mb_, nb_;
+        int tile_, kb0_, kb1_, piece_, b_, mb_, nb_;
         unit_of(u, p, tile_, kb0_, kb1_, piece_);
-        tile_coords(tile_, p, mb_, nb_);
-        prefetch_c_band<BN, EPI>(p, &tmOut, mb_ * kPairBM + static_cast<int>(rank) * 128 + band,
+        tile_coords(tile_, p, b_, mb_, nb_);
+        prefetch_c_band<BN, EPI>(p, &tmOut, b_,
+                                 mb_ * kPairBM + static_cast<int>(rank) * 128 + band,
                                  nb_ * Cfg::kOutCols);
       }
     };
@@ -209,8 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = cluster; u < p.num_units; u += nclusters, ++local) {
       int tile, kb0, kb1, piece;
       unit_of(u, p, tile, kb0, kb1, piece);
-      int mb, nb;
-      tile_coords(tile, p, mb, nb);
+      int bt, mb, nb;
+      tile_coords(tile, p, bt, mb, nb);
       // C of this CTA's next unit travels to L2 during this unit's epilogue
       // and the next unit's main loop.
       if (lane == 0) prefetch_unit(u + nclusters);
@@ -240,7 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         store = publish_partial(tacc, BN, lane, split, p.counters + tail * 8 + band_id,
                                 p.tail_split);
       }
-      if (store) epilogue_tile<BN, EPI>(p, &tmOut, tacc, m0, n0, staging, lane, sc, kb1 > kb0, split);
+      if (store)
+        epilogue_tile<BN, EPI>(p, &tmOut, tacc, bt, m0, n0, staging, lane, sc, kb1 > kb0, split);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acce0_even + 8u * buf);

@@ -25,16 +25,19 @@ constexpr int kSkinnyRows = 128;  // rows of B per unit (the MMA's M)
 constexpr int kSkinnyNX = 16;     // activation rows per MMA (the MMA's N)
 
 struct SkinnyParams {
-  int M, N, K;
+  int M, N, K;                // sizes of each matrix of the batch
   int n_blocks, k_blocks;
   int splits, kb_per_split;
-  int num_units;
+  int batch;
+  int num_units;              // batch * splits * n_blocks
   float alpha, beta;
   void* C;
   long long ldc;
-  int out_bf16;
-  float* ws;      // [splits][M][N] FP32 partial sums (splits > 1)
-  int* counters;  // [n_blocks * 4] arrival counters, zero between calls
+  long long c_stride;         // elements between consecutive matrices of C
+  int out_kind;               // 0 FP32, 1 BF16, 2 FP16
+  uint32_t idesc;             // tcgen05 instruction descriptor (BF16 or FP16 operands)
+  float* ws;      // [batch][splits][M][N] FP32 partial sums (splits > 1)
+  int* counters;  // [batch][n_blocks][4] arrival counters, zero between calls
 };
 
 template <int STAGES>
@@ -49,30 +52,33 @@ struct SkinnyCfg {
   static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
   static constexpr int kAccStride = kSkinnyNX;
   static constexpr int kTmemCols = 32;
-  static constexpr uint32_t kIdesc = idesc_bf16_f32(kSkinnyRows, kSkinnyNX);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ void skinny_unit(int u, const SkinnyParams& p, int& nb, int& sp,
+__device__ __forceinline__ void skinny_unit(int u, const SkinnyParams& p, int& b, int& nb, int& sp,
                                             int& kb0, int& kb1) {
   nb = u % p.n_blocks;
-  sp = u / p.n_blocks;
+  const int r = u / p.n_blocks;
+  sp = r % p.splits;
+  b = r / p.splits;
   kb0 = sp * p.kb_per_split;
   kb1 = min(p.k_blocks, kb0 + p.kb_per_split);
 }
 
-// Writes alpha * acc + beta * c for the M rows of output column n.
-__device__ __forceinline__ void skinny_store(const SkinnyParams& p, int n, const float (&acc)[16]) {
+// Writes alpha * acc + beta * c for the M rows of output column n of matrix b.
+__device__ __forceinline__ void skinny_store(const SkinnyParams& p, int b, int n,
+                                             const float (&acc)[16]) {
   if (n >= p.N) return;
 #pragma unroll
   for (int m = 0; m < kSkinnyNX; ++m) {
     if (m < p.M) {
-      const long long off = static_cast<long long>(m) * p.ldc + n;
+      const long long off = b * p.c_stride + static_cast<long long>(m) * p.ldc + n;
       float v = p.alpha * acc[m];
-      if (p.out_bf16) {
+      if (p.out_kind != 0) {
+        const bool f16 = p.out_kind == 2;
         uint16_t* c = static_cast<uint16_t*>(p.C);
-        if (p.beta != 0.0f) v += p.beta * bf16_bits_to_float(c[off]);
-        c[off] = static_cast<uint16_t>(pack_bf16x2(v, 0.0f) & 0xFFFFu);
+        if (p.beta != 0.0f) v += p.beta * half16_to_float(c[off], f16);
+        c[off] = static_cast<uint16_t>(pack_half16x2(v, 0.0f, f16) & 0xFFFFu);
       } else {
         float* c = static_cast<float*>(p.C);
         if (p.beta != 0.0f) v += p.beta * c[off];
@@ -138,8 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long issued = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        int nb, sp, kb0, kb1;
-        skinny_unit(u, p, nb, sp, kb0, kb1);
+        int bt, nb, sp, kb0, kb1;
+        skinny_unit(u, p, bt, nb, sp, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY)) {
             ok = false;
@@ -147,8 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t w_dst = sbase + s * Cfg::kStageBytes;
           mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);
-          tma_load_2d_hint(w_dst, &tmW, full_bar(s), kb * kBK, nb * kSkinnyRows, stream_policy);
-          tma_load_2d_hint(w_dst + Cfg::kWBytes, &tmX, full_bar(s), kb * kBK, 0, keep_policy);
+          tma_load_3d_hint(w_dst, &tmW, full_bar(s), kb * kBK, nb * kSkinnyRows, bt,
+                           stream_policy);
+          tma_load_3d_hint(w_dst + Cfg::kWBytes, &tmX, full_bar(s), kb * kBK, 0, bt,
+                           keep_policy);
           ++issued;
           if (++s == STAGES) {
             s = 0;
@@ -170,8 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int local = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++local) {
-        int nb, sp, kb0, kb1;
-        skinny_unit(u, p, nb, sp, kb0, kb1);
+        int bt, nb, sp, kb0, kb1;
+        skinny_unit(u, p, bt, nb, sp, kb0, kb1);
         const int buf = local & 1;
         const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
         if (!wait_bounded(acce_bar(buf), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY)) break;
@@ -188,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t xdesc = smem_desc_sw128(w_addr + Cfg::kWBytes);
 #pragma unroll
           for (int j = 0; j < kBK / kUmmaK; ++j)
-            umma_bf16(d_tmem, wdesc + 2u * j, xdesc + 2u * j, Cfg::kIdesc,
+            umma_bf16(d_tmem, wdesc + 2u * j, xdesc + 2u * j, p.idesc,
                       (kb != kb0 || j != 0) ? 1u : 0u);
           umma_commit(empty_bar(s));
           if (++s == STAGES) {
@@ -206,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int band = (warp & 3) * 32;
     int local = 0;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++local) {
-      int nb, sp, kb0, kb1;
-      skinny_unit(u, p, nb, sp, kb0, kb1);
+      int bt, nb, sp, kb0, kb1;
+      skinny_unit(u, p, bt, nb, sp, kb0, kb1);
       const int buf = local & 1;
       const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
       const bool got = wait_bounded(accf_bar(buf), aph, abort_flag, SITE_EPI_ACC_FULL);
@@ -228,19 +236,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const int n = nb * kSkinnyRows + band + lane;
       if (p.splits == 1) {
-        skinny_store(p, n, acc);
+        skinny_store(p, bt, n, acc);
         continue;
       }
+      float* ws_b = p.ws + static_cast<long long>(bt) * p.splits * p.M * p.N;
       // Publish this unit's partial, then count arrivals for this band.
       if (n < p.N) {
 #pragma unroll
         for (int m = 0; m < kSkinnyNX; ++m)
-          if (m < p.M) p.ws[(static_cast<long long>(sp) * p.M + m) * p.N + n] = acc[m];
+          if (m < p.M) ws_b[(static_cast<long long>(sp) * p.M + m) * p.N + n] = acc[m];
       }
       __threadfence();
       __syncwarp();
       int prev = 0;
-      int* counter = p.counters + nb * 4 + (warp & 3);
+      int* counter = p.counters + (static_cast<long long>(bt) * p.n_blocks + nb) * 4 + (warp & 3);
       if (lane == 0) prev = atomicAdd(counter, 1);
       prev = __shfl_sync(0xffffffffu, prev, 0);
       if (prev == p.splits - 1) {
@@ -255,13 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (m < p.M) {
                 const float part =
                     (s == sp) ? acc[m]
-                              : __ldcg(p.ws + (static_cast<long long>(s) * p.M + m) * p.N + n);
+                              : __ldcg(ws_b + (static_cast<long long>(s) * p.M + m) * p.N + n);
                 sum[m] += part;
               }
             }
           }
         }
-        skinny_store(p, n, sum);
+        skinny_store(p, bt, n, sum);
         if (lane == 0) *counter = 0;  // ready for the next call
       }
     }

@@ -50,10 +50,18 @@ enum gemm_status {
     GEMM_ERR_TIMEOUT = 5       /* a kernel's bounded pipeline wait expired (read via gemm_get_device_status) */
 };
 
-/* Output element type of gemm_bf16. */
+/* Output element type. */
 enum gemm_out_dtype {
     GEMM_OUT_F32 = 0,
-    GEMM_OUT_BF16 = 1
+    GEMM_OUT_BF16 = 1,
+    GEMM_OUT_F16 = 2   /* rounded to nearest-even FP16 ("TMEM tiles and transfers",
+                          section "Representation and windows": pack(Float16, f)) */
+};
+
+/* Operand element type of gemm_batched (A and B always share it). */
+enum gemm_in_dtype {
+    GEMM_IN_BF16 = 0,
+    GEMM_IN_F16 = 1
 };
 
 /*
@@ -69,9 +77,9 @@ enum gemm_out_dtype {
  * C, ldc     device matrix of type out_dtype, c(m,n) = C[m*ldc + n],
  *            ldc >= N.  Read only when beta != 0 (with beta == 0 it may hold
  *            NaN or garbage), always written.
- * out_dtype  GEMM_OUT_F32 or GEMM_OUT_BF16.  Accumulation is FP32; a BF16
- *            output is rounded to nearest-even once, from the FP32 value of
- *            alpha*acc + beta*c.
+ * out_dtype  GEMM_OUT_F32, GEMM_OUT_BF16 or GEMM_OUT_F16.  Accumulation is
+ *            FP32; a 16-bit output is rounded to nearest-even once, from the
+ *            FP32 value of alpha*acc + beta*c.
  * stream     cudaStream_t the work is enqueued on.
  *
  * Split K: for M <= 16, and for the tiles of a last, partial wave of the
@@ -89,6 +97,29 @@ GEMM_API int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha,
               const void *B, int64_t ldb,
               float beta, void *C, int64_t ldc,
               int out_dtype, void *stream);
+
+/*
+ * A batch of independent GEMMs: C_b = alpha * A_b.B_b + beta * C_b for
+ * b = 0 .. batch-1 ("TMA and Hopper WGMMA", section "The same storage
+ * contract on both sides": a three-dimensional binding whose third
+ * coordinate selects one matrix of a batch, each bounded separately).
+ *
+ * batch      number of matrices, 0 <= batch < 2^31 (0 does nothing).
+ * M, N, K, lda, ldb, ldc, alpha, beta, out_dtype  as gemm_bf16, per matrix.
+ * stride_a   elements between A_b and A_(b+1), >= M*lda when batch > 1;
+ * stride_b   elements between B_b and B_(b+1), >= N*ldb when batch > 1;
+ * stride_c   elements between C_b and C_(b+1), >= M*ldc when batch > 1;
+ *            (stride * element size) must be a multiple of 16 bytes.
+ *            Ignored when batch == 1.
+ * in_dtype   GEMM_IN_BF16 or GEMM_IN_F16: the type of both A and B.
+ * Rows and columns past a matrix's edges never read or write the next
+ * matrix.  With batch == 1 and GEMM_IN_BF16 this is gemm_bf16.
+ */
+GEMM_API int gemm_batched(int64_t batch, int64_t M, int64_t N, int64_t K, float alpha,
+                          const void *A, int64_t lda, int64_t stride_a,
+                          const void *B, int64_t ldb, int64_t stride_b,
+                          float beta, void *C, int64_t ldc, int64_t stride_c,
+                          int in_dtype, int out_dtype, void *stream);
 
 /*
  * Y = silu(X.Wg) * (X.Wu), elementwise product, silu(t) = t / (1 + exp(-t)).
@@ -189,6 +220,10 @@ typedef struct gemm_plan {
  */
 GEMM_API int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int num_sms,
                    gemm_plan *plan);
+
+/* Plan of gemm_batched(batch, M, N, K, ..., in_dtype, out_dtype, ...), as gemm_bf16_plan. */
+GEMM_API int gemm_batched_plan(int64_t batch, int64_t M, int64_t N, int64_t K, int in_dtype,
+                               int out_dtype, int num_sms, gemm_plan *plan);
 
 /* Plan of gemm_gate_up_silu(M, N, K, ...), as gemm_bf16_plan. */
 GEMM_API int gemm_gate_up_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_plan *plan);

@@ -428,3 +428,96 @@ def test_gate_up_split_k(g, monkeypatch, pieces):
     monkeypatch.setenv("GB3_GEMM_SPLIT_ALL", pieces)
     assert g.gate_up_plan(512, 640, 1024)["split_k"] == int(pieces)
     check_gate_up(g, 512, 640, 1024, seed=52, dist_w=("normal", 1.0 / 32))
+
+
+# ---------------------------------------------------------------------------
+# Batched GEMM (3-D descriptors) and FP16 operands / outputs
+# ---------------------------------------------------------------------------
+def batched_int_inputs(batch, M, N, K, seed, dtype):
+    g_ = torch.Generator().manual_seed(seed)
+    A = torch.randint(-2, 3, (batch, M, K), generator=g_).to(dtype)
+    B = torch.randint(-2, 3, (batch, N, K), generator=g_).to(dtype)
+    C = torch.randint(-3, 4, (batch, M, N), generator=g_).to(torch.float32)
+    return A, B, C
+
+
+def padded(t, rows_pad, cols_pad, fill):
+    """Copy of a (b, r, c) CPU tensor into a CUDA buffer with extra rows and
+    columns per matrix (so strides exceed the extents); returns (view, buffer)."""
+    b, r, c = t.shape
+    buf = torch.full((b, r + rows_pad, c + cols_pad), fill, dtype=t.dtype, device="cuda")
+    buf[:, :r, :c] = t.cuda()
+    return buf[:, :r, :c], buf
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (100, 264, 128), (7, 520, 1000)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_batched_bit_exact_with_padded_strides(g, M, N, K, out_dtype):
+    batch = 3
+    A, B, C = batched_int_inputs(batch, M, N, K, M + N, torch.bfloat16)
+    Cq = C.to(out_dtype)
+    Ad, _ = padded(A, 5, 24, 7.0)     # pad values would show up if rows leaked
+    Bd, _ = padded(B, 3, 8, -5.0)
+    Cd, Cbuf = padded(Cq, 4, 16, 1024.0)
+    g.gemm(Ad, Bd, Cd, alpha=2.0, beta=-0.5)
+    torch.cuda.synchronize()
+    for b in range(batch):
+        ref, _ = oracle.gemm_full(A[b], B[b], alpha=2.0, beta=-0.5, C=Cq[b].to(torch.float32))
+        if out_dtype == torch.float32:
+            assert np.array_equal(to_f64(Cd[b]), ref), b
+        else:
+            assert np.array_equal(bits(Cd[b].cpu()), oracle.round_to_bf16_bits(ref)), b
+    # padding rows and columns of C untouched
+    pad_rows = Cbuf[:, M:, :].float().cpu()
+    pad_cols = Cbuf[:, :, N:].float().cpu()
+    assert torch.all(pad_rows == 1024.0) and torch.all(pad_cols == 1024.0)
+    assert_status_ok(g)
+
+
+def test_batched_plan_counts_every_matrix(g):
+    p1 = g.batched_plan(1, 1024, 1024, 4096)
+    p8 = g.batched_plan(8, 1024, 1024, 4096)
+    assert p8["kernel_name"] == p1["kernel_name"] == "pair"
+    assert p8["tiles"] >= 8 * (1024 // 256) * -(-1024 // p8["tile_n"])
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (64, 264, 136), (5, 1000, 2048)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16, torch.bfloat16])
+def test_f16_operands_bit_exact(g, M, N, K, out_dtype):
+    A, B, C = batched_int_inputs(1, M, N, K, 3 * M + K, torch.float16)
+    A, B, C = A[0], B[0], C[0]
+    Cq = C.to(out_dtype)
+    ref, _ = oracle.gemm_full(A, B, alpha=1.0, beta=0.5, C=Cq.to(torch.float32))
+    out = run_gemm(g, A, B, C=Cq, alpha=1.0, beta=0.5, out_dtype=out_dtype)
+    if out_dtype == torch.float32:
+        assert np.array_equal(to_f64(out), ref)
+    elif out_dtype == torch.float16:
+        assert np.array_equal(bits(out.cpu()), oracle.round_to_f16_bits(ref))
+    else:
+        assert np.array_equal(bits(out.cpu()), oracle.round_to_bf16_bits(ref))
+    assert_status_ok(g)
+
+
+def test_f16_random_inputs_within_tolerance(g):
+    M, N, K = 1000, 1536, 3072
+    gen = torch.Generator().manual_seed(61)
+    A = torch.randn(M, K, generator=gen).to(torch.float16)
+    B = (torch.randn(N, K, generator=gen) / 32).to(torch.float16)
+    out = run_gemm(g, A, B, out_dtype=torch.float16)
+    ref, ab = oracle.gemm_full(A, B)
+    tol = oracle.gemm_tolerance(ref, ab, 1.0, 0.0, out_f16=True)
+    assert_within(to_f64(out), ref, tol, "fp16")
+    assert_status_ok(g)
+
+
+def test_batched_f16_split_pieces(g, monkeypatch):
+    monkeypatch.setenv("GB3_GEMM_SPLIT_ALL", "2")
+    batch, M, N, K = 2, 512, 768, 1024
+    A, B, _ = batched_int_inputs(batch, M, N, K, 62, torch.float16)
+    Cd = torch.empty((batch, M, N), dtype=torch.float32, device="cuda")
+    g.gemm(A.cuda(), B.cuda(), Cd)
+    torch.cuda.synchronize()
+    for b in range(batch):
+        ref, _ = oracle.gemm_full(A[b], B[b])
+        assert np.array_equal(to_f64(Cd[b]), ref), b
+    assert_status_ok(g)
