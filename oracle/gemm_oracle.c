@@ -67,10 +67,24 @@ static double f16_to_double(uint16_t bits)
     return sign ? -v : v;
 }
 
+/* f16_to_double of every bit pattern, filled once (before any parallel
+ * region) so the inner loops look values up instead of calling ldexp. */
+static double f16_values[65536];
+static int f16_values_ready;
+
+static void prepare_decode(int in_f16)
+{
+    if (!in_f16 || f16_values_ready)
+        return;
+    for (uint32_t b = 0; b < 65536u; ++b)
+        f16_values[b] = f16_to_double((uint16_t)b);
+    f16_values_ready = 1;
+}
+
 /* Operand element decoding: in_f16 = 0 for BF16, 1 for FP16. */
 static double to_double(uint16_t bits, int in_f16)
 {
-    return in_f16 ? f16_to_double(bits) : bf16_to_double(bits);
+    return in_f16 ? f16_values[bits] : bf16_to_double(bits);
 }
 
 static void dot_16(int64_t K, const uint16_t *x, const uint16_t *y, int in_f16,
@@ -95,7 +109,7 @@ static void dot_bf16(int64_t K, const uint16_t *x, const uint16_t *y,
 /* Exact value of one 16-bit pattern (for pinning the decoders). */
 double oracle_decode16(uint16_t bits, int in_f16)
 {
-    return to_double(bits, in_f16);
+    return in_f16 ? f16_to_double(bits) : bf16_to_double(bits);
 }
 
 int oracle_num_threads(void)
@@ -120,6 +134,7 @@ void oracle_gemm_entries(int64_t K, double alpha,
                          int64_t count, const int64_t *rows, const int64_t *cols,
                          double *out, double *abs_out, int in_f16)
 {
+    prepare_decode(in_f16);
 #pragma omp parallel for schedule(dynamic, 64)
     for (int64_t i = 0; i < count; ++i) {
         int64_t m = rows[i], n = cols[i];
@@ -144,6 +159,7 @@ void oracle_gemm_full(int64_t M, int64_t N, int64_t K, double alpha,
                       double beta, const float *C, int64_t ldc,
                       double *out, double *abs_out, int in_f16)
 {
+    prepare_decode(in_f16);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t m = 0; m < M; ++m) {
         for (int64_t n = 0; n < N; ++n) {
