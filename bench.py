@@ -185,9 +185,9 @@ def make_device_inputs(w, dev):
         return {"X": X.to(dev), "Wg": Wg.to(dev), "Wu": Wu.to(dev),
                 "Y": torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)}
     A, B, C = workloads.inputs_for(w)
-    out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
-    Cd = C.to(dev, out_dtype) if C is not None else torch.empty((w.M, w.N), dtype=out_dtype,
-                                                                device=dev)
+    shape = (w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N)
+    Cd = C.to(dev, w.out_dtype) if C is not None else torch.empty(shape, dtype=w.out_dtype,
+                                                                  device=dev)
     return {"A": A.to(dev), "B": B.to(dev), "C": Cd}
 
 
@@ -201,7 +201,8 @@ def call(lib, w, t, stream):
 def plan_of(lib, w):
     if w.kind == "gate_up":
         return lib.gate_up_plan(w.M, w.N, w.K)
-    return lib.plan(w.M, w.N, w.K, torch.bfloat16 if w.out_bf16 else torch.float32)
+    return lib.batched_plan(w.batch, w.M, w.N, w.K,
+                            torch.float16 if w.in_f16 else torch.bfloat16, w.out_dtype)
 
 
 def flush_l2(flush):
@@ -243,12 +244,13 @@ def time_e2e(lib, w, steps, warmup, stream, dev):
         out_dtype = torch.bfloat16
     else:
         A, B, C = workloads.inputs_for(w)
-        out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
+        out_dtype = w.out_dtype
         host_in = [A.pin_memory(), B.pin_memory()]
         if C is not None:
             host_in.append(C.to(out_dtype).pin_memory())
     dev_in = [torch.empty_like(h, device=dev) for h in host_in]
-    host_out = torch.empty((w.M, w.N), dtype=out_dtype).pin_memory()
+    host_out = torch.empty((w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N),
+                           dtype=out_dtype).pin_memory()
     h2d = sum(h.numel() * h.element_size() for h in host_in)
     d2h = host_out.numel() * host_out.element_size()
 
@@ -313,7 +315,7 @@ def cpu_baseline(w, target_s=12.0):
             c = np.tile(np.arange(w.N), rows)
             oracle.gate_up_entries(X, Wg, Wu, r, c)
     else:
-        A, B, C = workloads.inputs_for(w)
+        A, B, C = first_matrix(*workloads.inputs_for(w))
 
         def run(rows):
             Cs = C[:rows] if C is not None else None
@@ -328,13 +330,27 @@ def cpu_baseline(w, target_s=12.0):
     t0 = time.perf_counter()
     run(rows)
     dt = time.perf_counter() - t0
-    frac = rows / w.M
+    frac = rows / (w.M * w.batch)
     ms_full = dt / frac * 1e3
     value, unit = metric_of(w, ms_full)
     return {"value": round(value, 6), "unit": unit, "cores": oracle.num_threads(),
             "kind": "oracle", "seconds": round(dt, 3),
-            "sample": f"output rows 0..{rows - 1} of {w.M} (all {w.N} columns, K={w.K}); "
-                      f"metric scaled to the full workload by the row fraction"}
+            "sample": f"output rows 0..{rows - 1} of {w.M}{sample_of(w)} (all {w.N} columns, "
+                      f"K={w.K}); metric scaled to the full workload by the row fraction"}
+
+
+SHORT = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
+
+
+def first_matrix(A, B, C):
+    """The first problem of a batched workload (the workload itself otherwise)."""
+    if A.dim() == 3:
+        return A[0], B[0], (C[0] if C is not None else None)
+    return A, B, C
+
+
+def sample_of(w):
+    return f" of matrix 0 of {w.batch}" if w.batch > 1 else ""
 
 
 def run_ours(args):
@@ -416,10 +432,11 @@ def run_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16",
+            "dtype": "f16" if w.in_f16 else "bf16",
             "data": "synthetic (seeded torch.Generator, BF16-rounded)",
-            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
-                       "out_dtype": "bf16" if w.out_bf16 else "f32", "alpha": w.alpha,
+            "config": {"workload": w.name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K,
+                       "in_dtype": "f16" if w.in_f16 else "bf16",
+                       "out_dtype": SHORT[w.out_dtype], "alpha": w.alpha,
                        "beta": w.beta, "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)",
                        "parallelism": f"{world} independent replica(s), no collective",
                        "plan": pl},
@@ -448,7 +465,7 @@ def run_reference(args):
         return
     import oracle
     w = workloads.WORKLOADS[args.workload]
-    A, B, C = workloads.inputs_for(w) if w.kind == "gemm" else (None, None, None)
+    A, B, C = first_matrix(*workloads.inputs_for(w)) if w.kind == "gemm" else (None,) * 3
     if w.kind == "gate_up":
         X, Wg, Wu = workloads.gate_up_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.dist_b)
     rows = 8   # output rows per step: a bounded sample of the workload
@@ -468,10 +485,10 @@ def run_reference(args):
     for _ in range(args.steps):
         step()
     dt = (time.perf_counter() - t0) / args.steps
-    ms_full = dt / (rows / w.M) * 1e3
+    ms_full = dt / (rows / (w.M * w.batch)) * 1e3
     value, unit = metric_of(w, ms_full)
-    sample = (f"output rows 0..{rows - 1} of {w.M} per step (all {w.N} columns, K={w.K}); "
-              f"metric scaled to the full workload by the row fraction")
+    sample = (f"output rows 0..{rows - 1} of {w.M}{sample_of(w)} per step (all {w.N} "
+              f"columns, K={w.K}); metric scaled to the full workload by the row fraction")
     line = {
         "impl": "reference",
         "metric": "BF16 GEMM TFLOP/s & % of GB300 dense peak; GB/s & % of HBM for M=16 skinny",
@@ -479,7 +496,7 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded torch.Generator, BF16-rounded)",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K},
+        "config": {"workload": w.name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K},
         "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,

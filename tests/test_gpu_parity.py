@@ -150,6 +150,39 @@ def test_workload_skinny(g):
     check_gemm_workload(g, w, rows, cols)
 
 
+@pytest.mark.slow
+def test_workload_gemm_4096_f16(g):
+    """FP16 operands and output at full size: sampled entries plus every edge band."""
+    w = workloads.WORKLOADS["gemm_4096_f16"]
+    A, B, _ = workloads.inputs_for(w)
+    C = torch.full((w.M, w.N), float("nan"), dtype=torch.float16, device="cuda")
+    g.gemm(A.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    rows, cols = workloads.sample_entries(w.M, w.N, w.seed)
+    ref, ab = oracle.gemm_entries(A, B, rows, cols)
+    tol = oracle.gemm_tolerance(ref, ab, 1.0, 0.0, out_f16=True)
+    assert_within(to_f64(C)[rows, cols], ref, tol, w.name)
+    assert_status_ok(g)
+
+
+@pytest.mark.slow
+def test_workload_gemm_batched(g):
+    """Eight 2048^3 problems in one call: sampled entries plus edge bands of
+    every matrix, each against the oracle on its own operands."""
+    w = workloads.WORKLOADS["gemm_batched_8x2048"]
+    A, B, _ = workloads.inputs_for(w)
+    C = torch.full((w.batch, w.M, w.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    g.gemm(A.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    got = to_f64(C)
+    for b in range(w.batch):
+        rows, cols = workloads.sample_entries(w.M, w.N, w.seed + b, count=16384, edge=128)
+        ref, ab = oracle.gemm_entries(A[b], B[b], rows, cols)
+        tol = oracle.gemm_tolerance(ref, ab, 1.0, 0.0, out_bf16=True)
+        assert_within(got[b][rows, cols], ref, tol, f"{w.name}[{b}]")
+    assert_status_ok(g)
+
+
 def check_gate_up(g, M, N, K, seed, dist_w, rows=None, cols=None):
     X, Wg, Wu = workloads.gate_up_inputs(M, N, K, seed, ("normal", 1.0), dist_w)
     Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")

@@ -41,11 +41,20 @@ class Workload:
     out_bf16: bool = False
     check: str = "full"       # "full" or "sampled"
     notes: str = ""
+    batch: int = 1            # independent matrices (gemm only)
+    in_f16: bool = False      # FP16 operands instead of BF16
+    out_f16: bool = False     # FP16 output
+
+    @property
+    def out_dtype(self):
+        if self.out_f16:
+            return torch.float16
+        return torch.bfloat16 if self.out_bf16 else torch.float32
 
     @property
     def flops(self) -> float:
         """Useful floating-point operations: 2MNK per GEMM (two for gate/up)."""
-        per = 2.0 * self.M * self.N * self.K
+        per = 2.0 * self.M * self.N * self.K * self.batch
         return 2.0 * per if self.kind == "gate_up" else per
 
     @property
@@ -54,11 +63,11 @@ class Workload:
         (plus C read when beta != 0)."""
         if self.kind == "gate_up":
             return 2 * (self.M * self.K + 2 * self.N * self.K + self.M * self.N)
-        out_elem = 2 if self.out_bf16 else 4
+        out_elem = 2 if (self.out_bf16 or self.out_f16) else 4
         b = 2 * (self.M * self.K + self.N * self.K) + out_elem * self.M * self.N
         if self.beta != 0.0:
             b += out_elem * self.M * self.N
-        return b
+        return b * self.batch
 
 
 WORKLOADS = {
@@ -85,6 +94,15 @@ WORKLOADS = {
         dist_a=("normal", 1.0), dist_b=("normal", 1.0 / math.sqrt(8192)),
         out_bf16=True, check="sampled",
         notes="decode-shaped, weight 470 MB, HBM-bound"),
+    # Batched and FP16 variants (the next row after the five workloads above).
+    "gemm_4096_f16": Workload(
+        "gemm_4096_f16", "gemm", 4096, 4096, 4096, seed=5,
+        dist_a=("normal", 1.0), dist_b=("normal", 1.0), out_f16=True, in_f16=True,
+        notes="M=N=K=4096, FP16 operands and output"),
+    "gemm_batched_8x2048": Workload(
+        "gemm_batched_8x2048", "gemm", 2048, 2048, 2048, seed=6,
+        dist_a=("normal", 1.0), dist_b=("normal", 1.0), out_bf16=True, batch=8,
+        notes="8 independent 2048^3 BF16 GEMMs, one call"),
 }
 
 # The workload the benchmark times by default.
@@ -103,12 +121,14 @@ def _draw(gen: torch.Generator, shape, dist) -> torch.Tensor:
 
 
 def gemm_inputs(M: int, N: int, K: int, seed: int, dist_a=("uniform",),
-                dist_b=("uniform",), dist_c=None):
-    """CPU tensors ``A`` (M,K) bf16, ``B`` (N,K) bf16 and ``C`` (M,N) f32 or None."""
+                dist_b=("uniform",), dist_c=None, batch: int = 1, dtype=torch.bfloat16):
+    """CPU tensors ``A`` (M,K), ``B`` (N,K) of ``dtype`` (bf16 or f16) and ``C``
+    (M,N) f32 or None; with batch > 1 each gains a leading batch dimension."""
     gen = torch.Generator(device="cpu").manual_seed(int(seed))
-    A = _draw(gen, (M, K), dist_a).to(torch.bfloat16)
-    B = _draw(gen, (N, K), dist_b).to(torch.bfloat16)
-    C = _draw(gen, (M, N), dist_c) if dist_c is not None else None
+    lead = (batch,) if batch > 1 else ()
+    A = _draw(gen, lead + (M, K), dist_a).to(dtype)
+    B = _draw(gen, lead + (N, K), dist_b).to(dtype)
+    C = _draw(gen, lead + (M, N), dist_c) if dist_c is not None else None
     return A, B, C
 
 
@@ -125,7 +145,8 @@ def gate_up_inputs(M: int, N: int, K: int, seed: int, dist_x=("normal", 1.0),
 def inputs_for(w: Workload):
     if w.kind == "gate_up":
         return gate_up_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.dist_b)
-    return gemm_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.dist_b, w.dist_c)
+    return gemm_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.dist_b, w.dist_c, w.batch,
+                       torch.float16 if w.in_f16 else torch.bfloat16)
 
 
 def sample_entries(M: int, N: int, seed: int, count: int = 65536, edge: int = 256):
