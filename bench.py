@@ -41,8 +41,8 @@ FLUSH_BYTES = 256 << 20
 # DRAM traffic per launch from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`
 # (summarised under profiles/), valid only for the kernel sources it was taken with.
 NCU_TRAFFIC: dict = {
-    # profiles/gemm_pair_bf16_4096.md: 75.04 MB read + 29.95 MB written per launch
-    "gemm_4096_bf16": {"bytes": 104986880, "src_sha": "f94514fd18d78c37"},
+    # profiles/gemm_pair_bf16_4096.md: 75.23 MB read + 29.90 MB written per launch
+    "gemm_4096_bf16": {"bytes": 105130240, "src_sha": "16beb2a2762d052b"},
 }
 
 
