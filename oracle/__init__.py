@@ -25,8 +25,19 @@ Contents
   round-to-nearest-even narrowing ("TMEM tiles and transfers", section
   "Representation and windows": ``pack(BFloat16, f)`` converts FP32 values to
   BF16; the rounding mode is not stated there and is read as nearest-even).
-* ``gemm_tolerance`` / ``gate_up_tolerance``: the admissible distance between a
-  result accumulated in FP32 and the float64 reference.
+* ``rms_norm``: ``y = x * inv * g`` with ``inv = 1/sqrt(mean_k x^2 + eps)``
+  per row ("Tiles and shared memory", section "A complete kernel").
+* ``rmsnorm_gate_up_entries``: the gate/up projection of ``rms_norm(X)``, the
+  normalised activation kept in float64 (the steps on either side of the
+  projection).
+* ``gemm_row_stats``: sum, maximum and minimum along each row of
+  ``alpha * A.B + beta * C`` ("TMEM tiles and transfers", section "Storage and
+  a transfer": a reduction along the second axis of a loaded accumulator;
+  "TMA and Hopper WGMMA", section "WGMMA values and ownership": sum, maximum
+  and minimum along axis 2 of a finished accumulator), over the whole row.
+* ``gemm_tolerance`` / ``gate_up_tolerance`` / ``rms_norm_tolerance`` /
+  ``row_stats_tolerance``: the admissible distance between a result computed
+  in FP32 and the float64 reference.
 
 Every function here is pinned in ``tests/test_oracle.py`` to closed forms,
 identities, brute force on tiny shapes and library routines.
@@ -86,6 +97,13 @@ def _load():
                 _vp, _vp, ctypes.c_int]
             lib.oracle_decode16.restype = _dbl
             lib.oracle_decode16.argtypes = [ctypes.c_uint16, ctypes.c_int]
+            lib.oracle_rms_norm_rows.restype = None
+            lib.oracle_rms_norm_rows.argtypes = [
+                _i64, _vp, _i64, ctypes.c_int, _vp, _dbl, _i64, _vp, _vp, _vp]
+            lib.oracle_gate_up_entries_f64.restype = None
+            lib.oracle_gate_up_entries_f64.argtypes = [
+                _i64, _vp, _i64, _vp, _vp, _i64,
+                _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
             lib.oracle_gate_up_entries.restype = None
             lib.oracle_gate_up_entries.argtypes = [
                 _i64, _vp, _i64, _vp, _vp, _i64,
@@ -226,6 +244,88 @@ def gate_up_entries(X, Wg, Wu, rows, cols):
 
 
 # --------------------------------------------------------------------------
+# row normalisation and the reductions along a row
+# --------------------------------------------------------------------------
+def _norm_input(X):
+    """(array, kind) of a normalisation input: kind 0 FP32, 1 BF16, 2 FP16."""
+    if isinstance(X, np.ndarray):
+        if X.dtype == np.float32:
+            return np.ascontiguousarray(X), 0
+        raise TypeError("numpy inputs to rms_norm are float32")
+    import torch
+    if X.dtype == torch.float32:
+        return np.ascontiguousarray(X.contiguous().numpy()), 0
+    return _as_bits(X), (2 if X.dtype == torch.float16 else 1)
+
+
+def rms_norm(X, G, eps: float, rows=None):
+    """Rows of ``y = x * inv * g``, ``inv = 1/sqrt(sum_k x^2 / D + eps)``.
+
+    ``X`` is (M, D) FP32, BF16 or FP16 (a torch tensor, or float32 numpy);
+    ``G`` holds D FP32 gains.  Returns ``(y, inv)``: float64 arrays of shape
+    (len(rows), D) and (len(rows),); all rows when ``rows`` is None.
+    """
+    x, kind = _norm_input(X)
+    M, D = x.shape
+    g = _as_f32(G).reshape(-1)
+    if g.size != D:
+        raise ValueError("G must hold D gains")
+    r = np.arange(M, dtype=np.int64) if rows is None else \
+        np.ascontiguousarray(rows, dtype=np.int64)
+    if r.size and (r.min() < 0 or r.max() >= M):
+        raise IndexError("row outside X")
+    y = np.empty((r.size, D), np.float64)
+    inv = np.empty(r.size, np.float64)
+    _load().oracle_rms_norm_rows(D, _ptr(x), D, kind, _ptr(g), float(eps), r.size, _ptr(r),
+                                 _ptr(y), _ptr(inv))
+    return y, inv
+
+
+def rmsnorm_gate_up_entries(X, G, eps: float, Wg, Wu, rows, cols):
+    """Entries of ``silu(Xn.Wg) * (Xn.Wu)`` with ``Xn = rms_norm(X, G, eps)``
+    kept in float64.  Same result dict as :func:`gate_up_entries`."""
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    c_ = np.ascontiguousarray(cols, dtype=np.int64)
+    wg, wu = _as_bits(Wg), _as_bits(Wu)
+    N, K = wg.shape
+    if wu.shape != (N, K) or X.shape[1] != K:
+        raise ValueError("weights must both be (N, K) with K = X's columns")
+    if c_.size and (c_.min() < 0 or c_.max() >= N):
+        raise IndexError("entry outside the result")
+    uniq, xrows = np.unique(r, return_inverse=True)
+    xn, _ = rms_norm(X, G, eps, uniq)
+    xrows = np.ascontiguousarray(xrows, dtype=np.int64)
+    res = {k: np.empty(r.size, np.float64) for k in ("y", "g", "u", "abs_g", "abs_u")}
+    _load().oracle_gate_up_entries_f64(K, _ptr(xn), K, _ptr(wg), _ptr(wu), K,
+                                       r.size, _ptr(xrows), _ptr(c_),
+                                       _ptr(res["y"]), _ptr(res["g"]), _ptr(res["u"]),
+                                       _ptr(res["abs_g"]), _ptr(res["abs_u"]))
+    return res
+
+
+def gemm_row_stats(A, B, rows, alpha=1.0, beta=0.0, C=None, in_f16=None):
+    """Sum, maximum and minimum over n of ``alpha * A.B + beta * C`` for each
+    row in ``rows`` (whole rows, from :func:`gemm_entries`).
+
+    Returns a dict of float64 arrays over ``rows``: ``sum``, ``max``, ``min``,
+    and for the tolerance ``abs_sum`` (the (len(rows), N) array of
+    ``sum_k |a b|``), ``values`` (the (len(rows), N) results) and ``c``
+    (the matching entries of C, or None).
+    """
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    N = B.shape[0]
+    rr = np.repeat(r, N)
+    cc = np.tile(np.arange(N, dtype=np.int64), r.size)
+    v, ab = gemm_entries(A, B, rr, cc, alpha=alpha, beta=beta, C=C, in_f16=in_f16)
+    v = v.reshape(r.size, N)
+    cm = None
+    if beta != 0.0 and C is not None:
+        cm = _as_f32(C)[r].astype(np.float64)
+    return {"sum": v.sum(axis=1), "max": v.max(axis=1), "min": v.min(axis=1),
+            "values": v, "abs_sum": ab.reshape(r.size, N), "c": cm}
+
+
+# --------------------------------------------------------------------------
 # BF16 encoding
 # --------------------------------------------------------------------------
 def bf16_bits_to_f64(bits) -> np.ndarray:
@@ -315,7 +415,7 @@ def gemm_tolerance(ref, abs_sum, alpha, beta, c=None, out_bf16=False, out_f16=Fa
     return tol
 
 
-def gate_up_tolerance(res):
+def gate_up_tolerance(res, rel: float = None):
     """Propagate the accumulation bound through ``silu(g) * u``.
 
     With ``|g' - g| <= e_g`` and ``|u' - u| <= e_u``:
@@ -324,9 +424,73 @@ def gate_up_tolerance(res):
     arithmetic (exp, divide, multiply) and the BF16 half-ulp the final
     rounding.
     """
+    rel = REL_ACC if rel is None else rel
     g, u, y = res["g"], res["u"], res["y"]
-    e_g = REL_ACC * res["abs_g"]
-    e_u = REL_ACC * res["abs_u"]
+    e_g = rel * res["abs_g"]
+    e_u = rel * res["abs_u"]
     sg = np.abs(g / (1.0 + np.exp(-np.clip(g, -700, 700))))
     tol = SILU_LIPSCHITZ * e_g * (np.abs(u) + e_u) + sg * e_u + 1e-5 * np.abs(y)
     return tol + bf16_half_ulp(np.abs(y) + tol)
+
+
+U32 = 2.0 ** -24    # unit roundoff of binary32
+
+
+def rms_norm_rel_error(D: int) -> float:
+    """Relative error bound of ``x * inv * g`` computed in FP32 against the
+    exact value, for a row of D elements.
+
+    The sum of squares is formed by 32 lanes, each adding at most
+    ``ceil(D/32) + 1`` non-negative terms in order, then combined in 5
+    pairwise steps: relative error at most ``gamma_n``, ``n = ceil(D/32) + 6``,
+    ``gamma_n = n u / (1 - n u)``.  Dividing by D, adding eps, the square root
+    and the reciprocal each add one rounding (the root halves the error of its
+    argument), and the two products two more:
+    ``gamma_n / 2 + 6 u`` in all, which this bound rounds up by 1 %.
+    """
+    n = -(-int(D) // 32) + 6
+    gamma = n * U32 / (1.0 - n * U32)
+    return 1.01 * (gamma / 2.0 + 6.0 * U32)
+
+
+def rms_norm_tolerance(y_ref, D: int, out_bf16=False, out_f16=False):
+    """``rms_norm_rel_error(D) |y|`` plus the half-ulp of a 16-bit output."""
+    y = np.abs(np.asarray(y_ref, np.float64))
+    tol = rms_norm_rel_error(D) * y
+    if out_bf16:
+        tol = tol + bf16_half_ulp(y + tol)
+    if out_f16:
+        tol = tol + f16_half_ulp(y + tol)
+    return tol
+
+
+def rmsnorm_gate_up_rel(D: int) -> float:
+    """Relative accumulation factor of the gate/up projection of a BF16-rounded
+    normalised activation.
+
+    The tensor cores take BF16 operands, so the FP32 normalised value
+    ``y (1 + e)``, ``|e| <= rms_norm_rel_error(D)``, is rounded to BF16 (half
+    an ulp, at most ``2**-8`` relative) before the contraction: each operand
+    is within ``d = 2**-8 + e (1 + 2**-8)`` of the exact one, relative.  The
+    products' sum moves by at most ``d sum |xn w|``, and the FP32 accumulation
+    of the perturbed products adds ``REL_ACC (1 + d) sum |xn w|``.
+    """
+    e = rms_norm_rel_error(D)
+    d = 2.0 ** -8 + e * (1.0 + 2.0 ** -8)
+    return REL_ACC * (1.0 + d) + d
+
+
+def row_stats_tolerance(stats, alpha, beta):
+    """Admissible errors of FP32 row sums, maxima and minima.
+
+    Each entry ``v`` of the row is within ``t = gemm_tolerance(...)`` (no
+    output rounding: the reductions see the FP32 values).  The maximum and
+    the minimum move by at most ``max_n t``; the sum by ``sum_n t`` plus the
+    FP32 summation of N terms in any order, ``gamma_N sum_n (|v| + t)``.
+    """
+    v = stats["values"]
+    t = gemm_tolerance(v, stats["abs_sum"], alpha, beta, stats["c"])
+    N = v.shape[1]
+    gamma = N * U32 / (1.0 - N * U32)
+    return {"sum": t.sum(axis=1) + gamma * (np.abs(v) + t).sum(axis=1),
+            "max": t.max(axis=1), "min": t.max(axis=1)}

@@ -24,6 +24,14 @@
  *          projection without defining it; it is read as the SwiGLU form
  *          above, with no bias and no scaling.)
  *
+ *   rms_norm  ss(m) = sum_k x(m,k)^2,  inv(m) = 1 / sqrt(ss(m)/D + eps),
+ *             y(m,k) = x(m,k) * inv(m) * g(k)
+ *          ("Tiles and shared memory", section "A complete kernel": a row
+ *          normalisation that sums the squares of each row, scales the row by
+ *          the inverse root of their mean plus a small constant, then by a
+ *          per-column gain).  The normalised activation then feeds the gate/up
+ *          projection in oracle_gate_up_entries_f64.
+ *
  * Operands are BF16 or, for the FP16 variant, IEEE binary16 ("TMEM tiles and
  * transfers", section "Representation and windows": FP16 values packed with
  * pack(Float16, f)); the GEMM functions take the operand type as in_f16.
@@ -200,6 +208,75 @@ void oracle_gate_up_entries(int64_t K,
         double g, ag, u, au;
         dot_bf16(K, X + m * ldx, Wg + n * ldw, &g, &ag);
         dot_bf16(K, X + m * ldx, Wu + n * ldw, &u, &au);
+        y[i] = oracle_silu(g) * u;
+        if (g_out) g_out[i] = g;
+        if (u_out) u_out[i] = u;
+        if (abs_g) abs_g[i] = ag;
+        if (abs_u) abs_u[i] = au;
+    }
+}
+
+/* One element of a normalisation input: x_kind 0 FP32, 1 BF16, 2 FP16. */
+static double norm_input(const void *X, int64_t idx, int x_kind)
+{
+    if (x_kind == 0)
+        return (double)((const float *)X)[idx];
+    return x_kind == 1 ? bf16_to_double(((const uint16_t *)X)[idx])
+                       : f16_values[((const uint16_t *)X)[idx]];
+}
+
+/*
+ * Rows rows[i] of rms_norm(X) for i = 0 .. count-1: X(m,k) at X[m*ldx + k]
+ * of kind x_kind, k = 0 .. D-1; G(k) FP32.  out[i*D + k] receives y and
+ * inv_out[i] (if not NULL) receives inv.  The sum of squares is one running
+ * double over k in order; sqrt and the divisions are double.
+ */
+void oracle_rms_norm_rows(int64_t D, const void *X, int64_t ldx, int x_kind,
+                          const float *G, double eps, int64_t count,
+                          const int64_t *rows, double *out, double *inv_out)
+{
+    prepare_decode(x_kind == 2);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t i = 0; i < count; ++i) {
+        const int64_t base = rows[i] * ldx;
+        double ss = 0.0;
+        for (int64_t k = 0; k < D; ++k) {
+            double x = norm_input(X, base + k, x_kind);
+            ss += x * x;
+        }
+        double inv = 1.0 / sqrt(ss / (double)D + eps);
+        for (int64_t k = 0; k < D; ++k)
+            out[i * D + k] = norm_input(X, base + k, x_kind) * inv * (double)G[k];
+        if (inv_out)
+            inv_out[i] = inv;
+    }
+}
+
+/*
+ * Entries of the gate/up projection whose activation is given in double:
+ * row xrows[i] of Xd (at Xd[xrows[i]*ldx]) against weight column cols[i]
+ * (Wg(k,n) at Wg[n*ldw + k], Wu likewise, BF16).  Same outputs as
+ * oracle_gate_up_entries.
+ */
+void oracle_gate_up_entries_f64(int64_t K, const double *Xd, int64_t ldx,
+                                const uint16_t *Wg, const uint16_t *Wu, int64_t ldw,
+                                int64_t count, const int64_t *xrows, const int64_t *cols,
+                                double *y, double *g_out, double *u_out,
+                                double *abs_g, double *abs_u)
+{
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < count; ++i) {
+        const double *x = Xd + xrows[i] * ldx;
+        const uint16_t *wg = Wg + cols[i] * ldw, *wu = Wu + cols[i] * ldw;
+        double g = 0.0, ag = 0.0, u = 0.0, au = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double pg = x[k] * bf16_to_double(wg[k]);
+            double pu = x[k] * bf16_to_double(wu[k]);
+            g += pg;
+            ag += fabs(pg);
+            u += pu;
+            au += fabs(pu);
+        }
         y[i] = oracle_silu(g) * u;
         if (g_out) g_out[i] = g;
         if (u_out) u_out[i] = u;

@@ -333,3 +333,179 @@ def test_f16_operands_match_bruteforce_and_numpy():
     assert not np.allclose(vb, v)
     ve, _ = oracle.gemm_entries(A, B, [0, 6], [4, 0])
     assert np.array_equal(ve, v[[0, 6], [4, 0]])
+
+
+# ---------------------------------------------------------------------------
+# Row normalisation ("Tiles and shared memory", section "A complete kernel")
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("c,eps", [(3.0, 1e-6), (1e-4, 1e-6), (3.0, 0.5), (-2.5, 0.0)])
+def test_rms_norm_constant_row_closed_form(c, eps):
+    """A row of D equal values c: mean square c^2, so y_k = c g_k / sqrt(c^2 + eps)."""
+    D = 48
+    X = np.full((2, D), c, np.float32)
+    G = (np.arange(D) % 7 + 1).astype(np.float32) / 4.0
+    y, inv = oracle.rms_norm(X, G, eps)
+    c32 = float(np.float32(c))
+    want_inv = 1.0 / math.sqrt(c32 * c32 + eps)
+    assert np.allclose(inv, want_inv, rtol=1e-15, atol=0)
+    assert np.allclose(y, c32 * want_inv * G.astype(np.float64), rtol=1e-15, atol=0)
+
+
+def test_rms_norm_one_hot_row():
+    """Only x_j = c is nonzero: the mean square is c^2 / D (a sum of |x| or a
+    divisor other than D would give another value)."""
+    D, j, c, eps = 64, 11, 3.0, 1e-6
+    X = np.zeros((1, D), np.float32)
+    X[0, j] = c
+    G = np.linspace(0.5, 2.0, D).astype(np.float32)
+    y, inv = oracle.rms_norm(X, G, eps)
+    want = c / math.sqrt(c * c / D + eps) * float(G[j])
+    assert math.isclose(y[0, j], want, rel_tol=1e-15)
+    assert np.count_nonzero(y) == 1
+
+
+def test_rms_norm_has_unit_rms_without_eps():
+    """With unit gains and eps = 0 every output row has mean square exactly 1
+    (up to float64 rounding)."""
+    X = torch.randn(20, 333, generator=torch.Generator().manual_seed(5)) * 7.0
+    y, _ = oracle.rms_norm(X, np.ones(333, np.float32), 0.0)
+    assert np.allclose((y * y).mean(axis=1), 1.0, rtol=1e-13, atol=0)
+
+
+@pytest.mark.parametrize("j", [-3, 1, 5])
+def test_rms_norm_power_of_two_scale_invariance(j):
+    """Scaling a row by 2^j scales its root mean square by 2^j exactly, so
+    with eps = 0 the result is bit-identical."""
+    X = torch.randn(6, 96, generator=torch.Generator().manual_seed(6))
+    G = torch.rand(96, generator=torch.Generator().manual_seed(7)) + 0.5
+    y0, _ = oracle.rms_norm(X, G, 0.0)
+    y1, _ = oracle.rms_norm(X * 2.0 ** j, G, 0.0)
+    assert np.array_equal(y0, y1)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_rms_norm_16bit_inputs_equal_their_fp32_widening(dtype):
+    X = torch.randn(9, 200, generator=torch.Generator().manual_seed(8)).to(dtype)
+    G = torch.rand(200, generator=torch.Generator().manual_seed(9)) + 0.5
+    y16, inv16 = oracle.rms_norm(X, G, 1e-6, rows=[0, 4, 8])
+    y32, inv32 = oracle.rms_norm(X.float(), G, 1e-6, rows=[0, 4, 8])
+    assert np.array_equal(y16, y32) and np.array_equal(inv16, inv32)
+
+
+def _fp32_lane_rms_norm(x64, g, eps):
+    """The normalisation evaluated in binary32 with 32 lanes each summing
+    every 32nd element in order, then a pairwise combination of the lanes."""
+    x = x64.astype(np.float32)
+    D = x.shape[0]
+    lanes = np.zeros(32, np.float32)
+    for k in range(D):
+        lanes[k % 32] = np.float32(lanes[k % 32] + x[k] * x[k])
+    while lanes.size > 1:
+        lanes = (lanes[: lanes.size // 2] + lanes[lanes.size // 2:]).astype(np.float32)
+    ms = np.float32(lanes[0] / np.float32(D))
+    inv = np.float32(np.float32(1.0) / np.sqrt(np.float32(ms + np.float32(eps))))
+    return (x * inv).astype(np.float32) * g.astype(np.float32)
+
+
+def test_rms_norm_tolerance_covers_fp32_evaluation():
+    D = 4096
+    gen = torch.Generator().manual_seed(10)
+    X = (torch.randn(8, D, generator=gen) * torch.rand(8, 1, generator=gen) * 50).to(torch.bfloat16)
+    G = (torch.rand(D, generator=gen) + 0.5).numpy().astype(np.float32)
+    y, _ = oracle.rms_norm(X, G, 1e-6)
+    tol = oracle.rms_norm_tolerance(y, D)
+    xf = X.float().numpy().astype(np.float64)
+    for r in range(8):
+        y32 = _fp32_lane_rms_norm(xf[r], G, 1e-6).astype(np.float64)
+        assert np.all(np.abs(y32 - y[r]) <= tol[r])
+        # and the BF16-rounded operand stays within the gate/up perturbation bound
+        yb = oracle.bf16_bits_to_f64(oracle.round_to_bf16_bits(y32))
+        d = oracle.rmsnorm_gate_up_rel(D) - oracle.REL_ACC * (1 + 2.0 ** -8)
+        assert np.all(np.abs(yb - y[r]) <= d * np.abs(y[r]) + 1e-300)
+
+
+def test_rmsnorm_gate_up_reduces_to_gate_up_on_exact_rows():
+    """Rows of +-2 have root mean square 2, so with eps = 0 and power-of-two
+    gains the normalised row is +-g exactly and BF16; the projection must then
+    equal the plain gate/up oracle on that row."""
+    M, N, K = 6, 40, 96
+    gen = torch.Generator().manual_seed(11)
+    sign = torch.where(torch.rand(M, K, generator=gen) < 0.5, -1.0, 1.0)
+    X = (2.0 * sign).to(torch.bfloat16)
+    G = 2.0 ** torch.randint(-1, 3, (K,), generator=gen).float()
+    Wg = torch.randn(N, K, generator=gen).to(torch.bfloat16)
+    Wu = torch.randn(N, K, generator=gen).to(torch.bfloat16)
+    Xn = (sign * G).to(torch.bfloat16)
+    rows = np.repeat(np.arange(M), N)
+    cols = np.tile(np.arange(N), M)
+    a = oracle.rmsnorm_gate_up_entries(X, G, 0.0, Wg, Wu, rows, cols)
+    b = oracle.gate_up_entries(Xn, Wg, Wu, rows, cols)
+    for k in ("y", "g", "u", "abs_g", "abs_u"):
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_rmsnorm_gate_up_against_numpy_composition():
+    M, N, K = 5, 33, 128
+    gen = torch.Generator().manual_seed(12)
+    X = torch.randn(M, K, generator=gen).to(torch.bfloat16)
+    G = torch.rand(K, generator=gen) + 0.5
+    Wg = (torch.randn(N, K, generator=gen) / 8).to(torch.bfloat16)
+    Wu = (torch.randn(N, K, generator=gen) / 8).to(torch.bfloat16)
+    x = X.double().numpy()
+    xn = x / np.sqrt((x * x).mean(axis=1, keepdims=True) + 1e-6) * G.double().numpy()
+    g = xn @ Wg.double().numpy().T
+    u = xn @ Wu.double().numpy().T
+    y = g / (1.0 + np.exp(-g)) * u
+    rows = np.repeat(np.arange(M), N)
+    cols = np.tile(np.arange(N), M)
+    res = oracle.rmsnorm_gate_up_entries(X, G, 1e-6, Wg, Wu, rows, cols)
+    assert np.allclose(res["y"], y.ravel(), rtol=1e-12, atol=1e-14)
+    assert np.allclose(res["abs_g"], (np.abs(xn) @ np.abs(Wg.double().numpy()).T).ravel(),
+                       rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Reductions along a row of the GEMM result
+# ---------------------------------------------------------------------------
+def test_row_stats_of_ones_product():
+    M, N, K, alpha = 3, 10, 12, -0.5
+    A = np.full((M, K), ONE_BF16, np.uint16)
+    B = np.full((N, K), ONE_BF16, np.uint16)
+    s = oracle.gemm_row_stats(A, B, np.arange(M), alpha=alpha)
+    assert np.all(s["sum"] == N * K * alpha)
+    assert np.all(s["max"] == K * alpha) and np.all(s["min"] == K * alpha)
+
+
+def test_row_stats_of_identity_product_are_the_rows_of_A():
+    M, K = 7, 24
+    A = torch.randn(M, K, generator=torch.Generator().manual_seed(13)).to(torch.bfloat16)
+    I = torch.eye(K).to(torch.bfloat16)
+    s = oracle.gemm_row_stats(A, I, np.arange(M))
+    a = A.double().numpy()
+    assert np.array_equal(s["max"], a.max(axis=1)) and np.array_equal(s["min"], a.min(axis=1))
+    assert np.allclose(s["sum"], a.sum(axis=1), rtol=1e-15, atol=1e-15)
+
+
+def test_row_stats_against_numpy_with_beta():
+    M, N, K = 9, 31, 70
+    A, B, C = rand_inputs(M, N, K, seed=14)
+    rows = np.array([0, 3, 8])
+    s = oracle.gemm_row_stats(A, B, rows, alpha=0.5, beta=2.0, C=C)
+    v = 0.5 * (A.double().numpy() @ B.double().numpy().T) + 2.0 * C.double().numpy()
+    v = v[rows]
+    assert np.allclose(s["sum"], v.sum(axis=1), rtol=1e-13, atol=1e-12)
+    assert np.allclose(s["max"], v.max(axis=1), rtol=1e-14)
+    assert np.allclose(s["min"], v.min(axis=1), rtol=1e-14)
+
+
+def test_row_stats_tolerance_flags_a_planted_error():
+    M, N, K = 4, 50, 64
+    A, B, _ = rand_inputs(M, N, K, seed=15)
+    s = oracle.gemm_row_stats(A, B, np.arange(M))
+    tol = oracle.row_stats_tolerance(s, 1.0, 0.0)
+    for k in ("sum", "max", "min"):
+        assert np.all(tol[k] > 0)
+        assert not np.any(np.abs((s[k] + 2 * tol[k]) - s[k]) <= tol[k])
+    # FP32 evaluation of the same sums stays inside the bound
+    v32 = s["values"].astype(np.float32)
+    assert np.all(np.abs(v32.sum(axis=1, dtype=np.float32) - s["sum"]) <= tol["sum"])
