@@ -179,30 +179,74 @@ def max_over_ranks(pg, x: float) -> float:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def make_device_inputs(w, dev):
+def host_inputs(w):
+    """The workload's seeded CPU tensors, by name."""
     if w.kind == "gate_up":
         X, Wg, Wu = workloads.gate_up_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.dist_b)
-        return {"X": X.to(dev), "Wg": Wg.to(dev), "Wu": Wu.to(dev),
-                "Y": torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)}
+        return {"X": X, "Wg": Wg, "Wu": Wu}
+    if w.kind == "rms_norm":
+        X, G = workloads.inputs_for(w)
+        return {"X": X, "G": G}
+    if w.kind == "rmsnorm_gate_up":
+        X, G, Wg, Wu = workloads.inputs_for(w)
+        return {"X": X, "G": G, "Wg": Wg, "Wu": Wu}
     A, B, C = workloads.inputs_for(w)
-    shape = (w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N)
-    Cd = C.to(dev, w.out_dtype) if C is not None else torch.empty(shape, dtype=w.out_dtype,
-                                                                  device=dev)
-    return {"A": A.to(dev), "B": B.to(dev), "C": Cd}
+    d = {"A": A, "B": B}
+    if C is not None:
+        d["C"] = C.to(w.out_dtype)
+    return d
+
+
+def out_shape(w):
+    """Shape of the workload's main result."""
+    if w.kind == "rms_norm":
+        return (w.M, w.K)
+    return (w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N)
+
+
+def make_device_inputs(w, dev):
+    t = {k: v.to(dev) for k, v in host_inputs(w).items()}
+    if "C" not in t:
+        t["C"] = torch.empty(out_shape(w), dtype=w.out_dtype, device=dev)
+    if w.kind == "rmsnorm_gate_up":
+        t["Xn"] = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=dev)
+    if w.kind == "gemm_row_stats":
+        lead = (w.batch, w.M) if w.batch > 1 else (w.M,)
+        t["stats"] = [torch.empty(lead, dtype=torch.float32, device=dev) for _ in range(3)]
+    return t
 
 
 def call(lib, w, t, stream):
+    """One step: the workload's library call on device-resident tensors.
+    Returns the main result."""
     if w.kind == "gate_up":
-        lib.gate_up_silu(t["X"], t["Wg"], t["Wu"], t["Y"], stream=stream)
-    else:
-        lib.gemm(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, stream=stream)
+        return lib.gate_up_silu(t["X"], t["Wg"], t["Wu"], t["C"], stream=stream)
+    if w.kind == "rms_norm":
+        return lib.rms_norm(t["X"], t["G"], w.eps, Y=t["C"], stream=stream)
+    if w.kind == "rmsnorm_gate_up":
+        return lib.rmsnorm_gate_up_silu(t["X"], t["G"], w.eps, t["Wg"], t["Wu"], Xn=t["Xn"],
+                                        Y=t["C"], stream=stream)[0]
+    if w.kind == "gemm_row_stats":
+        return lib.gemm_row_stats(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta,
+                                  stream=stream, stats=t["stats"])[0]
+    return lib.gemm(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, stream=stream)
 
 
 def plan_of(lib, w):
     if w.kind == "gate_up":
         return lib.gate_up_plan(w.M, w.N, w.K)
-    return lib.batched_plan(w.batch, w.M, w.N, w.K,
-                            torch.float16 if w.in_f16 else torch.bfloat16, w.out_dtype)
+    if w.kind == "rmsnorm_gate_up":
+        pl = dict(lib.gate_up_plan(w.M, w.N, w.K))
+        pl["launches"] += 1          # the normalisation before the projection
+        pl["kernel_name"] = "rms_norm+" + pl["kernel_name"]
+        return pl
+    if w.kind == "rms_norm":
+        return {"kernel_name": "rms_norm", "tile_n": w.K, "split_k": 1, "grid": None,
+                "launches": 1}
+    in_dt = torch.float16 if w.in_f16 else torch.bfloat16
+    if w.kind == "gemm_row_stats":
+        return lib.row_stats_plan(w.batch, w.M, w.N, w.K, in_dt, w.out_dtype)
+    return lib.batched_plan(w.batch, w.M, w.N, w.K, in_dt, w.out_dtype)
 
 
 def flush_l2(flush):
@@ -238,31 +282,16 @@ def time_device(lib, w, t, steps, warmup, stream, flush, sampler=None):
 
 def time_e2e(lib, w, steps, warmup, stream, dev):
     """Public API end to end: pinned host inputs -> device, call, result -> host."""
-    if w.kind == "gate_up":
-        X, Wg, Wu = workloads.gate_up_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.dist_b)
-        host_in = [X.pin_memory(), Wg.pin_memory(), Wu.pin_memory()]
-        out_dtype = torch.bfloat16
-    else:
-        A, B, C = workloads.inputs_for(w)
-        out_dtype = w.out_dtype
-        host_in = [A.pin_memory(), B.pin_memory()]
-        if C is not None:
-            host_in.append(C.to(out_dtype).pin_memory())
-    dev_in = [torch.empty_like(h, device=dev) for h in host_in]
-    host_out = torch.empty((w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N),
-                           dtype=out_dtype).pin_memory()
-    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    host = {k: v.pin_memory() for k, v in host_inputs(w).items()}
+    dev_t = make_device_inputs(w, dev)
+    host_out = torch.empty(out_shape(w), dtype=w.out_dtype).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for h in host.values())
     d2h = host_out.numel() * host_out.element_size()
 
     def one():
-        for h, d in zip(host_in, dev_in):
-            d.copy_(h, non_blocking=True)
-        if w.kind == "gate_up":
-            out = lib.gate_up_silu(dev_in[0], dev_in[1], dev_in[2], stream=stream)
-        else:
-            Cd = dev_in[2] if len(dev_in) > 2 else None
-            out = lib.gemm(dev_in[0], dev_in[1], Cd, alpha=w.alpha, beta=w.beta,
-                           out_dtype=out_dtype, stream=stream)
+        for k, h in host.items():
+            dev_t[k].copy_(h, non_blocking=True)
+        out = call(lib, w, dev_t, stream)
         host_out.copy_(out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -279,15 +308,21 @@ def time_e2e(lib, w, steps, warmup, stream, dev):
     return t0.elapsed_time(t1) / steps, h2d, d2h
 
 
+def hbm_bound(w) -> bool:
+    """Workloads whose metric is bandwidth: the M=16 decode GEMM and the row
+    normalisation."""
+    return w.name.startswith("skinny") or w.kind == "rms_norm"
+
+
 def metric_of(w, ms):
     """(value, unit) of the workload's metric for a step time in ms."""
-    if w.name.startswith("skinny"):
+    if hbm_bound(w):
         return w.algorithmic_bytes / (ms * 1e-3) / 1e9, "GB/s"
     return w.flops / (ms * 1e-3) / 1e12, "TFLOP/s"
 
 
 def roofline(w, ms, peaks, traffic):
-    if w.name.startswith("skinny"):
+    if hbm_bound(w):
         achieved = w.algorithmic_bytes / (ms * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -303,26 +338,49 @@ def roofline(w, ms, peaks, traffic):
     return out
 
 
+def oracle_rows(w):
+    """A function computing whole output rows 0 .. rows-1 of the workload
+    (of its first matrix when batched) with the oracle, as it stands."""
+    import oracle
+    h = host_inputs(w)
+    if w.kind == "gate_up":
+        def run(rows):
+            r = np.repeat(np.arange(rows), w.N)
+            c = np.tile(np.arange(w.N), rows)
+            oracle.gate_up_entries(h["X"], h["Wg"], h["Wu"], r, c)
+    elif w.kind == "rmsnorm_gate_up":
+        def run(rows):
+            r = np.repeat(np.arange(rows), w.N)
+            c = np.tile(np.arange(w.N), rows)
+            oracle.rmsnorm_gate_up_entries(h["X"], h["G"], w.eps, h["Wg"], h["Wu"], r, c)
+    elif w.kind == "rms_norm":
+        def run(rows):
+            oracle.rms_norm(h["X"], h["G"], w.eps, np.arange(rows))
+    else:
+        A, B, C = first_matrix(h["A"], h["B"], h.get("C"))
+
+        def run(rows):
+            Cs = C[:rows].float() if C is not None else None
+            v, _ = oracle.gemm_full(A[:rows], B, alpha=w.alpha, beta=w.beta, C=Cs)
+            if w.kind == "gemm_row_stats":
+                v.sum(axis=1), v.max(axis=1), v.min(axis=1)
+    return run
+
+
+def sample_text(w, rows):
+    cols = f"all {w.K} columns" if w.kind == "rms_norm" else f"all {w.N} columns, K={w.K}"
+    return (f"output rows 0..{rows - 1} of {w.M}{sample_of(w)} ({cols}); "
+            f"metric scaled to the full workload by the row fraction")
+
+
 def cpu_baseline(w, target_s=12.0):
     """The oracle, as it stands, on a bounded sample of the workload: whole
     rows of the output, sized to take about target_s seconds."""
     import oracle
-    if w.kind == "gate_up":
-        X, Wg, Wu = workloads.gate_up_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.dist_b)
-
-        def run(rows):
-            r = np.repeat(np.arange(rows), w.N)
-            c = np.tile(np.arange(w.N), rows)
-            oracle.gate_up_entries(X, Wg, Wu, r, c)
-    else:
-        A, B, C = first_matrix(*workloads.inputs_for(w))
-
-        def run(rows):
-            Cs = C[:rows] if C is not None else None
-            oracle.gemm_full(A[:rows], B, alpha=w.alpha, beta=w.beta, C=Cs)
+    run = oracle_rows(w)
     rows = 1
     run(rows)                       # threads up, pages touched
-    rows = min(w.M, 32)
+    rows = min(w.M, 32 if w.kind != "rms_norm" else 4096)
     t0 = time.perf_counter()
     run(rows)
     dt = time.perf_counter() - t0
@@ -334,12 +392,23 @@ def cpu_baseline(w, target_s=12.0):
     ms_full = dt / frac * 1e3
     value, unit = metric_of(w, ms_full)
     return {"value": round(value, 6), "unit": unit, "cores": oracle.num_threads(),
-            "kind": "oracle", "seconds": round(dt, 3),
-            "sample": f"output rows 0..{rows - 1} of {w.M}{sample_of(w)} (all {w.N} columns, "
-                      f"K={w.K}); metric scaled to the full workload by the row fraction"}
+            "kind": "oracle", "seconds": round(dt, 3), "sample": sample_text(w, rows)}
 
 
 SHORT = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
+METRIC = "BF16 GEMM TFLOP/s & % of GB300 dense peak; GB/s & % of HBM for M=16 skinny"
+API = {"gemm": "gemm (C ABI gemm_bf16 / gemm_batched)",
+       "gate_up": "gate_up_silu (C ABI gemm_gate_up_silu)",
+       "gemm_row_stats": "gemm_row_stats (C ABI gemm_row_stats)",
+       "rms_norm": "rms_norm (C ABI gemm_rms_norm)",
+       "rmsnorm_gate_up": "rmsnorm_gate_up_silu (C ABI gemm_rmsnorm_gate_up_silu)"}
+
+
+def compute_dtype(w) -> str:
+    """The arithmetic type of the operands the path computes on."""
+    if w.kind == "rms_norm":
+        return w.norm_in
+    return "f16" if w.in_f16 else "bf16"
 
 
 def first_matrix(A, B, C):
@@ -421,7 +490,7 @@ def run_ours(args):
 
     if rank == 0:
         line = {
-            "metric": "BF16 GEMM TFLOP/s & % of GB300 dense peak; GB/s & % of HBM for M=16 skinny",
+            "metric": METRIC,
             "value": round(value, 2),
             "unit": unit,
             "n_gpus": world,
@@ -432,10 +501,10 @@ def run_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f16" if w.in_f16 else "bf16",
+            "dtype": compute_dtype(w),
             "data": "synthetic (seeded torch.Generator, BF16-rounded)",
             "config": {"workload": w.name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K,
-                       "in_dtype": "f16" if w.in_f16 else "bf16",
+                       "in_dtype": compute_dtype(w),
                        "out_dtype": SHORT[w.out_dtype], "alpha": w.alpha,
                        "beta": w.beta, "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)",
                        "parallelism": f"{world} independent replica(s), no collective",
@@ -444,7 +513,7 @@ def run_ours(args):
             "clocks": clocks,
             "e2e": {"value": round(e2e_value, 2), "unit": unit, "ms_per_step": round(e2e_ms, 4),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "api": "dense_bf16_gemm_gb300.gemm (C ABI gemm_bf16) with pinned host copies"},
+                    "api": f"dense_bf16_gemm_gb300.{API[w.kind]} with pinned host copies"},
             "gpu_launches": args.steps * pl["launches"],
             "kernel_src_sha": src_hash,
             "cpu_baseline": cpu,
@@ -465,33 +534,21 @@ def run_reference(args):
         return
     import oracle
     w = workloads.WORKLOADS[args.workload]
-    A, B, C = first_matrix(*workloads.inputs_for(w)) if w.kind == "gemm" else (None,) * 3
-    if w.kind == "gate_up":
-        X, Wg, Wu = workloads.gate_up_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.dist_b)
-    rows = 8   # output rows per step: a bounded sample of the workload
-
-    def step():
-        if w.kind == "gate_up":
-            r = np.repeat(np.arange(rows), w.N)
-            c = np.tile(np.arange(w.N), rows)
-            oracle.gate_up_entries(X, Wg, Wu, r, c)
-        else:
-            oracle.gemm_full(A[:rows], B, alpha=w.alpha, beta=w.beta,
-                             C=C[:rows] if C is not None else None)
-
+    run = oracle_rows(w)
+    # output rows per step: a bounded sample of the workload
+    rows = min(w.M, 8 if w.kind != "rms_norm" else 8192)
     for _ in range(args.warmup):
-        step()
+        run(rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step()
+        run(rows)
     dt = (time.perf_counter() - t0) / args.steps
     ms_full = dt / (rows / (w.M * w.batch)) * 1e3
     value, unit = metric_of(w, ms_full)
-    sample = (f"output rows 0..{rows - 1} of {w.M}{sample_of(w)} per step (all {w.N} "
-              f"columns, K={w.K}); metric scaled to the full workload by the row fraction")
+    sample = sample_text(w, rows).replace("; metric", " per step; metric")
     line = {
         "impl": "reference",
-        "metric": "BF16 GEMM TFLOP/s & % of GB300 dense peak; GB/s & % of HBM for M=16 skinny",
+        "metric": METRIC,
         "value": round(value, 6), "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",

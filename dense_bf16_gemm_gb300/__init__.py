@@ -6,7 +6,10 @@ tensors into that C ABI: PyTorch supplies device memory and streams.
 
     C = alpha * A @ B + beta * C       gemm(A, B, C, alpha, beta)   (2-D or batched 3-D,
                                                                      BF16 or FP16 operands)
+    ... and row sum/max/min of it      gemm_row_stats(A, B, C, alpha, beta)
     Y = silu(X @ Wg) * (X @ Wu)        gate_up_silu(X, Wg, Wu)
+    Y = x / rms(x) * g  (per row)      rms_norm(X, G, eps)
+    Y = gate_up_silu(rms_norm(X), ..)  rmsnorm_gate_up_silu(X, G, eps, Wg, Wu)
 
 Operands are K-contiguous: ``A`` is (M, K) and ``B`` is passed as its (N, K)
 storage, so ``gemm(A, B)`` equals ``A @ B.T`` in torch notation.
@@ -20,8 +23,9 @@ from ._native import (GEMM_ERR_ALIGNMENT, GEMM_ERR_CUDA, GEMM_ERR_INVALID_ARG,  
                       GEMM_ERR_TIMEOUT, GEMM_ERR_UNSUPPORTED, GEMM_IN_BF16, GEMM_IN_F16,
                       GEMM_OK, GEMM_OUT_BF16, GEMM_OUT_F16, GEMM_OUT_F32, GemmError)
 
-__all__ = ["gemm", "gate_up_silu", "device_status", "plan", "batched_plan", "gate_up_plan",
-           "prepare", "GemmError", "library_path"]
+__all__ = ["gemm", "gemm_row_stats", "gate_up_silu", "rms_norm", "rmsnorm_gate_up_silu",
+           "device_status", "plan", "batched_plan", "row_stats_plan", "gate_up_plan", "prepare",
+           "GemmError", "library_path"]
 
 _OUT_CODES = {torch.float32: GEMM_OUT_F32, torch.bfloat16: GEMM_OUT_BF16,
               torch.float16: GEMM_OUT_F16}
@@ -58,16 +62,8 @@ def _bstride(t) -> int:
     return t.stride(0) if t.dim() == 3 else 0
 
 
-def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
-         alpha: float = 1.0, beta: float = 0.0, out_dtype: torch.dtype | None = None,
-         stream: torch.cuda.Stream | None = None) -> torch.Tensor:
-    """``C = alpha * A.B + beta * C`` with FP32 accumulation.
-
-    A: (M, K) or a batch (b, M, K).  B: (N, K) or (b, N, K): the K-contiguous
-    storage of the (K, N) operand.  A and B are both bfloat16 or both float16.
-    C: (M, N) or (b, M, N), float32, bfloat16 or float16; created when None
-    (then ``beta`` must be 0).  Asynchronous on ``stream`` (default: current).
-    """
+def _gemm_operands(A, B, C, beta, out_dtype):
+    """Checks A, B (and C, created when None); returns (C, batched, batch, M, N, K)."""
     _check_operand("A", A, tuple(_IN_CODES), (2, 3))
     _check_operand("B", B, tuple(_IN_CODES), (A.dim(),))
     if B.dtype != A.dtype:
@@ -89,6 +85,20 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
         _check_operand("C", C, tuple(_OUT_CODES), (A.dim(),))
         if tuple(C.shape) != shape:
             raise ValueError(f"C must be {shape}")
+    return C, batched, batch, M, N, K
+
+
+def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
+         alpha: float = 1.0, beta: float = 0.0, out_dtype: torch.dtype | None = None,
+         stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """``C = alpha * A.B + beta * C`` with FP32 accumulation.
+
+    A: (M, K) or a batch (b, M, K).  B: (N, K) or (b, N, K): the K-contiguous
+    storage of the (K, N) operand.  A and B are both bfloat16 or both float16.
+    C: (M, N) or (b, M, N), float32, bfloat16 or float16; created when None
+    (then ``beta`` must be 0).  Asynchronous on ``stream`` (default: current).
+    """
+    C, batched, batch, M, N, K = _gemm_operands(A, B, C, beta, out_dtype)
     code = _OUT_CODES[C.dtype]
     with torch.cuda.device(A.device):
         if not batched and A.dtype == torch.bfloat16:
@@ -103,6 +113,106 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
     if st != GEMM_OK:
         raise GemmError(st, "gemm")
     return C
+
+
+def gemm_row_stats(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
+                   alpha: float = 1.0, beta: float = 0.0, out_dtype: torch.dtype | None = None,
+                   stream: torch.cuda.Stream | None = None, stats=None):
+    """``gemm`` plus the sum, maximum and minimum along each row of the FP32
+    result (before its output rounding).
+
+    Returns ``(C, row_sum, row_max, row_min)``; the three are float32 of
+    shape (M,) or (b, M), created unless ``stats`` gives them (any may be
+    None there: that reduction is not written).
+    """
+    C, batched, batch, M, N, K = _gemm_operands(A, B, C, beta, out_dtype)
+    lead = (batch, M) if batched else (M,)
+    if stats is None:
+        stats = [torch.empty(lead, dtype=torch.float32, device=A.device) for _ in range(3)]
+    stats = list(stats)
+    for t in stats:
+        if t is not None and (not t.is_cuda or t.dtype != torch.float32 or
+                              tuple(t.shape) != lead or not t.is_contiguous()):
+            raise ValueError(f"row statistics must be contiguous CUDA float32 {lead}")
+    with torch.cuda.device(A.device):
+        st = _native.gemm_row_stats(batch, M, N, K, float(alpha), A.data_ptr(), _ld(A),
+                                    _bstride(A), B.data_ptr(), _ld(B), _bstride(B),
+                                    float(beta), C.data_ptr(), _ld(C), _bstride(C),
+                                    _IN_CODES[A.dtype], _OUT_CODES[C.dtype],
+                                    *(t.data_ptr() if t is not None else 0 for t in stats),
+                                    _stream(stream, A.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_row_stats")
+    return (C, *stats)
+
+
+def rms_norm(X: torch.Tensor, G: torch.Tensor, eps: float = 1e-6, Y: torch.Tensor | None = None,
+             out_dtype: torch.dtype | None = None,
+             stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """``Y = X * rsqrt(mean(X^2, dim=1) + eps) * G`` row by row.
+
+    X: (rows, D) float32, bfloat16 or float16; G: (D,) float32; Y: (rows, D)
+    created when None (dtype ``out_dtype``, default X's).  Y may be X itself.
+    """
+    _check_operand("X", X, tuple(_OUT_CODES))
+    rows, D = X.shape
+    if not isinstance(G, torch.Tensor) or not G.is_cuda or G.dtype != torch.float32 or \
+            G.numel() != D or not G.is_contiguous():
+        raise ValueError("G must be a contiguous CUDA float32 tensor of D gains")
+    if Y is None:
+        Y = torch.empty((rows, D), dtype=out_dtype or X.dtype, device=X.device)
+    else:
+        _check_operand("Y", Y, tuple(_OUT_CODES))
+        if tuple(Y.shape) != (rows, D):
+            raise ValueError(f"Y must be ({rows}, {D})")
+    with torch.cuda.device(X.device):
+        st = _native.gemm_rms_norm(rows, D, X.data_ptr(), _ld(X), _OUT_CODES[X.dtype],
+                                   G.data_ptr(), float(eps), Y.data_ptr(), _ld(Y),
+                                   _OUT_CODES[Y.dtype], _stream(stream, X.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_rms_norm")
+    return Y
+
+
+def rmsnorm_gate_up_silu(X: torch.Tensor, G: torch.Tensor, eps: float, Wg: torch.Tensor,
+                         Wu: torch.Tensor, Xn: torch.Tensor | None = None,
+                         Y: torch.Tensor | None = None,
+                         stream: torch.cuda.Stream | None = None):
+    """``Y = silu(Xn.Wg) * (Xn.Wu)`` with ``Xn = rms_norm(X, G, eps)`` (BF16).
+
+    X (M, K) bf16, G (K,) float32, Wg/Wu stored (N, K) bf16.  Returns (Y, Xn);
+    Xn is created when None (it may be X itself for an in-place normalisation).
+    """
+    _check_operand("X", X)
+    _check_operand("Wg", Wg)
+    _check_operand("Wu", Wu)
+    M, K = X.shape
+    N = Wg.shape[0]
+    if tuple(Wg.shape) != (N, K) or tuple(Wu.shape) != (N, K) or Wg.stride(0) != Wu.stride(0):
+        raise ValueError("Wg and Wu must both be (N, K) with one row pitch")
+    if not isinstance(G, torch.Tensor) or not G.is_cuda or G.dtype != torch.float32 or \
+            G.numel() != K or not G.is_contiguous():
+        raise ValueError("G must be a contiguous CUDA float32 tensor of K gains")
+    if Xn is None:
+        Xn = torch.empty((M, K), dtype=torch.bfloat16, device=X.device)
+    else:
+        _check_operand("Xn", Xn)
+        if tuple(Xn.shape) != (M, K):
+            raise ValueError(f"Xn must be ({M}, {K})")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    else:
+        _check_operand("Y", Y)
+        if tuple(Y.shape) != (M, N):
+            raise ValueError(f"Y must be ({M}, {N})")
+    with torch.cuda.device(X.device):
+        st = _native.gemm_rmsnorm_gate_up_silu(M, N, K, X.data_ptr(), _ld(X), G.data_ptr(),
+                                               float(eps), Wg.data_ptr(), Wu.data_ptr(), _ld(Wg),
+                                               Xn.data_ptr(), _ld(Xn), Y.data_ptr(), _ld(Y),
+                                               _stream(stream, X.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_rmsnorm_gate_up_silu")
+    return Y, Xn
 
 
 def gate_up_silu(X: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor,
@@ -165,6 +275,16 @@ def batched_plan(batch: int, M: int, N: int, K: int, in_dtype: torch.dtype = tor
                                       num_sms)
     if st != GEMM_OK:
         raise GemmError(st, "gemm_batched_plan")
+    return p.as_dict()
+
+
+def row_stats_plan(batch: int, M: int, N: int, K: int, in_dtype: torch.dtype = torch.bfloat16,
+                   out_dtype: torch.dtype = torch.bfloat16, num_sms: int = 0) -> dict:
+    """How ``gemm_row_stats`` would run a batch of problems (host-side planning)."""
+    st, p = _native.gemm_row_stats_plan(batch, M, N, K, _IN_CODES[in_dtype],
+                                        _OUT_CODES[out_dtype], num_sms)
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_row_stats_plan")
     return p.as_dict()
 
 

@@ -42,6 +42,10 @@ EXPORTED = (
     "gemm_bf16_skinny_noalloc",
     "gemm_batched",
     "gemm_batched_plan",
+    "gemm_row_stats",
+    "gemm_row_stats_plan",
+    "gemm_rms_norm",
+    "gemm_rmsnorm_gate_up_silu",
 )
 
 
@@ -124,6 +128,19 @@ def lib() -> ctypes.CDLL:
             l.gemm_selftest_wait_timeout.argtypes = [_i64, _vp]
             l.gemm_gate_up_plan.restype = _int
             l.gemm_gate_up_plan.argtypes = [_i64, _i64, _i64, _int, ctypes.POINTER(GemmPlan)]
+            l.gemm_row_stats.restype = _int
+            l.gemm_row_stats.argtypes = [_i64, _i64, _i64, _i64, _f32, _vp, _i64, _i64, _vp,
+                                         _i64, _i64, _f32, _vp, _i64, _i64, _int, _int,
+                                         _vp, _vp, _vp, _vp]
+            l.gemm_row_stats_plan.restype = _int
+            l.gemm_row_stats_plan.argtypes = [_i64, _i64, _i64, _i64, _int, _int, _int,
+                                              ctypes.POINTER(GemmPlan)]
+            l.gemm_rms_norm.restype = _int
+            l.gemm_rms_norm.argtypes = [_i64, _i64, _vp, _i64, _int, _vp, _f32, _vp, _i64,
+                                        _int, _vp]
+            l.gemm_rmsnorm_gate_up_silu.restype = _int
+            l.gemm_rmsnorm_gate_up_silu.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _f32,
+                                                    _vp, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
             _lib = l
     return _lib
 
@@ -188,3 +205,31 @@ def gemm_gate_up_plan(M, N, K, num_sms=0):
     plan = GemmPlan()
     st = lib().gemm_gate_up_plan(M, N, K, num_sms, ctypes.byref(plan))
     return st, plan
+
+
+def gemm_row_stats(batch, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b, beta, C, ldc,
+                   stride_c, in_dtype, out_dtype, row_sum, row_max, row_min, stream) -> int:
+    return lib().gemm_row_stats(batch, M, N, K, alpha, A or None, lda, stride_a, B or None, ldb,
+                                stride_b, beta, C or None, ldc, stride_c, in_dtype, out_dtype,
+                                row_sum or None, row_max or None, row_min or None,
+                                stream or None)
+
+
+def gemm_row_stats_plan(batch, M, N, K, in_dtype=GEMM_IN_BF16, out_dtype=GEMM_OUT_BF16,
+                        num_sms=0):
+    plan = GemmPlan()
+    st = lib().gemm_row_stats_plan(batch, M, N, K, in_dtype, out_dtype, num_sms,
+                                   ctypes.byref(plan))
+    return st, plan
+
+
+def gemm_rms_norm(rows, D, X, ldx, x_dtype, G, eps, Y, ldy, y_dtype, stream) -> int:
+    return lib().gemm_rms_norm(rows, D, X or None, ldx, x_dtype, G or None, eps, Y or None,
+                               ldy, y_dtype, stream or None)
+
+
+def gemm_rmsnorm_gate_up_silu(M, N, K, X, ldx, G, eps, Wg, Wu, ldw, Xn, ldxn, Y, ldy,
+                              stream) -> int:
+    return lib().gemm_rmsnorm_gate_up_silu(M, N, K, X or None, ldx, G or None, eps, Wg or None,
+                                           Wu or None, ldw, Xn or None, ldxn, Y or None, ldy,
+                                           stream or None)

@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libgemm_bf16_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
-SOURCES = ["gemm_api.cu"]
+SOURCES = ["gemm_api.cu", "norm_api.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -50,16 +50,31 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     nvcc = _nvcc()
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64")
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc, ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared",
-           "-Xcompiler", "-fPIC,-fvisibility=hidden",
-           "-cudart", "shared",
-           f"-Xlinker", f"-rpath,{cuda_lib}",
-           "-I", os.path.join(REPO_DIR, "include"),
-           *extra_flags,
-           "-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES]
-    if verbose:
-        print(" ".join(cmd), file=sys.stderr)
-    subprocess.run(cmd, check=True)
+    common = [ARCH, "-O3", "-lineinfo", "-std=c++17",
+              "-Xcompiler", "-fPIC,-fvisibility=hidden",
+              "-I", os.path.join(REPO_DIR, "include"), *extra_flags]
+    # One object per translation unit, compiled in parallel, then one link.
+    objs, procs = [], []
+    for src in SOURCES:
+        obj = os.path.join(BUILD_DIR, src.replace(".cu", f".{os.getpid()}.o"))
+        cmd = [nvcc, *common, "-c", os.path.join(CSRC, src), "-o", obj]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        procs.append(subprocess.Popen(cmd))
+        objs.append(obj)
+    failed = [p.args for p in procs if p.wait() != 0]
+    try:
+        if failed:
+            raise subprocess.CalledProcessError(1, failed[0])
+        link = [nvcc, ARCH, "-shared", "-cudart", "shared",
+                "-Xlinker", f"-rpath,{cuda_lib}", "-o", tmp, *objs]
+        if verbose:
+            print(" ".join(link), file=sys.stderr)
+        subprocess.run(link, check=True)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
 

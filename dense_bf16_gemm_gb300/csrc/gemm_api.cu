@@ -28,6 +28,7 @@
 #include "gemm_kernels.cuh"
 #include "gemm_kernels_pair.cuh"
 #include "gemm_skinny.cuh"
+#include "norm_api.h"
 
 namespace {
 
@@ -78,6 +79,12 @@ struct Problem {
   int64_t ldc, sc;
   int in_dtype;      // gemm_in_dtype
   int out_dtype;     // gemm_out_dtype
+  // Reductions along each row of the result ([batch][M] FP32 each; nullptr:
+  // not wanted).  Any non-null one asks for all three to be computed.
+  float* row_sum = nullptr;
+  float* row_max = nullptr;
+  float* row_min = nullptr;
+  bool stats() const { return row_sum != nullptr || row_max != nullptr || row_min != nullptr; }
 };
 
 int out_elem_bytes(int out_dtype) { return out_dtype == GEMM_OUT_F32 ? 4 : 2; }
@@ -218,7 +225,7 @@ int64_t pair_workspace_bytes(const PairChoice& c) {
 // pair_slots: CTA pairs that fit on the device at once (0: assume sms / 2,
 // negative: pair kernels unavailable).
 int plan_gemm(int64_t batch, int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl,
-              int pair_slots = 0, bool allow_split = true) {
+              int pair_slots = 0, bool allow_split = true, bool row_stats = false) {
   std::memset(pl, 0, sizeof(*pl));
   pl->split_k = 1;
   if (batch == 0 || M == 0 || N == 0) return GEMM_OK;
@@ -226,11 +233,13 @@ int plan_gemm(int64_t batch, int64_t M, int64_t N, int64_t K, int sms, gemm_plan
     pl->kernel = K_SCALE;
     pl->tiles = 1;
     pl->grid = static_cast<int>(std::min<int64_t>(ceil_div(batch * M * N, 256), 4 * sms));
-    pl->launches = 1;
+    pl->launches = row_stats ? 2 : 1;
     return GEMM_OK;
   }
   pl->tile_k = kBK;
-  if (M <= kSkinnyMaxM) {
+  // Row reductions run in the tile epilogues; the swapped-operand M <= 16
+  // kernel holds rows across threads, so those problems take the tiled path.
+  if (M <= kSkinnyMaxM && !row_stats) {
     const int64_t nb = ceil_div(N, kSkinnyRows), kb = ceil_div(K, kBK);
     int s, kbp;
     choose_split(batch * nb, kb, sms, &s, &kbp);
@@ -385,6 +394,11 @@ struct DeviceState {
   size_t ws_bytes = 0;
   int* counters = nullptr;
   size_t counter_count = 0;
+  // row-reduction partials and arrival counters
+  float* stats_ws = nullptr;
+  size_t stats_ws_bytes = 0;
+  int* stats_counters = nullptr;
+  size_t stats_counter_count = 0;
 };
 
 std::mutex g_mu;
@@ -467,6 +481,59 @@ int ensure_workspace(int dev, size_t ws_bytes, size_t counters, cudaStream_t str
     }
     d.counter_count = counters;
   }
+  return GEMM_OK;
+}
+
+// Caller holds g_mu.  Grows one (buffer, counters) pair; refuses to allocate
+// while the stream is being captured.
+int grow_buffers(float** buf, size_t* buf_bytes, int** cnt, size_t* cnt_count, size_t need_bytes,
+                 size_t need_counters, cudaStream_t stream) {
+  if (*buf_bytes >= need_bytes && *cnt_count >= need_counters) return GEMM_OK;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return GEMM_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
+  if (*buf_bytes < need_bytes) {
+    if (*buf) cudaFree(*buf);
+    *buf = nullptr;
+    *buf_bytes = 0;
+    if (cudaMalloc(buf, need_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    *buf_bytes = need_bytes;
+  }
+  if (*cnt_count < need_counters) {
+    if (*cnt) cudaFree(*cnt);
+    *cnt = nullptr;
+    *cnt_count = 0;
+    if (cudaMalloc(cnt, need_counters * sizeof(int)) != cudaSuccess ||
+        cudaMemset(*cnt, 0, need_counters * sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    *cnt_count = need_counters;
+  }
+  return GEMM_OK;
+}
+
+// Fills rs with q's row-reduction outputs and the device's partials buffer,
+// grown for n_blocks column tiles.  Leaves rs empty when q wants none.
+int attach_row_stats(int dev, const Problem& q, int n_blocks, RowStatsParams* rs,
+                     cudaStream_t stream) {
+  *rs = RowStatsParams{nullptr, nullptr, nullptr, nullptr, nullptr};
+  if (!q.stats()) return GEMM_OK;
+  const size_t bytes = 3 * static_cast<size_t>(q.batch) * n_blocks * q.M * sizeof(float);
+  const size_t counters = static_cast<size_t>(q.batch) * ceil_div(q.M, 32);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  const int st = grow_buffers(&d.stats_ws, &d.stats_ws_bytes, &d.stats_counters,
+                              &d.stats_counter_count, bytes, counters, stream);
+  if (st != GEMM_OK) return st;
+  *rs = RowStatsParams{q.row_sum, q.row_max, q.row_min, d.stats_ws, d.stats_counters};
   return GEMM_OK;
 }
 
@@ -690,6 +757,44 @@ __global__ void scale_kernel(void* C, long long ldc, long long sc, int batch, in
   }
 }
 
+// Row reductions of beta * C when K == 0 (C not read when beta == 0): one
+// warp per row, lanes over the columns, then a shuffle butterfly.
+__global__ void row_stats_k0_kernel(const void* C, long long ldc, long long sc, int batch, int M,
+                                    int N, float beta, int out_kind, float* rsum, float* rmax,
+                                    float* rmin) {
+  const int lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(batch) * M;
+  const bool f16 = out_kind == 2;
+  for (long long r = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+       r < rows; r += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+    const long long b = r / M, m = r % M;
+    const long long off = b * sc + m * ldc;
+    float sum = 0.0f, mx = -INFINITY, mn = INFINITY;
+    for (int n = lane; n < N; n += 32) {
+      float v = 0.0f;
+      if (beta != 0.0f) {
+        const float c = out_kind == 0 ? static_cast<const float*>(C)[off + n]
+                                      : half16_to_float(static_cast<const uint16_t*>(C)[off + n], f16);
+        v = beta * c;
+      }
+      sum += v;
+      mx = fmaxf(mx, v);
+      mn = fminf(mn, v);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    }
+    if (lane == 0) {
+      if (rsum) rsum[r] = sum;
+      if (rmax) rmax[r] = mx;
+      if (rmin) rmin[r] = mn;
+    }
+  }
+}
+
 int run_scale(const gemm_plan& pl, void* C, int64_t ldc, int64_t sc, int64_t batch, int64_t M,
               int64_t N, float beta, int out_dtype, cudaStream_t stream) {
   return launch(scale_kernel, pl.grid, 256, 0, stream, C, static_cast<long long>(ldc),
@@ -765,32 +870,33 @@ void pair_units(int dev, gemm_plan* pl, const Problem& q, int out_cols, TilePara
   p->num_units = static_cast<int>(c.full + (c.tiles - c.full) * c.split);
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool STATS = false>
 int launch_pair_gemm(const gemm_plan& pl, int dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
                      const CUtensorMap& tmB2, const CUtensorMap& tmOut, const TileParams& p,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, const RowStatsParams& rs = RowStatsParams{}) {
   using Cfg = PairCfg<BN, kPairStages, EPI>;
-  auto kern = gemm_pair_kernel<BN, kPairStages, EPI>;
+  auto kern = gemm_pair_kernel<BN, kPairStages, EPI, STATS>;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     const int st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), Cfg::kSmemBytes);
     if (st != GEMM_OK) return st;
   }
-  return launch_pair(kern, pl.grid, Cfg::kSmemBytes, stream, tmA, tmB, tmB2, tmOut, p);
+  return launch_pair(kern, pl.grid, Cfg::kSmemBytes, stream, tmA, tmB, tmB2, tmOut, p, rs);
 }
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, bool STATS = false>
 int launch_single_gemm(const gemm_plan& pl, int dev, const CUtensorMap& tmA,
                        const CUtensorMap& tmB, const CUtensorMap& tmB2, const CUtensorMap& tmOut,
-                       const TileParams& p, cudaStream_t stream) {
+                       const TileParams& p, cudaStream_t stream,
+                       const RowStatsParams& rs = RowStatsParams{}) {
   using Cfg = GemmCfg<BN, STAGES, EPI>;
-  auto kern = gemm_tc_kernel<BN, STAGES, EPI>;
+  auto kern = gemm_tc_kernel<BN, STAGES, EPI, STATS>;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     const int st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), Cfg::kSmemBytes);
     if (st != GEMM_OK) return st;
   }
-  return launch(kern, pl.grid, kThreads, Cfg::kSmemBytes, stream, tmA, tmB, tmB2, tmOut, p);
+  return launch(kern, pl.grid, kThreads, Cfg::kSmemBytes, stream, tmA, tmB, tmB2, tmOut, p, rs);
 }
 
 int run_pair(gemm_plan& pl, int dev, int slots, const Problem& q, cudaStream_t stream) {
@@ -806,8 +912,22 @@ int run_pair(gemm_plan& pl, int dev, int slots, const Problem& q, cudaStream_t s
   if ((st = output_map(&tmOut, q.C, q.batch, q.M, q.N, q.ldc, q.sc, q.out_dtype, bn)) != GEMM_OK)
     return st;
   TileParams p = tile_params(q, kPairBM, bn, idesc_f32_acc(kPairBM, bn, f16in));
+  RowStatsParams rs;
+  if ((st = attach_row_stats(dev, q, p.n_blocks, &rs, stream)) != GEMM_OK) return st;
   pair_units(dev, &pl, q, bn, &p, stream, false, slots);
   const bool f32 = q.out_dtype == GEMM_OUT_F32;
+  if (q.stats()) {
+    switch (bn) {
+      case 256:
+        return f32 ? launch_pair_gemm<256, EPI_F32, true>(pl, dev, tmA, tmB, tmB, tmOut, p, stream, rs)
+                   : launch_pair_gemm<256, EPI_BF16, true>(pl, dev, tmA, tmB, tmB, tmOut, p, stream, rs);
+      case 224:
+        return f32 ? launch_pair_gemm<224, EPI_F32, true>(pl, dev, tmA, tmB, tmB, tmOut, p, stream, rs)
+                   : launch_pair_gemm<224, EPI_BF16, true>(pl, dev, tmA, tmB, tmB, tmOut, p, stream, rs);
+      default:
+        return GEMM_ERR_UNSUPPORTED;
+    }
+  }
   switch (bn) {
     case 256:
       return f32 ? launch_pair_gemm<256, EPI_F32>(pl, dev, tmA, tmB, tmB, tmOut, p, stream)
@@ -833,9 +953,17 @@ int run_single(const gemm_plan& pl, int dev, const Problem& q, cudaStream_t stre
       GEMM_OK)
     return st;
   const TileParams p = tile_params(q, kBM, kTileN, idesc_f32_acc(kBM, kTileN, f16in));
-  if (q.out_dtype == GEMM_OUT_F32)
-    return launch_single_gemm<kTileN, kStages, EPI_F32>(pl, dev, tmA, tmB, tmB, tmOut, p, stream);
-  return launch_single_gemm<kTileN, kStages, EPI_BF16>(pl, dev, tmA, tmB, tmB, tmOut, p, stream);
+  RowStatsParams rs;
+  if ((st = attach_row_stats(dev, q, p.n_blocks, &rs, stream)) != GEMM_OK) return st;
+  const bool f32 = q.out_dtype == GEMM_OUT_F32;
+  if (q.stats())
+    return f32 ? launch_single_gemm<kTileN, kStages, EPI_F32, true>(pl, dev, tmA, tmB, tmB, tmOut,
+                                                                     p, stream, rs)
+               : launch_single_gemm<kTileN, kStages, EPI_BF16, true>(pl, dev, tmA, tmB, tmB, tmOut,
+                                                                      p, stream, rs);
+  return f32 ? launch_single_gemm<kTileN, kStages, EPI_F32>(pl, dev, tmA, tmB, tmB, tmOut, p, stream)
+             : launch_single_gemm<kTileN, kStages, EPI_BF16>(pl, dev, tmA, tmB, tmB, tmOut, p,
+                                                             stream);
 }
 
 SkinnyParams skinny_params(const gemm_plan& pl, const Problem& q) {
@@ -904,9 +1032,18 @@ int run_problem(const Problem& q, void* stream_) {
     slots = query_pair_slots(dev);
   }
   gemm_plan pl;
-  plan_gemm(q.batch, q.M, q.N, q.K, sms, &pl, slots);
+  plan_gemm(q.batch, q.M, q.N, q.K, sms, &pl, slots, true, q.stats());
   switch (pl.kernel) {
     case K_SCALE:
+      if (q.stats()) {
+        const int64_t warps = q.batch * q.M;
+        const int grid = static_cast<int>(std::min<int64_t>(ceil_div(warps, 8), 4 * sms));
+        st = launch(row_stats_k0_kernel, grid, 256, 0, stream, static_cast<const void*>(q.C),
+                    static_cast<long long>(q.ldc), static_cast<long long>(q.batch > 1 ? q.sc : 0),
+                    static_cast<int>(q.batch), static_cast<int>(q.M), static_cast<int>(q.N),
+                    q.beta, q.out_dtype, q.row_sum, q.row_max, q.row_min);
+        if (st != GEMM_OK) return st;
+      }
       return run_scale(pl, q.C, q.ldc, q.batch > 1 ? q.sc : 0, q.batch, q.M, q.N, q.beta,
                        q.out_dtype, stream);
     case K_PAIR:
@@ -995,6 +1132,61 @@ int gemm_batched(int64_t batch, int64_t M, int64_t N, int64_t K, float alpha, co
   return run_problem(q, stream);
 }
 
+int gemm_row_stats(int64_t batch, int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                   int64_t lda, int64_t stride_a, const void* B, int64_t ldb, int64_t stride_b,
+                   float beta, void* C, int64_t ldc, int64_t stride_c, int in_dtype,
+                   int out_dtype, float* row_sum, float* row_max, float* row_min,
+                   void* stream) {
+  Problem q{batch, M,        N,   K,   alpha, beta,     A,        lda,      stride_a,
+            B,     ldb,      stride_b, C, ldc, stride_c, in_dtype, out_dtype};
+  q.row_sum = row_sum;
+  q.row_max = row_max;
+  q.row_min = row_min;
+  for (const float* r : {row_sum, row_max, row_min})
+    if (reinterpret_cast<uintptr_t>(r) % alignof(float) != 0) return GEMM_ERR_ALIGNMENT;
+  const int st = validate_problem(q);
+  if (st != GEMM_OK || !q.stats() || batch == 0 || M == 0 || N > 0) return run_problem(q, stream);
+  // N == 0: each row's reductions are over no values: sum 0, maximum -inf,
+  // minimum +inf (C is not touched).
+  int dev, sms;
+  int s2 = current_device(&dev);
+  if (s2 != GEMM_OK) return s2;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((s2 = probe_device(dev)) != GEMM_OK) return s2;
+    sms = g_dev[dev].sms;
+  }
+  const int grid = static_cast<int>(std::min<int64_t>(ceil_div(batch * M, 8), 4 * sms));
+  return launch(row_stats_k0_kernel, grid, 256, 0, static_cast<cudaStream_t>(stream),
+                static_cast<const void*>(nullptr), 0LL, 0LL, static_cast<int>(batch),
+                static_cast<int>(M), 0, 0.0f, out_dtype, row_sum, row_max, row_min);
+}
+
+int gemm_row_stats_plan(int64_t batch, int64_t M, int64_t N, int64_t K, int in_dtype,
+                        int out_dtype, int num_sms, gemm_plan* plan) {
+  if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
+  if (bad_dims(batch, M, N, K)) return GEMM_ERR_INVALID_ARG;
+  if (in_dtype != GEMM_IN_BF16 && in_dtype != GEMM_IN_F16) return GEMM_ERR_INVALID_ARG;
+  if (out_dtype != GEMM_OUT_F32 && out_dtype != GEMM_OUT_BF16 && out_dtype != GEMM_OUT_F16)
+    return GEMM_ERR_INVALID_ARG;
+  int slots = 0;
+  if (num_sms <= 0) {
+    int dev;
+    int st = current_device(&dev);
+    if (st != GEMM_OK) return st;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = probe_device(dev)) != GEMM_OK) return st;
+    num_sms = g_dev[dev].sms;
+    slots = query_pair_slots(dev);
+  }
+  const int st = plan_gemm(batch, M, N, K, num_sms, plan, slots, true, true);
+  if (st == GEMM_OK && batch > 0 && M > 0 && N == 0) {
+    plan->kernel = K_SCALE;   // the empty-row reductions alone
+    plan->launches = 1;
+  }
+  return st;
+}
+
 int gemm_gate_up_silu(int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx,
                       const void* Wg, const void* Wu, int64_t ldw, void* Y, int64_t ldy,
                       void* stream_) {
@@ -1035,6 +1227,22 @@ int gemm_gate_up_silu(int64_t M, int64_t N, int64_t K, const void* X, int64_t ld
                                                              stream);
 }
 
+int gemm_rmsnorm_gate_up_silu(int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx,
+                              const float* G, float eps, const void* Wg, const void* Wu,
+                              int64_t ldw, void* Xn, int64_t ldxn, void* Y, int64_t ldy,
+                              void* stream) {
+  // Every argument is checked before anything is enqueued.
+  int st = validate_gate_up(M, N, K, Xn, ldxn, Wg, Wu, ldw, Y, ldy);
+  if (st != GEMM_OK) return st;
+  if ((st = rms_norm_check(M, K, X, ldx, GEMM_OUT_BF16, G, eps, Xn, ldxn, GEMM_OUT_BF16)) !=
+      GEMM_OK)
+    return st;
+  if ((st = rms_norm_run(M, K, X, ldx, GEMM_OUT_BF16, G, eps, Xn, ldxn, GEMM_OUT_BF16,
+                         static_cast<cudaStream_t>(stream))) != GEMM_OK)
+    return st;
+  return gemm_gate_up_silu(M, N, K, Xn, ldxn, Wg, Wu, ldw, Y, ldy, stream);
+}
+
 int gemm_get_device_status(void* stream, int* site) {
   int dev;
   int st = current_device(&dev);
@@ -1058,6 +1266,9 @@ int gemm_get_device_status(void* stream, int* site) {
     DeviceState& d = g_dev[dev];
     if (d.counters != nullptr &&
         cudaMemset(d.counters, 0, d.counter_count * sizeof(int)) != cudaSuccess)
+      cudaGetLastError();
+    if (d.stats_counters != nullptr &&
+        cudaMemset(d.stats_counters, 0, d.stats_counter_count * sizeof(int)) != cudaSuccess)
       cudaGetLastError();
   }
   return h[0];

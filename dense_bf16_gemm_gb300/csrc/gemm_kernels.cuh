@@ -140,6 +140,21 @@ struct TileParams {
   int* counters;      // arrivals per (tail tile, 32-row band), zero between calls
 };
 
+// Reductions along each row of the result (kernels instantiated with STATS):
+// the sum, maximum and minimum over n of the FP32 values alpha*acc + beta*c,
+// before any output rounding.  Every warp band of every tile stores the
+// partials of its 32 rows over the tile's columns, and the band's last
+// arrival over the n_blocks column tiles combines them in column-tile order.
+// A separate kernel parameter, so that the plain kernels' parameters (and
+// code) do not change.
+struct RowStatsParams {
+  float* row_sum;       // [batch][M]; each may be nullptr (not wanted)
+  float* row_max;
+  float* row_min;
+  float* ws;            // partials [3][batch][n_blocks][M]
+  int* counters;        // arrivals per (matrix, 32-row band), zero between calls
+};
+
 // Tile, k-block range and piece (-1: whole tile) of work unit u.
 __device__ __forceinline__ void unit_of(int u, const TileParams& p, int& tile, int& kb0, int& kb1,
                                         int& piece) {
@@ -333,6 +348,72 @@ __device__ __forceinline__ bool publish_partial(uint32_t tacc, int acc_cols, int
   return last;
 }
 
+// Running reductions of one lane's row over the columns an epilogue visits.
+struct RowAcc {
+  float sum, max, min;
+};
+
+__device__ __forceinline__ void row_acc_init(RowAcc& r) {
+  r.sum = 0.0f;
+  r.max = -INFINITY;
+  r.min = INFINITY;
+}
+
+// Adds the 32 values of a slice at columns col0.. (those below N) in order.
+__device__ __forceinline__ void row_acc_slice(RowAcc& r, const float (&v)[32], int col0, int N) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    if (col0 + i < N) {
+      r.sum += v[i];
+      r.max = fmaxf(r.max, v[i]);
+      r.min = fminf(r.min, v[i]);
+    }
+  }
+}
+
+// Stores this warp band's partial reductions (rows m0..m0+31 of matrix b over
+// column tile nb) and counts the band's arrival; the last of the n_blocks
+// arrivals adds the partials in column-tile order 0, 1, ... and writes the
+// row results, so they do not depend on which tile finished last.
+__device__ __forceinline__ void publish_row_stats(const TileParams& p, const RowStatsParams& rs,
+                                                  int b, int nb, int m0, int lane,
+                                                  const RowAcc& r) {
+  const int row = m0 + lane;
+  const bool live = row < p.M;
+  const long long plane = static_cast<long long>(p.batch) * p.n_blocks * p.M;
+  const long long base = static_cast<long long>(b) * p.n_blocks * p.M + row;
+  if (live) {
+    const long long idx = base + static_cast<long long>(nb) * p.M;
+    __stcg(rs.ws + idx, r.sum);
+    __stcg(rs.ws + plane + idx, r.max);
+    __stcg(rs.ws + 2 * plane + idx, r.min);
+  }
+  __threadfence();
+  __syncwarp();
+  int* counter = rs.counters + static_cast<long long>(b) * ((p.M + 31) >> 5) + (m0 >> 5);
+  int prev = 0;
+  if (lane == 0) prev = atomicAdd(counter, 1);
+  prev = __shfl_sync(0xffffffffu, prev, 0);
+  if (prev != p.n_blocks - 1) return;
+  __threadfence();
+  if (live) {
+    float sum = 0.0f, mx = -INFINITY, mn = INFINITY;
+#pragma unroll 4
+    for (int j = 0; j < p.n_blocks; ++j) {
+      const long long idx = base + static_cast<long long>(j) * p.M;
+      sum += __ldcg(rs.ws + idx);
+      mx = fmaxf(mx, __ldcg(rs.ws + plane + idx));
+      mn = fminf(mn, __ldcg(rs.ws + 2 * plane + idx));
+    }
+    const long long out = static_cast<long long>(b) * p.M + row;
+    if (rs.row_sum != nullptr) rs.row_sum[out] = sum;
+    if (rs.row_max != nullptr) rs.row_max[out] = mx;
+    if (rs.row_min != nullptr) rs.row_min[out] = mn;
+  }
+  __syncwarp();
+  if (lane == 0) *counter = 0;  // ready for the next call
+}
+
 template <int EPI, int OUT_COLS>
 struct EpiBox {
   static constexpr int kCols = (EPI == EPI_F32) ? 32 : (OUT_COLS % 64 == 0 ? 64 : 32);
@@ -361,16 +442,20 @@ __device__ __forceinline__ uint32_t staging_offset(int row, uint32_t chunk) {
 // FP32, written to a staging slot in the swizzled layout and stored with TMA.
 // `sc` counts the boxes this warp staged (two slots alternate); every staged
 // box is committed as its own bulk group.
-template <int BN, int EPI>
+// STATS: also reduce each row (sum, max, min) into p's row-statistics outputs.
+template <int BN, int EPI, bool STATS = false>
 __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtensorMap* tmOut,
                                               uint32_t tacc, int b, int m0, int n0,
                                               uint32_t staging, int lane, int& sc, bool have_acc,
-                                              const SplitCtx& split) {
+                                              const SplitCtx& split, const RowStatsParams& rs) {
   constexpr int OUT = (EPI == EPI_GATE_UP) ? BN / 2 : BN;
   using Box = EpiBox<EPI, OUT>;
   constexpr int kSub = Box::kCols / 32;  // 32-column slices per box
   const int row = m0 + lane;
   const bool read_c = (EPI != EPI_GATE_UP) && p.beta != 0.0f;
+  constexpr bool stats = STATS && (EPI != EPI_GATE_UP);
+  RowAcc racc;
+  row_acc_init(racc);
   // C of the next slice is loaded one slice ahead so its latency overlaps the
   // TMEM load and conversion of the current one.
   float c_next[32];
@@ -418,6 +503,7 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] += beta * c_cur[i];
         }
+        if constexpr (stats) row_acc_slice(racc, v, n0 + c0 + 32 * h, p.N);
       }
       if constexpr (EPI == EPI_F32) {
 #pragma unroll
@@ -444,6 +530,9 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
     }
     ++sc;
   }
+  if constexpr (stats) {
+    if (m0 < p.M) publish_row_stats(p, rs, b, n0 / OUT, m0, lane, racc);
+  }
 }
 
 // When C is read (beta != 0): ask L2 for this warp's band of C of a coming
@@ -461,11 +550,12 @@ __device__ __forceinline__ void prefetch_c_band(const TileParams& p, const CUten
   }
 }
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, bool STATS = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2,
-                   const __grid_constant__ CUtensorMap tmOut, const TileParams p) {
+                   const __grid_constant__ CUtensorMap tmOut, const TileParams p,
+                   const RowStatsParams rs) {
   using Cfg = GemmCfg<BN, STAGES, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -625,8 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m0 = mb * kBM + band;
       const int n0 = nb * Cfg::kOutCols;
       const SplitCtx whole{1, 0, nullptr, 0};
-      epilogue_tile<BN, EPI>(p, &tmOut, tacc, bt, m0, n0, staging, lane, sc, p.k_blocks > 0,
-                             whole);
+      epilogue_tile<BN, EPI, STATS>(p, &tmOut, tacc, bt, m0, n0, staging, lane, sc,
+                                    p.k_blocks > 0, whole, rs);
       // The accumulator may be overwritten once every lane's TMEM reads are done.
       tc_fence_before_sync();
       __syncwarp();

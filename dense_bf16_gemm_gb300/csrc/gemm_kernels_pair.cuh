@@ -46,12 +46,13 @@ struct PairCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, bool STATS = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmB2,
-                     const __grid_constant__ CUtensorMap tmOut, const TileParams p) {
+                     const __grid_constant__ CUtensorMap tmOut, const TileParams p,
+                     const RowStatsParams rs) {
   using Cfg = PairCfg<BN, STAGES, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -241,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 p.tail_split);
       }
       if (store)
-        epilogue_tile<BN, EPI>(p, &tmOut, tacc, bt, m0, n0, staging, lane, sc, kb1 > kb0, split);
+        epilogue_tile<BN, EPI, STATS>(p, &tmOut, tacc, bt, m0, n0, staging, lane, sc, kb1 > kb0,
+                                      split, rs);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acce0_even + 8u * buf);

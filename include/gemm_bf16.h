@@ -138,6 +138,96 @@ GEMM_API int gemm_gate_up_silu(int64_t M, int64_t N, int64_t K,
                       const void *Wg, const void *Wu, int64_t ldw,
                       void *Y, int64_t ldy, void *stream);
 
+/*
+ * gemm_batched with reductions along each row of every result:
+ *
+ *   v_b(m,n)       = alpha * A_b.B_b(m,n) + beta * C_b(m,n)   (FP32, before the
+ *                    output rounding)
+ *   row_sum[b*M+m] = sum over n of v_b(m,n)
+ *   row_max[b*M+m] = max over n,   row_min[b*M+m] = min over n
+ *
+ * ("TMEM tiles and transfers", section "Storage and a transfer": a reduction
+ * along the second axis of a loaded accumulator, which each thread holds
+ * whole for its row; "TMA and Hopper WGMMA", section "WGMMA values and
+ * ownership": sum, maximum and minimum along axis 2 of a finished
+ * accumulator.  The pages reduce one tile; here the reduction covers the
+ * whole row, n = 0 .. N-1.)
+ *
+ * All arguments up to out_dtype are those of gemm_batched, and C is written
+ * as there.  row_sum, row_max, row_min: device arrays of batch*M FP32 values
+ * (4-byte aligned, owned by the caller); any of them may be NULL (not
+ * written).  Maxima and minima ignore NaN values (IEEE maxNum); sums
+ * propagate them.  N == 0 (with batch, M > 0) writes sum 0, max -inf and
+ * min +inf without touching C.
+ *
+ * Order and determinism: each tile's epilogue adds its row's values in column
+ * order in FP32; the per-tile partials are combined in column-tile order by
+ * the last tile of each 32-row band to finish, so the results do not depend
+ * on timing.  The partials live in a per-device workspace allocated on first
+ * use; a call made while `stream` is being captured returns GEMM_ERR_CUDA
+ * unless an earlier call of at least the same batch*M*N/256 size allocated
+ * it.  Problems with M <= 16 run on the 128-row tiled kernel instead of the
+ * swapped-operand one.
+ */
+GEMM_API int gemm_row_stats(int64_t batch, int64_t M, int64_t N, int64_t K, float alpha,
+                   const void *A, int64_t lda, int64_t stride_a,
+                   const void *B, int64_t ldb, int64_t stride_b,
+                   float beta, void *C, int64_t ldc, int64_t stride_c,
+                   int in_dtype, int out_dtype,
+                   float *row_sum, float *row_max, float *row_min, void *stream);
+
+/*
+ * Row normalisation ("Tiles and shared memory", section "A complete kernel":
+ * each row is scaled by the inverse root of the mean of its squares plus a
+ * small constant, then by a per-column gain):
+ *
+ *   inv(m) = 1 / sqrt((sum_k x(m,k)^2) / D + eps),   y(m,k) = x(m,k) * inv(m) * g(k)
+ *
+ * rows, D    0 <= rows, D < 2^31 (either 0: nothing is done).
+ * X          device, x(m,k) at X[m*ldx + k], element type x_dtype.
+ * x_dtype, y_dtype  element codes GEMM_OUT_F32, GEMM_OUT_BF16, GEMM_OUT_F16.
+ * G          device, D FP32 gains.
+ * eps        finite, >= 0.
+ * Y          device, y(m,k) at Y[m*ldy + k], element type y_dtype; may be X
+ *            itself when both element types have the same size and ldy ==
+ *            ldx; any other overlap with X is refused (GEMM_ERR_INVALID_ARG).
+ * X, Y and G must be 16-byte aligned and ldx, ldy keep rows 16-byte aligned
+ * (GEMM_ERR_ALIGNMENT otherwise); D itself may be any size.
+ *
+ * Arithmetic is FP32: per row, 32 lanes each add the squares of their
+ * elements in order and a 5-step butterfly combines them; the division,
+ * the addition of eps, the square root and the reciprocal are correctly
+ * rounded; y = (x * inv) * g, rounded to nearest even for a 16-bit output.
+ * Asynchronous on `stream`; allocates nothing.
+ */
+GEMM_API int gemm_rms_norm(int64_t rows, int64_t D, const void *X, int64_t ldx, int x_dtype,
+                  const float *G, float eps, void *Y, int64_t ldy, int y_dtype,
+                  void *stream);
+
+/*
+ * The gate/up projection of a normalised activation, the two steps on
+ * either side of it in one call:
+ *
+ *   Xn = rms_norm(X, G, eps)  (BF16, as gemm_rms_norm)
+ *   Y  = silu(Xn.Wg) * (Xn.Wu)  (as gemm_gate_up_silu)
+ *
+ * ("Tiles and shared memory", section "A complete kernel" for the
+ * normalisation; "TMA and Hopper WGMMA", sections "TMA and Hopper WGMMA" and
+ * "Worked consumers and current validation" for the fused gate/up
+ * projection.)  X (M, K) BF16 with pitch ldx; G K FP32 gains; Wg, Wu, Y as
+ * gemm_gate_up_silu.  Xn (M, K) BF16 with pitch ldxn is caller-owned scratch
+ * that also receives the normalised activation (it may be X itself, ldxn ==
+ * ldx).  The tensor cores take 16-bit operands, so the normalised values are
+ * rounded to BF16 (nearest even) before the contraction.  Two launches on
+ * `stream`, the normalisation then the projection; every argument is
+ * checked before either is enqueued.  Allocates nothing beyond what
+ * gemm_gate_up_silu does.
+ */
+GEMM_API int gemm_rmsnorm_gate_up_silu(int64_t M, int64_t N, int64_t K,
+                              const void *X, int64_t ldx, const float *G, float eps,
+                              const void *Wg, const void *Wu, int64_t ldw,
+                              void *Xn, int64_t ldxn, void *Y, int64_t ldy, void *stream);
+
 /* Static, NUL-terminated description of a return code. */
 GEMM_API const char *gemm_status_string(int status);
 
@@ -224,6 +314,10 @@ GEMM_API int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int 
 /* Plan of gemm_batched(batch, M, N, K, ..., in_dtype, out_dtype, ...), as gemm_bf16_plan. */
 GEMM_API int gemm_batched_plan(int64_t batch, int64_t M, int64_t N, int64_t K, int in_dtype,
                                int out_dtype, int num_sms, gemm_plan *plan);
+
+/* Plan of gemm_row_stats(batch, M, N, K, ..., in_dtype, out_dtype, ...), as gemm_bf16_plan. */
+GEMM_API int gemm_row_stats_plan(int64_t batch, int64_t M, int64_t N, int64_t K, int in_dtype,
+                                 int out_dtype, int num_sms, gemm_plan *plan);
 
 /* Plan of gemm_gate_up_silu(M, N, K, ...), as gemm_bf16_plan. */
 GEMM_API int gemm_gate_up_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_plan *plan);

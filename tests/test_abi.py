@@ -242,3 +242,95 @@ def test_plan_gate_up(lib):
 def test_selftest_rejects_out_of_range_limits(lib):
     assert _native.gemm_selftest_wait_timeout(10, 0) == _native.GEMM_ERR_INVALID_ARG
     assert _native.gemm_selftest_wait_timeout(5 * 10**9, 0) == _native.GEMM_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------------------
+# Row reductions, row normalisation and the normalised gate/up projection
+# ---------------------------------------------------------------------------
+F32, BF16, F16 = _native.GEMM_OUT_F32, _native.GEMM_OUT_BF16, _native.GEMM_OUT_F16
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (rows, D, X, ldx, xk, G, eps, Y, ldy, yk)
+    ((-1, 8, A16, 8, BF16, A16, 1e-6, A16 * 2, 8, BF16), _native.GEMM_ERR_INVALID_ARG),
+    ((8, -1, A16, 8, BF16, A16, 1e-6, A16 * 2, 8, BF16), _native.GEMM_ERR_INVALID_ARG),
+    ((1 << 31, 8, A16, 8, BF16, A16, 1e-6, A16 * 2, 8, BF16), _native.GEMM_ERR_INVALID_ARG),
+    ((8, 8, A16, 8, 3, A16, 1e-6, A16 * 2, 8, BF16), _native.GEMM_ERR_INVALID_ARG),   # x code
+    ((8, 8, A16, 8, BF16, A16, 1e-6, A16 * 2, 8, 5), _native.GEMM_ERR_INVALID_ARG),   # y code
+    ((8, 8, A16, 8, BF16, A16, -1.0, A16 * 2, 8, BF16), _native.GEMM_ERR_INVALID_ARG),
+    ((8, 8, A16, 8, BF16, A16, float("nan"), A16 * 2, 8, BF16), _native.GEMM_ERR_INVALID_ARG),
+    ((8, 8, A16, 8, BF16, A16, float("inf"), A16 * 2, 8, BF16), _native.GEMM_ERR_INVALID_ARG),
+    ((8, 8, 0, 8, BF16, A16, 1e-6, A16 * 2, 8, BF16), _native.GEMM_ERR_INVALID_ARG),  # NULL X
+    ((8, 8, A16, 8, BF16, 0, 1e-6, A16 * 2, 8, BF16), _native.GEMM_ERR_INVALID_ARG),  # NULL G
+    ((8, 8, A16, 8, BF16, A16, 1e-6, 0, 8, BF16), _native.GEMM_ERR_INVALID_ARG),      # NULL Y
+    ((8, 16, A16, 8, BF16, A16, 1e-6, A16 * 2, 16, BF16), _native.GEMM_ERR_INVALID_ARG),  # ldx<D
+    ((8, 8, A16 + 2, 8, BF16, A16, 1e-6, A16 * 2, 8, BF16), _native.GEMM_ERR_ALIGNMENT),
+    ((8, 8, A16, 8, BF16, A16 + 4, 1e-6, A16 * 2, 8, BF16), _native.GEMM_ERR_ALIGNMENT),
+    ((8, 8, A16, 8, BF16, A16, 1e-6, A16 * 2 + 8, 8, BF16), _native.GEMM_ERR_ALIGNMENT),
+    ((8, 4, A16, 4, BF16, A16, 1e-6, A16 * 2, 8, BF16), _native.GEMM_ERR_ALIGNMENT),  # ldx*2%16
+    ((8, 6, A16, 8, F32, A16, 1e-6, A16 * 2, 6, F32), _native.GEMM_ERR_ALIGNMENT),    # ldy*4%16
+    # Y overlapping X other than exactly in place
+    ((8, 8, A16, 8, BF16, A16 * 3, 1e-6, A16 + 16, 8, BF16), _native.GEMM_ERR_INVALID_ARG),
+    ((8, 8, A16, 8, F32, A16 * 3, 1e-6, A16, 8, BF16), _native.GEMM_ERR_INVALID_ARG),
+    ((8, 8, A16, 8, BF16, A16 * 3, 1e-6, A16, 16, BF16), _native.GEMM_ERR_INVALID_ARG),
+    ((0, 8, 0, 8, BF16, 0, 1e-6, 0, 8, BF16), _native.GEMM_OK),                       # empty
+    ((8, 0, 0, 0, BF16, 0, 0.0, 0, 0, BF16), _native.GEMM_OK),
+])
+def test_rms_norm_validation_without_gpu(lib, args, expect):
+    assert _native.gemm_rms_norm(*args, 0) == expect
+
+
+def test_rmsnorm_gate_up_validation_without_gpu(lib):
+    ok = dict(M=8, N=8, K=8, X=A16, ldx=8, G=A16 * 3, eps=1e-6, Wg=A16 * 4, Wu=A16 * 5, ldw=8,
+              Xn=A16 * 6, ldxn=8, Y=A16 * 7, ldy=8)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return _native.gemm_rmsnorm_gate_up_silu(a["M"], a["N"], a["K"], a["X"], a["ldx"],
+                                                 a["G"], a["eps"], a["Wg"], a["Wu"], a["ldw"],
+                                                 a["Xn"], a["ldxn"], a["Y"], a["ldy"], 0)
+    assert call(M=-1) == _native.GEMM_ERR_INVALID_ARG
+    assert call(eps=-1.0) == _native.GEMM_ERR_INVALID_ARG
+    assert call(G=0) == _native.GEMM_ERR_INVALID_ARG
+    assert call(Xn=0) == _native.GEMM_ERR_INVALID_ARG
+    assert call(Xn=A16 + 16) == _native.GEMM_ERR_INVALID_ARG      # partly overlaps X
+    assert call(G=A16 * 3 + 4) == _native.GEMM_ERR_ALIGNMENT
+    assert call(Wg=A16 * 4 + 2) == _native.GEMM_ERR_ALIGNMENT
+    assert call(ldxn=4) == _native.GEMM_ERR_INVALID_ARG
+    assert call(M=0) == _native.GEMM_OK
+
+
+def test_row_stats_validation_without_gpu(lib):
+    def call(M=8, N=8, K=8, C=A16 * 2, rs=A16 * 3, rm=0, rn=0, in_dt=0, out_dt=BF16):
+        return _native.gemm_row_stats(1, M, N, K, 1.0, A16, 8, 0, A16 * 4, 8, 0, 0.0, C, 8, 0,
+                                      in_dt, out_dt, rs, rm, rn, 0)
+    assert call(M=-1) == _native.GEMM_ERR_INVALID_ARG
+    assert call(in_dt=2) == _native.GEMM_ERR_INVALID_ARG
+    assert call(C=0) == _native.GEMM_ERR_INVALID_ARG
+    assert call(rs=A16 * 3 + 2) == _native.GEMM_ERR_ALIGNMENT
+    assert call(rm=A16 * 3 + 1) == _native.GEMM_ERR_ALIGNMENT
+    assert call(M=0) == _native.GEMM_OK
+
+
+def row_stats_plan(M, N, K, out=BF16):
+    st, p = _native.gemm_row_stats_plan(1, M, N, K, 0, out, 148)
+    assert st == _native.GEMM_OK
+    return p.as_dict()
+
+
+def test_row_stats_plans():
+    # M <= 16 takes the 128-row tiled kernel instead of the swapped-operand one
+    assert row_stats_plan(16, 4096, 4096)["kernel_name"] == "tiled"
+    assert _native.gemm_batched_plan(1, 16, 4096, 4096, 0, BF16, 148)[1].as_dict()[
+        "kernel_name"] == "skinny_splitk"
+    # otherwise the same plan as the plain GEMM
+    for shape in [(64, 1000, 512), (4096, 4096, 4096), (3000, 5000, 2000)]:
+        a = row_stats_plan(*shape)
+        b = _native.gemm_batched_plan(1, *shape, 0, BF16, 148)[1].as_dict()
+        assert a == b
+    # K == 0: the reductions of beta*C, then the scaling of C
+    k0 = row_stats_plan(64, 64, 0)
+    assert k0["kernel_name"] == "scale" and k0["launches"] == 2
+    # N == 0: only the empty-row reductions
+    n0 = row_stats_plan(64, 0, 64)
+    assert n0["kernel_name"] == "scale" and n0["launches"] == 1

@@ -11,6 +11,8 @@ Storage (both operands K-contiguous):
   B  (N, K)  b(k,n) = B[n, k]
   C  (M, N)  float32, only for beta != 0
 Gate/up:  X (M, K), Wg (N, K), Wu (N, K).
+Row normalisation:  X (rows, D) with a per-row magnitude exp(N(0,1)) so that
+rows of very different scale meet; gains G (D,) uniform on [0.5, 1.5).
 
 Draw order within one generator: A, then B, then C (or X, Wg, Wu).
 "uniform" is ``2 * rand - 1`` (uniform on [-1, 1)); "normal" is
@@ -28,7 +30,8 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "gemm" or "gate_up"
+    kind: str                 # "gemm", "gate_up", "gemm_row_stats", "rms_norm" or
+                              # "rmsnorm_gate_up"
     M: int
     N: int
     K: int
@@ -44,6 +47,8 @@ class Workload:
     batch: int = 1            # independent matrices (gemm only)
     in_f16: bool = False      # FP16 operands instead of BF16
     out_f16: bool = False     # FP16 output
+    norm_in: str = "bf16"     # rms_norm input element type: "f32", "bf16" or "f16"
+    eps: float = 1e-6         # rms_norm constant
 
     @property
     def out_dtype(self):
@@ -54,19 +59,29 @@ class Workload:
     @property
     def flops(self) -> float:
         """Useful floating-point operations: 2MNK per GEMM (two for gate/up)."""
+        if self.kind == "rms_norm":
+            return 3.0 * self.M * self.K
         per = 2.0 * self.M * self.N * self.K * self.batch
-        return 2.0 * per if self.kind == "gate_up" else per
+        return 2.0 * per if self.kind in ("gate_up", "rmsnorm_gate_up") else per
 
     @property
     def algorithmic_bytes(self) -> int:
         """Compulsory HBM bytes: each input read once, the output written once
         (plus C read when beta != 0)."""
+        out_elem = 2 if (self.out_bf16 or self.out_f16) else 4
+        if self.kind == "rms_norm":
+            in_elem = 4 if self.norm_in == "f32" else 2
+            return self.M * self.K * (in_elem + out_elem) + 4 * self.K
         if self.kind == "gate_up":
             return 2 * (self.M * self.K + 2 * self.N * self.K + self.M * self.N)
-        out_elem = 2 if (self.out_bf16 or self.out_f16) else 4
+        if self.kind == "rmsnorm_gate_up":
+            # X read, Xn written, both weights read, Y written (Xn is re-read from L2)
+            return 2 * (2 * self.M * self.K + 2 * self.N * self.K + self.M * self.N) + 4 * self.K
         b = 2 * (self.M * self.K + self.N * self.K) + out_elem * self.M * self.N
         if self.beta != 0.0:
             b += out_elem * self.M * self.N
+        if self.kind == "gemm_row_stats":
+            b += 3 * 4 * self.M
         return b * self.batch
 
 
@@ -103,6 +118,23 @@ WORKLOADS = {
         "gemm_batched_8x2048", "gemm", 2048, 2048, 2048, seed=6,
         dist_a=("normal", 1.0), dist_b=("normal", 1.0), out_bf16=True, batch=8,
         notes="8 independent 2048^3 BF16 GEMMs, one call"),
+    # Row reductions and the row normalisation (the row after those).
+    "gemm_row_stats_4096": Workload(
+        "gemm_row_stats_4096", "gemm_row_stats", 4096, 4096, 4096, seed=1,
+        dist_a=("normal", 1.0), dist_b=("normal", 1.0), out_bf16=True, check="sampled",
+        notes="the 4096^3 BF16 GEMM plus the sum, max and min of every row"),
+    "rms_norm_262144x256_f32": Workload(
+        "rms_norm_262144x256_f32", "rms_norm", 262144, 256, 256, seed=7,
+        dist_a=("normal", 1.0), dist_b=("uniform",), norm_in="f32", check="sampled",
+        notes="row normalisation, D=256, FP32 in and out"),
+    "rms_norm_16384x4096_bf16": Workload(
+        "rms_norm_16384x4096_bf16", "rms_norm", 16384, 4096, 4096, seed=8,
+        dist_a=("normal", 1.0), dist_b=("uniform",), norm_in="bf16", out_bf16=True,
+        check="sampled", notes="row normalisation, D=4096, BF16 in and out"),
+    "rmsnorm_gate_up_4096x14336x4096": Workload(
+        "rmsnorm_gate_up_4096x14336x4096", "rmsnorm_gate_up", 4096, 14336, 4096, seed=9,
+        dist_a=("normal", 1.0), dist_b=("normal", 1.0 / 64.0), out_bf16=True,
+        check="sampled", notes="Y = silu(Xn Wg) * (Xn Wu), Xn = rms_norm(X)"),
 }
 
 # The workload the benchmark times by default.
@@ -142,9 +174,39 @@ def gate_up_inputs(M: int, N: int, K: int, seed: int, dist_x=("normal", 1.0),
     return X, Wg, Wu
 
 
+_NORM_TYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+def rms_norm_inputs(rows: int, D: int, seed: int, dtype=torch.float32):
+    """CPU tensors ``X`` (rows, D) of ``dtype`` and gains ``G`` (D,) float32.
+
+    Draw order: the row magnitudes (rows, 1), then X, then G."""
+    gen = torch.Generator(device="cpu").manual_seed(int(seed))
+    mag = torch.exp(_draw(gen, (rows, 1), ("normal", 1.0)))
+    X = (_draw(gen, (rows, D), ("normal", 1.0)) * mag).to(dtype)
+    G = torch.rand(D, generator=gen, dtype=torch.float32) + 0.5
+    return X, G
+
+
+def rmsnorm_gate_up_inputs(M: int, N: int, K: int, seed: int, dist_w=("normal", 1.0)):
+    """CPU tensors ``X`` (M,K) bf16 with per-row magnitudes, ``G`` (K,) float32,
+    ``Wg``, ``Wu`` (N,K) bf16, drawn in that order from one generator."""
+    gen = torch.Generator(device="cpu").manual_seed(int(seed))
+    mag = torch.exp(_draw(gen, (M, 1), ("normal", 1.0)))
+    X = (_draw(gen, (M, K), ("normal", 1.0)) * mag).to(torch.bfloat16)
+    G = torch.rand(K, generator=gen, dtype=torch.float32) + 0.5
+    Wg = _draw(gen, (N, K), dist_w).to(torch.bfloat16)
+    Wu = _draw(gen, (N, K), dist_w).to(torch.bfloat16)
+    return X, G, Wg, Wu
+
+
 def inputs_for(w: Workload):
     if w.kind == "gate_up":
         return gate_up_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.dist_b)
+    if w.kind == "rms_norm":
+        return rms_norm_inputs(w.M, w.K, w.seed, _NORM_TYPES[w.norm_in])
+    if w.kind == "rmsnorm_gate_up":
+        return rmsnorm_gate_up_inputs(w.M, w.N, w.K, w.seed, w.dist_b)
     return gemm_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.dist_b, w.dist_c, w.batch,
                        torch.float16 if w.in_f16 else torch.bfloat16)
 
