@@ -309,9 +309,9 @@ def time_e2e(lib, w, steps, warmup, stream, dev):
 
 
 def hbm_bound(w) -> bool:
-    """Workloads whose metric is bandwidth: the M=16 decode GEMM and the row
-    normalisation."""
-    return w.name.startswith("skinny") or w.kind == "rms_norm"
+    """Workloads whose metric is bandwidth: the decode-shaped GEMMs (M = 16
+    and 64) and the row normalisation."""
+    return w.name.startswith(("skinny", "smallm")) or w.kind == "rms_norm"
 
 
 def metric_of(w, ms):

@@ -28,6 +28,7 @@
 #include "gemm_kernels.cuh"
 #include "gemm_kernels_pair.cuh"
 #include "gemm_skinny.cuh"
+#include "gemm_smallm.cuh"
 #include "norm_api.h"
 
 namespace {
@@ -104,8 +105,48 @@ enum KernelKind {
   K_SCALE = 3,
   K_GATE_UP = 4,
   K_PAIR = 5,
-  K_PAIR_GATE_UP = 6
+  K_PAIR_GATE_UP = 6,
+  K_SMALL_M = 7
 };
+
+constexpr int kSmallMMaxM = 128;   // the small-M kernel's widest activation tile
+
+// Activation tile (the MMA's N) of the small-M kernel for M rows.
+int smallm_nx(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+
+int smallm_smem(int nx) {
+  switch (nx) {
+    case 16: return SmallMCfg<16>::kSmemBytes;
+    case 32: return SmallMCfg<32>::kSmemBytes;
+    case 64: return SmallMCfg<64>::kSmemBytes;
+    default: return SmallMCfg<128>::kSmemBytes;
+  }
+}
+
+int smallm_stages(int nx) {
+  switch (nx) {
+    case 16: return SmallMCfg<16>::kStages;
+    case 32: return SmallMCfg<32>::kStages;
+    case 64: return SmallMCfg<64>::kStages;
+    default: return SmallMCfg<128>::kStages;
+  }
+}
+
+// Whether an M <= 128 problem runs on the small-M kernel.  A CTA streams B
+// from HBM at about 32-37 GB/s whatever the number of busy SMs (measured on
+// GB300), so what decides is how many SMs a plan keeps streaming and for how
+// long.  Measured against the split-K kernel (M <= 16) and the single-CTA
+// tiled kernel (16 < M <= 128), the 64-row units win while they fit in one
+// wave, and for M <= 16 in two; with more units the others read B as fast and
+// are kept.  GB3_GEMM_SMALL_M = 0 or 1 forces the choice.
+bool use_small_m(int64_t batch, int64_t M, int64_t N, int64_t K, int sms) {
+  (void)K;
+  if (M > kSmallMMaxM) return false;
+  const int force = env_int("GB3_GEMM_SMALL_M", -1);
+  if (force == 0 || force == 1) return force == 1;
+  const int64_t units = batch * ceil_div(N, kSmallRows);
+  return units <= sms || (M <= kSkinnyMaxM && units <= 2 * static_cast<int64_t>(sms));
+}
 
 template <int BN>
 constexpr int pair_smem_bytes() {
@@ -224,6 +265,28 @@ int64_t pair_workspace_bytes(const PairChoice& c) {
 
 // pair_slots: CTA pairs that fit on the device at once (0: assume sms / 2,
 // negative: pair kernels unavailable).
+// The split-K kernel's plan for an M <= 16, K > 0 problem (also the plan of
+// the allocation-free entry point, which runs that kernel whatever plan_gemm
+// would choose).
+int plan_skinny(int64_t batch, int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl) {
+  (void)M;
+  const int64_t nb = ceil_div(N, kSkinnyRows), kb = ceil_div(K, kBK);
+  int s, kbp;
+  choose_split(batch * nb, kb, sms, &s, &kbp);
+  pl->kernel = K_SKINNY;
+  pl->tile_m = kSkinnyRows;
+  pl->tile_n = kSkinnyNX;
+  pl->tile_k = kBK;
+  pl->stages = kSkinnyStages;
+  pl->split_k = s;
+  pl->tiles = batch * nb * s;
+  pl->grid = static_cast<int>(std::min<int64_t>(pl->tiles, sms));
+  pl->smem_bytes = CfgSkinny::kSmemBytes;
+  pl->launches = 1;
+  pl->stage_tx_bytes = CfgSkinny::kStageBytes;
+  return GEMM_OK;
+}
+
 int plan_gemm(int64_t batch, int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl,
               int pair_slots = 0, bool allow_split = true, bool row_stats = false) {
   std::memset(pl, 0, sizeof(*pl));
@@ -237,24 +300,23 @@ int plan_gemm(int64_t batch, int64_t M, int64_t N, int64_t K, int sms, gemm_plan
     return GEMM_OK;
   }
   pl->tile_k = kBK;
-  // Row reductions run in the tile epilogues; the swapped-operand M <= 16
-  // kernel holds rows across threads, so those problems take the tiled path.
-  if (M <= kSkinnyMaxM && !row_stats) {
-    const int64_t nb = ceil_div(N, kSkinnyRows), kb = ceil_div(K, kBK);
-    int s, kbp;
-    choose_split(batch * nb, kb, sms, &s, &kbp);
-    pl->kernel = K_SKINNY;
-    pl->tile_m = kSkinnyRows;
-    pl->tile_n = kSkinnyNX;
-    pl->stages = kSkinnyStages;
-    pl->split_k = s;
-    pl->tiles = batch * nb * s;
+  // Row reductions run in the tile epilogues; the swapped-operand kernels hold
+  // rows across threads, so those problems take the tiled path.
+  if (!row_stats && use_small_m(batch, M, N, K, sms)) {
+    const int nx = smallm_nx(M);
+    pl->kernel = K_SMALL_M;
+    pl->tile_m = kSmallRows;
+    pl->tile_n = nx;
+    pl->split_k = 1;
+    pl->tiles = batch * ceil_div(N, kSmallRows);
     pl->grid = static_cast<int>(std::min<int64_t>(pl->tiles, sms));
-    pl->smem_bytes = CfgSkinny::kSmemBytes;
+    pl->stages = smallm_stages(nx);
+    pl->smem_bytes = smallm_smem(nx);
     pl->launches = 1;
-    pl->stage_tx_bytes = CfgSkinny::kStageBytes;
+    pl->stage_tx_bytes = kSmallRows * kBK * 2 + static_cast<int64_t>(nx) * kBK * 2;
     return GEMM_OK;
   }
+  if (M <= kSkinnyMaxM && !row_stats) return plan_skinny(batch, M, N, K, sms, pl);
   if (M >= kPairMinM && pair_slots >= 0) {
     const int slots = pair_slots > 0 ? pair_slots : std::max(1, sms / 2);
     const PairChoice c = choose_pair(batch, M, N, K, slots, allow_split);
@@ -1002,7 +1064,7 @@ int run_skinny(const gemm_plan& pl, int dev, const Problem& q, cudaStream_t stre
   auto kern = gemm_skinny_kernel<kSkinnyStages>;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if ((st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), pl.smem_bytes)) !=
+    if ((st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), CfgSkinny::kSmemBytes)) !=
         GEMM_OK)
       return st;
     if (p.splits > 1) {
@@ -1014,7 +1076,53 @@ int run_skinny(const gemm_plan& pl, int dev, const Problem& q, cudaStream_t stre
       p.counters = g_dev[dev].counters;
     }
   }
-  return launch(kern, pl.grid, kThreads, pl.smem_bytes, stream, tmW, tmX, p);
+  return launch(kern, pl.grid, kThreads, CfgSkinny::kSmemBytes, stream, tmW, tmX, p);
+}
+
+template <int NX>
+int launch_smallm(const gemm_plan& pl, int dev, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                  const SmallMParams& p, cudaStream_t stream) {
+  auto kern = gemm_smallm_kernel<NX>;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const int st =
+        ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), SmallMCfg<NX>::kSmemBytes);
+    if (st != GEMM_OK) return st;
+  }
+  return launch(kern, pl.grid, kThreads, SmallMCfg<NX>::kSmemBytes, stream, tmW, tmX, p);
+}
+
+int run_smallm(const gemm_plan& pl, int dev, const Problem& q, cudaStream_t stream) {
+  const int nx = pl.tile_n;
+  CUtensorMap tmW, tmX;
+  int st;
+  if ((st = operand_map(&tmW, q.B, q.in_dtype, q.K, q.N, q.batch, q.ldb, q.sb, kSmallRows)) !=
+      GEMM_OK)
+    return st;
+  if ((st = operand_map(&tmX, q.A, q.in_dtype, q.K, q.M, q.batch, q.lda, q.sa, nx)) != GEMM_OK)
+    return st;
+  SmallMParams p;
+  p.M = static_cast<int>(q.M);
+  p.N = static_cast<int>(q.N);
+  p.K = static_cast<int>(q.K);
+  p.n_blocks = static_cast<int>(ceil_div(q.N, kSmallRows));
+  p.k_blocks = static_cast<int>(ceil_div(q.K, kBK));
+  p.batch = static_cast<int>(q.batch);
+  p.num_units = static_cast<int>(pl.tiles);
+  p.alpha = q.alpha;
+  p.beta = q.beta;
+  p.C = q.C;
+  p.ldc = q.ldc;
+  p.c_stride = q.batch > 1 ? q.sc : 0;
+  p.out_kind = q.out_dtype;
+  p.idesc = idesc_f32_acc(kSmallRows, nx, q.in_dtype == GEMM_IN_F16);
+  switch (nx) {
+    case 16: return launch_smallm<16>(pl, dev, tmW, tmX, p, stream);
+    case 32: return launch_smallm<32>(pl, dev, tmW, tmX, p, stream);
+    case 64: return launch_smallm<64>(pl, dev, tmW, tmX, p, stream);
+    case 128: return launch_smallm<128>(pl, dev, tmW, tmX, p, stream);
+    default: return GEMM_ERR_UNSUPPORTED;
+  }
 }
 
 int run_problem(const Problem& q, void* stream_) {
@@ -1050,6 +1158,8 @@ int run_problem(const Problem& q, void* stream_) {
       return run_pair(pl, dev, slots, q, stream);
     case K_SKINNY:
       return run_skinny(pl, dev, q, stream);
+    case K_SMALL_M:
+      return run_smallm(pl, dev, q, stream);
     default:
       return run_single(pl, dev, q, stream);
   }
@@ -1348,8 +1458,13 @@ extern "C" int gemm_bf16_skinny_noalloc(int64_t M, int64_t N, int64_t K, float a
     sms = g_dev[dev].sms;
   }
   gemm_plan pl;
-  plan_gemm(1, M, N, K, sms, &pl);
-  if (pl.kernel == K_SCALE) return run_scale(pl, C, ldc, 0, 1, M, N, beta, out_dtype, stream);
+  if (K == 0) {
+    plan_gemm(1, M, N, K, sms, &pl);   // the scaling of C alone
+    return run_scale(pl, C, ldc, 0, 1, M, N, beta, out_dtype, stream);
+  }
+  // Always the split-K kernel, with its own plan and shared-memory size.
+  std::memset(&pl, 0, sizeof(pl));
+  plan_skinny(1, M, N, K, sms, &pl);
 
   SkinnyParams p = skinny_params(pl, q);
   const size_t counter_bytes =
@@ -1375,7 +1490,7 @@ extern "C" int gemm_bf16_skinny_noalloc(int64_t M, int64_t N, int64_t K, float a
     if (!g_noalloc_smem_set[dev]) {
       if (cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               pl.smem_bytes) != cudaSuccess) {
+                               CfgSkinny::kSmemBytes) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
       }
@@ -1402,5 +1517,5 @@ extern "C" int gemm_bf16_skinny_noalloc(int64_t M, int64_t N, int64_t K, float a
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
-  return launch(kern, pl.grid, kThreads, pl.smem_bytes, stream, tmW, tmX, p);
+  return launch(kern, pl.grid, kThreads, CfgSkinny::kSmemBytes, stream, tmW, tmX, p);
 }

@@ -287,9 +287,10 @@ GEMM_API int gemm_selftest_wait_timeout(int64_t limit_ns, void *stream);
 /* How a call would be executed (host-side planning only). */
 typedef struct gemm_plan {
     int kernel;       /* 0 none, 1 single-CTA tiled GEMM, 2 skinny split-K, 3 scale only (K == 0),
-                         4 single-CTA gate/up, 5 CTA-pair tiled GEMM, 6 CTA-pair gate/up */
-    int tile_m;       /* output rows per tile (tcgen05 M, or weight rows for the skinny path) */
-    int tile_n;       /* output columns per tile */
+                         4 single-CTA gate/up, 5 CTA-pair tiled GEMM, 6 CTA-pair gate/up,
+                         7 small-M (64-row weight tiles, whole K, no workspace) */
+    int tile_m;       /* output rows per tile (tcgen05 M, or weight rows for kernels 2 and 7) */
+    int tile_n;       /* output columns per tile (activation rows for kernels 2 and 7) */
     int tile_k;       /* K per pipeline stage */
     int stages;       /* shared-memory ring depth */
     int split_k;      /* K splits (skinny path), else 1 */
@@ -306,7 +307,10 @@ typedef struct gemm_plan {
  * host logic otherwise; returns GEMM_INVALID_ARG for invalid sizes or dtype.
  * M > 128 runs on CTA pairs (256-row tiles) with the tile width that needs the
  * fewest waves; the environment variable GB3_GEMM_PAIR_TILE_N (256 or 224)
- * forces one width, for tuning and tests.
+ * forces one width, for tuning and tests.  M <= 128 runs on the small-M
+ * kernel when its waves of 64-row weight units stream less of B per SM than
+ * the alternative (the split-K kernel for M <= 16, the single-CTA tiled
+ * kernel above); GB3_GEMM_SMALL_M = 1 or 0 forces or forbids it.
  */
 GEMM_API int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int num_sms,
                    gemm_plan *plan);

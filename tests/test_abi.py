@@ -178,7 +178,8 @@ def test_plan_split_overrides(lib, monkeypatch):
     assert p.tiles == tiles * 3
 
 
-def test_plan_single_cta_below_two_row_blocks(lib):
+def test_plan_single_cta_below_two_row_blocks(lib, monkeypatch):
+    monkeypatch.setenv("GB3_GEMM_SMALL_M", "0")
     st, p = _native.gemm_bf16_plan(128, 4096, 4096, _native.GEMM_OUT_BF16, 152)
     d = p.as_dict()
     assert st == 0 and d["kernel_name"] == "tiled"
@@ -321,10 +322,11 @@ def row_stats_plan(M, N, K, out=BF16):
 def test_row_stats_plans():
     # M <= 16 takes the 128-row tiled kernel instead of the swapped-operand one
     assert row_stats_plan(16, 4096, 4096)["kernel_name"] == "tiled"
-    assert _native.gemm_batched_plan(1, 16, 4096, 4096, 0, BF16, 148)[1].as_dict()[
+    assert row_stats_plan(16, 28672, 8192)["kernel_name"] == "tiled"
+    assert _native.gemm_batched_plan(1, 16, 28672, 8192, 0, BF16, 148)[1].as_dict()[
         "kernel_name"] == "skinny_splitk"
-    # otherwise the same plan as the plain GEMM
-    for shape in [(64, 1000, 512), (4096, 4096, 4096), (3000, 5000, 2000)]:
+    # above M = 128 the same plan as the plain GEMM
+    for shape in [(300, 520, 200), (4096, 4096, 4096), (3000, 5000, 2000)]:
         a = row_stats_plan(*shape)
         b = _native.gemm_batched_plan(1, *shape, 0, BF16, 148)[1].as_dict()
         assert a == b
@@ -334,3 +336,57 @@ def test_row_stats_plans():
     # N == 0: only the empty-row reductions
     n0 = row_stats_plan(64, 0, 64)
     assert n0["kernel_name"] == "scale" and n0["launches"] == 1
+
+
+# ---------------------------------------------------------------------------
+# The small-M kernel: 64-row weight units over the whole of K, no workspace
+# ---------------------------------------------------------------------------
+def plan(M, N, K, batch=1, sms=152):
+    st, p = _native.gemm_batched_plan(batch, M, N, K, 0, BF16, sms)
+    assert st == _native.GEMM_OK
+    return p.as_dict()
+
+
+def test_plan_small_m_routing(lib):
+    # 64-row units that fit in one wave (two for M <= 16) take the small-M kernel
+    assert plan(64, 4096, 4096)["kernel_name"] == "small_m"          # 64 units
+    assert plan(96, 8192, 8192)["kernel_name"] == "small_m"          # 128 units
+    assert plan(16, 14336, 4096)["kernel_name"] == "small_m"         # 224 units, M <= 16
+    assert plan(128, 14336, 4096)["kernel_name"] == "tiled"          # 224 units, M > 16
+    assert plan(64, 28672, 8192)["kernel_name"] == "tiled"           # 448 units
+    assert plan(16, 28672, 8192)["kernel_name"] == "skinny_splitk"   # 448 units
+    assert plan(300, 4096, 4096)["kernel_name"] == "pair"            # M > 128
+    import workloads
+    w = workloads.WORKLOADS["smallm_16x14336x4096"]
+    assert plan(w.M, w.N, w.K)["kernel_name"] == "small_m"
+
+
+def test_plan_small_m_decode_shape(lib, monkeypatch):
+    monkeypatch.setenv("GB3_GEMM_SMALL_M", "1")
+    d = plan(64, 28672, 8192)
+    assert d["kernel_name"] == "small_m" and d["split_k"] == 1
+    assert d["tile_m"] == 64 and d["tile_n"] == 64
+    assert d["tiles"] == 28672 // 64 and d["grid"] == 152
+    assert d["stage_tx_bytes"] == 64 * 64 * 2 + 64 * 64 * 2
+    assert d["stages"] == 200 * 1024 // d["stage_tx_bytes"]
+    assert d["smem_bytes"] <= 232448
+
+
+@pytest.mark.parametrize("M,nx", [(1, 16), (16, 16), (17, 32), (32, 32), (33, 64), (64, 64),
+                                  (65, 128), (128, 128)])
+def test_plan_small_m_activation_tile(lib, monkeypatch, M, nx):
+    monkeypatch.setenv("GB3_GEMM_SMALL_M", "1")
+    d = plan(M, 5000, 1000, batch=3)
+    assert d["kernel_name"] == "small_m" and d["tile_n"] == nx
+    assert d["tiles"] == 3 * -(-5000 // 64)
+
+
+def test_plan_small_m_limits(lib, monkeypatch):
+    monkeypatch.setenv("GB3_GEMM_SMALL_M", "1")
+    assert plan(129, 28672, 8192)["kernel_name"] == "pair"      # above the widest tile
+    assert plan(64, 28672, 0)["kernel_name"] == "scale"         # K == 0
+    st, p = _native.gemm_row_stats_plan(1, 64, 28672, 8192, 0, BF16, 152)
+    assert p.as_dict()["kernel_name"] == "tiled"                # row reductions need rows
+    monkeypatch.setenv("GB3_GEMM_SMALL_M", "0")
+    assert plan(64, 28672, 8192)["kernel_name"] == "tiled"
+    assert plan(16, 28672, 8192)["kernel_name"] == "skinny_splitk"

@@ -75,14 +75,20 @@ EXACT_SHAPES = [
     (17, 296, 64),       # just above the skinny threshold
     (256, 256, 8),       # K smaller than one k-block
     (200, 264, 72),      # K tail of 8
-    (16, 1000, 4096),    # skinny split-K
-    (3, 520, 1000),      # skinny, M < 16, ragged N
+    (16, 1000, 4096),    # M <= 16: small-M kernel, or the split-K kernel when forced
+    (3, 520, 1000),      # M < 16, ragged N
 ]
 
 
 @pytest.mark.parametrize("M,N,K", EXACT_SHAPES)
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-def test_integer_inputs_bit_exact(g, M, N, K, out_dtype):
+@pytest.mark.parametrize("route", ["planned", "no_small_m"])
+def test_integer_inputs_bit_exact(g, M, N, K, out_dtype, route, monkeypatch):
+    if route == "no_small_m":
+        if M > 16:
+            pytest.skip("the route only changes for M <= 16")
+        monkeypatch.setenv("GB3_GEMM_SMALL_M", "0")   # the split-K kernel
+        assert g.plan(M, N, K, out_dtype)["kernel_name"] == "skinny_splitk"
     A, B, _ = int_inputs(M, N, K, seed=M + N + K)
     ref, _ = oracle.gemm_full(A, B)
     out = run_gemm(g, A, B, out_dtype=out_dtype)

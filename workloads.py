@@ -118,6 +118,17 @@ WORKLOADS = {
         "gemm_batched_8x2048", "gemm", 2048, 2048, 2048, seed=6,
         dist_a=("normal", 1.0), dist_b=("normal", 1.0), out_bf16=True, batch=8,
         notes="8 independent 2048^3 BF16 GEMMs, one call"),
+    # A decode batch of 64 rows: the small-M kernel's home ground.
+    "smallm_64x28672x8192": Workload(
+        "smallm_64x28672x8192", "gemm", 64, 28672, 8192, seed=10,
+        dist_a=("normal", 1.0), dist_b=("normal", 1.0 / math.sqrt(8192)),
+        out_bf16=True, check="sampled",
+        notes="decode batch of 64, weight 470 MB, HBM-bound"),
+    "smallm_16x14336x4096": Workload(
+        "smallm_16x14336x4096", "gemm", 16, 14336, 4096, seed=11,
+        dist_a=("normal", 1.0), dist_b=("normal", 1.0 / 64.0),
+        out_bf16=True, check="sampled",
+        notes="decode batch of 16 through a 4096 x 14336 projection (117 MB)"),
     # Row reductions and the row normalisation (the row after those).
     "gemm_row_stats_4096": Workload(
         "gemm_row_stats_4096", "gemm_row_stats", 4096, 4096, 4096, seed=1,
