@@ -35,9 +35,13 @@ Contents
   a transfer": a reduction along the second axis of a loaded accumulator;
   "TMA and Hopper WGMMA", section "WGMMA values and ownership": sum, maximum
   and minimum along axis 2 of a finished accumulator), over the whole row.
+* ``attention_rows``: ``softmax(scale * q.K^T) . V`` for chosen query rows
+  ("Tiles and shared memory", section "How long a tile lives": the
+  flash-attention loop with a running maximum and sum, finished by acc / l),
+  evaluated directly over all keys.
 * ``gemm_tolerance`` / ``gate_up_tolerance`` / ``rms_norm_tolerance`` /
-  ``row_stats_tolerance``: the admissible distance between a result computed
-  in FP32 and the float64 reference.
+  ``row_stats_tolerance`` / ``attention_tolerance``: the admissible distance
+  between a result computed in FP32 and the float64 reference.
 
 Every function here is pinned in ``tests/test_oracle.py`` to closed forms,
 identities, brute force on tiny shapes and library routines.
@@ -104,6 +108,9 @@ def _load():
             lib.oracle_gate_up_entries_f64.argtypes = [
                 _i64, _vp, _i64, _vp, _vp, _i64,
                 _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+            lib.oracle_attention_rows.restype = None
+            lib.oracle_attention_rows.argtypes = [
+                _i64, _i64, _i64, _dbl, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp]
             lib.oracle_gate_up_entries.restype = None
             lib.oracle_gate_up_entries.argtypes = [
                 _i64, _vp, _i64, _vp, _vp, _i64,
@@ -326,6 +333,39 @@ def gemm_row_stats(A, B, rows, alpha=1.0, beta=0.0, C=None, in_f16=None):
 
 
 # --------------------------------------------------------------------------
+# attention
+# --------------------------------------------------------------------------
+def attention_rows(Q, K, V, scale: float, heads, rows):
+    """Rows of ``O = softmax(scale * Q.K^T) . V`` per head.
+
+    ``Q`` is (H, Nq, D), ``K`` and ``V`` are (H, Nk, D), BF16 (torch tensors or
+    uint16 bits); ``heads[i]``, ``rows[i]`` name the query rows.  Returns a
+    dict of float64 arrays: ``o`` and ``abs_o`` (len(rows), D) and ``smax``
+    (len(rows),): ``abs_o = sum_j w_j |v_j|`` with the softmax weights w and
+    ``smax = |scale| max_j sum_d |q_d k_jd|``, both for the tolerance.
+    """
+    q, k, v = _as_bits(Q), _as_bits(K), _as_bits(V)
+    H, Nq, D = q.shape
+    _, Nk, _ = k.shape
+    if k.shape != (H, Nk, D) or v.shape != (H, Nk, D):
+        raise ValueError("K and V must be (H, Nk, D) with Q's H and D")
+    if Nk < 1:
+        raise ValueError("attention needs at least one key")
+    h = np.ascontiguousarray(heads, dtype=np.int64)
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    if h.shape != r.shape:
+        raise ValueError("heads and rows differ in length")
+    if r.size and (h.min() < 0 or h.max() >= H or r.min() < 0 or r.max() >= Nq):
+        raise IndexError("query row outside Q")
+    o = np.empty((r.size, D), np.float64)
+    ab = np.empty((r.size, D), np.float64)
+    smax = np.empty(r.size, np.float64)
+    _load().oracle_attention_rows(Nq, Nk, D, float(scale), _ptr(q), _ptr(k), _ptr(v), r.size,
+                                  _ptr(h), _ptr(r), _ptr(o), _ptr(ab), _ptr(smax))
+    return {"o": o, "abs_o": ab, "smax": smax}
+
+
+# --------------------------------------------------------------------------
 # BF16 encoding
 # --------------------------------------------------------------------------
 def bf16_bits_to_f64(bits) -> np.ndarray:
@@ -494,3 +534,36 @@ def row_stats_tolerance(stats, alpha, beta):
     gamma = N * U32 / (1.0 - N * U32)
     return {"sum": t.sum(axis=1) + gamma * (np.abs(v) + t).sum(axis=1),
             "max": t.max(axis=1), "min": t.max(axis=1)}
+
+
+def fp32_sum_rel(n: int) -> float:
+    """Relative error bound of an FP32 sum of n exact terms in any order,
+    each addition rounding (or truncating) with error at most 2u:
+    ``2 n u``."""
+    return 2.0 * n * U32
+
+
+def attention_tolerance(res, D: int, Nk: int, out_bf16=True):
+    """Admissible |O_gpu - O_ref| for attention computed as a flash loop in FP32
+    with BF16 probabilities.
+
+    * Scores: each is an FP32 accumulation of D exact BF16 products, so it is
+      within ``fp32_sum_rel(D) sum|q k|`` and the scaled score within
+      ``e = fp32_sum_rel(D) * smax`` of the exact one.
+    * Weights: exp and the running rescaling keep ratios between keys, so a
+      score shift of at most e moves each normalised weight by a factor within
+      ``exp(+-2e)``; the BF16 probabilities add 2^-9, the exp evaluation
+      2^-20, the FP32 sum of the Nk probabilities ``fp32_sum_rel(Nk)``:
+      ``eta = exp(2e)(1 + 2^-9)(1 + 2^-20)(1 + fp32_sum_rel(Nk)) - 1``.
+    * Output: the FP32 products of weights and values over Nk keys
+      (``fp32_sum_rel(Nk)``), the per-block rescaling (Nk/128 + 2 roundings)
+      and the final division: all relative to ``abs_o = sum_j w_j |v_j|``.
+    Plus the BF16 half-ulp of a BF16 output.
+    """
+    e = fp32_sum_rel(D) * res["smax"][:, None]
+    eta = np.exp(2.0 * e) * (1 + 2.0 ** -9) * (1 + 2.0 ** -20) * (1 + fp32_sum_rel(Nk)) - 1.0
+    acc = fp32_sum_rel(Nk) + (Nk / 128.0 + 2.0) * U32
+    tol = (eta + acc * (1.0 + eta)) * res["abs_o"]
+    if out_bf16:
+        tol = tol + bf16_half_ulp(np.abs(res["o"]) + tol)
+    return tol

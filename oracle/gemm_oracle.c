@@ -32,6 +32,15 @@
  *          per-column gain).  The normalised activation then feeds the gate/up
  *          projection in oracle_gate_up_entries_f64.
  *
+ *   attention  s(i,j) = sum_d q(i,d) k(j,d),  t = scale * s,
+ *              o(i,d) = sum_j exp(t(i,j) - max_j t(i,j)) v(j,d) / sum_j exp(...)
+ *          ("Tiles and shared memory", section "How long a tile lives": the
+ *          flash-attention loop keeps a query tile, a running maximum m and a
+ *          running sum l across the key loop, takes s = dot_t(q, k) per key
+ *          tile and finishes with acc / l -- the online form of the softmax
+ *          attention above, which the oracle evaluates directly, in one pass
+ *          over all keys).
+ *
  * Operands are BF16 or, for the FP16 variant, IEEE binary16 ("TMEM tiles and
  * transfers", section "Representation and windows": FP16 values packed with
  * pack(Float16, f)); the GEMM functions take the operand type as in_f16.
@@ -47,6 +56,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -282,5 +292,59 @@ void oracle_gate_up_entries_f64(int64_t K, const double *Xd, int64_t ldx,
         if (u_out) u_out[i] = u;
         if (abs_g) abs_g[i] = ag;
         if (abs_u) abs_u[i] = au;
+    }
+}
+
+/*
+ * Attention rows.  For each i in 0..count-1, query row qi = qrow[i] of head
+ * h = head[i]: Q(h,qi,d) at Q[(h*Nq + qi)*D + d], K(h,j,d) at K[(h*Nk + j)*D + d],
+ * V likewise (all BF16, contiguous).  Writes o[i*D + d], abs_o[i*D + d] =
+ * sum_j w_j |v(j,d)| (w the softmax weights) and smax[i] = scale *
+ * max_j sum_d |q k| (both for the tolerance).  Scores are float64 dot
+ * products in d order; the maximum is subtracted before exp (exact in real
+ * arithmetic); sums run over j in order.  `work` holds Nk doubles per thread.
+ */
+void oracle_attention_rows(int64_t Nq, int64_t Nk, int64_t D, double scale,
+                           const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                           int64_t count, const int64_t *head, const int64_t *qrow,
+                           double *o, double *abs_o, double *smax)
+{
+#pragma omp parallel
+    {
+        double *t = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t i = 0; i < count; ++i) {
+            const uint16_t *q = Q + (head[i] * Nq + qrow[i]) * D;
+            const uint16_t *kb = K + head[i] * Nk * D, *vb = V + head[i] * Nk * D;
+            double mx = -INFINITY, amax = 0.0;
+            for (int64_t j = 0; j < Nk; ++j) {
+                double sum = 0.0, a = 0.0;
+                for (int64_t d = 0; d < D; ++d) {
+                    double pr = bf16_to_double(q[d]) * bf16_to_double(kb[j * D + d]);
+                    sum += pr;
+                    a += fabs(pr);
+                }
+                t[j] = scale * sum;
+                if (t[j] > mx) mx = t[j];
+                if (a > amax) amax = a;
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < Nk; ++j) {
+                t[j] = exp(t[j] - mx);
+                l += t[j];
+            }
+            for (int64_t d = 0; d < D; ++d) {
+                double acc = 0.0, aa = 0.0;
+                for (int64_t j = 0; j < Nk; ++j) {
+                    double v = bf16_to_double(vb[j * D + d]);
+                    acc += t[j] * v;
+                    aa += t[j] * fabs(v);
+                }
+                o[i * D + d] = acc / l;
+                abs_o[i * D + d] = aa / l;
+            }
+            smax[i] = fabs(scale) * amax;
+        }
+        free(t);
     }
 }

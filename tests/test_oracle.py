@@ -509,3 +509,115 @@ def test_row_stats_tolerance_flags_a_planted_error():
     # FP32 evaluation of the same sums stays inside the bound
     v32 = s["values"].astype(np.float32)
     assert np.all(np.abs(v32.sum(axis=1, dtype=np.float32) - s["sum"]) <= tol["sum"])
+
+
+# ---------------------------------------------------------------------------
+# Attention ("Tiles and shared memory", section "How long a tile lives")
+# ---------------------------------------------------------------------------
+def _attn_inputs(H, Nq, Nk, D, seed):
+    gen = torch.Generator().manual_seed(seed)
+    Q = torch.randn(H, Nq, D, generator=gen).to(torch.bfloat16)
+    K = torch.randn(H, Nk, D, generator=gen).to(torch.bfloat16)
+    V = torch.randn(H, Nk, D, generator=gen).to(torch.bfloat16)
+    return Q, K, V
+
+
+def _all_rows(H, Nq):
+    hh, rr = np.meshgrid(np.arange(H), np.arange(Nq), indexing="ij")
+    return hh.ravel(), rr.ravel()
+
+
+def test_attention_zero_scale_is_the_mean_of_V():
+    """With scale 0 every score is equal: the output is the plain mean of V."""
+    Q, K, V = _attn_inputs(2, 3, 9, 8, 40)
+    h, r = _all_rows(2, 3)
+    res = oracle.attention_rows(Q, K, V, 0.0, h, r)
+    mean = V.double().mean(dim=1).numpy()
+    assert np.allclose(res["o"], mean[h], rtol=1e-14, atol=1e-15)
+
+
+def test_attention_single_key_returns_its_value():
+    Q, K, V = _attn_inputs(2, 4, 1, 16, 41)
+    h, r = _all_rows(2, 4)
+    res = oracle.attention_rows(Q, K, V, 0.7, h, r)
+    assert np.array_equal(res["o"], V.double().numpy()[h, 0])
+
+
+def test_attention_identical_keys_give_the_mean_of_V():
+    """Equal keys give equal scores whatever the query (a wrong axis in the
+    score, or a missing normalisation, would not)."""
+    Q, K, V = _attn_inputs(1, 5, 6, 8, 42)
+    K = K[:, :1].expand(1, 6, 8).contiguous()
+    h, r = _all_rows(1, 5)
+    res = oracle.attention_rows(Q, K, V, 1.3, h, r)
+    assert np.allclose(res["o"], V.double().mean(dim=1).numpy()[h], rtol=1e-13, atol=1e-14)
+
+
+def test_attention_dominant_key_selects_its_value():
+    """One key scoring 100 above the rest carries weight 1 - O(e^-100)."""
+    D, Nk = 8, 5
+    Q = torch.zeros(1, 1, D)
+    Q[0, 0, 0] = 10.0
+    K = torch.zeros(1, Nk, D)
+    K[0, 3, 0] = 10.0
+    V = torch.randn(1, Nk, D, generator=torch.Generator().manual_seed(43))
+    res = oracle.attention_rows(Q.to(torch.bfloat16), K.to(torch.bfloat16),
+                                V.to(torch.bfloat16), 1.0, [0], [0])
+    assert np.allclose(res["o"][0], V.to(torch.bfloat16).double().numpy()[0, 3], rtol=0,
+                       atol=1e-40)
+
+
+def test_attention_is_invariant_to_key_order():
+    Q, K, V = _attn_inputs(1, 4, 11, 16, 44)
+    perm = torch.randperm(11, generator=torch.Generator().manual_seed(45))
+    h, r = _all_rows(1, 4)
+    a = oracle.attention_rows(Q, K, V, 0.3, h, r)
+    b = oracle.attention_rows(Q, K[:, perm], V[:, perm], 0.3, h, r)
+    assert np.allclose(a["o"], b["o"], rtol=1e-13, atol=1e-14)
+
+
+def test_attention_against_torch_float64_softmax():
+    Q, K, V = _attn_inputs(3, 6, 37, 32, 46)
+    h, r = _all_rows(3, 6)
+    res = oracle.attention_rows(Q, K, V, 32 ** -0.5, h, r)
+    s = 32 ** -0.5 * Q.double() @ K.double().transpose(1, 2)
+    w = torch.softmax(s, dim=-1)
+    ref = (w @ V.double()).numpy()[h, r]
+    assert np.allclose(res["o"], ref, rtol=1e-12, atol=1e-14)
+    assert np.allclose(res["abs_o"], (w @ V.double().abs()).numpy()[h, r], rtol=1e-12)
+    amax = (Q.double().abs() @ K.double().abs().transpose(1, 2)).amax(dim=-1).numpy()[h, r]
+    assert np.allclose(res["smax"], 32 ** -0.5 * amax, rtol=1e-13)
+
+
+def _fp32_flash(q, k, v, scale, block=128):
+    """An FP32 flash loop over key blocks with BF16 probabilities, as the
+    GPU computes it, in numpy (independent of the oracle)."""
+    q, k, v = (np.asarray(x, np.float32) for x in (q, k, v))
+    m, l = np.float32(-np.inf), np.float32(0)
+    acc = np.zeros(q.shape[-1], np.float32)
+    for j0 in range(0, k.shape[0], block):
+        s = (k[j0:j0 + block] @ q).astype(np.float32) * np.float32(scale)
+        m_new = np.float32(max(m, s.max()))
+        alpha = np.float32(np.exp(np.float32(m - m_new))) if m != -np.inf else np.float32(0)
+        p = np.exp((s - m_new).astype(np.float32)).astype(np.float32)
+        pb = oracle.bf16_bits_to_f64(oracle.round_to_bf16_bits(p)).astype(np.float32)
+        l = np.float32(l * alpha + p.sum(dtype=np.float32))
+        acc = (acc * alpha + pb @ v[j0:j0 + block]).astype(np.float32)
+        m = m_new
+    return (acc / l).astype(np.float64)
+
+
+def test_attention_tolerance_covers_an_fp32_flash_loop():
+    H, Nq, Nk, D = 1, 8, 600, 64
+    Q, K, V = _attn_inputs(H, Nq, Nk, D, 47)
+    h, r = _all_rows(H, Nq)
+    res = oracle.attention_rows(Q, K, V, D ** -0.5, h, r)
+    tol = oracle.attention_tolerance(res, D, Nk, out_bf16=False)
+    qf, kf, vf = Q.float().numpy(), K.float().numpy(), V.float().numpy()
+    for i in range(Nq):
+        got = _fp32_flash(qf[0, i], kf[0], vf[0], D ** -0.5)
+        assert np.all(np.abs(got - res["o"][i]) <= tol[i])
+    # the bound is tight enough to flag a dropped or doubled key
+    assert np.all(tol > 0)
+    dropped = oracle.attention_rows(Q[:, :, :], K[:, 1:], V[:, 1:], D ** -0.5, h, r)
+    assert np.any(np.abs(dropped["o"] - res["o"]) > tol)
