@@ -548,8 +548,11 @@ def attention_tolerance(res, D: int, Nk: int, out_bf16=True):
     with BF16 probabilities.
 
     * Scores: each is an FP32 accumulation of D exact BF16 products, so it is
-      within ``fp32_sum_rel(D) sum|q k|`` and the scaled score within
-      ``e = fp32_sum_rel(D) * smax`` of the exact one.
+      within ``fp32_sum_rel(D) sum|q k|`` of the exact one.  The exponent
+      argument is then formed in FP32 from the score: the product with
+      scale * log2 e (itself rounded) and the subtraction of the running
+      maximum add at most 8 units of roundoff relative to |scale * s|.  So
+      the argument is within ``e = (fp32_sum_rel(D) + 8 u) * smax``.
     * Weights: exp and the running rescaling keep ratios between keys, so a
       score shift of at most e moves each normalised weight by a factor within
       ``exp(+-2e)``; the BF16 probabilities add 2^-9, the exp evaluation
@@ -560,7 +563,7 @@ def attention_tolerance(res, D: int, Nk: int, out_bf16=True):
       and the final division: all relative to ``abs_o = sum_j w_j |v_j|``.
     Plus the BF16 half-ulp of a BF16 output.
     """
-    e = fp32_sum_rel(D) * res["smax"][:, None]
+    e = (fp32_sum_rel(D) + 8.0 * U32) * res["smax"][:, None]
     eta = np.exp(2.0 * e) * (1 + 2.0 ** -9) * (1 + 2.0 ** -20) * (1 + fp32_sum_rel(Nk)) - 1.0
     acc = fp32_sum_rel(Nk) + (Nk / 128.0 + 2.0) * U32
     tol = (eta + acc * (1.0 + eta)) * res["abs_o"]
