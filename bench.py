@@ -190,6 +190,9 @@ def host_inputs(w):
     if w.kind == "rmsnorm_gate_up":
         X, G, Wg, Wu = workloads.inputs_for(w)
         return {"X": X, "G": G, "Wg": Wg, "Wu": Wu}
+    if w.kind == "attention":
+        Q, K, V = workloads.inputs_for(w)
+        return {"Q": Q, "K": K, "V": V}
     A, B, C = workloads.inputs_for(w)
     d = {"A": A, "B": B}
     if C is not None:
@@ -201,6 +204,8 @@ def out_shape(w):
     """Shape of the workload's main result."""
     if w.kind == "rms_norm":
         return (w.M, w.K)
+    if w.kind == "attention":
+        return (w.batch, w.M, w.K)
     return (w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N)
 
 
@@ -229,6 +234,8 @@ def call(lib, w, t, stream):
     if w.kind == "gemm_row_stats":
         return lib.gemm_row_stats(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta,
                                   stream=stream, stats=t["stats"])[0]
+    if w.kind == "attention":
+        return lib.attention(t["Q"], t["K"], t["V"], w.K ** -0.5, O=t["C"], stream=stream)
     return lib.gemm(t["A"], t["B"], t["C"], alpha=w.alpha, beta=w.beta, stream=stream)
 
 
@@ -243,6 +250,9 @@ def plan_of(lib, w):
     if w.kind == "rms_norm":
         return {"kernel_name": "rms_norm", "tile_n": w.K, "split_k": 1, "grid": None,
                 "launches": 1}
+    if w.kind == "attention":
+        return {"kernel_name": "attention", "tile_n": 128, "split_k": 1,
+                "grid": w.batch * -(-w.M // 128), "launches": 1}
     in_dt = torch.float16 if w.in_f16 else torch.bfloat16
     if w.kind == "gemm_row_stats":
         return lib.row_stats_plan(w.batch, w.M, w.N, w.K, in_dt, w.out_dtype)
@@ -356,6 +366,10 @@ def oracle_rows(w):
     elif w.kind == "rms_norm":
         def run(rows):
             oracle.rms_norm(h["X"], h["G"], w.eps, np.arange(rows))
+    elif w.kind == "attention":
+        def run(rows):
+            oracle.attention_rows(h["Q"], h["K"], h["V"], w.K ** -0.5, np.zeros(rows, np.int64),
+                                  np.arange(rows))
     else:
         A, B, C = first_matrix(h["A"], h["B"], h.get("C"))
 
@@ -369,6 +383,10 @@ def oracle_rows(w):
 
 def sample_text(w, rows):
     cols = f"all {w.K} columns" if w.kind == "rms_norm" else f"all {w.N} columns, K={w.K}"
+    if w.kind == "attention":
+        cols = f"all {w.K} columns over {w.N} keys, head 0 of {w.batch}"
+        return (f"query rows 0..{rows - 1} of {w.M} ({cols}); metric scaled to the full "
+                f"workload by the row fraction")
     return (f"output rows 0..{rows - 1} of {w.M}{sample_of(w)} ({cols}); "
             f"metric scaled to the full workload by the row fraction")
 
@@ -401,7 +419,8 @@ API = {"gemm": "gemm (C ABI gemm_bf16 / gemm_batched)",
        "gate_up": "gate_up_silu (C ABI gemm_gate_up_silu)",
        "gemm_row_stats": "gemm_row_stats (C ABI gemm_row_stats)",
        "rms_norm": "rms_norm (C ABI gemm_rms_norm)",
-       "rmsnorm_gate_up": "rmsnorm_gate_up_silu (C ABI gemm_rmsnorm_gate_up_silu)"}
+       "rmsnorm_gate_up": "rmsnorm_gate_up_silu (C ABI gemm_rmsnorm_gate_up_silu)",
+       "attention": "attention (C ABI gemm_attention)"}
 
 
 def compute_dtype(w) -> str:

@@ -10,6 +10,7 @@ tensors into that C ABI: PyTorch supplies device memory and streams.
     Y = silu(X @ Wg) * (X @ Wu)        gate_up_silu(X, Wg, Wu)
     Y = x / rms(x) * g  (per row)      rms_norm(X, G, eps)
     Y = gate_up_silu(rms_norm(X), ..)  rmsnorm_gate_up_silu(X, G, eps, Wg, Wu)
+    O = softmax(s Q.K^T) . V per head  attention(Q, K, V, scale)
 
 Operands are K-contiguous: ``A`` is (M, K) and ``B`` is passed as its (N, K)
 storage, so ``gemm(A, B)`` equals ``A @ B.T`` in torch notation.
@@ -23,7 +24,7 @@ from ._native import (GEMM_ERR_ALIGNMENT, GEMM_ERR_CUDA, GEMM_ERR_INVALID_ARG,  
                       GEMM_ERR_TIMEOUT, GEMM_ERR_UNSUPPORTED, GEMM_IN_BF16, GEMM_IN_F16,
                       GEMM_OK, GEMM_OUT_BF16, GEMM_OUT_F16, GEMM_OUT_F32, GemmError)
 
-__all__ = ["gemm", "gemm_row_stats", "gate_up_silu", "rms_norm", "rmsnorm_gate_up_silu",
+__all__ = ["gemm", "gemm_row_stats", "gate_up_silu", "rms_norm", "rmsnorm_gate_up_silu", "attention",
            "device_status", "plan", "batched_plan", "row_stats_plan", "gate_up_plan", "prepare",
            "GemmError", "library_path"]
 
@@ -213,6 +214,44 @@ def rmsnorm_gate_up_silu(X: torch.Tensor, G: torch.Tensor, eps: float, Wg: torch
     if st != GEMM_OK:
         raise GemmError(st, "gemm_rmsnorm_gate_up_silu")
     return Y, Xn
+
+
+def attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scale: float | None = None,
+              O: torch.Tensor | None = None, out_dtype: torch.dtype = torch.bfloat16,
+              stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """``O = softmax(scale * Q.K^T) . V`` per head (softmax over the keys).
+
+    Q: (heads, Nq, D) or (Nq, D); K, V: (heads, Nk, D) or (Nk, D); bfloat16,
+    D = 64 or 128.  ``scale`` defaults to 1/sqrt(D).  O: created when None
+    (``out_dtype`` float32 or bfloat16).
+    """
+    squeeze = Q.dim() == 2
+    if squeeze:
+        Q, K, V = Q.unsqueeze(0), K.unsqueeze(0), V.unsqueeze(0)
+        if O is not None:
+            O = O.unsqueeze(0)
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        _check_operand(name, t, (torch.bfloat16,), (3,))
+    H, Nq, D = Q.shape
+    Nk = K.shape[1]
+    if tuple(K.shape) != (H, Nk, D) or tuple(V.shape) != (H, Nk, D):
+        raise ValueError("K and V must be (heads, Nk, D) with Q's heads and D")
+    if scale is None:
+        scale = D ** -0.5
+    if O is None:
+        O = torch.empty((H, Nq, D), dtype=out_dtype, device=Q.device)
+    else:
+        _check_operand("O", O, (torch.float32, torch.bfloat16), (3,))
+        if tuple(O.shape) != (H, Nq, D):
+            raise ValueError(f"O must be {(H, Nq, D)}")
+    with torch.cuda.device(Q.device):
+        st = _native.gemm_attention(H, Nq, Nk, D, float(scale), Q.data_ptr(), _ld(Q), _bstride(Q),
+                                    K.data_ptr(), _ld(K), _bstride(K), V.data_ptr(), _ld(V),
+                                    _bstride(V), O.data_ptr(), _ld(O), _bstride(O),
+                                    _OUT_CODES[O.dtype], _stream(stream, Q.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_attention")
+    return O[0] if squeeze else O
 
 
 def gate_up_silu(X: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor,

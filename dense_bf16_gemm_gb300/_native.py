@@ -46,6 +46,7 @@ EXPORTED = (
     "gemm_row_stats_plan",
     "gemm_rms_norm",
     "gemm_rmsnorm_gate_up_silu",
+    "gemm_attention",
 )
 
 
@@ -141,6 +142,9 @@ def lib() -> ctypes.CDLL:
             l.gemm_rmsnorm_gate_up_silu.restype = _int
             l.gemm_rmsnorm_gate_up_silu.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _f32,
                                                     _vp, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
+            l.gemm_attention.restype = _int
+            l.gemm_attention.argtypes = [_i64, _i64, _i64, _i64, _f32, _vp, _i64, _i64, _vp, _i64,
+                                         _i64, _vp, _i64, _i64, _vp, _i64, _i64, _int, _vp]
             _lib = l
     return _lib
 
@@ -233,3 +237,9 @@ def gemm_rmsnorm_gate_up_silu(M, N, K, X, ldx, G, eps, Wg, Wu, ldw, Xn, ldxn, Y,
     return lib().gemm_rmsnorm_gate_up_silu(M, N, K, X or None, ldx, G or None, eps, Wg or None,
                                            Wu or None, ldw, Xn or None, ldxn, Y or None, ldy,
                                            stream or None)
+
+
+def gemm_attention(heads, Nq, Nk, D, scale, Q, ldq, sq, K, ldk, sk, V, ldv, sv, O, ldo, so,
+                   out_dtype, stream) -> int:
+    return lib().gemm_attention(heads, Nq, Nk, D, scale, Q or None, ldq, sq, K or None, ldk, sk,
+                                V or None, ldv, sv, O or None, ldo, so, out_dtype, stream or None)

@@ -1,0 +1,356 @@
+// attention.cuh -- softmax attention O = softmax(scale * Q.K^T) . V on the
+// tcgen05 tensor cores, as the flash-attention loop ("Tiles and shared
+// memory", section "How long a tile lives": a query tile, a running maximum m
+// and a running sum l kept across the key loop, s = dot_t(q, k) per key tile,
+// acc / l at the end).
+//
+// One CTA per (head, 128-row query block).  Per key block j of 128 keys:
+//
+//   S_j = Q . K_j^T                tcgen05.mma M = 128, N = 128 over D, into one of two
+//                                  TMEM score buffers (K_j is K-major: D contiguous)
+//   m_j = max(m_{j-1}, rowmax S_j)  softmax warps, one thread per query row: the row
+//   P_j = exp(S_j - m_j)            lives in that thread's TMEM lane, so the reduction
+//   l_j = l_{j-1} a_j + rowsum P_j  is thread-local; a_j = exp(m_{j-1} - m_j)
+//   O_j = P_j . V_j                tcgen05.mma M = 128, N = D over the 128 keys; P_j is
+//                                  BF16 in swizzled shared memory (K-major), V_j is
+//                                  the MN-major operand (D contiguous, as TMA loads it)
+//   acc = acc a_j + O_j            FP32 in the softmax threads' registers
+//
+// and finally O = acc / l.  Scores are handled in base-2 units (exp2 of
+// s * scale * log2 e), which is the same function.  Keys past Nk score -inf.
+//
+// Warp roles: warp 0 TMA (Q once, K_j and V_j through a ring), warp 1 MMA
+// issue and TMEM owner, warps 2-5 softmax and output.  The MMA warp issues
+// S_{j+1} before O_j, so the tensor core works on the next scores while the
+// softmax threads finish the current block.
+//
+// Every wait is bounded as in the GEMM kernels (status word, abort flag,
+// drained copies and MMAs, TMEM freed).
+#pragma once
+
+#include "gemm_kernels.cuh"
+
+namespace gb3 {
+
+constexpr int kAttnBR = 128;   // query rows per CTA (the MMA's M)
+constexpr int kAttnBC = 128;   // keys per block
+
+struct AttnParams {
+  int heads, Nq, Nk;
+  int q_blocks, k_blocks;     // ceil(Nq / 128), ceil(Nk / 128)
+  float scale_log2;           // scale * log2(e)
+  void* O;
+  long long ldo, o_stride;    // elements
+  int out_kind;               // 0 FP32, 1 BF16
+  uint32_t idesc_s;           // M = 128, N = 128, A and B K-major
+  uint32_t idesc_o;           // M = 128, N = D, B MN-major
+};
+
+template <int D>
+struct AttnCfg {
+  static_assert(D == 64 || D == 128, "head dimension");
+  static constexpr int kChunks = D / 64;                 // 64-element swizzle rows per row
+  static constexpr int kTileBytes = 128 * D * 2;         // Q, K_j or V_j (128 rows)
+  static constexpr int kStages = D == 128 ? 2 : 3;       // K/V ring depth
+  static constexpr int kStageBytes = 2 * kTileBytes;     // K_j and V_j
+  static constexpr int kPBytes = kAttnBR * kAttnBC * 2;  // 32 KB
+  static constexpr int kQOffset = 0;
+  static constexpr int kRingOffset = kTileBytes;
+  static constexpr int kPOffset = kRingOffset + kStages * kStageBytes;
+  static constexpr int kBarOffset = kPOffset + kPBytes;
+  // q_full, kv_full[S], kv_empty[S], s_full[2], s_empty[2], p_full, p_empty,
+  // o_full[2], o_empty[2], drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2 + 4 + 1;
+  static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+  static constexpr int kTmemCols = 512;                  // S: 2 x 128, O: 2 x D
+  static constexpr int kSCol = 0;
+  static constexpr int kOCol = 256;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// UMMA shared-memory descriptor of an MN-major operand in 128-byte swizzled
+// tiles as TMA writes a [rows = K][64 contiguous MN elements] box: eight-row
+// (K) groups 1024 bytes apart (SBO), consecutive 64-element MN chunks
+// `mn_chunk_bytes` apart (LBO).  Checked on GB300 against known products.
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t mn_chunk_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((mn_chunk_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using Cfg = AttnCfg<D>;
+  constexpr int S = Cfg::kStages;
+  constexpr int kChunkBytes = 128 * 128;  // one 64-element-wide swizzled chunk of 128 rows
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOffset);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t q_full = bar0;
+  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (1 + S + s); };
+  auto s_full = [&](int b) { return bar0 + 8u * (1 + 2 * S + b); };
+  auto s_empty = [&](int b) { return bar0 + 8u * (3 + 2 * S + b); };
+  const uint32_t p_full = bar0 + 8u * (5 + 2 * S);
+  const uint32_t p_empty = bar0 + 8u * (6 + 2 * S);
+  auto o_full = [&](int b) { return bar0 + 8u * (7 + 2 * S + b); };
+  auto o_empty = [&](int b) { return bar0 + 8u * (9 + 2 * S + b); };
+  const uint32_t drain_bar = bar0 + 8u * (11 + 2 * S);
+
+  const uint32_t q_smem = sb + Cfg::kQOffset;
+  auto k_smem = [&](int s) { return sb + Cfg::kRingOffset + static_cast<uint32_t>(s * Cfg::kStageBytes); };
+  auto v_smem = [&](int s) { return k_smem(s) + Cfg::kTileBytes; };
+  const uint32_t p_smem = sb + Cfg::kPOffset;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.x / p.q_blocks;
+  const int qb = blockIdx.x - h * p.q_blocks;
+  const int n = p.k_blocks;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(s_empty(b), kEpiWarps);
+      mbar_init(o_full(b), 1);
+      mbar_init(o_empty(b), kEpiWarps);
+    }
+    mbar_init(p_full, kEpiWarps);
+    mbar_init(p_empty, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, Cfg::kTileBytes);
+      for (int c = 0; c < Cfg::kChunks; ++c)
+        tma_load_3d(q_smem + c * kChunkBytes, &tmQ, q_full, c * 64, qb * kAttnBR, h);
+      int issued = 0;
+      for (int j = 0; j < n; ++j) {
+        const int s = j % S;
+        const uint32_t ph = static_cast<uint32_t>(j / S) & 1u;
+        if (!wait_bounded(kv_empty(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY)) break;
+        mbar_arrive_expect_tx(kv_full(s), Cfg::kStageBytes);
+        for (int c = 0; c < Cfg::kChunks; ++c) {
+          tma_load_3d(k_smem(s) + c * kChunkBytes, &tmK, kv_full(s), c * 64, j * kAttnBC, h);
+          tma_load_3d(v_smem(s) + c * kChunkBytes, &tmV, kv_full(s), c * 64, j * kAttnBC, h);
+        }
+        ++issued;
+      }
+      // Leave only when every issued copy has landed (bounded).
+      wait_bounded(q_full, 0, nullptr, SITE_DRAIN);
+      for (int j = issued > S ? issued - S : 0; j < issued; ++j)
+        wait_bounded(kv_full(j % S), static_cast<uint32_t>(j / S) & 1u, nullptr, SITE_DRAIN);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // S_j = Q . K_j^T into score buffer j % 2.
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % S, b = j & 1;
+        if (!wait_bounded(kv_full(s), static_cast<uint32_t>(j / S) & 1u, abort_flag, SITE_MMA_FULL))
+          return false;
+        if (!wait_bounded(s_empty(b), (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag,
+                          SITE_MMA_ACC_EMPTY))
+          return false;
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base + Cfg::kSCol + static_cast<uint32_t>(b * kAttnBC);
+#pragma unroll
+        for (int c = 0; c < Cfg::kChunks; ++c) {
+          const uint64_t qd = smem_desc_sw128(q_smem + c * kChunkBytes);
+          const uint64_t kd = smem_desc_sw128(k_smem(s) + c * kChunkBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(d, qd + 2u * kk, kd + 2u * kk, p.idesc_s, (c | kk) != 0 ? 1u : 0u);
+        }
+        umma_commit(s_full(b));
+        return true;
+      };
+      bool ok = wait_bounded(q_full, 0, abort_flag, SITE_MMA_FULL) && n > 0 && issue_s(0);
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n && !issue_s(j + 1)) break;
+        // O_j = P_j . V_j into output buffer j % 2.
+        const int s = j % S, b = j & 1;
+        if (!wait_bounded(p_full, static_cast<uint32_t>(j) & 1u, abort_flag, SITE_MMA_FULL)) break;
+        if (!wait_bounded(o_empty(b), (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag,
+                          SITE_MMA_ACC_EMPTY))
+          break;
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base + Cfg::kOCol + static_cast<uint32_t>(b * D);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint64_t pd = smem_desc_sw128(p_smem + c * kChunkBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t key_row = static_cast<uint32_t>(c * 64 + kk * 16);
+            umma_bf16(d, pd + 2u * kk, smem_desc_mn_sw128(v_smem(s) + key_row * 128u, kChunkBytes),
+                      p.idesc_o, (c | kk) != 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(o_full(b));
+        umma_commit(p_empty);
+        umma_commit(kv_empty(s));
+      }
+      // Leave only when every issued MMA has completed (bounded).
+      umma_commit(drain_bar);
+      wait_bounded(drain_bar, 0, nullptr, SITE_DRAIN);
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int row = 32 * quarter + lane;             // query row of this thread in the block
+    const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    float acc[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) acc[i] = 0.0f;
+    float m = -INFINITY, l = 0.0f, alpha_prev = 0.0f;
+    bool ok = true;
+    // acc = acc * alpha + O_j (read from TMEM), then hand the buffer back.
+    auto take_o = [&](int j, float alpha) -> bool {
+      const int b = j & 1;
+      const bool got = wait_bounded(o_full(b), static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
+                                    SITE_EPI_ACC_FULL);
+      if (!__all_sync(0xffffffffu, got)) return false;
+      tc_fence_after_sync();
+      const uint32_t to = tmem_base + lane_base + Cfg::kOCol + static_cast<uint32_t>(b * D);
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float o[32];
+        tmem_load_32x32b_x32(to + c0, o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[c0 + i] = fmaf(acc[c0 + i], alpha, o[i]);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty(b));
+      return true;
+    };
+    for (int j = 0; j < n; ++j) {
+      const int b = j & 1;
+      const bool got = wait_bounded(s_full(b), static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
+                                    SITE_EPI_ACC_FULL);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t ts = tmem_base + lane_base + Cfg::kSCol + static_cast<uint32_t>(b * kAttnBC);
+      const int col0 = j * kAttnBC;
+      // Pass 1: the row maximum of the scaled scores (thread-local: the whole
+      // row of S sits in this thread's TMEM lane).
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kAttnBC; c0 += 32) {
+        float v[32];
+        tmem_load_32x32b_x32(ts + c0, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col0 + c0 + i < p.Nk) mx = fmaxf(mx, v[i] * p.scale_log2);
+      }
+      const float m_new = fmaxf(m, mx);
+      const float alpha = exp2f(m - m_new);   // 0 on the first block (m = -inf)
+      // Pass 2: P = exp2(u - m_new) as BF16 into the swizzled P tile, and the row sum.
+      const bool free_p = wait_bounded(p_empty, (static_cast<uint32_t>(j) & 1u) ^ 1u, abort_flag,
+                                       SITE_EPI_ACC_FULL);
+      if (!__all_sync(0xffffffffu, free_p)) {
+        ok = false;
+        break;
+      }
+      float psum = 0.0f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kAttnBC; c0 += 32) {
+        float v[32];
+        tmem_load_32x32b_x32(ts + c0, v);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float p0 = (col0 + c0 + i < p.Nk) ? exp2f(v[i] * p.scale_log2 - m_new) : 0.0f;
+          const float p1 = (col0 + c0 + i + 1 < p.Nk) ? exp2f(v[i + 1] * p.scale_log2 - m_new) : 0.0f;
+          psum += p0;
+          psum += p1;
+          w[i / 2] = pack_bf16x2(p0, p1);
+        }
+        // Row `row`, keys c0..c0+31: chunk c0/64, 16-byte pieces (c0%64)/8 .. +3.
+        const uint32_t base = p_smem + static_cast<uint32_t>((c0 / 64) * kChunkBytes + row * 128);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t piece = static_cast<uint32_t>((c0 % 64) / 8 + q);
+          st_shared_v4(base + ((piece ^ static_cast<uint32_t>(row & 7)) << 4), w[4 * q], w[4 * q + 1],
+                       w[4 * q + 2], w[4 * q + 3]);
+        }
+      }
+      tc_fence_before_sync();
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(s_empty(b));
+        mbar_arrive(p_full);
+      }
+      l = fmaf(l, alpha, psum);
+      if (j > 0 && !take_o(j - 1, alpha_prev)) {
+        ok = false;
+        break;
+      }
+      alpha_prev = alpha;
+      m = m_new;
+    }
+    if (ok && n > 0) ok = take_o(n - 1, alpha_prev);
+    const int qrow = qb * kAttnBR + row;
+    if (ok && qrow < p.Nq) {
+      const float inv = 1.0f / l;
+      if (p.out_kind == 0) {
+        float* dst = static_cast<float*>(p.O) + h * p.o_stride + static_cast<long long>(qrow) * p.ldo;
+#pragma unroll
+        for (int d = 0; d < D; d += 4)
+          *reinterpret_cast<float4*>(dst + d) =
+              make_float4(acc[d] * inv, acc[d + 1] * inv, acc[d + 2] * inv, acc[d + 3] * inv);
+      } else {
+        uint16_t* dst = static_cast<uint16_t*>(p.O) + h * p.o_stride + static_cast<long long>(qrow) * p.ldo;
+#pragma unroll
+        for (int d = 0; d < D; d += 8)
+          *reinterpret_cast<uint4*>(dst + d) =
+              make_uint4(pack_bf16x2(acc[d] * inv, acc[d + 1] * inv),
+                         pack_bf16x2(acc[d + 2] * inv, acc[d + 3] * inv),
+                         pack_bf16x2(acc[d + 4] * inv, acc[d + 5] * inv),
+                         pack_bf16x2(acc[d + 6] * inv, acc[d + 7] * inv));
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace gb3

@@ -18,6 +18,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -28,6 +29,7 @@
 #include "gemm_kernels.cuh"
 #include "gemm_kernels_pair.cuh"
 #include "gemm_skinny.cuh"
+#include "attention.cuh"
 #include "gemm_smallm.cuh"
 #include "norm_api.h"
 
@@ -1125,6 +1127,48 @@ int run_smallm(const gemm_plan& pl, int dev, const Problem& q, cudaStream_t stre
   }
 }
 
+// ----------------------------------------------------------------------------
+// Attention
+// ----------------------------------------------------------------------------
+int validate_attention(int64_t heads, int64_t Nq, int64_t Nk, int64_t D, float scale,
+                       const void* Q, int64_t ldq, int64_t sq, const void* K, int64_t ldk,
+                       int64_t sk, const void* V, int64_t ldv, int64_t sv, const void* O,
+                       int64_t ldo, int64_t so, int out_dtype) {
+  if (heads < 0 || Nq < 0 || Nk < 0 || heads > kMaxDim || Nq > kMaxDim || Nk > kMaxDim)
+    return GEMM_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return GEMM_ERR_INVALID_ARG;
+  if (out_dtype != GEMM_OUT_F32 && out_dtype != GEMM_OUT_BF16) return GEMM_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return GEMM_ERR_INVALID_ARG;
+  if (heads == 0 || Nq == 0) return GEMM_OK;
+  if (Nk == 0) return GEMM_ERR_INVALID_ARG;   // a softmax over no keys is undefined
+  if (heads * ceil_div(Nq, kAttnBR) > kMaxDim) return GEMM_ERR_INVALID_ARG;
+  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr) return GEMM_ERR_INVALID_ARG;
+  if (ldq < D || ldk < D || ldv < D || ldo < D) return GEMM_ERR_INVALID_ARG;
+  if (heads > 1 && (sq < Nq * ldq || sk < Nk * ldk || sv < Nk * ldv || so < Nq * ldo))
+    return GEMM_ERR_INVALID_ARG;
+  const int64_t oe = out_elem_bytes(out_dtype);
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return GEMM_ERR_ALIGNMENT;
+  if ((ldq * 2) % 16 != 0 || (ldk * 2) % 16 != 0 || (ldv * 2) % 16 != 0 || (ldo * oe) % 16 != 0)
+    return GEMM_ERR_ALIGNMENT;
+  if (heads > 1 && ((sq * 2) % 16 != 0 || (sk * 2) % 16 != 0 || (sv * 2) % 16 != 0 ||
+                    (so * oe) % 16 != 0))
+    return GEMM_ERR_ALIGNMENT;
+  return GEMM_OK;
+}
+
+template <int D>
+int launch_attention(int dev, int grid, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                     const CUtensorMap& tmV, const AttnParams& p, cudaStream_t stream) {
+  auto kern = attention_kernel<D>;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const int st =
+        ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), AttnCfg<D>::kSmemBytes);
+    if (st != GEMM_OK) return st;
+  }
+  return launch(kern, grid, kThreads, AttnCfg<D>::kSmemBytes, stream, tmQ, tmK, tmV, p);
+}
+
 int run_problem(const Problem& q, void* stream_) {
   int st = validate_problem(q);
   if (st != GEMM_OK) return st;
@@ -1351,6 +1395,53 @@ int gemm_rmsnorm_gate_up_silu(int64_t M, int64_t N, int64_t K, const void* X, in
                          static_cast<cudaStream_t>(stream))) != GEMM_OK)
     return st;
   return gemm_gate_up_silu(M, N, K, Xn, ldxn, Wg, Wu, ldw, Y, ldy, stream);
+}
+
+int gemm_attention(int64_t heads, int64_t Nq, int64_t Nk, int64_t D, float scale, const void* Q,
+                   int64_t ldq, int64_t stride_q, const void* K, int64_t ldk, int64_t stride_k,
+                   const void* V, int64_t ldv, int64_t stride_v, void* O, int64_t ldo,
+                   int64_t stride_o, int out_dtype, void* stream_) {
+  int st = validate_attention(heads, Nq, Nk, D, scale, Q, ldq, stride_q, K, ldk, stride_k, V, ldv,
+                              stride_v, O, ldo, stride_o, out_dtype);
+  if (st != GEMM_OK || heads == 0 || Nq == 0) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev;
+  if ((st = current_device(&dev)) != GEMM_OK) return st;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = probe_device(dev)) != GEMM_OK) return st;
+  }
+  CUtensorMap tmQ, tmK, tmV;
+  const uint64_t pq = static_cast<uint64_t>(ldq) * 2, pk = static_cast<uint64_t>(ldk) * 2,
+                 pv = static_cast<uint64_t>(ldv) * 2;
+  if ((st = tensor_map_3d(&tmQ, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, Nq, heads, pq,
+                          heads > 1 ? static_cast<uint64_t>(stride_q) * 2 : pq * Nq, 64,
+                          kAttnBR)) != GEMM_OK)
+    return st;
+  if ((st = tensor_map_3d(&tmK, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, Nk, heads, pk,
+                          heads > 1 ? static_cast<uint64_t>(stride_k) * 2 : pk * Nk, 64,
+                          kAttnBC)) != GEMM_OK)
+    return st;
+  if ((st = tensor_map_3d(&tmV, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, Nk, heads, pv,
+                          heads > 1 ? static_cast<uint64_t>(stride_v) * 2 : pv * Nk, 64,
+                          kAttnBC)) != GEMM_OK)
+    return st;
+  AttnParams p;
+  p.heads = static_cast<int>(heads);
+  p.Nq = static_cast<int>(Nq);
+  p.Nk = static_cast<int>(Nk);
+  p.q_blocks = static_cast<int>(ceil_div(Nq, kAttnBR));
+  p.k_blocks = static_cast<int>(ceil_div(Nk, kAttnBC));
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.O = O;
+  p.ldo = ldo;
+  p.o_stride = heads > 1 ? stride_o : 0;
+  p.out_kind = out_dtype;
+  p.idesc_s = idesc_f32_acc(kAttnBR, kAttnBC, false);
+  p.idesc_o = idesc_f32_acc(kAttnBR, static_cast<int>(D), false) | (1u << 16);  // B MN-major
+  const int grid = static_cast<int>(heads * p.q_blocks);
+  return D == 64 ? launch_attention<64>(dev, grid, tmQ, tmK, tmV, p, stream)
+                 : launch_attention<128>(dev, grid, tmQ, tmK, tmV, p, stream);
 }
 
 int gemm_get_device_status(void* stream, int* site) {

@@ -228,6 +228,42 @@ GEMM_API int gemm_rmsnorm_gate_up_silu(int64_t M, int64_t N, int64_t K,
                               const void *Wg, const void *Wu, int64_t ldw,
                               void *Xn, int64_t ldxn, void *Y, int64_t ldy, void *stream);
 
+/*
+ * Softmax attention, per head h = 0 .. heads-1:
+ *
+ *   O_h = softmax(scale * Q_h . K_h^T) . V_h        (softmax along each row, over Nk keys)
+ *
+ * ("Tiles and shared memory", section "How long a tile lives": the
+ * flash-attention loop -- a query tile, a running maximum and a running sum
+ * kept across the loop over key tiles, s = dot_t(q, k) per tile, acc / l at
+ * the end.  The sketch shows no score scale; `scale` is a parameter, usually
+ * 1/sqrt(D).)
+ *
+ * heads, Nq, Nk  sizes, 0 <= each < 2^31; heads == 0 or Nq == 0 does nothing;
+ *            Nk == 0 is GEMM_ERR_INVALID_ARG (no keys to normalise over).
+ * D          head dimension, 64 or 128 (else GEMM_ERR_INVALID_ARG).
+ * scale      finite; the scores are s * scale.
+ * Q          device, BF16: q(h,i,d) at Q[h*stride_q + i*ldq + d], ldq >= D.
+ * K, V       device, BF16: k(h,j,d) at K[h*stride_k + j*ldk + d], V likewise.
+ * O          device, FP32 or BF16 (out_dtype GEMM_OUT_F32 / GEMM_OUT_BF16):
+ *            o(h,i,d) at O[h*stride_o + i*ldo + d]; written, never read.
+ * Strides are in elements and keep heads apart when heads > 1; pointers are
+ * 16-byte aligned and pitches / strides multiples of 16 bytes
+ * (GEMM_ERR_ALIGNMENT otherwise).
+ *
+ * Arithmetic: scores accumulate in FP32 on the tensor cores (BF16 operands);
+ * the softmax runs in FP32 in base 2 (exp2 of s * scale * log2 e minus the
+ * running maximum); the probabilities enter the second product as BF16
+ * (nearest even); the row sums, the rescaling of the running output and the
+ * final division are FP32; a BF16 output is rounded to nearest even once.
+ * One launch on `stream`; allocates nothing.
+ */
+GEMM_API int gemm_attention(int64_t heads, int64_t Nq, int64_t Nk, int64_t D, float scale,
+                   const void *Q, int64_t ldq, int64_t stride_q,
+                   const void *K, int64_t ldk, int64_t stride_k,
+                   const void *V, int64_t ldv, int64_t stride_v,
+                   void *O, int64_t ldo, int64_t stride_o, int out_dtype, void *stream);
+
 /* Static, NUL-terminated description of a return code. */
 GEMM_API const char *gemm_status_string(int status);
 

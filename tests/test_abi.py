@@ -390,3 +390,33 @@ def test_plan_small_m_limits(lib, monkeypatch):
     monkeypatch.setenv("GB3_GEMM_SMALL_M", "0")
     assert plan(64, 28672, 8192)["kernel_name"] == "tiled"
     assert plan(16, 28672, 8192)["kernel_name"] == "skinny_splitk"
+
+
+# ---------------------------------------------------------------------------
+# Attention
+# ---------------------------------------------------------------------------
+def attn(heads=2, Nq=256, Nk=256, D=128, scale=0.1, Q=A16, ldq=128, sq=256 * 128, K=A16 * 2,
+         ldk=128, sk=256 * 128, V=A16 * 3, ldv=128, sv=256 * 128, O=A16 * 4, ldo=128,
+         so=256 * 128, out=BF16):
+    return _native.gemm_attention(heads, Nq, Nk, D, scale, Q, ldq, sq, K, ldk, sk, V, ldv, sv, O,
+                                  ldo, so, out, 0)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(heads=-1), _native.GEMM_ERR_INVALID_ARG),
+    (dict(D=96), _native.GEMM_ERR_INVALID_ARG),                      # head dimension 64 or 128
+    (dict(out=F16), _native.GEMM_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), _native.GEMM_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), _native.GEMM_ERR_INVALID_ARG),
+    (dict(Nk=0), _native.GEMM_ERR_INVALID_ARG),                      # no keys
+    (dict(K=0), _native.GEMM_ERR_INVALID_ARG),
+    (dict(ldv=64), _native.GEMM_ERR_INVALID_ARG),                    # pitch < D
+    (dict(sq=255 * 128), _native.GEMM_ERR_INVALID_ARG),              # heads overlap
+    (dict(V=A16 * 3 + 8), _native.GEMM_ERR_ALIGNMENT),
+    (dict(heads=1, ldk=132), _native.GEMM_ERR_ALIGNMENT),
+    (dict(heads=1, out=F32, ldo=130), _native.GEMM_ERR_ALIGNMENT),
+    (dict(heads=0, Q=0, K=0, V=0, O=0), _native.GEMM_OK),            # empty: no-op
+    (dict(Nq=0, Q=0, O=0), _native.GEMM_OK),
+])
+def test_attention_validation_without_gpu(lib, kw, expect):
+    assert attn(**kw) == expect

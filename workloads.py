@@ -30,8 +30,9 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "gemm", "gate_up", "gemm_row_stats", "rms_norm" or
-                              # "rmsnorm_gate_up"
+    kind: str                 # "gemm", "gate_up", "gemm_row_stats", "rms_norm",
+                              # "rmsnorm_gate_up" or "attention" (M = Nq, N = Nk,
+                              # K = head dimension D, batch = heads)
     M: int
     N: int
     K: int
@@ -61,6 +62,8 @@ class Workload:
         """Useful floating-point operations: 2MNK per GEMM (two for gate/up)."""
         if self.kind == "rms_norm":
             return 3.0 * self.M * self.K
+        if self.kind == "attention":   # Q.K^T and P.V
+            return 4.0 * self.batch * self.M * self.N * self.K
         per = 2.0 * self.M * self.N * self.K * self.batch
         return 2.0 * per if self.kind in ("gate_up", "rmsnorm_gate_up") else per
 
@@ -74,6 +77,9 @@ class Workload:
             return self.M * self.K * (in_elem + out_elem) + 4 * self.K
         if self.kind == "gate_up":
             return 2 * (self.M * self.K + 2 * self.N * self.K + self.M * self.N)
+        if self.kind == "attention":   # Q and O once, K and V once per head
+            return self.batch * (2 * self.M * self.K + 4 * self.N * self.K +
+                                 out_elem * self.M * self.K)
         if self.kind == "rmsnorm_gate_up":
             # X read, Xn written, both weights read, Y written (Xn is re-read from L2)
             return 2 * (2 * self.M * self.K + 2 * self.N * self.K + self.M * self.N) + 4 * self.K
@@ -129,6 +135,15 @@ WORKLOADS = {
         dist_a=("normal", 1.0), dist_b=("normal", 1.0 / 64.0),
         out_bf16=True, check="sampled",
         notes="decode batch of 16 through a 4096 x 14336 projection (117 MB)"),
+    # Softmax attention (the flash-attention loop).
+    "attention_32x4096x4096x128": Workload(
+        "attention_32x4096x4096x128", "attention", 4096, 4096, 128, seed=12,
+        dist_a=("normal", 1.0), dist_b=("normal", 1.0), out_bf16=True, batch=32,
+        check="sampled", notes="32 heads, 4096 queries and keys, D = 128, scale 1/sqrt(D)"),
+    "attention_32x4096x4096x64": Workload(
+        "attention_32x4096x4096x64", "attention", 4096, 4096, 64, seed=13,
+        dist_a=("normal", 1.0), dist_b=("normal", 1.0), out_bf16=True, batch=32,
+        check="sampled", notes="32 heads, 4096 queries and keys, D = 64, scale 1/sqrt(D)"),
     # Row reductions and the row normalisation (the row after those).
     "gemm_row_stats_4096": Workload(
         "gemm_row_stats_4096", "gemm_row_stats", 4096, 4096, 4096, seed=1,
@@ -211,7 +226,18 @@ def rmsnorm_gate_up_inputs(M: int, N: int, K: int, seed: int, dist_w=("normal", 
     return X, G, Wg, Wu
 
 
+def attention_inputs(heads: int, Nq: int, Nk: int, D: int, seed: int, dist=("normal", 1.0)):
+    """CPU bf16 tensors Q (heads, Nq, D), K and V (heads, Nk, D), drawn in that order."""
+    gen = torch.Generator(device="cpu").manual_seed(int(seed))
+    Q = _draw(gen, (heads, Nq, D), dist).to(torch.bfloat16)
+    K = _draw(gen, (heads, Nk, D), dist).to(torch.bfloat16)
+    V = _draw(gen, (heads, Nk, D), dist).to(torch.bfloat16)
+    return Q, K, V
+
+
 def inputs_for(w: Workload):
+    if w.kind == "attention":
+        return attention_inputs(w.batch, w.M, w.N, w.K, w.seed, w.dist_a)
     if w.kind == "gate_up":
         return gate_up_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.dist_b)
     if w.kind == "rms_norm":
