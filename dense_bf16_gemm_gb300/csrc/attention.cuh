@@ -82,6 +82,14 @@ __device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t 
   return d;
 }
 
+// 2^x by the hardware's approximate exp2 (relative error about 2^-22;
+// results below the normal range flush to zero, exp2(-inf) = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -265,38 +273,85 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ts = tmem_base + lane_base + Cfg::kSCol + static_cast<uint32_t>(b * kAttnBC);
       const int col0 = j * kAttnBC;
       // Pass 1: the row maximum of the scaled scores (thread-local: the whole
-      // row of S sits in this thread's TMEM lane).
-      float mx = -INFINITY;
+      // row of S sits in this thread's TMEM lane).  A full block (warp-uniform)
+      // needs no key mask, and since scaling by c = scale * log2 e is
+      // monotonic its maximum is c times the largest raw score (the smallest
+      // for c < 0); four independent partial maxima keep the chain short.
+      const float c = p.scale_log2;
+      const bool full = col0 + kAttnBC <= p.Nk;
+      float mx;
+      if (full) {
+        const bool up = c >= 0.0f;
+        float r0 = up ? -INFINITY : INFINITY, r1 = r0, r2 = r0, r3 = r0;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kAttnBC; c0 += 32) {
-        float v[32];
-        tmem_load_32x32b_x32(ts + c0, v);
+        for (int c0 = 0; c0 < kAttnBC; c0 += 32) {
+          float v[32];
+          tmem_load_32x32b_x32(ts + c0, v);
+          if (up) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (col0 + c0 + i < p.Nk) mx = fmaxf(mx, v[i] * p.scale_log2);
+            for (int i = 0; i < 32; i += 4) {
+              r0 = fmaxf(r0, v[i]);
+              r1 = fmaxf(r1, v[i + 1]);
+              r2 = fmaxf(r2, v[i + 2]);
+              r3 = fmaxf(r3, v[i + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              r0 = fminf(r0, v[i]);
+              r1 = fminf(r1, v[i + 1]);
+              r2 = fminf(r2, v[i + 2]);
+              r3 = fminf(r3, v[i + 3]);
+            }
+          }
+        }
+        mx = (up ? fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)) : fminf(fminf(r0, r1), fminf(r2, r3))) * c;
+      } else {
+        mx = -INFINITY;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kAttnBC; c0 += 32) {
+          float v[32];
+          tmem_load_32x32b_x32(ts + c0, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (col0 + c0 + i < p.Nk) mx = fmaxf(mx, v[i] * c);
+        }
       }
       const float m_new = fmaxf(m, mx);
-      const float alpha = exp2f(m - m_new);   // 0 on the first block (m = -inf)
-      // Pass 2: P = exp2(u - m_new) as BF16 into the swizzled P tile, and the row sum.
+      const float alpha = fast_exp2(m - m_new);   // 0 on the first block (m = -inf)
+      // Pass 2: P = exp2(s * c - m_new) (one FFMA and one ex2) as BF16 into the
+      // swizzled P tile, and the row sum in four partial sums.
       const bool free_p = wait_bounded(p_empty, (static_cast<uint32_t>(j) & 1u) ^ 1u, abort_flag,
                                        SITE_EPI_ACC_FULL);
       if (!__all_sync(0xffffffffu, free_p)) {
         ok = false;
         break;
       }
-      float psum = 0.0f;
+      float ps0 = 0.0f, ps1 = 0.0f, ps2 = 0.0f, ps3 = 0.0f;
 #pragma unroll 1
       for (int c0 = 0; c0 < kAttnBC; c0 += 32) {
         float v[32];
         tmem_load_32x32b_x32(ts + c0, v);
         uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float p0 = (col0 + c0 + i < p.Nk) ? exp2f(v[i] * p.scale_log2 - m_new) : 0.0f;
-          const float p1 = (col0 + c0 + i + 1 < p.Nk) ? exp2f(v[i + 1] * p.scale_log2 - m_new) : 0.0f;
-          psum += p0;
-          psum += p1;
-          w[i / 2] = pack_bf16x2(p0, p1);
+        for (int i = 0; i < 32; i += 4) {
+          float q0 = fast_exp2(fmaf(v[i], c, -m_new));
+          float q1 = fast_exp2(fmaf(v[i + 1], c, -m_new));
+          float q2 = fast_exp2(fmaf(v[i + 2], c, -m_new));
+          float q3 = fast_exp2(fmaf(v[i + 3], c, -m_new));
+          if (!full) {
+            const int k = col0 + c0 + i;
+            q0 = k < p.Nk ? q0 : 0.0f;
+            q1 = k + 1 < p.Nk ? q1 : 0.0f;
+            q2 = k + 2 < p.Nk ? q2 : 0.0f;
+            q3 = k + 3 < p.Nk ? q3 : 0.0f;
+          }
+          ps0 += q0;
+          ps1 += q1;
+          ps2 += q2;
+          ps3 += q3;
+          w[i / 2] = pack_bf16x2(q0, q1);
+          w[i / 2 + 1] = pack_bf16x2(q2, q3);
         }
         // Row `row`, keys c0..c0+31: chunk c0/64, 16-byte pieces (c0%64)/8 .. +3.
         const uint32_t base = p_smem + static_cast<uint32_t>((c0 / 64) * kChunkBytes + row * 128);
@@ -314,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(s_empty(b));
         mbar_arrive(p_full);
       }
-      l = fmaf(l, alpha, psum);
+      l = fmaf(l, alpha, (ps0 + ps1) + (ps2 + ps3));
       if (j > 0 && !take_o(j - 1, alpha_prev)) {
         ok = false;
         break;
