@@ -8,21 +8,29 @@
 //
 //   S_j = Q . K_j^T                tcgen05.mma M = 128, N = 128 over D, into one of two
 //                                  TMEM score buffers (K_j is K-major: D contiguous)
-//   m_j = max(m_{j-1}, rowmax S_j)  softmax warps, one thread per query row: the row
-//   P_j = exp(S_j - m_j)            lives in that thread's TMEM lane, so the reduction
-//   l_j = l_{j-1} a_j + rowsum P_j  is thread-local; a_j = exp(m_{j-1} - m_j)
-//   O_j = P_j . V_j                tcgen05.mma M = 128, N = D over the 128 keys; P_j is
-//                                  BF16 in swizzled shared memory (K-major), V_j is
-//                                  the MN-major operand (D contiguous, as TMA loads it)
+//   m_j = max(m_{j-1}, rowmax S_j)  softmax warps: a query row is one TMEM lane, so the
+//   P_j = exp(S_j - m_j)            reduction is local to the threads of that lane (two
+//   l_j = l_{j-1} a_j + rowsum P_j  warps, half of the keys each); a_j = exp(m_{j-1} - m_j)
+//   O_j = P_j . V_j                tcgen05.mma M = 128, N = D over the 128 keys, with P_j
+//                                  written as BF16 back into Tensor Memory (the A
+//                                  operand read from TMEM) and V_j the MN-major operand
+//                                  (D contiguous, as TMA loads it)
 //   acc = acc a_j + O_j            FP32 in the softmax threads' registers
 //
 // and finally O = acc / l.  Scores are handled in base-2 units (exp2 of
 // s * scale * log2 e), which is the same function.  Keys past Nk score -inf.
 //
+// Tensor Memory: two 128-column buffers, each holding S_j as FP32 and then,
+// in the first 32 columns of each half's 64, that half's P_j as packed BF16
+// (its scores are in registers by then); two D-column output buffers.  A
+// buffer is reused for S_{j+2} once O_j = P_j . V_j has completed.
+//
 // Warp roles: warp 0 TMA (Q once, K_j and V_j through a ring), warp 1 MMA
-// issue and TMEM owner, warps 2-5 softmax and output.  The MMA warp issues
-// S_{j+1} before O_j, so the tensor core works on the next scores while the
-// softmax threads finish the current block.
+// issue and TMEM owner, warps 2-9 softmax and output (two warps per TMEM lane
+// quarter, each taking half of the keys of a block and half of the output
+// columns, so that two softmax warps share each SM sub-partition).  The MMA
+// warp issues S_{j+1} before O_j, so the tensor core works on the next scores
+// while the softmax threads finish the current block.
 //
 // Every wait is bounded as in the GEMM kernels (status word, abort flag,
 // drained copies and MMAs, TMEM freed).
@@ -34,6 +42,8 @@ namespace gb3 {
 
 constexpr int kAttnBR = 128;   // query rows per CTA (the MMA's M)
 constexpr int kAttnBC = 128;   // keys per block
+constexpr int kAttnSoftWarps = 8;                          // two per TMEM lane quarter
+constexpr int kAttnThreads = 32 * (2 + kAttnSoftWarps);    // TMA, MMA, softmax
 
 struct AttnParams {
   int heads, Nq, Nk;
@@ -51,18 +61,17 @@ struct AttnCfg {
   static_assert(D == 64 || D == 128, "head dimension");
   static constexpr int kChunks = D / 64;                 // 64-element swizzle rows per row
   static constexpr int kTileBytes = 128 * D * 2;         // Q, K_j or V_j (128 rows)
-  static constexpr int kStages = D == 128 ? 2 : 3;       // K/V ring depth
+  static constexpr int kStages = D == 128 ? 2 : 4;       // K/V ring depth
   static constexpr int kStageBytes = 2 * kTileBytes;     // K_j and V_j
-  static constexpr int kPBytes = kAttnBR * kAttnBC * 2;  // 32 KB
   static constexpr int kQOffset = 0;
   static constexpr int kRingOffset = kTileBytes;
-  static constexpr int kPOffset = kRingOffset + kStages * kStageBytes;
-  static constexpr int kBarOffset = kPOffset + kPBytes;
-  // q_full, kv_full[S], kv_empty[S], s_full[2], s_empty[2], p_full, p_empty,
-  // o_full[2], o_empty[2], drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2 + 4 + 1;
+  static constexpr int kRedOffset = kRingOffset + kStages * kStageBytes;  // [2][2][128] floats
+  static constexpr int kBarOffset = kRedOffset + 2 * 2 * kAttnBR * 4;
+  // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2],
+  // drain, xchg[4]
+  static constexpr int kNumBars = 1 + 2 * kStages + 8 + 1 + 4;
   static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
-  static constexpr int kTmemCols = 512;                  // S: 2 x 128, O: 2 x D
+  static constexpr int kTmemCols = 512;                  // S/P: 2 x 128, O: 2 x D
   static constexpr int kSCol = 0;
   static constexpr int kOCol = 256;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -91,12 +100,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kAttnThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using Cfg = AttnCfg<D>;
   constexpr int S = Cfg::kStages;
   constexpr int kChunkBytes = 128 * 128;  // one 64-element-wide swizzled chunk of 128 rows
+  constexpr int kHalfKeys = kAttnBC / 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -109,18 +119,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t q_full = bar0;
   auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
   auto kv_empty = [&](int s) { return bar0 + 8u * (1 + S + s); };
-  auto s_full = [&](int b) { return bar0 + 8u * (1 + 2 * S + b); };
-  auto s_empty = [&](int b) { return bar0 + 8u * (3 + 2 * S + b); };
-  const uint32_t p_full = bar0 + 8u * (5 + 2 * S);
-  const uint32_t p_empty = bar0 + 8u * (6 + 2 * S);
-  auto o_full = [&](int b) { return bar0 + 8u * (7 + 2 * S + b); };
-  auto o_empty = [&](int b) { return bar0 + 8u * (9 + 2 * S + b); };
-  const uint32_t drain_bar = bar0 + 8u * (11 + 2 * S);
+  auto s_full = [&](int b) { return bar0 + 8u * (1 + 2 * S + b); };   // S_j in buffer b
+  auto p_full = [&](int b) { return bar0 + 8u * (3 + 2 * S + b); };   // P_j written over it
+  auto o_full = [&](int b) { return bar0 + 8u * (5 + 2 * S + b); };   // O_j done (buffer b free)
+  auto o_empty = [&](int b) { return bar0 + 8u * (7 + 2 * S + b); };  // O_j taken
+  const uint32_t drain_bar = bar0 + 8u * (9 + 2 * S);
+  auto xchg_bar = [&](int qtr) { return bar0 + 8u * (10 + 2 * S + qtr); };
 
   const uint32_t q_smem = sb + Cfg::kQOffset;
   auto k_smem = [&](int s) { return sb + Cfg::kRingOffset + static_cast<uint32_t>(s * Cfg::kStageBytes); };
   auto v_smem = [&](int s) { return k_smem(s) + Cfg::kTileBytes; };
-  const uint32_t p_smem = sb + Cfg::kPOffset;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -136,13 +144,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
-      mbar_init(s_empty(b), kEpiWarps);
+      mbar_init(p_full(b), kAttnSoftWarps);
       mbar_init(o_full(b), 1);
-      mbar_init(o_empty(b), kEpiWarps);
+      mbar_init(o_empty(b), kAttnSoftWarps);
     }
-    mbar_init(p_full, kEpiWarps);
-    mbar_init(p_empty, 1);
     mbar_init(drain_bar, 1);
+    for (int qtr = 0; qtr < 4; ++qtr) mbar_init(xchg_bar(qtr), 2);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmQ);
@@ -182,13 +189,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // S_j = Q . K_j^T into score buffer j % 2.
+      // S_j = Q . K_j^T into buffer j % 2, once O_{j-2} (which read P_{j-2}
+      // from that buffer) has completed.
       auto issue_s = [&](int j) -> bool {
         const int s = j % S, b = j & 1;
-        if (!wait_bounded(kv_full(s), static_cast<uint32_t>(j / S) & 1u, abort_flag, SITE_MMA_FULL))
+        if (j >= 2 && !wait_bounded(o_full(b), static_cast<uint32_t>((j - 2) >> 1) & 1u, abort_flag,
+                                    SITE_MMA_ACC_EMPTY))
           return false;
-        if (!wait_bounded(s_empty(b), (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag,
-                          SITE_MMA_ACC_EMPTY))
+        if (!wait_bounded(kv_full(s), static_cast<uint32_t>(j / S) & 1u, abort_flag, SITE_MMA_FULL))
           return false;
         tc_fence_after_sync();
         const uint32_t d = tmem_base + Cfg::kSCol + static_cast<uint32_t>(b * kAttnBC);
@@ -206,26 +214,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = wait_bounded(q_full, 0, abort_flag, SITE_MMA_FULL) && n > 0 && issue_s(0);
       for (int j = 0; ok && j < n; ++j) {
         if (j + 1 < n && !issue_s(j + 1)) break;
-        // O_j = P_j . V_j into output buffer j % 2.
+        // O_j = P_j . V_j into output buffer j % 2; P_j is read from TMEM.
         const int s = j % S, b = j & 1;
-        if (!wait_bounded(p_full, static_cast<uint32_t>(j) & 1u, abort_flag, SITE_MMA_FULL)) break;
+        if (!wait_bounded(p_full(b), static_cast<uint32_t>(j >> 1) & 1u, abort_flag, SITE_MMA_FULL))
+          break;
         if (!wait_bounded(o_empty(b), (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag,
                           SITE_MMA_ACC_EMPTY))
           break;
         tc_fence_after_sync();
         const uint32_t d = tmem_base + Cfg::kOCol + static_cast<uint32_t>(b * D);
+        const uint32_t pa = tmem_base + Cfg::kSCol + static_cast<uint32_t>(b * kAttnBC);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint64_t pd = smem_desc_sw128(p_smem + c * kChunkBytes);
+        for (int half = 0; half < 2; ++half) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t key_row = static_cast<uint32_t>(c * 64 + kk * 16);
-            umma_bf16(d, pd + 2u * kk, smem_desc_mn_sw128(v_smem(s) + key_row * 128u, kChunkBytes),
-                      p.idesc_o, (c | kk) != 0 ? 1u : 0u);
+            const uint32_t key_row = static_cast<uint32_t>(half * kHalfKeys + kk * 16);
+            umma_bf16_tmem_a(d, pa + static_cast<uint32_t>(half * kHalfKeys + kk * 8),
+                             smem_desc_mn_sw128(v_smem(s) + key_row * 128u, kChunkBytes), p.idesc_o,
+                             (half | kk) != 0 ? 1u : 0u);
           }
         }
         umma_commit(o_full(b));
-        umma_commit(p_empty);
         umma_commit(kv_empty(s));
       }
       // Leave only when every issued MMA has completed (bounded).
@@ -233,34 +242,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_bounded(drain_bar, 0, nullptr, SITE_DRAIN);
     }
   } else {
+    // Softmax warps 2..9: warp w serves query rows 32*(w%4)..+31 (its TMEM
+    // lane quarter) and one half of the keys of each block and of the output
+    // columns; the two warps of a quarter exchange their partial row maxima
+    // through shared memory each block (a bounded mbarrier, values double
+    // buffered) and their partial row sums once at the end.
+    constexpr int kHalfD = D / 2;
+    const int half = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = 32 * quarter + lane;             // query row of this thread in the block
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
-    float acc[D];
+    float* xval = reinterpret_cast<float*>(smem + Cfg::kRedOffset);
+    const uint32_t xbar = xchg_bar(quarter);
+    // Publishes `mine` for the partner warp in exchange round r and returns
+    // the partner's value (false if a wait gave up).
+    auto exchange = [&](int r, float mine, float& other) -> bool {
+      const int buf = r & 1;
+      xval[(buf * 2 + half) * kAttnBR + row] = mine;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xbar);
+      const bool got = wait_bounded(xbar, static_cast<uint32_t>(r) & 1u, abort_flag,
+                                    SITE_EPI_ACC_FULL);
+      if (!__all_sync(0xffffffffu, got)) return false;
+      other = xval[(buf * 2 + (half ^ 1)) * kAttnBR + row];
+      return true;
+    };
+    float acc[kHalfD];
 #pragma unroll
-    for (int i = 0; i < D; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < kHalfD; ++i) acc[i] = 0.0f;
     float m = -INFINITY, l = 0.0f, alpha_prev = 0.0f;
     bool ok = true;
-    // acc = acc * alpha + O_j (read from TMEM), then hand the buffer back.
+    // acc = acc * alpha + this half of O_j (read from TMEM), then hand it back.
     auto take_o = [&](int j, float alpha) -> bool {
       const int b = j & 1;
       const bool got = wait_bounded(o_full(b), static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
                                     SITE_EPI_ACC_FULL);
       if (!__all_sync(0xffffffffu, got)) return false;
       tc_fence_after_sync();
-      const uint32_t to = tmem_base + lane_base + Cfg::kOCol + static_cast<uint32_t>(b * D);
+      const uint32_t to = tmem_base + lane_base + Cfg::kOCol + static_cast<uint32_t>(b * D + half * kHalfD);
+      if constexpr (kHalfD == 64) {
+        float o[64];
+        tmem_load_32x32b_x64(to, o);
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int i = 0; i < 64; ++i) acc[i] = fmaf(acc[i], alpha, o[i]);
+      } else {
         float o[32];
-        tmem_load_32x32b_x32(to + c0, o);
+        tmem_load_32x32b_x32(to, o);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[c0 + i] = fmaf(acc[c0 + i], alpha, o[i]);
+        for (int i = 0; i < 32; ++i) acc[i] = fmaf(acc[i], alpha, o[i]);
       }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_empty(b));
       return true;
     };
+    const float c = p.scale_log2;
     for (int j = 0; j < n; ++j) {
       const int b = j & 1;
       const bool got = wait_bounded(s_full(b), static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
@@ -270,105 +306,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const uint32_t ts = tmem_base + lane_base + Cfg::kSCol + static_cast<uint32_t>(b * kAttnBC);
-      const int col0 = j * kAttnBC;
-      // Pass 1: the row maximum of the scaled scores (thread-local: the whole
-      // row of S sits in this thread's TMEM lane).  A full block (warp-uniform)
-      // needs no key mask, and since scaling by c = scale * log2 e is
-      // monotonic its maximum is c times the largest raw score (the smallest
-      // for c < 0); four independent partial maxima keep the chain short.
-      const float c = p.scale_log2;
-      const bool full = col0 + kAttnBC <= p.Nk;
-      float mx;
+      const uint32_t ts = tmem_base + lane_base + Cfg::kSCol +
+                          static_cast<uint32_t>(b * kAttnBC + half * kHalfKeys);
+      const int col0 = j * kAttnBC + half * kHalfKeys;
+      const bool full = j * kAttnBC + kAttnBC <= p.Nk;   // the same for both halves
+      // This half of the row of S, once, into registers (64 scores).
+      float v[kHalfKeys];
+      tmem_load_32x32b_x64(ts, v);
+      // Pass 1: this half's maximum of the scaled scores (a full block needs no
+      // key mask, and scaling by c is monotonic: c times the largest raw score,
+      // the smallest for c < 0), four partial maxima.
+      float mine;
       if (full) {
         const bool up = c >= 0.0f;
         float r0 = up ? -INFINITY : INFINITY, r1 = r0, r2 = r0, r3 = r0;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kAttnBC; c0 += 32) {
-          float v[32];
-          tmem_load_32x32b_x32(ts + c0, v);
-          if (up) {
+        if (up) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              r0 = fmaxf(r0, v[i]);
-              r1 = fmaxf(r1, v[i + 1]);
-              r2 = fmaxf(r2, v[i + 2]);
-              r3 = fmaxf(r3, v[i + 3]);
-            }
-          } else {
+          for (int i = 0; i < kHalfKeys; i += 4) {
+            r0 = fmaxf(r0, v[i]);
+            r1 = fmaxf(r1, v[i + 1]);
+            r2 = fmaxf(r2, v[i + 2]);
+            r3 = fmaxf(r3, v[i + 3]);
+          }
+        } else {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              r0 = fminf(r0, v[i]);
-              r1 = fminf(r1, v[i + 1]);
-              r2 = fminf(r2, v[i + 2]);
-              r3 = fminf(r3, v[i + 3]);
-            }
+          for (int i = 0; i < kHalfKeys; i += 4) {
+            r0 = fminf(r0, v[i]);
+            r1 = fminf(r1, v[i + 1]);
+            r2 = fminf(r2, v[i + 2]);
+            r3 = fminf(r3, v[i + 3]);
           }
         }
-        mx = (up ? fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)) : fminf(fminf(r0, r1), fminf(r2, r3))) * c;
+        mine = (up ? fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)) : fminf(fminf(r0, r1), fminf(r2, r3))) * c;
       } else {
-        mx = -INFINITY;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kAttnBC; c0 += 32) {
-          float v[32];
-          tmem_load_32x32b_x32(ts + c0, v);
+        mine = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (col0 + c0 + i < p.Nk) mx = fmaxf(mx, v[i] * c);
-        }
+        for (int i = 0; i < kHalfKeys; ++i)
+          if (col0 + i < p.Nk) mine = fmaxf(mine, v[i] * c);
       }
-      const float m_new = fmaxf(m, mx);
-      const float alpha = fast_exp2(m - m_new);   // 0 on the first block (m = -inf)
-      // Pass 2: P = exp2(s * c - m_new) (one FFMA and one ex2) as BF16 into the
-      // swizzled P tile, and the row sum in four partial sums.
-      const bool free_p = wait_bounded(p_empty, (static_cast<uint32_t>(j) & 1u) ^ 1u, abort_flag,
-                                       SITE_EPI_ACC_FULL);
-      if (!__all_sync(0xffffffffu, free_p)) {
+      float other;
+      if (!exchange(j, mine, other)) {
         ok = false;
         break;
       }
+      const float m_new = fmaxf(m, fmaxf(mine, other));
+      const float alpha = fast_exp2(m - m_new);   // 0 on the first block (m = -inf)
+      // Pass 2: P = exp2(s * c - m_new), packed as BF16 pairs (even key in
+      // the low half) into the first 32 columns of this half's scores, and
+      // this half's row sum (four partial sums).
       float ps0 = 0.0f, ps1 = 0.0f, ps2 = 0.0f, ps3 = 0.0f;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kAttnBC; c0 += 32) {
-        float v[32];
-        tmem_load_32x32b_x32(ts + c0, v);
-        uint32_t w[16];
+      uint32_t w[kHalfKeys / 2];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          float q0 = fast_exp2(fmaf(v[i], c, -m_new));
-          float q1 = fast_exp2(fmaf(v[i + 1], c, -m_new));
-          float q2 = fast_exp2(fmaf(v[i + 2], c, -m_new));
-          float q3 = fast_exp2(fmaf(v[i + 3], c, -m_new));
-          if (!full) {
-            const int k = col0 + c0 + i;
-            q0 = k < p.Nk ? q0 : 0.0f;
-            q1 = k + 1 < p.Nk ? q1 : 0.0f;
-            q2 = k + 2 < p.Nk ? q2 : 0.0f;
-            q3 = k + 3 < p.Nk ? q3 : 0.0f;
-          }
-          ps0 += q0;
-          ps1 += q1;
-          ps2 += q2;
-          ps3 += q3;
-          w[i / 2] = pack_bf16x2(q0, q1);
-          w[i / 2 + 1] = pack_bf16x2(q2, q3);
+      for (int i = 0; i < kHalfKeys; i += 4) {
+        float q0 = fast_exp2(fmaf(v[i], c, -m_new));
+        float q1 = fast_exp2(fmaf(v[i + 1], c, -m_new));
+        float q2 = fast_exp2(fmaf(v[i + 2], c, -m_new));
+        float q3 = fast_exp2(fmaf(v[i + 3], c, -m_new));
+        if (!full) {
+          const int k = col0 + i;
+          q0 = k < p.Nk ? q0 : 0.0f;
+          q1 = k + 1 < p.Nk ? q1 : 0.0f;
+          q2 = k + 2 < p.Nk ? q2 : 0.0f;
+          q3 = k + 3 < p.Nk ? q3 : 0.0f;
         }
-        // Row `row`, keys c0..c0+31: chunk c0/64, 16-byte pieces (c0%64)/8 .. +3.
-        const uint32_t base = p_smem + static_cast<uint32_t>((c0 / 64) * kChunkBytes + row * 128);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t piece = static_cast<uint32_t>((c0 % 64) / 8 + q);
-          st_shared_v4(base + ((piece ^ static_cast<uint32_t>(row & 7)) << 4), w[4 * q], w[4 * q + 1],
-                       w[4 * q + 2], w[4 * q + 3]);
-        }
+        ps0 += q0;
+        ps1 += q1;
+        ps2 += q2;
+        ps3 += q3;
+        w[i / 2] = pack_bf16x2(q0, q1);
+        w[i / 2 + 1] = pack_bf16x2(q2, q3);
       }
+      tmem_store_32x32b_x32(ts, w);
       tc_fence_before_sync();
-      fence_proxy_async_shared();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(s_empty(b));
-        mbar_arrive(p_full);
-      }
+      if (lane == 0) mbar_arrive(p_full(b));
       l = fmaf(l, alpha, (ps0 + ps1) + (ps2 + ps3));
       if (j > 0 && !take_o(j - 1, alpha_prev)) {
         ok = false;
@@ -378,19 +389,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       m = m_new;
     }
     if (ok && n > 0) ok = take_o(n - 1, alpha_prev);
+    // The row sum is the two halves' sums (both at the final maximum).
+    float l_other = 0.0f;
+    if (ok) ok = exchange(n, l, l_other);
     const int qrow = qb * kAttnBR + row;
     if (ok && qrow < p.Nq) {
-      const float inv = 1.0f / l;
+      const float inv = 1.0f / (l + l_other);
       if (p.out_kind == 0) {
-        float* dst = static_cast<float*>(p.O) + h * p.o_stride + static_cast<long long>(qrow) * p.ldo;
+        float* dst = static_cast<float*>(p.O) + h * p.o_stride + static_cast<long long>(qrow) * p.ldo +
+                     half * kHalfD;
 #pragma unroll
-        for (int d = 0; d < D; d += 4)
+        for (int d = 0; d < kHalfD; d += 4)
           *reinterpret_cast<float4*>(dst + d) =
               make_float4(acc[d] * inv, acc[d + 1] * inv, acc[d + 2] * inv, acc[d + 3] * inv);
       } else {
-        uint16_t* dst = static_cast<uint16_t*>(p.O) + h * p.o_stride + static_cast<long long>(qrow) * p.ldo;
+        uint16_t* dst = static_cast<uint16_t*>(p.O) + h * p.o_stride +
+                        static_cast<long long>(qrow) * p.ldo + half * kHalfD;
 #pragma unroll
-        for (int d = 0; d < D; d += 8)
+        for (int d = 0; d < kHalfD; d += 8)
           *reinterpret_cast<uint4*>(dst + d) =
               make_uint4(pack_bf16x2(acc[d] * inv, acc[d + 1] * inv),
                          pack_bf16x2(acc[d + 2] * inv, acc[d + 3] * inv),

@@ -1166,7 +1166,7 @@ int launch_attention(int dev, int grid, const CUtensorMap& tmQ, const CUtensorMa
         ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), AttnCfg<D>::kSmemBytes);
     if (st != GEMM_OK) return st;
   }
-  return launch(kern, grid, kThreads, AttnCfg<D>::kSmemBytes, stream, tmQ, tmK, tmV, p);
+  return launch(kern, grid, kAttnThreads, AttnCfg<D>::kSmemBytes, stream, tmQ, tmK, tmV, p);
 }
 
 int run_problem(const Problem& q, void* stream_) {
