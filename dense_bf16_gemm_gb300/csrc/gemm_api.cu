@@ -163,6 +163,20 @@ int pair_smem_for(int bn) {
   }
 }
 
+// The CTA-pair epilogue reads C (beta != 0) through the staging ring unless
+// GB3_GEMM_C_RING = 0 (for comparisons and tests).
+bool pair_reads_c_ring(float beta) {
+  return beta != 0.0f && env_int("GB3_GEMM_C_RING", 1) != 0;
+}
+
+int pair_ring_smem_for(int bn) {
+  switch (bn) {
+    case 256: return PairCfg<256, kPairStages - 1, EPI_BF16, true>::kSmemBytes;
+    case 224: return PairCfg<224, kPairStages - 1, EPI_BF16, true>::kSmemBytes;
+    default: return 0;
+  }
+}
+
 int pair_stage_bytes(int bn) { return 128 * kBK * 2 + (bn / 2) * kBK * 2; }
 
 // Split of K for the skinny path: minimise the k-blocks of the busiest CTA,
@@ -934,12 +948,15 @@ void pair_units(int dev, gemm_plan* pl, const Problem& q, int out_cols, TilePara
   p->num_units = static_cast<int>(c.full + (c.tiles - c.full) * c.split);
 }
 
-template <int BN, int EPI, bool STATS = false>
+// RING: C is read through the deeper staging ring (beta != 0), which takes
+// the shared memory of one pipeline stage.
+template <int BN, int EPI, bool STATS = false, bool RING = false>
 int launch_pair_gemm(const gemm_plan& pl, int dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
                      const CUtensorMap& tmB2, const CUtensorMap& tmOut, const TileParams& p,
                      cudaStream_t stream, const RowStatsParams& rs = RowStatsParams{}) {
-  using Cfg = PairCfg<BN, kPairStages, EPI>;
-  auto kern = gemm_pair_kernel<BN, kPairStages, EPI, STATS>;
+  constexpr int kStagesHere = RING ? kPairStages - 1 : kPairStages;
+  using Cfg = PairCfg<BN, kStagesHere, EPI, RING>;
+  auto kern = gemm_pair_kernel<BN, kStagesHere, EPI, STATS, RING>;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     const int st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), Cfg::kSmemBytes);
@@ -979,29 +996,40 @@ int run_pair(gemm_plan& pl, int dev, int slots, const Problem& q, cudaStream_t s
   RowStatsParams rs;
   if ((st = attach_row_stats(dev, q, p.n_blocks, &rs, stream)) != GEMM_OK) return st;
   pair_units(dev, &pl, q, bn, &p, stream, false, slots);
-  const bool f32 = q.out_dtype == GEMM_OUT_F32;
-  if (q.stats()) {
-    switch (bn) {
-      case 256:
-        return f32 ? launch_pair_gemm<256, EPI_F32, true>(pl, dev, tmA, tmB, tmB, tmOut, p, stream, rs)
-                   : launch_pair_gemm<256, EPI_BF16, true>(pl, dev, tmA, tmB, tmB, tmOut, p, stream, rs);
-      case 224:
-        return f32 ? launch_pair_gemm<224, EPI_F32, true>(pl, dev, tmA, tmB, tmB, tmOut, p, stream, rs)
-                   : launch_pair_gemm<224, EPI_BF16, true>(pl, dev, tmA, tmB, tmB, tmOut, p, stream, rs);
-      default:
-        return GEMM_ERR_UNSUPPORTED;
-    }
+  if (bn != 256 && bn != 224) return GEMM_ERR_UNSUPPORTED;
+  // The ring kernels compute whole tiles only and always read C.
+  const bool ring = pair_reads_c_ring(q.beta) && p.tail_split == 1;
+  if (ring) {
+    pl.stages = kPairStages - 1;
+    pl.smem_bytes = pair_ring_smem_for(bn);
   }
-  switch (bn) {
-    case 256:
-      return f32 ? launch_pair_gemm<256, EPI_F32>(pl, dev, tmA, tmB, tmB, tmOut, p, stream)
-                 : launch_pair_gemm<256, EPI_BF16>(pl, dev, tmA, tmB, tmB, tmOut, p, stream);
-    case 224:
-      return f32 ? launch_pair_gemm<224, EPI_F32>(pl, dev, tmA, tmB, tmB, tmOut, p, stream)
-                 : launch_pair_gemm<224, EPI_BF16>(pl, dev, tmA, tmB, tmB, tmOut, p, stream);
+  const int sel = (q.out_dtype == GEMM_OUT_F32 ? 1 : 0) | (q.stats() ? 2 : 0) | (ring ? 4 : 0) |
+                  (bn == 224 ? 8 : 0);
+#define GB3_PAIR_CASE(S, BN_, EPI_, STATS_, RING_)                                              \
+  case S:                                                                                       \
+    return launch_pair_gemm<BN_, EPI_, STATS_, RING_>(pl, dev, tmA, tmB, tmB, tmOut, p, stream, \
+                                                      rs);
+  switch (sel) {
+    GB3_PAIR_CASE(0, 256, EPI_BF16, false, false)
+    GB3_PAIR_CASE(1, 256, EPI_F32, false, false)
+    GB3_PAIR_CASE(2, 256, EPI_BF16, true, false)
+    GB3_PAIR_CASE(3, 256, EPI_F32, true, false)
+    GB3_PAIR_CASE(4, 256, EPI_BF16, false, true)
+    GB3_PAIR_CASE(5, 256, EPI_F32, false, true)
+    GB3_PAIR_CASE(6, 256, EPI_BF16, true, true)
+    GB3_PAIR_CASE(7, 256, EPI_F32, true, true)
+    GB3_PAIR_CASE(8, 224, EPI_BF16, false, false)
+    GB3_PAIR_CASE(9, 224, EPI_F32, false, false)
+    GB3_PAIR_CASE(10, 224, EPI_BF16, true, false)
+    GB3_PAIR_CASE(11, 224, EPI_F32, true, false)
+    GB3_PAIR_CASE(12, 224, EPI_BF16, false, true)
+    GB3_PAIR_CASE(13, 224, EPI_F32, false, true)
+    GB3_PAIR_CASE(14, 224, EPI_BF16, true, true)
+    GB3_PAIR_CASE(15, 224, EPI_F32, true, true)
     default:
       return GEMM_ERR_UNSUPPORTED;
   }
+#undef GB3_PAIR_CASE
 }
 
 int run_single(const gemm_plan& pl, int dev, const Problem& q, cudaStream_t stream) {

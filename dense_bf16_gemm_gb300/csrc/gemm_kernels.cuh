@@ -45,7 +45,8 @@ enum WaitSite : int {
   SITE_EPI_ACC_FULL = 4,
   SITE_DRAIN = 5,
   SITE_SKINNY = 6,
-  SITE_SELFTEST = 7
+  SITE_SELFTEST = 7,
+  SITE_EPI_C_FULL = 8
 };
 
 // [0] status code, [1] wait site, [2] block index of the first failure.
@@ -441,7 +442,10 @@ __device__ __forceinline__ uint32_t staging_offset(int row, uint32_t chunk) {
 // from n0.  Each box is loaded from TMEM 32 columns at a time, transformed in
 // FP32, written to a staging slot in the swizzled layout and stored with TMA.
 // `sc` counts the boxes this warp staged (two slots alternate); every staged
-// box is committed as its own bulk group.
+// box is committed as its own bulk group.  The value before output rounding
+// is fma(beta, c, RN(alpha * acc)) in FP32, written out with intrinsics so
+// that no contraction choice of the compiler differs between the epilogues
+// of the different kernels.
 // STATS: also reduce each row (sum, max, min) into p's row-statistics outputs.
 template <int BN, int EPI, bool STATS = false>
 __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtensorMap* tmOut,
@@ -497,11 +501,11 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
         }
         const float alpha = p.alpha;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= alpha;
+        for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(alpha, v[i]);
         if (read_c) {
           const float beta = p.beta;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] += beta * c_cur[i];
+          for (int i = 0; i < 32; ++i) v[i] = __fmaf_rn(beta, c_cur[i], v[i]);
         }
         if constexpr (stats) row_acc_slice(racc, v, n0 + c0 + 32 * h, p.N);
       }
@@ -533,6 +537,108 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
   if constexpr (stats) {
     if (m0 < p.M) publish_row_stats(p, rs, b, n0 / OUT, m0, lane, racc);
   }
+}
+
+// C through a staging ring (beta != 0, whole tiles).  Each epilogue warp owns
+// kRingSlots staging slots.  Its lane 0 loads the boxes of C with TMA into
+// the slots kRingAhead boxes ahead of the box being computed; a box is then
+// computed in place (C read from the slot, the result written over it) and
+// stored from the same slot.  The look-ahead runs across tile boundaries, so
+// the first boxes of a tile load while the previous tile's last ones are
+// computed: one L2 round trip per tile band instead of one per 32-column
+// slice, with no registers held for C.
+constexpr int kRingSlots = 4;
+constexpr int kRingAhead = 2;  // boxes loaded beyond the one being computed
+static_assert(kRingAhead < kRingSlots, "a slot must be free before its next load");
+
+// The ring boxes of one warp are numbered r = 0, 1, ... in the order they are
+// computed: box r lives in slot r % kRingSlots, whose barrier completes phase
+// (r / kRingSlots) & 1 when the box has landed.  topup(r) issues the loads of
+// every box up to r + kRingAhead that exists.  Returns false when a wait gave
+// up (the abort flag is then set).
+template <int BN, int EPI, bool STATS, typename TopUp>
+__device__ __forceinline__ bool epilogue_tile_ring(const TileParams& p, const CUtensorMap* tmOut,
+                                                   uint32_t tacc, int b, int m0, int n0,
+                                                   uint32_t ring, uint32_t cbar0, int lane,
+                                                   long long& r, int& sc,
+                                                   const RowStatsParams& rs,
+                                                   volatile int* abort_flag, TopUp&& topup) {
+  static_assert(EPI != EPI_GATE_UP, "the gate/up epilogue reads no C");
+  using Box = EpiBox<EPI, BN>;
+  constexpr int kSub = Box::kCols / 32;
+  RowAcc racc;
+  row_acc_init(racc);
+  const SplitCtx whole{1, 0, nullptr, 0};
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN; c0 += Box::kCols) {
+    if (m0 >= p.M || n0 + c0 >= p.N) continue;
+    topup(r);
+    const int slot = static_cast<int>(r % kRingSlots);
+    const uint32_t stg = ring + slot * kStageBox;
+    const bool got = wait_bounded(cbar0 + 8u * slot, static_cast<uint32_t>((r / kRingSlots) & 1),
+                                  abort_flag, SITE_EPI_C_FULL);
+    if (!__all_sync(0xffffffffu, got)) return false;
+#pragma unroll 1
+    for (int h = 0; h < kSub; ++h) {
+      float v[32], c[32];
+      acc_slice(v, tacc, c0 + 32 * h, lane, whole);
+      if constexpr (EPI == EPI_F32) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 x = ld_shared_v4(stg + staging_offset<true>(lane, static_cast<uint32_t>(q)));
+          c[4 * q + 0] = __uint_as_float(x.x);
+          c[4 * q + 1] = __uint_as_float(x.y);
+          c[4 * q + 2] = __uint_as_float(x.z);
+          c[4 * q + 3] = __uint_as_float(x.w);
+        }
+      } else {
+        const bool f16 = p.out_f16 != 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 x = ld_shared_v4(
+              stg + staging_offset<Box::kSwizzle128>(lane, static_cast<uint32_t>(4 * h + q)));
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            c[8 * q + 2 * j + 0] = half16_to_float(w[j] & 0xFFFFu, f16);
+            c[8 * q + 2 * j + 1] = half16_to_float(w[j] >> 16, f16);
+          }
+        }
+      }
+      const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __fmaf_rn(beta, c[i], __fmul_rn(alpha, v[i]));
+      if constexpr (STATS) row_acc_slice(racc, v, n0 + c0 + 32 * h, p.N);
+      if constexpr (EPI == EPI_F32) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          st_shared_v4(stg + staging_offset<true>(lane, static_cast<uint32_t>(q)),
+                       __float_as_uint(v[4 * q + 0]), __float_as_uint(v[4 * q + 1]),
+                       __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
+      } else {
+        const bool f16 = p.out_f16 != 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          st_shared_v4(stg + staging_offset<Box::kSwizzle128>(lane, static_cast<uint32_t>(4 * h + q)),
+                       pack_half16x2(v[8 * q + 0], v[8 * q + 1], f16),
+                       pack_half16x2(v[8 * q + 2], v[8 * q + 3], f16),
+                       pack_half16x2(v[8 * q + 4], v[8 * q + 5], f16),
+                       pack_half16x2(v[8 * q + 6], v[8 * q + 7], f16));
+      }
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(tmOut, stg, n0 + c0, m0, b);
+      bulk_commit_group();
+    }
+    ++r;
+    ++sc;
+  }
+  if constexpr (STATS) {
+    if (m0 < p.M) publish_row_stats(p, rs, b, n0 / BN, m0, lane, racc);
+  }
+  return true;
 }
 
 // When C is read (beta != 0): ask L2 for this warp's band of C of a coming

@@ -28,7 +28,9 @@ namespace gb3 {
 
 constexpr int kPairBM = 256;  // tile rows of a CTA pair
 
-template <int BN, int STAGES, int EPI>
+// RING: the epilogue reads C through a ring of kRingSlots staging slots per
+// warp (epilogue_tile_ring), each slot with its own barrier.
+template <int BN, int STAGES, int EPI, bool RING = false>
 struct PairCfg {
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile width");
   static constexpr int kABytes = 128 * kBK * 2;       // this CTA's 128 rows of A
@@ -36,24 +38,28 @@ struct PairCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static_assert(kStageBytes % 1024 == 0, "stages must keep the 1024-byte swizzle phase");
   static constexpr int kRingBytes = STAGES * kStageBytes;
-  static constexpr int kStagingBytes = kEpiWarps * kStagingPerWarp * kStageBox;
+  static constexpr int kSlots = RING ? kRingSlots : kStagingPerWarp;  // staging slots per warp
+  static constexpr int kStagingBytes = kEpiWarps * kSlots * kStageBox;
   static constexpr int kBarOffset = kRingBytes + kStagingBytes;
-  static constexpr int kNumBars = 2 * STAGES + 5;
+  // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain, then with
+  // RING one barrier per staging slot of each epilogue warp
+  static constexpr int kNumBars = 2 * STAGES + 5 + (RING ? kEpiWarps * kRingSlots : 0);
   static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
   static constexpr int kOutCols = (EPI == EPI_GATE_UP) ? BN / 2 : BN;
+  static_assert(!RING || EPI != EPI_GATE_UP, "the gate/up epilogue reads no C");
   static constexpr int kAccStride = 256;
   static constexpr int kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <int BN, int STAGES, int EPI, bool STATS = false>
+template <int BN, int STAGES, int EPI, bool STATS = false, bool RING = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmB2,
                      const __grid_constant__ CUtensorMap tmOut, const TileParams p,
                      const RowStatsParams rs) {
-  using Cfg = PairCfg<BN, STAGES, EPI>;
+  using Cfg = PairCfg<BN, STAGES, EPI, RING>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -85,6 +91,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(acce_bar(b), 2 * kEpiWarps);
     }
     mbar_init(drain_bar, 1);
+    if constexpr (RING)
+      for (int i = 0; i < kEpiWarps * kRingSlots; ++i) mbar_init(drain_bar + 8u * (1 + i), 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA);
@@ -191,11 +199,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int ew = warp - 2;
     const int band = (warp & 3) * 32;
-    const uint32_t staging = sbase + Cfg::kRingBytes + ew * kStagingPerWarp * kStageBox;
+    const uint32_t staging = sbase + Cfg::kRingBytes + ew * Cfg::kSlots * kStageBox;
     const uint32_t acce0_even = mapa_shared(acce_bar(0), 0);
     const int band_id = static_cast<int>(rank) * 4 + (warp & 3);  // 32-row band of the pair tile
     int local = 0;
     int sc = 0;
+    // C ring: the load cursor walks this warp's boxes in the order the
+    // epilogue computes them.  The host launches RING kernels only with
+    // beta != 0 and whole tiles (no split pieces: which piece writes C is
+    // known only at run time, and their register path is left out of these
+    // kernels).
+    const uint32_t cbar0 = drain_bar + 8u * (1 + ew * kRingSlots);
+    long long r_done = 0, r_issued = 0;
+    int cu = p.num_units, cc0 = 0, cb = 0, cm0 = 0, cn0 = 0;
+    auto cursor_at = [&](int u) {
+      cu = u;
+      cc0 = 0;
+      if (u < p.num_units) {
+        int tile_, kb0_, kb1_, piece_, mb_, nb_;
+        unit_of(u, p, tile_, kb0_, kb1_, piece_);
+        tile_coords(tile_, p, cb, mb_, nb_);
+        cm0 = mb_ * kPairBM + static_cast<int>(rank) * 128 + band;
+        cn0 = nb_ * Cfg::kOutCols;
+      }
+    };
+    auto cursor_settle = [&]() {  // onto the next box inside C, or past the last unit
+      while (cu < p.num_units) {
+        if (cc0 < Cfg::kOutCols && cm0 < p.M && cn0 + cc0 < p.N) return;
+        cursor_at(cu + nclusters);
+      }
+    };
+    auto topup = [&](long long r_now) {
+      using Box = EpiBox<EPI == EPI_GATE_UP ? EPI_BF16 : EPI, Cfg::kOutCols>;
+      while (cu < p.num_units && r_issued <= r_now + kRingAhead) {
+        const int slot = static_cast<int>(r_issued % kRingSlots);
+        if (lane == 0) {
+          // The slot's previous box was stored kRingSlots boxes ago.
+          bulk_wait_group_read<kRingSlots - 1 - kRingAhead>();
+          mbar_arrive_expect_tx(cbar0 + 8u * slot, 32 * Box::kRowBytes);
+          tma_load_3d(staging + slot * kStageBox, &tmOut, cbar0 + 8u * slot, cn0 + cc0, cm0, cb);
+        }
+        ++r_issued;
+        cc0 += Box::kCols;
+        cursor_settle();
+      }
+    };
     auto prefetch_unit = [&](int u) {
       if (u < p.num_units) {
         int tile_, kb0_, kb1_, piece_, b_, mb_, nb_;
@@ -215,6 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // C of this CTA's next unit travels to L2 during this unit's epilogue
       // and the next unit's main loop.
       if (lane == 0) prefetch_unit(u + nclusters);
+      if (RING && r_issued == 0 && cu == p.num_units) {
+        // First tile: start the C loads before waiting for its accumulator.
+        cursor_at(u);
+        cursor_settle();
+        topup(0);
+      }
       const int buf = local & 1;
       const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
       const bool got = wait_bounded(accf_bar(buf), aph, abort_flag, SITE_EPI_ACC_FULL);
@@ -224,31 +278,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                             static_cast<uint32_t>(buf * Cfg::kAccStride);
       const int m0 = mb * kPairBM + static_cast<int>(rank) * 128 + band;
       const int n0 = nb * Cfg::kOutCols;
-      SplitCtx split{1, 0, nullptr, 0};
-      bool store = true;
-      if (piece >= 0) {
-        // One K piece of a tail tile: publish the partial; the band's last
-        // piece adds them all up and writes C.  Workspace: [tail tile][piece]
-        // [band 0..7][32 x BN floats].
-        const int tail = tile - p.num_full;
-        const long long band_f4 = 32LL * BN / 4;
-        split.pieces = p.tail_split;
-        split.piece = piece;
-        split.piece_stride = 8 * band_f4;
-        split.ws0 = reinterpret_cast<const float4*>(p.ws) +
-                    static_cast<long long>(tail) * p.tail_split * split.piece_stride +
-                    band_id * band_f4;
-        store = publish_partial(tacc, BN, lane, split, p.counters + tail * 8 + band_id,
-                                p.tail_split);
+      if constexpr (RING) {
+        if (!epilogue_tile_ring<BN, EPI, STATS>(p, &tmOut, tacc, bt, m0, n0, staging, cbar0,
+                                                lane, r_done, sc, rs, abort_flag, topup))
+          break;
+      } else {
+        SplitCtx split{1, 0, nullptr, 0};
+        bool store = true;
+        if (piece >= 0) {
+          // One K piece of a tail tile: publish the partial; the band's last
+          // piece adds them all up and writes C.  Workspace: [tail tile][piece]
+          // [band 0..7][32 x BN floats].
+          const int tail = tile - p.num_full;
+          const long long band_f4 = 32LL * BN / 4;
+          split.pieces = p.tail_split;
+          split.piece = piece;
+          split.piece_stride = 8 * band_f4;
+          split.ws0 = reinterpret_cast<const float4*>(p.ws) +
+                      static_cast<long long>(tail) * p.tail_split * split.piece_stride +
+                      band_id * band_f4;
+          store = publish_partial(tacc, BN, lane, split, p.counters + tail * 8 + band_id,
+                                  p.tail_split);
+        }
+        if (store)
+          epilogue_tile<BN, EPI, STATS>(p, &tmOut, tacc, bt, m0, n0, staging, lane, sc, kb1 > kb0,
+                                        split, rs);
       }
-      if (store)
-        epilogue_tile<BN, EPI, STATS>(p, &tmOut, tacc, bt, m0, n0, staging, lane, sc, kb1 > kb0,
-                                      split, rs);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acce0_even + 8u * buf);
     }
-    if (lane == 0) bulk_wait_group<0>();
+    if (lane == 0) {
+      // C loads still in flight (only after a wait gave up) land before exit.
+      for (long long g = r_done; g < r_issued; ++g)
+        wait_bounded(cbar0 + 8u * static_cast<uint32_t>(g % kRingSlots),
+                     static_cast<uint32_t>((g / kRingSlots) & 1), nullptr, SITE_DRAIN);
+      bulk_wait_group<0>();
+    }
     __syncwarp();
   }
 

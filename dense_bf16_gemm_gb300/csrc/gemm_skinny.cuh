@@ -73,15 +73,15 @@ __device__ __forceinline__ void skinny_store(const SkinnyParams& p, int b, int n
   for (int m = 0; m < kSkinnyNX; ++m) {
     if (m < p.M) {
       const long long off = b * p.c_stride + static_cast<long long>(m) * p.ldc + n;
-      float v = p.alpha * acc[m];
+      float v = __fmul_rn(p.alpha, acc[m]);
       if (p.out_kind != 0) {
         const bool f16 = p.out_kind == 2;
         uint16_t* c = static_cast<uint16_t*>(p.C);
-        if (p.beta != 0.0f) v += p.beta * half16_to_float(c[off], f16);
+        if (p.beta != 0.0f) v = __fmaf_rn(p.beta, half16_to_float(c[off], f16), v);
         c[off] = static_cast<uint16_t>(pack_half16x2(v, 0.0f, f16) & 0xFFFFu);
       } else {
         float* c = static_cast<float*>(p.C);
-        if (p.beta != 0.0f) v += p.beta * c[off];
+        if (p.beta != 0.0f) v = __fmaf_rn(p.beta, c[off], v);
         c[off] = v;
       }
     }

@@ -560,3 +560,83 @@ def test_batched_f16_split_pieces(g, monkeypatch):
         ref, _ = oracle.gemm_full(A[b], B[b])
         assert np.array_equal(to_f64(Cd[b]), ref), b
     assert_status_ok(g)
+
+
+# ---------------------------------------------------------------------------
+# beta != 0 on CTA pairs: C is loaded with TMA into a ring of staging slots a
+# few boxes ahead and each box is computed in place.  The register path
+# (GB3_GEMM_C_RING=0) is the one it replaced; both must give the oracle's bits.
+# ---------------------------------------------------------------------------
+RING_SHAPES = [
+    (300, 520, 200),     # one tile per pair; ragged rows and columns
+    (2000, 3000, 136),   # two tiles on some pairs: the look-ahead crosses a tile
+    (4000, 3896, 72),    # four tiles per pair: every slot reused many times
+    (2304, 4136, 64),    # last column tile 40 (or 104) columns wide: partial and empty boxes
+]
+
+
+@pytest.mark.parametrize("width", ["256", "224"])
+@pytest.mark.parametrize("M,N,K", RING_SHAPES)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_c_ring_bit_exact(g, monkeypatch, width, M, N, K, out_dtype):
+    monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", width)
+    monkeypatch.setenv("GB3_GEMM_TAIL_SPLIT", "0")   # whole tiles: the ring's domain
+    A, B, C = int_inputs(M, N, K, seed=M + 5 * N + K)
+    Cq = C.to(out_dtype)
+    ref, _ = oracle.gemm_full(A, B, alpha=2.0, beta=-0.5, C=Cq.to(torch.float32))
+    if out_dtype == torch.float32:
+        want = ref
+    elif out_dtype == torch.float16:
+        want = oracle.round_to_f16_bits(ref)
+    else:
+        want = oracle.round_to_bf16_bits(ref)
+    for ring in ("1", "0"):
+        monkeypatch.setenv("GB3_GEMM_C_RING", ring)
+        out = run_gemm(g, A, B, C=Cq, alpha=2.0, beta=-0.5, out_dtype=out_dtype)
+        got = to_f64(out) if out_dtype == torch.float32 else bits(out.cpu())
+        assert np.array_equal(got, want), f"ring={ring}"
+    assert_status_ok(g)
+
+
+def test_c_ring_matches_register_path_on_random_inputs(g, monkeypatch):
+    """Same FP32 operations in the same order on both paths: identical bits."""
+    M, N, K = 3000, 5000, 2000
+    A, B, C = workloads.gemm_inputs(M, N, K, 71, ("normal", 1.0), ("normal", 1.0), ("normal", 1.0))
+    Ad, Bd = A.cuda(), B.cuda()
+    outs = {}
+    for ring in ("1", "0"):
+        monkeypatch.setenv("GB3_GEMM_C_RING", ring)
+        Cd = C.cuda()
+        g.gemm(Ad, Bd, Cd, alpha=0.75, beta=1.5)
+        outs[ring] = Cd
+    torch.cuda.synchronize()
+    assert torch.equal(outs["1"], outs["0"])
+    rows = np.random.default_rng(71).choice(M, 64, replace=False)
+    ref, ab = oracle.gemm_entries(A, B, np.repeat(rows, N), np.tile(np.arange(N), rows.size),
+                                  alpha=0.75, beta=1.5, C=C)
+    got = to_f64(outs["1"])[np.repeat(rows, N), np.tile(np.arange(N), rows.size)]
+    cm = C.numpy()[np.repeat(rows, N), np.tile(np.arange(N), rows.size)]
+    assert_within(got, ref, oracle.gemm_tolerance(ref, ab, 0.75, 1.5, cm), "ring 3000x5000x2000")
+    assert_status_ok(g)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16])
+def test_c_ring_batched_padded(g, monkeypatch, out_dtype):
+    """The third TMA coordinate (matrix of the batch) and a padded pitch of C
+    on the ring's loads; padding of C untouched."""
+    monkeypatch.setenv("GB3_GEMM_TAIL_SPLIT", "0")
+    batch, M, N, K = 3, 600, 1000, 136
+    A, B, C = batched_int_inputs(batch, M, N, K, 72, torch.float16)
+    Cq = C.to(out_dtype)
+    Cd, Cbuf = padded(Cq, 4, 16, 1024.0)
+    g.gemm(A.cuda(), B.cuda(), Cd, alpha=2.0, beta=-0.5)
+    torch.cuda.synchronize()
+    for b in range(batch):
+        ref, _ = oracle.gemm_full(A[b], B[b], alpha=2.0, beta=-0.5, C=Cq[b].to(torch.float32))
+        if out_dtype == torch.float32:
+            assert np.array_equal(to_f64(Cd[b]), ref), b
+        else:
+            assert np.array_equal(bits(Cd[b].cpu()), oracle.round_to_f16_bits(ref)), b
+    assert torch.all(Cbuf[:, M:, :].float().cpu() == 1024.0)
+    assert torch.all(Cbuf[:, :, N:].float().cpu() == 1024.0)
+    assert_status_ok(g)
