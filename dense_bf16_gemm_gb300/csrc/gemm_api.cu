@@ -997,8 +997,8 @@ int run_pair(gemm_plan& pl, int dev, int slots, const Problem& q, cudaStream_t s
   if ((st = attach_row_stats(dev, q, p.n_blocks, &rs, stream)) != GEMM_OK) return st;
   pair_units(dev, &pl, q, bn, &p, stream, false, slots);
   if (bn != 256 && bn != 224) return GEMM_ERR_UNSUPPORTED;
-  // The ring kernels compute whole tiles only and always read C.
-  const bool ring = pair_reads_c_ring(q.beta) && p.tail_split == 1;
+  // The ring kernels always read C.
+  const bool ring = pair_reads_c_ring(q.beta);
   if (ring) {
     pl.stages = kPairStages - 1;
     pl.smem_bytes = pair_ring_smem_for(bn);

@@ -553,14 +553,19 @@ static_assert(kRingAhead < kRingSlots, "a slot must be free before its next load
 
 // The ring boxes of one warp are numbered r = 0, 1, ... in the order they are
 // computed: box r lives in slot r % kRingSlots, whose barrier completes phase
-// (r / kRingSlots) & 1 when the box has landed.  topup(r) issues the loads of
-// every box up to r + kRingAhead that exists.  Returns false when a wait gave
-// up (the abort flag is then set).
-template <int BN, int EPI, bool STATS, typename TopUp>
+// (r / kRingSlots) & 1 when the box has landed; `issued` counts the boxes
+// whose loads were issued.  Whole tiles (ON_DEMAND false): topup(r) issues
+// the loads of every box up to r + kRingAhead that exists.  The last piece
+// of a split tile (ON_DEMAND true, `split` its pieces), whose turn to write C
+// is known only when it arrives, loads each box just before computing it
+// (these come before every whole tile of the warp, so the two never
+// interleave).  Returns false when a wait gave up (the abort flag is then set).
+template <int BN, int EPI, bool STATS, bool ON_DEMAND, typename TopUp>
 __device__ __forceinline__ bool epilogue_tile_ring(const TileParams& p, const CUtensorMap* tmOut,
                                                    uint32_t tacc, int b, int m0, int n0,
                                                    uint32_t ring, uint32_t cbar0, int lane,
-                                                   long long& r, int& sc,
+                                                   long long& r, long long& issued, int& sc,
+                                                   const SplitCtx& split,
                                                    const RowStatsParams& rs,
                                                    volatile int* abort_flag, TopUp&& topup) {
   static_assert(EPI != EPI_GATE_UP, "the gate/up epilogue reads no C");
@@ -568,20 +573,28 @@ __device__ __forceinline__ bool epilogue_tile_ring(const TileParams& p, const CU
   constexpr int kSub = Box::kCols / 32;
   RowAcc racc;
   row_acc_init(racc);
-  const SplitCtx whole{1, 0, nullptr, 0};
 #pragma unroll 1
   for (int c0 = 0; c0 < BN; c0 += Box::kCols) {
     if (m0 >= p.M || n0 + c0 >= p.N) continue;
-    topup(r);
     const int slot = static_cast<int>(r % kRingSlots);
     const uint32_t stg = ring + slot * kStageBox;
+    if constexpr (ON_DEMAND) {
+      if (lane == 0) {
+        bulk_wait_group_read<kRingSlots - 1>();  // the slot's previous store has read it
+        mbar_arrive_expect_tx(cbar0 + 8u * slot, 32 * Box::kRowBytes);
+        tma_load_3d(stg, tmOut, cbar0 + 8u * slot, n0 + c0, m0, b);
+      }
+      issued = r + 1;
+    } else {
+      topup(r);
+    }
     const bool got = wait_bounded(cbar0 + 8u * slot, static_cast<uint32_t>((r / kRingSlots) & 1),
                                   abort_flag, SITE_EPI_C_FULL);
     if (!__all_sync(0xffffffffu, got)) return false;
 #pragma unroll 1
     for (int h = 0; h < kSub; ++h) {
       float v[32], c[32];
-      acc_slice(v, tacc, c0 + 32 * h, lane, whole);
+      acc_slice(v, tacc, c0 + 32 * h, lane, split);
       if constexpr (EPI == EPI_F32) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) {

@@ -204,11 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int band_id = static_cast<int>(rank) * 4 + (warp & 3);  // 32-row band of the pair tile
     int local = 0;
     int sc = 0;
-    // C ring: the load cursor walks this warp's boxes in the order the
-    // epilogue computes them.  The host launches RING kernels only with
-    // beta != 0 and whole tiles (no split pieces: which piece writes C is
-    // known only at run time, and their register path is left out of these
-    // kernels).
+    // C ring (RING kernels run only with beta != 0): the load cursor walks
+    // this warp's boxes of whole tiles in the order the epilogue computes
+    // them, starting at the first whole tile.  Split pieces come first in the
+    // unit order; the last piece of a split tile loads its boxes on demand.
+    bool cursor_started = false;
     const uint32_t cbar0 = drain_bar + 8u * (1 + ew * kRingSlots);
     long long r_done = 0, r_issued = 0;
     int cu = p.num_units, cc0 = 0, cb = 0, cm0 = 0, cn0 = 0;
@@ -244,30 +244,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         cursor_settle();
       }
     };
-    auto prefetch_unit = [&](int u) {
-      if (u < p.num_units) {
-        int tile_, kb0_, kb1_, piece_, b_, mb_, nb_;
-        unit_of(u, p, tile_, kb0_, kb1_, piece_);
-        tile_coords(tile_, p, b_, mb_, nb_);
-        prefetch_c_band<BN, EPI>(p, &tmOut, b_,
-                                 mb_ * kPairBM + static_cast<int>(rank) * 128 + band,
-                                 nb_ * Cfg::kOutCols);
-      }
-    };
-    if (lane == 0) prefetch_unit(cluster);
     for (int u = cluster; u < p.num_units; u += nclusters, ++local) {
       int tile, kb0, kb1, piece;
       unit_of(u, p, tile, kb0, kb1, piece);
       int bt, mb, nb;
       tile_coords(tile, p, bt, mb, nb);
-      // C of this CTA's next unit travels to L2 during this unit's epilogue
-      // and the next unit's main loop.
-      if (lane == 0) prefetch_unit(u + nclusters);
-      if (RING && r_issued == 0 && cu == p.num_units) {
-        // First tile: start the C loads before waiting for its accumulator.
+      if (RING && piece < 0 && !cursor_started) {
+        // First whole tile: start its C loads before waiting for its accumulator.
+        cursor_started = true;
+        r_issued = r_done;
         cursor_at(u);
         cursor_settle();
-        topup(0);
+        topup(r_done);
       }
       const int buf = local & 1;
       const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
@@ -278,28 +266,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                             static_cast<uint32_t>(buf * Cfg::kAccStride);
       const int m0 = mb * kPairBM + static_cast<int>(rank) * 128 + band;
       const int n0 = nb * Cfg::kOutCols;
+      SplitCtx split{1, 0, nullptr, 0};
+      bool store = true;
+      if (piece >= 0) {
+        // One K piece of a tail tile: publish the partial; the band's last
+        // piece adds them all up and writes C.  Workspace: [tail tile][piece]
+        // [band 0..7][32 x BN floats].
+        const int tail = tile - p.num_full;
+        const long long band_f4 = 32LL * BN / 4;
+        split.pieces = p.tail_split;
+        split.piece = piece;
+        split.piece_stride = 8 * band_f4;
+        split.ws0 = reinterpret_cast<const float4*>(p.ws) +
+                    static_cast<long long>(tail) * p.tail_split * split.piece_stride +
+                    band_id * band_f4;
+        store = publish_partial(tacc, BN, lane, split, p.counters + tail * 8 + band_id,
+                                p.tail_split);
+      }
       if constexpr (RING) {
-        if (!epilogue_tile_ring<BN, EPI, STATS>(p, &tmOut, tacc, bt, m0, n0, staging, cbar0,
-                                                lane, r_done, sc, rs, abort_flag, topup))
-          break;
+        bool ok = true;
+        if (piece < 0)
+          ok = epilogue_tile_ring<BN, EPI, STATS, false>(p, &tmOut, tacc, bt, m0, n0, staging,
+                                                         cbar0, lane, r_done, r_issued, sc, split,
+                                                         rs, abort_flag, topup);
+        else if (store)
+          ok = epilogue_tile_ring<BN, EPI, STATS, true>(p, &tmOut, tacc, bt, m0, n0, staging,
+                                                        cbar0, lane, r_done, r_issued, sc, split,
+                                                        rs, abort_flag, topup);
+        if (!ok) break;
       } else {
-        SplitCtx split{1, 0, nullptr, 0};
-        bool store = true;
-        if (piece >= 0) {
-          // One K piece of a tail tile: publish the partial; the band's last
-          // piece adds them all up and writes C.  Workspace: [tail tile][piece]
-          // [band 0..7][32 x BN floats].
-          const int tail = tile - p.num_full;
-          const long long band_f4 = 32LL * BN / 4;
-          split.pieces = p.tail_split;
-          split.piece = piece;
-          split.piece_stride = 8 * band_f4;
-          split.ws0 = reinterpret_cast<const float4*>(p.ws) +
-                      static_cast<long long>(tail) * p.tail_split * split.piece_stride +
-                      band_id * band_f4;
-          store = publish_partial(tacc, BN, lane, split, p.counters + tail * 8 + band_id,
-                                  p.tail_split);
-        }
         if (store)
           epilogue_tile<BN, EPI, STATS>(p, &tmOut, tacc, bt, m0, n0, staging, lane, sc, kb1 > kb0,
                                         split, rs);

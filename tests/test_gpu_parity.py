@@ -426,10 +426,13 @@ def test_pair_widths_bit_exact(g, monkeypatch, width, M, N, K, out_dtype):
 @pytest.mark.parametrize("pieces", ["2", "3", "5"])
 @pytest.mark.parametrize("M,N,K", [(512, 1000, 1000), (300, 520, 704), (1000, 712, 2048)])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-def test_split_k_pieces_bit_exact(g, monkeypatch, pieces, M, N, K, out_dtype):
+@pytest.mark.parametrize("ring", ["1", "0"])
+def test_split_k_pieces_bit_exact(g, monkeypatch, pieces, M, N, K, out_dtype, ring):
     """Every pair tile cut into K pieces whose partials are summed by the last
-    piece; integer inputs keep every partial exact."""
+    piece (which reads C through the staging ring, or with the register loads
+    it replaced); integer inputs keep every partial exact."""
     monkeypatch.setenv("GB3_GEMM_SPLIT_ALL", pieces)
+    monkeypatch.setenv("GB3_GEMM_C_RING", ring)
     p = g.plan(M, N, K, out_dtype)
     kb = -(-K // 64)
     kbp = -(-kb // min(int(pieces), kb))
@@ -580,7 +583,7 @@ RING_SHAPES = [
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16, torch.float16])
 def test_c_ring_bit_exact(g, monkeypatch, width, M, N, K, out_dtype):
     monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", width)
-    monkeypatch.setenv("GB3_GEMM_TAIL_SPLIT", "0")   # whole tiles: the ring's domain
+    monkeypatch.setenv("GB3_GEMM_TAIL_SPLIT", "0")   # whole tiles: the look-ahead cursor alone
     A, B, C = int_inputs(M, N, K, seed=M + 5 * N + K)
     Cq = C.to(out_dtype)
     ref, _ = oracle.gemm_full(A, B, alpha=2.0, beta=-0.5, C=Cq.to(torch.float32))
@@ -639,4 +642,23 @@ def test_c_ring_batched_padded(g, monkeypatch, out_dtype):
             assert np.array_equal(bits(Cd[b].cpu()), oracle.round_to_f16_bits(ref)), b
     assert torch.all(Cbuf[:, M:, :].float().cpu() == 1024.0)
     assert torch.all(Cbuf[:, :, N:].float().cpu() == 1024.0)
+    assert_status_ok(g)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_c_ring_with_split_tail(g, monkeypatch, out_dtype):
+    """A planned split tail: the pieces' last arrivals load C on demand, then
+    the whole tiles run the look-ahead cursor, in one launch."""
+    M, N, K = 2048, 2560, 3072
+    p = g.plan(M, N, K, out_dtype)
+    assert p["kernel_name"] == "pair" and p["split_k"] > 1
+    A, B, C = int_inputs(M, N, K, seed=73)
+    Cq = C.to(out_dtype)
+    ref, _ = oracle.gemm_full(A, B, alpha=2.0, beta=-0.5, C=Cq.to(torch.float32))
+    want = ref if out_dtype == torch.float32 else oracle.round_to_bf16_bits(ref)
+    for ring in ("1", "0"):
+        monkeypatch.setenv("GB3_GEMM_C_RING", ring)
+        out = run_gemm(g, A, B, C=Cq, alpha=2.0, beta=-0.5, out_dtype=out_dtype)
+        got = to_f64(out) if out_dtype == torch.float32 else bits(out.cpu())
+        assert np.array_equal(got, want), f"ring={ring}"
     assert_status_ok(g)
