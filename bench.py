@@ -39,22 +39,40 @@ import workloads  # noqa: E402
 FLUSH_BYTES = 256 << 20
 
 # DRAM traffic per launch from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`
-# (summarised under profiles/), valid only for the kernel sources it was taken with.
+# (summarised under profiles/), valid only for the sources the kernel is compiled from
+# (`src_sha` over `PAIR_KERNEL_SOURCES`) and for the plan it ran with.
+PAIR_KERNEL_SOURCES = ("ptx.cuh", "gemm_kernels.cuh", "gemm_kernels_pair.cuh")
 NCU_TRAFFIC: dict = {
-    # profiles/gemm_pair_bf16_4096.md: 75.23 MB read + 29.90 MB written per launch
-    "gemm_4096_bf16": {"bytes": 105130240, "src_sha": "16beb2a2762d052b"},
+    # profiles/gemm_pair_bf16_4096.md: 75.98 MB read + 30.52 MB written per launch
+    "gemm_4096_bf16": {"bytes": 106498048, "sources": PAIR_KERNEL_SOURCES,
+                       "src_sha": "3114f2627f9d8afb",
+                       "plan": {"kernel_name": "pair", "tile_n": 256, "split_k": 2,
+                                "tiles": 284, "stages": 6}},
 }
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files=None) -> str:
+    """sha256 prefix over the named csrc files (all .cu/.cuh files when None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_bf16_gemm_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode())
-                h.update(fh.read())
+    names = sorted(files) if files else sorted(f for f in os.listdir(csrc)
+                                               if f.endswith((".cu", ".cuh")))
+    for f in names:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def traffic_of(w, plan) -> int | None:
+    """ncu DRAM bytes per launch of workload w, if taken with these kernel
+    sources and this plan."""
+    tr = NCU_TRAFFIC.get(w.name)
+    if not tr or tr.get("src_sha") != kernel_source_hash(tr["sources"]):
+        return None
+    if any(plan.get(k) != v for k, v in tr["plan"].items()):
+        return None
+    return tr["bytes"]
 
 
 def load_peaks() -> dict:
@@ -472,10 +490,7 @@ def run_ours(args):
     value, unit = metric_of(w, ms_step)
     value *= world          # weak scaling: every rank runs its own problem
     src_hash = kernel_source_hash()
-    traffic = None
-    tr = NCU_TRAFFIC.get(w.name)
-    if tr and tr.get("src_sha") == src_hash:
-        traffic = tr["bytes"]
+    traffic = traffic_of(w, plan_of(lib, w))
     roof = roofline(w, ms_mean, peaks, traffic)
 
     e2e_steps = max(3, min(args.steps, 20))

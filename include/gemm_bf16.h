@@ -271,7 +271,10 @@ GEMM_API const char *gemm_status_string(int status);
  * Synchronizes `stream`, then returns and clears the device status word of
  * the current device (GEMM_OK if no kernel reported an error since the last
  * read).  The site of the failure (which pipeline wait) is written to
- * *site when site is not NULL.
+ * *site when site is not NULL: 1 producer waiting for a free stage, 2 MMA
+ * waiting for a full stage, 3 MMA waiting for a free accumulator, 4 epilogue
+ * waiting for a full accumulator, 5 a drain before exit, 6 the split-K kernel,
+ * 7 gemm_selftest_wait_timeout, 8 epilogue waiting for a box of C.
  */
 GEMM_API int gemm_get_device_status(void *stream, int *site);
 
@@ -343,7 +346,9 @@ typedef struct gemm_plan {
  * host logic otherwise; returns GEMM_INVALID_ARG for invalid sizes or dtype.
  * M > 128 runs on CTA pairs (256-row tiles) with the tile width that needs the
  * fewest waves; the environment variable GB3_GEMM_PAIR_TILE_N (256 or 224)
- * forces one width, for tuning and tests.  M <= 128 runs on the small-M
+ * forces one width, for tuning and tests.  The plan is that of beta == 0: with
+ * beta != 0 the CTA-pair kernel runs one stage fewer (its shared memory holds
+ * a deeper staging ring for C) unless GB3_GEMM_C_RING = 0.  M <= 128 runs on the small-M
  * kernel when its waves of 64-row weight units stream less of B per SM than
  * the alternative (the split-K kernel for M <= 16, the single-CTA tiled
  * kernel above); GB3_GEMM_SMALL_M = 1 or 0 forces or forbids it.
