@@ -555,16 +555,18 @@ def attention_tolerance(res, D: int, Nk: int, out_bf16=True):
       the argument is within ``e = (fp32_sum_rel(D) + 8 u) * smax``.
     * Weights: exp and the running rescaling keep ratios between keys, so a
       score shift of at most e moves each normalised weight by a factor within
-      ``exp(+-2e)``; the BF16 probabilities add 2^-9, the exp evaluation
-      2^-20, the FP32 sum of the Nk probabilities ``fp32_sum_rel(Nk)``:
-      ``eta = exp(2e)(1 + 2^-9)(1 + 2^-20)(1 + fp32_sum_rel(Nk)) - 1``.
+      ``exp(+-2e)``; the BF16 probabilities add 2^-8 (round to nearest with an
+      8-bit significand, whatever the scale the probabilities are taken at),
+      the exp evaluation 2^-20, the FP32 sum of the Nk probabilities
+      ``fp32_sum_rel(Nk)``:
+      ``eta = exp(2e)(1 + 2^-8)(1 + 2^-20)(1 + fp32_sum_rel(Nk)) - 1``.
     * Output: the FP32 products of weights and values over Nk keys
       (``fp32_sum_rel(Nk)``), the per-block rescaling (Nk/128 + 2 roundings)
       and the final division: all relative to ``abs_o = sum_j w_j |v_j|``.
     Plus the BF16 half-ulp of a BF16 output.
     """
     e = (fp32_sum_rel(D) + 8.0 * U32) * res["smax"][:, None]
-    eta = np.exp(2.0 * e) * (1 + 2.0 ** -9) * (1 + 2.0 ** -20) * (1 + fp32_sum_rel(Nk)) - 1.0
+    eta = np.exp(2.0 * e) * (1 + 2.0 ** -8) * (1 + 2.0 ** -20) * (1 + fp32_sum_rel(Nk)) - 1.0
     acc = fp32_sum_rel(Nk) + (Nk / 128.0 + 2.0) * U32
     tol = (eta + acc * (1.0 + eta)) * res["abs_o"]
     if out_bf16:
