@@ -252,10 +252,13 @@ GEMM_API int gemm_rmsnorm_gate_up_silu(int64_t M, int64_t N, int64_t K,
  * (GEMM_ERR_ALIGNMENT otherwise).
  *
  * Arithmetic: scores accumulate in FP32 on the tensor cores (BF16 operands);
- * the softmax runs in FP32 in base 2 (exp2 of s * scale * log2 e minus the
- * running maximum); the probabilities enter the second product as BF16
- * (nearest even); the row sums, the rescaling of the running output and the
- * final division are FP32; a BF16 output is rounded to nearest even once.
+ * the softmax runs in FP32 in base 2 (exp2 of s * scale * log2 e minus a
+ * running maximum that moves only when a key block's maximum exceeds it by
+ * more than 8, so probabilities stay below 2^8); the probabilities enter the
+ * second product as BF16 (nearest even) and the output accumulates over all
+ * keys in FP32 on the tensor cores; the row sums, the rescaling of the
+ * running output when the maximum moves and the final division are FP32; a
+ * BF16 output is rounded to nearest even once.
  * One launch on `stream`; allocates nothing.
  */
 GEMM_API int gemm_attention(int64_t heads, int64_t Nq, int64_t Nk, int64_t D, float scale,

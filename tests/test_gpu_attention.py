@@ -103,6 +103,30 @@ def test_attention_dominant_key(g):
     assert_status_ok(g)
 
 
+@pytest.mark.parametrize("direction", ["growing", "shrinking"])
+def test_attention_running_maximum_moves(g, direction):
+    """Scores that climb by about 17 (base 2) from one key block to the next
+    move every row's running maximum past the rescaling threshold on every
+    block (the output accumulator is rescaled each time); falling scores never
+    move it after the first block."""
+    H, Nq, Nk, D = 2, 200, 1000, 64
+    gen = torch.Generator().manual_seed(11)
+    Q = torch.randn(H, Nq, D, generator=gen) * 0.1
+    Q[..., 0] = 1.0
+    K = torch.randn(H, Nk, D, generator=gen) * 0.1
+    ramp = torch.arange(Nk, dtype=torch.float32) / 128.0 * 12.0
+    K[..., 0] = ramp if direction == "growing" else ramp.flip(0)
+    V = torch.randn(H, Nk, D, generator=gen)
+    Q, K, V = (x.to(BF16) for x in (Q, K, V))
+    O = g.attention(Q.cuda(), K.cuda(), V.cuda(), 1.0, out_dtype=F32)
+    torch.cuda.synchronize()
+    hh, rr = np.meshgrid(np.arange(H), np.arange(Nq), indexing="ij")
+    res = oracle.attention_rows(Q, K, V, 1.0, hh.ravel(), rr.ravel())
+    tol = oracle.attention_tolerance(res, D, Nk, out_bf16=False)
+    assert_within(to_f64(O)[hh.ravel(), rr.ravel()], res["o"], tol, direction)
+    assert_status_ok(g)
+
+
 def test_attention_padded_strides_and_2d(g):
     H, Nq, Nk, D = 3, 150, 260, 64
     Q, K, V = workloads.attention_inputs(H, Nq, Nk, D, 8)
