@@ -139,15 +139,15 @@ int smallm_stages(int nx) {
 // GB300), so what decides is how many SMs a plan keeps streaming and for how
 // long.  Measured against the split-K kernel (M <= 16) and the single-CTA
 // tiled kernel (16 < M <= 128), the 64-row units win while they fit in one
-// wave, and for M <= 16 in two; with more units the others read B as fast and
-// are kept.  GB3_GEMM_SMALL_M = 0 or 1 forces the choice.
+// wave; with more units the others read B as fast or faster and are kept
+// (two waves at M <= 16: even with K = 4096, 2x slower with K = 8192).
+// GB3_GEMM_SMALL_M = 0 or 1 forces the choice.
 bool use_small_m(int64_t batch, int64_t M, int64_t N, int64_t K, int sms) {
   (void)K;
   if (M > kSmallMMaxM) return false;
   const int force = env_int("GB3_GEMM_SMALL_M", -1);
   if (force == 0 || force == 1) return force == 1;
-  const int64_t units = batch * ceil_div(N, kSmallRows);
-  return units <= sms || (M <= kSkinnyMaxM && units <= 2 * static_cast<int64_t>(sms));
+  return batch * ceil_div(N, kSmallRows) <= sms;
 }
 
 template <int BN>
@@ -1058,6 +1058,15 @@ int run_single(const gemm_plan& pl, int dev, const Problem& q, cudaStream_t stre
                                                              stream);
 }
 
+// k-blocks of the weight the split-K producer issues back to back (see the
+// kernel); GB3_SKINNY_ISSUE_GROUP overrides it for tuning.
+int skinny_issue_group(int kb_per_split) {
+  (void)kb_per_split;
+  const int forced = env_int("GB3_SKINNY_ISSUE_GROUP", 0);
+  if (forced > 0) return std::min(forced, kSkinnyStages);
+  return 4;
+}
+
 SkinnyParams skinny_params(const gemm_plan& pl, const Problem& q) {
   SkinnyParams p;
   p.M = static_cast<int>(q.M);
@@ -1078,6 +1087,7 @@ SkinnyParams skinny_params(const gemm_plan& pl, const Problem& q) {
   p.idesc = idesc_f32_acc(kSkinnyRows, kSkinnyNX, q.in_dtype == GEMM_IN_F16);
   p.ws = nullptr;
   p.counters = nullptr;
+  p.issue_group = skinny_issue_group(p.kb_per_split);
   return p;
 }
 

@@ -23,10 +23,6 @@ namespace gb3 {
 
 constexpr int kSkinnyRows = 128;  // rows of B per unit (the MMA's M)
 constexpr int kSkinnyNX = 16;     // activation rows per MMA (the MMA's N)
-#ifndef GB3_SKINNY_ISSUE_GROUP
-#define GB3_SKINNY_ISSUE_GROUP 4
-#endif
-constexpr int kSkinnyIssueGroup = GB3_SKINNY_ISSUE_GROUP;  // k-blocks issued back to back
 
 struct SkinnyParams {
   int M, N, K;                // sizes of each matrix of the batch
@@ -42,11 +38,11 @@ struct SkinnyParams {
   uint32_t idesc;             // tcgen05 instruction descriptor (BF16 or FP16 operands)
   float* ws;      // [batch][splits][M][N] FP32 partial sums (splits > 1)
   int* counters;  // [batch][n_blocks][4] arrival counters, zero between calls
+  int issue_group;  // k-blocks the producer issues back to back (1 .. STAGES)
 };
 
 template <int STAGES>
 struct SkinnyCfg {
-  static_assert(STAGES >= kSkinnyIssueGroup, "a group of k-blocks must fit in the ring");
   static constexpr int kWBytes = kSkinnyRows * kBK * 2;  // 16 KB
   static constexpr int kXBytes = kSkinnyNX * kBK * 2;    // 2 KB
   static constexpr int kStageBytes = kWBytes + kXBytes;  // 18 KB, keeps 1024-byte alignment
@@ -151,12 +147,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
         int bt, nb, sp, kb0, kb1;
         skinny_unit(u, p, bt, nb, sp, kb0, kb1);
-        // k-blocks are issued kSkinnyIssueGroup at a time, back to back, once
+        // k-blocks are issued p.issue_group at a time, back to back, once
         // that many stages are free: each row of B is then read as one
-        // longer run of consecutive bytes (about 5 % more HBM throughput than
-        // issuing each stage as soon as it frees).
-        for (int g0 = kb0; ok && g0 < kb1; g0 += kSkinnyIssueGroup) {
-          const int gn = min(kSkinnyIssueGroup, kb1 - g0);
+        // longer run of consecutive bytes.
+        const int group = max(1, min(p.issue_group, STAGES));
+        for (int g0 = kb0; ok && g0 < kb1; g0 += group) {
+          const int gn = min(group, kb1 - g0);
           int s_free = s;
           uint32_t ph_free = ph;
           for (int j = 0; j < gn; ++j) {
