@@ -137,16 +137,18 @@ int smallm_stages(int nx) {
 // Whether an M <= 128 problem runs on the small-M kernel.  A CTA streams B
 // from HBM at about 32-37 GB/s whatever the number of busy SMs (measured on
 // GB300), so what decides is how many SMs a plan keeps streaming and for how
-// long.  Measured against the split-K kernel (M <= 16) and the single-CTA
-// tiled kernel (16 < M <= 128), the 64-row units win while they fit in one
-// wave; with more units the others read B as fast or faster and are kept
-// (two waves at M <= 16: even with K = 4096, 2x slower with K = 8192).
+// long.  Against the single-CTA tiled kernel (16 < M <= 128) the 64-row units
+// win while they fit in one wave; with more units the tiled kernel reads B
+// as fast and is kept.  For M <= 16 the split-K kernel, with its split chosen
+// by the time model of choose_split, was as fast or faster on every measured
+// shape (16x8192x8192 37.0 us against 41.0, 16x14336x4096 28.7 against 42.0).
 // GB3_GEMM_SMALL_M = 0 or 1 forces the choice.
 bool use_small_m(int64_t batch, int64_t M, int64_t N, int64_t K, int sms) {
   (void)K;
   if (M > kSmallMMaxM) return false;
   const int force = env_int("GB3_GEMM_SMALL_M", -1);
   if (force == 0 || force == 1) return force == 1;
+  if (M <= kSkinnyMaxM) return false;
   return batch * ceil_div(N, kSmallRows) <= sms;
 }
 
@@ -179,10 +181,21 @@ int pair_ring_smem_for(int bn) {
 
 int pair_stage_bytes(int bn) { return 128 * kBK * 2 + (bn / 2) * kBK * 2; }
 
-// Split of K for the skinny path: minimise the k-blocks of the busiest CTA,
-// ceil(units / grid) * ceil(k_blocks / S), with a small charge per extra split
-// for the partial-sum traffic.
+// Split of K for the skinny path, from a time model fit to same-box
+// measurements of nine decode shapes at 1..8 splits (it picks the fastest
+// measured split for each).  Every wave of units streams each unit's weight
+// rows at min(60 GB/s per SM, 7.1 TB/s shared by the busy SMs), and every
+// split beyond the first costs about 4 us per wave (partial sums, arrival
+// counters and the combine).  GB3_SKINNY_SPLITS forces a split (tuning).
 void choose_split(int64_t n_blocks, int64_t k_blocks, int sms, int* splits, int* kb_per) {
+  const int forced = env_int("GB3_SKINNY_SPLITS", 0);
+  if (forced > 0) {
+    const int64_t kbp = ceil_div(k_blocks, std::min<int64_t>(forced, k_blocks));
+    *kb_per = static_cast<int>(kbp);
+    *splits = static_cast<int>(ceil_div(k_blocks, kbp));
+    return;
+  }
+  constexpr double kSmGBs = 60.0, kTotalGBs = 7100.0, kSplitNs = 4000.0;
   int best_s = 1;
   double best = 1e300;
   for (int s = 1; s <= 32; ++s) {
@@ -191,8 +204,11 @@ void choose_split(int64_t n_blocks, int64_t k_blocks, int sms, int* splits, int*
     const int64_t real_s = ceil_div(k_blocks, kbp);  // splits that get work
     if (real_s != s) continue;
     const int64_t units = n_blocks * s;
-    const double cost = static_cast<double>(ceil_div(units, sms)) * static_cast<double>(kbp) +
-                        0.5 * static_cast<double>(s - 1);
+    const double waves = static_cast<double>(ceil_div(units, sms));
+    const double active = static_cast<double>(std::min<int64_t>(units, sms));
+    const double gbs = std::min(kSmGBs, kTotalGBs / active);        // bytes per ns per SM
+    const double unit_bytes = static_cast<double>(kSkinnyRows) * kbp * kBK * 2;
+    const double cost = waves * (unit_bytes / gbs + kSplitNs * (s - 1));  // ns
     if (cost < best) {
       best = cost;
       best_s = s;

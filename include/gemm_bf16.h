@@ -351,11 +351,11 @@ typedef struct gemm_plan {
  * fewest waves; the environment variable GB3_GEMM_PAIR_TILE_N (256 or 224)
  * forces one width, for tuning and tests.  The plan is that of beta == 0: with
  * beta != 0 the CTA-pair kernel runs one stage fewer (its shared memory holds
- * a deeper staging ring for C) unless GB3_GEMM_C_RING = 0.  M <= 128 runs on
- * the small-M kernel when its 64-row weight units (batch * ceil(N / 64)) fit
- * in one wave on the SMs, else on the split-K kernel (M <= 16) or the
- * single-CTA tiled kernel (16 < M <= 128); GB3_GEMM_SMALL_M = 1 or 0 forces
- * or forbids it.
+ * a deeper staging ring for C) unless GB3_GEMM_C_RING = 0.  M <= 16 runs on
+ * the split-K kernel (K split by a time model of the weight stream).  For
+ * 16 < M <= 128 the small-M kernel runs when its 64-row weight units (batch *
+ * ceil(N / 64)) fit in one wave on the SMs, else the single-CTA tiled kernel.
+ * GB3_GEMM_SMALL_M = 1 or 0 forces or forbids the small-M kernel.
  */
 GEMM_API int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int num_sms,
                    gemm_plan *plan);

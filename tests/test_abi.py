@@ -204,7 +204,7 @@ def test_plan_skinny_split_k(lib):
     d = p.as_dict()
     assert d["kernel_name"] == "skinny_splitk"
     assert d["tile_m"] == 128 and d["tile_n"] == 16
-    assert d["split_k"] >= 2               # 224 row blocks alone leave SMs idle
+    assert d["split_k"] == 2               # 224 row blocks alone: 1.5 waves
     kb = 8192 // 64
     kb_per = -(-kb // d["split_k"])
     assert -(-kb // kb_per) == d["split_k"]   # every split gets work
@@ -348,19 +348,21 @@ def plan(M, N, K, batch=1, sms=152):
 
 
 def test_plan_small_m_routing(lib):
-    # 64-row units that fit in one wave take the small-M kernel
+    # 16 < M <= 128: 64-row units that fit in one wave take the small-M kernel
     assert plan(64, 4096, 4096)["kernel_name"] == "small_m"          # 64 units
     assert plan(96, 8192, 8192)["kernel_name"] == "small_m"          # 128 units
-    assert plan(16, 8192, 8192)["kernel_name"] == "small_m"          # 128 units, M <= 16
-    assert plan(16, 9728, 4096)["kernel_name"] == "small_m"          # 152 units: one wave
-    assert plan(16, 9792, 4096)["kernel_name"] == "skinny_splitk"    # 153 units
-    assert plan(4, 14336, 8192)["kernel_name"] == "skinny_splitk"    # 224 units, M <= 16
+    assert plan(17, 9728, 4096)["kernel_name"] == "small_m"          # 152 units: one wave
+    assert plan(17, 9792, 4096)["kernel_name"] == "tiled"            # 153 units
     assert plan(128, 14336, 4096)["kernel_name"] == "tiled"          # 224 units, M > 16
+    # M <= 16: the split-K kernel
+    assert plan(16, 8192, 8192)["kernel_name"] == "skinny_splitk"
+    assert plan(1, 4096, 4096)["kernel_name"] == "skinny_splitk"
+    assert plan(4, 14336, 8192)["kernel_name"] == "skinny_splitk"
     assert plan(64, 28672, 8192)["kernel_name"] == "tiled"           # 448 units
     assert plan(16, 28672, 8192)["kernel_name"] == "skinny_splitk"   # 448 units
     assert plan(300, 4096, 4096)["kernel_name"] == "pair"            # M > 128
     import workloads
-    w = workloads.WORKLOADS["smallm_16x8192x8192"]
+    w = workloads.WORKLOADS["smallm_64x8192x8192"]
     assert plan(w.M, w.N, w.K)["kernel_name"] == "small_m"
 
 

@@ -163,7 +163,7 @@ def test_small_m_graph_capture_needs_no_workspace(g, small_m):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["skinny_16x28672x8192", "smallm_64x28672x8192",
-                                  "smallm_16x8192x8192"])
+                                  "smallm_64x8192x8192"])
 def test_workload_small_m(g, small_m, name):
     """Full size: every entry within 256 columns of either edge, every row,
     plus 65,536 sampled entries."""

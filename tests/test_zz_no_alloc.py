@@ -74,11 +74,14 @@ def test_noalloc_rejects_problems_larger_than_its_array(native):
     """A decode problem whose partial sums exceed the 8 MiB array is refused
     before any launch.  Real buffers are used so that nothing could touch an
     invalid address even if the call were accepted."""
-    M, N, K = 16, 86016, 8192
-    st, plan = native.gemm_bf16_plan(M, N, K, native.GEMM_OUT_BF16, 0)
-    assert st == 0
-    need = plan.split_k * M * N * 4
-    assert plan.split_k > 1 and need > 8 << 20, "shape no longer exceeds the array"
+    M = 16
+    for N, K in ((77952, 16384), (86016, 8192), (155648, 16384), (163840, 32768)):
+        st, plan = native.gemm_bf16_plan(M, N, K, native.GEMM_OUT_BF16, 0)
+        assert st == 0
+        if plan.split_k > 1 and plan.split_k * M * N * 4 > 8 << 20:
+            break
+    else:
+        pytest.fail("no candidate shape splits K with partials beyond the array")
     A = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
     B = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
     C = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")

@@ -130,11 +130,11 @@ WORKLOADS = {
         dist_a=("normal", 1.0), dist_b=("normal", 1.0 / math.sqrt(8192)),
         out_bf16=True, check="sampled",
         notes="decode batch of 64, weight 470 MB, HBM-bound"),
-    "smallm_16x8192x8192": Workload(
-        "smallm_16x8192x8192", "gemm", 16, 8192, 8192, seed=11,
+    "smallm_64x8192x8192": Workload(
+        "smallm_64x8192x8192", "gemm", 64, 8192, 8192, seed=11,
         dist_a=("normal", 1.0), dist_b=("normal", 1.0 / math.sqrt(8192)),
         out_bf16=True, check="sampled",
-        notes="decode batch of 16 through an 8192 x 8192 projection (134 MB), one wave "
+        notes="decode batch of 64 through an 8192 x 8192 projection (134 MB), one wave "
               "of 64-row units"),
     # Softmax attention (the flash-attention loop).
     "attention_32x4096x4096x128": Workload(
