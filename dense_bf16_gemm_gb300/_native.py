@@ -27,7 +27,7 @@ GEMM_IN_BF16 = 0
 GEMM_IN_F16 = 1
 
 KERNEL_NAMES = {0: "none", 1: "tiled", 2: "skinny_splitk", 3: "scale", 4: "gate_up",
-                5: "pair", 6: "pair_gate_up", 7: "small_m"}
+                5: "pair", 6: "pair_gate_up", 7: "small_m", 8: "skinny_gate_up"}
 
 # Every symbol the header declares.
 EXPORTED = (

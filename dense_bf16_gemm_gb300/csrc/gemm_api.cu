@@ -44,6 +44,7 @@ constexpr int kTileN = 256;        // output columns per tile of the single-CTA 
 constexpr int kStages = 4;         // its ring depth (48 KB per stage)
 constexpr int kGateUpStages = 4;   // single-CTA gate/up: 16 KB X + 16 KB Wg + 16 KB Wu per stage
 constexpr int kSkinnyStages = 12;  // 18 KB per stage
+constexpr int kSkinnyGateUpStages = 6;  // 34 KB per stage (Wg, Wu and X rows)
 constexpr int kSkinnyMaxM = 16;
 constexpr int kGroupM = 16;
 
@@ -54,6 +55,7 @@ using CfgF32 = GemmCfg<kTileN, kStages, EPI_F32>;
 using CfgBF16 = GemmCfg<kTileN, kStages, EPI_BF16>;
 using CfgGU = GemmCfg<256, kGateUpStages, EPI_GATE_UP>;
 using CfgSkinny = SkinnyCfg<kSkinnyStages>;
+using CfgSkinnyGU = SkinnyCfg<kSkinnyGateUpStages, true>;
 using CfgPairGU = PairCfg<256, kPairStages, EPI_GATE_UP>;
 
 // Tile widths compiled for the CTA-pair GEMM.
@@ -108,7 +110,8 @@ enum KernelKind {
   K_GATE_UP = 4,
   K_PAIR = 5,
   K_PAIR_GATE_UP = 6,
-  K_SMALL_M = 7
+  K_SMALL_M = 7,
+  K_SKINNY_GATE_UP = 8
 };
 
 constexpr int kSmallMMaxM = 128;   // the small-M kernel's widest activation tile
@@ -187,7 +190,9 @@ int pair_stage_bytes(int bn) { return 128 * kBK * 2 + (bn / 2) * kBK * 2; }
 // rows at min(60 GB/s per SM, 7.1 TB/s shared by the busy SMs), and every
 // split beyond the first costs about 4 us per wave (partial sums, arrival
 // counters and the combine).  GB3_SKINNY_SPLITS forces a split (tuning).
-void choose_split(int64_t n_blocks, int64_t k_blocks, int sms, int* splits, int* kb_per) {
+// weights: weight matrices a unit streams (2 for gate/up).
+void choose_split(int64_t n_blocks, int64_t k_blocks, int sms, int* splits, int* kb_per,
+                  int weights = 1) {
   const int forced = env_int("GB3_SKINNY_SPLITS", 0);
   if (forced > 0) {
     const int64_t kbp = ceil_div(k_blocks, std::min<int64_t>(forced, k_blocks));
@@ -207,7 +212,7 @@ void choose_split(int64_t n_blocks, int64_t k_blocks, int sms, int* splits, int*
     const double waves = static_cast<double>(ceil_div(units, sms));
     const double active = static_cast<double>(std::min<int64_t>(units, sms));
     const double gbs = std::min(kSmGBs, kTotalGBs / active);        // bytes per ns per SM
-    const double unit_bytes = static_cast<double>(kSkinnyRows) * kbp * kBK * 2;
+    const double unit_bytes = static_cast<double>(kSkinnyRows) * kbp * kBK * 2 * weights;
     const double cost = waves * (unit_bytes / gbs + kSplitNs * (s - 1));  // ns
     if (cost < best) {
       best = cost;
@@ -407,6 +412,24 @@ int plan_gate_up(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pa
     pl->smem_bytes = CfgPairGU::kSmemBytes;
     pl->launches = 1;
     pl->stage_tx_bytes = 2 * CfgPairGU::kStageBytes;
+    return GEMM_OK;
+  }
+  if (M <= kSkinnyMaxM && env_int("GB3_GATE_UP_SKINNY", 1) != 0) {
+    // Decode sizes: Wg and Wu stream through the split-K kernel together.
+    const int64_t nb = ceil_div(N, kSkinnyRows), kb = ceil_div(K, kBK);
+    int s, kbp;
+    choose_split(nb, kb, sms, &s, &kbp, 2);
+    pl->kernel = K_SKINNY_GATE_UP;
+    pl->tile_m = kSkinnyRows;
+    pl->tile_n = kSkinnyNX;
+    pl->tile_k = kBK;
+    pl->stages = kSkinnyGateUpStages;
+    pl->split_k = s;
+    pl->tiles = nb * s;
+    pl->grid = static_cast<int>(std::min<int64_t>(pl->tiles, sms));
+    pl->smem_bytes = CfgSkinnyGU::kSmemBytes;
+    pl->launches = 1;
+    pl->stage_tx_bytes = CfgSkinnyGU::kStageBytes;
     return GEMM_OK;
   }
   pl->kernel = K_GATE_UP;
@@ -1132,7 +1155,36 @@ int run_skinny(const gemm_plan& pl, int dev, const Problem& q, cudaStream_t stre
       p.counters = g_dev[dev].counters;
     }
   }
-  return launch(kern, pl.grid, kThreads, CfgSkinny::kSmemBytes, stream, tmW, tmX, p);
+  return launch(kern, pl.grid, kThreads, CfgSkinny::kSmemBytes, stream, tmW, tmW, tmX, p);
+}
+
+// The decode-sized gate/up: the split-K kernel with Wg (as B) and Wu.
+int run_skinny_gate_up(const gemm_plan& pl, int dev, const Problem& q, const void* Wu,
+                       cudaStream_t stream) {
+  CUtensorMap tmWg, tmWu, tmX;
+  int st;
+  if ((st = operand_map(&tmWg, q.B, GEMM_IN_BF16, q.K, q.N, 1, q.ldb, 0, kSkinnyRows)) != GEMM_OK)
+    return st;
+  if ((st = operand_map(&tmWu, Wu, GEMM_IN_BF16, q.K, q.N, 1, q.ldb, 0, kSkinnyRows)) != GEMM_OK)
+    return st;
+  if ((st = operand_map(&tmX, q.A, GEMM_IN_BF16, q.K, q.M, 1, q.lda, 0, kSkinnyNX)) != GEMM_OK)
+    return st;
+  SkinnyParams p = skinny_params(pl, q);
+  auto kern = gemm_skinny_kernel<kSkinnyGateUpStages, true>;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern),
+                               CfgSkinnyGU::kSmemBytes)) != GEMM_OK)
+      return st;
+    if (p.splits > 1) {
+      const size_t ws_bytes = static_cast<size_t>(p.splits) * 2 * q.M * q.N * sizeof(float);
+      const size_t counters = static_cast<size_t>(p.n_blocks) * 4;
+      if ((st = ensure_workspace(dev, ws_bytes, counters, stream)) != GEMM_OK) return st;
+      p.ws = g_dev[dev].ws;
+      p.counters = g_dev[dev].counters;
+    }
+  }
+  return launch(kern, pl.grid, kThreads, CfgSkinnyGU::kSmemBytes, stream, tmWg, tmWu, tmX, p);
 }
 
 template <int NX>
@@ -1417,6 +1469,7 @@ int gemm_gate_up_silu(int64_t M, int64_t N, int64_t K, const void* X, int64_t ld
   // Wg and Wu play the part of B; the output is BF16.
   const Problem q{1, M, N, K, 1.0f, 0.0f, X, ldx, 0, Wg, ldw, 0, Y, ldy, 0, GEMM_IN_BF16,
                   GEMM_OUT_BF16};
+  if (pl.kernel == K_SKINNY_GATE_UP) return run_skinny_gate_up(pl, dev, q, Wu, stream);
   const bool pair = pl.kernel == K_PAIR_GATE_UP;
   const int out_cols = pair ? CfgPairGU::kOutCols : CfgGU::kOutCols;
   CUtensorMap tmX, tmWg, tmWu, tmY;
@@ -1662,5 +1715,5 @@ extern "C" int gemm_bf16_skinny_noalloc(int64_t M, int64_t N, int64_t K, float a
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
-  return launch(kern, pl.grid, kThreads, CfgSkinny::kSmemBytes, stream, tmW, tmX, p);
+  return launch(kern, pl.grid, kThreads, CfgSkinny::kSmemBytes, stream, tmW, tmW, tmX, p);
 }

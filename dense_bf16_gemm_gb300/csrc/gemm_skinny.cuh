@@ -15,6 +15,13 @@
 // Roles as in the tiled kernel: warp 0 TMA producer, warp 1 MMA issuer and
 // TMEM owner, warps 2-5 epilogue (warp w reads TMEM lanes 32*(w%4)..+31, i.e.
 // rows n of B; lane i holds the 16 activation rows of output column n).
+//
+// GATE: the fused gate/up projection Y = silu(X Wg^T) * (X Wu^T) at decode
+// sizes ("TMA and Hopper WGMMA", section "Worked consumers and current
+// validation": the fused gate/up consumer).  A stage holds the same 128 rows
+// of Wg and of Wu; two MMAs per K step accumulate gate and up side by side in
+// TMEM; split partials keep gate and up apart, and silu(g) * u is formed only
+// on the summed values.
 #pragma once
 
 #include "gemm_kernels.cuh"
@@ -41,18 +48,20 @@ struct SkinnyParams {
   int issue_group;  // k-blocks the producer issues back to back (1 .. STAGES)
 };
 
-template <int STAGES>
+template <int STAGES, bool GATE = false>
 struct SkinnyCfg {
-  static constexpr int kWBytes = kSkinnyRows * kBK * 2;  // 16 KB
+  static constexpr int kWeights = GATE ? 2 : 1;           // Wg and Wu, or B
+  static constexpr int kWBytes = kSkinnyRows * kBK * 2;  // 16 KB per weight
   static constexpr int kXBytes = kSkinnyNX * kBK * 2;    // 2 KB
-  static constexpr int kStageBytes = kWBytes + kXBytes;  // 18 KB, keeps 1024-byte alignment
+  static constexpr int kXOffset = kWeights * kWBytes;
+  static constexpr int kStageBytes = kXOffset + kXBytes;  // keeps 1024-byte alignment
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
   static constexpr int kRingBytes = STAGES * kStageBytes;
   static constexpr int kBarOffset = kRingBytes;
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
-  static constexpr int kAccStride = kSkinnyNX;
-  static constexpr int kTmemCols = 32;
+  static constexpr int kAccStride = kWeights * kSkinnyNX;  // gate in columns 0..15, up in 16..31
+  static constexpr int kTmemCols = 2 * kAccStride < 32 ? 32 : 2 * kAccStride;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -89,11 +98,25 @@ __device__ __forceinline__ void skinny_store(const SkinnyParams& p, int b, int n
   }
 }
 
-template <int STAGES>
+// Writes silu(g) * u (BF16, nearest even) for the M rows of output column n.
+__device__ __forceinline__ void skinny_store_gate_up(const SkinnyParams& p, int n,
+                                                     const float (&g)[16], const float (&u)[16]) {
+  if (n >= p.N) return;
+  uint16_t* y = static_cast<uint16_t*>(p.C);
+#pragma unroll
+  for (int m = 0; m < kSkinnyNX; ++m)
+    if (m < p.M)
+      y[static_cast<long long>(m) * p.ldc + n] =
+          static_cast<uint16_t>(pack_bf16x2(silu_f32(g[m]) * u[m], 0.0f) & 0xFFFFu);
+}
+
+// tmW2: Wu (GATE only; tmW is then Wg).
+template <int STAGES, bool GATE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW,
+                       const __grid_constant__ CUtensorMap tmW2,
                        const __grid_constant__ CUtensorMap tmX, const SkinnyParams p) {
-  using Cfg = SkinnyCfg<STAGES>;
+  using Cfg = SkinnyCfg<STAGES, GATE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -125,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmW);
+    if constexpr (GATE) prefetch_tensormap(&tmW2);
     prefetch_tensormap(&tmX);
   }
   if (warp == 1) {
@@ -171,7 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);
             tma_load_3d_hint(w_dst, &tmW, full_bar(s), kb * kBK, nb * kSkinnyRows, bt,
                              stream_policy);
-            tma_load_3d_hint(w_dst + Cfg::kWBytes, &tmX, full_bar(s), kb * kBK, 0, bt,
+            if constexpr (GATE)
+              tma_load_3d_hint(w_dst + Cfg::kWBytes, &tmW2, full_bar(s), kb * kBK,
+                               nb * kSkinnyRows, bt, stream_policy);
+            tma_load_3d_hint(w_dst + Cfg::kXOffset, &tmX, full_bar(s), kb * kBK, 0, bt,
                              keep_policy);
             ++issued;
             if (++s == STAGES) {
@@ -210,11 +237,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after_sync();
           const uint32_t w_addr = sbase + s * Cfg::kStageBytes;
           const uint64_t wdesc = smem_desc_sw128(w_addr);
-          const uint64_t xdesc = smem_desc_sw128(w_addr + Cfg::kWBytes);
+          const uint64_t xdesc = smem_desc_sw128(w_addr + Cfg::kXOffset);
 #pragma unroll
-          for (int j = 0; j < kBK / kUmmaK; ++j)
+          for (int j = 0; j < kBK / kUmmaK; ++j) {
             umma_bf16(d_tmem, wdesc + 2u * j, xdesc + 2u * j, p.idesc,
                       (kb != kb0 || j != 0) ? 1u : 0u);
+            if constexpr (GATE)
+              umma_bf16(d_tmem + kSkinnyNX, smem_desc_sw128(w_addr + Cfg::kWBytes) + 2u * j,
+                        xdesc + 2u * j, p.idesc, (kb != kb0 || j != 0) ? 1u : 0u);
+          }
           umma_commit(empty_bar(s));
           if (++s == STAGES) {
             s = 0;
@@ -238,30 +269,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool got = wait_bounded(accf_bar(buf), aph, abort_flag, SITE_EPI_ACC_FULL);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
-      float acc[16];
-      if (kb1 > kb0) {
-        tmem_load_32x32b_x16(tmem_base + (static_cast<uint32_t>(band) << 16) +
-                                 static_cast<uint32_t>(buf * Cfg::kAccStride),
-                             acc);
-      } else {
+      // acc[w][m]: weight w (0: B or Wg, 1: Wu) for activation row m
+      float acc[Cfg::kWeights][16];
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(band) << 16) +
+                            static_cast<uint32_t>(buf * Cfg::kAccStride);
 #pragma unroll
-        for (int m = 0; m < 16; ++m) acc[m] = 0.0f;
+      for (int w = 0; w < Cfg::kWeights; ++w) {
+        if (kb1 > kb0) {
+          tmem_load_32x32b_x16(tacc + w * kSkinnyNX, acc[w]);
+        } else {
+#pragma unroll
+          for (int m = 0; m < 16; ++m) acc[w][m] = 0.0f;
+        }
       }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce_bar(buf));
 
       const int n = nb * kSkinnyRows + band + lane;
+      auto store = [&](const float (&v)[Cfg::kWeights][16]) {
+        if constexpr (GATE)
+          skinny_store_gate_up(p, n, v[0], v[1]);
+        else
+          skinny_store(p, bt, n, v[0]);
+      };
       if (p.splits == 1) {
-        skinny_store(p, bt, n, acc);
+        store(acc);
         continue;
       }
-      float* ws_b = p.ws + static_cast<long long>(bt) * p.splits * p.M * p.N;
+      // Partials [batch][split][weight][M][N].
+      float* ws_b = p.ws + static_cast<long long>(bt) * p.splits * Cfg::kWeights * p.M * p.N;
+      auto ws_at = [&](int sp_, int w, int m) {
+        return ws_b + ((static_cast<long long>(sp_) * Cfg::kWeights + w) * p.M + m) * p.N + n;
+      };
       // Publish this unit's partial, then count arrivals for this band.
       if (n < p.N) {
 #pragma unroll
-        for (int m = 0; m < kSkinnyNX; ++m)
-          if (m < p.M) ws_b[(static_cast<long long>(sp) * p.M + m) * p.N + n] = acc[m];
+        for (int w = 0; w < Cfg::kWeights; ++w)
+#pragma unroll
+          for (int m = 0; m < kSkinnyNX; ++m)
+            if (m < p.M) *ws_at(sp, w, m) = acc[w][m];
       }
       __threadfence();
       __syncwarp();
@@ -271,23 +318,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       prev = __shfl_sync(0xffffffffu, prev, 0);
       if (prev == p.splits - 1) {
         __threadfence();
-        float sum[16];
+        float sum[Cfg::kWeights][16];
 #pragma unroll
-        for (int m = 0; m < kSkinnyNX; ++m) sum[m] = 0.0f;
+        for (int w = 0; w < Cfg::kWeights; ++w)
+#pragma unroll
+          for (int m = 0; m < kSkinnyNX; ++m) sum[w][m] = 0.0f;
         if (n < p.N) {
           for (int s = 0; s < p.splits; ++s) {
 #pragma unroll
-            for (int m = 0; m < kSkinnyNX; ++m) {
-              if (m < p.M) {
-                const float part =
-                    (s == sp) ? acc[m]
-                              : __ldcg(ws_b + (static_cast<long long>(s) * p.M + m) * p.N + n);
-                sum[m] += part;
+            for (int w = 0; w < Cfg::kWeights; ++w) {
+#pragma unroll
+              for (int m = 0; m < kSkinnyNX; ++m) {
+                if (m < p.M) sum[w][m] += (s == sp) ? acc[w][m] : __ldcg(ws_at(s, w, m));
               }
             }
           }
         }
-        skinny_store(p, bt, n, sum);
+        store(sum);
         if (lane == 0) *counter = 0;  // ready for the next call
       }
     }

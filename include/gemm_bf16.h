@@ -330,7 +330,8 @@ GEMM_API int gemm_selftest_wait_timeout(int64_t limit_ns, void *stream);
 typedef struct gemm_plan {
     int kernel;       /* 0 none, 1 single-CTA tiled GEMM, 2 skinny split-K, 3 scale only (K == 0),
                          4 single-CTA gate/up, 5 CTA-pair tiled GEMM, 6 CTA-pair gate/up,
-                         7 small-M (64-row weight tiles, whole K, no workspace) */
+                         7 small-M (64-row weight tiles, whole K, no workspace),
+                         8 split-K gate/up (M <= 16: Wg and Wu rows streamed together) */
     int tile_m;       /* output rows per tile (tcgen05 M, or weight rows for kernels 2 and 7) */
     int tile_n;       /* output columns per tile (activation rows for kernels 2 and 7) */
     int tile_k;       /* K per pipeline stage */

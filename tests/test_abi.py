@@ -240,6 +240,22 @@ def test_plan_gate_up(lib):
     assert d["stage_tx_bytes"] == 3 * 16384
 
 
+def test_plan_gate_up_decode(lib, monkeypatch):
+    """M <= 16: Wg and Wu rows stream together through the split-K kernel."""
+    for M in (1, 16):
+        st, p = _native.gemm_gate_up_plan(M, 14336, 4096, 152)
+        d = p.as_dict()
+        assert st == 0 and d["kernel_name"] == "skinny_gate_up"
+        assert d["tile_m"] == 128 and d["tile_n"] == 16
+        assert d["stage_tx_bytes"] == 2 * 16384 + 2048      # Wg, Wu and X rows
+        assert d["tiles"] == 112 * d["split_k"] and d["grid"] == min(d["tiles"], 152)
+    st, p = _native.gemm_gate_up_plan(17, 14336, 4096, 152)
+    assert p.as_dict()["kernel_name"] == "gate_up"
+    monkeypatch.setenv("GB3_GATE_UP_SKINNY", "0")
+    st, p = _native.gemm_gate_up_plan(16, 14336, 4096, 152)
+    assert p.as_dict()["kernel_name"] == "gate_up"
+
+
 def test_selftest_rejects_out_of_range_limits(lib):
     assert _native.gemm_selftest_wait_timeout(10, 0) == _native.GEMM_ERR_INVALID_ARG
     assert _native.gemm_selftest_wait_timeout(5 * 10**9, 0) == _native.GEMM_ERR_INVALID_ARG

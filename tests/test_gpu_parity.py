@@ -208,6 +208,49 @@ def test_gate_up_ragged(g, M, N, K):
     check_gate_up(g, M, N, K, seed=M + N, dist_w=("normal", 1.0 / np.sqrt(K)))
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 296, 640), (7, 1000, 2048), (16, 1160, 4160), (16, 128, 64)])
+@pytest.mark.parametrize("splits", ["planned", "1", "3"])
+def test_gate_up_decode(g, monkeypatch, M, N, K, splits):
+    """M <= 16 on the split-K kernel: ragged weight rows, K tails, and K split
+    into pieces whose gate and up partials are summed apart before silu(g)*u."""
+    if splits != "planned":
+        monkeypatch.setenv("GB3_SKINNY_SPLITS", splits)
+    p = g.gate_up_plan(M, N, K)
+    assert p["kernel_name"] == "skinny_gate_up"
+    if splits != "planned":
+        kb = -(-K // 64)
+        assert p["split_k"] == -(-kb // -(-kb // min(int(splits), kb)))
+    check_gate_up(g, M, N, K, seed=M + N + K, dist_w=("normal", 1.0 / np.sqrt(K)))
+
+
+@pytest.mark.slow
+def test_workload_skinny_gate_up(g):
+    """Full size, every entry."""
+    w = workloads.WORKLOADS["skinny_gate_up_16x14336x4096"]
+    assert g.gate_up_plan(w.M, w.N, w.K)["kernel_name"] == "skinny_gate_up"
+    check_gate_up(g, w.M, w.N, w.K, w.seed, w.dist_b)
+
+
+def test_gate_up_decode_matches_tiled_kernel(g, monkeypatch):
+    """The decode path and the tiled gate/up kernel agree within tolerance of
+    the oracle on the same inputs, and the decode path is deterministic."""
+    M, N, K = 16, 2000, 3072
+    X, Wg, Wu = workloads.gate_up_inputs(M, N, K, 81, ("normal", 1.0), ("normal", 1.0 / 55))
+    Xd, Wgd, Wud = X.cuda(), Wg.cuda(), Wu.cuda()
+    outs = [g.gate_up_silu(Xd, Wgd, Wud) for _ in range(2)]
+    monkeypatch.setenv("GB3_GATE_UP_SKINNY", "0")
+    assert g.gate_up_plan(M, N, K)["kernel_name"] == "gate_up"
+    tiled = g.gate_up_silu(Xd, Wgd, Wud)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    rr, cc = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    res = oracle.gate_up_entries(X, Wg, Wu, rr.ravel(), cc.ravel())
+    tol = oracle.gate_up_tolerance(res)
+    for name, y in (("decode", outs[0]), ("tiled", tiled)):
+        assert_within(to_f64(y)[rr.ravel(), cc.ravel()], res["y"], tol, name)
+    assert_status_ok(g)
+
+
 @pytest.mark.slow
 def test_workload_gate_up(g):
     w = workloads.WORKLOADS["gate_up_4096x14336x4096"]

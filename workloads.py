@@ -110,6 +110,12 @@ WORKLOADS = {
         dist_a=("normal", 1.0), dist_b=("normal", 1.0 / 64.0), out_bf16=True,
         check="sampled",
         notes="Y = silu(X Wg) * (X Wu), BF16 [4096, 14336]"),
+    # The gate/up projection at a decode batch of 16: HBM-bound on Wg and Wu.
+    "skinny_gate_up_16x14336x4096": Workload(
+        "skinny_gate_up_16x14336x4096", "gate_up", 16, 14336, 4096, seed=14,
+        dist_a=("normal", 1.0), dist_b=("normal", 1.0 / 64.0), out_bf16=True,
+        check="sampled",
+        notes="Y = silu(X Wg) * (X Wu) for 16 rows, Wg and Wu 117 MB each"),
     "skinny_16x28672x8192": Workload(
         "skinny_16x28672x8192", "gemm", 16, 28672, 8192, seed=4,
         dist_a=("normal", 1.0), dist_b=("normal", 1.0 / math.sqrt(8192)),
