@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -85,10 +86,10 @@ int resident_blocks(int dev, const void* fn) {
   return blocks;
 }
 
-template <int XK, int YK, int CACHE>
+template <int XK, int YK, int CACHE, int RW = 1>
 int launch_norm(int64_t rows, int64_t D, const void* X, int64_t ldx, const float* G, float eps,
                 void* Y, int64_t ldy, cudaStream_t stream) {
-  auto kern = rms_norm_kernel<XK, YK, CACHE>;
+  auto kern = rms_norm_kernel<XK, YK, CACHE, RW>;
   int dev, sms, per_sm;
   {
     std::lock_guard<std::mutex> lk(g_norm_mu);
@@ -96,8 +97,8 @@ int launch_norm(int64_t rows, int64_t D, const void* X, int64_t ldx, const float
     if (st != GEMM_OK) return st;
     per_sm = resident_blocks(dev, reinterpret_cast<const void*>(kern));
   }
-  constexpr int kWarps = kNormThreads / 32;
-  const int64_t want = (rows + kWarps - 1) / kWarps;
+  constexpr int kGroups = kNormThreads / 32 / RW;   // rows a block works on at a time
+  const int64_t want = (rows + kGroups - 1) / kGroups;
   const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sms) * per_sm));
   kern<<<grid, kNormThreads, 0, stream>>>(X, static_cast<long long>(ldx), G, eps, Y,
                                           static_cast<long long>(ldy), static_cast<int>(rows),
@@ -106,13 +107,18 @@ int launch_norm(int64_t rows, int64_t D, const void* X, int64_t ldx, const float
   return GEMM_OK;
 }
 
-// Rows whose 16-byte vectors fit in 4 registers per lane use the small cache.
+// Rows whose 16-byte vectors fit in 4 registers per lane take one warp and
+// the small cache; longer rows take two warps of 8 cached vectors each
+// (GB3_NORM_ROW_WARPS = 1 keeps them on one warp of 16, for comparison).
 template <int XK, int YK>
 int launch_sized(int64_t rows, int64_t D, const void* X, int64_t ldx, const float* G, float eps,
                  void* Y, int64_t ldy, cudaStream_t stream) {
   const int64_t vecs_per_lane = (D * NormElems<XK>::kBytes + 32 * 16 - 1) / (32 * 16);
   if (vecs_per_lane <= 4) return launch_norm<XK, YK, 4>(rows, D, X, ldx, G, eps, Y, ldy, stream);
-  return launch_norm<XK, YK, 16>(rows, D, X, ldx, G, eps, Y, ldy, stream);
+  const char* env = std::getenv("GB3_NORM_ROW_WARPS");
+  if (env != nullptr && std::atoi(env) == 1)
+    return launch_norm<XK, YK, 16>(rows, D, X, ldx, G, eps, Y, ldy, stream);
+  return launch_norm<XK, YK, 8, 2>(rows, D, X, ldx, G, eps, Y, ldy, stream);
 }
 
 template <int XK>

@@ -5,18 +5,20 @@
 //   y(m,k) = x(m,k) * inv(m) * g(k)
 //
 // The operation reads each element once and writes it once, so it is bound by
-// HBM bandwidth, not arithmetic: one warp owns one row at a time (rows are
-// visited warp-stride over the grid), lanes read 16-byte vectors so that every
-// warp-wide load moves 512 contiguous bytes, and the first CACHE vectors of
-// each lane stay in registers between the sum of squares and the scaling pass
-// (with CACHE = 16 a BF16 row of 4096 elements is held whole; short rows use
-// CACHE = 4, fewer registers and more resident warps to keep enough loads in
-// flight).  Longer rows are read a second time, from L1/L2.
+// HBM bandwidth, not arithmetic: one warp (short rows) or two warps (long
+// rows) own one row at a time (rows are visited group-stride over the grid),
+// lanes read 16-byte vectors so that every warp-wide load moves 512
+// contiguous bytes, and the first CACHE vectors of each lane stay in registers
+// between the sum of squares and the scaling pass (two warps with CACHE = 8
+// hold a BF16 row of 4096 elements whole; short rows use one warp and
+// CACHE = 4).  Fewer registers per warp keep more warps, and so more loads,
+// in flight.  Longer rows are read a second time, from L1/L2.
 //
 // Arithmetic (FP32): each lane adds the squares of its elements in order
-// (vector v = i*32 + lane, elements of a vector in order, then the scalar tail
-// k = tail0 + lane + 32 j), the 32 lane sums are combined by a butterfly of 5
-// shuffle steps, then ss / D, + eps, sqrtf and the reciprocal are each
+// (vector v = (i*RW + sub)*32 + lane, elements of a vector in order, then the
+// scalar tail k = tail0 + lane + 32 j in the first warp), the 32 lane sums
+// are combined by a butterfly of 5 shuffle steps and the RW warp sums in
+// warp order, then ss / D, + eps, sqrtf and the reciprocal are each
 // correctly rounded; y = (x * inv) * g, rounded to the output type (nearest
 // even for BF16/FP16).
 #pragma once
@@ -122,16 +124,29 @@ __device__ __forceinline__ void store_scalar(void* base, long long idx, float y)
 // are 16-byte aligned and ldx, ldy keep every row 16-byte aligned (checked on
 // the host).  Y may be X itself (same pitch): every element is read by the
 // thread that writes it, before it writes it.
-template <int XK, int YK, int CACHE>
-__global__ void __launch_bounds__(kNormThreads)
+//
+// RW warps share a row (RW = 2 for long rows: half the registers per warp, so
+// twice the warps, and twice the bytes, in flight per SM).  Warp `sub` of a
+// row takes vectors v = (i*RW + sub)*32 + lane; the warps' sums meet in
+// shared memory (double-buffered by row parity, one named barrier per row)
+// and are added in sub order, so both warps hold the same value.
+template <int XK, int YK, int CACHE, int RW = 1>
+__global__ void __launch_bounds__(kNormThreads, RW == 2 ? 3 : 1)
     rms_norm_kernel(const void* X, long long ldx, const float* __restrict__ G, float eps, void* Y,
                     long long ldy, int rows, int D) {
+  static_assert(RW == 1 || RW == 2, "warps per row");
   constexpr int V = NormElems<XK>::kPerVec;
+  constexpr int kWarps = kNormThreads / 32;
+  constexpr int kGroups = kWarps / RW;  // rows a block works on at a time
   const int lane = threadIdx.x & 31;
-  const int warps = gridDim.x * (kNormThreads / 32);
+  const int warp = threadIdx.x >> 5;
+  const int grp = warp / RW, sub = warp % RW;
+  const int groups = gridDim.x * kGroups;
   const int nvec = D / V;          // whole vectors per row
   const int tail0 = nvec * V;      // first element of the scalar tail
-  for (int m = blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5); m < rows; m += warps) {
+  __shared__ float partial[2][kWarps];
+  int parity = 0;
+  for (int m = blockIdx.x * kGroups + grp; m < rows; m += groups, parity ^= 1) {
     const uint4* xrow = reinterpret_cast<const uint4*>(
         static_cast<const uint8_t*>(X) + static_cast<long long>(m) * ldx * NormElems<XK>::kBytes);
     uint8_t* yrow = static_cast<uint8_t*>(Y) + static_cast<long long>(m) * ldy * NormElems<YK>::kBytes;
@@ -139,36 +154,47 @@ __global__ void __launch_bounds__(kNormThreads)
     float ss = 0.0f;
 #pragma unroll
     for (int i = 0; i < CACHE; ++i) {
-      const int v = i * 32 + lane;
+      const int v = (i * RW + sub) * 32 + lane;
       if (v < nvec) cache[i] = xrow[v];
     }
 #pragma unroll
     for (int i = 0; i < CACHE; ++i) {
-      const int v = i * 32 + lane;
+      const int v = (i * RW + sub) * 32 + lane;
       if (v < nvec) ss = sum_squares<XK>(cache[i], ss);
     }
-    for (int v = CACHE * 32 + lane; v < nvec; v += 32) ss = sum_squares<XK>(xrow[v], ss);
+    for (int v = (CACHE * RW + sub) * 32 + lane; v < nvec; v += 32 * RW)
+      ss = sum_squares<XK>(xrow[v], ss);
     const void* xr = static_cast<const uint8_t*>(X) + static_cast<long long>(m) * ldx * NormElems<XK>::kBytes;
-    for (int k = tail0 + lane; k < D; k += 32) {
-      const float x = norm_scalar<XK>(xr, k);
-      ss = fmaf(x, x, ss);
+    if (sub == 0) {
+      for (int k = tail0 + lane; k < D; k += 32) {
+        const float x = norm_scalar<XK>(xr, k);
+        ss = fmaf(x, x, ss);
+      }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if constexpr (RW > 1) {
+      if (lane == 0) partial[parity][warp] = ss;
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(32 * RW) : "memory");
+      ss = 0.0f;
+#pragma unroll
+      for (int w = 0; w < RW; ++w) ss += partial[parity][grp * RW + w];
+    }
     const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + eps);
 
 #pragma unroll
     for (int i = 0; i < CACHE; ++i) {
-      const int v = i * 32 + lane;
+      const int v = (i * RW + sub) * 32 + lane;
       if (v < nvec)
         scale_store<XK, YK>(cache[i], inv, G + static_cast<long long>(v) * V,
                             yrow + static_cast<long long>(v) * V * NormElems<YK>::kBytes);
     }
-    for (int v = CACHE * 32 + lane; v < nvec; v += 32)
+    for (int v = (CACHE * RW + sub) * 32 + lane; v < nvec; v += 32 * RW)
       scale_store<XK, YK>(xrow[v], inv, G + static_cast<long long>(v) * V,
                           yrow + static_cast<long long>(v) * V * NormElems<YK>::kBytes);
-    for (int k = tail0 + lane; k < D; k += 32)
-      store_scalar<YK>(yrow, k, norm_scalar<XK>(xr, k) * inv * __ldg(G + k));
+    if (sub == 0)
+      for (int k = tail0 + lane; k < D; k += 32)
+        store_scalar<YK>(yrow, k, norm_scalar<XK>(xr, k) * inv * __ldg(G + k));
   }
 }
 
