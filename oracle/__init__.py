@@ -487,6 +487,9 @@ def rms_norm_rel_error(D: int) -> float:
     and the reciprocal each add one rounding (the root halves the error of its
     argument), and the two products two more:
     ``gamma_n / 2 + 6 u`` in all, which this bound rounds up by 1 %.
+    (When two warps share a row, each lane adds at most ``ceil(D/64) + 1``
+    terms, then 5 pairwise steps and one more addition: a shorter chain, so
+    the same bound holds.)
     """
     n = -(-int(D) // 32) + 6
     gamma = n * U32 / (1.0 - n * U32)
