@@ -222,7 +222,11 @@ def norm_case(g, rows, D, x_dtype, y_dtype, seed, ld=None, eps=1e-6, check_rows=
     (257, 3, F32, BF16, 8),          # shorter than one vector: all scalar
     (1, 20000, F32, F32, None),      # one long row, second pass from L2
 ])
-def test_rms_norm_within_tolerance(g, rows, D, xd, yd, ld):
+@pytest.mark.parametrize("row_warps", ["2", "1"])
+def test_rms_norm_within_tolerance(g, monkeypatch, rows, D, xd, yd, ld, row_warps):
+    """Long rows run on two warps per row by default; GB3_NORM_ROW_WARPS=1
+    keeps them on one (short rows always take one)."""
+    monkeypatch.setenv("GB3_NORM_ROW_WARPS", row_warps)
     norm_case(g, rows, D, xd, yd, seed=rows + D, ld=ld)
     assert_status_ok(g)
 
