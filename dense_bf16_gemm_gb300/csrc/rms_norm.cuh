@@ -131,7 +131,9 @@ __device__ __forceinline__ void store_scalar(void* base, long long idx, float y)
 // shared memory (double-buffered by row parity, one named barrier per row)
 // and are added in sub order, so both warps hold the same value.
 template <int XK, int YK, int CACHE, int RW = 1>
-__global__ void __launch_bounds__(kNormThreads, RW == 2 ? 3 : 1)
+// Resident blocks per SM the registers must allow: 4 for short rows, 2 for
+// one warp holding 16 vectors, 3 for two warps holding 8 each.
+__global__ void __launch_bounds__(kNormThreads, RW == 2 ? 3 : (CACHE <= 4 ? 4 : 2))
     rms_norm_kernel(const void* X, long long ldx, const float* __restrict__ G, float eps, void* Y,
                     long long ldy, int rows, int D) {
   static_assert(RW == 1 || RW == 2, "warps per row");
