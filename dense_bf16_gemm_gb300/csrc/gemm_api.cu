@@ -137,22 +137,67 @@ int smallm_stages(int nx) {
   }
 }
 
-// Whether an M <= 128 problem runs on the small-M kernel.  A CTA streams B
-// from HBM at about 32-37 GB/s whatever the number of busy SMs (measured on
-// GB300), so what decides is how many SMs a plan keeps streaming and for how
-// long.  Against the single-CTA tiled kernel (16 < M <= 128) the 64-row units
-// win while they fit in one wave; with more units the tiled kernel reads B
-// as fast and is kept.  For M <= 16 the split-K kernel, with its split chosen
-// by the time model of choose_split, was as fast or faster on every measured
-// shape (16x8192x8192 37.0 us against 41.0, 16x14336x4096 28.7 against 42.0).
+// Shortest share of the k-block sequence worth giving a CTA of the small-M
+// kernel when the tiles alone leave SMs idle (512 of K: below that the
+// partial sums cost about what the extra streaming SMs save).
+constexpr int64_t kSmallMinShareKb = 8;
+
+// CTAs the small-M kernel runs.  Tiles that fill at most half the SMs are
+// divided over every SM (stream-K); between half and all of the SMs each CTA
+// takes one whole tile, because the combine of shared tiles (the last piece
+// writes C after the others' partial sums) costs more there than the idle SMs
+// (measured on GB300: 64 x 14336 x 4096, 112 tiles, 28.7 us whole against 38.7
+// divided; 64 x 8192 x 8192, 64 tiles, 43.1 against 41.0).  More tiles than
+// SMs are divided over every SM.  GB3_SMALL_M_STREAM_K = 1 or 0 forces the
+// division or whole tiles (one CTA per tile, up to one per SM).
+int smallm_grid(int64_t tiles, int64_t k_blocks, int sms) {
+  const int64_t work = tiles * k_blocks;
+  const int mode = env_int("GB3_SMALL_M_STREAM_K", -1);
+  if (mode == 0 || (mode != 1 && tiles > sms / 2 && tiles <= sms))
+    return static_cast<int>(std::min<int64_t>(tiles, sms));
+  const int64_t g = std::max<int64_t>(tiles, work / kSmallMinShareKb);
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(g, sms)));
+}
+
+// The stream-K division of a small-M problem on `grid` CTAs: each CTA's share
+// of the k-block sequence and the most CTAs any one tile is shared by.
+void smallm_divide(int64_t tiles, int64_t k_blocks, int grid, SmallMParams* p) {
+  p->work = tiles * k_blocks;
+  p->work_per_cta = p->work / grid;
+  p->work_extra = static_cast<int>(p->work % grid);
+  int most = 1;
+  for (int64_t t = 0; t < tiles; ++t) {
+    const int first = smallm_cta_of(*p, t * k_blocks);
+    const int last = smallm_cta_of(*p, t * k_blocks + k_blocks - 1);
+    most = std::max(most, last - first + 1);
+  }
+  p->max_pieces = most;
+}
+
+// Partial-sum slots of the small-M kernel: one per (CTA, tile) it touches,
+// numbered CTA + tile, so at most grid + tiles - 1 of them.
+size_t smallm_workspace_bytes(int64_t grid, int64_t tiles, int64_t M) {
+  return static_cast<size_t>(grid + tiles - 1) * M * kSmallRows * sizeof(float);
+}
+
+// Whether an M <= 128 problem runs on the small-M kernel (128-row weight
+// tiles, see smallm_grid for how the work is divided).  Measured on GB300
+// against the kernel each problem would otherwise take: with tiles for at
+// most every SM it beat the single-CTA tiled kernel on every 16 < M <= 128
+// shape measured (64 x 8192 x 8192 41.0 us against 59.0, 64 x 14336 x 4096
+// 28.7 against 36.2); for M <= 16 it beat the split-K kernel while its tiles
+// fill at most half the SMs (16 x 8192 x 8192 32.8 against 37.6, 8 x 4096 x
+// 4096 18.5 against 20.5) and matched it above.  With more tiles than SMs the
+// tiled kernel (M > 16) or the split-K kernel is as fast or faster.
 // GB3_GEMM_SMALL_M = 0 or 1 forces the choice.
 bool use_small_m(int64_t batch, int64_t M, int64_t N, int64_t K, int sms) {
   (void)K;
   if (M > kSmallMMaxM) return false;
   const int force = env_int("GB3_GEMM_SMALL_M", -1);
   if (force == 0 || force == 1) return force == 1;
-  if (M <= kSkinnyMaxM) return false;
-  return batch * ceil_div(N, kSmallRows) <= sms;
+  const int64_t tiles = batch * ceil_div(N, kSmallRows);
+  if (M <= kSkinnyMaxM) return tiles <= sms / 2;
+  return tiles <= sms;
 }
 
 template <int BN>
@@ -344,9 +389,11 @@ int plan_gemm(int64_t batch, int64_t M, int64_t N, int64_t K, int sms, gemm_plan
     pl->kernel = K_SMALL_M;
     pl->tile_m = kSmallRows;
     pl->tile_n = nx;
-    pl->split_k = 1;
     pl->tiles = batch * ceil_div(N, kSmallRows);
-    pl->grid = static_cast<int>(std::min<int64_t>(pl->tiles, sms));
+    pl->grid = smallm_grid(pl->tiles, ceil_div(K, kBK), sms);
+    SmallMParams d;
+    smallm_divide(pl->tiles, ceil_div(K, kBK), pl->grid, &d);
+    pl->split_k = d.max_pieces;
     pl->stages = smallm_stages(nx);
     pl->smem_bytes = smallm_smem(nx);
     pl->launches = 1;
@@ -1216,7 +1263,8 @@ int run_smallm(const gemm_plan& pl, int dev, const Problem& q, cudaStream_t stre
   p.n_blocks = static_cast<int>(ceil_div(q.N, kSmallRows));
   p.k_blocks = static_cast<int>(ceil_div(q.K, kBK));
   p.batch = static_cast<int>(q.batch);
-  p.num_units = static_cast<int>(pl.tiles);
+  p.num_tiles = static_cast<int>(pl.tiles);
+  smallm_divide(pl.tiles, p.k_blocks, pl.grid, &p);
   p.alpha = q.alpha;
   p.beta = q.beta;
   p.C = q.C;
@@ -1224,6 +1272,16 @@ int run_smallm(const gemm_plan& pl, int dev, const Problem& q, cudaStream_t stre
   p.c_stride = q.batch > 1 ? q.sc : 0;
   p.out_kind = q.out_dtype;
   p.idesc = idesc_f32_acc(kSmallRows, nx, q.in_dtype == GEMM_IN_F16);
+  p.ws = nullptr;
+  p.counters = nullptr;
+  if (p.max_pieces > 1) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const size_t ws_bytes = smallm_workspace_bytes(pl.grid, pl.tiles, q.M);
+    const size_t counters = static_cast<size_t>(pl.tiles) * 4;
+    if ((st = ensure_workspace(dev, ws_bytes, counters, stream)) != GEMM_OK) return st;
+    p.ws = g_dev[dev].ws;
+    p.counters = g_dev[dev].counters;
+  }
   switch (nx) {
     case 16: return launch_smallm<16>(pl, dev, tmW, tmX, p, stream);
     case 32: return launch_smallm<32>(pl, dev, tmW, tmX, p, stream);
@@ -1602,10 +1660,14 @@ int gemm_prepare(int64_t max_N, void* stream) {
   if (st != GEMM_OK) return st;
   std::lock_guard<std::mutex> lk(g_mu);
   if ((st = probe_device(dev)) != GEMM_OK) return st;
-  // Largest split the planner can choose is 32.
+  // M <= 16: the largest split the planner can choose is 32.
   const int64_t nb = ceil_div(std::max<int64_t>(max_N, 1), kSkinnyRows);
-  const size_t ws_bytes = static_cast<size_t>(32) * kSkinnyMaxM * max_N * sizeof(float);
-  return ensure_workspace(dev, ws_bytes, static_cast<size_t>(nb) * 4,
+  const size_t skinny_bytes = static_cast<size_t>(32) * kSkinnyMaxM * max_N * sizeof(float);
+  // 16 < M <= 128: the small-M kernel on at most one CTA per SM.
+  const int64_t tiles = ceil_div(std::max<int64_t>(max_N, 1), kSmallRows);
+  const size_t small_bytes = smallm_workspace_bytes(g_dev[dev].sms, tiles, kSmallMMaxM);
+  return ensure_workspace(dev, std::max(skinny_bytes, small_bytes),
+                          static_cast<size_t>(std::max(nb, tiles)) * 4,
                           static_cast<cudaStream_t>(stream));
 }
 

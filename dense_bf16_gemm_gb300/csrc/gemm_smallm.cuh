@@ -1,55 +1,101 @@
-// gemm_smallm.cuh -- small-M GEMM (M <= 128) without split-K, bound by the
-// HBM stream of B.
+// gemm_smallm.cuh -- small-M GEMM (M <= 128), bound by the HBM stream of B.
 //
-// As in the swapped-operand decode kernel, C^T = B(N,K) . A(M,K)^T: the weight
-// rows fill the MMA's M side and the activation rows its N side.  Here the
-// weight tile is 64 rows (tcgen05.mma cta_group::1 with M = 64), so a weight
-// splits into twice as many units as 128-row tiles would give, and each unit
-// streams its 64 rows through the whole of K into one TMEM accumulator.  No
-// workspace, no second pass, no arrival counters: every output is written once
-// by the unit that owns it, so the call allocates nothing and is
-// deterministic by construction.
+// As in the swapped-operand decode kernel, C^T = B(N,K) . A(M,K)^T: 128 weight
+// rows fill the MMA's M side and the activation rows its N side (NX = 16, 32,
+// 64 or 128).
 //
-// Where it pays (measured on GB300): a CTA's TMA stream of B from HBM runs at
-// about 32-37 GB/s whatever the number of busy SMs, so a weight is read at full
-// speed only when every SM streams.  64-row units spread a moderate weight over
-// more SMs than 128- or 256-row tiles do without cutting K; for weights of many
-// waves the other kernels are as fast and this one is not chosen.
+// Work division (stream-K): the k-blocks of all tiles, tile after tile, form
+// one sequence that is cut into gridDim.x contiguous ranges whose lengths
+// differ by at most one.  A CTA walks its range as segments, one per tile it
+// touches, each accumulated in one TMEM accumulator.  A segment that covers a
+// whole tile is written straight to C.  A tile shared by several CTAs (its
+// "pieces", numbered in K order) has each piece's FP32 partial written to a
+// workspace slot (CTA index + tile index: both only grow along the sequence
+// and every new segment advances one of them, so no two pieces share a slot);
+// the last piece to arrive (an atomic counter per tile) adds the
+// partials in piece order 0..P-1, applies alpha/beta and writes C, so the
+// result does not depend on which CTA finishes last and no CTA waits for
+// another.
 //
-// Accumulator placement of an M = 64 MMA (measured on GB300): D row i sits in
-// TMEM lane 32*(i/16) + i%16, its columns unchanged.  So epilogue warp w (which
-// may access lanes 32*(w%4)..+31) finds weight rows 16*(w%4)..+15 in its lanes
-// 0..15; lanes 16..31 carry nothing and store nothing.
+// Why this shape (measured on GB300): a tcgen05.mma of K = 16 occupies the
+// tensor pipe for about 130 cycles whatever its M (64 or 128) and N (16 to
+// 256), so a CTA can consume at most (weight bytes per MMA) / 130 cycles of
+// B: 32 GB/s with 64-row tiles, 65 GB/s with 128-row tiles.  HBM needs about
+// 45 GB/s from each of the 152 SMs, so the tiles are 128 rows and K is cut
+// wherever the tiles alone would leave SMs idle (a 64 x 8192 x 8192 problem
+// has 64 tiles for 152 SMs).
+//
+// Accumulator: D row i (weight row i of the tile) in TMEM lane i, activation
+// row m in column m, so epilogue warp w (lanes 32*(w%4)..+31) holds weight
+// rows 32*(w%4)..+31, one per lane.
 //
 // Roles: warp 0 TMA producer, warp 1 MMA issuer and TMEM owner, warps 2-5
-// epilogue.  Two accumulators (2*NX TMEM columns) let the epilogue of one unit
-// overlap the main loop of the next.
+// epilogue.  Two accumulators (2*NX TMEM columns) let the epilogue of one
+// segment overlap the main loop of the next.
 #pragma once
 
 #include "gemm_kernels.cuh"
 
 namespace gb3 {
 
-constexpr int kSmallRows = 64;   // weight rows per unit (the MMA's M)
+constexpr int kSmallRows = 128;  // weight rows per tile (the MMA's M)
 
 struct SmallMParams {
   int M, N, K;                // sizes of each matrix of the batch
-  int n_blocks, k_blocks;     // ceil(N / 64), ceil(K / 64)
+  int n_blocks, k_blocks;     // ceil(N / 128), ceil(K / 64)
   int batch;
-  int num_units;              // batch * n_blocks
+  int num_tiles;              // batch * n_blocks
+  long long work;             // num_tiles * k_blocks: the k-block sequence
+  long long work_per_cta;     // floor(work / gridDim.x) (>= 1)
+  int work_extra;             // work % gridDim.x: CTAs 0..work_extra-1 take one more
+  int max_pieces;             // most CTAs sharing one tile (reported by the plan)
   float alpha, beta;
   void* C;
   long long ldc;
   long long c_stride;         // elements between consecutive matrices of C
   int out_kind;               // 0 FP32, 1 BF16, 2 FP16
-  uint32_t idesc;             // tcgen05 instruction descriptor (M = 64, N = NX)
+  uint32_t idesc;             // tcgen05 instruction descriptor (M = 128, N = NX)
+  float* ws;      // [gridDim.x + num_tiles - 1][M][128] FP32 partials (max_pieces > 1)
+  int* counters;  // [num_tiles][4] arrival counters, zero between calls
 };
+
+// First position of CTA c's range in the k-block sequence.
+__host__ __device__ __forceinline__ long long smallm_range_start(const SmallMParams& p, int c) {
+  return static_cast<long long>(c) * p.work_per_cta + (c < p.work_extra ? c : p.work_extra);
+}
+
+// The CTA whose range holds position x of the k-block sequence.
+__host__ __device__ __forceinline__ int smallm_cta_of(const SmallMParams& p, long long x) {
+  const long long big = static_cast<long long>(p.work_extra) * (p.work_per_cta + 1);
+  if (x < big) return static_cast<int>(x / (p.work_per_cta + 1));
+  return p.work_extra + static_cast<int>((x - big) / p.work_per_cta);
+}
+
+// One tile's share of a CTA's range: k-blocks kb0..kb1-1 of tile `tile`.
+struct SmallMSeg {
+  int tile, kb0, kb1;
+};
+
+// Walks CTA c's range: seg is the segment at `pos`; returns false past the end.
+__device__ __forceinline__ bool smallm_segment(const SmallMParams& p, long long pos,
+                                               long long end, SmallMSeg& seg) {
+  if (pos >= end) return false;
+  seg.tile = static_cast<int>(pos / p.k_blocks);
+  const long long base = static_cast<long long>(seg.tile) * p.k_blocks;
+  seg.kb0 = static_cast<int>(pos - base);
+  seg.kb1 = static_cast<int>(end - base < p.k_blocks ? end - base : p.k_blocks);
+  return true;
+}
+
+__device__ __forceinline__ long long smallm_next(const SmallMParams& p, const SmallMSeg& seg) {
+  return static_cast<long long>(seg.tile) * p.k_blocks + seg.kb1;
+}
 
 // NX: activation rows per MMA (the MMA's N), 16, 32, 64 or 128.
 template <int NX>
 struct SmallMCfg {
   static_assert(NX == 16 || NX == 32 || NX == 64 || NX == 128, "activation tile");
-  static constexpr int kWBytes = kSmallRows * kBK * 2;  // 8 KB
+  static constexpr int kWBytes = kSmallRows * kBK * 2;  // 16 KB
   static constexpr int kXBytes = NX * kBK * 2;          // 2..16 KB
   static constexpr int kStageBytes = kWBytes + kXBytes;
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
@@ -64,26 +110,129 @@ struct SmallMCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// alpha * acc + beta * c for activation rows m0..m0+kCols-1 of output column n.
+// C[m][n] of matrix b = alpha * acc + beta * C[m][n] (one rounding to a 16-bit
+// output, from the FP32 value).
+__device__ __forceinline__ void smallm_store_one(const SmallMParams& p, int b, int m, int n,
+                                                 float acc) {
+  const long long off = b * p.c_stride + static_cast<long long>(m) * p.ldc + n;
+  float v = __fmul_rn(p.alpha, acc);
+  if (p.out_kind != 0) {
+    const bool f16 = p.out_kind == 2;
+    uint16_t* c = static_cast<uint16_t*>(p.C);
+    if (p.beta != 0.0f) v = __fmaf_rn(p.beta, half16_to_float(c[off], f16), v);
+    c[off] = static_cast<uint16_t>(pack_half16x2(v, 0.0f, f16) & 0xFFFFu);
+  } else {
+    float* c = static_cast<float*>(p.C);
+    if (p.beta != 0.0f) v = __fmaf_rn(p.beta, c[off], v);
+    c[off] = v;
+  }
+}
+
+// C[m][n0..n0+3] of matrix b, the same values as four smallm_store_one calls.
+// Where all four exist and their address is aligned, one 8-byte (16-bit C) or
+// 16-byte (FP32 C) access: scattered 2-byte stores that each fill part of a
+// sector of a C not held in L2 were measured to cost about 18 us per call.
+__device__ __forceinline__ void smallm_store_four(const SmallMParams& p, int b, int m, int n0,
+                                                  float4 acc) {
+  const long long off = b * p.c_stride + static_cast<long long>(m) * p.ldc + n0;
+  const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+  if (n0 + 3 < p.N) {
+    if (p.out_kind != 0) {
+      uint16_t* c = static_cast<uint16_t*>(p.C) + off;
+      if ((reinterpret_cast<uintptr_t>(c) & 7u) == 0) {
+        const bool f16 = p.out_kind == 2;
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(p.alpha, a[i]);
+        if (p.beta != 0.0f) {
+          const uint2 old = *reinterpret_cast<const uint2*>(c);
+          v[0] = __fmaf_rn(p.beta, half16_to_float(old.x & 0xFFFFu, f16), v[0]);
+          v[1] = __fmaf_rn(p.beta, half16_to_float(old.x >> 16, f16), v[1]);
+          v[2] = __fmaf_rn(p.beta, half16_to_float(old.y & 0xFFFFu, f16), v[2]);
+          v[3] = __fmaf_rn(p.beta, half16_to_float(old.y >> 16, f16), v[3]);
+        }
+        *reinterpret_cast<uint2*>(c) =
+            make_uint2(pack_half16x2(v[0], v[1], f16), pack_half16x2(v[2], v[3], f16));
+        return;
+      }
+    } else {
+      float* c = static_cast<float*>(p.C) + off;
+      if ((reinterpret_cast<uintptr_t>(c) & 15u) == 0) {
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(p.alpha, a[i]);
+        if (p.beta != 0.0f) {
+          const float4 old = *reinterpret_cast<const float4*>(c);
+          v[0] = __fmaf_rn(p.beta, old.x, v[0]);
+          v[1] = __fmaf_rn(p.beta, old.y, v[1]);
+          v[2] = __fmaf_rn(p.beta, old.z, v[2]);
+          v[3] = __fmaf_rn(p.beta, old.w, v[3]);
+        }
+        *reinterpret_cast<float4*>(c) = make_float4(v[0], v[1], v[2], v[3]);
+        return;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (n0 + i < p.N) smallm_store_one(p, b, m, n0 + i, a[i]);
+}
+
+// Activation rows m0..m0+kCols-1 of output column n.
 template <int kCols>
 __device__ __forceinline__ void smallm_store(const SmallMParams& p, int b, int n, int m0,
                                              const float* acc) {
   if (n >= p.N) return;
 #pragma unroll
-  for (int i = 0; i < kCols; ++i) {
-    const int m = m0 + i;
-    if (m < p.M) {
-      const long long off = b * p.c_stride + static_cast<long long>(m) * p.ldc + n;
-      float v = __fmul_rn(p.alpha, acc[i]);
-      if (p.out_kind != 0) {
-        const bool f16 = p.out_kind == 2;
-        uint16_t* c = static_cast<uint16_t*>(p.C);
-        if (p.beta != 0.0f) v = __fmaf_rn(p.beta, half16_to_float(c[off], f16), v);
-        c[off] = static_cast<uint16_t>(pack_half16x2(v, 0.0f, f16) & 0xFFFFu);
-      } else {
-        float* c = static_cast<float*>(p.C);
-        if (p.beta != 0.0f) v = __fmaf_rn(p.beta, c[off], v);
-        c[off] = v;
+  for (int i = 0; i < kCols; ++i)
+    if (m0 + i < p.M) smallm_store_one(p, b, m0 + i, n, acc[i]);
+}
+
+// The combine of a shared tile by the 128 epilogue threads (tid 0..127): the
+// partials of pieces 0..pieces-1 (slot first + pc + tile, laid out [M][128])
+// are added in piece order and written to C.  16 threads cover one row of the
+// tile (8 consecutive outputs each), so every C row segment is written whole
+// and at once: per-warp 32-column slices written at different times were
+// measured to make the final stores of the call several times slower.  Each
+// thread issues the loads of 4 rows of a piece before adding them.
+__device__ __forceinline__ void smallm_combine_tile(const SmallMParams& p, int bt, int tile,
+                                                    int nb, int first, int pieces, int tid) {
+  const int cn = (tid & 15) * 8;  // first of 8 weight rows within the tile
+  const int n0 = nb * kSmallRows + cn;
+#pragma unroll 1
+  for (int m0 = tid >> 4; m0 < p.M; m0 += 32) {
+    float4 sum[4][2];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sum[k][0] = sum[k][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 1
+    for (int pc = 0; pc < pieces; ++pc) {
+      const float* base =
+          p.ws + (static_cast<long long>(first + pc) + tile) * p.M * kSmallRows + cn;
+      float4 v[4][2];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int m = m0 + 8 * k;
+        const float4* src = reinterpret_cast<const float4*>(base + static_cast<long long>(m) * kSmallRows);
+        const bool in = m < p.M;
+        v[k][0] = in ? __ldcg(src) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        v[k][1] = in ? __ldcg(src + 1) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          sum[k][h].x += v[k][h].x;
+          sum[k][h].y += v[k][h].y;
+          sum[k][h].z += v[k][h].z;
+          sum[k][h].w += v[k][h].w;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int m = m0 + 8 * k;
+      if (m < p.M) {
+        smallm_store_four(p, bt, m, n0, sum[k][0]);
+        smallm_store_four(p, bt, m, n0 + 4, sum[k][1]);
       }
     }
   }
@@ -136,6 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_holder;
+  // This CTA's range of the k-block sequence (every segment is non-empty).
+  const long long range0 = smallm_range_start(p, blockIdx.x);
+  const long long range1 = smallm_range_start(p, blockIdx.x + 1);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -145,9 +297,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       long long issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        const int bt = u / p.n_blocks, nb = u - bt * p.n_blocks;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+      SmallMSeg seg;
+      for (long long pos = range0; ok && smallm_segment(p, pos, range1, seg);
+           pos = smallm_next(p, seg)) {
+        const int bt = seg.tile / p.n_blocks, nb = seg.tile - bt * p.n_blocks;
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
           if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY)) {
             ok = false;
             break;
@@ -175,13 +329,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       int local = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++local) {
+      SmallMSeg seg;
+      for (long long pos = range0; ok && smallm_segment(p, pos, range1, seg);
+           pos = smallm_next(p, seg), ++local) {
         const int buf = local & 1;
         const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
         if (!wait_bounded(acce_bar(buf), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
           if (!wait_bounded(full_bar(s), ph, abort_flag, SITE_MMA_FULL)) {
             ok = false;
             break;
@@ -193,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < kBK / kUmmaK; ++j)
             umma_bf16(d_tmem, wdesc + 2u * j, xdesc + 2u * j, p.idesc,
-                      (kb != 0 || j != 0) ? 1u : 0u);
+                      (kb != seg.kb0 || j != 0) ? 1u : 0u);
           umma_commit(empty_bar(s));
           if (++s == STAGES) {
             s = 0;
@@ -208,18 +364,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_bounded(drain_bar, 0, nullptr, SITE_DRAIN);
     }
   } else {
-    const int quarter = warp & 3;
+    const int quarter = warp & 3;  // TMEM lanes (weight rows) 32*quarter..+31
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
     constexpr int kGroup = NX < 64 ? NX : 64;  // columns held in registers at once
+    const int col = 32 * quarter + lane;  // weight row within the tile
+    const int tid = static_cast<int>(threadIdx.x) - 64;  // 0..127 over the epilogue warps
+    __shared__ int arrivals_before;  // pieces of the current tile that arrived before this one
     int local = 0;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++local) {
-      const int bt = u / p.n_blocks, nb = u - bt * p.n_blocks;
+    SmallMSeg seg;
+    for (long long pos = range0; smallm_segment(p, pos, range1, seg);
+         pos = smallm_next(p, seg), ++local) {
+      const int bt = seg.tile / p.n_blocks, nb = seg.tile - bt * p.n_blocks;
       const int buf = local & 1;
       const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
       const bool got = wait_bounded(accf_bar(buf), aph, abort_flag, SITE_EPI_ACC_FULL);
-      if (!__all_sync(0xffffffffu, got)) break;
+      // All four epilogue warps leave together (they meet at named barriers below).
+      if (!named_barrier_and(1, 128, got)) break;
       tc_fence_after_sync();
-      const int n = nb * kSmallRows + 16 * quarter + lane;
+      const int n = nb * kSmallRows + col;
+      // A tile shared by several CTAs: its pieces are the CTAs whose ranges
+      // hold its first to its last k-block, in K order.
+      const bool whole = seg.kb0 == 0 && seg.kb1 == p.k_blocks;
+      int first = static_cast<int>(blockIdx.x), pieces = 1;
+      if (!whole) {
+        const long long tile_pos = static_cast<long long>(seg.tile) * p.k_blocks;
+        first = smallm_cta_of(p, tile_pos);
+        pieces = smallm_cta_of(p, tile_pos + p.k_blocks - 1) - first + 1;
+      }
+      const int piece = static_cast<int>(blockIdx.x) - first;
+      // Piece pc of this tile in slot first + pc + tile.
+      auto ws_at = [&](int pc, int m) {
+        return p.ws + ((static_cast<long long>(first + pc) + seg.tile) * p.M + m) * kSmallRows +
+               col;
+      };
       const uint32_t tacc = tmem_base + lane_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
 #pragma unroll 1
       for (int g0 = 0; g0 < NX; g0 += kGroup) {
@@ -237,8 +414,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(acce_bar(buf));
         }
-        if (lane < 16 && g0 < p.M) smallm_store<kGroup>(p, bt, n, g0, acc);
+        if (g0 < p.M) {
+          if (whole) {
+            smallm_store<kGroup>(p, bt, n, g0, acc);
+          } else if (n < p.N) {
+#pragma unroll
+            for (int i = 0; i < kGroup; ++i)
+              if (g0 + i < p.M) *ws_at(piece, g0 + i) = acc[i];
+          }
+        }
       }
+      if (whole) continue;
+      // Publish this piece (all four bands), then count it once for the tile.
+      int* counter = p.counters + seg.tile;
+      named_barrier_sync(1, 128);
+      if (tid == 0) {
+        __threadfence();
+        arrivals_before = atomicAdd(counter, 1);
+      }
+      named_barrier_sync(1, 128);
+      if (arrivals_before != pieces - 1) continue;
+      __threadfence();
+      smallm_combine_tile(p, bt, seg.tile, nb, first, pieces, tid);
+      if (tid == 0) *counter = 0;  // ready for the next call
     }
   }
 

@@ -82,13 +82,14 @@ enum gemm_in_dtype {
  *            FP32 value of alpha*acc + beta*c.
  * stream     cudaStream_t the work is enqueued on.
  *
- * Split K: for M <= 16, and for the tiles of a last, partial wave of the
+ * Split K: for M <= 16, for the small-M kernel (16 < M <= 128, tiles shared
+ * by several CTAs), and for the tiles of a last, partial wave of the
  * CTA-pair kernel, K is cut into pieces whose FP32 partial sums live in a
  * per-device workspace the library allocates on first use; the last piece
  * of each tile adds them in a fixed order, so results do not depend on
  * timing.  A call made while `stream` is being captured into a CUDA graph
- * cannot allocate: the M <= 16 path then returns GEMM_ERR_CUDA (make one such
- * call, or gemm_prepare(), before capturing) and the tiled path runs its
+ * cannot allocate: the M <= 128 paths then return GEMM_ERR_CUDA (make one
+ * such call, or gemm_prepare(), before capturing) and the tiled path runs its
  * tiles whole.  Calls that use the workspace and run concurrently on
  * different streams share it and must not overlap on the GPU.
  */
@@ -283,7 +284,7 @@ GEMM_API int gemm_get_device_status(void *stream, int *site);
 
 /*
  * Allocates, on the current device, the split-K workspace that a gemm_bf16
- * call with M <= 16 and the given N would need, so that later calls (for
+ * call with M <= 128 and N <= max_N would need, so that later calls (for
  * example inside CUDA-graph capture) allocate nothing.  Ordered on `stream`.
  */
 GEMM_API int gemm_prepare(int64_t max_N, void *stream);
@@ -330,13 +331,16 @@ GEMM_API int gemm_selftest_wait_timeout(int64_t limit_ns, void *stream);
 typedef struct gemm_plan {
     int kernel;       /* 0 none, 1 single-CTA tiled GEMM, 2 skinny split-K, 3 scale only (K == 0),
                          4 single-CTA gate/up, 5 CTA-pair tiled GEMM, 6 CTA-pair gate/up,
-                         7 small-M (64-row weight tiles, whole K, no workspace),
+                         7 small-M (64-row weight tiles; the k-blocks of all tiles
+                           divided evenly over the CTAs, shared tiles summed in
+                           the workspace),
                          8 split-K gate/up (M <= 16: Wg and Wu rows streamed together) */
     int tile_m;       /* output rows per tile (tcgen05 M, or weight rows for kernels 2 and 7) */
     int tile_n;       /* output columns per tile (activation rows for kernels 2 and 7) */
     int tile_k;       /* K per pipeline stage */
     int stages;       /* shared-memory ring depth */
-    int split_k;      /* K splits (skinny path), else 1 */
+    int split_k;      /* K splits (skinny path); most CTAs sharing one tile (small-M);
+                         else 1 */
     int64_t tiles;    /* work units (output tiles x splits) */
     int grid;         /* CTAs launched (persistent: at most one per SM) */
     int smem_bytes;   /* dynamic shared memory per CTA */
@@ -352,11 +356,15 @@ typedef struct gemm_plan {
  * fewest waves; the environment variable GB3_GEMM_PAIR_TILE_N (256 or 224)
  * forces one width, for tuning and tests.  The plan is that of beta == 0: with
  * beta != 0 the CTA-pair kernel runs one stage fewer (its shared memory holds
- * a deeper staging ring for C) unless GB3_GEMM_C_RING = 0.  M <= 16 runs on
- * the split-K kernel (K split by a time model of the weight stream).  For
- * 16 < M <= 128 the small-M kernel runs when its 64-row weight units (batch *
- * ceil(N / 64)) fit in one wave on the SMs, else the single-CTA tiled kernel.
- * GB3_GEMM_SMALL_M = 1 or 0 forces or forbids the small-M kernel.
+ * a deeper staging ring for C) unless GB3_GEMM_C_RING = 0.  M <= 128 runs on
+ * the small-M kernel when its 128-row weight tiles (batch * ceil(N / 128))
+ * number at most the SMs (16 < M) or half the SMs (M <= 16); otherwise the
+ * single-CTA tiled kernel (16 < M) or the split-K kernel (M <= 16, K split by
+ * a time model of the weight stream).  The small-M kernel divides the
+ * k-blocks of all tiles over every SM when its tiles fill at most half of
+ * them (or exceed them), unless that gives a CTA fewer than 8 k-blocks; else
+ * one CTA per tile.  GB3_GEMM_SMALL_M = 1 or 0 forces or forbids the small-M
+ * kernel; GB3_SMALL_M_STREAM_K = 1 or 0 forces the division or whole tiles.
  */
 GEMM_API int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int num_sms,
                    gemm_plan *plan);

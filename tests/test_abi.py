@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 from dense_bf16_gemm_gb300 import _native, build
@@ -355,7 +356,8 @@ def test_row_stats_plans():
 
 
 # ---------------------------------------------------------------------------
-# The small-M kernel: 64-row weight units over the whole of K, no workspace
+# The small-M kernel: 64-row weight tiles, k-block sequence divided evenly
+# over the CTAs (stream-K)
 # ---------------------------------------------------------------------------
 def plan(M, N, K, batch=1, sms=152):
     st, p = _native.gemm_batched_plan(batch, M, N, K, 0, BF16, sms)
@@ -364,18 +366,20 @@ def plan(M, N, K, batch=1, sms=152):
 
 
 def test_plan_small_m_routing(lib):
-    # 16 < M <= 128: 64-row units that fit in one wave take the small-M kernel
-    assert plan(64, 4096, 4096)["kernel_name"] == "small_m"          # 64 units
-    assert plan(96, 8192, 8192)["kernel_name"] == "small_m"          # 128 units
-    assert plan(17, 9728, 4096)["kernel_name"] == "small_m"          # 152 units: one wave
-    assert plan(17, 9792, 4096)["kernel_name"] == "tiled"            # 153 units
-    assert plan(128, 14336, 4096)["kernel_name"] == "tiled"          # 224 units, M > 16
-    # M <= 16: the split-K kernel
-    assert plan(16, 8192, 8192)["kernel_name"] == "skinny_splitk"
-    assert plan(1, 4096, 4096)["kernel_name"] == "skinny_splitk"
-    assert plan(4, 14336, 8192)["kernel_name"] == "skinny_splitk"
-    assert plan(64, 28672, 8192)["kernel_name"] == "tiled"           # 448 units
-    assert plan(16, 28672, 8192)["kernel_name"] == "skinny_splitk"   # 448 units
+    # 16 < M <= 128: 128-row weight tiles for at most every SM take the small-M kernel
+    assert plan(64, 4096, 4096)["kernel_name"] == "small_m"          # 32 tiles
+    assert plan(96, 8192, 8192)["kernel_name"] == "small_m"          # 64 tiles
+    assert plan(128, 14336, 4096)["kernel_name"] == "small_m"        # 112 tiles
+    assert plan(17, 19456, 4096)["kernel_name"] == "small_m"         # 152 tiles: one each
+    assert plan(17, 19584, 4096)["kernel_name"] == "tiled"           # 153 tiles
+    assert plan(64, 28672, 8192)["kernel_name"] == "tiled"           # 224 tiles
+    # M <= 16: the small-M kernel while its tiles fill at most half the SMs
+    assert plan(16, 8192, 8192)["kernel_name"] == "small_m"          # 64 tiles
+    assert plan(1, 4096, 4096)["kernel_name"] == "small_m"           # 32 tiles
+    assert plan(16, 9728, 4096)["kernel_name"] == "small_m"          # 76 tiles
+    assert plan(16, 9856, 4096)["kernel_name"] == "skinny_splitk"    # 77 tiles
+    assert plan(4, 14336, 8192)["kernel_name"] == "skinny_splitk"    # 112 tiles
+    assert plan(16, 28672, 8192)["kernel_name"] == "skinny_splitk"   # 224 tiles
     assert plan(300, 4096, 4096)["kernel_name"] == "pair"            # M > 128
     import workloads
     w = workloads.WORKLOADS["smallm_64x8192x8192"]
@@ -385,10 +389,12 @@ def test_plan_small_m_routing(lib):
 def test_plan_small_m_decode_shape(lib, monkeypatch):
     monkeypatch.setenv("GB3_GEMM_SMALL_M", "1")
     d = plan(64, 28672, 8192)
-    assert d["kernel_name"] == "small_m" and d["split_k"] == 1
-    assert d["tile_m"] == 64 and d["tile_n"] == 64
-    assert d["tiles"] == 28672 // 64 and d["grid"] == 152
-    assert d["stage_tx_bytes"] == 64 * 64 * 2 + 64 * 64 * 2
+    # 224 tiles of 128 k-blocks on 152 CTAs: each CTA takes 188 or 189
+    # k-blocks, so no tile is shared by more than two CTAs
+    assert d["kernel_name"] == "small_m" and d["split_k"] == 2
+    assert d["tile_m"] == 128 and d["tile_n"] == 64
+    assert d["tiles"] == 28672 // 128 and d["grid"] == 152
+    assert d["stage_tx_bytes"] == 128 * 64 * 2 + 64 * 64 * 2
     assert d["stages"] == 200 * 1024 // d["stage_tx_bytes"]
     assert d["smem_bytes"] <= 232448
 
@@ -399,7 +405,55 @@ def test_plan_small_m_activation_tile(lib, monkeypatch, M, nx):
     monkeypatch.setenv("GB3_GEMM_SMALL_M", "1")
     d = plan(M, 5000, 1000, batch=3)
     assert d["kernel_name"] == "small_m" and d["tile_n"] == nx
-    assert d["tiles"] == 3 * -(-5000 // 64)
+    assert d["tiles"] == 3 * -(-5000 // 128)
+
+
+def _most_ctas_per_tile(tiles, k_blocks, grid):
+    """Brute force: cut tiles * k_blocks positions into `grid` contiguous ranges
+    whose lengths differ by at most one (the longer ones first) and count, for
+    every tile, the ranges its positions fall in."""
+    work = tiles * k_blocks
+    owner = np.empty(work, dtype=np.int64)
+    q, r = divmod(work, grid)
+    pos = 0
+    for c in range(grid):
+        n = q + (1 if c < r else 0)
+        owner[pos:pos + n] = c
+        pos += n
+    assert pos == work
+    return max(len(set(owner[t * k_blocks:(t + 1) * k_blocks])) for t in range(tiles))
+
+
+@pytest.mark.parametrize("batch,M,N,K,grid", [
+    (1, 64, 8192, 8192, 152),    # 64 tiles x 128 k-blocks: divided over every SM
+    (1, 64, 4096, 4096, 152),    # 32 tiles x 64
+    (1, 16, 1000, 4096, 64),     # 8 tiles x 64: shares of 8 k-blocks
+    (1, 128, 640, 1024, 10),     # 5 tiles x 16
+    (3, 40, 200, 2048, 24),      # batched: ranges cross from one matrix to the next
+    (1, 40, 1800, 8008, 152),    # ragged K
+    (1, 33, 520, 200, 5),        # 4 k-blocks: one CTA per tile
+    (1, 64, 9728, 4096, 152),    # 76 tiles: half the SMs, still divided
+    (1, 64, 14336, 4096, 112),   # 112 tiles: one whole tile per CTA
+    (1, 64, 28672, 8192, 152),   # 224 tiles: more than the SMs, divided
+])
+def test_plan_small_m_stream_k_division(lib, monkeypatch, batch, M, N, K, grid):
+    monkeypatch.setenv("GB3_GEMM_SMALL_M", "1")
+    d = plan(M, N, K, batch=batch)
+    tiles, kb = batch * -(-N // 128), -(-K // 64)
+    assert d["kernel_name"] == "small_m" and d["tiles"] == tiles
+    assert d["grid"] == grid
+    assert d["split_k"] == _most_ctas_per_tile(tiles, kb, grid)
+
+
+def test_plan_small_m_stream_k_switch(lib, monkeypatch):
+    monkeypatch.setenv("GB3_GEMM_SMALL_M", "1")
+    assert plan(64, 8192, 8192)["split_k"] > 1
+    monkeypatch.setenv("GB3_SMALL_M_STREAM_K", "0")
+    d = plan(64, 8192, 8192)
+    assert d["grid"] == 64 and d["split_k"] == 1      # one CTA per whole tile
+    monkeypatch.setenv("GB3_SMALL_M_STREAM_K", "1")
+    d = plan(64, 14336, 4096)
+    assert d["grid"] == 152 and d["split_k"] > 1      # divided although 112 tiles
 
 
 def test_plan_small_m_limits(lib, monkeypatch):

@@ -140,8 +140,8 @@ WORKLOADS = {
         "smallm_64x8192x8192", "gemm", 64, 8192, 8192, seed=11,
         dist_a=("normal", 1.0), dist_b=("normal", 1.0 / math.sqrt(8192)),
         out_bf16=True, check="sampled",
-        notes="decode batch of 64 through an 8192 x 8192 projection (134 MB), one wave "
-              "of 64-row units"),
+        notes="decode batch of 64 through an 8192 x 8192 projection (134 MB): 64 weight "
+              "tiles of 128 rows, their k-blocks divided over every SM"),
     # Softmax attention (the flash-attention loop).
     "attention_32x4096x4096x128": Workload(
         "attention_32x4096x4096x128", "attention", 4096, 4096, 128, seed=12,
