@@ -1279,7 +1279,7 @@ int run_smallm(const gemm_plan& pl, int dev, const Problem& q, cudaStream_t stre
   if (p.max_pieces > 1) {
     std::lock_guard<std::mutex> lk(g_mu);
     const size_t ws_bytes = smallm_workspace_bytes(pl.grid, pl.tiles, q.M);
-    const size_t counters = static_cast<size_t>(pl.tiles) * 4;
+    const size_t counters = static_cast<size_t>(pl.tiles);
     if ((st = ensure_workspace(dev, ws_bytes, counters, stream)) != GEMM_OK) return st;
     p.ws = g_dev[dev].ws;
     p.counters = g_dev[dev].counters;
@@ -1669,7 +1669,7 @@ int gemm_prepare(int64_t max_N, void* stream) {
   const int64_t tiles = ceil_div(std::max<int64_t>(max_N, 1), kSmallRows);
   const size_t small_bytes = smallm_workspace_bytes(g_dev[dev].sms, tiles, kSmallMMaxM);
   return ensure_workspace(dev, std::max(skinny_bytes, small_bytes),
-                          static_cast<size_t>(std::max(nb, tiles)) * 4,
+                          static_cast<size_t>(std::max(nb * 4, tiles)),
                           static_cast<cudaStream_t>(stream));
 }
 

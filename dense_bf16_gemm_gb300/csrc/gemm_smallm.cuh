@@ -56,7 +56,7 @@ struct SmallMParams {
   int out_kind;               // 0 FP32, 1 BF16, 2 FP16
   uint32_t idesc;             // tcgen05 instruction descriptor (M = 128, N = NX)
   float* ws;      // [gridDim.x + num_tiles - 1][M][128] FP32 partials (max_pieces > 1)
-  int* counters;  // [num_tiles][4] arrival counters, zero between calls
+  int* counters;  // [num_tiles] arrival counters (pieces of a tile), zero between calls
 };
 
 // First position of CTA c's range in the k-block sequence.
