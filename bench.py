@@ -42,12 +42,18 @@ FLUSH_BYTES = 256 << 20
 # (summarised under profiles/), valid only for the sources the kernel is compiled from
 # (`src_sha` over `PAIR_KERNEL_SOURCES`) and for the plan it ran with.
 PAIR_KERNEL_SOURCES = ("ptx.cuh", "gemm_kernels.cuh", "gemm_kernels_pair.cuh")
+SMALLM_KERNEL_SOURCES = ("ptx.cuh", "gemm_kernels.cuh", "gemm_smallm.cuh")
 NCU_TRAFFIC: dict = {
-    # profiles/gemm_pair_bf16_4096.md: 75.98 MB read + 30.52 MB written per launch
-    "gemm_4096_bf16": {"bytes": 106498048, "sources": PAIR_KERNEL_SOURCES,
-                       "src_sha": "3114f2627f9d8afb",
+    # profiles/gemm_pair_bf16_4096.md: 75.86 MB read + 29.53 MB written per launch
+    "gemm_4096_bf16": {"bytes": 105387776, "sources": PAIR_KERNEL_SOURCES,
+                       "src_sha": "2cd5f8f0cc429dbf",
                        "plan": {"kernel_name": "pair", "tile_n": 256, "split_k": 2,
                                 "tiles": 284, "stages": 6}},
+    # profiles/gemm_smallm_64x8192x8192.md: 135.49 MB read + 3.29 MB written per launch
+    "smallm_64x8192x8192": {"bytes": 138783744, "sources": SMALLM_KERNEL_SOURCES,
+                            "src_sha": "dfaa1f9a932d4d10",
+                            "plan": {"kernel_name": "small_m", "tile_n": 64, "split_k": 4,
+                                     "tiles": 64, "stages": 8}},
 }
 
 
