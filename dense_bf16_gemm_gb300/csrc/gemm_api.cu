@@ -1665,8 +1665,10 @@ int gemm_prepare(int64_t max_N, void* stream) {
   // M <= 16: the largest split the planner can choose is 32.
   const int64_t nb = ceil_div(std::max<int64_t>(max_N, 1), kSkinnyRows);
   const size_t skinny_bytes = static_cast<size_t>(32) * kSkinnyMaxM * max_N * sizeof(float);
-  // 16 < M <= 128: the small-M kernel on at most one CTA per SM.
-  const int64_t tiles = ceil_div(std::max<int64_t>(max_N, 1), kSmallRows);
+  // 16 < M <= 128: the small-M kernel, which the planner picks only while its
+  // tiles number at most the SMs, on at most one CTA per SM.
+  const int64_t tiles =
+      std::min<int64_t>(ceil_div(std::max<int64_t>(max_N, 1), kSmallRows), g_dev[dev].sms);
   const size_t small_bytes = smallm_workspace_bytes(g_dev[dev].sms, tiles, kSmallMMaxM);
   return ensure_workspace(dev, std::max(skinny_bytes, small_bytes),
                           static_cast<size_t>(std::max(nb * 4, tiles)),

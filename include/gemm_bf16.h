@@ -284,7 +284,8 @@ GEMM_API int gemm_get_device_status(void *stream, int *site);
 
 /*
  * Allocates, on the current device, the split-K workspace that a gemm_bf16
- * call with M <= 128 and N <= max_N would need, so that later calls (for
+ * call with M <= 128 and N <= max_N would need as planned (the GB3_* tuning
+ * variables can force plans that need more), so that later calls (for
  * example inside CUDA-graph capture) allocate nothing.  Ordered on `stream`.
  */
 GEMM_API int gemm_prepare(int64_t max_N, void *stream);
