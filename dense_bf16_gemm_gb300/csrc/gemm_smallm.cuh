@@ -188,6 +188,27 @@ __device__ __forceinline__ void smallm_store(const SmallMParams& p, int b, int n
     if (m0 + i < p.M) smallm_store_one(p, b, m0 + i, n, acc[i]);
 }
 
+// Reads tile nb's rows of C (matrix b) once, by the 128 epilogue threads, so
+// that they sit in L2 when the combine writes them at the end of the call:
+// measured on GB300 after an L2 flush, 64 x 4096 x 4096 22.6 us with this
+// against 24.6 without.  Only whole 16-byte pieces inside the row are read;
+// the values are not used.
+__device__ __forceinline__ void smallm_touch_c(const SmallMParams& p, int b, int nb, int tid) {
+  const int es = p.out_kind != 0 ? 2 : 4;
+  const int per_row = kSmallRows * es / 16;  // 16-byte pieces per tile row
+  const char* base = static_cast<const char*>(p.C);
+  for (int idx = tid; idx < p.M * per_row; idx += 128) {
+    const int m = idx / per_row, piece = idx - m * per_row;
+    const long long n = static_cast<long long>(nb) * kSmallRows + piece * (16 / es);
+    if (n + 16 / es > p.N) continue;
+    const char* a = base + (b * p.c_stride + static_cast<long long>(m) * p.ldc + n) * es;
+    uint32_t x, y, z, w;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(x), "=r"(y), "=r"(z), "=r"(w)
+                 : "l"(a));
+  }
+}
+
 // The combine of a shared tile by the 128 epilogue threads (tid 0..127): the
 // partials of pieces 0..pieces-1 (slot first + pc + tile, laid out [M][128])
 // are added in piece order and written to C.  16 threads cover one row of the
@@ -377,6 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bt = seg.tile / p.n_blocks, nb = seg.tile - bt * p.n_blocks;
       const int buf = local & 1;
       const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
+      // The last segment of a range is a tile's first piece, which almost
+      // always arrives last and combines: fetch that tile's C while it runs.
+      if (!(seg.kb0 == 0 && seg.kb1 == p.k_blocks) && smallm_next(p, seg) >= range1)
+        smallm_touch_c(p, bt, nb, tid);
       const bool got = wait_bounded(accf_bar(buf), aph, abort_flag, SITE_EPI_ACC_FULL);
       // All four epilogue warps leave together (they meet at named barriers below).
       if (!named_barrier_and(1, 128, got)) break;
