@@ -281,7 +281,53 @@ struct PairChoice {
   int64_t full = 0;      // tiles run whole
   int split = 1;         // K pieces per tail tile
   int kb_per_piece = 0;
+  // Balanced division (see TileParams): every cluster takes one contiguous
+  // range of the tiles' k-blocks; `units` counts the (tile, range) units and
+  // `max_pieces` the most ranges any tile falls in.
+  bool balanced = false;
+  int64_t per = 0;       // k-blocks per cluster (floor)
+  int extra = 0;         // clusters 0..extra-1 take one more
+  int64_t units = 0;
+  int max_pieces = 1;
+  int64_t unit_count() const { return balanced ? units : full + (tiles - full) * split; }
 };
+
+// The balanced division of `tiles` pair tiles of `k_blocks` k-blocks over
+// `slots` clusters.
+void plan_balanced(int64_t tiles, int64_t k_blocks, int slots, PairChoice* c) {
+  c->tiles = tiles;
+  c->full = tiles;
+  c->split = 1;
+  c->kb_per_piece = static_cast<int>(k_blocks);
+  c->balanced = true;
+  const int64_t work = tiles * k_blocks;
+  c->per = work / slots;
+  c->extra = static_cast<int>(work % slots);
+  c->units = 0;
+  c->max_pieces = 1;
+  for (int k = 0; k < slots; ++k) {
+    const int n = balanced_units(c->per, c->extra, static_cast<int>(k_blocks), k);
+    c->units += n;
+    for (int i = 0; i < std::min(n, 2); ++i)
+      c->max_pieces = std::max(
+          c->max_pieces, balanced_unit(c->per, c->extra, static_cast<int>(k_blocks), k, i).pieces);
+  }
+}
+
+// Whether the balanced division is used: only when GB3_GEMM_BALANCED = 1
+// (then wherever it applies: every cluster gets at least one tile's worth of
+// k-blocks); the tests' forced split of every tile (GB3_GEMM_SPLIT_ALL)
+// turns it off.  It is not chosen by default because it measured slower on
+// GB300 than the tail split: 4096^3 1519 against 1667 TFLOP/s, 3000 x 5000 x
+// 2000 66.3 against 56.9 us, gate/up 4096 x 14336 x 4096 718 against 509 us.
+// The last piece of a cut tile sums the partials while the next main loop
+// streams its operands, and its loads from L2 queue behind that stream: a
+// combining epilogue took 13-22 us against 3-6 us for a whole tile, and with
+// up to two cut tiles per cluster, placed first, both accumulators wait.
+int balanced_mode() {
+  if (env_int("GB3_GEMM_SPLIT_ALL", 0) > 1) return 0;
+  return env_int("GB3_GEMM_BALANCED", 0) == 1 ? 1 : 0;
+}
 
 // Tail split of `tiles` pair tiles on `slots` resident pairs: the last,
 // partial wave's tiles are cut along K so that their pieces fill the pairs.
@@ -309,9 +355,37 @@ void plan_tail(int64_t tiles, int64_t k_blocks, int slots, bool allow_split, Pai
   c->split = static_cast<int>(ceil_div(k_blocks, kbp));
 }
 
-// Tile width of the CTA-pair GEMM and its tail split: the fewest waves of
-// pair tiles (a split tail wave counts 1/split of a wave plus a charge for its
-// partial sums) weighted by the time a wave of that width takes.
+// Waves of pair tiles a division takes on `slots` pairs: a split tail wave
+// counts 1/split of a wave, the balanced division its longest range in
+// tiles; either adds a charge for its partial sums.
+double pair_waves(const PairChoice& c, int64_t k_blocks, int slots) {
+  if (c.balanced) {
+    const double w = static_cast<double>(ceil_div(c.tiles * k_blocks, slots)) / k_blocks;
+    return w + (c.max_pieces > 1 ? kSplitCharge : 0.0);
+  }
+  double waves = static_cast<double>(c.full / slots);
+  const int64_t left = c.tiles - (c.full / slots) * slots;
+  if (left > 0) waves += c.split > 1 ? 1.0 / c.split + kSplitCharge : 1.0;
+  return waves;
+}
+
+// The division of `tiles` pair tiles of one width: the tail split, or the
+// balanced division where it is enabled and applies.
+PairChoice choose_pair_division(int64_t tiles, int64_t k_blocks, int slots, bool allow_split,
+                                int bn) {
+  PairChoice c;
+  c.bn = bn;
+  plan_tail(tiles, k_blocks, slots, allow_split, &c);
+  const int mode = balanced_mode();
+  if (!allow_split || mode == 0 || tiles < slots) return c;
+  PairChoice b;
+  b.bn = bn;
+  plan_balanced(tiles, k_blocks, slots, &b);
+  return b;
+}
+
+// Tile width of the CTA-pair GEMM and its division: the fewest waves of pair
+// tiles weighted by the time a wave of that width takes.
 PairChoice choose_pair(int64_t batch, int64_t M, int64_t N, int64_t K, int slots,
                        bool allow_split) {
   PairChoice best;
@@ -325,15 +399,10 @@ PairChoice choose_pair(int64_t batch, int64_t M, int64_t N, int64_t K, int slots
   for (int bn : kPairWidths) forced_valid |= (bn == forced);
   for (int bn : kPairWidths) {
     if (forced_valid && bn != forced) continue;
-    PairChoice c;
-    c.bn = bn;
-    plan_tail(batch * mb * ceil_div(N, bn), kb, slots, allow_split, &c);
-    double waves = static_cast<double>(c.full / slots);
-    const int64_t left = c.tiles - (c.full / slots) * slots;
-    if (left > 0) waves += c.split > 1 ? 1.0 / c.split + kSplitCharge : 1.0;
+    PairChoice c = choose_pair_division(batch * mb * ceil_div(N, bn), kb, slots, allow_split, bn);
     // Measured on GB300 (8192^3): a wave of 256-wide pair tiles takes 1.057x
     // the time of 224-wide ones for 1.143x the work, i.e. time ~ width + 320.
-    const double cost = waves * static_cast<double>(bn + kWidthCostOffset);
+    const double cost = pair_waves(c, kb, slots) * static_cast<double>(bn + kWidthCostOffset);
     if (cost < best_cost) {
       best_cost = cost;
       best = c;
@@ -342,9 +411,21 @@ PairChoice choose_pair(int64_t batch, int64_t M, int64_t N, int64_t K, int slots
   return best;
 }
 
-int64_t pair_workspace_bytes(const PairChoice& c) {
+// Partial sums of a division: one 256 x bn FP32 tile per piece of a split
+// tail tile, or per slot of the balanced division (two per cluster).
+int64_t pair_workspace_bytes(const PairChoice& c, int slots) {
+  if (c.balanced) return c.max_pieces > 1 ? 2LL * slots * kPairBM * c.bn * 4 : 0;
   if (c.split <= 1) return 0;
   return (c.tiles - c.full) * c.split * static_cast<int64_t>(kPairBM) * c.bn * 4;
+}
+
+// Arrival counters of a division (8 bands of 32 rows per split tile): per
+// tail tile, or per cluster of the balanced division (a split tile's counter
+// belongs to the cluster holding its second piece).
+int64_t pair_counter_count(const PairChoice& c, int slots) {
+  if (c.balanced) return c.max_pieces > 1 ? 8LL * (slots + 1) : 0;
+  if (c.split <= 1) return 0;
+  return 8 * (c.tiles - c.full);
 }
 
 // pair_slots: CTA pairs that fit on the device at once (0: assume sms / 2,
@@ -406,12 +487,12 @@ int plan_gemm(int64_t batch, int64_t M, int64_t N, int64_t K, int sms, gemm_plan
   if (M >= kPairMinM && pair_slots >= 0) {
     const int slots = pair_slots > 0 ? pair_slots : std::max(1, sms / 2);
     const PairChoice c = choose_pair(batch, M, N, K, slots, allow_split);
-    const int64_t units = c.full + (c.tiles - c.full) * c.split;
+    const int64_t units = c.unit_count();
     pl->kernel = K_PAIR;
     pl->tile_m = kPairBM;
     pl->tile_n = c.bn;
     pl->stages = kPairStages;
-    pl->split_k = c.split;
+    pl->split_k = c.balanced ? c.max_pieces : c.split;
     pl->tiles = units;
     pl->grid = 2 * static_cast<int>(std::min<int64_t>(units, slots));
     pl->smem_bytes = pair_smem_for(c.bn);
@@ -445,17 +526,16 @@ int plan_gate_up(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pa
   }
   if (M >= kPairMinM && pair_slots >= 0) {
     const int slots = pair_slots > 0 ? pair_slots : std::max(1, sms / 2);
-    PairChoice c;
-    c.bn = 256;
-    plan_tail(ceil_div(M, kPairBM) * ceil_div(N, CfgPairGU::kOutCols), ceil_div(K, kBK), slots,
-              allow_split, &c);
-    const int64_t units = c.full + (c.tiles - c.full) * c.split;
+    const PairChoice c =
+        choose_pair_division(ceil_div(M, kPairBM) * ceil_div(N, CfgPairGU::kOutCols),
+                             ceil_div(K, kBK), slots, allow_split, 256);
+    const int64_t units = c.unit_count();
     pl->kernel = K_PAIR_GATE_UP;
     pl->tile_m = kPairBM;
     pl->tile_n = CfgPairGU::kOutCols;
     pl->tile_k = kBK;
     pl->stages = kPairStages;
-    pl->split_k = c.split;
+    pl->split_k = c.balanced ? c.max_pieces : c.split;
     pl->tiles = units;
     pl->grid = 2 * static_cast<int>(std::min<int64_t>(units, slots));
     pl->smem_bytes = CfgPairGU::kSmemBytes;
@@ -991,6 +1071,9 @@ TileParams tile_params(const Problem& q, int tile_m, int tile_n_out, uint32_t id
   p.tail_split = 1;
   p.kb_per_piece = p.k_blocks;
   p.num_units = p.num_tiles;
+  p.balanced = 0;
+  p.work_per_cluster = 0;
+  p.work_extra = 0;
   p.ws = nullptr;
   p.counters = nullptr;
   return p;
@@ -1003,15 +1086,14 @@ void pair_units(int dev, gemm_plan* pl, const Problem& q, int out_cols, TilePara
                 cudaStream_t stream, bool gate_up, int slots) {
   PairChoice c;
   if (gate_up) {
-    c.bn = 256;
-    plan_tail(p->num_tiles, p->k_blocks, slots, true, &c);
+    c = choose_pair_division(p->num_tiles, p->k_blocks, slots, true, 256);
   } else {
     c = choose_pair(q.batch, q.M, q.N, q.K, slots, true);
   }
   (void)out_cols;
-  if (c.split > 1) {
-    const size_t ws = static_cast<size_t>(pair_workspace_bytes(c));
-    const size_t counters = static_cast<size_t>(c.tiles - c.full) * 8;
+  if (pair_workspace_bytes(c, slots) > 0) {
+    const size_t ws = static_cast<size_t>(pair_workspace_bytes(c, slots));
+    const size_t counters = static_cast<size_t>(pair_counter_count(c, slots));
     int st;
     {
       std::lock_guard<std::mutex> lk(g_mu);
@@ -1022,6 +1104,7 @@ void pair_units(int dev, gemm_plan* pl, const Problem& q, int out_cols, TilePara
       }
     }
     if (st != GEMM_OK) {
+      c.balanced = false;
       c.full = c.tiles;
       c.split = 1;
       c.kb_per_piece = p->k_blocks;
@@ -1033,7 +1116,10 @@ void pair_units(int dev, gemm_plan* pl, const Problem& q, int out_cols, TilePara
   p->num_full = static_cast<int>(c.full);
   p->tail_split = c.split;
   p->kb_per_piece = c.kb_per_piece;
-  p->num_units = static_cast<int>(c.full + (c.tiles - c.full) * c.split);
+  p->num_units = static_cast<int>(c.unit_count());
+  p->balanced = c.balanced ? 1 : 0;
+  p->work_per_cluster = c.per;
+  p->work_extra = c.extra;
 }
 
 // RING: C is read through the deeper staging ring (beta != 0), which takes

@@ -137,8 +137,24 @@ struct TileParams {
   int tail_split;
   int kb_per_piece;
   int num_units;
-  float* ws;          // FP32 partial tiles of the tail pieces (tail_split > 1)
-  int* counters;      // arrivals per (tail tile, 32-row band), zero between calls
+  // Balanced division (CTA-pair kernels, balanced != 0): the k-blocks of all
+  // tiles, tile after tile, form one sequence of num_tiles * k_blocks
+  // positions cut into one contiguous range per cluster, the ranges differing
+  // in length by at most one (cluster c starts at c * work_per_cluster +
+  // min(c, work_extra)).  A tile whose k-blocks fall in several ranges is
+  // summed from its pieces (one per range, numbered in K order) by the
+  // piece that arrives last.  The tail-split fields above are then unused.
+  int balanced;
+  long long work_per_cluster;
+  int work_extra;
+  float* ws;          // FP32 partial tiles of split pieces
+  int* counters;      // arrivals per (split tile, 32-row band), zero between calls
+};
+
+// One unit of a cluster's work: k-blocks kb0..kb1-1 of tile `tile`, piece
+// `piece` of `pieces` (pieces == 1: the whole tile, piece 0).
+struct WorkUnit {
+  int tile, kb0, kb1, piece, pieces;
 };
 
 // Reductions along each row of the result (kernels instantiated with STATS):
@@ -173,17 +189,131 @@ __device__ __forceinline__ void unit_of(int u, const TileParams& p, int& tile, i
   }
 }
 
+// First position of cluster c's range in the balanced division.
+__host__ __device__ __forceinline__ long long balanced_start(long long per, int extra, int c) {
+  return static_cast<long long>(c) * per + (c < extra ? c : extra);
+}
+
+// The cluster whose balanced range holds position x.
+__host__ __device__ __forceinline__ int balanced_owner(long long per, int extra, long long x) {
+  const long long big = static_cast<long long>(extra) * (per + 1);
+  if (x < big) return static_cast<int>(x / (per + 1));
+  return extra + static_cast<int>((x - big) / per);
+}
+
+// The tiles a balanced range [r0, r1) touches: first and last tile, and
+// whether the range holds only part of each.
+struct BalancedRange {
+  int t_first, t_last;
+  bool first_part, last_part;  // last_part is false when t_last == t_first
+};
+
+__host__ __device__ __forceinline__ BalancedRange balanced_range(long long r0, long long r1,
+                                                                 int k_blocks) {
+  BalancedRange b;
+  b.t_first = static_cast<int>(r0 / k_blocks);
+  b.t_last = static_cast<int>((r1 - 1) / k_blocks);
+  const long long f0 = static_cast<long long>(b.t_first) * k_blocks;
+  b.first_part = r0 != f0 || r1 < f0 + k_blocks;
+  b.last_part = b.t_last != b.t_first && r1 != static_cast<long long>(b.t_last + 1) * k_blocks;
+  return b;
+}
+
+// Units of cluster c under the balanced division: the partial tiles of its
+// range first, the shorter one first (so that their partial-sum epilogues
+// overlap later main loops, and the first one's epilogue the longer second
+// main loop), then its whole tiles in order.
+__host__ __device__ __forceinline__ int balanced_units(long long per, int extra, int k_blocks,
+                                                       int c) {
+  const long long r0 = balanced_start(per, extra, c), r1 = balanced_start(per, extra, c + 1);
+  if (r1 <= r0) return 0;
+  const BalancedRange b = balanced_range(r0, r1, k_blocks);
+  return b.t_last - b.t_first + 1;
+}
+
+__host__ __device__ __forceinline__ WorkUnit balanced_unit(long long per, int extra, int k_blocks,
+                                                           int c, int i) {
+  const long long r0 = balanced_start(per, extra, c), r1 = balanced_start(per, extra, c + 1);
+  const BalancedRange b = balanced_range(r0, r1, k_blocks);
+  const int parts = (b.first_part ? 1 : 0) + (b.last_part ? 1 : 0);
+  int t;
+  if (parts == 2) {
+    // k-blocks of the first tile's piece and of the last tile's piece
+    const long long len_first = static_cast<long long>(b.t_first + 1) * k_blocks - r0;
+    const long long len_last = r1 - static_cast<long long>(b.t_last) * k_blocks;
+    const bool last_first = len_last < len_first;
+    if (i == 0) t = last_first ? b.t_last : b.t_first;
+    else if (i == 1) t = last_first ? b.t_first : b.t_last;
+    else t = b.t_first + 1 + (i - 2);
+  } else if (i < parts)
+    t = b.first_part ? b.t_first : b.t_last;
+  else
+    t = b.t_first + (b.first_part ? 1 : 0) + (i - parts);
+  const long long f0 = static_cast<long long>(t) * k_blocks;
+  WorkUnit u;
+  u.tile = t;
+  u.kb0 = static_cast<int>((r0 > f0 ? r0 : f0) - f0);
+  u.kb1 = static_cast<int>((r1 < f0 + k_blocks ? r1 : f0 + k_blocks) - f0);
+  const int c0 = balanced_owner(per, extra, f0);
+  u.piece = c - c0;
+  u.pieces = balanced_owner(per, extra, f0 + k_blocks - 1) - c0 + 1;
+  return u;
+}
+
+// Partial-sum slot of piece q of tile t under the balanced division: every
+// cluster has at most two partial tiles, the one its range starts in (slot
+// 2c) and the one it ends in (slot 2c + 1).  Pieces q >= 1 start their
+// cluster's range; piece 0 does only when the tile starts its range.
+__host__ __device__ __forceinline__ long long balanced_slot(long long per, int extra, int k_blocks,
+                                                            int t, int q) {
+  const long long f0 = static_cast<long long>(t) * k_blocks;
+  const int c0 = balanced_owner(per, extra, f0);
+  if (q > 0) return 2LL * (c0 + q);
+  return 2LL * c0 + (balanced_start(per, extra, c0) == f0 ? 0 : 1);
+}
+
+// Arrival counters (eight, one per 32-row band) of split tile t under the
+// balanced division: those of the cluster holding its piece 1, whose range
+// starts inside t (every range starts in one tile).
+__host__ __device__ __forceinline__ int balanced_counter(long long per, int extra, int k_blocks,
+                                                         int t) {
+  return balanced_owner(per, extra, static_cast<long long>(t) * k_blocks) + 1;
+}
+
+// Units of cluster `cluster` (of `nclusters`) and the i-th of them: the
+// balanced division, or the round-robin order of the tail-split units.
+__device__ __forceinline__ int cluster_unit_count(const TileParams& p, int cluster, int nclusters) {
+  if (p.balanced) return balanced_units(p.work_per_cluster, p.work_extra, p.k_blocks, cluster);
+  return cluster < p.num_units ? (p.num_units - 1 - cluster) / nclusters + 1 : 0;
+}
+
+__device__ __forceinline__ WorkUnit cluster_unit(const TileParams& p, int cluster, int nclusters,
+                                                 int i) {
+  if (p.balanced) return balanced_unit(p.work_per_cluster, p.work_extra, p.k_blocks, cluster, i);
+  WorkUnit u;
+  unit_of(cluster + i * nclusters, p, u.tile, u.kb0, u.kb1, u.piece);
+  u.pieces = u.piece < 0 ? 1 : p.tail_split;
+  if (u.piece < 0) u.piece = 0;
+  return u;
+}
+
 // Where one warp band (32 rows) of a split tile keeps its partial sums.  The
 // layout is private to the kernel and chosen for coalescing: 32-column slice
 // c of the band is stored as 8 runs of 32 float4, run q holding lane i's
 // q-th float4 at position i, so every warp-wide store or load of a run moves
-// 512 contiguous bytes.  A band's partial is 32 * width floats.
+// 512 contiguous bytes.  A band's partial is 32 * width floats.  Piece 0's
+// partial is at ws0, piece q >= 1's at ws1 + (q - 1) * rest_stride.
 struct SplitCtx {
   int pieces;              // 1: the unit is a whole tile
   int piece;               // this unit's piece
   const float4* ws0;       // band partial of piece 0
-  long long piece_stride;  // float4s between the partials of consecutive pieces
+  const float4* ws1;       // band partial of piece 1
+  long long rest_stride;   // float4s between the partials of pieces q and q + 1 (q >= 1)
 };
+
+__device__ __forceinline__ const float4* piece_partial(const SplitCtx& sp, int q) {
+  return q == 0 ? sp.ws0 : sp.ws1 + (q - 1) * sp.rest_stride;
+}
 
 __device__ __forceinline__ long long split_index(int col, int q, int lane) {
   return (static_cast<long long>(col >> 5) * 8 + q) * 32 + lane;
@@ -294,7 +424,7 @@ __device__ __forceinline__ void acc_slice(float (&v)[32], uint32_t tacc, int col
     for (int h = 0; h < 2; ++h) {
       const int q = q0 + h;
       if (q < sp.pieces && q != sp.piece) {
-        const float4* src = sp.ws0 + q * sp.piece_stride;
+        const float4* src = piece_partial(sp, q);
 #pragma unroll
         for (int j = 0; j < 8; ++j) x[h][j] = __ldcg(src + split_index(col, j, lane));
       }
@@ -327,7 +457,7 @@ __device__ __forceinline__ void acc_slice(float (&v)[32], uint32_t tacc, int col
 // the band's last arrival (the caller then runs the epilogue on the sum).
 __device__ __forceinline__ bool publish_partial(uint32_t tacc, int acc_cols, int lane,
                                                 const SplitCtx& sp, int* counter, int pieces) {
-  float4* dst = const_cast<float4*>(sp.ws0) + sp.piece * sp.piece_stride;
+  float4* dst = const_cast<float4*>(piece_partial(sp, sp.piece));
 #pragma unroll 1
   for (int c = 0; c < acc_cols; c += 32) {
     float v[32];
@@ -347,6 +477,64 @@ __device__ __forceinline__ bool publish_partial(uint32_t tacc, int acc_cols, int
     if (lane == 0) *counter = 0;  // ready for the next call
   }
   return last;
+}
+
+// The last piece of a split tile (publish_partial returned true) adds the
+// other pieces' partials into its own accumulator in TMEM, in piece order
+// 0, 1, ... with its own partial taken from TMEM -- the same FP32 additions,
+// in the same order, as acc_slice -- so that the tile's epilogue then runs
+// as for a whole tile.  With two pieces the workspace loads run kAhead
+// 32-column slices ahead of the additions, so that several L2 round trips
+// overlap instead of one per slice.
+template <int ACC_COLS>
+__device__ __forceinline__ void combine_into_tmem(uint32_t tacc, int lane, const SplitCtx& sp) {
+  static_assert(ACC_COLS % 32 == 0, "whole slices");
+  constexpr int kSlices = ACC_COLS / 32;
+  if (sp.pieces == 2) {
+    constexpr int kAhead = 2;
+    const float4* src = piece_partial(sp, 1 - sp.piece);
+    float4 buf[kAhead][8];
+#pragma unroll
+    for (int s = 0; s < kAhead && s < kSlices; ++s)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) buf[s][j] = __ldcg(src + split_index(32 * s, j, lane));
+#pragma unroll
+    for (int s = 0; s < kSlices; ++s) {
+      float4 cur[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) cur[j] = buf[s % kAhead][j];
+      if (s + kAhead < kSlices) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          buf[s % kAhead][j] = __ldcg(src + split_index(32 * (s + kAhead), j, lane));
+      }
+      float v[32];
+      tmem_load_32x32b_x32(tacc + 32 * s, v);
+      uint32_t r[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float o[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float mine = v[4 * j + e];
+          // 0 + p0 + p1, as acc_slice adds them
+          const float sum = sp.piece == 0 ? (0.0f + mine) + o[e] : (0.0f + o[e]) + mine;
+          r[4 * j + e] = __float_as_uint(sum);
+        }
+      }
+      tmem_store_32x32b_x32(tacc + 32 * s, r);
+    }
+  } else {
+#pragma unroll 1
+    for (int s = 0; s < kSlices; ++s) {
+      float v[32];
+      acc_slice(v, tacc, 32 * s, lane, sp);
+      uint32_t r[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+      tmem_store_32x32b_x32(tacc + 32 * s, r);
+    }
+  }
 }
 
 // Running reductions of one lane's row over the columns an epilogue visits.
@@ -573,21 +761,32 @@ __device__ __forceinline__ bool epilogue_tile_ring(const TileParams& p, const CU
   constexpr int kSub = Box::kCols / 32;
   RowAcc racc;
   row_acc_init(racc);
+  // ON_DEMAND: the tile's boxes inside C (a prefix of its columns) take ring
+  // positions r0, r0 + 1, ...; their loads run kRingAhead boxes ahead of the
+  // one computed, starting once every earlier store has read its slot.
+  const long long r0 = r;
+  const int nbox = (m0 < p.M && n0 < p.N)
+                       ? (min(BN, p.N - n0) + Box::kCols - 1) / Box::kCols
+                       : 0;
+  auto load_box = [&](int j) {  // lane 0: box j of this tile into its slot
+    const int sl = static_cast<int>((r0 + j) % kRingSlots);
+    mbar_arrive_expect_tx(cbar0 + 8u * sl, 32 * Box::kRowBytes);
+    tma_load_3d(ring + sl * kStageBox, tmOut, cbar0 + 8u * sl, n0 + j * Box::kCols, m0, b);
+  };
+  if constexpr (ON_DEMAND) {
+    const int first = min(nbox, kRingAhead + 1);
+    if (lane == 0 && first > 0) {
+      bulk_wait_group_read<0>();
+      for (int j = 0; j < first; ++j) load_box(j);
+    }
+    issued = r0 + first;
+  }
 #pragma unroll 1
   for (int c0 = 0; c0 < BN; c0 += Box::kCols) {
     if (m0 >= p.M || n0 + c0 >= p.N) continue;
     const int slot = static_cast<int>(r % kRingSlots);
     const uint32_t stg = ring + slot * kStageBox;
-    if constexpr (ON_DEMAND) {
-      if (lane == 0) {
-        bulk_wait_group_read<kRingSlots - 1>();  // the slot's previous store has read it
-        mbar_arrive_expect_tx(cbar0 + 8u * slot, 32 * Box::kRowBytes);
-        tma_load_3d(stg, tmOut, cbar0 + 8u * slot, n0 + c0, m0, b);
-      }
-      issued = r + 1;
-    } else {
-      topup(r);
-    }
+    if constexpr (!ON_DEMAND) topup(r);
     const bool got = wait_bounded(cbar0 + 8u * slot, static_cast<uint32_t>((r / kRingSlots) & 1),
                                   abort_flag, SITE_EPI_C_FULL);
     if (!__all_sync(0xffffffffu, got)) return false;
@@ -644,6 +843,18 @@ __device__ __forceinline__ bool epilogue_tile_ring(const TileParams& p, const CU
     if (lane == 0) {
       tma_store_3d(tmOut, stg, n0 + c0, m0, b);
       bulk_commit_group();
+    }
+    if constexpr (ON_DEMAND) {
+      // The next box's slot was last stored from kRingSlots - kRingAhead - 1
+      // boxes before this one's store.
+      const int next = static_cast<int>(r - r0) + kRingAhead + 1;
+      if (next < nbox) {
+        if (lane == 0) {
+          bulk_wait_group_read<kRingSlots - 1 - kRingAhead>();
+          load_box(next);
+        }
+        issued = r0 + next + 1;
+      }
     }
     ++r;
     ++sc;
@@ -833,7 +1044,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             static_cast<uint32_t>(buf * Cfg::kAccStride);
       const int m0 = mb * kBM + band;
       const int n0 = nb * Cfg::kOutCols;
-      const SplitCtx whole{1, 0, nullptr, 0};
+      const SplitCtx whole{1, 0, nullptr, nullptr, 0};
       epilogue_tile<BN, EPI, STATS>(p, &tmOut, tacc, bt, m0, n0, staging, lane, sc,
                                     p.k_blocks > 0, whole, rs);
       // The accumulator may be overwritten once every lane's TMEM reads are done.

@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs, 1: its peer
   const int cluster = static_cast<int>(cluster_id_x());
   const int nclusters = static_cast<int>(num_clusters_x());
+  const int nunits = cluster_unit_count(p, cluster, nclusters);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -117,13 +118,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       long long issued = 0;
       bool ok = true;
-      for (int u = cluster; ok && u < p.num_units; u += nclusters) {
-        int tile, kb0, kb1, piece;
-        unit_of(u, p, tile, kb0, kb1, piece);
+      for (int i = 0; ok && i < nunits; ++i) {
+        const WorkUnit un = cluster_unit(p, cluster, nclusters, i);
         int bt, mb, nb;
-        tile_coords(tile, p, bt, mb, nb);
+        tile_coords(un.tile, p, bt, mb, nb);
         const int a_row = mb * kPairBM + static_cast<int>(rank) * 128;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY)) {
             ok = false;
             break;
@@ -162,15 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       int local = 0;
       bool ok = true;
-      for (int u = cluster; ok && u < p.num_units; u += nclusters, ++local) {
-        int tile, kb0, kb1, piece;
-        unit_of(u, p, tile, kb0, kb1, piece);
+      for (int i = 0; ok && i < nunits; ++i, ++local) {
+        const WorkUnit un = cluster_unit(p, cluster, nclusters, i);
         const int buf = local & 1;
         const uint32_t aph = static_cast<uint32_t>(local >> 1) & 1u;
         if (!wait_bounded_cluster(acce_bar(buf), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (!wait_bounded(full_bar(s), ph, abort_flag, SITE_MMA_FULL)) {
             ok = false;
             break;
@@ -182,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < kBK / kUmmaK; ++j)
             umma_bf16_pair(d_tmem, adesc + 2u * j, bdesc + 2u * j, p.idesc,
-                           (kb != kb0 || j != 0) ? 1u : 0u);
+                           (kb != un.kb0 || j != 0) ? 1u : 0u);
           umma_commit_pair_multicast(empty_bar(s), 0x3);
           if (++s == STAGES) {
             s = 0;
@@ -206,32 +205,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     int sc = 0;
     // C ring (RING kernels run only with beta != 0): the load cursor walks
     // this warp's boxes of whole tiles in the order the epilogue computes
-    // them, starting at the first whole tile.  Split pieces come first in the
-    // unit order; the last piece of a split tile loads its boxes on demand.
+    // them, starting at the first whole tile.  Split pieces come first in
+    // every cluster's unit order; the last piece of a split tile loads its
+    // boxes on demand.
     bool cursor_started = false;
     const uint32_t cbar0 = drain_bar + 8u * (1 + ew * kRingSlots);
     long long r_done = 0, r_issued = 0;
-    int cu = p.num_units, cc0 = 0, cb = 0, cm0 = 0, cn0 = 0;
-    auto cursor_at = [&](int u) {
-      cu = u;
+    int cu = nunits, cc0 = 0, cb = 0, cm0 = 0, cn0 = 0;
+    auto cursor_at = [&](int i) {  // onto this cluster's unit i
+      cu = i;
       cc0 = 0;
-      if (u < p.num_units) {
-        int tile_, kb0_, kb1_, piece_, mb_, nb_;
-        unit_of(u, p, tile_, kb0_, kb1_, piece_);
-        tile_coords(tile_, p, cb, mb_, nb_);
+      if (i < nunits) {
+        const WorkUnit cun = cluster_unit(p, cluster, nclusters, i);
+        int mb_, nb_;
+        tile_coords(cun.tile, p, cb, mb_, nb_);
         cm0 = mb_ * kPairBM + static_cast<int>(rank) * 128 + band;
         cn0 = nb_ * Cfg::kOutCols;
       }
     };
     auto cursor_settle = [&]() {  // onto the next box inside C, or past the last unit
-      while (cu < p.num_units) {
+      while (cu < nunits) {
         if (cc0 < Cfg::kOutCols && cm0 < p.M && cn0 + cc0 < p.N) return;
-        cursor_at(cu + nclusters);
+        cursor_at(cu + 1);
       }
     };
     auto topup = [&](long long r_now) {
       using Box = EpiBox<EPI == EPI_GATE_UP ? EPI_BF16 : EPI, Cfg::kOutCols>;
-      while (cu < p.num_units && r_issued <= r_now + kRingAhead) {
+      while (cu < nunits && r_issued <= r_now + kRingAhead) {
         const int slot = static_cast<int>(r_issued % kRingSlots);
         if (lane == 0) {
           // The slot's previous box was stored kRingSlots boxes ago.
@@ -244,16 +244,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         cursor_settle();
       }
     };
-    for (int u = cluster; u < p.num_units; u += nclusters, ++local) {
-      int tile, kb0, kb1, piece;
-      unit_of(u, p, tile, kb0, kb1, piece);
+    for (int i = 0; i < nunits; ++i, ++local) {
+      const WorkUnit un = cluster_unit(p, cluster, nclusters, i);
       int bt, mb, nb;
-      tile_coords(tile, p, bt, mb, nb);
-      if (RING && piece < 0 && !cursor_started) {
+      tile_coords(un.tile, p, bt, mb, nb);
+      if (RING && un.pieces == 1 && !cursor_started) {
         // First whole tile: start its C loads before waiting for its accumulator.
         cursor_started = true;
         r_issued = r_done;
-        cursor_at(u);
+        cursor_at(i);
         cursor_settle();
         topup(r_done);
       }
@@ -266,26 +265,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                             static_cast<uint32_t>(buf * Cfg::kAccStride);
       const int m0 = mb * kPairBM + static_cast<int>(rank) * 128 + band;
       const int n0 = nb * Cfg::kOutCols;
-      SplitCtx split{1, 0, nullptr, 0};
+      SplitCtx split{1, 0, nullptr, nullptr, 0};
       bool store = true;
-      if (piece >= 0) {
-        // One K piece of a tail tile: publish the partial; the band's last
-        // piece adds them all up and writes C.  Workspace: [tail tile][piece]
-        // [band 0..7][32 x BN floats].
-        const int tail = tile - p.num_full;
+      if (un.pieces > 1) {
+        // One K piece of a split tile: publish the partial; the band's last
+        // piece adds them all up and writes C.  A piece's partial is 8 bands
+        // of 32 x BN floats.  Tail split: [tail tile][piece][band]; balanced
+        // division: [slot][band] with the slots of balanced_slot; arrival
+        // counters per (tail tile or tile, band).
         const long long band_f4 = 32LL * BN / 4;
-        split.pieces = p.tail_split;
-        split.piece = piece;
-        split.piece_stride = 8 * band_f4;
-        split.ws0 = reinterpret_cast<const float4*>(p.ws) +
-                    static_cast<long long>(tail) * p.tail_split * split.piece_stride +
-                    band_id * band_f4;
-        store = publish_partial(tacc, BN, lane, split, p.counters + tail * 8 + band_id,
-                                p.tail_split);
+        const long long piece_f4 = 8 * band_f4;
+        const float4* ws = reinterpret_cast<const float4*>(p.ws) + band_id * band_f4;
+        int* counter;
+        split.pieces = un.pieces;
+        split.piece = un.piece;
+        if (p.balanced) {
+          split.ws0 = ws + balanced_slot(p.work_per_cluster, p.work_extra, p.k_blocks, un.tile, 0) *
+                               piece_f4;
+          split.ws1 = ws + balanced_slot(p.work_per_cluster, p.work_extra, p.k_blocks, un.tile, 1) *
+                               piece_f4;
+          split.rest_stride = 2 * piece_f4;
+          counter = p.counters +
+                    balanced_counter(p.work_per_cluster, p.work_extra, p.k_blocks, un.tile) * 8 +
+                    band_id;
+        } else {
+          const int tail = un.tile - p.num_full;
+          split.ws0 = ws + static_cast<long long>(tail) * p.tail_split * piece_f4;
+          split.ws1 = split.ws0 + piece_f4;
+          split.rest_stride = piece_f4;
+          counter = p.counters + tail * 8 + band_id;
+        }
+        store = publish_partial(tacc, BN, lane, split, counter, un.pieces);
+        if (store) {
+          // Last piece: the sum goes into this accumulator; from here on the
+          // tile is finished like a whole one.
+          combine_into_tmem<BN>(tacc, lane, split);
+          split = SplitCtx{1, 0, nullptr, nullptr, 0};
+        }
       }
       if constexpr (RING) {
         bool ok = true;
-        if (piece < 0)
+        if (un.pieces == 1)
           ok = epilogue_tile_ring<BN, EPI, STATS, false>(p, &tmOut, tacc, bt, m0, n0, staging,
                                                          cbar0, lane, r_done, r_issued, sc, split,
                                                          rs, abort_flag, topup);
@@ -296,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
       } else {
         if (store)
-          epilogue_tile<BN, EPI, STATS>(p, &tmOut, tacc, bt, m0, n0, staging, lane, sc, kb1 > kb0,
-                                        split, rs);
+          epilogue_tile<BN, EPI, STATS>(p, &tmOut, tacc, bt, m0, n0, staging, lane, sc,
+                                        un.kb1 > un.kb0, split, rs);
       }
       tc_fence_before_sync();
       __syncwarp();

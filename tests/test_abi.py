@@ -99,9 +99,31 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
     assert st in (_native.GEMM_ERR_CUDA, _native.GEMM_ERR_UNSUPPORTED)
 
 
-def pair_model(M, N, K, slots=76, widths=(256, 224)):
+def balanced_division(tiles, kb, slots):
+    """The balanced division restated: cluster c takes positions
+    [c*per + min(c, extra), ...) of the tile-major k-block sequence.  Returns
+    (units, most pieces of one tile, k-blocks of the longest range)."""
+    work = tiles * kb
+    per, extra = divmod(work, slots)
+    starts = [c * per + min(c, extra) for c in range(slots + 1)]
+    units, owners = 0, {}
+    for c in range(slots):
+        r0, r1 = starts[c], starts[c + 1]
+        if r1 <= r0:
+            continue
+        for t in range(r0 // kb, (r1 - 1) // kb + 1):
+            units += 1
+            owners.setdefault(t, set()).add(c)
+    assert sorted(owners) == list(range(tiles))       # every tile is covered
+    return units, max(len(v) for v in owners.values()), -(-work // slots)
+
+
+def pair_model(M, N, K, slots=76, widths=(256, 224), balanced=False):
     """Restatement of the planner's rule: fewest waves (a split tail wave counts
-    1/split + 0.1) weighted by width + 320."""
+    1/split + 0.1; with the balanced division enabled, that division where it
+    applies, counting its longest range in tiles + 0.1 when a tile is cut)
+    weighted by width + 320.  Returns (width, most pieces of a tile, units,
+    balanced)."""
     best = None
     kb = -(-K // 64)
     for bn in widths:
@@ -116,10 +138,26 @@ def pair_model(M, N, K, slots=76, widths=(256, 224)):
         if split == 1:
             full = tiles
         waves = full // slots + ((1 / split + 0.1) if split > 1 else (1 if tiles - full // slots * slots else 0))
+        cand = (bn, split, full + (tiles - full) * split, False)
+        if balanced and tiles >= slots:
+            units, pieces, longest = balanced_division(tiles, kb, slots)
+            waves = longest / kb + (0.1 if pieces > 1 else 0.0)
+            cand = (bn, pieces, units, True)
         cost = waves * (bn + 320)
         if best is None or cost < best[0]:
-            best = (cost, bn, split, full + (tiles - full) * split)
+            best = (cost,) + cand
     return best[1:]
+
+
+def test_balanced_division_restatement():
+    # 3000 x 5000 x 2000 on 256-wide tiles: 240 tiles of 32 k-blocks over 76
+    # pairs, ranges of 101 or 102 k-blocks; a cut tile has two pieces
+    units, pieces, longest = balanced_division(240, 32, 76)
+    assert longest == 102 and pieces == 2 and 240 < units <= 240 + 75
+    # whole waves: ranges end on tile boundaries, nothing is cut
+    assert balanced_division(152, 10, 76) == (152, 1, 20)
+    # ranges shorter than a tile: a tile falls in several ranges
+    assert balanced_division(3, 100, 76)[1] >= 25
 
 
 def test_plan_pair_4096(lib):
@@ -146,11 +184,12 @@ def test_plan_pair_matches_wave_model(lib, M, N, K):
     st, p = _native.gemm_bf16_plan(M, N, K, _native.GEMM_OUT_F32, 152)
     d = p.as_dict()
     assert st == 0 and d["kernel_name"] == "pair"
-    bn, split, units = pair_model(M, N, K)
+    bn, split, units, _ = pair_model(M, N, K)
     assert (d["tile_n"], d["split_k"], d["tiles"]) == (bn, split, units)
 
 
-def test_plan_tail_split_pieces_are_long_enough(lib):
+def test_plan_tail_split_pieces_are_long_enough(lib, monkeypatch):
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "0")   # the tail split alone
     # K = 2048 is 32 k-blocks: two pieces would be shorter than 24 k-blocks
     st, p = _native.gemm_bf16_plan(4096, 4096, 2048, _native.GEMM_OUT_BF16, 152)
     assert st == 0 and p.split_k == 1
@@ -169,8 +208,13 @@ def test_plan_forced_pair_width(lib, monkeypatch):
 
 def test_plan_split_overrides(lib, monkeypatch):
     monkeypatch.setenv("GB3_GEMM_TAIL_SPLIT", "0")
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "0")
     st, p = _native.gemm_bf16_plan(4096, 4096, 4096, _native.GEMM_OUT_BF16, 152)
     assert st == 0 and p.split_k == 1
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "1")
+    st, p = _native.gemm_bf16_plan(4096, 4096, 4096, _native.GEMM_OUT_BF16, 152)
+    assert st == 0 and p.split_k == 2 and p.tiles == balanced_division(256, 64, 76)[0]
+    monkeypatch.delenv("GB3_GEMM_BALANCED")
     monkeypatch.delenv("GB3_GEMM_TAIL_SPLIT")
     monkeypatch.setenv("GB3_GEMM_SPLIT_ALL", "3")
     st, p = _native.gemm_bf16_plan(512, 1024, 1024, _native.GEMM_OUT_BF16, 152)
@@ -197,6 +241,23 @@ def test_plan_ragged_tiles_cover_the_output(lib):
     # units: whole tiles plus split pieces of the tail tiles; every tile is covered
     whole = tiles - (tiles % 76 if d["split_k"] > 1 else 0)
     assert d["tiles"] == whole + (tiles - whole) * d["split_k"]
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (3000, 5000, 2000), (8192, 8192, 8192),
+                                   (1000, 712, 136), (2304, 4136, 200)])
+def test_plan_balanced_division_when_enabled(lib, monkeypatch, M, N, K):
+    """GB3_GEMM_BALANCED=1: every pair takes one contiguous range of the tiles'
+    k-blocks (where there are at least as many tiles as pairs)."""
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "1")
+    st, p = _native.gemm_bf16_plan(M, N, K, _native.GEMM_OUT_F32, 152)
+    d = p.as_dict()
+    assert st == 0 and d["kernel_name"] == "pair"
+    bn, split, units, balanced = pair_model(M, N, K, balanced=True)
+    assert (d["tile_n"], d["split_k"], d["tiles"]) == (bn, split, units)
+    tiles = -(-M // 256) * -(-N // bn)
+    assert balanced == (tiles >= 76)
+    if balanced:
+        assert d["grid"] == 152
 
 
 def test_plan_skinny_split_k(lib):
@@ -239,6 +300,15 @@ def test_plan_gate_up(lib):
     d = p.as_dict()
     assert d["kernel_name"] == "gate_up" and d["tile_m"] == 128
     assert d["stage_tx_bytes"] == 3 * 16384
+
+
+def test_plan_gate_up_balanced_when_enabled(lib, monkeypatch):
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "1")
+    st, p = _native.gemm_gate_up_plan(4096, 14336, 4096, 152)
+    d = p.as_dict()
+    units, pieces, _ = balanced_division(16 * 112, 64, 76)
+    assert st == 0 and d["kernel_name"] == "pair_gate_up"
+    assert d["tiles"] == units and d["split_k"] == pieces == 2
 
 
 def test_plan_gate_up_decode(lib, monkeypatch):

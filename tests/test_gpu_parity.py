@@ -627,6 +627,7 @@ RING_SHAPES = [
 def test_c_ring_bit_exact(g, monkeypatch, width, M, N, K, out_dtype):
     monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", width)
     monkeypatch.setenv("GB3_GEMM_TAIL_SPLIT", "0")   # whole tiles: the look-ahead cursor alone
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "0")
     A, B, C = int_inputs(M, N, K, seed=M + 5 * N + K)
     Cq = C.to(out_dtype)
     ref, _ = oracle.gemm_full(A, B, alpha=2.0, beta=-0.5, C=Cq.to(torch.float32))
@@ -671,6 +672,7 @@ def test_c_ring_batched_padded(g, monkeypatch, out_dtype):
     """The third TMA coordinate (matrix of the batch) and a padded pitch of C
     on the ring's loads; padding of C untouched."""
     monkeypatch.setenv("GB3_GEMM_TAIL_SPLIT", "0")
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "0")
     batch, M, N, K = 3, 600, 1000, 136
     A, B, C = batched_int_inputs(batch, M, N, K, 72, torch.float16)
     Cq = C.to(out_dtype)
@@ -692,6 +694,7 @@ def test_c_ring_batched_padded(g, monkeypatch, out_dtype):
 def test_c_ring_with_split_tail(g, monkeypatch, out_dtype):
     """A planned split tail: the pieces' last arrivals load C on demand, then
     the whole tiles run the look-ahead cursor, in one launch."""
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "0")
     M, N, K = 2048, 2560, 3072
     p = g.plan(M, N, K, out_dtype)
     assert p["kernel_name"] == "pair" and p["split_k"] > 1
@@ -704,4 +707,107 @@ def test_c_ring_with_split_tail(g, monkeypatch, out_dtype):
         out = run_gemm(g, A, B, C=Cq, alpha=2.0, beta=-0.5, out_dtype=out_dtype)
         got = to_f64(out) if out_dtype == torch.float32 else bits(out.cpu())
         assert np.array_equal(got, want), f"ring={ring}"
+    assert_status_ok(g)
+
+
+# ---------------------------------------------------------------------------
+# Balanced division of the CTA-pair kernels: every pair takes one contiguous
+# range of the tiles' k-blocks; a tile cut by a range boundary is summed from
+# its pieces by the last one to arrive.  Integer inputs keep every partial
+# exact, so the result must equal the oracle bit for bit.
+# ---------------------------------------------------------------------------
+BALANCED_SHAPES = [
+    (2304, 4136, 200),   # 153 tiles of 256 columns: ranges of ~8 k-blocks over 4-k-block tiles
+    (4000, 3896, 72),    # 256 tiles, 2 k-blocks each: most tiles cut
+    (3000, 5000, 264),   # the ragged workload's tiles with a short K (5 k-blocks, a K tail)
+    (1300, 15000, 192),  # 6 x 59 tiles, 3 k-blocks
+]
+
+
+def split_tiles_planned(p, M, N):
+    tiles = -(-M // 256) * -(-N // p["tile_n"])
+    return p["tiles"] - tiles     # every cut tile adds one unit
+
+
+@pytest.mark.parametrize("M,N,K", BALANCED_SHAPES)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("beta", [0.0, -0.5])
+def test_balanced_division_bit_exact(g, monkeypatch, M, N, K, out_dtype, beta):
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "1")
+    p = g.plan(M, N, K, out_dtype)
+    assert p["kernel_name"] == "pair" and p["split_k"] >= 2 and split_tiles_planned(p, M, N) > 0
+    A, B, C = int_inputs(M, N, K, seed=M + N + 3 * K)
+    Cq = C.to(out_dtype) if beta != 0.0 else None
+    ref, _ = oracle.gemm_full(A, B, alpha=2.0, beta=beta,
+                              C=Cq.to(torch.float32) if Cq is not None else None)
+    want = ref if out_dtype == torch.float32 else oracle.round_to_bf16_bits(ref)
+    out = run_gemm(g, A, B, C=Cq, alpha=2.0, beta=beta, out_dtype=out_dtype)
+    got = to_f64(out) if out_dtype == torch.float32 else bits(out.cpu())
+    assert np.array_equal(got, want)
+    assert_status_ok(g)
+
+
+@pytest.mark.parametrize("width", ["256", "224"])
+def test_balanced_division_random_inputs_within_tolerance(g, monkeypatch, width):
+    """The ragged workload's shape on random inputs: the balanced division
+    (pieces summed in K order by the last arrival) and the plan without it
+    both sit within the bound, and the balanced result is identical from
+    call to call."""
+    monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", width)
+    M, N, K = 3000, 5000, 2000
+    A, B, C = workloads.gemm_inputs(M, N, K, 2, ("uniform",), ("uniform",), ("normal", 1.0))
+    Ad, Bd = A.cuda(), B.cuda()
+    outs = []
+    for mode in ("1", "1", "0"):
+        monkeypatch.setenv("GB3_GEMM_BALANCED", mode)
+        Cd = C.cuda()
+        g.gemm(Ad, Bd, Cd, alpha=0.5, beta=2.0)
+        outs.append(Cd)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    rows = np.random.default_rng(81).choice(M, 48, replace=False)
+    rr, cc = np.repeat(rows, N), np.tile(np.arange(N), rows.size)
+    ref, ab = oracle.gemm_entries(A, B, rr, cc, alpha=0.5, beta=2.0, C=C)
+    tol = oracle.gemm_tolerance(ref, ab, 0.5, 2.0, C.numpy()[rr, cc])
+    for mode, o in (("balanced", outs[0]), ("whole tiles", outs[2])):
+        assert_within(to_f64(o)[rr, cc], ref, tol, f"{mode} {width}")
+    assert_status_ok(g)
+
+
+def test_balanced_division_gate_up(g, monkeypatch):
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "1")
+    M, N, K = 1024, 2600, 320           # 4 x 21 = 84 tiles of 128 output columns
+    p = g.gate_up_plan(M, N, K)
+    assert p["kernel_name"] == "pair_gate_up" and p["split_k"] >= 2
+    check_gate_up(g, M, N, K, seed=83, dist_w=("normal", 1.0 / np.sqrt(K)))
+
+
+def test_balanced_division_batched_f16(g, monkeypatch):
+    """Ranges cross matrix boundaries of a batch: a tile's coordinates come
+    from its index alone, so a range may end in one matrix and go on in the
+    next."""
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "1")
+    batch, M, N, K = 4, 1000, 2000, 200  # 4 x 4 x 8 = 128 tiles
+    A, B, C = batched_int_inputs(batch, M, N, K, 84, torch.float16)
+    Cd = C.cuda()
+    g.gemm(A.cuda(), B.cuda(), Cd, alpha=2.0, beta=-0.5)
+    torch.cuda.synchronize()
+    for b in range(batch):
+        ref, _ = oracle.gemm_full(A[b], B[b], alpha=2.0, beta=-0.5, C=C[b])
+        assert np.array_equal(to_f64(Cd[b]), ref), b
+    assert_status_ok(g)
+
+
+def test_balanced_division_row_stats(g, monkeypatch):
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "1")
+    M, N, K = 2304, 4136, 200           # 9 x 17 = 153 tiles of 4 k-blocks
+    A, B, _ = workloads.gemm_inputs(M, N, K, 85, ("int", -2, 2), ("int", -2, 2))
+    Cd = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    Cd, rs, rmax, rmin = g.gemm_row_stats(A.cuda(), B.cuda(), Cd)
+    torch.cuda.synchronize()
+    ref = oracle.gemm_row_stats(A, B, np.arange(M))
+    assert np.array_equal(to_f64(Cd), ref["values"])
+    assert np.array_equal(to_f64(rs), ref["sum"])
+    assert np.array_equal(to_f64(rmax), ref["max"])
+    assert np.array_equal(to_f64(rmin), ref["min"])
     assert_status_ok(g)
