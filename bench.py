@@ -2,7 +2,7 @@
 """Benchmark of the GB300 BF16 GEMM library.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-others] [--no-cpu-baseline]
+                    [--workload NAME] [--shard] [--no-others] [--no-cpu-baseline]
 
 One step is one library call on the headline workload (BF16 GEMM, M=N=K=4096,
 BF16 output; other workloads with --workload).  Inputs are seeded synthetic
@@ -14,10 +14,16 @@ Prints ONE JSON line on rank 0.
 
 ``--impl reference`` times the CPU oracle (the reference arm of this
 benchmark) on a bounded sample of the same workload on the host cores.
+
+Under torchrun every rank runs its own copy of the workload (weak scaling),
+or with ``--shard`` one copy of the workload is split over the ranks by
+columns of the output (rank r computes C[:, n-slice r] from A and its rows of
+B, with no collective: strong scaling).
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -39,17 +45,17 @@ import workloads  # noqa: E402
 FLUSH_BYTES = 256 << 20
 
 # DRAM traffic per launch from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`
-# (summarised under profiles/), valid only for the sources the kernel is compiled from
-# (`src_sha` over `PAIR_KERNEL_SOURCES`) and for the plan it ran with.
+# on the named workload, valid only for the sources the kernel is compiled from
+# (`src_sha` over the kernel's source files) and for the plan it ran with.
 PAIR_KERNEL_SOURCES = ("ptx.cuh", "gemm_kernels.cuh", "gemm_kernels_pair.cuh")
 SMALLM_KERNEL_SOURCES = ("ptx.cuh", "gemm_kernels.cuh", "gemm_smallm.cuh")
 NCU_TRAFFIC: dict = {
-    # profiles/gemm_pair_bf16_4096.md: 75.86 MB read + 29.53 MB written per launch
+    # the CTA-pair kernel on 4096^3 BF16: 75.86 MB read + 29.53 MB written per launch
     "gemm_4096_bf16": {"bytes": 105387776, "sources": PAIR_KERNEL_SOURCES,
                        "src_sha": "2cd5f8f0cc429dbf",
                        "plan": {"kernel_name": "pair", "tile_n": 256, "split_k": 2,
                                 "tiles": 284, "stages": 6}},
-    # profiles/gemm_smallm_64x8192x8192.md: 135.49 MB read + 3.17 MB written per launch
+    # the small-M kernel on 64 x 8192 x 8192: 135.49 MB read + 3.17 MB written per launch
     "smallm_64x8192x8192": {"bytes": 138657792, "sources": SMALLM_KERNEL_SOURCES,
                             "src_sha": "6108b7e75a2820eb",
                             "plan": {"kernel_name": "small_m", "tile_n": 64, "split_k": 4,
@@ -200,6 +206,58 @@ def max_over_ranks(pg, x: float) -> float:
     return float(t.item())
 
 
+def sum_over_ranks(pg, x: float) -> float:
+    if pg is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.SUM)
+    return float(t.item())
+
+
+SHARD_ALIGN = 256   # the widest tile: every slice but the last is whole tiles
+
+
+def shard_bounds(N: int, world: int, rank: int, align: int = SHARD_ALIGN):
+    """Columns [n0, n1) of rank `rank` when N output columns are split over
+    `world` ranks: contiguous slices of whole `align`-column blocks, as equal
+    as the blocks allow (the last slice takes the ragged end)."""
+    blocks = -(-N // align)
+    per, extra = divmod(blocks, world)
+    b0 = rank * per + min(rank, extra)
+    b1 = b0 + per + (1 if rank < extra else 0)
+    return min(N, b0 * align), min(N, b1 * align)
+
+
+def shardable(w) -> bool:
+    """Workloads whose output columns are independent (split N, no exchange)."""
+    return w.kind in ("gemm", "gate_up") and w.batch == 1
+
+
+def shard_host_inputs(w, host, n0, n1):
+    """The slice of the workload's inputs one rank needs for columns [n0, n1):
+    all of A (or X), rows n0..n1-1 of B (or Wg, Wu), columns n0..n1-1 of C."""
+    out = {}
+    for k, v in host.items():
+        if k in ("B", "Wg", "Wu"):
+            out[k] = v[n0:n1].contiguous()
+        elif k == "C":
+            out[k] = v[:, n0:n1].contiguous()
+        else:
+            out[k] = v
+    return out
+
+
+def workload_config(w, world: int, shard: bool) -> dict:
+    """The `config` object of the JSON line, the same for both arms."""
+    return {"workload": w.name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K,
+            "in_dtype": compute_dtype(w), "out_dtype": SHORT[w.out_dtype],
+            "alpha": w.alpha, "beta": w.beta,
+            "l2": "GPU arm: flushed between steps (256 MiB write + 256 MiB read, untimed)",
+            "parallelism": (f"{world}-way split of the output columns, no collective" if shard
+                            else f"{world} independent replica(s), no collective")}
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -233,8 +291,8 @@ def out_shape(w):
     return (w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N)
 
 
-def make_device_inputs(w, dev):
-    t = {k: v.to(dev) for k, v in host_inputs(w).items()}
+def make_device_inputs(w, dev, host=None):
+    t = {k: v.to(dev) for k, v in (host if host is not None else host_inputs(w)).items()}
     if "C" not in t:
         t["C"] = torch.empty(out_shape(w), dtype=w.out_dtype, device=dev)
     if w.kind == "rmsnorm_gate_up":
@@ -314,7 +372,7 @@ def time_device(lib, w, t, steps, warmup, stream, flush, sampler=None):
     return [a.elapsed_time(b) for a, b in ev]
 
 
-def time_e2e(lib, w, steps, warmup, stream, dev):
+def time_e2e(lib, w, steps, warmup, stream, dev, host=None):
     """Public API end to end, run as a serving loop runs it: every step copies
     its inputs from pinned host memory to the device, makes the library call and
     copies its result back to pinned host memory, all inside the timed region.
@@ -322,8 +380,8 @@ def time_e2e(lib, w, steps, warmup, stream, dev):
     step i-1 computes and step i-2's result travels back on a third stream
     (two device buffer sets, each reused once its previous step's result is
     back on the host)."""
-    host = {k: v.pin_memory() for k, v in host_inputs(w).items()}
-    sets = [make_device_inputs(w, dev) for _ in range(2)]
+    host = {k: v.pin_memory() for k, v in (host if host is not None else host_inputs(w)).items()}
+    sets = [make_device_inputs(w, dev, host) for _ in range(2)]
     host_out = [torch.empty(out_shape(w), dtype=w.out_dtype).pin_memory() for _ in range(2)]
     h2d = sum(h.numel() * h.element_size() for h in host.values())
     d2h = host_out[0].numel() * host_out[0].element_size()
@@ -495,12 +553,22 @@ def run_ours(args):
     _b.build()
     import dense_bf16_gemm_gb300 as lib
     lib._native.lib()
-    w = workloads.WORKLOADS[args.workload]
+    w_full = workloads.WORKLOADS[args.workload]
+    shard = args.shard and world > 1
+    if args.shard and not shardable(w_full):
+        raise SystemExit(f"--shard splits the output columns of gemm or gate/up workloads, "
+                         f"not {w_full.name}")
+    w, host = w_full, None
+    if shard:
+        # this rank's columns of the one problem all ranks share
+        n0, n1 = shard_bounds(w_full.N, world, rank)
+        w = dataclasses.replace(w_full, N=n1 - n0)
+        host = shard_host_inputs(w_full, host_inputs(w_full), n0, n1)
     peaks = load_peaks()
     stream = torch.cuda.Stream(device=dev)
     flush = (torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=dev),
              torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=dev))
-    t = make_device_inputs(w, dev)
+    t = make_device_inputs(w, dev, host)
     pl = plan_of(lib, w)
 
     sampler = ClockSampler(local)
@@ -516,17 +584,22 @@ def run_ours(args):
         raise SystemExit(f"device status {st} at site {site}")
     ms_mean = sum(times) / len(times)
     ms_step = max_over_ranks(pg, ms_mean)
-    value, unit = metric_of(w, ms_step)
-    value *= world          # weak scaling: every rank runs its own problem
+    # weak scaling: every rank runs its own problem; shards: the ranks share one
+    value, unit = metric_of(w_full, ms_step)
+    if not shard:
+        value *= world
     src_hash = kernel_source_hash()
-    traffic = traffic_of(w, plan_of(lib, w))
+    traffic = traffic_of(w, plan_of(lib, w)) if not shard else None
     roof = roofline(w, ms_mean, peaks, traffic)
 
     e2e_steps = max(3, min(args.steps, 20))
-    e2e_ms, h2d, d2h = time_e2e(lib, w, e2e_steps, 2, stream, dev)
+    e2e_ms, h2d, d2h = time_e2e(lib, w, e2e_steps, 2, stream, dev, host)
     e2e_ms = max_over_ranks(pg, e2e_ms)
-    e2e_value, _ = metric_of(w, e2e_ms)
-    e2e_value *= world
+    e2e_value, _ = metric_of(w_full, e2e_ms)
+    if not shard:
+        e2e_value *= world
+    h2d = int(sum_over_ranks(pg, h2d))
+    d2h = int(sum_over_ranks(pg, d2h))
 
     others = {}
     if not args.no_others and rank == 0 and world == 1:
@@ -562,23 +635,19 @@ def run_ours(args):
             "ms_per_step": round(ms_step, 5),
             "ms_per_step_median": round(statistics.median(times), 5),
             "higher_is_better": True,
-            "scaling": "weak",
+            "scaling": "strong" if shard else "weak",
             "vs_baseline": None,
             "dtype": compute_dtype(w),
             "data": "synthetic (seeded torch.Generator, BF16-rounded)",
-            "config": {"workload": w.name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K,
-                       "in_dtype": compute_dtype(w),
-                       "out_dtype": SHORT[w.out_dtype], "alpha": w.alpha,
-                       "beta": w.beta, "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)",
-                       "parallelism": f"{world} independent replica(s), no collective",
-                       "plan": pl},
+            "config": workload_config(w_full, world, shard),
+            "plan": pl if not shard else dict(pl, shard_columns=[n0, n1]),
             "roofline": roof,
             "clocks": clocks,
             "e2e": {"value": round(e2e_value, 2), "unit": unit, "ms_per_step": round(e2e_ms, 4),
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,  # all ranks
                     "api": f"dense_bf16_gemm_gb300.{API[w.kind]} with pinned host copies, "
                            "consecutive steps overlapped on three streams"},
-            "gpu_launches": args.steps * pl["launches"],
+            "gpu_launches": world * args.steps * pl["launches"],   # every rank's launches
             "kernel_src_sha": src_hash,
             "cpu_baseline": cpu,
             "others": others,
@@ -591,6 +660,17 @@ def run_ours(args):
 # ---------------------------------------------------------------------------
 # reference arm: the CPU oracle
 # ---------------------------------------------------------------------------
+def reference_rows(w, cores: int) -> int:
+    """Output rows per reference step: a bounded sample of the workload that
+    keeps every core of the oracle's thread pool busy (it splits rows over its
+    threads): a whole multiple of the thread count, at least 8 rows (8192 for
+    the row normalisation, whose rows are short)."""
+    want = 8192 if w.kind == "rms_norm" else 8
+    rows = max(want, cores)
+    rows = -(-rows // cores) * cores
+    return min(w.M, rows)
+
+
 def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -599,8 +679,7 @@ def run_reference(args):
     import oracle
     w = workloads.WORKLOADS[args.workload]
     run = oracle_rows(w)
-    # output rows per step: a bounded sample of the workload
-    rows = min(w.M, 8 if w.kind != "rms_norm" else 8192)
+    rows = reference_rows(w, oracle.num_threads())
     for _ in range(args.warmup):
         run(rows)
     t0 = time.perf_counter()
@@ -617,7 +696,7 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded torch.Generator, BF16-rounded)",
-        "config": {"workload": w.name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K},
+        "config": workload_config(w, world, args.shard and world > 1),
         "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
@@ -634,6 +713,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=workloads.HEADLINE, choices=list(workloads.WORKLOADS))
+    ap.add_argument("--shard", action="store_true",
+                    help="under torchrun: split one problem's output columns over the ranks")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

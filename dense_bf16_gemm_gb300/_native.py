@@ -47,6 +47,10 @@ EXPORTED = (
     "gemm_rms_norm",
     "gemm_rmsnorm_gate_up_silu",
     "gemm_attention",
+    "gemm_layout_smem_descriptor",
+    "gemm_layout_instr_descriptor",
+    "gemm_layout_swizzle128_offset",
+    "gemm_layout_tmem_address",
 )
 
 
@@ -142,6 +146,14 @@ def lib() -> ctypes.CDLL:
             l.gemm_rmsnorm_gate_up_silu.restype = _int
             l.gemm_rmsnorm_gate_up_silu.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _f32,
                                                     _vp, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
+            l.gemm_layout_smem_descriptor.restype = ctypes.c_uint64
+            l.gemm_layout_smem_descriptor.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
+            l.gemm_layout_instr_descriptor.restype = ctypes.c_uint32
+            l.gemm_layout_instr_descriptor.argtypes = [_int, _int, _int]
+            l.gemm_layout_swizzle128_offset.restype = ctypes.c_uint32
+            l.gemm_layout_swizzle128_offset.argtypes = [_int, _int]
+            l.gemm_layout_tmem_address.restype = ctypes.c_uint32
+            l.gemm_layout_tmem_address.argtypes = [ctypes.c_uint32, _int, _int]
             l.gemm_attention.restype = _int
             l.gemm_attention.argtypes = [_i64, _i64, _i64, _i64, _f32, _vp, _i64, _i64, _vp, _i64,
                                          _i64, _vp, _i64, _i64, _vp, _i64, _i64, _int, _vp]

@@ -94,20 +94,6 @@ struct AttnCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// UMMA shared-memory descriptor of an MN-major operand in 128-byte swizzled
-// tiles as TMA writes a [rows = K][64 contiguous MN elements] box: eight-row
-// (K) groups 1024 bytes apart (SBO), consecutive 64-element MN chunks
-// `mn_chunk_bytes` apart (LBO).  Checked on GB300 against known products.
-__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t mn_chunk_bytes) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((mn_chunk_bytes >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
-  return d;
-}
-
 // 2^x by the hardware's approximate exp2 (relative error about 2^-22;
 // results below the normal range flush to zero, exp2(-inf) = 0).
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -125,6 +111,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   constexpr int VS = Cfg::kVStages;
   constexpr int kChunkBytes = 128 * 128;  // one 64-element-wide swizzled chunk of 128 rows
   constexpr int kHalfKeys = kAttnBC / 2;
+  if (!launch_smem_ok(Cfg::kSmemBytes)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -296,7 +283,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int half = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = 32 * quarter + lane;             // query row of this thread in the block
-    const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    const uint32_t lane_base = tmem_addr(0, 32 * quarter, 0);
     float* xval = reinterpret_cast<float*>(smem + Cfg::kRedOffset);
     const uint32_t xbar = xchg_bar(quarter);
     // Publishes `mine` for the partner warp in exchange round r and returns

@@ -1741,6 +1741,23 @@ int gemm_selftest_wait_timeout(int64_t limit_ns, void* stream) {
                 static_cast<unsigned long long>(limit_ns));
 }
 
+uint64_t gemm_layout_smem_descriptor(uint32_t smem_address, uint32_t mn_chunk_bytes) {
+  return mn_chunk_bytes == 0 ? smem_desc_sw128(smem_address)
+                             : smem_desc_mn_sw128(smem_address, mn_chunk_bytes);
+}
+
+uint32_t gemm_layout_instr_descriptor(int M, int N, int in_dtype) {
+  return idesc_f32_acc(M, N, in_dtype == GEMM_IN_F16);
+}
+
+uint32_t gemm_layout_swizzle128_offset(int row, int chunk) {
+  return staging_offset<true>(row, static_cast<uint32_t>(chunk));
+}
+
+uint32_t gemm_layout_tmem_address(uint32_t base, int lane, int column) {
+  return tmem_addr(base, static_cast<uint32_t>(lane), static_cast<uint32_t>(column));
+}
+
 int gemm_prepare(int64_t max_N, void* stream) {
   if (max_N < 0 || max_N > kMaxDim) return GEMM_ERR_INVALID_ARG;
   int dev;
@@ -1784,6 +1801,9 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 std::mutex g_noalloc_mu;
 unsigned char* g_noalloc_base[kMaxDevices];  // device address of the array, per device
+// Whether the split-K kernel's shared-memory attribute was set by this entry
+// point (guarded by g_mu, as ensure_smem_attr is; a fixed array rather than
+// ensure_smem_attr's list, whose growth would allocate host memory).
 bool g_noalloc_smem_set[kMaxDevices];
 
 }  // namespace
@@ -1801,11 +1821,21 @@ extern "C" int gemm_bf16_skinny_noalloc(int64_t M, int64_t N, int64_t K, float a
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int dev;
   if ((st = current_device(&dev)) != GEMM_OK) return st;
+  auto kern = gemm_skinny_kernel<kSkinnyStages>;
   int sms;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if ((st = probe_device(dev)) != GEMM_OK) return st;
     sms = g_dev[dev].sms;
+    if (!g_noalloc_smem_set[dev]) {
+      if (cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               CfgSkinny::kSmemBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+      }
+      g_noalloc_smem_set[dev] = true;
+    }
   }
   gemm_plan pl;
   if (K == 0) {
@@ -1823,7 +1853,6 @@ extern "C" int gemm_bf16_skinny_noalloc(int64_t M, int64_t N, int64_t K, float a
       p.splits > 1 ? static_cast<size_t>(p.splits) * M * N * sizeof(float) : 0;
   if (counter_bytes + partial_bytes > kNoAllocScratchBytes) return GEMM_ERR_INVALID_ARG;
 
-  auto kern = gemm_skinny_kernel<kSkinnyStages>;
   unsigned char* base = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
@@ -1836,15 +1865,6 @@ extern "C" int gemm_bf16_skinny_noalloc(int64_t M, int64_t N, int64_t K, float a
         return GEMM_ERR_CUDA;
       }
       g_noalloc_base[dev] = static_cast<unsigned char*>(addr);
-    }
-    if (!g_noalloc_smem_set[dev]) {
-      if (cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               CfgSkinny::kSmemBytes) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_CUDA;
-      }
-      g_noalloc_smem_set[dev] = true;
     }
     base = g_noalloc_base[dev];
   }

@@ -46,7 +46,8 @@ enum WaitSite : int {
   SITE_DRAIN = 5,
   SITE_SKINNY = 6,
   SITE_SELFTEST = 7,
-  SITE_EPI_C_FULL = 8
+  SITE_EPI_C_FULL = 8,
+  SITE_LAUNCH_SMEM = 9
 };
 
 // [0] status code, [1] wait site, [2] block index of the first failure.
@@ -57,6 +58,23 @@ __device__ __noinline__ void record_timeout(int site) {
     g_gemm_status[1] = site;
     g_gemm_status[2] = static_cast<int>(blockIdx.x);
   }
+}
+
+// Entry check of every kernel with a dynamic shared-memory layout: a launch
+// that gave less dynamic shared memory than the layout needs records status
+// 4 (GEMM_ERR_CUDA) at site SITE_LAUNCH_SMEM, and every thread of the grid
+// returns before touching shared memory, instead of running past the end of
+// its allocation.  Uniform over the grid, so no CTA of a cluster is left
+// waiting for a peer.
+__device__ __forceinline__ bool launch_smem_ok(uint32_t need) {
+  uint32_t have;
+  asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(have));
+  if (have >= need) return true;
+  if (threadIdx.x == 0 && atomicCAS(&g_gemm_status[0], 0, 4) == 0) {
+    g_gemm_status[1] = SITE_LAUNCH_SMEM;
+    g_gemm_status[2] = static_cast<int>(blockIdx.x);
+  }
+  return false;
 }
 
 template <bool kClusterScope = false>
@@ -617,7 +635,7 @@ struct EpiBox {
 // 64-byte rows XOR it with (row / 2) % 4 (both are the address bits 7.. folded
 // into bits 4..).  Consecutive rows then hit different banks.
 template <bool kSw128>
-__device__ __forceinline__ uint32_t staging_offset(int row, uint32_t chunk) {
+__host__ __device__ __forceinline__ uint32_t staging_offset(int row, uint32_t chunk) {
   if constexpr (kSw128)
     return static_cast<uint32_t>(row) * 128u + ((chunk ^ static_cast<uint32_t>(row & 7)) << 4);
   else
@@ -887,6 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmOut, const TileParams p,
                    const RowStatsParams rs) {
   using Cfg = GemmCfg<BN, STAGES, EPI>;
+  if (!launch_smem_ok(Cfg::kSmemBytes)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -1040,8 +1059,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool got = wait_bounded(accf_bar(buf), aph, abort_flag, SITE_EPI_ACC_FULL);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
-      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(band) << 16) +
-                            static_cast<uint32_t>(buf * Cfg::kAccStride);
+      const uint32_t tacc = tmem_addr(tmem_base, static_cast<uint32_t>(band),
+                                      static_cast<uint32_t>(buf * Cfg::kAccStride));
       const int m0 = mb * kBM + band;
       const int n0 = nb * Cfg::kOutCols;
       const SplitCtx whole{1, 0, nullptr, nullptr, 0};

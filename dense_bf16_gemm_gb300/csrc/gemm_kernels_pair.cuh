@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmOut, const TileParams p,
                      const RowStatsParams rs) {
   using Cfg = PairCfg<BN, STAGES, EPI, RING>;
+  if (!launch_smem_ok(Cfg::kSmemBytes)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -261,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool got = wait_bounded(accf_bar(buf), aph, abort_flag, SITE_EPI_ACC_FULL);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
-      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(band) << 16) +
-                            static_cast<uint32_t>(buf * Cfg::kAccStride);
+      const uint32_t tacc = tmem_addr(tmem_base, static_cast<uint32_t>(band),
+                                      static_cast<uint32_t>(buf * Cfg::kAccStride));
       const int m0 = mb * kPairBM + static_cast<int>(rank) * 128 + band;
       const int n0 = nb * Cfg::kOutCols;
       SplitCtx split{1, 0, nullptr, nullptr, 0};

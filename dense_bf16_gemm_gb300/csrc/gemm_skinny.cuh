@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmW2,
                        const __grid_constant__ CUtensorMap tmX, const SkinnyParams p) {
   using Cfg = SkinnyCfg<STAGES, GATE>;
+  if (!launch_smem_ok(Cfg::kSmemBytes)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -271,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       // acc[w][m]: weight w (0: B or Wg, 1: Wu) for activation row m
       float acc[Cfg::kWeights][16];
-      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(band) << 16) +
-                            static_cast<uint32_t>(buf * Cfg::kAccStride);
+      const uint32_t tacc = tmem_addr(tmem_base, static_cast<uint32_t>(band),
+                                      static_cast<uint32_t>(buf * Cfg::kAccStride));
 #pragma unroll
       for (int w = 0; w < Cfg::kWeights; ++w) {
         if (kb1 > kb0) {

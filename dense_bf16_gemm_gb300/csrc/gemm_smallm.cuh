@@ -265,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmX, const SmallMParams p) {
   using Cfg = SmallMCfg<NX>;
   constexpr int STAGES = Cfg::kStages;
+  if (!launch_smem_ok(Cfg::kSmemBytes)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -386,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int quarter = warp & 3;  // TMEM lanes (weight rows) 32*quarter..+31
-    const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    const uint32_t lane_base = tmem_addr(0, 32 * quarter, 0);
     constexpr int kGroup = NX < 64 ? NX : 64;  // columns held in registers at once
     const int col = 32 * quarter + lane;  // weight row within the tile
     const int tid = static_cast<int>(threadIdx.x) - 64;  // 0..127 over the epilogue warps

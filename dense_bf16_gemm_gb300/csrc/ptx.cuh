@@ -243,7 +243,7 @@ __device__ __forceinline__ void tc_fence_after_sync() {
 // >> 4 (bits 32-45: 1024 bytes between eight-row groups), descriptor version
 // 1 (bits 46-47), base offset 0 (bits 49-51: tiles are 1024-byte aligned),
 // layout type 2 = 128-byte swizzle (bits 61-63).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+__host__ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>(1) << 16;
@@ -260,6 +260,29 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_f32_acc(int M, int N, bool f16_operands) {
   return (1u << 4) | ((f16_operands ? 0u : 1u) << 7) | ((f16_operands ? 0u : 1u) << 10) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// UMMA shared-memory descriptor of an MN-major operand in 128-byte swizzled
+// tiles as TMA writes a [rows = K][64 contiguous MN elements] box: eight-row
+// (K) groups 1024 bytes apart (SBO), consecutive 64-element MN chunks
+// `mn_chunk_bytes` apart (LBO).  Checked on GB300 against known products.
+__host__ __device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr,
+                                                                uint32_t mn_chunk_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((mn_chunk_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Tensor Memory address of (lane, column) in an allocation based at `base`:
+// lane in bits 31:16, 32-bit column in bits 15:0 ("TMEM tiles and transfers",
+// section "Storage units").
+__host__ __device__ __forceinline__ constexpr uint32_t tmem_addr(uint32_t base, uint32_t lane,
+                                                                 uint32_t column) {
+  return base + (lane << 16) + column;
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T over K = 16, issued by one thread.

@@ -278,7 +278,9 @@ GEMM_API const char *gemm_status_string(int status);
  * *site when site is not NULL: 1 producer waiting for a free stage, 2 MMA
  * waiting for a full stage, 3 MMA waiting for a free accumulator, 4 epilogue
  * waiting for a full accumulator, 5 a drain before exit, 6 the split-K kernel,
- * 7 gemm_selftest_wait_timeout, 8 epilogue waiting for a box of C.
+ * 7 gemm_selftest_wait_timeout, 8 epilogue waiting for a box of C; with
+ * status GEMM_ERR_CUDA, 9 a kernel launched with less dynamic shared memory
+ * than its layout needs (it returned without touching shared memory).
  */
 GEMM_API int gemm_get_device_status(void *stream, int *site);
 
@@ -355,7 +357,11 @@ typedef struct gemm_plan {
  * host logic otherwise; returns GEMM_INVALID_ARG for invalid sizes or dtype.
  * M > 128 runs on CTA pairs (256-row tiles) with the tile width that needs the
  * fewest waves; the environment variable GB3_GEMM_PAIR_TILE_N (256 or 224)
- * forces one width, for tuning and tests.  The plan is that of beta == 0: with
+ * forces one width, for tuning and tests.  The tiles of a partial last wave
+ * are cut into 2 K pieces when that shortens the wave; GB3_GEMM_BALANCED = 1
+ * instead gives every CTA pair one contiguous range of all tiles' k-blocks
+ * (measured slower on GB300, so off by default; split_k then reports the most
+ * pieces of a tile and `tiles` the units).  The plan is that of beta == 0: with
  * beta != 0 the CTA-pair kernel runs one stage fewer (its shared memory holds
  * a deeper staging ring for C) unless GB3_GEMM_C_RING = 0.  M <= 128 runs on
  * the small-M kernel when its 128-row weight tiles (batch * ceil(N / 128))
@@ -380,6 +386,45 @@ GEMM_API int gemm_row_stats_plan(int64_t batch, int64_t M, int64_t N, int64_t K,
 
 /* Plan of gemm_gate_up_silu(M, N, K, ...), as gemm_bf16_plan. */
 GEMM_API int gemm_gate_up_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_plan *plan);
+
+/* ------------------------------------------------------------------------
+ * Layout inspection (host only, no GPU needed): the encodings the kernels
+ * compute, returned by the same functions the kernels call, so that they can
+ * be checked field by field without running a kernel.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * Shared-memory matrix descriptor of an operand tile stored as TMA writes it
+ * with the 128-byte swizzle ("TMA and Hopper WGMMA", section "The same storage
+ * contract on both sides": 16-byte chunk j of 128-byte row r at chunk
+ * j xor (r mod 8), eight-row groups 1024 bytes apart).  smem_address: the
+ * tile's shared-memory byte address (1024-byte aligned for a whole tile).
+ * mn_chunk_bytes == 0: a K-major tile (rows of 64 K elements); otherwise an
+ * MN-major tile whose 64-element MN chunks are mn_chunk_bytes apart.
+ */
+GEMM_API uint64_t gemm_layout_smem_descriptor(uint32_t smem_address, uint32_t mn_chunk_bytes);
+
+/*
+ * Instruction descriptor of one tcgen05.mma kind::f16 with FP32 accumulation
+ * and K-major operands: M rows, N columns (M in {64, 128, 256}, N a multiple
+ * of 8 or 16), both operands in_dtype (GEMM_IN_BF16 or GEMM_IN_F16).
+ */
+GEMM_API uint32_t gemm_layout_instr_descriptor(int M, int N, int in_dtype);
+
+/*
+ * Byte offset, inside one 32-row epilogue staging box or one operand tile
+ * with 128-byte rows and the 128-byte swizzle, of 16-byte chunk `chunk` of
+ * row `row` ("TMA and Hopper WGMMA", section "The same storage contract on
+ * both sides": element (r, k) of a 16-bit tile at 64 r + (k xor 8 (r mod 8))).
+ */
+GEMM_API uint32_t gemm_layout_swizzle128_offset(int row, int chunk);
+
+/*
+ * Tensor Memory address of (lane, column) in an allocation whose address is
+ * `base` ("TMEM tiles and transfers", section "Storage units": lane in bits
+ * 31:16, 32-bit column in bits 15:0).
+ */
+GEMM_API uint32_t gemm_layout_tmem_address(uint32_t base, int lane, int column);
 
 #ifdef __cplusplus
 }

@@ -565,3 +565,53 @@ def attn(heads=2, Nq=256, Nk=256, D=128, scale=0.1, Q=A16, ldq=128, sq=256 * 128
 ])
 def test_attention_validation_without_gpu(lib, kw, expect):
     assert attn(**kw) == expect
+
+
+def layout_smem(stages, stage_bytes, barriers, staging=0):
+    """Dynamic shared memory of a kernel layout: 1024 bytes of alignment slack,
+    the stage ring, the epilogue staging boxes, 8 bytes per mbarrier and 16
+    bytes for the TMEM address and the abort flag."""
+    return 1024 + stages * stage_bytes + staging + barriers * 8 + 16
+
+
+@pytest.mark.parametrize("case", ["pair256", "pair224", "tiled", "skinny", "small_m16",
+                                  "small_m64", "small_m128", "pair_gate_up", "gate_up",
+                                  "skinny_gate_up"])
+def test_plan_shared_memory_matches_kernel_layout(lib, monkeypatch, case):
+    """The dynamic shared memory a plan reports (the size the library launches
+    with) equals the layout its kernel indexes: A/B (or W/X) rows per stage,
+    staging boxes of 4 KB (four epilogue warps x two), 2 * stages + 5 barriers.
+    Every kernel also compares the size it was given with its layout at entry
+    and records GEMM_ERR_CUDA (site 9) instead of running past its allocation."""
+    kb = 64 * 2                                     # one 64-element BF16 row of a stage
+    staging = 4 * 2 * 4096
+    if case.startswith("pair2"):
+        bn = int(case[4:])
+        monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", str(bn))
+        st, p = _native.gemm_bf16_plan(4096, 4096, 4096, _native.GEMM_OUT_BF16, 152)
+        want = layout_smem(6, 128 * kb + bn // 2 * kb, 2 * 6 + 5, staging)
+    elif case == "tiled":
+        monkeypatch.setenv("GB3_GEMM_SMALL_M", "0")
+        st, p = _native.gemm_bf16_plan(128, 4096, 4096, _native.GEMM_OUT_BF16, 152)
+        want = layout_smem(4, 128 * kb + 256 * kb, 2 * 4 + 5, staging)
+    elif case == "skinny":
+        st, p = _native.gemm_bf16_plan(16, 28672, 8192, _native.GEMM_OUT_BF16, 152)
+        want = layout_smem(12, 128 * kb + 16 * kb, 2 * 12 + 5)
+    elif case.startswith("small_m"):
+        nx = int(case[7:])
+        st, p = _native.gemm_bf16_plan(nx, 8192, 8192, _native.GEMM_OUT_BF16, 152)
+        stage = 128 * kb + nx * kb
+        stages = (200 * 1024) // stage              # as many stages as fit in 200 KB
+        want = layout_smem(stages, stage, 2 * stages + 5)
+        assert p.stages == stages
+    elif case == "pair_gate_up":
+        st, p = _native.gemm_gate_up_plan(4096, 14336, 4096, 152)
+        want = layout_smem(6, 128 * kb + 128 * kb, 2 * 6 + 5, staging)
+    elif case == "gate_up":
+        st, p = _native.gemm_gate_up_plan(100, 14336, 4096, 152)
+        want = layout_smem(4, 128 * kb + 256 * kb, 2 * 4 + 5, staging)
+    else:
+        st, p = _native.gemm_gate_up_plan(16, 14336, 4096, 152)
+        want = layout_smem(6, 2 * 128 * kb + 16 * kb, 2 * 6 + 5)
+    assert st == 0
+    assert p.smem_bytes == want and want <= 232448, (p.as_dict(), want)
