@@ -326,8 +326,14 @@ def plan_of(lib, w):
         return lib.gate_up_plan(w.M, w.N, w.K)
     if w.kind == "rmsnorm_gate_up":
         pl = dict(lib.gate_up_plan(w.M, w.N, w.K))
-        pl["launches"] += 1          # the normalisation before the projection
-        pl["kernel_name"] = "rms_norm+" + pl["kernel_name"]
+        single = (pl["kernel_name"] == "pair_gate_up" and w.K % 8 == 0 and w.K * 10 <= 224 * 1024
+                  and os.environ.get("GB3_NORM_ROW_WARPS") != "1"
+                  and os.environ.get("GB3_RMSNORM_SINGLE_LAUNCH", "0") == "1")
+        if single:
+            pl["kernel_name"] = "pair_gate_up with the normalisation in the same launch"
+        else:
+            pl["launches"] += 1      # the normalisation, then the projection
+            pl["kernel_name"] = "rms_norm+" + pl["kernel_name"]
         return pl
     if w.kind == "rms_norm":
         return {"kernel_name": "rms_norm", "tile_n": w.K, "split_k": 1, "grid": None,

@@ -645,6 +645,8 @@ struct DeviceState {
   size_t stats_ws_bytes = 0;
   int* stats_counters = nullptr;
   size_t stats_counter_count = 0;
+  // device address of the grid-barrier counters (a library array, not allocated)
+  unsigned int* grid_sync = nullptr;
 };
 
 std::mutex g_mu;
@@ -924,21 +926,25 @@ int launch(void (*kernel)(ExpT...), int grid, int block, int smem, cudaStream_t 
   return GEMM_OK;
 }
 
+// cooperative: every CTA of the grid is resident at once (the kernel's CTAs
+// wait on one another at a grid-wide barrier); the launch fails otherwise.
 template <typename... ExpT, typename... ActT>
-int launch_pair(void (*kernel)(ExpT...), int grid, int smem, cudaStream_t stream,
+int launch_pair(void (*kernel)(ExpT...), int grid, int smem, cudaStream_t stream, bool cooperative,
                 ActT&&... args) {
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(kThreads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cooperative ? 2 : 1;
   if (cudaLaunchKernelEx(&cfg, kernel, std::forward<ActT>(args)...) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
@@ -978,6 +984,37 @@ int query_pair_slots(int dev) {
     d.pair_slots = n;
   }
   return d.pair_slots;
+}
+
+// Row geometry of the normalisation the gate/up kernel runs before its GEMM,
+// the one the standalone normalisation takes for BF16 rows of D elements (so
+// that Xn has the same bits): 1 for rows of at most 4 vectors of 16 bytes per
+// lane (one warp, 4 cached), 2 above (two warps of 8 cached each); 0 when the
+// standalone normalisation is forced onto one warp per long row
+// (GB3_NORM_ROW_WARPS = 1), which the two-launch path then runs.
+int fused_norm_geometry(int64_t D) {
+  const int64_t vecs_per_lane = (D * 2 + 32 * 16 - 1) / (32 * 16);
+  if (vecs_per_lane <= 4) return 1;
+  return env_int("GB3_NORM_ROW_WARPS", 2) == 1 ? 0 : 2;
+}
+
+// The device address of the grid-barrier counters (a fixed array of the
+// library, zero at load, reset by the last CTA of every launch).
+__device__ unsigned int g_grid_sync[2];
+
+// Caller holds g_mu.
+int grid_sync_counters(int dev, unsigned int** out) {
+  DeviceState& d = g_dev[dev];
+  if (d.grid_sync == nullptr) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_grid_sync) != cudaSuccess || addr == nullptr) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    d.grid_sync = static_cast<unsigned int*>(addr);
+  }
+  *out = d.grid_sync;
+  return GEMM_OK;
 }
 
 // C = beta * C for every matrix of the batch (K == 0); C is not read when
@@ -1124,19 +1161,23 @@ void pair_units(int dev, gemm_plan* pl, const Problem& q, int out_cols, TilePara
 
 // RING: C is read through the deeper staging ring (beta != 0), which takes
 // the shared memory of one pipeline stage.
-template <int BN, int EPI, bool STATS = false, bool RING = false>
+// NORM != 0: the gate/up kernel that normalises its activation first (one
+// cooperative launch, see NormParams).
+template <int BN, int EPI, bool STATS = false, bool RING = false, int NORM = 0>
 int launch_pair_gemm(const gemm_plan& pl, int dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
                      const CUtensorMap& tmB2, const CUtensorMap& tmOut, const TileParams& p,
-                     cudaStream_t stream, const RowStatsParams& rs = RowStatsParams{}) {
+                     cudaStream_t stream, const RowStatsParams& rs = RowStatsParams{},
+                     const NormParams& nrm = NormParams{}) {
   constexpr int kStagesHere = RING ? kPairStages - 1 : kPairStages;
   using Cfg = PairCfg<BN, kStagesHere, EPI, RING>;
-  auto kern = gemm_pair_kernel<BN, kStagesHere, EPI, STATS, RING>;
+  auto kern = gemm_pair_kernel<BN, kStagesHere, EPI, STATS, RING, NORM>;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     const int st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), Cfg::kSmemBytes);
     if (st != GEMM_OK) return st;
   }
-  return launch_pair(kern, pl.grid, Cfg::kSmemBytes, stream, tmA, tmB, tmB2, tmOut, p, rs);
+  return launch_pair(kern, pl.grid, Cfg::kSmemBytes, stream, NORM != 0, tmA, tmB, tmB2, tmOut, p,
+                     rs, nrm);
 }
 
 template <int BN, int STAGES, int EPI, bool STATS = false>
@@ -1637,17 +1678,68 @@ int gemm_gate_up_silu(int64_t M, int64_t N, int64_t K, const void* X, int64_t ld
 int gemm_rmsnorm_gate_up_silu(int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx,
                               const float* G, float eps, const void* Wg, const void* Wu,
                               int64_t ldw, void* Xn, int64_t ldxn, void* Y, int64_t ldy,
-                              void* stream) {
+                              void* stream_) {
   // Every argument is checked before anything is enqueued.
   int st = validate_gate_up(M, N, K, Xn, ldxn, Wg, Wu, ldw, Y, ldy);
   if (st != GEMM_OK) return st;
   if ((st = rms_norm_check(M, K, X, ldx, GEMM_OUT_BF16, G, eps, Xn, ldxn, GEMM_OUT_BF16)) !=
       GEMM_OK)
     return st;
-  if ((st = rms_norm_run(M, K, X, ldx, GEMM_OUT_BF16, G, eps, Xn, ldxn, GEMM_OUT_BF16,
-                         static_cast<cudaStream_t>(stream))) != GEMM_OK)
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (M > 0 && N > 0 && K > 0) {
+    int dev;
+    if ((st = current_device(&dev)) != GEMM_OK) return st;
+    int sms, slots;
+    unsigned int* sync = nullptr;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if ((st = probe_device(dev)) != GEMM_OK) return st;
+      sms = g_dev[dev].sms;
+      slots = query_pair_slots(dev);
+      if ((st = grid_sync_counters(dev, &sync)) != GEMM_OK) return st;
+    }
+    gemm_plan pl;
+    plan_gate_up(M, N, K, sms, &pl, slots);
+    // GB3_RMSNORM_SINGLE_LAUNCH = 1: one launch, the pair gate/up kernel
+    // normalising its activation first.  It copies the gains and whole rows
+    // of X into the pipeline's shared memory: rows of whole 16-byte vectors,
+    // three chunks of at least one row beside the gains.  Not the default:
+    // measured on GB300 (4096 x 14336 x 4096, same box) at 512.7 us against
+    // 508.5 us for the two launches and 490.4 us for the plain gate/up.
+    // Both are bound by writing Xn (32 MB): from every SM at once, with
+    // nothing else to overlap, it runs at about 3 TB/s in the single launch,
+    // while the standalone normalisation overlaps it with its reads.
+    const bool rows_fit =
+        (K * 2) % 16 == 0 && K * (4 + 3 * 2) <= PairCfg<256, kPairStages, EPI_GATE_UP>::kBarOffset &&
+        env_int("GB3_RMSNORM_SINGLE_LAUNCH", 0) == 1;
+    const int norm = rows_fit ? fused_norm_geometry(K) : 0;
+    if (pl.kernel == K_PAIR_GATE_UP && norm != 0) {
+      // One launch: the pair gate/up kernel normalises X into Xn first.
+      const Problem q{1, M, N, K, 1.0f, 0.0f, Xn, ldxn, 0, Wg, ldw, 0, Y, ldy, 0, GEMM_IN_BF16,
+                      GEMM_OUT_BF16};
+      const int out_cols = CfgPairGU::kOutCols;
+      CUtensorMap tmX, tmWg, tmWu, tmY;
+      if ((st = operand_map(&tmX, Xn, GEMM_IN_BF16, K, M, 1, ldxn, 0, 128)) != GEMM_OK) return st;
+      if ((st = operand_map(&tmWg, Wg, GEMM_IN_BF16, K, N, 1, ldw, 0, out_cols)) != GEMM_OK)
+        return st;
+      if ((st = operand_map(&tmWu, Wu, GEMM_IN_BF16, K, N, 1, ldw, 0, out_cols)) != GEMM_OK)
+        return st;
+      if ((st = output_map(&tmY, Y, 1, M, N, ldy, 0, GEMM_OUT_BF16, out_cols)) != GEMM_OK)
+        return st;
+      TileParams p = tile_params(q, kPairBM, out_cols, idesc_f32_acc(kPairBM, 256, false));
+      pair_units(dev, &pl, q, out_cols, &p, stream, true, slots);
+      const NormParams nrm{X,  ldx, G, eps, Xn, ldxn, static_cast<int>(M), static_cast<int>(K),
+                           sync};
+      return norm == 2 ? launch_pair_gemm<256, EPI_GATE_UP, false, false, 2>(
+                             pl, dev, tmX, tmWg, tmWu, tmY, p, stream, RowStatsParams{}, nrm)
+                       : launch_pair_gemm<256, EPI_GATE_UP, false, false, 1>(
+                             pl, dev, tmX, tmWg, tmWu, tmY, p, stream, RowStatsParams{}, nrm);
+    }
+  }
+  if ((st = rms_norm_run(M, K, X, ldx, GEMM_OUT_BF16, G, eps, Xn, ldxn, GEMM_OUT_BF16, stream)) !=
+      GEMM_OK)
     return st;
-  return gemm_gate_up_silu(M, N, K, Xn, ldxn, Wg, Wu, ldw, Y, ldy, stream);
+  return gemm_gate_up_silu(M, N, K, Xn, ldxn, Wg, Wu, ldw, Y, ldy, stream_);
 }
 
 int gemm_attention(int64_t heads, int64_t Nq, int64_t Nk, int64_t D, float scale, const void* Q,
@@ -1720,6 +1812,8 @@ int gemm_get_device_status(void* stream, int* site) {
     DeviceState& d = g_dev[dev];
     if (d.counters != nullptr &&
         cudaMemset(d.counters, 0, d.counter_count * sizeof(int)) != cudaSuccess)
+      cudaGetLastError();
+    if (d.grid_sync != nullptr && cudaMemset(d.grid_sync, 0, 2 * sizeof(unsigned int)) != cudaSuccess)
       cudaGetLastError();
     if (d.stats_counters != nullptr &&
         cudaMemset(d.stats_counters, 0, d.stats_counter_count * sizeof(int)) != cudaSuccess)

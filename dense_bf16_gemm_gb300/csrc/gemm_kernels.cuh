@@ -47,7 +47,8 @@ enum WaitSite : int {
   SITE_SKINNY = 6,
   SITE_SELFTEST = 7,
   SITE_EPI_C_FULL = 8,
-  SITE_LAUNCH_SMEM = 9
+  SITE_LAUNCH_SMEM = 9,
+  SITE_GRID_SYNC = 10
 };
 
 // [0] status code, [1] wait site, [2] block index of the first failure.

@@ -23,10 +23,57 @@
 #pragma once
 
 #include "gemm_kernels.cuh"
+#include "rms_norm.cuh"
 
 namespace gb3 {
 
 constexpr int kPairBM = 256;  // tile rows of a CTA pair
+
+// The normalisation of the activation that the gate/up kernel runs before its
+// GEMM when instantiated with NORM != 0 ("Tiles and shared memory", section
+// "A complete kernel"): Xn = rms_norm(X, G, eps) in BF16, written to the
+// buffer its A operand map reads.  NORM selects the row geometry the
+// standalone normalisation would use for this row length (1: one warp and 4
+// cached vectors per lane; 2: two warps of 8), so Xn has the same bits.
+struct NormParams {
+  const void* X;
+  long long ldx;
+  const float* G;
+  float eps;
+  void* Xn;
+  long long ldxn;
+  int rows, D;
+  unsigned int* sync;  // grid barrier counters [arrivals, departures], zero between launches
+};
+
+// Grid-wide barrier of a cooperative launch, run by thread 0 of every CTA:
+// arrive (release: the CTA's writes, fenced before, are visible first), wait
+// (acquire, bounded) until all gridDim.x CTAs have arrived, then count the
+// departure; the last CTA to leave resets both counters for the next launch.
+// On timeout the CTA's abort flag and the device status word are set and
+// false is returned (the counters are then cleared by the host when it reads
+// the status).
+__device__ __noinline__ bool grid_sync_bounded(unsigned int* sync, volatile int* abort_flag) {
+  __threadfence();
+  atomicAdd(&sync[0], 1u);
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    unsigned int arrived;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(arrived) : "l"(sync) : "memory");
+    if (arrived >= gridDim.x) break;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      record_timeout(SITE_GRID_SYNC);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  if (atomicAdd(&sync[1], 1u) == gridDim.x - 1) {
+    sync[0] = 0;
+    sync[1] = 0;
+  }
+  return true;
+}
 
 // RING: the epilogue reads C through a ring of kRingSlots staging slots per
 // warp (epilogue_tile_ring), each slot with its own barrier.
@@ -52,14 +99,15 @@ struct PairCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <int BN, int STAGES, int EPI, bool STATS = false, bool RING = false>
+template <int BN, int STAGES, int EPI, bool STATS = false, bool RING = false, int NORM = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmB2,
                      const __grid_constant__ CUtensorMap tmOut, const TileParams p,
-                     const RowStatsParams rs) {
+                     const RowStatsParams rs, const NormParams nrm) {
   using Cfg = PairCfg<BN, STAGES, EPI, RING>;
+  static_assert(NORM == 0 || EPI == EPI_GATE_UP, "the normalised activation feeds gate/up");
   if (!launch_smem_ok(Cfg::kSmemBytes)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -76,6 +124,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
 
+  if constexpr (NORM != 0) {
+    // Phase 1: this CTA's contiguous share of the rows of X, normalised into
+    // Xn.  The rows (and the gains) come into the still unused pipeline
+    // shared memory by bulk copies, as many rows per batch as fit, so that a
+    // whole batch is in flight at once; the row groups (1 or 2 warps, the
+    // standalone normalisation's geometry, two rows at a time) normalise each
+    // row over its copy and send it to Xn with one bulk copy.  Those copies
+    // have completed before the grid barrier below, after which every CTA's
+    // TMA loads read Xn.
+    constexpr int kRW = NORM == 2 ? 2 : 1;
+    constexpr int kGroups = (kThreads / 32) / kRW;
+    constexpr int kSlots = 3;  // chunks of rows in flight
+    __shared__ float norm_partial[2][2][kThreads / 32];
+    __shared__ __align__(8) uint64_t chunk_bar[kSlots];
+    const uint32_t row_bytes = (static_cast<uint32_t>(nrm.D) * 2 + 15u) & ~15u;
+    const uint32_t g_bytes = static_cast<uint32_t>(nrm.D) * 4;  // the gains, first
+    const int per_cta = (nrm.rows + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+    const int r0 = min(nrm.rows, static_cast<int>(blockIdx.x) * per_cta);
+    const int r1 = min(nrm.rows, r0 + per_cta);
+    // Rows per chunk: kSlots chunks fit in the pipeline region beside the
+    // gains (the host takes this path only for rows of whole 16-byte vectors
+    // of which kSlots fit there with the gains).
+    const uint32_t room = static_cast<uint32_t>(Cfg::kBarOffset);
+    const int chunk = room > g_bytes ? static_cast<int>((room - g_bytes) / row_bytes) / kSlots : 0;
+    const int nchunks = chunk > 0 ? (r1 - r0 + chunk - 1) / chunk : 0;
+    auto slot_addr = [&](int c) {
+      return sbase + g_bytes + static_cast<uint32_t>((c % kSlots) * chunk) * row_bytes;
+    };
+    auto load_chunk = [&](int c) {  // thread 0: chunk c's rows (and, first, the gains)
+      const int first = r0 + c * chunk, n = min(chunk, r1 - first);
+      const uint32_t bar = smem_u32(&chunk_bar[c % kSlots]);
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * row_bytes + (c == 0 ? g_bytes : 0u));
+      if (c == 0) bulk_load(sbase, nrm.G, g_bytes, bar);
+      for (int r = 0; r < n; ++r)
+        bulk_load(slot_addr(c) + static_cast<uint32_t>(r) * row_bytes,
+                  static_cast<const uint8_t*>(nrm.X) + static_cast<long long>(first + r) * nrm.ldx * 2,
+                  row_bytes, bar);
+    };
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < kSlots; ++i) mbar_init(smem_u32(&chunk_bar[i]), 1);
+      fence_barrier_init();
+      for (int c = 0; c < min(kSlots, nchunks); ++c) load_chunk(c);
+    }
+    __syncthreads();
+    for (int c = 0; c < nchunks; ++c) {
+      const int first = r0 + c * chunk, n = min(chunk, r1 - first);
+      const uint32_t bar = smem_u32(&chunk_bar[c % kSlots]);
+      const bool landed =
+          wait_bounded(bar, static_cast<uint32_t>(c / kSlots) & 1u, nullptr, SITE_GRID_SYNC);
+      // One decision for the whole CTA (the row groups meet at named barriers).
+      if (__syncthreads_and(landed))
+        rms_norm_rows<NORM_BF16, NORM_BF16, NORM == 2 ? 8 : 4, kRW, kThreads / 32, true, 2, true>(
+            smem + (slot_addr(c) - sbase), row_bytes / 2, reinterpret_cast<const float*>(smem),
+            nrm.eps, nrm.Xn, nrm.ldxn, first + n, nrm.D,
+            first + static_cast<int>(threadIdx.x >> 5) / kRW, kGroups, norm_partial, 1, first,
+            row_bytes);
+      if (c + kSlots < nchunks) {
+        // The chunk's copies to Xn have read its slot before the slot is refilled.
+        bulk_wait_group_read<0>();
+        __syncthreads();
+        if (threadIdx.x == 0) load_chunk(c + kSlots);
+      }
+    }
+    // Every copy to Xn has completed before the grid barrier below.
+    bulk_wait_group<0>();
+    __syncthreads();
+  }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs, 1: its peer
@@ -110,15 +225,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // both CTAs' barriers exist and TMEM is allocated in both
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_holder;
+  if constexpr (NORM != 0) {
+    // Every CTA's rows of Xn are written before any CTA loads a tile of it.
+    // A barrier that gives up sets the abort flag: every role then leaves
+    // through its bounded waits.
+    if (threadIdx.x == 0) grid_sync_bounded(nrm.sync, abort_flag);
+    __syncthreads();
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // Xn was written by other CTAs through the generic proxy (NORM).
+      if constexpr (NORM != 0) asm volatile("fence.proxy.async.global;" ::: "memory");
       const uint32_t full0_even = mapa_shared(full_bar(0), 0);
       int s = 0;
       uint32_t ph = 0;
       long long issued = 0;
-      bool ok = true;
+      bool ok = *abort_flag == 0;
       for (int i = 0; ok && i < nunits; ++i) {
         const WorkUnit un = cluster_unit(p, cluster, nclusters, i);
         int bt, mb, nb;

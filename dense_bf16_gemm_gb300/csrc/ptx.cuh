@@ -105,6 +105,38 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Untiled copy of `bytes` contiguous bytes (a multiple of 16, both addresses
+// 16-byte aligned) from global memory into this CTA's shared memory,
+// completing as a transaction count on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Untiled copy of `bytes` contiguous bytes (a multiple of 16, both addresses
+// 16-byte aligned) from this CTA's shared memory to global memory, completing
+// through the bulk-group mechanism (bulk_commit_group / bulk_wait_group*).
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
+
+// bulk_store with an L2 eviction-priority hint (a createpolicy value).
+__device__ __forceinline__ void bulk_store_hint(void* dst, uint32_t src, uint32_t bytes,
+                                                uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(
+          reinterpret_cast<uint64_t>(dst)),
+      "r"(src), "r"(bytes), "l"(policy)
+      : "memory");
+}
+
 // 3-D tiled store of one shared-memory box (z selects the matrix).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t x,
                                              int32_t y, int32_t z) {

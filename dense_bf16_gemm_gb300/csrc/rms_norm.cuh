@@ -76,20 +76,24 @@ __device__ __forceinline__ float sum_squares(const uint4& q, float ss) {
   return ss;
 }
 
-// y = (x * inv) * g for one vector; `gv` points at the vector's gains.
-template <int XK, int YK>
+// y = (x * inv) * g for one vector; `gv` points at the vector's gains (in
+// global memory, read through the read-only path, or with G_GENERIC a
+// generic address, e.g. a copy in shared memory: the same values).
+template <int XK, int YK, bool G_GENERIC = false>
 __device__ __forceinline__ void scale_store(const uint4& q, float inv, const float* gv, void* dst) {
   constexpr int V = NormElems<XK>::kPerVec;
   float x[8];
   unpack_vec<XK>(q, x);
   float y[8];
-  const float4 g0 = __ldg(reinterpret_cast<const float4*>(gv));
+  const float4 g0 = G_GENERIC ? *reinterpret_cast<const float4*>(gv)
+                              : __ldg(reinterpret_cast<const float4*>(gv));
   y[0] = x[0] * inv * g0.x;
   y[1] = x[1] * inv * g0.y;
   y[2] = x[2] * inv * g0.z;
   y[3] = x[3] * inv * g0.w;
   if constexpr (V == 8) {
-    const float4 g1 = __ldg(reinterpret_cast<const float4*>(gv) + 1);
+    const float4 g1 = G_GENERIC ? reinterpret_cast<const float4*>(gv)[1]
+                                : __ldg(reinterpret_cast<const float4*>(gv) + 1);
     y[4] = x[4] * inv * g1.x;
     y[5] = x[5] * inv * g1.y;
     y[6] = x[6] * inv * g1.z;
@@ -128,76 +132,160 @@ __device__ __forceinline__ void store_scalar(void* base, long long idx, float y)
 // RW warps share a row (RW = 2 for long rows: half the registers per warp, so
 // twice the warps, and twice the bytes, in flight per SM).  Warp `sub` of a
 // row takes vectors v = (i*RW + sub)*32 + lane; the warps' sums meet in
-// shared memory (double-buffered by row parity, one named barrier per row)
-// and are added in sub order, so both warps hold the same value.
+// shared memory (`partial`, double-buffered by row parity, one named barrier
+// per row group: id bar0 + group) and are added in sub order, so both warps
+// hold the same value.
+//
+// The rows a group normalises: m = group0, group0 + group_stride, ... up to
+// `rows`.  Row m is read from X + (m - src_row0) * ldx (elements), written to
+// Y + m * ldy: the normalisation kernel reads X itself (src_row0 = 0); the
+// gate/up kernel that normalises its activation first reads a batch of rows
+// it copied into shared memory (X = the copy, src_row0 its first row), and
+// with G_GENERIC the gains from a copy in shared memory too.  ROWS rows
+// (1 or 2, m and m + group_stride) go through the steps together, so that
+// their independent work overlaps; every row takes exactly the operations,
+// in the same order, of ROWS = 1, so the bits are the same in every case.
+// Y_BULK (X a copy in shared memory, YK == XK): each normalised row is
+// written over its copy and sent to Y by one bulk copy of row_bytes bytes
+// (issued by the group's first lane, committed as one bulk group); the
+// caller waits for those copies before it reuses the shared memory.
+template <int XK, int YK, int CACHE, int RW, int WARPS, bool G_GENERIC = false, int ROWS = 1,
+          bool Y_BULK = false>
+__device__ __forceinline__ void rms_norm_rows(const void* X, long long ldx,
+                                              const float* __restrict__ G, float eps, void* Y,
+                                              long long ldy, int rows, int D, int group0,
+                                              int group_stride, float (&partial)[2][ROWS][WARPS],
+                                              int bar0, int src_row0 = 0,
+                                              uint32_t row_bytes = 0) {
+  static_assert(RW == 1 || RW == 2, "warps per row");
+  static_assert(ROWS == 1 || ROWS == 2, "rows together");
+  static_assert(!Y_BULK || XK == YK, "the row is normalised in place before its copy");
+  constexpr int V = NormElems<XK>::kPerVec;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int grp = warp / RW, sub = warp % RW;
+  const int nvec = D / V;          // whole vectors per row
+  const int tail0 = nvec * V;      // first element of the scalar tail
+  int parity = 0;
+  for (int m0 = group0; m0 < rows; m0 += ROWS * group_stride, parity ^= 1) {
+    const uint4* xrow[ROWS];
+    uint8_t* yrow[ROWS];
+    bool live[ROWS];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+      const int m = m0 + r * group_stride;
+      live[r] = m < rows;
+      xrow[r] = reinterpret_cast<const uint4*>(
+          static_cast<const uint8_t*>(X) +
+          static_cast<long long>(m - src_row0) * ldx * NormElems<XK>::kBytes);
+      yrow[r] = Y_BULK ? const_cast<uint8_t*>(reinterpret_cast<const uint8_t*>(xrow[r]))
+                       : static_cast<uint8_t*>(Y) +
+                             static_cast<long long>(m) * ldy * NormElems<YK>::kBytes;
+    }
+    uint4 cache[ROWS][CACHE];
+    float ss[ROWS];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+      ss[r] = 0.0f;
+#pragma unroll
+      for (int i = 0; i < CACHE; ++i) {
+        const int v = (i * RW + sub) * 32 + lane;
+        if (live[r] && v < nvec) cache[r][i] = xrow[r][v];
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < CACHE; ++i) {
+      const int v = (i * RW + sub) * 32 + lane;
+#pragma unroll
+      for (int r = 0; r < ROWS; ++r)
+        if (live[r] && v < nvec) ss[r] = sum_squares<XK>(cache[r][i], ss[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+      if (!live[r]) continue;
+      for (int v = (CACHE * RW + sub) * 32 + lane; v < nvec; v += 32 * RW)
+        ss[r] = sum_squares<XK>(xrow[r][v], ss[r]);
+      if (sub == 0) {
+        for (int k = tail0 + lane; k < D; k += 32) {
+          const float x = norm_scalar<XK>(xrow[r], k);
+          ss[r] = fmaf(x, x, ss[r]);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+      for (int r = 0; r < ROWS; ++r) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], off);
+    if constexpr (RW > 1) {
+      if (lane == 0)
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) partial[parity][r][warp] = ss[r];
+      asm volatile("bar.sync %0, %1;" ::"r"(bar0 + grp), "r"(32 * RW) : "memory");
+#pragma unroll
+      for (int r = 0; r < ROWS; ++r) {
+        ss[r] = 0.0f;
+#pragma unroll
+        for (int w = 0; w < RW; ++w) ss[r] += partial[parity][r][grp * RW + w];
+      }
+    }
+    float inv[ROWS];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) inv[r] = 1.0f / sqrtf(ss[r] / static_cast<float>(D) + eps);
+
+#pragma unroll
+    for (int i = 0; i < CACHE; ++i) {
+      const int v = (i * RW + sub) * 32 + lane;
+#pragma unroll
+      for (int r = 0; r < ROWS; ++r)
+        if (live[r] && v < nvec)
+          scale_store<XK, YK, G_GENERIC>(cache[r][i], inv[r], G + static_cast<long long>(v) * V,
+                                         yrow[r] + static_cast<long long>(v) * V * NormElems<YK>::kBytes);
+    }
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+      if (!live[r]) continue;
+      for (int v = (CACHE * RW + sub) * 32 + lane; v < nvec; v += 32 * RW)
+        scale_store<XK, YK, G_GENERIC>(xrow[r][v], inv[r], G + static_cast<long long>(v) * V,
+                                       yrow[r] + static_cast<long long>(v) * V * NormElems<YK>::kBytes);
+      if (sub == 0)
+        for (int k = tail0 + lane; k < D; k += 32)
+          store_scalar<YK>(yrow[r], k,
+                           norm_scalar<XK>(xrow[r], k) * inv[r] * (G_GENERIC ? G[k] : __ldg(G + k)));
+    }
+    if constexpr (Y_BULK) {
+      // The group's normalised rows are in shared memory: one lane sends each.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("bar.sync %0, %1;" ::"r"(bar0 + grp), "r"(32 * RW) : "memory");
+      if (sub == 0 && lane == 0) {
+        // Kept in L2: the rows are read again right away (by TMA, every CTA).
+        const uint64_t keep = l2_policy_evict_last();
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+          if (!live[r]) continue;
+          bulk_store_hint(static_cast<uint8_t*>(Y) + static_cast<long long>(m0 + r * group_stride) *
+                                                         ldy * NormElems<YK>::kBytes,
+                          static_cast<uint32_t>(__cvta_generic_to_shared(yrow[r])), row_bytes,
+                          keep);
+        }
+        bulk_commit_group();
+      }
+    }
+  }
+}
+
 template <int XK, int YK, int CACHE, int RW = 1>
 // Resident blocks per SM the registers must allow: 4 for short rows, 2 for
 // one warp holding 16 vectors, 3 for two warps holding 8 each.
 __global__ void __launch_bounds__(kNormThreads, RW == 2 ? 3 : (CACHE <= 4 ? 4 : 2))
     rms_norm_kernel(const void* X, long long ldx, const float* __restrict__ G, float eps, void* Y,
                     long long ldy, int rows, int D) {
-  static_assert(RW == 1 || RW == 2, "warps per row");
-  constexpr int V = NormElems<XK>::kPerVec;
   constexpr int kWarps = kNormThreads / 32;
   constexpr int kGroups = kWarps / RW;  // rows a block works on at a time
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int grp = warp / RW, sub = warp % RW;
-  const int groups = gridDim.x * kGroups;
-  const int nvec = D / V;          // whole vectors per row
-  const int tail0 = nvec * V;      // first element of the scalar tail
-  __shared__ float partial[2][kWarps];
-  int parity = 0;
-  for (int m = blockIdx.x * kGroups + grp; m < rows; m += groups, parity ^= 1) {
-    const uint4* xrow = reinterpret_cast<const uint4*>(
-        static_cast<const uint8_t*>(X) + static_cast<long long>(m) * ldx * NormElems<XK>::kBytes);
-    uint8_t* yrow = static_cast<uint8_t*>(Y) + static_cast<long long>(m) * ldy * NormElems<YK>::kBytes;
-    uint4 cache[CACHE];
-    float ss = 0.0f;
-#pragma unroll
-    for (int i = 0; i < CACHE; ++i) {
-      const int v = (i * RW + sub) * 32 + lane;
-      if (v < nvec) cache[i] = xrow[v];
-    }
-#pragma unroll
-    for (int i = 0; i < CACHE; ++i) {
-      const int v = (i * RW + sub) * 32 + lane;
-      if (v < nvec) ss = sum_squares<XK>(cache[i], ss);
-    }
-    for (int v = (CACHE * RW + sub) * 32 + lane; v < nvec; v += 32 * RW)
-      ss = sum_squares<XK>(xrow[v], ss);
-    const void* xr = static_cast<const uint8_t*>(X) + static_cast<long long>(m) * ldx * NormElems<XK>::kBytes;
-    if (sub == 0) {
-      for (int k = tail0 + lane; k < D; k += 32) {
-        const float x = norm_scalar<XK>(xr, k);
-        ss = fmaf(x, x, ss);
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    if constexpr (RW > 1) {
-      if (lane == 0) partial[parity][warp] = ss;
-      asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(32 * RW) : "memory");
-      ss = 0.0f;
-#pragma unroll
-      for (int w = 0; w < RW; ++w) ss += partial[parity][grp * RW + w];
-    }
-    const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + eps);
-
-#pragma unroll
-    for (int i = 0; i < CACHE; ++i) {
-      const int v = (i * RW + sub) * 32 + lane;
-      if (v < nvec)
-        scale_store<XK, YK>(cache[i], inv, G + static_cast<long long>(v) * V,
-                            yrow + static_cast<long long>(v) * V * NormElems<YK>::kBytes);
-    }
-    for (int v = (CACHE * RW + sub) * 32 + lane; v < nvec; v += 32 * RW)
-      scale_store<XK, YK>(xrow[v], inv, G + static_cast<long long>(v) * V,
-                          yrow + static_cast<long long>(v) * V * NormElems<YK>::kBytes);
-    if (sub == 0)
-      for (int k = tail0 + lane; k < D; k += 32)
-        store_scalar<YK>(yrow, k, norm_scalar<XK>(xr, k) * inv * __ldg(G + k));
-  }
+  __shared__ float partial[2][1][kWarps];
+  const int grp = (threadIdx.x >> 5) / RW;
+  rms_norm_rows<XK, YK, CACHE, RW, kWarps>(X, ldx, G, eps, Y, ldy, rows, D,
+                                           blockIdx.x * kGroups + grp, gridDim.x * kGroups,
+                                           partial, 1);
 }
 
 }  // namespace gb3

@@ -222,7 +222,13 @@ GEMM_API int gemm_rms_norm(int64_t rows, int64_t D, const void *X, int64_t ldx, 
  * rounded to BF16 (nearest even) before the contraction.  Two launches on
  * `stream`, the normalisation then the projection; every argument is
  * checked before either is enqueued.  Allocates nothing beyond what
- * gemm_gate_up_silu does.
+ * gemm_gate_up_silu does.  With GB3_RMSNORM_SINGLE_LAUNCH = 1 (M > 128, K a
+ * multiple of 8 and at most 22937) it is one cooperative launch instead: the
+ * pair gate/up kernel normalises X into Xn, meets at a grid-wide barrier
+ * (status site 10 if it times out) and then reads Xn; the same bits, but
+ * measured slower on GB300 than the two launches, hence not the default.
+ * Calls of this form on one device must not overlap (they share the
+ * barrier's counters).
  */
 GEMM_API int gemm_rmsnorm_gate_up_silu(int64_t M, int64_t N, int64_t K,
                               const void *X, int64_t ldx, const float *G, float eps,
@@ -278,9 +284,10 @@ GEMM_API const char *gemm_status_string(int status);
  * *site when site is not NULL: 1 producer waiting for a free stage, 2 MMA
  * waiting for a full stage, 3 MMA waiting for a free accumulator, 4 epilogue
  * waiting for a full accumulator, 5 a drain before exit, 6 the split-K kernel,
- * 7 gemm_selftest_wait_timeout, 8 epilogue waiting for a box of C; with
- * status GEMM_ERR_CUDA, 9 a kernel launched with less dynamic shared memory
- * than its layout needs (it returned without touching shared memory).
+ * 7 gemm_selftest_wait_timeout, 8 epilogue waiting for a box of C, 10 the
+ * grid-wide barrier of gemm_rmsnorm_gate_up_silu's single launch; with status
+ * GEMM_ERR_CUDA, 9 a kernel launched with less dynamic shared memory than its
+ * layout needs (it returned without touching shared memory).
  */
 GEMM_API int gemm_get_device_status(void *stream, int *site);
 

@@ -301,9 +301,88 @@ def check_rmsnorm_gate_up(g, M, N, K, seed, rows=None, cols=None, dist_w=("norma
     assert_status_ok(g)
 
 
-@pytest.mark.parametrize("M,N,K", [(200, 296, 256), (300, 520, 1000), (16, 256, 4096)])
-def test_rmsnorm_gate_up(g, M, N, K):
+@pytest.fixture(params=["two_launches", "single_launch"])
+def launches(request, monkeypatch):
+    """Both forms of the normalised gate/up: the default two launches, and
+    (GB3_RMSNORM_SINGLE_LAUNCH=1, M > 128) one launch of the pair gate/up
+    kernel that normalises its rows of X first, with the geometry the
+    standalone normalisation takes (one warp per row for K <= 1024, two
+    warps for longer rows), so the bits are the same."""
+    monkeypatch.setenv("GB3_RMSNORM_SINGLE_LAUNCH", "1" if request.param == "single_launch" else "0")
+    return request.param
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 296, 256), (300, 520, 1000), (16, 256, 4096),
+                                   (512, 1000, 4096), (1100, 2600, 320)])
+def test_rmsnorm_gate_up(g, launches, M, N, K):
     check_rmsnorm_gate_up(g, M, N, K, seed=M + N + K)
+
+
+def test_rmsnorm_gate_up_two_launches_when_forced(g, monkeypatch):
+    """With the standalone normalisation forced onto one warp per long row the
+    call takes the two-launch path, still bit-identical to the two steps."""
+    monkeypatch.setenv("GB3_NORM_ROW_WARPS", "1")
+    check_rmsnorm_gate_up(g, 300, 520, 2048, seed=91)
+
+
+def test_rmsnorm_gate_up_rows_of_partial_vectors(g):
+    """K = 1004 (rows of 2008 bytes, not whole 16-byte vectors) in a padded X:
+    the call takes the two-launch path, bit-identical to the two steps."""
+    M, N, K = 300, 520, 1004
+    X, G, Wg, Wu = workloads.rmsnorm_gate_up_inputs(M, N, K, 94, ("normal", 0.0625))
+    Xbuf = torch.zeros((M, 1008), dtype=torch.bfloat16, device="cuda")
+    Xbuf[:, :K] = X.cuda()
+    Xd = Xbuf[:, :K]
+    Wgb = torch.zeros((N, 1008), dtype=torch.bfloat16, device="cuda")
+    Wub = torch.zeros((N, 1008), dtype=torch.bfloat16, device="cuda")
+    Wgb[:, :K], Wub[:, :K] = Wg.cuda(), Wu.cuda()
+    Gd = G.cuda()
+    Y, Xn = g.rmsnorm_gate_up_silu(Xd, Gd, 1e-6, Wgb[:, :K], Wub[:, :K],
+                                   Xn=torch.zeros((M, 1008), dtype=torch.bfloat16,
+                                                  device="cuda")[:, :K])
+    Xn2 = g.rms_norm(Xd, Gd, 1e-6, Y=torch.zeros((M, 1008), dtype=BF16, device="cuda")[:, :K])
+    torch.cuda.synchronize()
+    assert torch.equal(Xn.contiguous().view(torch.int16), Xn2.contiguous().view(torch.int16))
+    rr, cc = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    res = oracle.rmsnorm_gate_up_entries(X, G, 1e-6, Wg, Wu, rr.ravel(), cc.ravel())
+    tol = oracle.gate_up_tolerance(res, rel=oracle.rmsnorm_gate_up_rel(K))
+    assert_within(to_f64(Y).ravel(), res["y"], tol, "rmsnorm gate/up K=1004")
+    assert_status_ok(g)
+
+
+def test_rmsnorm_gate_up_in_place(g, launches):
+    """Xn may be X itself: each row is read by the threads that then write it."""
+    M, N, K = 400, 704, 2048
+    X, G, Wg, Wu = workloads.rmsnorm_gate_up_inputs(M, N, K, 92, ("normal", 0.0625))
+    Gd, Wgd, Wud = G.cuda(), Wg.cuda(), Wu.cuda()
+    Xd = X.cuda()
+    Y, Xn = g.rmsnorm_gate_up_silu(Xd, Gd, 1e-6, Wgd, Wud, Xn=Xd)
+    torch.cuda.synchronize()
+    assert Xn.data_ptr() == Xd.data_ptr()
+    Xn2 = g.rms_norm(X.cuda(), Gd, 1e-6, out_dtype=BF16)
+    Y2 = g.gate_up_silu(Xn2, Wgd, Wud)
+    torch.cuda.synchronize()
+    assert torch.equal(Xn.view(torch.int16), Xn2.view(torch.int16))
+    assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))
+    assert_status_ok(g)
+
+
+def test_rmsnorm_gate_up_grids_of_different_sizes_back_to_back(g, monkeypatch):
+    """The single launch's grid-wide barrier counters return to zero after every
+    launch, so launches with grids of different sizes (20 CTAs, then all
+    resident pairs, then 20 again) each wait for exactly their own CTAs."""
+    monkeypatch.setenv("GB3_RMSNORM_SINGLE_LAUNCH", "1")
+    shapes = [(300, 520, 1024), (2048, 4096, 512), (300, 520, 1024)]
+    for i, (M, N, K) in enumerate(shapes):
+        X, G, Wg, Wu = workloads.rmsnorm_gate_up_inputs(M, N, K, 93 + i, ("normal", 0.0625))
+        Xd, Gd, Wgd, Wud = X.cuda(), G.cuda(), Wg.cuda(), Wu.cuda()
+        Y, Xn = g.rmsnorm_gate_up_silu(Xd, Gd, 1e-6, Wgd, Wud)
+        Xn2 = g.rms_norm(Xd, Gd, 1e-6, out_dtype=BF16)
+        Y2 = g.gate_up_silu(Xn2, Wgd, Wud)
+        torch.cuda.synchronize()
+        assert torch.equal(Xn.view(torch.int16), Xn2.view(torch.int16)), (M, N, K)
+        assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16)), (M, N, K)
+    assert_status_ok(g)
 
 
 @pytest.mark.slow
