@@ -233,10 +233,10 @@ int pair_stage_bytes(int bn) { return 128 * kBK * 2 + (bn / 2) * kBK * 2; }
 // measurements of nine decode shapes at 1..8 splits (it picks the fastest
 // measured split for each).  Every wave of units streams each unit's weight
 // rows at min(60 GB/s per SM, 7.1 TB/s shared by the busy SMs) -- 60 GB/s is
-// about what one SM's MMAs consume, 4 KB of B per ~130-cycle tcgen05.mma of a
-// 128-row unit -- and every
-// split beyond the first costs about 4 us per wave (partial sums, arrival
-// counters and the combine).  GB3_SKINNY_SPLITS forces a split (tuning).
+// the measured rate of one SM streaming 128-row units through its MMAs and
+// barriers -- and every split beyond the first costs about 4 us per wave
+// (partial sums, arrival counters and the combine).  GB3_SKINNY_SPLITS forces
+// a split (tuning).
 // weights: weight matrices a unit streams (2 for gate/up).
 void choose_split(int64_t n_blocks, int64_t k_blocks, int sms, int* splits, int* kb_per,
                   int weights = 1) {

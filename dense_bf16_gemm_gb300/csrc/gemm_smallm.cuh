@@ -17,13 +17,15 @@
 // result does not depend on which CTA finishes last and no CTA waits for
 // another.
 //
-// Why this shape (measured on GB300): a tcgen05.mma of K = 16 occupies the
-// tensor pipe for about 130 cycles whatever its M (64 or 128) and N (16 to
-// 256), so a CTA can consume at most (weight bytes per MMA) / 130 cycles of
-// B: 32 GB/s with 64-row tiles, 65 GB/s with 128-row tiles.  HBM needs about
-// 45 GB/s from each of the 152 SMs, so the tiles are 128 rows and K is cut
-// wherever the tiles alone would leave SMs idle (a 64 x 8192 x 8192 problem
-// has 64 tiles for 152 SMs).
+// Why this shape (measured on GB300): one thread issues at most one
+// tcgen05.mma of K = 16 per ~65 cycles when N (the activation rows) is small,
+// and an M = 64 instruction takes as long as an M = 128 one, so a 128-row
+// weight tile gives each instruction twice the bytes of B of a 64-row tile;
+// each k-block also pays a barrier wait and a commit.  A 64-row kernel
+// streamed B at about 32 GB/s per CTA, the 128-row one at about 60 GB/s, and
+// HBM needs about 45 GB/s from each of the 152 SMs: so the tiles are 128
+// rows and K is cut wherever the tiles alone would leave SMs idle (a 64 x
+// 8192 x 8192 problem has 64 tiles for 152 SMs).
 //
 // Accumulator: D row i (weight row i of the tile) in TMEM lane i, activation
 // row m in column m, so epilogue warp w (lanes 32*(w%4)..+31) holds weight
