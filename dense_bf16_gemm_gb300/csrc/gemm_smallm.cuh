@@ -130,56 +130,6 @@ __device__ __forceinline__ void smallm_store_one(const SmallMParams& p, int b, i
   }
 }
 
-// C[m][n0..n0+3] of matrix b, the same values as four smallm_store_one calls.
-// Where all four exist and their address is aligned, one 8-byte (16-bit C) or
-// 16-byte (FP32 C) access: scattered 2-byte stores that each fill part of a
-// sector of a C not held in L2 were measured to cost about 18 us per call.
-__device__ __forceinline__ void smallm_store_four(const SmallMParams& p, int b, int m, int n0,
-                                                  float4 acc) {
-  const long long off = b * p.c_stride + static_cast<long long>(m) * p.ldc + n0;
-  const float a[4] = {acc.x, acc.y, acc.z, acc.w};
-  if (n0 + 3 < p.N) {
-    if (p.out_kind != 0) {
-      uint16_t* c = static_cast<uint16_t*>(p.C) + off;
-      if ((reinterpret_cast<uintptr_t>(c) & 7u) == 0) {
-        const bool f16 = p.out_kind == 2;
-        float v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(p.alpha, a[i]);
-        if (p.beta != 0.0f) {
-          const uint2 old = *reinterpret_cast<const uint2*>(c);
-          v[0] = __fmaf_rn(p.beta, half16_to_float(old.x & 0xFFFFu, f16), v[0]);
-          v[1] = __fmaf_rn(p.beta, half16_to_float(old.x >> 16, f16), v[1]);
-          v[2] = __fmaf_rn(p.beta, half16_to_float(old.y & 0xFFFFu, f16), v[2]);
-          v[3] = __fmaf_rn(p.beta, half16_to_float(old.y >> 16, f16), v[3]);
-        }
-        *reinterpret_cast<uint2*>(c) =
-            make_uint2(pack_half16x2(v[0], v[1], f16), pack_half16x2(v[2], v[3], f16));
-        return;
-      }
-    } else {
-      float* c = static_cast<float*>(p.C) + off;
-      if ((reinterpret_cast<uintptr_t>(c) & 15u) == 0) {
-        float v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(p.alpha, a[i]);
-        if (p.beta != 0.0f) {
-          const float4 old = *reinterpret_cast<const float4*>(c);
-          v[0] = __fmaf_rn(p.beta, old.x, v[0]);
-          v[1] = __fmaf_rn(p.beta, old.y, v[1]);
-          v[2] = __fmaf_rn(p.beta, old.z, v[2]);
-          v[3] = __fmaf_rn(p.beta, old.w, v[3]);
-        }
-        *reinterpret_cast<float4*>(c) = make_float4(v[0], v[1], v[2], v[3]);
-        return;
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    if (n0 + i < p.N) smallm_store_one(p, b, m, n0 + i, a[i]);
-}
-
 // Activation rows m0..m0+kCols-1 of output column n.
 template <int kCols>
 __device__ __forceinline__ void smallm_store(const SmallMParams& p, int b, int n, int m0,
@@ -208,42 +158,97 @@ __device__ __forceinline__ void smallm_touch_c(const SmallMParams& p, int b, int
     asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(x), "=r"(y), "=r"(z), "=r"(w)
                  : "l"(a));
+    asm volatile("" ::"r"(x), "r"(y), "r"(z), "r"(w));  // the values are not needed
   }
+}
+
+// C[m][n0..n0+CPT-1] of matrix b from the FP32 sums v (alpha, beta as in
+// smallm_store_one), written by one 16-byte store when all CPT columns exist
+// and the address is aligned: CPT = 8 for a 16-bit C, 4 for FP32 C.
+template <int CPT>
+__device__ __forceinline__ void smallm_store_run(const SmallMParams& p, int b, int m, int n0,
+                                                 const float (&v)[CPT]) {
+  const long long off = b * p.c_stride + static_cast<long long>(m) * p.ldc + n0;
+  if (n0 + CPT - 1 < p.N) {
+    const int es = p.out_kind != 0 ? 2 : 4;
+    void* c = static_cast<char*>(p.C) + off * es;
+    if ((reinterpret_cast<uintptr_t>(c) & 15u) == 0 && CPT * es == 16) {
+      float y[CPT];
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) y[i] = __fmul_rn(p.alpha, v[i]);
+      if constexpr (CPT == 8) {
+        const bool f16 = p.out_kind == 2;
+        if (p.beta != 0.0f) {
+          const uint4 old = *static_cast<const uint4*>(c);
+          const uint32_t w[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            y[2 * j] = __fmaf_rn(p.beta, half16_to_float(w[j] & 0xFFFFu, f16), y[2 * j]);
+            y[2 * j + 1] = __fmaf_rn(p.beta, half16_to_float(w[j] >> 16, f16), y[2 * j + 1]);
+          }
+        }
+        *static_cast<uint4*>(c) =
+            make_uint4(pack_half16x2(y[0], y[1], f16), pack_half16x2(y[2], y[3], f16),
+                       pack_half16x2(y[4], y[5], f16), pack_half16x2(y[6], y[7], f16));
+      } else {
+        if (p.beta != 0.0f) {
+          const float4 old = *static_cast<const float4*>(c);
+          y[0] = __fmaf_rn(p.beta, old.x, y[0]);
+          y[1] = __fmaf_rn(p.beta, old.y, y[1]);
+          y[2] = __fmaf_rn(p.beta, old.z, y[2]);
+          y[3] = __fmaf_rn(p.beta, old.w, y[3]);
+        }
+        *static_cast<float4*>(c) = make_float4(y[0], y[1], y[2], y[3]);
+      }
+      return;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < CPT; ++i)
+    if (n0 + i < p.N) smallm_store_one(p, b, m, n0 + i, v[i]);
 }
 
 // The combine of a shared tile by the 128 epilogue threads (tid 0..127): the
 // partials of pieces 0..pieces-1 (slot first + pc + tile, laid out [M][128])
-// are added in piece order and written to C.  16 threads cover one row of the
-// tile (8 consecutive outputs each), so every C row segment is written whole
-// and at once: per-warp 32-column slices written at different times were
+// are added in piece order and written to C.  128 / CPT threads cover one row
+// of the tile (CPT consecutive outputs each: 16 bytes of C), so every warp
+// store writes whole 32-byte sectors of C rows, and every C row segment is
+// written at once: per-warp 32-column slices written at different times were
 // measured to make the final stores of the call several times slower.  Each
 // thread issues the loads of 4 rows of a piece before adding them.
-__device__ __forceinline__ void smallm_combine_tile(const SmallMParams& p, int bt, int tile,
+template <int CPT>
+__device__ __forceinline__ void smallm_combine_rows(const SmallMParams& p, int bt, int tile,
                                                     int nb, int first, int pieces, int tid) {
-  const int cn = (tid & 15) * 8;  // first of 8 weight rows within the tile
+  constexpr int kTpr = kSmallRows / CPT;  // threads per row
+  constexpr int kRpp = 128 / kTpr;        // rows per pass of the 128 threads
+  constexpr int kV = CPT / 4;             // float4 per thread and row
+  const int cn = (tid % kTpr) * CPT;      // first weight row within the tile
   const int n0 = nb * kSmallRows + cn;
 #pragma unroll 1
-  for (int m0 = tid >> 4; m0 < p.M; m0 += 32) {
-    float4 sum[4][2];
+  for (int m0 = tid / kTpr; m0 < p.M; m0 += 4 * kRpp) {
+    float4 sum[4][kV];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) sum[k][0] = sum[k][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int h = 0; h < kV; ++h) sum[k][h] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll 1
     for (int pc = 0; pc < pieces; ++pc) {
       const float* base =
           p.ws + (static_cast<long long>(first + pc) + tile) * p.M * kSmallRows + cn;
-      float4 v[4][2];
+      float4 v[4][kV];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int m = m0 + 8 * k;
+        const int m = m0 + kRpp * k;
         const float4* src = reinterpret_cast<const float4*>(base + static_cast<long long>(m) * kSmallRows);
         const bool in = m < p.M;
-        v[k][0] = in ? __ldcg(src) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        v[k][1] = in ? __ldcg(src + 1) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int h = 0; h < kV; ++h)
+          v[k][h] = in ? __ldcg(src + h) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kV; ++h) {
           sum[k][h].x += v[k][h].x;
           sum[k][h].y += v[k][h].y;
           sum[k][h].z += v[k][h].z;
@@ -252,13 +257,28 @@ __device__ __forceinline__ void smallm_combine_tile(const SmallMParams& p, int b
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int m = m0 + 8 * k;
+      const int m = m0 + kRpp * k;
       if (m < p.M) {
-        smallm_store_four(p, bt, m, n0, sum[k][0]);
-        smallm_store_four(p, bt, m, n0 + 4, sum[k][1]);
+        float out[CPT];
+#pragma unroll
+        for (int h = 0; h < kV; ++h) {
+          out[4 * h + 0] = sum[k][h].x;
+          out[4 * h + 1] = sum[k][h].y;
+          out[4 * h + 2] = sum[k][h].z;
+          out[4 * h + 3] = sum[k][h].w;
+        }
+        smallm_store_run<CPT>(p, bt, m, n0, out);
       }
     }
   }
+}
+
+__device__ __forceinline__ void smallm_combine_tile(const SmallMParams& p, int bt, int tile,
+                                                    int nb, int first, int pieces, int tid) {
+  if (p.out_kind != 0)
+    smallm_combine_rows<8>(p, bt, tile, nb, first, pieces, tid);
+  else
+    smallm_combine_rows<4>(p, bt, tile, nb, first, pieces, tid);
 }
 
 template <int NX>
