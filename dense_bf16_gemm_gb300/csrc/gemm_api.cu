@@ -289,8 +289,22 @@ struct PairChoice {
   int extra = 0;         // clusters 0..extra-1 take one more
   int64_t units = 0;
   int max_pieces = 1;
-  int64_t unit_count() const { return balanced ? units : full + (tiles - full) * split; }
+  // Strips: the last strip_tiles tiles run as 256 / kPairStripN strips each.
+  int64_t strip_tiles = 0;
+  int64_t unit_count() const {
+    if (balanced) return units;
+    if (strip_tiles > 0) return tiles - strip_tiles + strip_tiles * (256 / kPairStripN);
+    return full + (tiles - full) * split;
+  }
 };
+
+// Time of a wave of kPairStripN-column strips of 256-column pair tiles, in
+// waves of whole tiles of the same K.  A strip streams all of A's k-blocks
+// but a quarter of B's (20 of 32 KB per CTA and k-block).  Measured on GB300
+// at 3000 x 5000 x 2000 (32 k-blocks, 12 tail tiles as 48 strips): 55.6 us
+// against 57.9 us for four waves of 224-wide tiles, i.e. (3 + 0.63) x 576
+// against 4 x 544 in the width-weighted wave model.
+constexpr double kStripWave = 0.63;
 
 // The balanced division of `tiles` pair tiles of `k_blocks` k-blocks over
 // `slots` clusters.
@@ -359,6 +373,7 @@ void plan_tail(int64_t tiles, int64_t k_blocks, int slots, bool allow_split, Pai
 // counts 1/split of a wave, the balanced division its longest range in
 // tiles; either adds a charge for its partial sums.
 double pair_waves(const PairChoice& c, int64_t k_blocks, int slots) {
+  if (c.strip_tiles > 0) return static_cast<double>((c.tiles - c.strip_tiles) / slots) + kStripWave;
   if (c.balanced) {
     const double w = static_cast<double>(ceil_div(c.tiles * k_blocks, slots)) / k_blocks;
     return w + (c.max_pieces > 1 ? kSplitCharge : 0.0);
@@ -369,13 +384,31 @@ double pair_waves(const PairChoice& c, int64_t k_blocks, int slots) {
   return waves;
 }
 
-// The division of `tiles` pair tiles of one width: the tail split, or the
-// balanced division where it is enabled and applies.
+// The division of `tiles` pair tiles of one width: the tail split; for
+// 256-column tiles whose partial last wave cannot be split along K (pieces
+// would be shorter than kMinPieceKb), strips of that wave's tiles along N
+// when they fit on the resident pairs (GB3_GEMM_STRIPS = 0 turns them off,
+// 1 takes them wherever they apply); or the balanced division where it is
+// enabled and applies.
 PairChoice choose_pair_division(int64_t tiles, int64_t k_blocks, int slots, bool allow_split,
-                                int bn) {
+                                int bn, bool allow_strips = false) {
   PairChoice c;
   c.bn = bn;
   plan_tail(tiles, k_blocks, slots, allow_split, &c);
+  const int64_t tail = tiles % slots;
+  const int strips_env = env_int("GB3_GEMM_STRIPS", -1);
+  if (allow_strips && allow_split && bn == 256 && strips_env != 0 && tail > 0 &&
+      tail * (256 / kPairStripN) <= slots && env_int("GB3_GEMM_SPLIT_ALL", 0) <= 1 &&
+      (c.split == 1 || strips_env == 1)) {
+    PairChoice st;
+    st.bn = bn;
+    st.tiles = tiles;
+    st.full = tiles;
+    st.split = 1;
+    st.kb_per_piece = static_cast<int>(k_blocks);
+    st.strip_tiles = tail;
+    if (strips_env == 1 || pair_waves(st, k_blocks, slots) < pair_waves(c, k_blocks, slots)) c = st;
+  }
   const int mode = balanced_mode();
   if (!allow_split || mode == 0 || tiles < slots) return c;
   PairChoice b;
@@ -387,7 +420,7 @@ PairChoice choose_pair_division(int64_t tiles, int64_t k_blocks, int slots, bool
 // Tile width of the CTA-pair GEMM and its division: the fewest waves of pair
 // tiles weighted by the time a wave of that width takes.
 PairChoice choose_pair(int64_t batch, int64_t M, int64_t N, int64_t K, int slots,
-                       bool allow_split) {
+                       bool allow_split, bool allow_strips = false) {
   PairChoice best;
   double best_cost = 1e300;
   const int64_t mb = ceil_div(M, kPairBM);
@@ -399,7 +432,8 @@ PairChoice choose_pair(int64_t batch, int64_t M, int64_t N, int64_t K, int slots
   for (int bn : kPairWidths) forced_valid |= (bn == forced);
   for (int bn : kPairWidths) {
     if (forced_valid && bn != forced) continue;
-    PairChoice c = choose_pair_division(batch * mb * ceil_div(N, bn), kb, slots, allow_split, bn);
+    PairChoice c =
+        choose_pair_division(batch * mb * ceil_div(N, bn), kb, slots, allow_split, bn, allow_strips);
     // Measured on GB300 (8192^3): a wave of 256-wide pair tiles takes 1.057x
     // the time of 224-wide ones for 1.143x the work, i.e. time ~ width + 320.
     const double cost = pair_waves(c, kb, slots) * static_cast<double>(bn + kWidthCostOffset);
@@ -486,7 +520,7 @@ int plan_gemm(int64_t batch, int64_t M, int64_t N, int64_t K, int sms, gemm_plan
   if (M <= kSkinnyMaxM && !row_stats) return plan_skinny(batch, M, N, K, sms, pl);
   if (M >= kPairMinM && pair_slots >= 0) {
     const int slots = pair_slots > 0 ? pair_slots : std::max(1, sms / 2);
-    const PairChoice c = choose_pair(batch, M, N, K, slots, allow_split);
+    const PairChoice c = choose_pair(batch, M, N, K, slots, allow_split, !row_stats);
     const int64_t units = c.unit_count();
     pl->kernel = K_PAIR;
     pl->tile_m = kPairBM;
@@ -1111,6 +1145,8 @@ TileParams tile_params(const Problem& q, int tile_m, int tile_n_out, uint32_t id
   p.balanced = 0;
   p.work_per_cluster = 0;
   p.work_extra = 0;
+  p.strip_tiles = 0;
+  p.idesc_strip = idesc_f32_acc(kPairBM, kPairStripN, q.in_dtype == GEMM_IN_F16);
   p.ws = nullptr;
   p.counters = nullptr;
   return p;
@@ -1125,7 +1161,7 @@ void pair_units(int dev, gemm_plan* pl, const Problem& q, int out_cols, TilePara
   if (gate_up) {
     c = choose_pair_division(p->num_tiles, p->k_blocks, slots, true, 256);
   } else {
-    c = choose_pair(q.batch, q.M, q.N, q.K, slots, true);
+    c = choose_pair(q.batch, q.M, q.N, q.K, slots, true, !q.stats());
   }
   (void)out_cols;
   if (pair_workspace_bytes(c, slots) > 0) {
@@ -1157,6 +1193,7 @@ void pair_units(int dev, gemm_plan* pl, const Problem& q, int out_cols, TilePara
   p->balanced = c.balanced ? 1 : 0;
   p->work_per_cluster = c.per;
   p->work_extra = c.extra;
+  p->strip_tiles = static_cast<int>(c.strip_tiles);
 }
 
 // RING: C is read through the deeper staging ring (beta != 0), which takes
@@ -1212,6 +1249,12 @@ int run_pair(gemm_plan& pl, int dev, int slots, const Problem& q, cudaStream_t s
   if ((st = attach_row_stats(dev, q, p.n_blocks, &rs, stream)) != GEMM_OK) return st;
   pair_units(dev, &pl, q, bn, &p, stream, false, slots);
   if (bn != 256 && bn != 224) return GEMM_ERR_UNSUPPORTED;
+  // Strip units load kPairStripN / 2 rows of B per CTA.
+  CUtensorMap tmBs = tmB;
+  if (p.strip_tiles > 0 &&
+      (st = operand_map(&tmBs, q.B, q.in_dtype, q.K, q.N, q.batch, q.ldb, q.sb,
+                        kPairStripN / 2)) != GEMM_OK)
+    return st;
   // The ring kernels always read C.
   const bool ring = pair_reads_c_ring(q.beta);
   if (ring) {
@@ -1222,8 +1265,8 @@ int run_pair(gemm_plan& pl, int dev, int slots, const Problem& q, cudaStream_t s
                   (bn == 224 ? 8 : 0);
 #define GB3_PAIR_CASE(S, BN_, EPI_, STATS_, RING_)                                              \
   case S:                                                                                       \
-    return launch_pair_gemm<BN_, EPI_, STATS_, RING_>(pl, dev, tmA, tmB, tmB, tmOut, p, stream, \
-                                                      rs);
+    return launch_pair_gemm<BN_, EPI_, STATS_, RING_>(pl, dev, tmA, tmB, tmBs, tmOut, p,      \
+                                                      stream, rs);
   switch (sel) {
     GB3_PAIR_CASE(0, 256, EPI_BF16, false, false)
     GB3_PAIR_CASE(1, 256, EPI_F32, false, false)

@@ -166,15 +166,24 @@ struct TileParams {
   int balanced;
   long long work_per_cluster;
   int work_extra;
+  // Strips (CTA-pair kernels of 256-column tiles, strip_tiles > 0): the last
+  // strip_tiles tiles run as kPairStripN-column strips of the whole K, one
+  // unit each, after every whole tile; num_full = num_tiles - strip_tiles and
+  // tail_split = 1.  A strip needs no partial sums.
+  int strip_tiles;
+  uint32_t idesc_strip;       // tcgen05 instruction descriptor of a strip (N = kPairStripN)
   float* ws;          // FP32 partial tiles of split pieces
   int* counters;      // arrivals per (split tile, 32-row band), zero between calls
 };
 
 // One unit of a cluster's work: k-blocks kb0..kb1-1 of tile `tile`, piece
-// `piece` of `pieces` (pieces == 1: the whole tile, piece 0).
+// `piece` of `pieces` (pieces == 1: the whole tile, piece 0); strip >= 0: the
+// unit is that kPairStripN-column strip of the tile (all of K).
 struct WorkUnit {
-  int tile, kb0, kb1, piece, pieces;
+  int tile, kb0, kb1, piece, pieces, strip;
 };
+
+constexpr int kPairStripN = 64;   // columns of a strip of a 256-column pair tile
 
 // Reductions along each row of the result (kernels instantiated with STATS):
 // the sum, maximum and minimum over n of the FP32 values alpha*acc + beta*c,
@@ -271,6 +280,7 @@ __host__ __device__ __forceinline__ WorkUnit balanced_unit(long long per, int ex
   const long long f0 = static_cast<long long>(t) * k_blocks;
   WorkUnit u;
   u.tile = t;
+  u.strip = -1;
   u.kb0 = static_cast<int>((r0 > f0 ? r0 : f0) - f0);
   u.kb1 = static_cast<int>((r1 < f0 + k_blocks ? r1 : f0 + k_blocks) - f0);
   const int c0 = balanced_owner(per, extra, f0);
@@ -310,6 +320,24 @@ __device__ __forceinline__ WorkUnit cluster_unit(const TileParams& p, int cluste
                                                  int i) {
   if (p.balanced) return balanced_unit(p.work_per_cluster, p.work_extra, p.k_blocks, cluster, i);
   WorkUnit u;
+  u.strip = -1;
+  if (p.strip_tiles > 0) {
+    // whole tiles first, then the strips of the last strip_tiles tiles
+    const int v = cluster + i * nclusters;
+    const int whole = p.num_tiles - p.strip_tiles;
+    u.kb0 = 0;
+    u.kb1 = p.k_blocks;
+    u.piece = 0;
+    u.pieces = 1;
+    if (v < whole) {
+      u.tile = v;
+    } else {
+      constexpr int kStrips = 256 / kPairStripN;
+      u.tile = whole + (v - whole) / kStrips;
+      u.strip = (v - whole) % kStrips;
+    }
+    return u;
+  }
   unit_of(cluster + i * nclusters, p, u.tile, u.kb0, u.kb1, u.piece);
   u.pieces = u.piece < 0 ? 1 : p.tail_split;
   if (u.piece < 0) u.piece = 0;
@@ -654,11 +682,14 @@ __host__ __device__ __forceinline__ uint32_t staging_offset(int row, uint32_t ch
 // that no contraction choice of the compiler differs between the epilogues
 // of the different kernels.
 // STATS: also reduce each row (sum, max, min) into p's row-statistics outputs.
+// cols: the output columns computed, a multiple of the box width up to the
+// tile's (a strip of a pair tile: its first cols accumulator columns).
 template <int BN, int EPI, bool STATS = false>
 __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtensorMap* tmOut,
                                               uint32_t tacc, int b, int m0, int n0,
                                               uint32_t staging, int lane, int& sc, bool have_acc,
-                                              const SplitCtx& split, const RowStatsParams& rs) {
+                                              const SplitCtx& split, const RowStatsParams& rs,
+                                              int cols = (EPI == EPI_GATE_UP) ? BN / 2 : BN) {
   constexpr int OUT = (EPI == EPI_GATE_UP) ? BN / 2 : BN;
   using Box = EpiBox<EPI, OUT>;
   constexpr int kSub = Box::kCols / 32;  // 32-column slices per box
@@ -672,7 +703,7 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
   float c_next[32];
   if (read_c) load_c_slice<EPI>(c_next, p, b, row, n0);
 #pragma unroll 1
-  for (int c0 = 0; c0 < OUT; c0 += Box::kCols) {
+  for (int c0 = 0; c0 < cols; c0 += Box::kCols) {
     // Boxes wholly outside C are neither computed nor stored (warp-uniform).
     if (m0 >= p.M || n0 + c0 >= p.N) continue;
     const uint32_t stg = staging + (sc & 1) * kStageBox;
@@ -698,7 +729,7 @@ __device__ __forceinline__ void epilogue_tile(const TileParams& p, const CUtenso
 #pragma unroll
           for (int i = 0; i < 32; ++i) c_cur[i] = c_next[i];
           const int next = c0 + 32 * (h + 1);
-          if (next < OUT) load_c_slice<EPI>(c_next, p, b, row, n0 + next);
+          if (next < cols) load_c_slice<EPI>(c_next, p, b, row, n0 + next);
         }
         if (have_acc) {
           acc_slice(v, tacc, c0 + 32 * h, lane, split);
@@ -774,7 +805,8 @@ __device__ __forceinline__ bool epilogue_tile_ring(const TileParams& p, const CU
                                                    long long& r, long long& issued, int& sc,
                                                    const SplitCtx& split,
                                                    const RowStatsParams& rs,
-                                                   volatile int* abort_flag, TopUp&& topup) {
+                                                   volatile int* abort_flag, TopUp&& topup,
+                                                   int cols = BN) {
   static_assert(EPI != EPI_GATE_UP, "the gate/up epilogue reads no C");
   using Box = EpiBox<EPI, BN>;
   constexpr int kSub = Box::kCols / 32;
@@ -785,7 +817,7 @@ __device__ __forceinline__ bool epilogue_tile_ring(const TileParams& p, const CU
   // one computed, starting once every earlier store has read its slot.
   const long long r0 = r;
   const int nbox = (m0 < p.M && n0 < p.N)
-                       ? (min(BN, p.N - n0) + Box::kCols - 1) / Box::kCols
+                       ? (min(cols, p.N - n0) + Box::kCols - 1) / Box::kCols
                        : 0;
   auto load_box = [&](int j) {  // lane 0: box j of this tile into its slot
     const int sl = static_cast<int>((r0 + j) % kRingSlots);
@@ -801,7 +833,7 @@ __device__ __forceinline__ bool epilogue_tile_ring(const TileParams& p, const CU
     issued = r0 + first;
   }
 #pragma unroll 1
-  for (int c0 = 0; c0 < BN; c0 += Box::kCols) {
+  for (int c0 = 0; c0 < cols; c0 += Box::kCols) {
     if (m0 >= p.M || n0 + c0 >= p.N) continue;
     const int slot = static_cast<int>(r % kRingSlots);
     const uint32_t stg = ring + slot * kStageBox;

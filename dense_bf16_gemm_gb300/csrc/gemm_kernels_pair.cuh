@@ -108,6 +108,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const RowStatsParams rs, const NormParams nrm) {
   using Cfg = PairCfg<BN, STAGES, EPI, RING>;
   static_assert(NORM == 0 || EPI == EPI_GATE_UP, "the normalised activation feeds gate/up");
+  // Strip units (TileParams::strip_tiles) exist only for plain GEMMs of 256-column
+  // tiles; each CTA then loads kPairStripN / 2 rows of B through tmB2.
+  constexpr bool kStrips = BN == 256 && EPI != EPI_GATE_UP && !STATS;
+  constexpr int kStripBBytes = (kPairStripN / 2) * kBK * 2;
   if (!launch_smem_ok(Cfg::kSmemBytes)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -256,13 +260,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_dst = sbase + s * Cfg::kStageBytes;
           const uint32_t b_dst = a_dst + Cfg::kABytes;
           const uint32_t fbar = full0_even + 8u * s;
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * Cfg::kStageBytes);
+          const bool strip = kStrips && un.strip >= 0;
+          if (rank == 0)
+            mbar_arrive_expect_tx(full_bar(s), strip ? 2 * (Cfg::kABytes + kStripBBytes)
+                                                     : 2 * Cfg::kStageBytes);
           tma_load_3d_pair(a_dst, &tmA, fbar, kb * kBK, a_row, bt);
           if constexpr (EPI == EPI_GATE_UP) {
             tma_load_3d_pair(b_dst, rank == 0 ? &tmB : &tmB2, fbar, kb * kBK, nb * (BN / 2), bt);
           } else {
-            tma_load_3d_pair(b_dst, &tmB, fbar, kb * kBK,
-                             nb * BN + static_cast<int>(rank) * (BN / 2), bt);
+            if (strip)
+              tma_load_3d_pair(b_dst, &tmB2, fbar, kb * kBK,
+                               nb * BN + un.strip * kPairStripN +
+                                   static_cast<int>(rank) * (kPairStripN / 2),
+                               bt);
+            else
+              tma_load_3d_pair(b_dst, &tmB, fbar, kb * kBK,
+                               nb * BN + static_cast<int>(rank) * (BN / 2), bt);
           }
           ++issued;
           if (++s == STAGES) {
@@ -294,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bounded_cluster(acce_bar(buf), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
+        const uint32_t idesc = (kStrips && un.strip >= 0) ? p.idesc_strip : p.idesc;
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (!wait_bounded(full_bar(s), ph, abort_flag, SITE_MMA_FULL)) {
             ok = false;
@@ -305,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bdesc = smem_desc_sw128(a_addr + Cfg::kABytes);
 #pragma unroll
           for (int j = 0; j < kBK / kUmmaK; ++j)
-            umma_bf16_pair(d_tmem, adesc + 2u * j, bdesc + 2u * j, p.idesc,
+            umma_bf16_pair(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc,
                            (kb != un.kb0 || j != 0) ? 1u : 0u);
           umma_commit_pair_multicast(empty_bar(s), 0x3);
           if (++s == STAGES) {
@@ -336,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool cursor_started = false;
     const uint32_t cbar0 = drain_bar + 8u * (1 + ew * kRingSlots);
     long long r_done = 0, r_issued = 0;
-    int cu = nunits, cc0 = 0, cb = 0, cm0 = 0, cn0 = 0;
+    int cu = nunits, cc0 = 0, cb = 0, cm0 = 0, cn0 = 0, cw = Cfg::kOutCols;
     auto cursor_at = [&](int i) {  // onto this cluster's unit i
       cu = i;
       cc0 = 0;
@@ -345,12 +359,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mb_, nb_;
         tile_coords(cun.tile, p, cb, mb_, nb_);
         cm0 = mb_ * kPairBM + static_cast<int>(rank) * 128 + band;
-        cn0 = nb_ * Cfg::kOutCols;
+        const bool strip = kStrips && cun.strip >= 0;
+        cn0 = strip ? nb_ * BN + cun.strip * kPairStripN : nb_ * Cfg::kOutCols;
+        cw = strip ? kPairStripN : Cfg::kOutCols;
       }
     };
     auto cursor_settle = [&]() {  // onto the next box inside C, or past the last unit
       while (cu < nunits) {
-        if (cc0 < Cfg::kOutCols && cm0 < p.M && cn0 + cc0 < p.N) return;
+        if (cc0 < cw && cm0 < p.M && cn0 + cc0 < p.N) return;
         cursor_at(cu + 1);
       }
     };
@@ -389,7 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tacc = tmem_addr(tmem_base, static_cast<uint32_t>(band),
                                       static_cast<uint32_t>(buf * Cfg::kAccStride));
       const int m0 = mb * kPairBM + static_cast<int>(rank) * 128 + band;
-      const int n0 = nb * Cfg::kOutCols;
+      const bool strip = kStrips && un.strip >= 0;
+      const int n0 = strip ? nb * BN + un.strip * kPairStripN : nb * Cfg::kOutCols;
       SplitCtx split{1, 0, nullptr, nullptr, 0};
       bool store = true;
       if (un.pieces > 1) {
@@ -428,12 +445,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           split = SplitCtx{1, 0, nullptr, nullptr, 0};
         }
       }
+      // A strip computes the first kPairStripN columns of its accumulator.
+      const int cols = strip ? kPairStripN : Cfg::kOutCols;
       if constexpr (RING) {
         bool ok = true;
         if (un.pieces == 1)
           ok = epilogue_tile_ring<BN, EPI, STATS, false>(p, &tmOut, tacc, bt, m0, n0, staging,
                                                          cbar0, lane, r_done, r_issued, sc, split,
-                                                         rs, abort_flag, topup);
+                                                         rs, abort_flag, topup, cols);
         else if (store)
           ok = epilogue_tile_ring<BN, EPI, STATS, true>(p, &tmOut, tacc, bt, m0, n0, staging,
                                                         cbar0, lane, r_done, r_issued, sc, split,
@@ -442,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         if (store)
           epilogue_tile<BN, EPI, STATS>(p, &tmOut, tacc, bt, m0, n0, staging, lane, sc,
-                                        un.kb1 > un.kb0, split, rs);
+                                        un.kb1 > un.kb0, split, rs, cols);
       }
       tc_fence_before_sync();
       __syncwarp();

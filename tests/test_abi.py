@@ -118,10 +118,12 @@ def balanced_division(tiles, kb, slots):
     return units, max(len(v) for v in owners.values()), -(-work // slots)
 
 
-def pair_model(M, N, K, slots=76, widths=(256, 224), balanced=False):
+def pair_model(M, N, K, slots=76, widths=(256, 224), balanced=False, strips=True):
     """Restatement of the planner's rule: fewest waves (a split tail wave counts
-    1/split + 0.1; with the balanced division enabled, that division where it
-    applies, counting its longest range in tiles + 0.1 when a tile is cut)
+    1/split + 0.1; a tail wave of 256-wide tiles that is not split along K and
+    whose tiles, cut into four 64-column strips, fit on the pairs counts 0.63
+    when that is fewer; with the balanced division enabled, that division where
+    it applies, counting its longest range in tiles + 0.1 when a tile is cut)
     weighted by width + 320.  Returns (width, most pieces of a tile, units,
     balanced)."""
     best = None
@@ -139,6 +141,10 @@ def pair_model(M, N, K, slots=76, widths=(256, 224), balanced=False):
             full = tiles
         waves = full // slots + ((1 / split + 0.1) if split > 1 else (1 if tiles - full // slots * slots else 0))
         cand = (bn, split, full + (tiles - full) * split, False)
+        if strips and bn == 256 and tail and split == 1 and 4 * tail <= slots:
+            if tiles // slots + 0.63 < waves:
+                waves = tiles // slots + 0.63
+                cand = (bn, 1, tiles - tail + 4 * tail, False)
         if balanced and tiles >= slots:
             units, pieces, longest = balanced_division(tiles, kb, slots)
             waves = longest / kb + (0.1 if pieces > 1 else 0.0)
@@ -186,6 +192,39 @@ def test_plan_pair_matches_wave_model(lib, M, N, K):
     assert st == 0 and d["kernel_name"] == "pair"
     bn, split, units, _ = pair_model(M, N, K)
     assert (d["tile_n"], d["split_k"], d["tiles"]) == (bn, split, units)
+
+
+def test_plan_strips_cut_the_unsplit_tail_wave(lib, monkeypatch):
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "0")
+    # 3000 x 5000 x 2000: 12 x 20 = 240 tiles of 256 columns, 3 waves on 76
+    # pairs and 12 left; 32 k-blocks cannot be cut into two pieces of 24, so
+    # the 12 tiles run as 48 strips of 64 columns (3.63 waves x 576 against 4
+    # waves of 224-wide tiles x 544)
+    st, p = _native.gemm_bf16_plan(3000, 5000, 2000, _native.GEMM_OUT_F32, 152)
+    assert st == 0
+    assert (p.tile_n, p.split_k, p.tiles, p.grid) == (256, 1, 228 + 48, 152)
+    monkeypatch.setenv("GB3_GEMM_STRIPS", "0")
+    st, p = _native.gemm_bf16_plan(3000, 5000, 2000, _native.GEMM_OUT_F32, 152)
+    assert (p.tile_n, p.split_k, p.tiles) == (224, 1, 276)
+    # a tail that a K split serves keeps the split (4096^3: 28 tiles x 2 pieces)
+    monkeypatch.delenv("GB3_GEMM_STRIPS")
+    st, p = _native.gemm_bf16_plan(4096, 4096, 4096, _native.GEMM_OUT_BF16, 152)
+    assert (p.tile_n, p.split_k, p.tiles) == (256, 2, 228 + 56)
+    # forced: strips wherever the tail fits, also in place of a K split
+    monkeypatch.setenv("GB3_GEMM_STRIPS", "1")
+    monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", "256")
+    st, p = _native.gemm_bf16_plan(2304, 4136, 4096, _native.GEMM_OUT_BF16, 152)
+    assert (p.split_k, p.tiles) == (1, 153 - 1 + 4)
+    # too many tail tiles for the pairs: 28 x 4 > 76
+    st, p = _native.gemm_bf16_plan(4096, 4096, 2048, _native.GEMM_OUT_BF16, 152)
+    assert (p.split_k, p.tiles) == (1, 256)
+
+
+def test_plan_strips_not_with_row_stats(lib, monkeypatch):
+    # the row-statistics kernels have no strip units: whole tiles only
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "0")
+    st, p = _native.gemm_row_stats_plan(1, 3000, 5000, 2000, 0, _native.GEMM_OUT_F32, 152)
+    assert st == 0 and (p.tile_n, p.tiles) == (224, 276)
 
 
 def test_plan_tail_split_pieces_are_long_enough(lib, monkeypatch):
@@ -238,9 +277,13 @@ def test_plan_ragged_tiles_cover_the_output(lib):
     assert st == 0
     d = p.as_dict()
     tiles = -(-3000 // d["tile_m"]) * -(-5000 // d["tile_n"])
-    # units: whole tiles plus split pieces of the tail tiles; every tile is covered
-    whole = tiles - (tiles % 76 if d["split_k"] > 1 else 0)
-    assert d["tiles"] == whole + (tiles - whole) * d["split_k"]
+    # units: whole tiles plus the split pieces, or the four 64-column strips,
+    # of the tail tiles; every tile is covered
+    tail = tiles % 76
+    if d["split_k"] > 1:
+        assert d["tiles"] == tiles - tail + tail * d["split_k"]
+    else:
+        assert d["tile_n"] == 256 and d["tiles"] == tiles - tail + tail * 4
 
 
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (3000, 5000, 2000), (8192, 8192, 8192),
@@ -412,11 +455,16 @@ def test_row_stats_plans():
     assert row_stats_plan(16, 28672, 8192)["kernel_name"] == "tiled"
     assert _native.gemm_batched_plan(1, 16, 28672, 8192, 0, BF16, 148)[1].as_dict()[
         "kernel_name"] == "skinny_splitk"
-    # above M = 128 the same plan as the plain GEMM
+    # above M = 128 the same plan as the plain GEMM, except that the tail
+    # wave is never cut into strips (the row-statistics kernels have none)
     for shape in [(300, 520, 200), (4096, 4096, 4096), (3000, 5000, 2000)]:
         a = row_stats_plan(*shape)
         b = _native.gemm_batched_plan(1, *shape, 0, BF16, 148)[1].as_dict()
-        assert a == b
+        tiles = -(-shape[0] // 256) * -(-shape[1] // b["tile_n"])
+        if b["tile_n"] == 256 and b["split_k"] == 1 and b["tiles"] > tiles:
+            assert a["tiles"] == -(-shape[0] // 256) * -(-shape[1] // a["tile_n"])
+        else:
+            assert a == b
     # K == 0: the reductions of beta*C, then the scaling of C
     k0 = row_stats_plan(64, 64, 0)
     assert k0["kernel_name"] == "scale" and k0["launches"] == 2

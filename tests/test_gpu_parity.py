@@ -811,3 +811,87 @@ def test_balanced_division_row_stats(g, monkeypatch):
     assert np.array_equal(to_f64(rmax), ref["max"])
     assert np.array_equal(to_f64(rmin), ref["min"])
     assert_status_ok(g)
+
+
+# ---------------------------------------------------------------------------
+# strips: the tail wave's 256-column tiles cut along N into four 64-column
+# strips of the whole K (an MMA of N = 64 per strip, its own B boxes of 32
+# rows per CTA, and the epilogue over its 64 columns).
+# ---------------------------------------------------------------------------
+STRIP_SHAPES = [
+    (300, 520, 200),     # 6 tiles, 24 strips; of the last column block only strip 0 is inside C
+    (1000, 712, 1000),   # 12 tiles, 48 strips
+    (256, 256, 8),       # one tile, K below one k-block
+    (3000, 5000, 264),   # 240 tiles: 3 waves, then 12 tiles as 48 strips; a K tail
+    (2304, 4136, 200),   # 153 tiles: 2 waves, then 1 tile (its N ragged) as 4 strips
+]
+
+
+def strips_planned(p, M, N):
+    tiles = -(-M // 256) * -(-N // 256)
+    return p["tile_n"] == 256 and p["split_k"] == 1 and p["tiles"] > tiles and \
+        (p["tiles"] - tiles) % 3 == 0
+
+
+@pytest.mark.parametrize("M,N,K", STRIP_SHAPES)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("beta", [0.0, -0.5])
+def test_strips_bit_exact(g, monkeypatch, M, N, K, out_dtype, beta):
+    monkeypatch.setenv("GB3_GEMM_STRIPS", "1")
+    monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", "256")
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "0")
+    p = g.plan(M, N, K, out_dtype)
+    assert p["kernel_name"] == "pair" and strips_planned(p, M, N), p
+    A, B, C = int_inputs(M, N, K, seed=M + 2 * N + K)
+    Cq = C.to(out_dtype) if beta != 0.0 else None
+    ref, _ = oracle.gemm_full(A, B, alpha=2.0, beta=beta,
+                              C=Cq.to(torch.float32) if Cq is not None else None)
+    want = ref if out_dtype == torch.float32 else oracle.round_to_bf16_bits(ref)
+    out = run_gemm(g, A, B, C=Cq, alpha=2.0, beta=beta, out_dtype=out_dtype)
+    got = to_f64(out) if out_dtype == torch.float32 else bits(out.cpu())
+    assert np.array_equal(got, want)
+    assert_status_ok(g)
+
+
+def test_strips_batched_f16(g, monkeypatch):
+    """Strips of tiles of different matrices of a batch, FP16 operands."""
+    monkeypatch.setenv("GB3_GEMM_STRIPS", "1")
+    monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", "256")
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "0")
+    batch, M, N, K = 2, 512, 1000, 200   # 2 x 2 x 4 = 16 tiles, all as strips
+    A, B, C = batched_int_inputs(batch, M, N, K, 85, torch.float16)
+    Cd = C.cuda()
+    g.gemm(A.cuda(), B.cuda(), Cd, alpha=2.0, beta=-0.5)
+    torch.cuda.synchronize()
+    for b in range(batch):
+        ref, _ = oracle.gemm_full(A[b], B[b], alpha=2.0, beta=-0.5, C=C[b])
+        assert np.array_equal(to_f64(Cd[b]), ref), b
+    assert_status_ok(g)
+
+
+def test_strips_random_inputs_match_whole_tiles(g, monkeypatch):
+    """The ragged workload (3000 x 5000 x 2000, alpha 0.5, beta 2, FP32 C) as
+    planned (strips of its 12 tail tiles): within the bound of the oracle on
+    sampled rows, identical from call to call, and identical to the same
+    tiles run whole (an element's sum over K does not depend on the MMA's N)."""
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "0")
+    M, N, K = 3000, 5000, 2000
+    A, B, C = workloads.gemm_inputs(M, N, K, 2, ("uniform",), ("uniform",), ("normal", 1.0))
+    Ad, Bd = A.cuda(), B.cuda()
+    assert strips_planned(g.plan(M, N, K, torch.float32), M, N)
+    outs = []
+    for strips in ("-1", "-1", "0"):
+        monkeypatch.setenv("GB3_GEMM_STRIPS", strips)
+        monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", "256")
+        Cd = C.cuda()
+        g.gemm(Ad, Bd, Cd, alpha=0.5, beta=2.0)
+        outs.append(Cd)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(outs[0], outs[2])
+    rows = np.random.default_rng(86).choice(M, 48, replace=False)
+    rr, cc = np.repeat(rows, N), np.tile(np.arange(N), rows.size)
+    ref, ab = oracle.gemm_entries(A, B, rr, cc, alpha=0.5, beta=2.0, C=C)
+    tol = oracle.gemm_tolerance(ref, ab, 0.5, 2.0, C.numpy()[rr, cc])
+    assert_within(to_f64(outs[0])[rr, cc], ref, tol, "strips")
+    assert_status_ok(g)
