@@ -4,43 +4,53 @@
 // and a running sum l kept across the key loop, s = dot_t(q, k) per key tile,
 // acc / l at the end).
 //
-// One CTA per (head, 128-row query block).  Per key block j of 128 keys:
+// One CTA per (head, 128-row query block).  The key blocks of 128 keys are
+// dealt to two independent flash loops ("chains"): the even blocks to chain
+// 0, the odd ones to chain 1.  Chain c owns a score buffer S_c and an output
+// accumulator O_c in Tensor Memory and keeps its own m_c and l_c.  Per key
+// block j of chain c = j % 2:
 //
-//   S_j = Q . K_j^T                tcgen05.mma M = 128, N = 128 over D, into one of two
-//                                  TMEM score buffers (K_j is K-major: D contiguous)
-//   m_j = max(m_{j-1}, rowmax S_j)  softmax warps: a query row is one TMEM lane, so the
-//   P_j = exp(S_j - m_j)            reduction is local to the threads of that lane (two
-//   l_j = l_{j-1} a_j + rowsum P_j  warps, half of the keys each); a_j = exp(m_{j-1} - m_j)
-//   O += P_j . V_j                 tcgen05.mma M = 128, N = D over the 128 keys into one
-//                                  FP32 accumulator in Tensor Memory, with P_j written as
-//                                  BF16 back into Tensor Memory (the A operand read from
-//                                  TMEM) and V_j the MN-major operand (D contiguous, as
-//                                  TMA loads it)
+//   S_c = Q . K_j^T                tcgen05.mma M = 128, N = 128 over D (K_j is K-major:
+//                                  D contiguous)
+//   m_c = max(m_c, rowmax S_c)     softmax warps of chain c: a query row is one TMEM lane
+//   P_j = exp(S_c - m_c)           and one thread, which holds all 128 scores of its row
+//   l_c = l_c a + rowsum P_j       (a = exp(m_old - m_new))
+//   O_c += P_j . V_j               tcgen05.mma M = 128, N = D over the 128 keys, P_j written
+//                                  as BF16 over S_c and read from Tensor Memory as the A
+//                                  operand, V_j the MN-major operand (D contiguous, as TMA
+//                                  loads it)
 //
-// and finally O / l.  Scores are handled in base-2 units (exp2 of
-// s * scale * log2 e), which is the same function.  Keys past Nk score -inf.
+// and at the end, with m = max(m_0, m_1),
+//   O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)):
+// the softmax sums over two disjoint key sets, each taken against its own
+// maximum, merged exactly up to rounding.  Scores are handled in base-2
+// units (exp2 of s * scale * log2 e), which is the same function.  Keys past
+// Nk score -inf.
 //
-// The running maximum is updated lazily: the m a row's probabilities are
+// Why two chains: a chain is serial -- its next scores overwrite the P that
+// its P.V product reads, so S_c for block j + 2 is issued only once
+// O_c += P_j . V_j has completed -- but the chains are independent, so the
+// tensor core works on one chain's products while the other chain's softmax
+// threads run, and every SM sub-partition has a warp of each chain to issue
+// from.  No value is exchanged between warps inside the loop.
+//
+// The running maximum is updated lazily: the m a chain's probabilities are
 // taken against moves only when a block's maximum exceeds it by more than
-// kAttnRescaleLog2 (so probabilities stay below 2^8 and l, O keep their
-// ratio), and only then is that row of O (and l) multiplied by a_j, in
-// Tensor Memory, after O += P_{j-1} . V_{j-1} has completed.  The result
-// O / l does not depend on which m was used.
+// kAttnRescaleLog2 (so probabilities stay below 2^8 and l_c, O_c keep their
+// ratio), and only then is that row of O_c (and l_c) multiplied by a, in
+// Tensor Memory.  O_c += P_{j-2} . V_{j-2} has completed by then: S_c for
+// block j was issued after it.
 //
-// Tensor Memory: three 128-column buffers, each holding S_j as FP32 and then,
-// in the first 32 columns of each half's 64, that half's P_j as packed BF16
-// (its scores are in registers by then); one D-column output accumulator.
-// A buffer is reused for S_{j+3} once O += P_j . V_j has completed (an MMA
-// is not ordered after an earlier one into another accumulator, so the
-// wait is needed; with three buffers it is almost never on the critical
-// path, and the tensor core runs S and P.V products back to back).
+// Tensor Memory (512 columns): S_0 at 0, S_1 at 128 (each 128 FP32 scores,
+// then P as packed BF16 in its first 64 columns); O_0 at 256, O_1 at 256 + D.
 //
-// Warp roles: warp 0 TMA (Q once, K_j and V_j through a ring), warp 1 MMA
-// issue and TMEM owner, warps 2-9 softmax and output (two warps per TMEM lane
-// quarter, each taking half of the keys of a block and half of the output
-// columns, so that two softmax warps share each SM sub-partition).  The MMA
-// warp issues S_{j+1} before P_j . V_j, so the tensor core works on the next
-// scores while the softmax threads finish the current block.
+// Warp roles: warp 0 TMA (Q once; K_j and V_j through separate rings, in the
+// order the MMAs take them), warp 1 MMA issue and TMEM owner, warps 2-5 the
+// softmax of chain 0 and warps 6-9 that of chain 1 (warp w serves TMEM lane
+// quarter w % 4).  The MMA thread polls the conditions of both chains and
+// issues whichever product is ready: the scores of block j once K_j has
+// landed and O_c += P_{j-2} . V_{j-2} has completed, the P.V of block j once
+// P_j is stored and V_j has landed.
 //
 // Every wait is bounded as in the GEMM kernels (status word, abort flag,
 // drained copies and MMAs, TMEM freed).
@@ -52,8 +62,8 @@ namespace gb3 {
 
 constexpr int kAttnBR = 128;   // query rows per CTA (the MMA's M)
 constexpr int kAttnBC = 128;   // keys per block
-constexpr int kAttnSoftWarps = 8;                          // two per TMEM lane quarter
-constexpr int kAttnSBufs = 3;                              // S/P buffers in Tensor Memory
+constexpr int kAttnChains = 2;                             // key blocks dealt even / odd
+constexpr int kAttnSoftWarps = 4 * kAttnChains;            // one per TMEM lane quarter and chain
 constexpr int kAttnThreads = 32 * (2 + kAttnSoftWarps);    // TMA, MMA, softmax
 constexpr float kAttnRescaleLog2 = 8.0f;  // lazy rescaling: probabilities stay below 2^8
 
@@ -73,26 +83,44 @@ struct AttnCfg {
   static_assert(D == 64 || D == 128, "head dimension");
   static constexpr int kChunks = D / 64;                 // 64-element swizzle rows per row
   static constexpr int kTileBytes = 128 * D * 2;         // Q, K_j or V_j (128 rows)
-  // Separate rings: a K slot frees when S_j has completed, a V slot when
-  // O += P_j . V_j has, so K can be fetched further ahead than V.
-  static constexpr int kKStages = D == 128 ? 3 : 4;
-  static constexpr int kVStages = D == 128 ? 2 : 4;
+  // Separate rings, each refilled as soon as a slot frees: a K slot when
+  // S_j has completed, a V slot when O_c += P_j . V_j has.
+  static constexpr int kKStages = D == 128 ? 3 : 6;
+  static constexpr int kVStages = D == 128 ? 3 : 6;
   static constexpr int kQOffset = 0;
   static constexpr int kKOffset = kTileBytes;
   static constexpr int kVOffset = kKOffset + kKStages * kTileBytes;
-  static constexpr int kRedOffset = kVOffset + kVStages * kTileBytes;  // [2][2][128] floats
-  static constexpr int kBarOffset = kRedOffset + 2 * 2 * kAttnBR * 4;
-  // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[3], p_full[3],
-  // o_done[3], drain, xchg[4]
+  // [2 values (m, l)][2 chains][128 rows] floats, exchanged once at the end,
+  // over Q (every MMA has completed by then)
+  static constexpr int kRedOffset = kQOffset;
+  static_assert(2 * kAttnChains * kAttnBR * 4 <= kTileBytes, "exchange area");
+  static constexpr int kBarOffset = kVOffset + kVStages * kTileBytes;
+  // Score buffers in Tensor Memory: block j's scores go to buffer j % kSBufs.
+  static constexpr int kSBufs = D == 128 ? 1 : 2;
+  // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_free[NS],
+  // s_full[2], p_full[2], o_done[2], drain, xchg[4]
   static constexpr int kNumBars =
-      1 + 2 * kKStages + 2 * kVStages + 3 * kAttnSBufs + 1 + 4;
+      1 + 2 * kKStages + 2 * kVStages + kSBufs + 3 * kAttnChains + 1 + 4;
   static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
-  static constexpr int kTmemCols = 512;                  // S/P: 3 x 128, O: D
+  // Tensor Memory columns: S_b (128 FP32 scores) at kSCol + 128 b; P_c (128
+  // BF16 probabilities, packed in pairs) at kPCol + 64 c; O_c at kOCol + D c.
+  static constexpr int kTmemCols = 512;
   static constexpr int kSCol = 0;
-  static constexpr int kOCol = kAttnSBufs * kAttnBC;
-  static_assert(kOCol + D <= kTmemCols, "Tensor Memory columns");
+  static constexpr int kPCol = kSBufs * kAttnBC;
+  static constexpr int kOCol = kPCol + kAttnChains * (kAttnBC / 2);
+  static_assert(kOCol + kAttnChains * D <= kTmemCols, "Tensor Memory columns");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
+
+// Two non-negative finite floats rounded to BF16 (to nearest, ties away from
+// zero: adding half a BF16 unit of the last place to the FP32 bit pattern
+// and keeping the upper 16 bits, which carries into the exponent where the
+// significand overflows), packed with the first in the low half.  Integer
+// arithmetic, so that the probabilities' conversion does not compete with
+// exp2 for the special-function unit.
+__device__ __forceinline__ uint32_t pack_bf16x2_nonneg(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo) + 0x8000u, __float_as_uint(hi) + 0x8000u, 0x7632);
+}
 
 // 2^x by the hardware's approximate exp2 (relative error about 2^-22;
 // results below the normal range flush to zero, exp2(-inf) = 0).
@@ -109,8 +137,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   using Cfg = AttnCfg<D>;
   constexpr int KS = Cfg::kKStages;
   constexpr int VS = Cfg::kVStages;
+  constexpr int NS = Cfg::kSBufs;
+  constexpr int NC = kAttnChains;
   constexpr int kChunkBytes = 128 * 128;  // one 64-element-wide swizzled chunk of 128 rows
-  constexpr int kHalfKeys = kAttnBC / 2;
   if (!launch_smem_ok(Cfg::kSmemBytes)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -122,22 +151,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   const uint32_t bar0 = smem_u32(bars);
   const uint32_t q_full = bar0;
-  // Ring and buffer barriers complete once per use; block j's use of a ring
-  // of R slots is j / R, so its phase parity is (j / R) & 1.
+  // A barrier that completes once per use of a set of R slots (a ring, the
+  // score buffers, a chain) completes for block j's use in phase j / R, of
+  // parity (j / R) & 1 (block j is use j / 2 of chain j % 2).  Each barrier
+  // has one waiting role, which waits for every one of its phases in turn,
+  // so a parity names one phase: the chain's own s_full, p_full and o_done
+  // (not the shared score buffer's) are what the softmax warps and the MMA
+  // thread wait on.
   auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
   auto k_empty = [&](int s) { return bar0 + 8u * (1 + KS + s); };
   auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * KS + s); };
   auto v_empty = [&](int s) { return bar0 + 8u * (1 + 2 * KS + VS + s); };
   constexpr int R0 = 1 + 2 * KS + 2 * VS;
-  constexpr int NB = kAttnSBufs;
-  auto s_full = [&](int b) { return bar0 + 8u * (R0 + b); };        // S_j in buffer b = j % NB
-  auto p_full = [&](int b) { return bar0 + 8u * (R0 + NB + b); };   // P_j written over it
-  // O += P_j . V_j done (buffer b's P read, O holds block j)
-  auto o_done = [&](int b) { return bar0 + 8u * (R0 + 2 * NB + b); };
-  const uint32_t drain_bar = bar0 + 8u * (R0 + 3 * NB);
-  auto xchg_bar = [&](int qtr) { return bar0 + 8u * (R0 + 3 * NB + 1 + qtr); };
+  auto s_free = [&](int b) { return bar0 + 8u * (R0 + b); };            // S_b read by the softmax
+  constexpr int R1 = R0 + NS;
+  auto s_full = [&](int c) { return bar0 + 8u * (R1 + c); };            // chain c's scores ready
+  auto p_full = [&](int c) { return bar0 + 8u * (R1 + NC + c); };       // P_j stored in P_c
+  auto o_done = [&](int c) { return bar0 + 8u * (R1 + 2 * NC + c); };   // O_c += P_j . V_j done
+  const uint32_t drain_bar = bar0 + 8u * (R1 + 3 * NC);                 // every MMA done
+  auto xchg_bar = [&](int qtr) { return bar0 + 8u * (R1 + 3 * NC + 1 + qtr); };
   auto parity = [](int j, int r) { return static_cast<uint32_t>(j / r) & 1u; };
-  auto use_parity = [&](int j) { return parity(j, NB); };
 
   const uint32_t q_smem = sb + Cfg::kQOffset;
   auto k_smem = [&](int s) { return sb + Cfg::kKOffset + static_cast<uint32_t>(s * Cfg::kTileBytes); };
@@ -159,13 +192,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
     }
-    for (int b = 0; b < NB; ++b) {
-      mbar_init(s_full(b), 1);
-      mbar_init(p_full(b), kAttnSoftWarps);
-      mbar_init(o_done(b), 1);
+    for (int b = 0; b < NS; ++b) mbar_init(s_free(b), 4);   // the block's chain's four warps
+    for (int c = 0; c < NC; ++c) {
+      mbar_init(s_full(c), 1);
+      mbar_init(p_full(c), 4);
+      mbar_init(o_done(c), 1);
     }
     mbar_init(drain_bar, 1);
-    for (int qtr = 0; qtr < 4; ++qtr) mbar_init(xchg_bar(qtr), 2);
+    for (int qtr = 0; qtr < 4; ++qtr) mbar_init(xchg_bar(qtr), NC);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmQ);
@@ -186,34 +220,39 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_arrive_expect_tx(q_full, Cfg::kTileBytes);
       for (int c = 0; c < Cfg::kChunks; ++c)
         tma_load_3d(q_smem + c * kChunkBytes, &tmQ, q_full, c * 64, qb * kAttnBR, h);
-      // Loads in the order the MMAs consume them: K_0, then K_{j+1} before V_j.
-      auto load_k = [&](int j) -> bool {
+      // K_j and V_j stream through their own rings, each refilled as soon
+      // as a slot frees, so a late V does not hold back the next K.
+      auto load_k = [&](int j) {
         const int s = j % KS;
-        if (!wait_bounded(k_empty(s), parity(j, KS) ^ 1u, abort_flag, SITE_PRODUCER_EMPTY))
-          return false;
         mbar_arrive_expect_tx(k_full(s), Cfg::kTileBytes);
         for (int c = 0; c < Cfg::kChunks; ++c)
           tma_load_3d(k_smem(s) + c * kChunkBytes, &tmK, k_full(s), c * 64, j * kAttnBC, h);
-        return true;
       };
-      auto load_v = [&](int j) -> bool {
+      auto load_v = [&](int j) {
         const int s = j % VS;
-        if (!wait_bounded(v_empty(s), parity(j, VS) ^ 1u, abort_flag, SITE_PRODUCER_EMPTY))
-          return false;
         mbar_arrive_expect_tx(v_full(s), Cfg::kTileBytes);
         for (int c = 0; c < Cfg::kChunks; ++c)
           tma_load_3d(v_smem(s) + c * kChunkBytes, &tmV, v_full(s), c * 64, j * kAttnBC, h);
-        return true;
       };
       int k_issued = 0, v_issued = 0;
-      if (n > 0 && load_k(0)) k_issued = 1;
-      for (int j = 0; j < n && k_issued == j + 1; ++j) {
-        if (j + 1 < n) {
-          if (!load_k(j + 1)) break;
-          ++k_issued;
+      IdleBound bound;
+      while (k_issued < n || v_issued < n) {
+        bool issued = false;
+        if (k_issued < n && mbar_test_wait(k_empty(k_issued % KS), parity(k_issued, KS) ^ 1u)) {
+          load_k(k_issued++);
+          issued = true;
         }
-        if (!load_v(j)) break;
-        ++v_issued;
+        if (v_issued < k_issued &&
+            mbar_test_wait(v_empty(v_issued % VS), parity(v_issued, VS) ^ 1u)) {
+          load_v(v_issued++);
+          issued = true;
+        }
+        if (issued) {
+          bound.progress();
+          continue;
+        }
+        if (bound.expired(abort_flag, SITE_PRODUCER_EMPTY)) break;
+        __nanosleep(20);
       }
       // Leave only when every issued copy has landed (bounded).
       wait_bounded(q_full, 0, nullptr, SITE_DRAIN);
@@ -224,130 +263,129 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // S_j = Q . K_j^T into buffer j % NB, once O += P_{j-NB} . V_{j-NB}
-      // (which read P_{j-NB} from that buffer) has completed.
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % KS, b = j % NB;
-        if (j >= NB && !wait_bounded(o_done(b), use_parity(j - NB), abort_flag, SITE_MMA_ACC_EMPTY))
-          return false;
-        if (!wait_bounded(k_full(s), parity(j, KS), abort_flag, SITE_MMA_FULL)) return false;
-        tc_fence_after_sync();
+      // S_b = Q . K_j^T for block j into score buffer b = j % NS; chain
+      // j % 2 is told on its own barrier.
+      auto issue_s = [&](int j) {
+        const int s = j % KS, b = j % NS;
         const uint32_t d = tmem_base + Cfg::kSCol + static_cast<uint32_t>(b * kAttnBC);
 #pragma unroll
-        for (int c = 0; c < Cfg::kChunks; ++c) {
-          const uint64_t qd = smem_desc_sw128(q_smem + c * kChunkBytes);
-          const uint64_t kd = smem_desc_sw128(k_smem(s) + c * kChunkBytes);
+        for (int ch = 0; ch < Cfg::kChunks; ++ch) {
+          const uint64_t qd = smem_desc_sw128(q_smem + ch * kChunkBytes);
+          const uint64_t kd = smem_desc_sw128(k_smem(s) + ch * kChunkBytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, qd + 2u * kk, kd + 2u * kk, p.idesc_s, (c | kk) != 0 ? 1u : 0u);
+            umma_bf16(d, qd + 2u * kk, kd + 2u * kk, p.idesc_s, (ch | kk) != 0 ? 1u : 0u);
         }
-        umma_commit(s_full(b));
+        umma_commit(s_full(j % NC));
         umma_commit(k_empty(s));
-        return true;
       };
-      bool ok = wait_bounded(q_full, 0, abort_flag, SITE_MMA_FULL) && n > 0 && issue_s(0);
-      for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n && !issue_s(j + 1)) break;
-        // O += P_j . V_j (O = P_0 . V_0 first); P_j is read from TMEM.  The
-        // softmax threads arrive on p_full only after any rescaling of O.
-        const int s = j % VS, b = j % NB;
-        if (!wait_bounded(p_full(b), use_parity(j), abort_flag, SITE_MMA_FULL)) break;
-        if (!wait_bounded(v_full(s), parity(j, VS), abort_flag, SITE_MMA_FULL)) break;
-        tc_fence_after_sync();
-        const uint32_t d = tmem_base + Cfg::kOCol;
-        const uint32_t pa = tmem_base + Cfg::kSCol + static_cast<uint32_t>(b * kAttnBC);
+      // O_c += P_j . V_j for chain c = j % 2 (O_c = P_j . V_j for the chain's
+      // first block); P_j is read from P_c, 16 keys per 8 columns.
+      auto issue_pv = [&](int j) {
+        const int s = j % VS, c = j % NC;
+        const uint32_t d = tmem_base + Cfg::kOCol + static_cast<uint32_t>(c * D);
+        const uint32_t pa = tmem_base + Cfg::kPCol + static_cast<uint32_t>(c * (kAttnBC / 2));
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t key_row = static_cast<uint32_t>(half * kHalfKeys + kk * 16);
-            umma_bf16_tmem_a(d, pa + static_cast<uint32_t>(half * kHalfKeys + kk * 8),
-                             smem_desc_mn_sw128(v_smem(s) + key_row * 128u, kChunkBytes), p.idesc_o,
-                             (j | half | kk) != 0 ? 1u : 0u);
+        for (int kk = 0; kk < kAttnBC / 16; ++kk)
+          umma_bf16_tmem_a(d, pa + static_cast<uint32_t>(kk * 8),
+                           smem_desc_mn_sw128(v_smem(s) + static_cast<uint32_t>(kk * 16) * 128u,
+                                              kChunkBytes),
+                           p.idesc_o, (j >= NC || kk != 0) ? 1u : 0u);
+        umma_commit(o_done(c));
+        umma_commit(v_empty(s));
+      };
+      // Issue in whichever order the conditions come true: the scores of
+      // block j once K_j has landed and the softmax has read block j - NS's
+      // scores out of the same buffer; the P.V of block j once P_j is stored
+      // and V_j has landed.  Each kind is issued in block order.
+      bool ok = wait_bounded(q_full, 0, abort_flag, SITE_MMA_FULL);
+      int ns = 0, npv = 0;
+      IdleBound bound;
+      while (ok && npv < n) {
+        bool issued = false;
+        if (ns < n) {
+          const int j = ns;
+          if ((j < NS || mbar_test_wait(s_free(j % NS), parity(j - NS, NS))) &&
+              mbar_test_wait(k_full(j % KS), parity(j, KS))) {
+            tc_fence_after_sync();
+            issue_s(j);
+            ++ns;
+            issued = true;
           }
         }
-        umma_commit(o_done(b));
-        umma_commit(v_empty(s));
+        if (npv < ns) {
+          const int j = npv;
+          if (mbar_test_wait(p_full(j % NC), parity(j, NC)) &&
+              mbar_test_wait(v_full(j % VS), parity(j, VS))) {
+            tc_fence_after_sync();
+            issue_pv(j);
+            ++npv;
+            issued = true;
+          }
+        }
+        if (issued) {
+          bound.progress();
+          continue;
+        }
+        if (bound.expired(abort_flag, SITE_MMA_FULL)) break;
+        __nanosleep(20);
       }
-      // Leave only when every issued MMA has completed (bounded).
+      // Every issued MMA completes before drain_bar does (bounded); the
+      // softmax warps read O_0 and O_1 only after it.
       umma_commit(drain_bar);
       wait_bounded(drain_bar, 0, nullptr, SITE_DRAIN);
     }
   } else {
-    // Softmax warps 2..9: warp w serves query rows 32*(w%4)..+31 (its TMEM
-    // lane quarter) and one half of the keys of each block and of the output
-    // columns; the two warps of a quarter exchange their partial row maxima
-    // through shared memory each block (a bounded mbarrier, values double
-    // buffered) and their partial row sums once at the end.
-    constexpr int kHalfD = D / 2;
-    const int half = (warp - 2) >> 2;
+    // Softmax warps 2..9: warp w runs chain (w - 2) / 4 for query rows
+    // 32*(w%4)..+31 (its TMEM lane quarter), one row per thread.
+    const int chain = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = 32 * quarter + lane;             // query row of this thread in the block
-    const uint32_t lane_base = tmem_addr(0, 32 * quarter, 0);
-    float* xval = reinterpret_cast<float*>(smem + Cfg::kRedOffset);
-    const uint32_t xbar = xchg_bar(quarter);
-    // Publishes `mine` for the partner warp in exchange round r and returns
-    // the partner's value (false if a wait gave up).
-    auto exchange = [&](int r, float mine, float& other) -> bool {
-      const int buf = r & 1;
-      xval[(buf * 2 + half) * kAttnBR + row] = mine;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(xbar);
-      const bool got = wait_bounded(xbar, static_cast<uint32_t>(r) & 1u, abort_flag,
-                                    SITE_EPI_ACC_FULL);
-      if (!__all_sync(0xffffffffu, got)) return false;
-      other = xval[(buf * 2 + (half ^ 1)) * kAttnBR + row];
-      return true;
-    };
-    // This thread's row of O: this warp's half of the D columns.
-    const uint32_t t_o = tmem_base + lane_base + Cfg::kOCol + static_cast<uint32_t>(half * kHalfD);
-    // Waits until O += P_j . V_j has completed (block j's products are in O).
-    auto wait_o = [&](int j) -> bool {
-      const bool got = wait_bounded(o_done(j % NB), use_parity(j), abort_flag, SITE_EPI_ACC_FULL);
-      if (!__all_sync(0xffffffffu, got)) return false;
-      tc_fence_after_sync();
-      return true;
-    };
-    // This warp's half of O, 32 columns at a time, multiplied by f (per row).
+    const uint32_t lane_base = tmem_base + tmem_addr(0, 32 * quarter, 0);
+    const uint32_t t_p = lane_base + Cfg::kPCol + static_cast<uint32_t>(chain * (kAttnBC / 2));
+    auto t_o = [&](int c) { return lane_base + Cfg::kOCol + static_cast<uint32_t>(c * D); };
+    // This thread's row of O_chain, multiplied by f.
     auto scale_o = [&](float f) {
 #pragma unroll
-      for (int c0 = 0; c0 < kHalfD; c0 += 32) {
+      for (int c0 = 0; c0 < D; c0 += 32) {
         float o[32];
-        tmem_load_32x32b_x32(t_o + c0, o);
+        tmem_load_32x32b_x32(t_o(chain) + c0, o);
         uint32_t w[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(o[i] * f);
-        tmem_store_32x32b_x32(t_o + c0, w);
+        tmem_store_32x32b_x32(t_o(chain) + c0, w);
       }
     };
-    float m = -INFINITY, l = 0.0f;   // m: the maximum this row's probabilities are taken against
+    float m = -INFINITY, l = 0.0f;   // m: the maximum this chain's probabilities are taken against
     bool ok = true;
     const float c = p.scale_log2;
-    for (int j = 0; j < n; ++j) {
-      const int b = j % NB;
-      const bool got = wait_bounded(s_full(b), use_parity(j), abort_flag, SITE_EPI_ACC_FULL);
+    for (int j = chain; j < n; j += NC) {
+      const int b = j % NS;
+      const bool got = wait_bounded(s_full(chain), parity(j, NC), abort_flag, SITE_EPI_ACC_FULL);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      const uint32_t ts = tmem_base + lane_base + Cfg::kSCol +
-                          static_cast<uint32_t>(b * kAttnBC + half * kHalfKeys);
-      const int col0 = j * kAttnBC + half * kHalfKeys;
-      const bool full = j * kAttnBC + kAttnBC <= p.Nk;   // the same for both halves
-      // This half of the row of S, once, into registers (64 scores).
-      float v[kHalfKeys];
-      tmem_load_32x32b_x64(ts, v);
-      // Pass 1: this half's maximum of the scaled scores (a full block needs no
-      // key mask, and scaling by c is monotonic: c times the largest raw score,
+      const int col0 = j * kAttnBC;
+      const bool full = col0 + kAttnBC <= p.Nk;
+      // The row of S, once, into registers (128 scores); the buffer is then
+      // free for the scores of block j + NS.
+      float v[kAttnBC];
+      tmem_load_32x32b_x128(lane_base + Cfg::kSCol + static_cast<uint32_t>(b * kAttnBC), v);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free(b));
+      // The block's maximum of the scaled scores (a full block needs no key
+      // mask, and scaling by c is monotonic: c times the largest raw score,
       // the smallest for c < 0), four partial maxima.
-      float mine;
+      float m_blk;
       if (full) {
         const bool up = c >= 0.0f;
         float r0 = up ? -INFINITY : INFINITY, r1 = r0, r2 = r0, r3 = r0;
         if (up) {
 #pragma unroll
-          for (int i = 0; i < kHalfKeys; i += 4) {
+          for (int i = 0; i < kAttnBC; i += 4) {
             r0 = fmaxf(r0, v[i]);
             r1 = fmaxf(r1, v[i + 1]);
             r2 = fmaxf(r2, v[i + 2]);
@@ -355,52 +393,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < kHalfKeys; i += 4) {
+          for (int i = 0; i < kAttnBC; i += 4) {
             r0 = fminf(r0, v[i]);
             r1 = fminf(r1, v[i + 1]);
             r2 = fminf(r2, v[i + 2]);
             r3 = fminf(r3, v[i + 3]);
           }
         }
-        mine = (up ? fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)) : fminf(fminf(r0, r1), fminf(r2, r3))) * c;
+        m_blk = (up ? fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)) : fminf(fminf(r0, r1), fminf(r2, r3))) * c;
       } else {
-        mine = -INFINITY;
+        m_blk = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < kHalfKeys; ++i)
-          if (col0 + i < p.Nk) mine = fmaxf(mine, v[i] * c);
+        for (int i = 0; i < kAttnBC; ++i)
+          if (col0 + i < p.Nk) m_blk = fmaxf(m_blk, v[i] * c);
       }
-      float other;
-      if (!exchange(j, mine, other)) {
-        ok = false;
-        break;
-      }
-      // Lazy rescaling: both warps of the row see the same block maximum and
-      // the same m, so they take the same decision.  On the first block m is
-      // -inf, so m moves and alpha = 0 (O and l hold nothing yet).
-      const float m_blk = fmaxf(mine, other);
+      // Lazy rescaling.  On the chain's first block m is -inf, so m moves
+      // and alpha = 0 (O_chain and l hold nothing yet).
       float alpha = 1.0f;
       bool moved = false;
       if (m_blk > m + kAttnRescaleLog2) {
         alpha = fast_exp2(m - m_blk);
         m = m_blk;
-        moved = j > 0;
+        moved = j >= NC;
       }
-      if (__any_sync(0xffffffffu, moved)) {
-        // O += P_{j-1} . V_{j-1} must be complete before its rows are scaled;
-        // P_j . V_j is issued only after this warp arrives on p_full below.
-        if (!wait_o(j - 1)) {
-          ok = false;
-          break;
-        }
-        scale_o(alpha);
-      }
-      // Pass 2: P = exp2(s * c - m) (at most 2^8), packed as BF16 pairs (even
-      // key in the low half) into the first 32 columns of this half's scores,
-      // and this half's row sum (four partial sums).
+      // P = exp2(s * c - m) (at most 2^8) as BF16 pairs (even key in the
+      // low half), and the row sum (four partial sums).
       float ps0 = 0.0f, ps1 = 0.0f, ps2 = 0.0f, ps3 = 0.0f;
-      uint32_t w[kHalfKeys / 2];
+      uint32_t w[kAttnBC / 2];
 #pragma unroll
-      for (int i = 0; i < kHalfKeys; i += 4) {
+      for (int i = 0; i < kAttnBC; i += 4) {
         float q0 = fast_exp2(fmaf(v[i], c, -m));
         float q1 = fast_exp2(fmaf(v[i + 1], c, -m));
         float q2 = fast_exp2(fmaf(v[i + 2], c, -m));
@@ -416,44 +437,89 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         ps1 += q1;
         ps2 += q2;
         ps3 += q3;
-        w[i / 2] = pack_bf16x2(q0, q1);
-        w[i / 2 + 1] = pack_bf16x2(q2, q3);
+        w[i / 2] = pack_bf16x2_nonneg(q0, q1);
+        w[i / 2 + 1] = pack_bf16x2_nonneg(q2, q3);
       }
-      tmem_store_32x32b_x32(ts, w);
+      // O_chain += P_{j-2} . V_{j-2} must have completed: it reads P_chain,
+      // and a rescaling of O_chain comes after it.
+      if (j >= NC) {
+        const bool done = wait_bounded(o_done(chain), parity(j - NC, NC), abort_flag,
+                                       SITE_EPI_ACC_FULL);
+        if (!__all_sync(0xffffffffu, done)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+      }
+      if (__any_sync(0xffffffffu, moved)) scale_o(alpha);
+      tmem_store_32x32b_x64(t_p, w);
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(b));
+      if (lane == 0) mbar_arrive(p_full(chain));
       l = fmaf(l, alpha, (ps0 + ps1) + (ps2 + ps3));
     }
-    if (ok && n > 0) ok = wait_o(n - 1);
-    // The row sum is the two halves' sums (both against the same m).
-    float l_other = 0.0f;
-    if (ok) ok = exchange(n, l, l_other);
+    // Every MMA has completed once drain_bar has (O_0 and O_1 final).
+    if (ok && n > 0) {
+      const bool got = wait_bounded(drain_bar, 0, abort_flag, SITE_EPI_ACC_FULL);
+      ok = __all_sync(0xffffffffu, got) && *abort_flag == 0;
+      if (ok) tc_fence_after_sync();
+    }
+    // Exchange (m, l) with the other chain's warp of this lane quarter.
+    float* xval = reinterpret_cast<float*>(smem + Cfg::kRedOffset);
+    float m_x = -INFINITY, l_x = 0.0f;
+    if (ok) {
+      xval[(0 * NC + chain) * kAttnBR + row] = m;
+      xval[(1 * NC + chain) * kAttnBR + row] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xchg_bar(quarter));
+      const bool got = wait_bounded(xchg_bar(quarter), 0, abort_flag, SITE_EPI_ACC_FULL);
+      ok = __all_sync(0xffffffffu, got);
+      if (ok) {
+        m_x = xval[(0 * NC + (chain ^ 1)) * kAttnBR + row];
+        l_x = xval[(1 * NC + (chain ^ 1)) * kAttnBR + row];
+      }
+    }
     const int qrow = qb * kAttnBR + row;
     if (ok && n > 0) {
-      const float inv = 1.0f / (l + l_other);
+      // Chain 1 has no blocks when n == 1: its O is never read.
+      const bool two = n > 1;
+      const float m0 = chain == 0 ? m : m_x, m1 = chain == 0 ? m_x : m;
+      const float l0 = chain == 0 ? l : l_x, l1 = chain == 0 ? l_x : l;
+      const float mm = fmaxf(m0, m1);
+      const float f0 = fast_exp2(m0 - mm);
+      const float f1 = two ? fast_exp2(m1 - mm) : 0.0f;
+      const float inv = 1.0f / fmaf(l0, f0, l1 * f1);
+      const float g0 = f0 * inv, g1 = f1 * inv;
+      // This warp writes half of the D output columns of its rows.
+      constexpr int kHalfD = D / 2;
 #pragma unroll
       for (int c0 = 0; c0 < kHalfD; c0 += 32) {
-        float o[32];
-        tmem_load_32x32b_x32(t_o + c0, o);
+        const int col = chain * kHalfD + c0;
+        float o[32], o1[32];
+        tmem_load_32x32b_x32(t_o(0) + col, o);
+        if (two) {
+          tmem_load_32x32b_x32(t_o(1) + col, o1);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = fmaf(o[i], g0, o1[i] * g1);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= g0;
+        }
         if (qrow < p.Nq) {
           if (p.out_kind == 0) {
             float* dst = static_cast<float*>(p.O) + h * p.o_stride +
-                         static_cast<long long>(qrow) * p.ldo + half * kHalfD + c0;
+                         static_cast<long long>(qrow) * p.ldo + col;
 #pragma unroll
             for (int d = 0; d < 32; d += 4)
-              *reinterpret_cast<float4*>(dst + d) =
-                  make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+              *reinterpret_cast<float4*>(dst + d) = make_float4(o[d], o[d + 1], o[d + 2], o[d + 3]);
           } else {
             uint16_t* dst = static_cast<uint16_t*>(p.O) + h * p.o_stride +
-                            static_cast<long long>(qrow) * p.ldo + half * kHalfD + c0;
+                            static_cast<long long>(qrow) * p.ldo + col;
 #pragma unroll
             for (int d = 0; d < 32; d += 8)
               *reinterpret_cast<uint4*>(dst + d) =
-                  make_uint4(pack_bf16x2(o[d] * inv, o[d + 1] * inv),
-                             pack_bf16x2(o[d + 2] * inv, o[d + 3] * inv),
-                             pack_bf16x2(o[d + 4] * inv, o[d + 5] * inv),
-                             pack_bf16x2(o[d + 6] * inv, o[d + 7] * inv));
+                  make_uint4(pack_bf16x2(o[d], o[d + 1]), pack_bf16x2(o[d + 2], o[d + 3]),
+                             pack_bf16x2(o[d + 4], o[d + 5]), pack_bf16x2(o[d + 6], o[d + 7]));
           }
         }
       }

@@ -86,15 +86,21 @@ __device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
     return mbar_try_wait(bar, parity);
 }
 
+// The global timer is read only every 256 failed attempts, starting from the
+// first such check (a timer read costs the waiting thread far more than a
+// try_wait), so a wait that completes soon pays nothing for its bound.
 template <bool kClusterScope>
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                        int site, uint64_t limit_ns) {
-  const uint64_t t0 = global_timer_ns();
+  uint64_t t0 = 0;
   for (uint32_t i = 1;; ++i) {
     if (try_wait_scoped<kClusterScope>(bar, parity)) return true;
     if ((i & 255u) == 0) {
       if (abort_flag != nullptr && *abort_flag) return false;
-      if (global_timer_ns() - t0 > limit_ns) {
+      const uint64_t now = global_timer_ns();
+      if (i == 256u) {
+        t0 = now;
+      } else if (now - t0 > limit_ns) {
         if (abort_flag != nullptr) *abort_flag = 1;
         record_timeout(site);
         return false;
@@ -102,6 +108,29 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile i
     }
   }
 }
+
+// Bound of a polling loop that serves several barriers (mbar_test_wait on
+// each, no thread suspended): the clock starts at the 32nd pass in a row
+// that made no progress and is read every 32 such passes, so progress never
+// waits for a timer read.  expired() also reports an abort of the CTA.
+struct IdleBound {
+  uint64_t t0 = 0;
+  uint32_t idle = 0;
+  __device__ __forceinline__ void progress() { idle = 0; }
+  __device__ __forceinline__ bool expired(volatile int* abort_flag, int site) {
+    if ((++idle & 31u) != 0) return false;
+    if (*abort_flag) return true;
+    const uint64_t now = global_timer_ns();
+    if (idle == 32u) {
+      t0 = now;
+      return false;
+    }
+    if (now - t0 <= kWaitLimitNs) return false;
+    *abort_flag = 1;
+    record_timeout(site);
+    return true;
+  }
+};
 
 // Waits for the phase of parity `parity` of `bar` to complete.  Returns false
 // if the CTA aborted or the wait exceeded its limit.

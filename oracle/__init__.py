@@ -564,13 +564,18 @@ def attention_tolerance(res, D: int, Nk: int, out_bf16=True):
       ``fp32_sum_rel(Nk)``:
       ``eta = exp(2e)(1 + 2^-8)(1 + 2^-20)(1 + fp32_sum_rel(Nk)) - 1``.
     * Output: the FP32 products of weights and values over Nk keys
-      (``fp32_sum_rel(Nk)``), the per-block rescaling (Nk/128 + 2 roundings)
-      and the final division: all relative to ``abs_o = sum_j w_j |v_j|``.
+      (``fp32_sum_rel(Nk)``), the per-block rescaling (at most one rounding
+      per 128-key block) and the final normalisation: the division, and the
+      merge of the two partial sums over disjoint key sets (even and odd
+      blocks) that the loop may keep -- two scalings by 2^(m_c - m) (an
+      approximate exp2, within 2^-22 = 4 units), their sum and the scaled
+      reciprocal, 12 units in all; all relative to
+      ``abs_o = sum_j w_j |v_j|``.
     Plus the BF16 half-ulp of a BF16 output.
     """
     e = (fp32_sum_rel(D) + 8.0 * U32) * res["smax"][:, None]
     eta = np.exp(2.0 * e) * (1 + 2.0 ** -8) * (1 + 2.0 ** -20) * (1 + fp32_sum_rel(Nk)) - 1.0
-    acc = fp32_sum_rel(Nk) + (Nk / 128.0 + 2.0) * U32
+    acc = fp32_sum_rel(Nk) + (Nk / 128.0 + 12.0) * U32
     tol = (eta + acc * (1.0 + eta)) * res["abs_o"]
     if out_bf16:
         tol = tol + bf16_half_ulp(np.abs(res["o"]) + tol)
