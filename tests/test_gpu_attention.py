@@ -178,3 +178,48 @@ def test_workload_attention(g, name):
     tol = oracle.attention_tolerance(res, w.K, w.N, out_bf16=True)
     assert_within(to_f64(O)[hh, rr], res["o"], tol, name)
     assert_status_ok(g)
+
+
+@pytest.mark.parametrize("Nk,key", [(384, 200), (384, 290), (129, 128), (256, 255), (640, 520)])
+def test_attention_dominant_key_in_either_chain(g, Nk, key):
+    """The key blocks are dealt to two loops (even and odd blocks) merged at
+    the end: a dominant key in an odd block (chain 1), in the only key of the
+    second block, or in a later even block, selects its value exactly as one
+    in block 0 does."""
+    H, Nq, D = 1, 200, 64
+    Q = torch.zeros(H, Nq, D)
+    Q[..., 0] = 8.0
+    K = torch.zeros(H, Nk, D)
+    K[0, key, 0] = 8.0          # score 64 against 0 for every other key
+    V = torch.randn(H, Nk, D, generator=torch.Generator().manual_seed(Nk + key))
+    Q, K, V = (x.to(BF16) for x in (Q, K, V))
+    O = g.attention(Q.cuda(), K.cuda(), V.cuda(), 1.0, out_dtype=F32)
+    torch.cuda.synchronize()
+    want = V.double()[0, key].expand(Nq, D).numpy()
+    assert np.allclose(to_f64(O)[0], want, rtol=0, atol=1e-6)
+    assert_status_ok(g)
+
+
+@pytest.mark.parametrize("Nk", [129, 256, 257, 1152])
+def test_attention_chains_with_different_maxima(g, Nk):
+    """Scores whose scale differs between even and odd key blocks (odd blocks
+    ~20 higher in base 2, then lower), so the two loops' maxima and sums
+    differ and the merge's scaling decides the result; checked against the
+    oracle within the derived bound."""
+    H, Nq, D = 2, 160, 128
+    gen = torch.Generator().manual_seed(Nk)
+    Q = torch.randn(H, Nq, D, generator=gen) * 0.3
+    Q[..., 0] = 1.0
+    K = torch.randn(H, Nk, D, generator=gen) * 0.3
+    blk = (torch.arange(Nk) // 128) % 2
+    K[..., 0] = torch.where(blk == 1, torch.tensor(14.0), torch.tensor(0.0)) \
+        - (torch.arange(Nk) >= 768).float() * 28.0
+    V = torch.randn(H, Nk, D, generator=gen)
+    Q, K, V = (x.to(BF16) for x in (Q, K, V))
+    O = g.attention(Q.cuda(), K.cuda(), V.cuda(), 1.0, out_dtype=F32)
+    torch.cuda.synchronize()
+    hh, rr = np.meshgrid(np.arange(H), np.arange(Nq), indexing="ij")
+    res = oracle.attention_rows(Q, K, V, 1.0, hh.ravel(), rr.ravel())
+    tol = oracle.attention_tolerance(res, D, Nk, out_bf16=False)
+    assert_within(to_f64(O)[hh.ravel(), rr.ravel()], res["o"], tol, f"Nk={Nk}")
+    assert_status_ok(g)
