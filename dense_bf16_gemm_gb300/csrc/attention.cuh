@@ -47,10 +47,10 @@
 // Warp roles: warp 0 TMA (Q once; K_j and V_j through separate rings, in the
 // order the MMAs take them), warp 1 MMA issue and TMEM owner, warps 2-5 the
 // softmax of chain 0 and warps 6-9 that of chain 1 (warp w serves TMEM lane
-// quarter w % 4).  The MMA thread polls the conditions of both chains and
-// issues whichever product is ready: the scores of block j once K_j has
-// landed and O_c += P_{j-2} . V_{j-2} has completed, the P.V of block j once
-// P_j is stored and V_j has landed.
+// quarter w % 4).  The MMA thread issues the scores of block j + NS (NS
+// score buffers) as soon as the softmax has read block j's scores out of the
+// same buffer, and the P.V of block j once P_j is stored: in a fixed order
+// with a buffer per chain, polling both conditions with one shared buffer.
 //
 // Every wait is bounded as in the GEMM kernels (status word, abort flag,
 // drained copies and MMAs, TMEM freed).
@@ -112,14 +112,41 @@ struct AttnCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// Two non-negative finite floats rounded to BF16 (to nearest, ties away from
-// zero: adding half a BF16 unit of the last place to the FP32 bit pattern
-// and keeping the upper 16 bits, which carries into the exponent where the
-// significand overflows), packed with the first in the low half.  Integer
-// arithmetic, so that the probabilities' conversion does not compete with
-// exp2 for the special-function unit.
-__device__ __forceinline__ uint32_t pack_bf16x2_nonneg(float lo, float hi) {
-  return __byte_perm(__float_as_uint(lo) + 0x8000u, __float_as_uint(hi) + 0x8000u, 0x7632);
+// Three-input maximum and minimum (one instruction each).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// (d0, d1) = (fma(a0, b, c), fma(a1, b, c)) as one paired FP32 instruction,
+// each lane rounded exactly as fmaf rounds it.
+__device__ __forceinline__ void fma2_bc(float& d0, float& d1, float a0, float a1, float b,
+                                        float c) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %4};\n\t"
+      "mov.b64 rc, {%5, %5};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+// (s0, s1) += (a0, a1) as one paired FP32 add.
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
+  asm("{\n\t.reg .b64 rs, ra;\n\t"
+      "mov.b64 rs, {%0, %1};\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "add.rn.f32x2 rs, rs, ra;\n\t"
+      "mov.b64 {%0, %1}, rs;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
 }
 
 // 2^x by the hardware's approximate exp2 (relative error about 2^-22;
@@ -294,41 +321,74 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         umma_commit(o_done(c));
         umma_commit(v_empty(s));
       };
-      // Issue in whichever order the conditions come true: the scores of
-      // block j once K_j has landed and the softmax has read block j - NS's
-      // scores out of the same buffer; the P.V of block j once P_j is stored
-      // and V_j has landed.  Each kind is issued in block order.
       bool ok = wait_bounded(q_full, 0, abort_flag, SITE_MMA_FULL);
-      int ns = 0, npv = 0;
-      IdleBound bound;
-      while (ok && npv < n) {
-        bool issued = false;
-        if (ns < n) {
-          const int j = ns;
-          if ((j < NS || mbar_test_wait(s_free(j % NS), parity(j - NS, NS))) &&
-              mbar_test_wait(k_full(j % KS), parity(j, KS))) {
+      if constexpr (NS >= 2) {
+        // With a score buffer per chain, a fixed order: S_0 .. S_{NS-1}, then
+        // for each block j the scores of block j + NS (once the softmax has
+        // read block j's scores out of the same buffer and K_{j+NS} has
+        // landed) and then the P.V of block j (once P_j is stored and V_j
+        // has landed).  The softmax of block j frees its score buffer before
+        // it stores P_j.  (Issuing the P.V one block later instead measured
+        // slower.)
+        for (int j = 0; ok && j < NS && j < n; ++j) {
+          ok = wait_bounded(k_full(j % KS), parity(j, KS), abort_flag, SITE_MMA_FULL);
+          if (ok) {
             tc_fence_after_sync();
             issue_s(j);
-            ++ns;
-            issued = true;
           }
         }
-        if (npv < ns) {
-          const int j = npv;
-          if (mbar_test_wait(p_full(j % NC), parity(j, NC)) &&
-              mbar_test_wait(v_full(j % VS), parity(j, VS))) {
+        for (int j = 0; ok && j < n; ++j) {
+          const int js = j + NS;
+          if (js < n) {
+            if (!wait_bounded(s_free(js % NS), parity(j, NS), abort_flag, SITE_MMA_ACC_EMPTY) ||
+                !wait_bounded(k_full(js % KS), parity(js, KS), abort_flag, SITE_MMA_FULL))
+              break;
             tc_fence_after_sync();
-            issue_pv(j);
-            ++npv;
-            issued = true;
+            issue_s(js);
           }
+          if (!wait_bounded(p_full(j % NC), parity(j, NC), abort_flag, SITE_MMA_FULL) ||
+              !wait_bounded(v_full(j % VS), parity(j, VS), abort_flag, SITE_MMA_FULL))
+            break;
+          tc_fence_after_sync();
+          issue_pv(j);
         }
-        if (issued) {
-          bound.progress();
-          continue;
+      } else {
+        // With one score buffer shared by the chains, the scores of block j + 1
+        // can be issued as soon as the other chain has read block j's, which
+        // comes before or after P_{j-1} depending on the two softmaxes' pace:
+        // poll both conditions and issue whichever product is ready (each
+        // kind in block order).
+        int ns = 0, npv = 0;
+        IdleBound bound;
+        while (ok && npv < n) {
+          bool issued = false;
+          if (ns < n) {
+            const int j = ns;
+            if ((j < NS || mbar_test_wait(s_free(j % NS), parity(j - NS, NS))) &&
+                mbar_test_wait(k_full(j % KS), parity(j, KS))) {
+              tc_fence_after_sync();
+              issue_s(j);
+              ++ns;
+              issued = true;
+            }
+          }
+          if (npv < ns) {
+            const int j = npv;
+            if (mbar_test_wait(p_full(j % NC), parity(j, NC)) &&
+                mbar_test_wait(v_full(j % VS), parity(j, VS))) {
+              tc_fence_after_sync();
+              issue_pv(j);
+              ++npv;
+              issued = true;
+            }
+          }
+          if (issued) {
+            bound.progress();
+            continue;
+          }
+          if (bound.expired(abort_flag, SITE_MMA_FULL)) break;
+          __nanosleep(20);
         }
-        if (bound.expired(abort_flag, SITE_MMA_FULL)) break;
-        __nanosleep(20);
       }
       // Every issued MMA completes before drain_bar does (bounded); the
       // softmax warps read O_0 and O_1 only after it.
@@ -385,19 +445,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float r0 = up ? -INFINITY : INFINITY, r1 = r0, r2 = r0, r3 = r0;
         if (up) {
 #pragma unroll
-          for (int i = 0; i < kAttnBC; i += 4) {
-            r0 = fmaxf(r0, v[i]);
-            r1 = fmaxf(r1, v[i + 1]);
-            r2 = fmaxf(r2, v[i + 2]);
-            r3 = fmaxf(r3, v[i + 3]);
+          for (int i = 0; i < kAttnBC; i += 8) {
+            r0 = max3f(r0, v[i], v[i + 1]);
+            r1 = max3f(r1, v[i + 2], v[i + 3]);
+            r2 = max3f(r2, v[i + 4], v[i + 5]);
+            r3 = max3f(r3, v[i + 6], v[i + 7]);
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < kAttnBC; i += 4) {
-            r0 = fminf(r0, v[i]);
-            r1 = fminf(r1, v[i + 1]);
-            r2 = fminf(r2, v[i + 2]);
-            r3 = fminf(r3, v[i + 3]);
+          for (int i = 0; i < kAttnBC; i += 8) {
+            r0 = min3f(r0, v[i], v[i + 1]);
+            r1 = min3f(r1, v[i + 2], v[i + 3]);
+            r2 = min3f(r2, v[i + 4], v[i + 5]);
+            r3 = min3f(r3, v[i + 6], v[i + 7]);
           }
         }
         m_blk = (up ? fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)) : fminf(fminf(r0, r1), fminf(r2, r3))) * c;
@@ -416,16 +476,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         m = m_blk;
         moved = j >= NC;
       }
-      // P = exp2(s * c - m) (at most 2^8) as BF16 pairs (even key in the
-      // low half), and the row sum (four partial sums).
+      // P = exp2(s * c - m) (at most 2^8) rounded to BF16 pairs (to nearest
+      // even; even key in the low half), and the row sum (four partial sums).
       float ps0 = 0.0f, ps1 = 0.0f, ps2 = 0.0f, ps3 = 0.0f;
       uint32_t w[kAttnBC / 2];
 #pragma unroll
       for (int i = 0; i < kAttnBC; i += 4) {
-        float q0 = fast_exp2(fmaf(v[i], c, -m));
-        float q1 = fast_exp2(fmaf(v[i + 1], c, -m));
-        float q2 = fast_exp2(fmaf(v[i + 2], c, -m));
-        float q3 = fast_exp2(fmaf(v[i + 3], c, -m));
+        float q0, q1, q2, q3;
+        fma2_bc(q0, q1, v[i], v[i + 1], c, -m);
+        fma2_bc(q2, q3, v[i + 2], v[i + 3], c, -m);
+        q0 = fast_exp2(q0);
+        q1 = fast_exp2(q1);
+        q2 = fast_exp2(q2);
+        q3 = fast_exp2(q3);
         if (!full) {
           const int k = col0 + i;
           q0 = k < p.Nk ? q0 : 0.0f;
@@ -433,12 +496,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           q2 = k + 2 < p.Nk ? q2 : 0.0f;
           q3 = k + 3 < p.Nk ? q3 : 0.0f;
         }
-        ps0 += q0;
-        ps1 += q1;
-        ps2 += q2;
-        ps3 += q3;
-        w[i / 2] = pack_bf16x2_nonneg(q0, q1);
-        w[i / 2 + 1] = pack_bf16x2_nonneg(q2, q3);
+        add2(ps0, ps1, q0, q1);
+        add2(ps2, ps3, q2, q3);
+        w[i / 2] = pack_bf16x2(q0, q1);
+        w[i / 2 + 1] = pack_bf16x2(q2, q3);
       }
       // O_chain += P_{j-2} . V_{j-2} must have completed: it reads P_chain,
       // and a rescaling of O_chain comes after it.
