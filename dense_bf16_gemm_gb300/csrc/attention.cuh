@@ -157,6 +157,38 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// One block's probabilities for one query row: p_i = exp2(s_i c - m), zero
+// for keys at or past Nk when MASKED, rounded to BF16 pairs (to nearest
+// even; even key in the low half) into w, and the row sum as four partial
+// sums (lane-wise paired adds: partial k takes keys i with i % 4 == k).
+template <bool MASKED>
+__device__ __forceinline__ void attn_probabilities(const float (&v)[kAttnBC], float c, float m,
+                                                   int col0, int Nk, uint32_t (&w)[kAttnBC / 2],
+                                                   float& ps0, float& ps1, float& ps2,
+                                                   float& ps3) {
+#pragma unroll
+  for (int i = 0; i < kAttnBC; i += 4) {
+    float q0, q1, q2, q3;
+    fma2_bc(q0, q1, v[i], v[i + 1], c, -m);
+    fma2_bc(q2, q3, v[i + 2], v[i + 3], c, -m);
+    q0 = fast_exp2(q0);
+    q1 = fast_exp2(q1);
+    q2 = fast_exp2(q2);
+    q3 = fast_exp2(q3);
+    if constexpr (MASKED) {
+      const int k = col0 + i;
+      q0 = k < Nk ? q0 : 0.0f;
+      q1 = k + 1 < Nk ? q1 : 0.0f;
+      q2 = k + 2 < Nk ? q2 : 0.0f;
+      q3 = k + 3 < Nk ? q3 : 0.0f;
+    }
+    add2(ps0, ps1, q0, q1);
+    add2(ps2, ps3, q2, q3);
+    w[i / 2] = pack_bf16x2(q0, q1);
+    w[i / 2 + 1] = pack_bf16x2(q2, q3);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -480,27 +512,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // even; even key in the low half), and the row sum (four partial sums).
       float ps0 = 0.0f, ps1 = 0.0f, ps2 = 0.0f, ps3 = 0.0f;
       uint32_t w[kAttnBC / 2];
-#pragma unroll
-      for (int i = 0; i < kAttnBC; i += 4) {
-        float q0, q1, q2, q3;
-        fma2_bc(q0, q1, v[i], v[i + 1], c, -m);
-        fma2_bc(q2, q3, v[i + 2], v[i + 3], c, -m);
-        q0 = fast_exp2(q0);
-        q1 = fast_exp2(q1);
-        q2 = fast_exp2(q2);
-        q3 = fast_exp2(q3);
-        if (!full) {
-          const int k = col0 + i;
-          q0 = k < p.Nk ? q0 : 0.0f;
-          q1 = k + 1 < p.Nk ? q1 : 0.0f;
-          q2 = k + 2 < p.Nk ? q2 : 0.0f;
-          q3 = k + 3 < p.Nk ? q3 : 0.0f;
-        }
-        add2(ps0, ps1, q0, q1);
-        add2(ps2, ps3, q2, q3);
-        w[i / 2] = pack_bf16x2(q0, q1);
-        w[i / 2 + 1] = pack_bf16x2(q2, q3);
-      }
+      // Two copies of the loop, so that a full block runs with no key test.
+      if (full)
+        attn_probabilities<false>(v, c, m, col0, p.Nk, w, ps0, ps1, ps2, ps3);
+      else
+        attn_probabilities<true>(v, c, m, col0, p.Nk, w, ps0, ps1, ps2, ps3);
       // O_chain += P_{j-2} . V_{j-2} must have completed: it reads P_chain,
       // and a rescaling of O_chain comes after it.
       if (j >= NC) {
