@@ -324,16 +324,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       // S_b = Q . K_j^T for block j into score buffer b = j % NS; chain
       // j % 2 is told on its own barrier.
+      // Descriptors step through an operand by adding to their start-address
+      // field (16-byte units): 2 per K = 16 step of a 128-byte row, 1024 per
+      // 64-element chunk of 128 rows, 128 per 16 rows.
+      const uint64_t qd0 = smem_desc_sw128(q_smem);
       auto issue_s = [&](int j) {
         const int s = j % KS, b = j % NS;
         const uint32_t d = tmem_base + Cfg::kSCol + static_cast<uint32_t>(b * kAttnBC);
+        const uint64_t kd0 = smem_desc_sw128(k_smem(s));
 #pragma unroll
         for (int ch = 0; ch < Cfg::kChunks; ++ch) {
-          const uint64_t qd = smem_desc_sw128(q_smem + ch * kChunkBytes);
-          const uint64_t kd = smem_desc_sw128(k_smem(s) + ch * kChunkBytes);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, qd + 2u * kk, kd + 2u * kk, p.idesc_s, (ch | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t step = static_cast<uint64_t>(ch * (kChunkBytes >> 4) + 2 * kk);
+            umma_bf16(d, qd0 + step, kd0 + step, p.idesc_s, (ch | kk) != 0 ? 1u : 0u);
+          }
         }
         umma_commit(s_full(j % NC));
         umma_commit(k_empty(s));
@@ -344,12 +349,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int s = j % VS, c = j % NC;
         const uint32_t d = tmem_base + Cfg::kOCol + static_cast<uint32_t>(c * D);
         const uint32_t pa = tmem_base + Cfg::kPCol + static_cast<uint32_t>(c * (kAttnBC / 2));
+        const uint64_t vd0 = smem_desc_mn_sw128(v_smem(s), kChunkBytes);
 #pragma unroll
         for (int kk = 0; kk < kAttnBC / 16; ++kk)
           umma_bf16_tmem_a(d, pa + static_cast<uint32_t>(kk * 8),
-                           smem_desc_mn_sw128(v_smem(s) + static_cast<uint32_t>(kk * 16) * 128u,
-                                              kChunkBytes),
-                           p.idesc_o, (j >= NC || kk != 0) ? 1u : 0u);
+                           vd0 + static_cast<uint64_t>(kk * (16 * 128 >> 4)), p.idesc_o,
+                           (j >= NC || kk != 0) ? 1u : 0u);
         umma_commit(o_done(c));
         umma_commit(v_empty(s));
       };

@@ -129,3 +129,17 @@ def test_layout_calls_are_exported(lib):
     for name in ("gemm_layout_smem_descriptor", "gemm_layout_instr_descriptor",
                  "gemm_layout_swizzle128_offset", "gemm_layout_tmem_address"):
         assert name in _native.EXPORTED and hasattr(lib, name)
+
+
+def test_descriptors_step_by_adding_to_the_start_field(lib):
+    # the attention kernel steps its descriptors instead of re-encoding them:
+    # 16 rows of an MN-major operand (2048 bytes) add 128, a 64-element chunk
+    # of 128 K-major rows (16384 bytes) adds 1024, a K = 16 step adds 2
+    for base in (1024, 17408, 98304, 200704):
+        for kk in range(8):
+            assert (lib.gemm_layout_smem_descriptor(base + kk * 2048, 16384)
+                    == lib.gemm_layout_smem_descriptor(base, 16384) + 128 * kk)
+        for ch in range(2):
+            for kk in range(4):
+                assert (lib.gemm_layout_smem_descriptor(base + ch * 16384 + 32 * kk, 0)
+                        == lib.gemm_layout_smem_descriptor(base, 0) + 1024 * ch + 2 * kk)
