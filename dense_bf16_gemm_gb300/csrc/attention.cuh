@@ -6,17 +6,17 @@
 //
 // One CTA per (head, 128-row query block).  The key blocks of 128 keys are
 // dealt to two independent flash loops ("chains"): the even blocks to chain
-// 0, the odd ones to chain 1.  Chain c owns a score buffer S_c and an output
-// accumulator O_c in Tensor Memory and keeps its own m_c and l_c.  Per key
-// block j of chain c = j % 2:
+// 0, the odd ones to chain 1.  Chain c owns a probability buffer P_c and an
+// output accumulator O_c in Tensor Memory and keeps its own m_c and l_c.  Per
+// key block j of chain c = j % 2:
 //
-//   S_c = Q . K_j^T                tcgen05.mma M = 128, N = 128 over D (K_j is K-major:
-//                                  D contiguous)
-//   m_c = max(m_c, rowmax S_c)     softmax warps of chain c: a query row is one TMEM lane
-//   P_j = exp(S_c - m_c)           and one thread, which holds all 128 scores of its row
+//   S = Q . K_j^T                  tcgen05.mma M = 128, N = 128 over D (K_j is K-major:
+//                                  D contiguous), into score buffer j % NS
+//   m_c = max(m_c, rowmax S)       softmax warps of chain c: a query row is one TMEM lane
+//   P_j = exp(S - m_c)             and one thread, which holds all 128 scores of its row
 //   l_c = l_c a + rowsum P_j       (a = exp(m_old - m_new))
-//   O_c += P_j . V_j               tcgen05.mma M = 128, N = D over the 128 keys, P_j written
-//                                  as BF16 over S_c and read from Tensor Memory as the A
+//   O_c += P_j . V_j               tcgen05.mma M = 128, N = D over the 128 keys, P_j stored
+//                                  as BF16 in P_c and read from Tensor Memory as the A
 //                                  operand, V_j the MN-major operand (D contiguous, as TMA
 //                                  loads it)
 //
@@ -27,30 +27,33 @@
 // units (exp2 of s * scale * log2 e), which is the same function.  Keys past
 // Nk score -inf.
 //
-// Why two chains: a chain is serial -- its next scores overwrite the P that
-// its P.V product reads, so S_c for block j + 2 is issued only once
-// O_c += P_j . V_j has completed -- but the chains are independent, so the
-// tensor core works on one chain's products while the other chain's softmax
-// threads run, and every SM sub-partition has a warp of each chain to issue
-// from.  No value is exchanged between warps inside the loop.
+// Why two chains: a chain is serial -- P_j can be stored only once
+// O_c += P_{j-2} . V_{j-2} has read P_c -- but the chains are independent,
+// so the tensor core works on one chain's products while the other chain's
+// softmax threads run, and every SM sub-partition has a warp of each chain
+// to issue from.  No value is exchanged between warps inside the loop.  A
+// score buffer is freed as soon as the softmax has loaded its scores into
+// registers, so the next scores are computed while the softmax runs.
 //
 // The running maximum is updated lazily: the m a chain's probabilities are
 // taken against moves only when a block's maximum exceeds it by more than
 // kAttnRescaleLog2 (so probabilities stay below 2^8 and l_c, O_c keep their
 // ratio), and only then is that row of O_c (and l_c) multiplied by a, in
-// Tensor Memory.  O_c += P_{j-2} . V_{j-2} has completed by then: S_c for
-// block j was issued after it.
+// Tensor Memory, after O_c += P_{j-2} . V_{j-2} has completed and before
+// P_j is stored.
 //
-// Tensor Memory (512 columns): S_0 at 0, S_1 at 128 (each 128 FP32 scores,
-// then P as packed BF16 in its first 64 columns); O_0 at 256, O_1 at 256 + D.
+// Tensor Memory (512 columns): NS score buffers of 128 FP32 columns (NS = 2,
+// one per chain, at D = 64; NS = 1, shared by the chains, at D = 128), then
+// P_0 and P_1 (64 columns of packed BF16 each), then O_0 and O_1 (D columns
+// each).
 //
-// Warp roles: warp 0 TMA (Q once; K_j and V_j through separate rings, in the
-// order the MMAs take them), warp 1 MMA issue and TMEM owner, warps 2-5 the
-// softmax of chain 0 and warps 6-9 that of chain 1 (warp w serves TMEM lane
-// quarter w % 4).  The MMA thread issues the scores of block j + NS (NS
-// score buffers) as soon as the softmax has read block j's scores out of the
-// same buffer, and the P.V of block j once P_j is stored: in a fixed order
-// with a buffer per chain, polling both conditions with one shared buffer.
+// Warp roles: warp 0 TMA (Q once; K_j and V_j through separate rings, each
+// refilled as soon as a slot frees), warp 1 MMA issue and TMEM owner, warps
+// 2-5 the softmax of chain 0 and warps 6-9 that of chain 1 (warp w serves
+// TMEM lane quarter w % 4).  The MMA thread issues the scores of block
+// j + NS as soon as the softmax has read block j's scores out of the same
+// buffer, and the P.V of block j once P_j is stored: in a fixed order with a
+// buffer per chain, polling both conditions with one shared buffer.
 //
 // Every wait is bounded as in the GEMM kernels (status word, abort flag,
 // drained copies and MMAs, TMEM freed).

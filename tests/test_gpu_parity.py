@@ -895,3 +895,21 @@ def test_strips_random_inputs_match_whole_tiles(g, monkeypatch):
     tol = oracle.gemm_tolerance(ref, ab, 0.5, 2.0, C.numpy()[rr, cc])
     assert_within(to_f64(outs[0])[rr, cc], ref, tol, "strips")
     assert_status_ok(g)
+
+
+@pytest.mark.parametrize("beta", [0.0, 0.5])
+def test_strips_f16_output(g, monkeypatch, beta):
+    """Strips writing FP16 output (the 16-bit epilogue with its FP16 packing),
+    with and without C read through the ring."""
+    monkeypatch.setenv("GB3_GEMM_STRIPS", "1")
+    monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", "256")
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "0")
+    M, N, K = 1000, 712, 1000
+    A, B, C = batched_int_inputs(1, M, N, K, 91, torch.float16)
+    A, B, C = A[0], B[0], C[0]
+    Cq = C.to(torch.float16) if beta != 0.0 else None
+    ref, _ = oracle.gemm_full(A, B, alpha=1.0, beta=beta,
+                              C=Cq.to(torch.float32) if Cq is not None else None)
+    out = run_gemm(g, A, B, C=Cq, alpha=1.0, beta=beta, out_dtype=torch.float16)
+    assert np.array_equal(bits(out.cpu()), oracle.round_to_f16_bits(ref))
+    assert_status_ok(g)
