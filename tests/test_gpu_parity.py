@@ -913,3 +913,32 @@ def test_strips_f16_output(g, monkeypatch, beta):
     out = run_gemm(g, A, B, C=Cq, alpha=1.0, beta=beta, out_dtype=torch.float16)
     assert np.array_equal(bits(out.cpu()), oracle.round_to_f16_bits(ref))
     assert_status_ok(g)
+
+
+def test_strips_under_graph_capture(g):
+    """A plan with strips (the ragged workload's shape with a short K) captured
+    into a CUDA graph on a fresh stream replays to the eager result: strips
+    need no workspace, so nothing is allocated during capture."""
+    M, N, K = 3000, 5000, 264
+    assert strips_planned(g.plan(M, N, K, torch.float32), M, N)
+    A, B, C = int_inputs(M, N, K, 35)
+    Ad, Bd, C0 = A.cuda(), B.cuda(), C.cuda()
+    Cd = C0.clone()
+    g.gemm(Ad, Bd, Cd, alpha=2.0, beta=-0.5)
+    torch.cuda.synchronize()
+    eager = Cd.clone()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    Cd.copy_(C0)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            g.gemm(Ad, Bd, Cd, alpha=2.0, beta=-0.5, stream=s)
+    for _ in range(2):
+        Cd.copy_(C0)
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(Cd, eager)
+    ref, _ = oracle.gemm_full(A, B, alpha=2.0, beta=-0.5, C=C)
+    assert np.array_equal(to_f64(Cd), ref)
+    assert_status_ok(g)
