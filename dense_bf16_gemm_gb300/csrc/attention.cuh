@@ -397,21 +397,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // can be issued as soon as the other chain has read block j's, which
         // comes before or after P_{j-1} depending on the two softmaxes' pace:
         // poll both conditions and issue whichever product is ready (each
-        // kind in block order).
+        // kind in block order; a ready P.V first, which measured ~1 % faster).
         int ns = 0, npv = 0;
         IdleBound bound;
         while (ok && npv < n) {
           bool issued = false;
-          if (ns < n) {
-            const int j = ns;
-            if ((j < NS || mbar_test_wait(s_free(j % NS), parity(j - NS, NS))) &&
-                mbar_test_wait(k_full(j % KS), parity(j, KS))) {
-              tc_fence_after_sync();
-              issue_s(j);
-              ++ns;
-              issued = true;
-            }
-          }
           if (npv < ns) {
             const int j = npv;
             if (mbar_test_wait(p_full(j % NC), parity(j, NC)) &&
@@ -419,6 +409,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               tc_fence_after_sync();
               issue_pv(j);
               ++npv;
+              issued = true;
+            }
+          }
+          if (ns < n) {
+            const int j = ns;
+            if ((j < NS || mbar_test_wait(s_free(j % NS), parity(j - NS, NS))) &&
+                mbar_test_wait(k_full(j % KS), parity(j, KS))) {
+              tc_fence_after_sync();
+              issue_s(j);
+              ++ns;
               issued = true;
             }
           }
