@@ -363,28 +363,60 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       };
       bool ok = wait_bounded(q_full, 0, abort_flag, SITE_MMA_FULL);
       if constexpr (NS >= 2) {
-        // With a score buffer per chain, a fixed order: S_0 .. S_{NS-1}, then
-        // for each block j the scores of block j + NS (once the softmax has
-        // read block j's scores out of the same buffer and K_{j+NS} has
-        // landed) and then the P.V of block j (once P_j is stored and V_j
-        // has landed).  The softmax of block j frees its score buffer before
-        // it stores P_j.  (Issuing the P.V one block later instead measured
-        // slower.)
-        for (int j = 0; ok && j < NS && j < n; ++j) {
-          ok = wait_bounded(k_full(j % KS), parity(j, KS), abort_flag, SITE_MMA_FULL);
-          if (ok) {
-            tc_fence_after_sync();
-            issue_s(j);
+        // With a score buffer per chain, a fixed order: the scores of blocks
+        // 0 and 1, then for each block j: at even j the scores of blocks j + 2
+        // and j + 3 (once the softmax has read blocks j and j + 1 out of the
+        // same buffers and the K blocks have landed), and the P.V of block j
+        // (once P_j is stored and V_j has landed).  The softmax of block j
+        // frees its score buffer before it stores P_j.  (Issuing the P.V one
+        // block later instead measured slower; issuing the two blocks' scores
+        // as one set of N = 256 MMAs saves an instruction per pair.)
+        // The scores of blocks j and j + 1 (one per chain, buffers 0 and 1,
+        // adjacent in Tensor Memory; K_j and K_{j+1} in adjacent ring slots)
+        // as one set of N = 256 MMAs.
+        constexpr uint32_t kIdescS2 = idesc_f32_acc(kAttnBR, 2 * kAttnBC, false);
+        static_assert(KS % 2 == 0, "pairs of K slots must be adjacent");
+        auto issue_s2 = [&](int j) {
+          const int s = j % KS;
+          const uint32_t d = tmem_base + Cfg::kSCol;
+          const uint64_t kd0 = smem_desc_sw128(k_smem(s));
+#pragma unroll
+          for (int ch = 0; ch < Cfg::kChunks; ++ch) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t step = static_cast<uint64_t>(ch * (kChunkBytes >> 4) + 2 * kk);
+              umma_bf16(d, qd0 + step, kd0 + step, kIdescS2, (ch | kk) != 0 ? 1u : 0u);
+            }
           }
-        }
-        for (int j = 0; ok && j < n; ++j) {
-          const int js = j + NS;
-          if (js < n) {
-            if (!wait_bounded(s_free(js % NS), parity(j, NS), abort_flag, SITE_MMA_ACC_EMPTY) ||
-                !wait_bounded(k_full(js % KS), parity(js, KS), abort_flag, SITE_MMA_FULL))
-              break;
+          umma_commit(s_full(0));
+          umma_commit(s_full(1));
+          umma_commit(k_empty(s));
+          umma_commit(k_empty(s + 1));
+        };
+        auto scores_from = [&](int js) -> bool {   // the scores of js (even) and js + 1
+          if (js + 1 < n) {
+            if (!wait_bounded(k_full(js % KS), parity(js, KS), abort_flag, SITE_MMA_FULL) ||
+                !wait_bounded(k_full((js + 1) % KS), parity(js + 1, KS), abort_flag, SITE_MMA_FULL))
+              return false;
+            tc_fence_after_sync();
+            issue_s2(js);
+          } else {
+            if (!wait_bounded(k_full(js % KS), parity(js, KS), abort_flag, SITE_MMA_FULL))
+              return false;
             tc_fence_after_sync();
             issue_s(js);
+          }
+          return true;
+        };
+        if (n > 0) ok = scores_from(0);
+        for (int j = 0; ok && j < n; ++j) {
+          const int js = j + 2;
+          if (j % 2 == 0 && js < n) {
+            if (!wait_bounded(s_free(0), parity(j, NS), abort_flag, SITE_MMA_ACC_EMPTY) ||
+                (js + 1 < n &&
+                 !wait_bounded(s_free(1), parity(j + 1, NS), abort_flag, SITE_MMA_ACC_EMPTY)) ||
+                !scores_from(js))
+              break;
           }
           if (!wait_bounded(p_full(j % NC), parity(j, NC), abort_flag, SITE_MMA_FULL) ||
               !wait_bounded(v_full(j % VS), parity(j, VS), abort_flag, SITE_MMA_FULL))
