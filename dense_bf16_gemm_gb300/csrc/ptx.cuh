@@ -502,24 +502,6 @@ __device__ __forceinline__ void tmem_store_32x32b_x64(uint32_t taddr, const uint
       : "memory");
 }
 
-// Whole warp: lane i writes 16 consecutive 32-bit columns of TMEM lane (lane
-// field of taddr) + i, without waiting; tmem_store_wait() completes every
-// earlier store of the thread.
-__device__ __forceinline__ void tmem_store_32x32b_x16_async(uint32_t taddr,
-                                                            const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {"
-      "%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_store_wait() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
 // Non-blocking test of whether the phase of parity `parity` of `bar` has
 // completed (the caller polls; nothing suspends the thread).
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
