@@ -365,7 +365,12 @@ typedef struct gemm_plan {
  * M > 128 runs on CTA pairs (256-row tiles) with the tile width that needs the
  * fewest waves; the environment variable GB3_GEMM_PAIR_TILE_N (256 or 224)
  * forces one width, for tuning and tests.  The tiles of a partial last wave
- * are cut into 2 K pieces when that shortens the wave; GB3_GEMM_BALANCED = 1
+ * are cut into 2 K pieces when that shortens the wave; where K is too short
+ * for that (pieces under 24 k-blocks) and four times the wave's 256-wide
+ * tiles fit on the pairs, they run as 256 x 64 strips over all of K instead
+ * (not with row statistics; `tiles` then counts the strips as units;
+ * GB3_GEMM_STRIPS = 0 turns strips off, 1 takes them wherever the wave fits,
+ * even in place of a K split); GB3_GEMM_BALANCED = 1
  * instead gives every CTA pair one contiguous range of all tiles' k-blocks
  * (measured slower on GB300, so off by default; split_k then reports the most
  * pieces of a tile and `tiles` the units).  The plan is that of beta == 0: with
