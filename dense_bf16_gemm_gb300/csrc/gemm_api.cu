@@ -289,6 +289,7 @@ struct PairChoice {
   int extra = 0;         // clusters 0..extra-1 take one more
   int64_t units = 0;
   int max_pieces = 1;
+  int64_t dp_tiles = 0;  // balanced: whole tiles run first, data-parallel
   // Strips: the last strip_tiles tiles run as 256 / kPairStripN strips each.
   int64_t strip_tiles = 0;
   int64_t unit_count() const {
@@ -307,17 +308,20 @@ struct PairChoice {
 constexpr double kStripWave = 0.63;
 
 // The balanced division of `tiles` pair tiles of `k_blocks` k-blocks over
-// `slots` clusters.
-void plan_balanced(int64_t tiles, int64_t k_blocks, int slots, PairChoice* c) {
+// `slots` clusters, after dp_waves waves of whole tiles (dp_waves * slots
+// tiles run data-parallel first; the ranges cover the rest).
+void plan_balanced(int64_t tiles, int64_t k_blocks, int slots, PairChoice* c,
+                   int64_t dp_waves = 0) {
   c->tiles = tiles;
   c->full = tiles;
   c->split = 1;
   c->kb_per_piece = static_cast<int>(k_blocks);
   c->balanced = true;
-  const int64_t work = tiles * k_blocks;
+  c->dp_tiles = dp_waves * slots;
+  const int64_t work = (tiles - c->dp_tiles) * k_blocks;
   c->per = work / slots;
   c->extra = static_cast<int>(work % slots);
-  c->units = 0;
+  c->units = c->dp_tiles;
   c->max_pieces = 1;
   for (int k = 0; k < slots; ++k) {
     const int n = balanced_units(c->per, c->extra, static_cast<int>(k_blocks), k);
@@ -340,7 +344,8 @@ void plan_balanced(int64_t tiles, int64_t k_blocks, int slots, PairChoice* c) {
 // up to two cut tiles per cluster, placed first, both accumulators wait.
 int balanced_mode() {
   if (env_int("GB3_GEMM_SPLIT_ALL", 0) > 1) return 0;
-  return env_int("GB3_GEMM_BALANCED", 0) == 1 ? 1 : 0;
+  const int m = env_int("GB3_GEMM_BALANCED", 0);
+  return m == 1 || m == 2 ? m : 0;
 }
 
 // Tail split of `tiles` pair tiles on `slots` resident pairs: the last,
@@ -375,7 +380,9 @@ void plan_tail(int64_t tiles, int64_t k_blocks, int slots, bool allow_split, Pai
 double pair_waves(const PairChoice& c, int64_t k_blocks, int slots) {
   if (c.strip_tiles > 0) return static_cast<double>((c.tiles - c.strip_tiles) / slots) + kStripWave;
   if (c.balanced) {
-    const double w = static_cast<double>(ceil_div(c.tiles * k_blocks, slots)) / k_blocks;
+    const double w = static_cast<double>(c.dp_tiles / slots) +
+                     static_cast<double>(ceil_div((c.tiles - c.dp_tiles) * k_blocks, slots)) /
+                         k_blocks;
     return w + (c.max_pieces > 1 ? kSplitCharge : 0.0);
   }
   double waves = static_cast<double>(c.full / slots);
@@ -391,7 +398,7 @@ double pair_waves(const PairChoice& c, int64_t k_blocks, int slots) {
 // 1 takes them wherever they apply); or the balanced division where it is
 // enabled and applies.
 PairChoice choose_pair_division(int64_t tiles, int64_t k_blocks, int slots, bool allow_split,
-                                int bn, bool allow_strips = false) {
+                                int bn, bool allow_strips = false, bool allow_dp_prefix = true) {
   PairChoice c;
   c.bn = bn;
   plan_tail(tiles, k_blocks, slots, allow_split, &c);
@@ -410,17 +417,19 @@ PairChoice choose_pair_division(int64_t tiles, int64_t k_blocks, int slots, bool
     if (strips_env == 1 || pair_waves(st, k_blocks, slots) < pair_waves(c, k_blocks, slots)) c = st;
   }
   const int mode = balanced_mode();
-  if (!allow_split || mode == 0 || tiles < slots) return c;
+  if (!allow_split || mode == 0 || tiles < slots || (mode == 2 && !allow_dp_prefix)) return c;
   PairChoice b;
   b.bn = bn;
-  plan_balanced(tiles, k_blocks, slots, &b);
+  // mode 2: all whole waves but the last run data-parallel, the last whole
+  // wave and the partial one are divided
+  plan_balanced(tiles, k_blocks, slots, &b, mode == 2 ? tiles / slots - 1 : 0);
   return b;
 }
 
 // Tile width of the CTA-pair GEMM and its division: the fewest waves of pair
 // tiles weighted by the time a wave of that width takes.
 PairChoice choose_pair(int64_t batch, int64_t M, int64_t N, int64_t K, int slots,
-                       bool allow_split, bool allow_strips = false) {
+                       bool allow_split, bool allow_strips = false, bool allow_dp_prefix = true) {
   PairChoice best;
   double best_cost = 1e300;
   const int64_t mb = ceil_div(M, kPairBM);
@@ -433,7 +442,8 @@ PairChoice choose_pair(int64_t batch, int64_t M, int64_t N, int64_t K, int slots
   for (int bn : kPairWidths) {
     if (forced_valid && bn != forced) continue;
     PairChoice c =
-        choose_pair_division(batch * mb * ceil_div(N, bn), kb, slots, allow_split, bn, allow_strips);
+        choose_pair_division(batch * mb * ceil_div(N, bn), kb, slots, allow_split, bn, allow_strips,
+                             allow_dp_prefix);
     // Measured on GB300 (8192^3): a wave of 256-wide pair tiles takes 1.057x
     // the time of 224-wide ones for 1.143x the work, i.e. time ~ width + 320.
     const double cost = pair_waves(c, kb, slots) * static_cast<double>(bn + kWidthCostOffset);
@@ -1145,6 +1155,7 @@ TileParams tile_params(const Problem& q, int tile_m, int tile_n_out, uint32_t id
   p.balanced = 0;
   p.work_per_cluster = 0;
   p.work_extra = 0;
+  p.dp_tiles = 0;
   p.strip_tiles = 0;
   p.idesc_strip = idesc_f32_acc(kPairBM, kPairStripN, q.in_dtype == GEMM_IN_F16);
   p.ws = nullptr;
@@ -1161,7 +1172,9 @@ void pair_units(int dev, gemm_plan* pl, const Problem& q, int out_cols, TilePara
   if (gate_up) {
     c = choose_pair_division(p->num_tiles, p->k_blocks, slots, true, 256);
   } else {
-    c = choose_pair(q.batch, q.M, q.N, q.K, slots, true, !q.stats());
+    // The C ring's look-ahead assumes a cluster's split pieces come before its
+    // whole tiles, which whole waves ahead of the divided ranges break.
+    c = choose_pair(q.batch, q.M, q.N, q.K, slots, true, !q.stats(), !pair_reads_c_ring(q.beta));
   }
   (void)out_cols;
   if (pair_workspace_bytes(c, slots) > 0) {
@@ -1178,6 +1191,7 @@ void pair_units(int dev, gemm_plan* pl, const Problem& q, int out_cols, TilePara
     }
     if (st != GEMM_OK) {
       c.balanced = false;
+      c.dp_tiles = 0;
       c.full = c.tiles;
       c.split = 1;
       c.kb_per_piece = p->k_blocks;
@@ -1193,6 +1207,7 @@ void pair_units(int dev, gemm_plan* pl, const Problem& q, int out_cols, TilePara
   p->balanced = c.balanced ? 1 : 0;
   p->work_per_cluster = c.per;
   p->work_extra = c.extra;
+  p->dp_tiles = static_cast<int>(c.dp_tiles);
   p->strip_tiles = static_cast<int>(c.strip_tiles);
 }
 

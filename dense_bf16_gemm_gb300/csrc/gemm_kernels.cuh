@@ -195,6 +195,11 @@ struct TileParams {
   int balanced;
   long long work_per_cluster;
   int work_extra;
+  // With the balanced division: its first dp_tiles tiles (a multiple of the
+  // clusters) run whole, dp_tiles / clusters per cluster in round-robin order,
+  // before each cluster's balanced range over the remaining tiles' k-blocks
+  // (whose tile indices the ranges count from dp_tiles).
+  int dp_tiles;
   // Strips (CTA-pair kernels of 256-column tiles, strip_tiles > 0): the last
   // strip_tiles tiles run as kPairStripN-column strips of the whole K, one
   // unit each, after every whole tile; num_full = num_tiles - strip_tiles and
@@ -341,13 +346,30 @@ __host__ __device__ __forceinline__ int balanced_counter(long long per, int extr
 // Units of cluster `cluster` (of `nclusters`) and the i-th of them: the
 // balanced division, or the round-robin order of the tail-split units.
 __device__ __forceinline__ int cluster_unit_count(const TileParams& p, int cluster, int nclusters) {
-  if (p.balanced) return balanced_units(p.work_per_cluster, p.work_extra, p.k_blocks, cluster);
+  if (p.balanced)
+    return p.dp_tiles / nclusters +
+           balanced_units(p.work_per_cluster, p.work_extra, p.k_blocks, cluster);
   return cluster < p.num_units ? (p.num_units - 1 - cluster) / nclusters + 1 : 0;
 }
 
 __device__ __forceinline__ WorkUnit cluster_unit(const TileParams& p, int cluster, int nclusters,
                                                  int i) {
-  if (p.balanced) return balanced_unit(p.work_per_cluster, p.work_extra, p.k_blocks, cluster, i);
+  if (p.balanced) {
+    const int dp = p.dp_tiles / nclusters;
+    if (i < dp) {
+      WorkUnit w;
+      w.tile = cluster + i * nclusters;
+      w.kb0 = 0;
+      w.kb1 = p.k_blocks;
+      w.piece = 0;
+      w.pieces = 1;
+      w.strip = -1;
+      return w;
+    }
+    WorkUnit w = balanced_unit(p.work_per_cluster, p.work_extra, p.k_blocks, cluster, i - dp);
+    w.tile += p.dp_tiles;
+    return w;
+  }
   WorkUnit u;
   u.strip = -1;
   if (p.strip_tiles > 0) {

@@ -422,13 +422,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         split.pieces = un.pieces;
         split.piece = un.piece;
         if (p.balanced) {
-          split.ws0 = ws + balanced_slot(p.work_per_cluster, p.work_extra, p.k_blocks, un.tile, 0) *
+          const int bt_ = un.tile - p.dp_tiles;   // tile index within the balanced ranges
+          split.ws0 = ws + balanced_slot(p.work_per_cluster, p.work_extra, p.k_blocks, bt_, 0) *
                                piece_f4;
-          split.ws1 = ws + balanced_slot(p.work_per_cluster, p.work_extra, p.k_blocks, un.tile, 1) *
+          split.ws1 = ws + balanced_slot(p.work_per_cluster, p.work_extra, p.k_blocks, bt_, 1) *
                                piece_f4;
           split.rest_stride = 2 * piece_f4;
           counter = p.counters +
-                    balanced_counter(p.work_per_cluster, p.work_extra, p.k_blocks, un.tile) * 8 +
+                    balanced_counter(p.work_per_cluster, p.work_extra, p.k_blocks, bt_) * 8 +
                     band_id;
         } else {
           const int tail = un.tile - p.num_full;

@@ -373,7 +373,9 @@ typedef struct gemm_plan {
  * even in place of a K split); GB3_GEMM_BALANCED = 1
  * instead gives every CTA pair one contiguous range of all tiles' k-blocks
  * (measured slower on GB300, so off by default; split_k then reports the most
- * pieces of a tile and `tiles` the units).  The plan is that of beta == 0: with
+ * pieces of a tile and `tiles` the units), and GB3_GEMM_BALANCED = 2 runs all
+ * whole waves but the last as whole tiles first and divides the rest (also
+ * slower; not with beta != 0, whose C ring keeps the default division).  The plan is that of beta == 0: with
  * beta != 0 the CTA-pair kernel runs one stage fewer (its shared memory holds
  * a deeper staging ring for C) unless GB3_GEMM_C_RING = 0.  M <= 128 runs on
  * the small-M kernel when its 128-row weight tiles (batch * ceil(N / 128))

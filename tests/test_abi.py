@@ -227,6 +227,19 @@ def test_plan_strips_not_with_row_stats(lib, monkeypatch):
     assert st == 0 and (p.tile_n, p.tiles) == (224, 276)
 
 
+def test_plan_balanced_after_whole_waves(lib, monkeypatch):
+    """GB3_GEMM_BALANCED=2: all whole waves but the last run whole tiles, the
+    rest of the tiles' k-blocks are divided into one range per pair."""
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "2")
+    for M, N, K in [(4096, 4096, 4096), (8192, 8192, 8192), (2304, 4136, 200)]:
+        st, p = _native.gemm_bf16_plan(M, N, K, _native.GEMM_OUT_F32, 152)
+        assert st == 0 and p.tile_n in (256, 224)
+        tiles = -(-M // 256) * -(-N // p.tile_n)
+        dp = (tiles // 76 - 1) * 76
+        units, pieces, _ = balanced_division(tiles - dp, -(-K // 64), 76)
+        assert (p.tiles, p.split_k, p.grid) == (dp + units, pieces, 152)
+
+
 def test_plan_tail_split_pieces_are_long_enough(lib, monkeypatch):
     monkeypatch.setenv("GB3_GEMM_BALANCED", "0")   # the tail split alone
     # K = 2048 is 32 k-blocks: two pieces would be shorter than 24 k-blocks

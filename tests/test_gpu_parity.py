@@ -942,3 +942,52 @@ def test_strips_under_graph_capture(g):
     ref, _ = oracle.gemm_full(A, B, alpha=2.0, beta=-0.5, C=C)
     assert np.array_equal(to_f64(Cd), ref)
     assert_status_ok(g)
+
+
+# the balanced division after data-parallel waves (GB3_GEMM_BALANCED=2): all
+# whole waves but the last run whole tiles, the rest is divided into ranges
+HYBRID_SHAPES = [
+    (4096, 4096, 512),   # 256 tiles: 2 waves whole, 104 tiles (8 k-blocks each) divided
+    (3000, 5000, 264),   # 240 tiles: 2 waves whole, 88 tiles divided; a K tail
+    (2304, 4136, 200),   # 153 tiles: 1 wave whole, 77 tiles divided
+]
+
+
+@pytest.mark.parametrize("M,N,K", HYBRID_SHAPES)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("beta", [0.0, -0.5])
+def test_balanced_after_whole_waves_bit_exact(g, monkeypatch, M, N, K, out_dtype, beta):
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "2")
+    monkeypatch.setenv("GB3_GEMM_PAIR_TILE_N", "256")
+    p = g.plan(M, N, K, out_dtype)
+    tiles = -(-M // 256) * -(-N // 256)
+    assert p["kernel_name"] == "pair" and p["split_k"] >= 2 and p["tiles"] > tiles
+    A, B, C = int_inputs(M, N, K, seed=M + N + 5 * K)
+    Cq = C.to(out_dtype) if beta != 0.0 else None
+    ref, _ = oracle.gemm_full(A, B, alpha=2.0, beta=beta,
+                              C=Cq.to(torch.float32) if Cq is not None else None)
+    want = ref if out_dtype == torch.float32 else oracle.round_to_bf16_bits(ref)
+    out = run_gemm(g, A, B, C=Cq, alpha=2.0, beta=beta, out_dtype=out_dtype)
+    got = to_f64(out) if out_dtype == torch.float32 else bits(out.cpu())
+    assert np.array_equal(got, want)
+    assert_status_ok(g)
+
+
+def test_balanced_after_whole_waves_random_and_deterministic(g, monkeypatch):
+    monkeypatch.setenv("GB3_GEMM_BALANCED", "2")
+    M, N, K = 4096, 4096, 4096
+    A, B, _ = workloads.gemm_inputs(M, N, K, 3, ("uniform",), ("uniform",), None)
+    Ad, Bd = A.cuda(), B.cuda()
+    outs = []
+    for _ in range(2):
+        Cd = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        g.gemm(Ad, Bd, Cd)
+        outs.append(Cd)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    rows = np.random.default_rng(87).choice(M, 24, replace=False)
+    rr, cc = np.repeat(rows, N), np.tile(np.arange(N), rows.size)
+    ref, ab = oracle.gemm_entries(A, B, rr, cc)
+    tol = oracle.gemm_tolerance(ref, ab, 1.0, 0.0, None)
+    assert_within(to_f64(outs[0])[rr, cc], ref, tol, "balanced after whole waves")
+    assert_status_ok(g)
