@@ -102,32 +102,149 @@ def load_peaks() -> dict:
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
+# Clock-event reason bits of NVML (nvml.h, nvmlClocksEventReason* /
+# nvmlClocksThrottleReason*) that slow the SM clock, by the names nvidia-smi uses.
+CLOCK_EVENT_REASONS = ((0x4, "sw_power_cap"), (0x8, "hw_slowdown"),
+                       (0x20, "sw_thermal_slowdown"), (0x40, "hw_thermal_slowdown"),
+                       (0x80, "hw_power_brake_slowdown"))
+
+
+def reason_names(mask: int) -> list[str]:
+    """The slow-down reasons set in an NVML clock-event reason mask."""
+    return [name for bit, name in CLOCK_EVENT_REASONS if mask & bit]
+
+
+class NvmlReader:
+    """Reads one GPU's SM clock, maximum SM clock, power draw and active clock-event
+    reasons through NVML's C library.  Queries only: nothing is set."""
+
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, index: int, pci_bus_id: str | None = None):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self.lib = lib
+        h = ctypes.c_void_p()
+        rc = 1
+        if pci_bus_id:
+            rc = lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h))
+        if rc != 0:
+            rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h))
+        if rc != 0:
+            lib.nvmlShutdown()
+            raise OSError(f"no NVML handle for GPU {pci_bus_id or index}")
+        self.h = h
+        self.get_reasons = (getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                            or lib.nvmlDeviceGetCurrentClocksThrottleReasons)
+
+    def read(self):
+        """(SM MHz, max SM MHz, watts, [reasons]); None for a value NVML does not give.
+        The power is the driver's averaged reading, so a region of a few
+        milliseconds shows less than the draw under load."""
+        ct = self.ct
+        sm, smax, mw, mask = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        ok_sm = self.lib.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, ct.byref(sm)) == 0
+        ok_max = self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.NVML_CLOCK_SM,
+                                                    ct.byref(smax)) == 0
+        ok_w = self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw)) == 0
+        ok_r = self.get_reasons(self.h, ct.byref(mask)) == 0
+        return (float(sm.value) if ok_sm else None, float(smax.value) if ok_max else None,
+                mw.value / 1000.0 if ok_w else None, reason_names(mask.value) if ok_r else [])
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
+def parse_smi_line(line: str):
+    """One line of `nvidia-smi --query-gpu=<ClockSampler.FIELDS> --format=csv,noheader,
+    nounits` as (SM MHz, max SM MHz, watts, [reasons]), or None."""
+    parts = [p.strip() for p in line.split(",")]
+    if len(parts) < 9:
+        return None
+
+    def num(x):
+        try:
+            return float(x)
+        except ValueError:
+            return None
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = [n for n, v in zip(names, parts[5:9]) if v.lower() == "active"]
+    return num(parts[1]), num(parts[2]), num(parts[3]), reasons
+
+
+def pci_bus_id(dev) -> str | None:
+    """The device's PCI address in NVML's form (domain:bus:device.0), or None."""
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except (AttributeError, RuntimeError, AssertionError):
+        return None
+
+
 class ClockSampler:
+    """Samples the GPU's clocks while a timed region runs: through NVML every
+    `period` seconds (so even a timed region of a few milliseconds gets several
+    samples), else through `nvidia-smi -lms 100`.  `reader` replaces the NVML
+    reader (tests)."""
+
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, pci_bus_id: str | None = None, reader=None,
+                 period: float = 0.002):
         self.gpu = gpu_index
+        self.pci_bus_id = pci_bus_id
+        self.reader = reader
+        self.period = period
+        self.source = None
         self.proc = None
-        self.lines: list[tuple[float, str]] = []
+        self._th = None
+        self._stop = threading.Event()
+        self.rows: list[tuple[float, tuple]] = []
         self.t0 = self.t1 = None
 
     def start(self):
+        if self.reader is None:
+            try:
+                self.reader = NvmlReader(self.gpu, self.pci_bus_id)
+            except (OSError, AttributeError):
+                self.reader = None
+        if self.reader is not None:
+            self.source = "nvml"
+            self._th = threading.Thread(target=self._poll, daemon=True)
+            self._th.start()
+            return
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                ["nvidia-smi", f"--id={self.pci_bus_id or self.gpu}",
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
             return
-        self._th = threading.Thread(target=self._read, daemon=True)
+        self.source = "nvidia-smi"
+        self._th = threading.Thread(target=self._read_smi, daemon=True)
         self._th.start()
 
-    def _read(self):
+    def _poll(self):
+        while not self._stop.is_set():
+            t = time.time()
+            try:
+                r = self.reader.read()
+            except Exception:  # a failing query ends the sampling, not the run
+                return
+            self.rows.append((t, r))
+            self._stop.wait(self.period)
+
+    def _read_smi(self):
         for line in self.proc.stdout:
-            self.lines.append((time.time(), line.strip()))
+            r = parse_smi_line(line)
+            if r is not None:
+                self.rows.append((time.time(), r))
 
     def mark(self, begin: bool):
         if begin:
@@ -136,41 +253,46 @@ class ClockSampler:
             self.t1 = time.time()
 
     def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
-                    "samples": 0}
-        time.sleep(0.25)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        rows = []
-        for t, line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            rows.append((t, parts))
-        inside = [r for t, r in rows if self.t0 is not None and self.t0 - 0.05 <= t <= self.t1 + 0.05]
-        use = inside if inside else rows
-        def num(x):
+        if self.source is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock source unavailable"],
+                    "samples": 0, "source": None}
+        if self.source == "nvml":
+            time.sleep(2 * self.period)
+            self._stop.set()
+            self._th.join(timeout=5)
             try:
-                return float(x)
-            except ValueError:
-                return None
-        sm = [num(r[1]) for r in use if num(r[1]) is not None]
-        smax = [num(r[2]) for r in use if num(r[2]) is not None]
-        reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in use:
-            for name, v in zip(names, r[5:9]):
-                if v.strip().lower() == "active":
-                    reasons.add(name)
+                self.reader.close()
+            except Exception:
+                pass
+        else:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return self.summary()
+
+    def summary(self) -> dict:
+        """Median SM clock, maximum SM clock, reasons seen and peak power over the
+        samples inside the marked region, widened on each side by one sampling
+        period (100 ms for nvidia-smi); all samples if none fell inside."""
+        rows = list(self.rows)
+        pad = self.period if self.source == "nvml" else 0.1
+        inside = [r for t, r in rows
+                  if self.t0 is not None and self.t1 is not None
+                  and self.t0 - pad <= t <= self.t1 + pad]
+        use = inside if inside else [r for _, r in rows]
+        sm = [r[0] for r in use if r[0] is not None]
+        smax = [r[1] for r in use if r[1] is not None]
+        watts = [r[2] for r in use if r[2] is not None]
+        reasons = sorted({name for r in use for name in r[3]})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons),
+                "reasons": reasons,
                 "samples": len(inside),
-                "power_w_max": max((num(r[3]) or 0.0) for r in use) if use else None}
+                "power_w_max": max(watts) if watts else None,
+                "source": self.source}
 
 
 # ---------------------------------------------------------------------------
@@ -582,7 +704,7 @@ def run_ours(args):
     t = make_device_inputs(w, dev, host)
     pl = plan_of(lib, w)
 
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(local, pci_bus_id(dev))
     sampler.start()
     barrier(pg)
     torch.cuda.synchronize()
