@@ -39,6 +39,7 @@ EXPORTED = (
     "gemm_bf16_plan",
     "gemm_gate_up_plan",
     "gemm_selftest_wait_timeout",
+    "gemm_selftest_pipeline_timeout",
     "gemm_bf16_skinny_noalloc",
     "gemm_batched",
     "gemm_batched_plan",
@@ -131,6 +132,9 @@ def lib() -> ctypes.CDLL:
                                                    _f32, _vp, _i64, _int, _vp]
             l.gemm_selftest_wait_timeout.restype = _int
             l.gemm_selftest_wait_timeout.argtypes = [_i64, _vp]
+            l.gemm_selftest_pipeline_timeout.restype = _int
+            l.gemm_selftest_pipeline_timeout.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64,
+                                                         _vp, _i64, _int, _vp]
             l.gemm_gate_up_plan.restype = _int
             l.gemm_gate_up_plan.argtypes = [_i64, _i64, _i64, _int, ctypes.POINTER(GemmPlan)]
             l.gemm_row_stats.restype = _int
@@ -209,6 +213,13 @@ def gemm_prepare(max_n: int, stream=0) -> int:
 
 def gemm_selftest_wait_timeout(limit_ns: int, stream=0) -> int:
     return lib().gemm_selftest_wait_timeout(limit_ns, stream or None)
+
+
+def gemm_selftest_pipeline_timeout(M, N, K, A, lda, B, ldb, C, ldc, stall_after,
+                                   stream=0) -> int:
+    """A, B, C: device addresses (ints) of BF16 matrices."""
+    return lib().gemm_selftest_pipeline_timeout(M, N, K, A or None, lda, B or None, ldb,
+                                                C or None, ldc, stall_after, stream or None)
 
 
 def gemm_bf16_plan(M, N, K, out_dtype=GEMM_OUT_BF16, num_sms=0):

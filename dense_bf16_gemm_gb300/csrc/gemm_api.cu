@@ -1361,6 +1361,7 @@ SkinnyParams skinny_params(const gemm_plan& pl, const Problem& q) {
   p.ws = nullptr;
   p.counters = nullptr;
   p.issue_group = skinny_issue_group(p.kb_per_split);
+  p.stall_after = -1;
   return p;
 }
 
@@ -1891,6 +1892,46 @@ int gemm_selftest_wait_timeout(int64_t limit_ns, void* stream) {
   }
   return launch(wait_timeout_probe_kernel, 1, 32, 0, static_cast<cudaStream_t>(stream),
                 static_cast<unsigned long long>(limit_ns));
+}
+
+int gemm_selftest_pipeline_timeout(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                                   const void* B, int64_t ldb, void* C, int64_t ldc,
+                                   int stall_after, void* stream_) {
+  const Problem q{1, M, N, K, 1.0f, 0.0f, A, lda, 0, B, ldb, 0, C, ldc, 0, GEMM_IN_BF16,
+                  GEMM_OUT_BF16};
+  int st = validate_problem(q);
+  if (st != GEMM_OK) return st;
+  if (M < 1 || M > kSkinnyMaxM || N < 1 || K < 1 || stall_after < 0 ||
+      stall_after >= ceil_div(K, kBK))
+    return GEMM_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev;
+  if ((st = current_device(&dev)) != GEMM_OK) return st;
+  auto kern = gemm_skinny_kernel<kSkinnyStages>;
+  int sms;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = probe_device(dev)) != GEMM_OK) return st;
+    sms = g_dev[dev].sms;
+    if ((st = ensure_smem_attr(dev, reinterpret_cast<const void*>(kern), CfgSkinny::kSmemBytes)) !=
+        GEMM_OK)
+      return st;
+  }
+  // Whole K per unit (no split, so no workspace or arrival counter is
+  // touched), one unit per CTA at most; every unit stops inside its K range.
+  gemm_plan pl;
+  std::memset(&pl, 0, sizeof(pl));
+  pl.split_k = 1;
+  pl.tiles = ceil_div(N, kSkinnyRows);
+  pl.grid = static_cast<int>(std::min<int64_t>(pl.tiles, sms));
+  SkinnyParams p = skinny_params(pl, q);
+  p.stall_after = stall_after;
+  CUtensorMap tmW, tmX;
+  if ((st = operand_map(&tmW, B, GEMM_IN_BF16, K, N, 1, ldb, 0, kSkinnyRows)) != GEMM_OK)
+    return st;
+  if ((st = operand_map(&tmX, A, GEMM_IN_BF16, K, M, 1, lda, 0, kSkinnyNX)) != GEMM_OK)
+    return st;
+  return launch(kern, pl.grid, kThreads, CfgSkinny::kSmemBytes, stream, tmW, tmW, tmX, p);
 }
 
 uint64_t gemm_layout_smem_descriptor(uint32_t smem_address, uint32_t mn_chunk_bytes) {

@@ -46,6 +46,10 @@ struct SkinnyParams {
   float* ws;      // [batch][splits][M][N] FP32 partial sums (splits > 1)
   int* counters;  // [batch][n_blocks][4] arrival counters, zero between calls
   int issue_group;  // k-blocks the producer issues back to back (1 .. STAGES)
+  // -1, except in the failure-path self-test: the producer issues only this
+  // many k-blocks and then stops, as if the next copy never landed, so the
+  // MMA thread's wait for it runs out and the CTA takes its abort path.
+  int stall_after;
 };
 
 template <int STAGES, bool GATE = false>
@@ -191,6 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           for (int j = 0; ok && j < gn; ++j) {
+            if (issued == p.stall_after) {
+              ok = false;
+              break;
+            }
             const int kb = g0 + j;
             const uint32_t w_dst = sbase + s * Cfg::kStageBytes;
             mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);

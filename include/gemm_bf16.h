@@ -337,13 +337,36 @@ GEMM_API int gemm_bf16_skinny_noalloc(int64_t M, int64_t N, int64_t K, float alp
  */
 GEMM_API int gemm_selftest_wait_timeout(int64_t limit_ns, void *stream);
 
+/*
+ * Self-test of a GEMM pipeline's abort path.  Launches the M <= 16 split-K
+ * kernel (without a split: one CTA per 128 rows of B) on C = A . B^T with
+ * BF16 operands and output, A row-major M x K (lda), B row-major N x K (ldb),
+ * C row-major M x N (ldc), all device memory of the caller.  Its TMA producer
+ * issues only `stall_after` k-blocks (64 columns of K each) and then stops,
+ * as if the next copy never landed, so the MMA thread's wait for that stage
+ * runs out after the pipelines' 2 s bound ("TMEM tiles and transfers",
+ * section "Completion and validation": completion is observed through
+ * mbarriers).  Each CTA then sets its abort flag, lets its epilogue warps
+ * leave, waits (bounded) for the copies and MMAs it issued, frees its Tensor
+ * Memory and returns; the device status word then reads GEMM_ERR_TIMEOUT at
+ * wait site 2 (the MMA thread waiting for a full stage).  C is not written,
+ * and no workspace or arrival counter is touched.  Takes about 2 s on the
+ * GPU.  Returns GEMM_ERR_INVALID_ARG unless 1 <= M <= 16, N >= 1 and
+ * 0 <= stall_after < ceil(K / 64); alignment as for gemm_bf16.
+ */
+GEMM_API int gemm_selftest_pipeline_timeout(int64_t M, int64_t N, int64_t K,
+                                            const void *A, int64_t lda,
+                                            const void *B, int64_t ldb,
+                                            void *C, int64_t ldc,
+                                            int stall_after, void *stream);
+
 /* How a call would be executed (host-side planning only). */
 typedef struct gemm_plan {
     int kernel;       /* 0 none, 1 single-CTA tiled GEMM, 2 skinny split-K, 3 scale only (K == 0),
                          4 single-CTA gate/up, 5 CTA-pair tiled GEMM, 6 CTA-pair gate/up,
-                         7 small-M (64-row weight tiles; the k-blocks of all tiles
-                           divided evenly over the CTAs, shared tiles summed in
-                           the workspace),
+                         7 small-M (128-row weight tiles; whole tiles per CTA, or
+                           the k-blocks of all tiles divided evenly over the CTAs
+                           with shared tiles summed in the workspace),
                          8 split-K gate/up (M <= 16: Wg and Wu rows streamed together) */
     int tile_m;       /* output rows per tile (tcgen05 M, or weight rows for kernels 2 and 7) */
     int tile_n;       /* output columns per tile (activation rows for kernels 2 and 7) */

@@ -448,6 +448,41 @@ def test_bounded_wait_reports_timeout(g):
     assert np.array_equal(to_f64(out), ref)
 
 
+def test_gemm_pipeline_abort_path(g, monkeypatch):
+    """A GEMM pipeline whose TMA producer stops after two k-blocks (the M <= 16
+    kernel's self-test hook): the MMA thread's wait for the third runs out,
+    every CTA leaves through its abort path (epilogue warps leave, the issued
+    copies and MMAs are drained, Tensor Memory is freed), the status word names
+    the MMA thread's wait (site 2), C is untouched, and the context still
+    computes, the split-K kernel's arrival counters included."""
+    from dense_bf16_gemm_gb300 import _native
+    assert_status_ok(g)
+    M, N, K = 16, 1024, 1024
+    A, B, _ = int_inputs(M, N, K, 11)
+    Ad, Bd = A.cuda(), B.cuda()
+    Cd = torch.full((M, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    st = _native.gemm_selftest_pipeline_timeout(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K,
+                                                Cd.data_ptr(), N, 2, stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    st, site = g.device_status()
+    assert st == _native.GEMM_ERR_TIMEOUT and site == 2
+    assert_status_ok(g)                 # reading cleared the word
+    assert bool((Cd.float() == 7.0).all())
+    # the same problem on the split-K kernel, forced to split K in 4 (so its
+    # workspace and arrival counters are used), twice
+    monkeypatch.setenv("GB3_GEMM_SMALL_M", "0")
+    monkeypatch.setenv("GB3_SKINNY_SPLITS", "4")
+    p = g.plan(M, N, K, torch.float32)
+    assert p["kernel_name"] == "skinny_splitk" and p["split_k"] == 4
+    ref, _ = oracle.gemm_full(A, B)
+    for _ in range(2):
+        out = run_gemm(g, A, B, out_dtype=torch.float32)
+        assert np.array_equal(to_f64(out), ref)
+    assert_status_ok(g)
+
+
 @pytest.mark.parametrize("width", ["256", "224"])
 @pytest.mark.parametrize("M,N,K", [(300, 520, 200), (512, 1000, 1000), (2000, 712, 136)])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
