@@ -38,6 +38,52 @@ def test_library_exports_every_declared_symbol(lib):
     assert gemm_like == set(declared_symbols())
 
 
+def declared_prototypes():
+    """name -> (return type, [parameter types]) of every GEMM_API function."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    protos = {}
+    for ret, name, params in re.findall(r"GEMM_API\s+([\w\s\*]*?)\b(\w+)\s*\(([^)]*)\)\s*;",
+                                        text):
+        params = " ".join(params.split())
+        types = [] if params in ("", "void") else [
+            re.sub(r"\s*\b\w+$", "", p.strip()).replace(" *", "*") for p in params.split(",")]
+        protos[name] = (" ".join(ret.split()), types)
+    return protos
+
+
+def _ctype_of(decl):
+    """The ctypes type the binding must use for a C parameter or return type."""
+    decl = decl.replace("const ", "").strip()
+    if decl.endswith("*"):
+        return "ptr"
+    return {"int": ctypes.c_int, "int64_t": ctypes.c_int64, "float": ctypes.c_float,
+            "uint32_t": ctypes.c_uint32, "uint64_t": ctypes.c_uint64}[decl]
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every ctypes binding passes as many arguments as the header's prototype
+    takes, each of the C type's width and kind, and reads the declared return
+    type: a dropped or swapped argument in the binding fails here, not on a GPU."""
+    protos = declared_prototypes()
+    assert sorted(protos) == declared_symbols()
+    for name, (ret, params) in protos.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, name
+        assert len(fn.argtypes) == len(params), (name, params)
+        for i, (ct, decl) in enumerate(zip(fn.argtypes, params)):
+            want = _ctype_of(decl)
+            if want == "ptr":
+                assert ct in (ctypes.c_void_p, ctypes.c_char_p) or \
+                    issubclass(ct, ctypes._Pointer), (name, i, decl, ct)
+            else:
+                assert ct is want, (name, i, decl, ct)
+        want = _ctype_of(ret)
+        if want == "ptr":
+            assert fn.restype in (ctypes.c_void_p, ctypes.c_char_p), (name, ret)
+        else:
+            assert fn.restype is want, (name, ret, fn.restype)
+
+
 def test_status_strings(lib):
     for st in range(6):
         assert _native.status_string(st)
