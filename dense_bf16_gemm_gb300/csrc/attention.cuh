@@ -11,7 +11,9 @@
 // key block j of chain c = j % 2:
 //
 //   S = Q . K_j^T                  tcgen05.mma M = 128, N = 128 over D (K_j is K-major:
-//                                  D contiguous), into score buffer j % NS
+//                                  D contiguous), into score buffer j % NS (at D = 64
+//                                  blocks j and j + 1 as one set of N = 256 MMAs into
+//                                  the two adjacent buffers)
 //   m_c = max(m_c, rowmax S)       softmax warps of chain c: a query row is one TMEM lane
 //   P_j = exp(S - m_c)             and one thread, which holds all 128 scores of its row
 //   l_c = l_c a + rowsum P_j       (a = exp(m_old - m_new))
