@@ -372,9 +372,12 @@ typedef struct gemm_plan {
     int tile_n;       /* output columns per tile (activation rows for kernels 2 and 7) */
     int tile_k;       /* K per pipeline stage */
     int stages;       /* shared-memory ring depth */
-    int split_k;      /* K splits (skinny path); most CTAs sharing one tile (small-M);
+    int split_k;      /* K pieces of a split tile (skinny path; the CTA-pair kernel's
+                         split last-wave tiles, or the most pieces of one tile under
+                         its balanced division); most CTAs sharing one tile (small-M);
                          else 1 */
-    int64_t tiles;    /* work units (output tiles x splits) */
+    int64_t tiles;    /* work units: whole tiles plus split pieces (and, for the
+                         CTA-pair kernel, 64-column strips of last-wave tiles) */
     int grid;         /* CTAs launched (persistent: at most one per SM) */
     int smem_bytes;   /* dynamic shared memory per CTA */
     int launches;     /* kernels one call launches */

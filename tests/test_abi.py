@@ -240,6 +240,55 @@ def test_plan_pair_matches_wave_model(lib, M, N, K):
     assert (d["tile_n"], d["split_k"], d["tiles"]) == (bn, split, units)
 
 
+def test_plan_pair_matches_wave_model_on_random_shapes(lib):
+    """The planner against its restated wave model on seeded random shapes
+    (M > 128, N and K up to 20000, FP32 and BF16 output)."""
+    rng = np.random.default_rng(7)
+    for _ in range(400):
+        M = int(rng.integers(129, 20000))
+        N, K = (int(x) for x in rng.integers(1, 20000, size=2))
+        for od in (_native.GEMM_OUT_F32, _native.GEMM_OUT_BF16):
+            st, p = _native.gemm_bf16_plan(M, N, K, od, 152)
+            d = p.as_dict()
+            assert st == 0 and d["kernel_name"] == "pair", (M, N, K)
+            bn, split, units, _ = pair_model(M, N, K)
+            assert (d["tile_n"], d["split_k"], d["tiles"]) == (bn, split, units), (M, N, K, od)
+
+
+def test_plans_keep_their_invariants_on_random_shapes(lib):
+    """Every plan over seeded random (batch, M, N, K), operand and output types
+    fits the hardware and the kernels' fixed shapes: 1..232448 bytes of shared
+    memory, 1..152 CTAs (an even number for CTA pairs), 64-element k-blocks,
+    one launch; 256-row pair tiles, 128-row tiles elsewhere; the small-M
+    activation tile the smallest of 16, 32, 64, 128 that holds M."""
+    rng = np.random.default_rng(8)
+    kinds = set()
+    for _ in range(600):
+        batch = int(rng.choice([1, 1, 1, int(rng.integers(2, 17))]))
+        M = int(rng.choice([rng.integers(1, 17), rng.integers(17, 129), rng.integers(129, 8193)]))
+        N, K = (int(x) for x in rng.integers(1, 20000, size=2))
+        in_dtype, out_dtype = int(rng.integers(0, 2)), int(rng.integers(0, 3))
+        st, p = _native.gemm_batched_plan(batch, M, N, K, in_dtype, out_dtype, 152)
+        d = p.as_dict()
+        case = (batch, M, N, K, in_dtype, out_dtype, d)
+        assert st == 0, case
+        assert 0 < d["smem_bytes"] <= 232448, case
+        assert 1 <= d["grid"] <= 152, case
+        assert d["split_k"] >= 1 and d["tiles"] >= 1, case
+        assert d["tile_k"] == 64 and d["launches"] == 1, case
+        k = d["kernel_name"]
+        kinds.add(k)
+        if k == "pair":
+            assert d["grid"] % 2 == 0 and d["tile_m"] == 256 and d["tile_n"] in (224, 256), case
+        else:
+            assert d["tile_m"] == 128, case
+        if k == "small_m":
+            assert d["tile_n"] == min(n for n in (16, 32, 64, 128) if n >= M), case
+        if k == "skinny_splitk":
+            assert M <= 16 and d["tile_n"] == 16, case
+    assert kinds == {"pair", "tiled", "skinny_splitk", "small_m"}
+
+
 def test_plan_strips_cut_the_unsplit_tail_wave(lib, monkeypatch):
     monkeypatch.setenv("GB3_GEMM_BALANCED", "0")
     # 3000 x 5000 x 2000: 12 x 20 = 240 tiles of 256 columns, 3 waves on 76
