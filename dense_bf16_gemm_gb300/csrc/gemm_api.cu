@@ -241,8 +241,8 @@ int pair_stage_bytes(int bn) { return 128 * kBK * 2 + (bn / 2) * kBK * 2; }
 void choose_split(int64_t n_blocks, int64_t k_blocks, int sms, int* splits, int* kb_per,
                   int weights = 1) {
   const int forced = env_int("GB3_SKINNY_SPLITS", 0);
-  if (forced > 0) {
-    const int64_t kbp = ceil_div(k_blocks, std::min<int64_t>(forced, k_blocks));
+  if (forced > 0) {   // at most 32 splits, as the model below
+    const int64_t kbp = ceil_div(k_blocks, std::min<int64_t>({forced, k_blocks, 32}));
     *kb_per = static_cast<int>(kbp);
     *splits = static_cast<int>(ceil_div(k_blocks, kbp));
     return;
@@ -623,9 +623,20 @@ int plan_gate_up(int64_t M, int64_t N, int64_t K, int sms, gemm_plan* pl, int pa
 // ----------------------------------------------------------------------------
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The kernels count work units (output tiles, split pieces, strips) in 32-bit
+// integers, and a plan has at most 32 units per block of 128 x 128 outputs
+// (split K), so a call may hold at most 2^25 such blocks: at least 5.5 * 10^11
+// output elements (1.1 TB in BF16), more than any GPU memory holds, so no
+// problem whose operands fit is refused.
+constexpr int64_t kMaxOutputBlocks = int64_t{1} << 25;
+
 bool bad_dims(int64_t batch, int64_t M, int64_t N, int64_t K) {
-  return batch < 0 || M < 0 || N < 0 || K < 0 || batch > kMaxDim || M > kMaxDim || N > kMaxDim ||
-         K > kMaxDim;
+  if (batch < 0 || M < 0 || N < 0 || K < 0 || batch > kMaxDim || M > kMaxDim || N > kMaxDim ||
+      K > kMaxDim)
+    return true;
+  if (batch == 0 || M == 0 || N == 0) return false;
+  const int64_t mb = ceil_div(M, 128), nb = ceil_div(N, 128);   // each at most 2^24
+  return mb * nb > kMaxOutputBlocks || batch > kMaxOutputBlocks / (mb * nb);
 }
 
 int validate_problem(const Problem& p) {

@@ -70,8 +70,11 @@ enum gemm_in_dtype {
  *                                        writes alpha*acc + beta*c_old over
  *                                        the slice of C it read)
  *
- * M, N, K    problem sizes, 0 <= M, N, K < 2^31.  M == 0 or N == 0 does
- *            nothing and returns GEMM_OK.  K == 0 gives C = beta * C.
+ * M, N, K    problem sizes, 0 <= M, N, K < 2^31, and at most 2^25 blocks of
+ *            128 x 128 outputs per call (ceil(M/128) * ceil(N/128), times the
+ *            batch in gemm_batched: more output than any GPU memory holds).
+ *            M == 0 or N == 0 does nothing and returns GEMM_OK.  K == 0 gives
+ *            C = beta * C.
  * A, lda     device BF16 matrix, a(m,k) = A[m*lda + k], lda >= K.
  * B, ldb     device BF16 matrix, b(k,n) = B[n*ldb + k], ldb >= K.
  * C, ldc     device matrix of type out_dtype, c(m,n) = C[m*ldc + n],
@@ -105,7 +108,8 @@ GEMM_API int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha,
  * contract on both sides": a three-dimensional binding whose third
  * coordinate selects one matrix of a batch, each bounded separately).
  *
- * batch      number of matrices, 0 <= batch < 2^31 (0 does nothing).
+ * batch      number of matrices, 0 <= batch < 2^31 (0 does nothing); the
+ *            2^25 limit on 128 x 128 output blocks counts every matrix.
  * M, N, K, lda, ldb, ldc, alpha, beta, out_dtype  as gemm_bf16, per matrix.
  * stride_a   elements between A_b and A_(b+1), >= M*lda when batch > 1;
  * stride_b   elements between B_b and B_(b+1), >= N*ldb when batch > 1;
@@ -131,6 +135,7 @@ GEMM_API int gemm_batched(int64_t batch, int64_t M, int64_t N, int64_t K, float 
  * Wg, Wu     device BF16, wg(k,n) = Wg[n*ldw + k], wu(k,n) = Wu[n*ldw + k],
  *            ldw >= K (both K-contiguous like B of gemm_bf16).
  * Y, ldy     device BF16 output, y(m,n) = Y[m*ldy + n], ldy >= N.
+ * M, N, K    as gemm_bf16 (the same limits).
  * Both products accumulate in FP32; silu(g)*u is evaluated in FP32 and
  * rounded to BF16 once.  K == 0 gives Y = 0.
  */

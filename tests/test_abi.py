@@ -137,6 +137,29 @@ def test_gate_up_validation_without_gpu(lib, args, expect):
     assert _native.gemm_gate_up_silu(M, N, K, X, ldx, Wg, Wu, ldw, Y, ldy, 0) == expect
 
 
+def test_problems_beyond_32_bit_work_units_are_refused(lib):
+    """At most 2^25 blocks of 128 x 128 outputs per call (the kernels count work
+    units in 32 bits, at most 32 per block); the limit sits far above what any
+    GPU memory holds, so it refuses only problems that cannot exist, in the
+    plans and the calls."""
+    big = (1 << 31) - 1
+    for batch, M, N in [(1, big, big), (1 << 20, 1 << 20, 1 << 12), ((1 << 25) + 1, 1, 1),
+                        (3, 1 << 19, (1 << 20) + 1)]:
+        st, _ = _native.gemm_batched_plan(batch, M, N, 64, 0, 1, 152)
+        assert st == _native.GEMM_ERR_INVALID_ARG, (batch, M, N)
+    st = _native.gemm_bf16(big, big, 64, 1.0, A16, 64, A16, 64, 0.0, A16, big, 1, 0)
+    assert st == _native.GEMM_ERR_INVALID_ARG
+    st = _native.gemm_gate_up_silu(big, big, 64, A16, 64, A16, A16, 64, A16, big, 0)
+    assert st == _native.GEMM_ERR_INVALID_ARG
+    # exactly 2^25 blocks is allowed, with every unit count within 32 bits
+    for batch, M, N, K in [(1 << 25, 1, 1, 8192), (1, 1 << 19, 1 << 19, 64),
+                           (1, big, 1 << 7, 4096), (1 << 20, 16, 1 << 12, 1 << 20)]:
+        st, p = _native.gemm_batched_plan(batch, M, N, K, 0, 1, 152)
+        d = p.as_dict()
+        assert st == 0 and 1 <= d["grid"] <= 152, (batch, M, N, K)
+        assert 1 <= d["tiles"] < (1 << 31) and 1 <= d["split_k"] <= 32, (batch, M, N, K, d)
+
+
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     import torch
     if torch.cuda.is_available():
