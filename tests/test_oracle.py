@@ -609,6 +609,58 @@ def _fp32_flash(q, k, v, scale, block=128, lag=0.0):
     return (acc / l).astype(np.float64)
 
 
+def _fp32_flash_two_chains(q, k, v, scale, block=128, lag=0.0):
+    """The FP32 flash loop run as two independent chains, the even key blocks
+    in one and the odd ones in the other (each with its own maximum, sum and
+    accumulator, BF16 probabilities), merged at the end in FP32:
+    O = (acc_0 f_0 + acc_1 f_1) / (l_0 f_0 + l_1 f_1), f_c = exp(m_c - m),
+    m = max(m_0, m_1).  Numpy, independent of the oracle."""
+    q, k, v = (np.asarray(x, np.float32) for x in (q, k, v))
+    m = [np.float32(-np.inf)] * 2
+    l = [np.float32(0)] * 2
+    acc = [np.zeros(q.shape[-1], np.float32) for _ in range(2)]
+    for j, j0 in enumerate(range(0, k.shape[0], block)):
+        c = j % 2
+        s = (k[j0:j0 + block] @ q).astype(np.float32) * np.float32(scale)
+        m_new = np.float32(s.max()) if s.max() > m[c] + lag else m[c]
+        alpha = np.float32(np.exp(np.float32(m[c] - m_new))) if m[c] != -np.inf else np.float32(0)
+        p = np.exp((s - m_new).astype(np.float32)).astype(np.float32)
+        pb = oracle.bf16_bits_to_f64(oracle.round_to_bf16_bits(p)).astype(np.float32)
+        l[c] = np.float32(l[c] * alpha + p.sum(dtype=np.float32))
+        acc[c] = (acc[c] * alpha + pb @ v[j0:j0 + block]).astype(np.float32)
+        m[c] = m_new
+    mm = max(m)
+    f = [np.float32(np.exp(np.float32(mc - mm))) if mc != -np.inf else np.float32(0) for mc in m]
+    num = (acc[0] * f[0] + acc[1] * f[1]).astype(np.float32)
+    den = np.float32(l[0] * f[0] + l[1] * f[1])
+    return (num / den).astype(np.float64)
+
+
+@pytest.mark.parametrize("Nk,scale,lag", [(600, None, 0.0), (1153, None, 8.0), (520, 1.0, 8.0)])
+def test_attention_tolerance_covers_two_merged_chains(Nk, scale, lag):
+    """Key blocks dealt to two chains and merged at the end (lazy maxima that
+    lag by up to 8 in base 2, peaked rows at scale 1): the bound still holds,
+    so the merge's extra roundings are inside it."""
+    H, Nq, D = 1, 24, 64
+    Q, K, V = _attn_inputs(H, Nq, Nk, D, Nk)
+    h, r = _all_rows(H, Nq)
+    sc = D ** -0.5 if scale is None else scale
+    res = oracle.attention_rows(Q, K, V, sc, h, r)
+    tol = oracle.attention_tolerance(res, D, Nk, out_bf16=False)
+    qf, kf, vf = Q.float().numpy(), K.float().numpy(), V.float().numpy()
+    blocks = [np.arange(j0, min(j0 + 128, Nk)) for j0 in range(0, Nk, 128)]
+    even, odd = np.concatenate(blocks[0::2]), np.concatenate(blocks[1::2])
+    flagged = 0
+    for i in range(Nq):
+        got = _fp32_flash_two_chains(qf[0, i], kf[0], vf[0], sc, lag=lag * np.log(2.0))
+        assert np.all(np.abs(got - res["o"][i]) <= tol[i]), i
+        # a merge that weights the two chains' outputs equally is caught
+        wrong = (_fp32_flash(qf[0, i], kf[0][even], vf[0][even], sc) +
+                 _fp32_flash(qf[0, i], kf[0][odd], vf[0][odd], sc)) / 2
+        flagged += bool(np.any(np.abs(wrong - res["o"][i]) > tol[i]))
+    assert flagged >= Nq // 2
+
+
 def test_attention_tolerance_covers_an_fp32_flash_loop():
     H, Nq, Nk, D = 1, 8, 600, 64
     Q, K, V = _attn_inputs(H, Nq, Nk, D, 47)
